@@ -1,0 +1,281 @@
+"""Plain fp64 CPU oracle of the grouped expert MLP: forward and input gradient.
+
+TEST INFRASTRUCTURE. Imported only by ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline / reference arm of ``bench.py``. It shares no code with the
+CUDA library (no kernels, headers, tables or helpers) and is written to be
+checked by eye against the pages it follows:
+
+* "perf(moe): add frozen grouped GEMM for adapter training" (AlignmentResearch/
+  Megatron-LM PR #3), sections "Why this change" and "Why existing behavior
+  remains safe": the frozen, bias-free BF16 expert weights of all local experts
+  are applied by one grouped GEMM over ragged per-expert token groups; experts
+  with zero tokens are legal; the weights receive no gradient, only the input
+  does.
+* "[Main] Support paged stash with device-initiated GroupedLinear" (NVIDIA/
+  Megatron-LM PR #6828), section "What does this PR do?": grouped FC1, a fused
+  gated activation (SwiGLU) with GLU interleaving disabled, grouped FC2, and the
+  routing probability applied at the activation / combine boundary.
+* NVIDIA/Megatron-LM PR #7333, section "Summary": expert rows padded to a fixed
+  multiple (256) with device-resident per-expert metadata.
+
+Notation: T tokens, k routed slots per token, R = T*k routed rows, E experts,
+H hidden, F expert FFN width (FC1 produces 2F columns), P the per-expert row
+padding multiple and R_cap = T*k + E*(P-1). Weights are row-major per expert
+in nn.Linear [out, in] layout: W1[E, 2F, H], W2[E, H, F].
+
+Readings taken where the pages are silent (each also listed in the design notes):
+* gate/up order: GLU interleaving is disabled, so the 2F FC1 outputs are two
+  contiguous halves; the first F columns are the gate (SiLU side), the last F
+  the linear "up" side.
+* permutation order: expert-ascending, then (token, slot)-ascending, i.e. a
+  stable sort of the flattened pairs by expert id.
+* offsets: int32, E+1 entries, exclusive prefix sum of the padded counts.
+* the routing probability multiplies each expert's output in the combine (FC2
+  is linear and bias-free, so this equals weighting at the activation).
+* padding rows hold zeros and carry slot id -1.
+
+Two modes: exact fp64 (the pass/fail reference) and ``faithful=True``, which
+rounds to BF16 (nearest-even) exactly where the GPU path stores BF16. The
+faithful mode only sizes the error budget; it is never the parity reference.
+
+All functions take BF16 tensors as uint16 bit patterns or as float64 arrays
+that already hold BF16-representable values.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+# ---------------------------------------------------------------- BF16 helpers
+
+def bf16_bits_to_f64(u16: np.ndarray) -> np.ndarray:
+    """Exact value of BF16 bit patterns (BF16 is the top half of an fp32)."""
+    u32 = np.asarray(u16, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return u32.view(np.float32).astype(np.float64)
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Round fp64 values to the nearest BF16 value, ties to even.
+
+    BF16 keeps 8 significant bits. Writing x = m * 2**e with 0.5 <= |m| < 1,
+    the BF16 grid spacing near x is 2**(e-8); below the smallest normal
+    exponent the spacing stays at the subnormal step 2**-133. Overflow is not
+    handled (the workloads stay far from it).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)
+    e = np.maximum(e, -125)
+    scale = np.ldexp(1.0, 8 - e)
+    return np.rint(x * scale) / scale
+
+
+def _as_f64(a: np.ndarray) -> np.ndarray:
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return bf16_bits_to_f64(a)
+    return a.astype(np.float64)
+
+
+def _sigmoid(z: np.ndarray) -> np.ndarray:
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+# ---------------------------------------------------------------- row mapping
+
+def route(idx: np.ndarray, E: int, P: int = 1):
+    """Expert-contiguous row map of the routed (token, slot) pairs.
+
+    Expert e's rows are the pairs (t, j) with idx[t, j] == e, in ascending
+    (t, j) order, followed by zero rows up to a multiple of P. Returns
+    ``offsets[E+1]`` (exclusive prefix of padded counts), ``row_of_slot[T*k]``
+    (row of pair t*k+j) and ``slot_of_row[R_cap]`` (pair id of a row, -1 for
+    padding and for rows past offsets[E]).
+    """
+    idx = np.asarray(idx, dtype=np.int64)
+    T, k = idx.shape if idx.ndim == 2 else (0, 1)
+    flat = idx.reshape(-1)
+    if flat.size and (flat.min() < 0 or flat.max() >= E):
+        raise ValueError("expert id out of range")
+    R_cap = T * k + E * (P - 1)
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    row_of_slot = np.full(T * k, -1, dtype=np.int64)
+    slot_of_row = np.full(R_cap, -1, dtype=np.int64)
+    for e in range(E):
+        pairs = np.nonzero(flat == e)[0]  # ascending pair id = ascending (t, j)
+        cnt = pairs.size
+        padded = -(-cnt // P) * P
+        base = offsets[e]
+        row_of_slot[pairs] = base + np.arange(cnt)
+        slot_of_row[base:base + cnt] = pairs
+        offsets[e + 1] = base + padded
+    return offsets.astype(np.int32), row_of_slot.astype(np.int32), slot_of_row.astype(np.int32)
+
+
+def permute(x, idx, prob, E: int, P: int = 1):
+    """Gather the routed token rows into expert-contiguous order.
+
+    Returns Xp[R_cap, H] (fp64, zero on padding and unused rows), the row maps
+    and prob_of_row[R_cap] (the pair's probability, 0 on padding).
+    """
+    xf = _as_f64(x)
+    T, H = xf.shape
+    k = np.asarray(idx).shape[1]
+    offsets, row_of_slot, slot_of_row = route(np.asarray(idx).reshape(T, k), E, P)
+    R_cap = slot_of_row.size
+    Xp = np.zeros((R_cap, H), dtype=np.float64)
+    prob_of_row = np.zeros(R_cap, dtype=np.float64)
+    live = slot_of_row >= 0
+    Xp[live] = xf[slot_of_row[live] // k]
+    prob_of_row[live] = np.asarray(prob, dtype=np.float64).reshape(-1)[slot_of_row[live]]
+    return Xp, offsets, row_of_slot, slot_of_row, prob_of_row
+
+
+# ---------------------------------------------------------------- grouped GEMMs
+
+def grouped_linear(Xp: np.ndarray, W, offsets) -> np.ndarray:
+    """Y[rows of e] = Xp[rows of e] @ W[e]^T for every expert (nn.Linear)."""
+    Wf = _as_f64(W)
+    E, N, K = Wf.shape
+    Y = np.zeros((Xp.shape[0], N), dtype=np.float64)
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 > r0:
+            Y[r0:r1] = Xp[r0:r1] @ Wf[e].T
+    return Y
+
+
+def grouped_linear_t(dY: np.ndarray, W, offsets) -> np.ndarray:
+    """Input gradient of ``grouped_linear``: dX[rows of e] = dY[rows of e] @ W[e]."""
+    Wf = _as_f64(W)
+    E, N, K = Wf.shape
+    dX = np.zeros((dY.shape[0], K), dtype=np.float64)
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 > r0:
+            dX[r0:r1] = dY[r0:r1] @ Wf[e]
+    return dX
+
+
+# ---------------------------------------------------------------- activation
+
+def swiglu(H1: np.ndarray) -> np.ndarray:
+    """A = silu(g) * u with g the first and u the second half of FC1's output."""
+    F = H1.shape[1] // 2
+    g, u = H1[:, :F], H1[:, F:]
+    return g * _sigmoid(g) * u
+
+
+def swiglu_backward(dA: np.ndarray, H1: np.ndarray) -> np.ndarray:
+    """Gradient of ``swiglu`` w.r.t. its input [g, u], given dA.
+
+    d silu(g)/dg = s + g*s*(1-s) = s*(1 + g*(1-s)) with s = sigmoid(g);
+    dL/dg = dA * u * s*(1 + g*(1-s)),  dL/du = dA * g*s.
+    """
+    F = H1.shape[1] // 2
+    g, u = H1[:, :F], H1[:, F:]
+    s = _sigmoid(g)
+    dg = dA * u * s * (1.0 + g * (1.0 - s))
+    du = dA * g * s
+    return np.concatenate([dg, du], axis=1)
+
+
+# ---------------------------------------------------------------- combine
+
+def combine(Yp: np.ndarray, row_of_slot, prob, T: int, k: int) -> np.ndarray:
+    """out[t] = sum_j prob[t, j] * Yp[row_of_slot[t*k + j]], slots in order.
+
+    ``prob=None`` gives the unweighted sum (the input-gradient combine).
+    """
+    H = Yp.shape[1]
+    out = np.zeros((T, H), dtype=np.float64)
+    rows = np.asarray(row_of_slot, dtype=np.int64).reshape(T, k)
+    p = None if prob is None else np.asarray(prob, dtype=np.float64).reshape(T, k)
+    for j in range(k):
+        term = Yp[rows[:, j]]
+        out += term if p is None else p[:, j:j + 1] * term
+    return out
+
+
+# ---------------------------------------------------------------- full layer
+
+def moe_forward(x, idx, prob, W1, W2, E: int, P: int = 1, faithful: bool = False):
+    """Forward of the expert layer. Returns a dict of every intermediate.
+
+    Steps: permute -> FC1 (grouped) -> SwiGLU -> FC2 (grouped) -> weighted
+    combine. With ``faithful`` the values are rounded to BF16 where the GPU
+    path stores BF16 (H1, A, Yp, out).
+    """
+    rnd = round_to_bf16 if faithful else (lambda v: v)
+    idx = np.asarray(idx)
+    T = _as_f64(x).shape[0]
+    k = idx.shape[1] if idx.ndim == 2 else 1
+    Xp, offsets, row_of_slot, slot_of_row, prob_of_row = permute(x, idx, prob, E, P)
+    H1 = rnd(grouped_linear(Xp, W1, offsets))
+    A = rnd(swiglu(H1))
+    Yp = rnd(grouped_linear(A, W2, offsets))
+    out = rnd(combine(Yp, row_of_slot, prob, T, k))
+    return dict(Xp=Xp, offsets=offsets, row_of_slot=row_of_slot, slot_of_row=slot_of_row,
+                prob_of_row=prob_of_row, H1=H1, A=A, Yp=Yp, out=out, T=T, k=k, E=E, P=P)
+
+
+def moe_backward(dOut, fwd: dict, W1, W2, faithful: bool = False):
+    """Input gradient dX of ``moe_forward`` (weights are frozen: no dW).
+
+    dYp[r] = dOut[t] for the pair (t, j) of row r (0 on padding); the pair's
+    probability scales FC2's input gradient: dA = p_r * (dYp @ W2_e);
+    dH = SwiGLU'(H1) applied to dA; dXp = dH @ W1_e; dX[t] = sum_j dXp[row(t, j)].
+    With ``faithful`` the values are rounded to BF16 where the GPU path stores
+    BF16 (dH, dXp, dX).
+    """
+    rnd = round_to_bf16 if faithful else (lambda v: v)
+    dO = _as_f64(dOut)
+    T, k = fwd["T"], fwd["k"]
+    slot_of_row = fwd["slot_of_row"]
+    offsets = fwd["offsets"]
+    live = slot_of_row >= 0
+    dYp = np.zeros((slot_of_row.size, dO.shape[1]), dtype=np.float64)
+    dYp[live] = dO[slot_of_row[live] // k]
+    dA = fwd["prob_of_row"][:, None] * grouped_linear_t(dYp, W2, offsets)
+    dH = rnd(swiglu_backward(dA, fwd["H1"]))
+    dXp = rnd(grouped_linear_t(dH, W1, offsets))
+    dX = rnd(combine(dXp, fwd["row_of_slot"], None, T, k))
+    return dict(dYp=dYp, dH=dH, dXp=dXp, dX=dX)
+
+
+# ---------------------------------------------------------------- one token
+
+def token_forward(x_t, experts, probs, W1, W2) -> np.ndarray:
+    """Output of one token: sum over its routed experts of p * FC2(SwiGLU(FC1 x)).
+
+    ``W1``/``W2`` may be the full [E, ...] BF16 arrays (uint16 bits); only the
+    routed experts are converted. Used for sampled checks at full size.
+    """
+    xt = _as_f64(x_t).reshape(-1)
+    y = np.zeros_like(xt)
+    for e, p in zip(np.asarray(experts).reshape(-1), np.asarray(probs, dtype=np.float64).reshape(-1)):
+        w1 = _as_f64(W1[int(e)])
+        w2 = _as_f64(W2[int(e)])
+        h = w1 @ xt
+        F = h.size // 2
+        a = h[:F] * _sigmoid(h[:F]) * h[F:]
+        y += p * (w2 @ a)
+    return y
+
+
+def token_backward(x_t, dout_t, experts, probs, W1, W2) -> np.ndarray:
+    """Input gradient of ``token_forward`` for one token, given dOut[t]."""
+    xt = _as_f64(x_t).reshape(-1)
+    do = _as_f64(dout_t).reshape(-1)
+    dx = np.zeros_like(xt)
+    for e, p in zip(np.asarray(experts).reshape(-1), np.asarray(probs, dtype=np.float64).reshape(-1)):
+        w1 = _as_f64(W1[int(e)])
+        w2 = _as_f64(W2[int(e)])
+        h = w1 @ xt
+        F = h.size // 2
+        g, u = h[:F], h[F:]
+        s = _sigmoid(g)
+        da = p * (do @ w2)
+        dh = np.concatenate([da * u * s * (1.0 + g * (1.0 - s)), da * g * s])
+        dx += dh @ w1
+    return dx
