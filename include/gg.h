@@ -1,0 +1,284 @@
+/*
+ * gg.h — C ABI of the GB300 (sm_103) grouped expert MLP.
+ *
+ * One Mixture-of-Experts expert layer over frozen, bias-free BF16 expert
+ * weights with ragged per-expert token counts (experts with zero tokens are
+ * legal): the routed-token permute, grouped FC1 with a fused SwiGLU, grouped
+ * FC2, the probability-weighted unpermute/combine, and the input gradient
+ * (dgrad) through the same frozen weights. Each grouped GEMM is one persistent
+ * kernel launch over all experts that reads the per-expert row offsets from
+ * device memory, so no call synchronises with the host.
+ *
+ * Sources, by page title and section:
+ *  [P1] "perf(moe): add frozen grouped GEMM for adapter training"
+ *       (AlignmentResearch/Megatron-LM PR #3) — "Why this change": the frozen
+ *       base weights of all local experts go through one grouped kernel
+ *       instead of one small GEMM per expert; "Why existing behavior remains
+ *       safe": only grouped, frozen, bias-free BF16 expert weights are
+ *       accepted, everything else fails during preparation; each expert
+ *       parameter is a view into one contiguous buffer; forward output and
+ *       input gradient, empty batches and zero-token experts are covered.
+ *  [P2] "feat(moe+ssm): expert-LoRA GEMM stack and hybrid-recompute guard on
+ *       the d12f6c8c base" (AlignmentResearch/Megatron-LM issue #1) — "What's
+ *       in it": the grouped-offsets dtype and zero-token grouped-split
+ *       contracts.
+ *  [P3] NVIDIA/Megatron-LM PR #7333 — "Summary": device-metadata grouped GEMM
+ *       (per-expert sizes stay on the device), 256-row expert padding,
+ *       separate workspace per forward/dgrad layout, unsupported GPU/library
+ *       pairs fail explicitly, batch-invariant results.
+ *  [P4] "[Main] Support paged stash with device-initiated GroupedLinear"
+ *       (NVIDIA/Megatron-LM PR #6828) — "What does this PR do?": grouped FC1,
+ *       fused SwiGLU with GLU interleaving disabled, grouped FC2; the routing
+ *       probability is applied at the fused-activation boundary; unsupported
+ *       combinations are rejected instead of falling back.
+ *
+ * Notation: T tokens, k routed slots per token, E experts, H hidden size,
+ * F expert FFN width (FC1 has 2F outputs: gate = first F, up = last F),
+ * P per-expert row padding multiple, R_cap = T*k + E*(P-1) rows of every
+ * permuted buffer. All matrices are row-major. Weights use the nn.Linear
+ * [out, in] layout per expert and are packed contiguously over experts:
+ * W1[E][2F][H], W2[E][H][F].
+ *
+ * Conventions common to every call:
+ *  - All data pointers are DEVICE pointers owned by the caller; the library
+ *    allocates nothing and keeps no state besides cached device attributes and
+ *    the driver entry point used to encode TMA tensor maps. Tensor maps are
+ *    encoded per call, so rewriting an expert's weights needs no invalidation.
+ *  - BF16 tensors are passed as gg_bf16 (the 16-bit pattern). Every BF16
+ *    matrix pointer must be 16-byte aligned; H and F must be multiples of 64.
+ *  - Calls only enqueue work on `stream` (a cudaStream_t); none synchronises
+ *    and none allocates. gg_read_status() is the only call that waits.
+ *  - Arguments the host can check are checked before anything is launched;
+ *    a failing check returns its gg_status and enqueues nothing.
+ *  - Data errors only the device can see (an expert id outside [0, E),
+ *    offsets that are not a valid padded prefix sum, a bounded wait inside a
+ *    kernel that ran out) are written as a gg_status code into the status
+ *    word at the start of the workspace `ws` (first error wins); the kernels
+ *    skip the offending work and never trap. Read it with gg_read_status()
+ *    and clear it with gg_clear_status().
+ *  - The device must have compute capability 10.3 (GB300, sm_103); any other
+ *    device gets GG_ERR_UNSUPPORTED_DEVICE. There is no fallback path.
+ */
+#ifndef GG_H_
+#define GG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t gg_bf16;                 /* BF16 bit pattern */
+typedef struct CUstream_st* gg_stream_t;  /* same handle as cudaStream_t */
+
+typedef enum gg_status {
+  GG_OK = 0,
+  GG_ERR_INVALID_ARG = 1,          /* null pointer, negative size, k > E, ... */
+  GG_ERR_UNSUPPORTED_SHAPE = 2,    /* H or F not a multiple of 64, E > 1024, ... */
+  GG_ERR_MISALIGNED = 3,           /* a matrix pointer is not 16-byte aligned */
+  GG_ERR_WORKSPACE_TOO_SMALL = 4,
+  GG_ERR_UNSUPPORTED_DEVICE = 5,   /* not compute capability 10.3 */
+  GG_ERR_CUDA = 6,                 /* a CUDA runtime or driver call failed */
+  /* codes written by kernels into the workspace status word */
+  GG_ERR_DEVICE_BAD_EXPERT_ID = 16,  /* idx[t][j] outside [0, E): pair skipped */
+  GG_ERR_DEVICE_BAD_OFFSETS = 17,    /* offsets not monotone / offsets[E] > R_cap */
+  GG_ERR_DEVICE_BAD_ROW = 18,        /* a row map entry outside [-1, R_cap) */
+  GG_ERR_DEVICE_TIMEOUT = 19         /* a bounded in-kernel wait gave up */
+} gg_status;
+
+typedef enum gg_epilogue {
+  GG_EPI_NONE = 0,        /* store the BF16-rounded accumulator */
+  GG_EPI_SWIGLU = 1,      /* gg_grouped_fwd only: fused SwiGLU, see below */
+  GG_EPI_SWIGLU_BWD = 2   /* gg_grouped_dgrad only: fused SwiGLU backward */
+} gg_epilogue;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* gg_status_string(int status);
+
+/* Library version string, e.g. "gg 0.1 sm_103a". */
+const char* gg_version(void);
+
+/* Number of kernels this library has launched in this process (all devices,
+ * all threads). Lets a caller count the launches inside a timed region. */
+uint64_t gg_launch_count(void);
+
+/* Bytes of workspace every call below needs for a batch of T tokens with
+ * top-k routing over E experts. The first 256 bytes hold the status word;
+ * the rest is scratch for the permute's per-block expert histograms. */
+size_t gg_workspace_size(int T, int k, int E);
+
+/* Zero the status word at the start of `ws` (stream-ordered). */
+gg_status gg_clear_status(void* ws, gg_stream_t stream);
+
+/* Copy the status word to *host_status after all work queued on `stream`
+ * so far has finished. The only call that waits for the device. */
+gg_status gg_read_status(const void* ws, gg_stream_t stream, int32_t* host_status);
+
+/* ---------------------------------------------------------------------------
+ * gg_permute — routed-token permute ([P1] "B200 throughput evidence": ordinary
+ * all-to-all dispatch groups tokens by expert before the grouped GEMM; [P2]
+ * zero-token grouped-split contracts; [P3] 256-row expert padding).
+ *
+ * Stable counting sort of the T*k (token, slot) pairs by expert id: expert
+ * e's rows are its pairs in ascending (t, j) order, then zero rows up to a
+ * multiple of `pad_multiple` (P >= 1). Outputs:
+ *   offsets[E+1]      int32, offsets[0] = 0, offsets[e+1] - offsets[e] = the
+ *                     padded row count of expert e (0 for an empty expert);
+ *   row_of_slot[T*k]  int32, row of pair t*k+j (-1 if its id was invalid);
+ *   slot_of_row[R_cap] int32, pair id t*k+j of a row, -1 on padding rows and
+ *                     on rows >= offsets[E];
+ *   prob_of_row[R_cap] fp32, prob[t][j] of the row's pair, 0 on padding and
+ *                     on rows >= offsets[E];
+ *   Xp[R_cap][H]      BF16, Xp[row] = x[t]; zero on padding rows; rows
+ *                     >= offsets[E] are left untouched.
+ * Inputs: x[T][H] BF16, idx[T][k] int32 expert ids, prob[T][k] fp32; k <= 32.
+ * Indices are bit-exact and independent of scheduling. T = 0 only writes
+ * offsets (all zero). An id outside [0, E) sets GG_ERR_DEVICE_BAD_EXPERT_ID
+ * and that pair is dropped. Workspace: gg_workspace_size(T, k, E) bytes.
+ * ------------------------------------------------------------------------- */
+gg_status gg_permute(const gg_bf16* x, const int32_t* idx, const float* prob,
+                     int T, int H, int k, int E, int pad_multiple,
+                     gg_bf16* Xp, int32_t* offsets, int32_t* row_of_slot,
+                     int32_t* slot_of_row, float* prob_of_row,
+                     void* ws, size_t ws_bytes, gg_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gg_permute_rows — gather of a token-major tensor into the permuted row
+ * order of an earlier gg_permute (the combine's backward: the output
+ * gradient dOut[T][H] is routed to the rows its token was sent to).
+ *   dst[row] = src[slot_of_row[row] / k] for rows < offsets[E] with a valid
+ *   slot, zero on padding rows; rows >= offsets[E] are left untouched.
+ * src[T][H], dst[R_cap][H] BF16. The probability is NOT applied here; the
+ * dgrad FC2 epilogue applies it (prob_of_row) because FC2 is linear.
+ * ------------------------------------------------------------------------- */
+gg_status gg_permute_rows(const gg_bf16* src, const int32_t* slot_of_row,
+                          const int32_t* offsets, int T, int H, int k, int E,
+                          int R_cap, gg_bf16* dst, void* ws, size_t ws_bytes,
+                          gg_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gg_grouped_fwd — grouped GEMM over all experts in one persistent launch
+ * ([P1] "Why this change": one grouped kernel instead of one small GEMM per
+ * expert; [P3] "Summary": per-expert sizes read from device metadata).
+ *
+ * For every expert e and every row r in [offsets[e], offsets[e+1]):
+ *   acc[r][n] = sum_c A[r][c] * B[e][n][c]     (fp32 accumulation, n < N)
+ * A[R_cap][K] BF16 row-major, B[E][N][K] BF16 (nn.Linear weight per expert),
+ * offsets[E+1] int32 on the device. K and N must be multiples of 64.
+ *   GG_EPI_NONE:   C[R_cap][N]   = bf16(acc). H1_save must be NULL.
+ *   GG_EPI_SWIGLU: N = 2F; with g = bf16(acc[:, :F]) and u = bf16(acc[:, F:])
+ *                  ([P4] "What does this PR do?": fused SwiGLU, gate and up
+ *                  halves not interleaved), C[R_cap][F] = bf16(silu(g) * u)
+ *                  computed in fp32 from the rounded g and u, and, when
+ *                  H1_save is not NULL, H1_save[R_cap][2F] = [g, u] (kept
+ *                  for the backward pass).
+ * Rows outside [0, offsets[E]) are never written. Results of a row depend
+ * only on that row and its expert's weights (bitwise batch invariance).
+ * Offsets that are not monotone, do not start at 0 or end past R_cap set
+ * GG_ERR_DEVICE_BAD_OFFSETS and nothing is computed.
+ * ------------------------------------------------------------------------- */
+gg_status gg_grouped_fwd(const gg_bf16* A, const gg_bf16* B, const int32_t* offsets,
+                         int E, int R_cap, int K, int N, gg_epilogue epi,
+                         gg_bf16* C, gg_bf16* H1_save,
+                         void* ws, size_t ws_bytes, gg_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gg_swiglu — the unfused SwiGLU ([P4] "What does this PR do?") on a stored
+ * FC1 output, bitwise identical to the GG_EPI_SWIGLU epilogue:
+ *   A[r][j] = bf16(silu(H1[r][j]) * H1[r][F + j]) in fp32, r < offsets[E].
+ * H1[R_cap][2F], A[R_cap][F] BF16; F a multiple of 64.
+ * ------------------------------------------------------------------------- */
+gg_status gg_swiglu(const gg_bf16* H1, const int32_t* offsets, int E, int R_cap,
+                    int F, gg_bf16* A, gg_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gg_grouped_dgrad — input gradient of gg_grouped_fwd through the same
+ * frozen weights ([P1] "Why existing behavior remains safe": input-gradient
+ * parity; the weights get no gradient). B is the FORWARD weight B[E][N][K];
+ * the kernel reads it transposed (N-contiguous) straight from that layout:
+ *   acc[r][c] = sum_n dC[r][n] * B[e][n][c]    (fp32, c < K)
+ * dC[R_cap][N] BF16. K and N multiples of 64.
+ *   prob_of_row (nullable): acc[r][:] *= prob_of_row[r] in fp32 first
+ *                  ([P4]: the routing probability at the activation boundary).
+ *   GG_EPI_NONE:   dA[R_cap][K] = bf16(acc). H1 must be NULL.
+ *   GG_EPI_SWIGLU_BWD: the SwiGLU backward with K = F, using the saved
+ *                  H1[R_cap][2F] = [g, u] (BF16) and s = sigmoid(g):
+ *                    dA[r][j]     = bf16(acc * u * s * (1 + g * (1 - s)))
+ *                    dA[r][F + j] = bf16(acc * g * s)
+ *                  so dA is [R_cap][2F] (the gradient w.r.t. FC1's output).
+ * Rows outside [0, offsets[E]) are never written.
+ * ------------------------------------------------------------------------- */
+gg_status gg_grouped_dgrad(const gg_bf16* dC, const gg_bf16* B, const int32_t* offsets,
+                           int E, int R_cap, int K, int N, gg_epilogue epi,
+                           const gg_bf16* H1, const float* prob_of_row, gg_bf16* dA,
+                           void* ws, size_t ws_bytes, gg_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gg_unpermute_combine — probability-weighted combine ([P4] "What does this
+ * PR do?": the probability boundary; [P1]: the all-to-all combine side):
+ *   out[t] = bf16( sum_{j<k} prob[t][j] * Yp[row_of_slot[t*k+j]] )
+ * accumulated in fp32 in slot order j = 0..k-1 and rounded once. prob NULL
+ * gives the unweighted sum (the input-gradient combine). Pairs whose row is
+ * -1 contribute nothing. Yp[R_cap][H], out[T][H] BF16; k <= 32. A row outside
+ * [-1, R_cap) sets GG_ERR_DEVICE_BAD_ROW and is skipped.
+ * ------------------------------------------------------------------------- */
+gg_status gg_unpermute_combine(const gg_bf16* Yp, const int32_t* row_of_slot,
+                               const float* prob, int T, int k, int H, int R_cap,
+                               gg_bf16* out, void* ws, size_t ws_bytes,
+                               gg_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Whole expert layer. The caller owns one device buffer that holds every
+ * intermediate; gg_moe_buffers_bind() carves it (256-byte aligned pieces).
+ * ------------------------------------------------------------------------- */
+typedef struct gg_moe_buffers {
+  gg_bf16* Xp;          /* [R_cap][H]  permuted input                     */
+  gg_bf16* H1;          /* [R_cap][2F] FC1 output (BF16), kept for dgrad  */
+  gg_bf16* A;           /* [R_cap][F]  SwiGLU output                      */
+  gg_bf16* Yp;          /* [R_cap][H]  FC2 output                         */
+  gg_bf16* dYp;         /* [R_cap][H]  permuted output gradient           */
+  gg_bf16* dH;          /* [R_cap][2F] gradient w.r.t. FC1 output         */
+  gg_bf16* dXp;         /* [R_cap][H]  gradient w.r.t. permuted input     */
+  int32_t* offsets;     /* [E+1]                                          */
+  int32_t* row_of_slot; /* [T*k]                                          */
+  int32_t* slot_of_row; /* [R_cap]                                        */
+  float* prob_of_row;   /* [R_cap]                                        */
+  void* ws;             /* gg_workspace_size(T, k, E) bytes, status first */
+  size_t ws_bytes;
+} gg_moe_buffers;
+
+/* Bytes of the single buffer gg_moe_buffers_bind() carves. */
+size_t gg_moe_buffers_size(int T, int H, int F, int k, int E, int pad_multiple);
+
+/* Fill *out with pointers into `base` (device memory, 256-byte aligned,
+ * `bytes` >= gg_moe_buffers_size(...)). Host-only; enqueues nothing. */
+gg_status gg_moe_buffers_bind(void* base, size_t bytes, int T, int H, int F, int k,
+                              int E, int pad_multiple, gg_moe_buffers* out);
+
+/* Forward: permute -> grouped FC1 + fused SwiGLU (H1 kept) -> grouped FC2
+ * -> probability-weighted combine into out[T][H]. Four stages, all on
+ * `stream`, no host synchronisation. */
+gg_status gg_moe_mlp_fwd(const gg_bf16* x, const int32_t* idx, const float* prob,
+                         const gg_bf16* W1, const gg_bf16* W2,
+                         int T, int H, int F, int k, int E, int pad_multiple,
+                         gg_bf16* out, const gg_moe_buffers* buf, gg_stream_t stream);
+
+/* Input gradient of gg_moe_mlp_fwd (same buffers, after the forward):
+ * permute dOut -> dgrad FC2 with probability scale and fused SwiGLU
+ * backward -> dgrad FC1 -> unweighted combine into dX[T][H]. */
+gg_status gg_moe_mlp_bwd(const gg_bf16* dOut, const gg_bf16* W1, const gg_bf16* W2,
+                         int T, int H, int F, int k, int E, int pad_multiple,
+                         gg_bf16* dX, const gg_moe_buffers* buf, gg_stream_t stream);
+
+/* Test hook for the bounded waits: one CTA waits on a barrier that nothing
+ * completes, gives up after `limit_ns` nanoseconds (clamped to 1 s), writes
+ * GG_ERR_DEVICE_TIMEOUT into the status word and returns normally. */
+gg_status gg_selftest_bounded_wait(void* ws, size_t ws_bytes, uint64_t limit_ns,
+                                   gg_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GG_H_ */

@@ -1,0 +1,410 @@
+// gg_api.cu — the C ABI declared in include/gg.h: argument validation,
+// workspace layout, device checks, and the composed forward / input-gradient
+// of the expert layer. Host code only; kernels live in gg_permute.cu and
+// gg_gemm.cu.
+//
+// Validation rules follow "perf(moe): add frozen grouped GEMM for adapter
+// training" (AlignmentResearch/Megatron-LM PR #3), "Why existing behavior
+// remains safe" (only grouped, frozen, bias-free BF16 expert weights; other
+// configurations fail during preparation), NVIDIA/Megatron-LM PR #7333
+// "Summary" (other GPU/library pairs fail explicitly) and "[Main] Support
+// paged stash with device-initiated GroupedLinear" (NVIDIA/Megatron-LM PR
+// #6828), "What does this PR do?" (reject instead of falling back).
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include "gg_internal.h"
+
+namespace gg {
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+
+struct DevCache {
+  std::once_flag once;
+  DeviceInfo info;
+  gg_status status = GG_ERR_CUDA;
+};
+DevCache g_dev[64];
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline gg_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GG_OK : GG_ERR_CUDA; }
+
+inline int32_t* status_ptr(void* ws) { return static_cast<int32_t*>(ws); }
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+gg_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
+  if (ws == nullptr) return GG_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return GG_ERR_MISALIGNED;
+  if (ws_bytes < need) return GG_ERR_WORKSPACE_TOO_SMALL;
+  return GG_OK;
+}
+
+gg_status device_ok(DeviceInfo* dev) {
+  gg_status s = current_device(dev);
+  if (s != GG_OK) return s;
+  if (dev->cc_major != 10 || dev->cc_minor != 3) return GG_ERR_UNSUPPORTED_DEVICE;
+  return GG_OK;
+}
+
+long long r_cap_of(int T, int k, int E, int P) {
+  return static_cast<long long>(T) * k + static_cast<long long>(E) * (P - 1);
+}
+}  // namespace
+
+void count_launch(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
+
+gg_status current_device(DeviceInfo* out) {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return GG_ERR_CUDA;
+  DevCache& c = g_dev[d];
+  std::call_once(c.once, [&c, d] {
+    DeviceInfo i;
+    i.device = d;
+    if (cudaDeviceGetAttribute(&i.sm_count, cudaDevAttrMultiProcessorCount, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&i.cc_major, cudaDevAttrComputeCapabilityMajor, d) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&i.cc_minor, cudaDevAttrComputeCapabilityMinor, d) !=
+            cudaSuccess) {
+      c.status = GG_ERR_CUDA;
+      return;
+    }
+    c.info = i;
+    c.status = GG_OK;
+  });
+  *out = c.info;
+  return c.status;
+}
+
+}  // namespace gg
+
+using namespace gg;
+
+extern "C" {
+
+const char* gg_status_string(int status) {
+  switch (status) {
+    case GG_OK: return "GG_OK";
+    case GG_ERR_INVALID_ARG: return "GG_ERR_INVALID_ARG: invalid argument";
+    case GG_ERR_UNSUPPORTED_SHAPE: return "GG_ERR_UNSUPPORTED_SHAPE: unsupported shape";
+    case GG_ERR_MISALIGNED: return "GG_ERR_MISALIGNED: pointer not 16-byte aligned";
+    case GG_ERR_WORKSPACE_TOO_SMALL: return "GG_ERR_WORKSPACE_TOO_SMALL: workspace too small";
+    case GG_ERR_UNSUPPORTED_DEVICE:
+      return "GG_ERR_UNSUPPORTED_DEVICE: needs compute capability 10.3";
+    case GG_ERR_CUDA: return "GG_ERR_CUDA: a CUDA call failed";
+    case GG_ERR_DEVICE_BAD_EXPERT_ID:
+      return "GG_ERR_DEVICE_BAD_EXPERT_ID: expert id out of range";
+    case GG_ERR_DEVICE_BAD_OFFSETS: return "GG_ERR_DEVICE_BAD_OFFSETS: invalid expert offsets";
+    case GG_ERR_DEVICE_BAD_ROW: return "GG_ERR_DEVICE_BAD_ROW: row map entry out of range";
+    case GG_ERR_DEVICE_TIMEOUT:
+      return "GG_ERR_DEVICE_TIMEOUT: a bounded in-kernel wait ran out";
+    default: return "unknown gg_status";
+  }
+}
+
+const char* gg_version(void) { return "gg 0.1 sm_103a"; }
+
+uint64_t gg_launch_count(void) { return g_launches.load(); }
+
+size_t gg_workspace_size(int T, int k, int E) {
+  if (T < 0 || k < 0 || E <= 0) return 0;
+  const long long R = static_cast<long long>(T) * k;
+  const size_t hist = sizeof(int32_t) * static_cast<size_t>(permute_blocks(R)) * E;
+  return kWsHeader + align256(hist);
+}
+
+gg_status gg_clear_status(void* ws, gg_stream_t stream) {
+  if (ws == nullptr) return GG_ERR_INVALID_ARG;
+  return from_cuda(
+      cudaMemsetAsync(ws, 0, sizeof(int32_t), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gg_status gg_read_status(const void* ws, gg_stream_t stream, int32_t* host_status) {
+  if (ws == nullptr || host_status == nullptr) return GG_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(host_status, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return GG_ERR_CUDA;
+  return from_cuda(cudaStreamSynchronize(s));
+}
+
+gg_status gg_permute(const gg_bf16* x, const int32_t* idx, const float* prob, int T, int H,
+                     int k, int E, int pad_multiple, gg_bf16* Xp, int32_t* offsets,
+                     int32_t* row_of_slot, int32_t* slot_of_row, float* prob_of_row, void* ws,
+                     size_t ws_bytes, gg_stream_t stream) {
+  if (T < 0 || H <= 0 || k <= 0 || E <= 0 || pad_multiple <= 0) return GG_ERR_INVALID_ARG;
+  if (k > E || k > 32) return GG_ERR_INVALID_ARG;
+  if (E > kMaxExperts || H % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
+  if (r_cap_of(T, k, E, pad_multiple) > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
+  if (offsets == nullptr) return GG_ERR_INVALID_ARG;
+  if (T > 0 && (x == nullptr || idx == nullptr || prob == nullptr || Xp == nullptr ||
+                row_of_slot == nullptr || slot_of_row == nullptr || prob_of_row == nullptr))
+    return GG_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Xp)) return GG_ERR_MISALIGNED;
+  gg_status s = check_ws(ws, ws_bytes, gg_workspace_size(T, k, E));
+  if (s != GG_OK) return s;
+  DeviceInfo dev;
+  if ((s = device_ok(&dev)) != GG_OK) return s;
+  int32_t* block_hist = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + kWsHeader);
+  return from_cuda(launch_permute(x, idx, prob, T, H, k, E, pad_multiple, Xp, offsets,
+                                  row_of_slot, slot_of_row, prob_of_row, status_ptr(ws),
+                                  block_hist, dev.sm_count,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gg_status gg_permute_rows(const gg_bf16* src, const int32_t* slot_of_row, const int32_t* offsets,
+                          int T, int H, int k, int E, int R_cap, gg_bf16* dst, void* ws,
+                          size_t ws_bytes, gg_stream_t stream) {
+  if (T < 0 || H <= 0 || k <= 0 || E <= 0 || R_cap < 0) return GG_ERR_INVALID_ARG;
+  if (E > kMaxExperts || H % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
+  if (offsets == nullptr || ws == nullptr) return GG_ERR_INVALID_ARG;
+  if (R_cap > 0 && (src == nullptr || slot_of_row == nullptr || dst == nullptr))
+    return GG_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst)) return GG_ERR_MISALIGNED;
+  gg_status s = check_ws(ws, ws_bytes, kWsHeader);
+  if (s != GG_OK) return s;
+  DeviceInfo dev;
+  if ((s = device_ok(&dev)) != GG_OK) return s;
+  return from_cuda(launch_gather_rows(src, slot_of_row, offsets, H, k, E, R_cap, T, dst,
+                                      status_ptr(ws), dev.sm_count,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static gg_status gemm_common_checks(const gg_bf16* A, const gg_bf16* B, const int32_t* offsets,
+                                    int E, int R_cap, int K, int N, const gg_bf16* C, void* ws,
+                                    size_t ws_bytes) {
+  if (E <= 0 || R_cap < 0 || K <= 0 || N <= 0) return GG_ERR_INVALID_ARG;
+  if (A == nullptr || B == nullptr || offsets == nullptr || C == nullptr)
+    return GG_ERR_INVALID_ARG;
+  if (E > kMaxExperts || K % 64 != 0 || N % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return GG_ERR_MISALIGNED;
+  return check_ws(ws, ws_bytes, kWsHeader);
+}
+
+gg_status gg_grouped_fwd(const gg_bf16* A, const gg_bf16* B, const int32_t* offsets, int E,
+                         int R_cap, int K, int N, gg_epilogue epi, gg_bf16* C, gg_bf16* H1_save,
+                         void* ws, size_t ws_bytes, gg_stream_t stream) {
+  gg_status s = gemm_common_checks(A, B, offsets, E, R_cap, K, N, C, ws, ws_bytes);
+  if (s != GG_OK) return s;
+  if (epi != GG_EPI_NONE && epi != GG_EPI_SWIGLU) return GG_ERR_INVALID_ARG;
+  if (epi == GG_EPI_NONE && H1_save != nullptr) return GG_ERR_INVALID_ARG;
+  if (epi == GG_EPI_SWIGLU && N % 128 != 0) return GG_ERR_UNSUPPORTED_SHAPE;  // F % 64
+  if (!aligned16(H1_save)) return GG_ERR_MISALIGNED;
+  DeviceInfo dev;
+  if ((s = device_ok(&dev)) != GG_OK) return s;
+  if (R_cap == 0) return GG_OK;
+  GemmArgs a{};
+  a.mode = epi == GG_EPI_SWIGLU ? kFwdSwiglu : kFwdPlain;
+  a.A = A;
+  a.B = B;
+  a.offsets = offsets;
+  a.E = E;
+  a.R_cap = R_cap;
+  a.Kred = K;
+  a.Nout = N;
+  a.Nw = N;
+  a.Kw = K;
+  a.C = C;
+  a.H1_save = H1_save;
+  a.status = status_ptr(ws);
+  gg_status he = GG_OK;
+  cudaError_t e = launch_grouped_gemm(a, dev, reinterpret_cast<cudaStream_t>(stream), &he);
+  if (he != GG_OK) return he;
+  return from_cuda(e);
+}
+
+gg_status gg_swiglu(const gg_bf16* H1, const int32_t* offsets, int E, int R_cap, int F,
+                    gg_bf16* A, gg_stream_t stream) {
+  if (E <= 0 || R_cap < 0 || F <= 0) return GG_ERR_INVALID_ARG;
+  if (H1 == nullptr || offsets == nullptr || A == nullptr) return GG_ERR_INVALID_ARG;
+  if (E > kMaxExperts || F % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(H1) || !aligned16(A)) return GG_ERR_MISALIGNED;
+  DeviceInfo dev;
+  gg_status s = device_ok(&dev);
+  if (s != GG_OK) return s;
+  return from_cuda(launch_swiglu(H1, offsets, E, R_cap, F, A, dev.sm_count,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gg_status gg_grouped_dgrad(const gg_bf16* dC, const gg_bf16* B, const int32_t* offsets, int E,
+                           int R_cap, int K, int N, gg_epilogue epi, const gg_bf16* H1,
+                           const float* prob_of_row, gg_bf16* dA, void* ws, size_t ws_bytes,
+                           gg_stream_t stream) {
+  gg_status s = gemm_common_checks(dC, B, offsets, E, R_cap, K, N, dA, ws, ws_bytes);
+  if (s != GG_OK) return s;
+  if (epi != GG_EPI_NONE && epi != GG_EPI_SWIGLU_BWD) return GG_ERR_INVALID_ARG;
+  if (epi == GG_EPI_NONE && H1 != nullptr) return GG_ERR_INVALID_ARG;
+  if (epi == GG_EPI_SWIGLU_BWD && H1 == nullptr) return GG_ERR_INVALID_ARG;
+  if (!aligned16(H1)) return GG_ERR_MISALIGNED;
+  DeviceInfo dev;
+  if ((s = device_ok(&dev)) != GG_OK) return s;
+  if (R_cap == 0) return GG_OK;
+  GemmArgs a{};
+  a.mode = epi == GG_EPI_SWIGLU_BWD ? kDgradSwigluBwd : kDgradPlain;
+  a.A = dC;
+  a.B = B;
+  a.offsets = offsets;
+  a.E = E;
+  a.R_cap = R_cap;
+  a.Kred = N;
+  a.Nout = K;
+  a.Nw = N;
+  a.Kw = K;
+  a.C = dA;
+  a.H1 = H1;
+  a.row_scale = prob_of_row;
+  a.status = status_ptr(ws);
+  gg_status he = GG_OK;
+  cudaError_t e = launch_grouped_gemm(a, dev, reinterpret_cast<cudaStream_t>(stream), &he);
+  if (he != GG_OK) return he;
+  return from_cuda(e);
+}
+
+gg_status gg_unpermute_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const float* prob,
+                               int T, int k, int H, int R_cap, gg_bf16* out, void* ws,
+                               size_t ws_bytes, gg_stream_t stream) {
+  if (T < 0 || k <= 0 || k > 32 || H <= 0 || R_cap < 0) return GG_ERR_INVALID_ARG;
+  if (H % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
+  if (T > 0 && (Yp == nullptr || row_of_slot == nullptr || out == nullptr))
+    return GG_ERR_INVALID_ARG;
+  if (!aligned16(Yp) || !aligned16(out)) return GG_ERR_MISALIGNED;
+  gg_status s = check_ws(ws, ws_bytes, kWsHeader);
+  if (s != GG_OK) return s;
+  DeviceInfo dev;
+  if ((s = device_ok(&dev)) != GG_OK) return s;
+  return from_cuda(launch_combine(Yp, row_of_slot, prob, T, k, H, R_cap, out, status_ptr(ws),
+                                  dev.sm_count, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// ------------------------------------------------------------------ composite
+
+size_t gg_moe_buffers_size(int T, int H, int F, int k, int E, int pad_multiple) {
+  if (T < 0 || H <= 0 || F <= 0 || k <= 0 || E <= 0 || pad_multiple <= 0) return 0;
+  const size_t R_cap = static_cast<size_t>(r_cap_of(T, k, E, pad_multiple));
+  const size_t b2 = sizeof(gg_bf16);
+  size_t n = 0;
+  n += align256(R_cap * H * b2) * 4;         // Xp, Yp, dYp, dXp
+  n += align256(R_cap * 2 * F * b2) * 2;     // H1, dH
+  n += align256(R_cap * F * b2);             // A
+  n += align256(sizeof(int32_t) * (E + 1));  // offsets
+  n += align256(sizeof(int32_t) * static_cast<size_t>(T) * k);  // row_of_slot
+  n += align256(sizeof(int32_t) * R_cap);    // slot_of_row
+  n += align256(sizeof(float) * R_cap);      // prob_of_row
+  n += align256(gg_workspace_size(T, k, E)); // workspace (status first)
+  return n;
+}
+
+gg_status gg_moe_buffers_bind(void* base, size_t bytes, int T, int H, int F, int k, int E,
+                              int pad_multiple, gg_moe_buffers* out) {
+  if (base == nullptr || out == nullptr) return GG_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(base) & 255u) return GG_ERR_MISALIGNED;
+  const size_t need = gg_moe_buffers_size(T, H, F, k, E, pad_multiple);
+  if (need == 0) return GG_ERR_INVALID_ARG;
+  if (bytes < need) return GG_ERR_WORKSPACE_TOO_SMALL;
+  const size_t R_cap = static_cast<size_t>(r_cap_of(T, k, E, pad_multiple));
+  uint8_t* p = static_cast<uint8_t*>(base);
+  auto take = [&p](size_t n) {
+    uint8_t* q = p;
+    p += align256(n);
+    return q;
+  };
+  const size_t b2 = sizeof(gg_bf16);
+  std::memset(out, 0, sizeof(*out));
+  out->Xp = reinterpret_cast<gg_bf16*>(take(R_cap * H * b2));
+  out->Yp = reinterpret_cast<gg_bf16*>(take(R_cap * H * b2));
+  out->dYp = reinterpret_cast<gg_bf16*>(take(R_cap * H * b2));
+  out->dXp = reinterpret_cast<gg_bf16*>(take(R_cap * H * b2));
+  out->H1 = reinterpret_cast<gg_bf16*>(take(R_cap * 2 * F * b2));
+  out->dH = reinterpret_cast<gg_bf16*>(take(R_cap * 2 * F * b2));
+  out->A = reinterpret_cast<gg_bf16*>(take(R_cap * F * b2));
+  out->offsets = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (E + 1)));
+  out->row_of_slot =
+      reinterpret_cast<int32_t*>(take(sizeof(int32_t) * static_cast<size_t>(T) * k));
+  out->slot_of_row = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * R_cap));
+  out->prob_of_row = reinterpret_cast<float*>(take(sizeof(float) * R_cap));
+  out->ws_bytes = align256(gg_workspace_size(T, k, E));
+  out->ws = take(out->ws_bytes);
+  return GG_OK;
+}
+
+static gg_status check_buffers(const gg_moe_buffers* b, int T, int k, int E) {
+  if (b == nullptr) return GG_ERR_INVALID_ARG;
+  if (b->Xp == nullptr || b->H1 == nullptr || b->A == nullptr || b->Yp == nullptr ||
+      b->dYp == nullptr || b->dH == nullptr || b->dXp == nullptr || b->offsets == nullptr ||
+      b->row_of_slot == nullptr || b->slot_of_row == nullptr || b->prob_of_row == nullptr)
+    return GG_ERR_INVALID_ARG;
+  return check_ws(b->ws, b->ws_bytes, gg_workspace_size(T, k, E));
+}
+
+gg_status gg_moe_mlp_fwd(const gg_bf16* x, const int32_t* idx, const float* prob,
+                         const gg_bf16* W1, const gg_bf16* W2, int T, int H, int F, int k, int E,
+                         int pad_multiple, gg_bf16* out, const gg_moe_buffers* buf,
+                         gg_stream_t stream) {
+  if (T < 0 || H <= 0 || k <= 0 || E <= 0 || pad_multiple <= 0) return GG_ERR_INVALID_ARG;
+  gg_status s = check_buffers(buf, T, k, E);
+  if (s != GG_OK) return s;
+  if (W1 == nullptr || W2 == nullptr || F <= 0) return GG_ERR_INVALID_ARG;
+  if (F % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
+  if (T > 0 && out == nullptr) return GG_ERR_INVALID_ARG;
+  const long long rc = r_cap_of(T, k, E, pad_multiple);
+  if (rc > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
+  const int R_cap = static_cast<int>(rc);
+  s = gg_permute(x, idx, prob, T, H, k, E, pad_multiple, buf->Xp, buf->offsets, buf->row_of_slot,
+                 buf->slot_of_row, buf->prob_of_row, buf->ws, buf->ws_bytes, stream);
+  if (s != GG_OK || T == 0) return s;
+  s = gg_grouped_fwd(buf->Xp, W1, buf->offsets, E, R_cap, H, 2 * F, GG_EPI_SWIGLU, buf->A,
+                     buf->H1, buf->ws, buf->ws_bytes, stream);
+  if (s != GG_OK) return s;
+  s = gg_grouped_fwd(buf->A, W2, buf->offsets, E, R_cap, F, H, GG_EPI_NONE, buf->Yp, nullptr,
+                     buf->ws, buf->ws_bytes, stream);
+  if (s != GG_OK) return s;
+  return gg_unpermute_combine(buf->Yp, buf->row_of_slot, prob, T, k, H, R_cap, out, buf->ws,
+                              buf->ws_bytes, stream);
+}
+
+gg_status gg_moe_mlp_bwd(const gg_bf16* dOut, const gg_bf16* W1, const gg_bf16* W2, int T, int H,
+                         int F, int k, int E, int pad_multiple, gg_bf16* dX,
+                         const gg_moe_buffers* buf, gg_stream_t stream) {
+  if (T < 0 || H <= 0 || k <= 0 || E <= 0 || pad_multiple <= 0 || F <= 0)
+    return GG_ERR_INVALID_ARG;
+  gg_status s = check_buffers(buf, T, k, E);
+  if (s != GG_OK) return s;
+  if (W1 == nullptr || W2 == nullptr) return GG_ERR_INVALID_ARG;
+  if (F % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return GG_OK;
+  if (dOut == nullptr || dX == nullptr) return GG_ERR_INVALID_ARG;
+  const long long rc = r_cap_of(T, k, E, pad_multiple);
+  if (rc > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
+  const int R_cap = static_cast<int>(rc);
+  s = gg_permute_rows(dOut, buf->slot_of_row, buf->offsets, T, H, k, E, R_cap, buf->dYp, buf->ws,
+                      buf->ws_bytes, stream);
+  if (s != GG_OK) return s;
+  // dH = SwiGLU'(H1) applied to prob_of_row * (dYp @ W2_e); W2 is [E][H][F]
+  s = gg_grouped_dgrad(buf->dYp, W2, buf->offsets, E, R_cap, F, H, GG_EPI_SWIGLU_BWD, buf->H1,
+                       buf->prob_of_row, buf->dH, buf->ws, buf->ws_bytes, stream);
+  if (s != GG_OK) return s;
+  // dXp = dH @ W1_e; W1 is [E][2F][H]
+  s = gg_grouped_dgrad(buf->dH, W1, buf->offsets, E, R_cap, H, 2 * F, GG_EPI_NONE, nullptr,
+                       nullptr, buf->dXp, buf->ws, buf->ws_bytes, stream);
+  if (s != GG_OK) return s;
+  return gg_unpermute_combine(buf->dXp, buf->row_of_slot, nullptr, T, k, H, R_cap, dX, buf->ws,
+                              buf->ws_bytes, stream);
+}
+
+gg_status gg_selftest_bounded_wait(void* ws, size_t ws_bytes, uint64_t limit_ns,
+                                   gg_stream_t stream) {
+  gg_status s = check_ws(ws, ws_bytes, kWsHeader);
+  if (s != GG_OK) return s;
+  DeviceInfo dev;
+  if ((s = device_ok(&dev)) != GG_OK) return s;
+  if (limit_ns > 1000000000ull) limit_ns = 1000000000ull;
+  return from_cuda(launch_bounded_wait_selftest(status_ptr(ws), limit_ns,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

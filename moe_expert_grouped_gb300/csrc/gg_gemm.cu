@@ -1,0 +1,547 @@
+// gg_gemm.cu — the persistent grouped GEMM of the expert layer on sm_103a.
+//
+// One launch covers every expert ("perf(moe): add frozen grouped GEMM for
+// adapter training", AlignmentResearch/Megatron-LM PR #3, "Why this change":
+// one grouped kernel instead of one small GEMM per expert). Per-expert row
+// counts are read from the device-resident offsets array (NVIDIA/Megatron-LM
+// PR #7333, "Summary": device metadata, no host synchronisation).
+//
+// Design (one CTA per SM, 192 threads, warp-specialised):
+//   warp 0     TMA producer: A tile 128 x 64 and B tile 256 x 64 (BF16,
+//              128-byte swizzle) per stage into a 4-stage shared-memory ring;
+//   warp 1     allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
+//              and one elected lane issues tcgen05.mma (M=128, N=256, K=16);
+//   warps 2-5  epilogue: tcgen05.ld the accumulator (one TMEM lane = one
+//              output row per thread), fused SwiGLU / SwiGLU-backward /
+//              probability scale, BF16 stores masked to the expert's rows.
+// The two accumulators let the epilogue of tile i overlap the MMAs of tile
+// i+1. Tiles are (expert, 128-row block, 256-column block), enumerated
+// expert-major with the column block fastest and dealt round-robin to CTAs.
+// A row block that runs past its expert's last row reads the next expert's
+// rows (or TMA zero fill past R_cap) and those rows are simply not stored:
+// every output row depends only on its own input row and its expert's weight
+// (bitwise batch invariance).
+//
+// The dgrad variants read the forward weight [E][N][K] as an N-contiguous
+// ("MN-major") B operand straight from its forward layout, so no transposed
+// copy of the frozen weights exists.
+//
+// Every wait is bounded (gg_ptx.cuh); a wait that runs out records
+// GG_ERR_DEVICE_TIMEOUT, raises a CTA-wide abort flag, and the CTA drains its
+// in-flight TMA loads and MMAs, frees TMEM and exits.
+
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "gg_internal.h"
+#include "gg_ptx.cuh"
+
+namespace gg {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KB
+constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 512;
+
+struct SmemTail {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+  int total_tiles;
+  int pad_;
+  int tiles_before[kMaxExperts + 1];
+  int row_start[kMaxExperts + 1];
+};
+
+constexpr size_t kSmemBytes = 1024 + STAGES * STAGE_BYTES + sizeof(SmemTail);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+struct KParams {
+  const int32_t* offsets;
+  int E;
+  int R_cap;
+  int Kred;
+  int Nout;
+  int F;
+  int NT;
+  gg_bf16* C;
+  long long ldc;
+  gg_bf16* H1_save;
+  const gg_bf16* H1;
+  const float* row_scale;
+  int32_t* status;
+};
+
+__device__ __forceinline__ void decode_tile(int tile, const int* tb, int E, int NT, int& e,
+                                            int& mt, int& nt) {
+  int lo = 0, hi = E;  // tb[lo] <= tile < tb[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tb[mid] <= tile)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  e = lo;
+  const int local = tile - tb[lo];
+  mt = local / NT;
+  nt = local - mt * NT;
+}
+
+__device__ __forceinline__ void store_bf16x32(gg_bf16* dst, const float (&v)[32], float scale) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 o;
+    o.x = pack_bf16x2(__fmul_rn(v[8 * i + 0], scale), __fmul_rn(v[8 * i + 1], scale));
+    o.y = pack_bf16x2(__fmul_rn(v[8 * i + 2], scale), __fmul_rn(v[8 * i + 3], scale));
+    o.z = pack_bf16x2(__fmul_rn(v[8 * i + 4], scale), __fmul_rn(v[8 * i + 5], scale));
+    o.w = pack_bf16x2(__fmul_rn(v[8 * i + 6], scale), __fmul_rn(v[8 * i + 7], scale));
+    d[i] = o;
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
+                    const __grid_constant__ CUtensorMap mapB, const KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw_addr + pad;  // 1024-aligned: required by the 128B swizzle
+  SmemTail& st = *reinterpret_cast<SmemTail*>(smem + STAGES * STAGE_BYTES);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int E = p.E;
+  const int NT = p.NT;
+  const int KB = p.Kred / BK;
+
+  // ---- tile table from the device offsets (warp 0), TMEM (warp 1)
+  if (warp == 0) {
+    bool bad = false;
+    int carry = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      int tiles = 0;
+      if (e < E) {
+        const int o0 = p.offsets[e];
+        const int o1 = p.offsets[e + 1];
+        if (o1 < o0) bad = true;
+        tiles = o1 > o0 ? ((o1 - o0 + BM - 1) / BM) * NT : 0;
+        st.row_start[e] = o0;
+      }
+      int incl = tiles;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += n;
+      }
+      if (e < E) st.tiles_before[e] = carry + incl - tiles;
+      carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (lane == 0) {
+      const int o_first = p.offsets[0];
+      const int o_last = p.offsets[E];
+      if (o_first != 0 || o_last > p.R_cap || o_last < 0) bad = true;
+      st.row_start[E] = o_last;
+      st.tiles_before[E] = carry;
+    }
+    bad = __any_sync(0xFFFFFFFFu, bad);
+    if (lane == 0) {
+      st.total_tiles = bad ? 0 : carry;
+      st.abort_flag = 0;
+      if (bad && blockIdx.x == 0) set_status(p.status, GG_ERR_DEVICE_BAD_OFFSETS);
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) {
+        mbar_init(smem_u32(&st.full[s]), 1);
+        mbar_init(smem_u32(&st.empty[s]), 1);
+      }
+      for (int a = 0; a < 2; ++a) {
+        mbar_init(smem_u32(&st.tfull[a]), 1);
+        mbar_init(smem_u32(&st.tempty[a]), 128);
+      }
+      mbar_init(smem_u32(&st.mma_done), 1);
+      mbar_fence_init();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+  } else if (warp == 1) {
+    tmem_alloc(smem_u32(&st.tmem_base), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem_base = st.tmem_base;
+  const int total = st.total_tiles;
+  volatile int* abort_flag = &st.abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      tma_prefetch_desc(&mapA);
+      tma_prefetch_desc(&mapB);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t used = 0, last_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        int e, mt, nt;
+        decode_tile(tile, st.tiles_before, E, NT, e, mt, nt);
+        const int row0 = st.row_start[e] + mt * BM;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&st.empty[stage]), phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&st.full[stage]);
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t sa = sbase + stage * A_BYTES;
+          const uint32_t sb = sbase + STAGES * A_BYTES + stage * B_BYTES;
+          tma_load_2d(sa, &mapA, fb, kb * BK, row0);
+          if (MODE == kFwdPlain) {
+            tma_load_3d(sb, &mapB, fb, kb * BK, nt * BN, e);
+          } else if (MODE == kFwdSwiglu) {
+            const int j0 = nt * (BN / 2);
+            tma_load_3d(sb, &mapB, fb, kb * BK, j0, e);
+            tma_load_3d(sb + B_BYTES / 2, &mapB, fb, kb * BK, p.F + j0, e);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_3d(sb + j * (B_BYTES / 4), &mapB, fb, nt * BN + 64 * j, kb * BK, e);
+          }
+          used |= 1u << stage;
+          last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every issued load must have landed before the CTA may exit.
+      for (int s = 0; s < STAGES; ++s)
+        if (used & (1u << s))
+          (void)mbar_wait_bounded(smem_u32(&st.full[s]), (last_phase >> s) & 1u, nullptr,
+                                  p.status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      constexpr bool kMN = (MODE == kDgradPlain || MODE == kDgradSwigluBwd);
+      constexpr uint32_t idesc = make_idesc_bf16(BM, BN, kMN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        if (!mbar_wait_bounded(smem_u32(&st.tempty[acc]), acc_phase ^ 1u, abort_flag, p.status))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&st.full[stage]), phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = sbase + stage * A_BYTES;
+          const uint32_t sb = sbase + STAGES * A_BYTES + stage * B_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t adesc = make_sdesc(sa + kk * 32, 16, 1024);
+            const uint64_t bdesc = kMN ? make_sdesc(sb + kk * 2048, B_BYTES / 4, 1024)
+                                       : make_sdesc(sb + kk * 32, 16, 1024);
+            tc_mma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&st.empty[stage]));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&st.tfull[acc]));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // All MMAs of this thread must retire before TMEM is freed.
+      tc_commit(smem_u32(&st.mma_done));
+      (void)mbar_wait_bounded(smem_u32(&st.mma_done), 0, nullptr, p.status);
+    }
+  } else {
+    // -------------------------------------------------- epilogue (128 threads)
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int r = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, mt, nt;
+      decode_tile(tile, st.tiles_before, E, NT, e, mt, nt);
+      const long long grow = static_cast<long long>(st.row_start[e]) + mt * BM + r;
+      const bool valid = grow < st.row_start[e + 1];
+      if (!mbar_wait_bounded(smem_u32(&st.tfull[acc]), acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+
+      if (MODE == kFwdPlain || MODE == kDgradPlain) {
+        float scale = 1.0f;
+        if (MODE == kDgradPlain && p.row_scale != nullptr && valid) scale = p.row_scale[grow];
+        const int n0 = nt * BN;
+        gg_bf16* crow = p.C + grow * p.ldc + n0;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          if (n0 + c >= p.Nout) break;
+          float v[32];
+          tmem_ld32(tbase + c, v);
+          if (valid) store_bf16x32(crow + c, v, scale);
+        }
+      } else if (MODE == kFwdSwiglu) {
+        const int F = p.F;
+        const int j0 = nt * (BN / 2);
+        gg_bf16* arow = p.C + grow * F + j0;
+        gg_bf16* hrow = p.H1_save != nullptr ? p.H1_save + grow * (2LL * F) + j0 : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          if (j0 + c >= F) break;
+          float g[32], u[32];
+          tmem_ld32(tbase + c, g);
+          tmem_ld32(tbase + BN / 2 + c, u);
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              g[i] = round_bf16(g[i]);
+              u[i] = round_bf16(u[i]);
+            }
+            if (hrow != nullptr) {
+              store_bf16x32(hrow + c, g, 1.0f);
+              store_bf16x32(hrow + F + c, u, 1.0f);
+            }
+            float a[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] = silu_mul(g[i], u[i]);
+            store_bf16x32(arow + c, a, 1.0f);
+          }
+        }
+      } else {  // kDgradSwigluBwd: F = Nout, output row [dg | du] of width 2F
+        const int F = p.Nout;
+        float scale = 1.0f;
+        if (p.row_scale != nullptr && valid) scale = p.row_scale[grow];
+        const int n0 = nt * BN;
+        const gg_bf16* hrow = p.H1 + grow * (2LL * F) + n0;
+        gg_bf16* drow = p.C + grow * (2LL * F) + n0;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          if (n0 + c >= F) break;
+          float v[32];
+          tmem_ld32(tbase + c, v);
+          if (valid) {
+            const uint4* gp = reinterpret_cast<const uint4*>(hrow + c);
+            const uint4* up = reinterpret_cast<const uint4*>(hrow + F + c);
+            uint4 gw[4], uw[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              gw[i] = __ldg(gp + i);
+              uw[i] = __ldg(up + i);
+            }
+            float dg[32], du[32];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t gs[4] = {gw[i].x, gw[i].y, gw[i].z, gw[i].w};
+              const uint32_t us[4] = {uw[i].x, uw[i].y, uw[i].z, uw[i].w};
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                const int i0 = 8 * i + 2 * h;
+                silu_mul_bwd(__fmul_rn(v[i0], scale), bf16_lo(gs[h]), bf16_lo(us[h]), dg[i0],
+                             du[i0]);
+                silu_mul_bwd(__fmul_rn(v[i0 + 1], scale), bf16_hi(gs[h]), bf16_hi(us[h]),
+                             dg[i0 + 1], du[i0 + 1]);
+              }
+            }
+            store_bf16x32(drow + c, dg, 1.0f);
+            store_bf16x32(drow + F + c, du, 1.0f);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&st.tempty[acc]));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// Standalone SwiGLU over rows [0, offsets[E]) — same arithmetic as the fused
+// FC1 epilogue (silu_mul on the BF16 values of g and u).
+__global__ void __launch_bounds__(256)
+swiglu_kernel(const uint4* __restrict__ H1, const int32_t* __restrict__ offsets, int E, int F,
+              uint4* __restrict__ A) {
+  const long long rows = offsets[E];
+  const int vec = F / 8;
+  const long long n = rows * vec;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = i / vec;
+    const int c = static_cast<int>(i - r * vec);
+    const uint4 gw = __ldg(H1 + r * (2LL * vec) + c);
+    const uint4 uw = __ldg(H1 + r * (2LL * vec) + vec + c);
+    const uint32_t gs[4] = {gw.x, gw.y, gw.z, gw.w};
+    const uint32_t us[4] = {uw.x, uw.y, uw.z, uw.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+      o[h] = pack_bf16x2(silu_mul(bf16_lo(gs[h]), bf16_lo(us[h])),
+                         silu_mul(bf16_hi(gs[h]), bf16_hi(us[h])));
+    A[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+bool encode_bf16_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                     const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint32_t elem_strides[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+                        const_cast<void*>(base), dims, strides_bytes, box, elem_strides,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& kp,
+                        const DeviceInfo& dev, cudaStream_t stream) {
+  static int configured_for[64] = {0};
+  const int d = dev.device & 63;
+  if (!configured_for[d]) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    configured_for[d] = 1;
+  }
+  grouped_gemm_kernel<MODE><<<dev.sm_count, kThreads, kSmemBytes, stream>>>(ma, mb, kp);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t stream,
+                                gg_status* host_err) {
+  *host_err = GG_OK;
+  CUtensorMap ma, mb;
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.Kred), static_cast<cuuint64_t>(a.R_cap)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.Kred) * 2};
+    const cuuint32_t box[2] = {BK, BM};
+    if (!encode_bf16_map(&ma, a.A, 2, dims, strides, box)) {
+      *host_err = GG_ERR_CUDA;
+      return cudaErrorInvalidValue;
+    }
+  }
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.Kw), static_cast<cuuint64_t>(a.Nw),
+                                static_cast<cuuint64_t>(a.E)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.Kw) * 2,
+                                   static_cast<cuuint64_t>(a.Kw) * a.Nw * 2};
+    cuuint32_t box[3] = {BK, BN, 1};
+    if (a.mode == kFwdSwiglu) box[1] = BN / 2;
+    if (a.mode == kDgradPlain || a.mode == kDgradSwigluBwd) box[1] = 64;
+    if (!encode_bf16_map(&mb, a.B, 3, dims, strides, box)) {
+      *host_err = GG_ERR_CUDA;
+      return cudaErrorInvalidValue;
+    }
+  }
+  KParams kp{};
+  kp.offsets = a.offsets;
+  kp.E = a.E;
+  kp.R_cap = a.R_cap;
+  kp.Kred = a.Kred;
+  kp.Nout = a.Nout;
+  kp.C = a.C;
+  kp.H1_save = a.H1_save;
+  kp.H1 = a.H1;
+  kp.row_scale = a.row_scale;
+  kp.status = a.status;
+  switch (a.mode) {
+    case kFwdPlain:
+      kp.F = 0;
+      kp.NT = (a.Nout + BN - 1) / BN;
+      kp.ldc = a.Nout;
+      return launch_mode<kFwdPlain>(ma, mb, kp, dev, stream);
+    case kFwdSwiglu:
+      kp.F = a.Nout / 2;
+      kp.NT = (kp.F + BN / 2 - 1) / (BN / 2);
+      kp.ldc = kp.F;
+      return launch_mode<kFwdSwiglu>(ma, mb, kp, dev, stream);
+    case kDgradPlain:
+      kp.F = 0;
+      kp.NT = (a.Nout + BN - 1) / BN;
+      kp.ldc = a.Nout;
+      return launch_mode<kDgradPlain>(ma, mb, kp, dev, stream);
+    case kDgradSwigluBwd:
+      kp.F = a.Nout;
+      kp.NT = (a.Nout + BN - 1) / BN;
+      kp.ldc = 2LL * a.Nout;
+      return launch_mode<kDgradSwigluBwd>(ma, mb, kp, dev, stream);
+  }
+  *host_err = GG_ERR_INVALID_ARG;
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_swiglu(const gg_bf16* H1, const int32_t* offsets, int E, int R_cap, int F,
+                          gg_bf16* A, int sm_count, cudaStream_t stream) {
+  if (R_cap <= 0) return cudaSuccess;
+  const long long n = static_cast<long long>(R_cap) * (F / 8);
+  long long blocks = (n + 255) / 256;
+  const long long cap = static_cast<long long>(sm_count) * 8;
+  if (blocks > cap) blocks = cap;
+  swiglu_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+      reinterpret_cast<const uint4*>(H1), offsets, E, F, reinterpret_cast<uint4*>(A));
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace gg

@@ -1,0 +1,85 @@
+// gg_internal.h — declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/gg.h"
+
+namespace gg {
+
+// Workspace layout: [0, 256) status word + reserved; then the permute's
+// per-block expert histograms (int32 [n_blocks][E]).
+constexpr size_t kWsHeader = 256;
+constexpr int kPermuteBlockThreads = 256;
+constexpr int kPermutePairsPerWarp = 256;  // 8 steps of 32 pairs
+constexpr int kPermutePairsPerBlock = kPermutePairsPerWarp * (kPermuteBlockThreads / 32);
+constexpr int kMaxExperts = 1024;
+
+inline int permute_blocks(long long pairs) {
+  return static_cast<int>((pairs + kPermutePairsPerBlock - 1) / kPermutePairsPerBlock);
+}
+
+void count_launch(int n = 1);
+
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int cc_major = 0;
+  int cc_minor = 0;
+};
+
+// Attributes of the current device (cached per device).
+gg_status current_device(DeviceInfo* out);
+
+// ------------------------------------------------------------------ gg_permute.cu
+cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* prob, int T, int H,
+                           int k, int E, int P, gg_bf16* Xp, int32_t* offsets,
+                           int32_t* row_of_slot, int32_t* slot_of_row, float* prob_of_row,
+                           int32_t* status, int32_t* block_hist, int sm_count,
+                           cudaStream_t stream);
+
+cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* slot_of_row,
+                               const int32_t* offsets, int H, int k, int E, int R_cap,
+                               long long n_src_rows, gg_bf16* dst, int32_t* status, int sm_count,
+                               cudaStream_t stream);
+
+cudaError_t launch_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const float* prob,
+                           int T, int k, int H, int R_cap, gg_bf16* out, int32_t* status,
+                           int sm_count, cudaStream_t stream);
+
+cudaError_t launch_bounded_wait_selftest(int32_t* status, uint64_t limit_ns, cudaStream_t stream);
+
+// ------------------------------------------------------------------ gg_gemm.cu
+enum GemmMode : int {
+  kFwdPlain = 0,
+  kFwdSwiglu = 1,
+  kDgradPlain = 2,
+  kDgradSwigluBwd = 3,
+};
+
+struct GemmArgs {
+  GemmMode mode;
+  const gg_bf16* A;        // [R_cap][Kred] activations (K-major)
+  const gg_bf16* B;        // [E][Nw][Kw] forward weight
+  const int32_t* offsets;  // [E+1]
+  int E, R_cap;
+  int Kred;                // reduction length
+  int Nout;                // accumulator columns that exist (fwd: N, dgrad: K of the weight)
+  int Nw, Kw;              // forward weight dims
+  gg_bf16* C;              // output
+  gg_bf16* H1_save;        // fwd SwiGLU: [R_cap][2F] or null
+  const gg_bf16* H1;       // dgrad SwiGLU backward: [R_cap][2F]
+  const float* row_scale;  // dgrad: prob_of_row or null
+  int32_t* status;
+};
+
+cudaError_t launch_grouped_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t stream,
+                                gg_status* host_err);
+
+cudaError_t launch_swiglu(const gg_bf16* H1, const int32_t* offsets, int E, int R_cap, int F,
+                          gg_bf16* A, int sm_count, cudaStream_t stream);
+
+}  // namespace gg

@@ -1,0 +1,383 @@
+// gg_permute.cu — memory-bound kernels of the expert layer: the routed-token
+// permute (stable counting sort of (token, slot) pairs by expert plus the row
+// gather), the gather of a token-major gradient into permuted order, and the
+// probability-weighted combine. Sources: "perf(moe): add frozen grouped GEMM
+// for adapter training" (AlignmentResearch/Megatron-LM PR #3), "B200
+// throughput evidence" (tokens grouped by expert after all-to-all dispatch);
+// NVIDIA/Megatron-LM PR #7333 "Summary" (256-row expert padding); "[Main]
+// Support paged stash with device-initiated GroupedLinear" (NVIDIA/Megatron-LM
+// PR #6828), "What does this PR do?" (probability boundary).
+//
+// Determinism: every index is computed by counting, never by atomics whose
+// order matters, so row maps are bit-exact and run-to-run identical. The
+// combine sums a token's k slots in slot order in fp32 with one rounding.
+
+#include <cuda_runtime.h>
+
+#include "gg_internal.h"
+#include "gg_ptx.cuh"
+
+namespace gg {
+namespace {
+
+constexpr int kWarps = kPermuteBlockThreads / 32;
+constexpr int kSteps = kPermutePairsPerWarp / 32;
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Per-warp expert histogram of this block's pairs, into hist[warp][E].
+// Pairs with an id outside [0, E) are ignored (and reported).
+__device__ __forceinline__ void warp_histogram(const int32_t* __restrict__ idx, long long R, int E,
+                                               long long block_first, int* hist,
+                                               int32_t* status) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* h = hist + warp * E;
+  const long long first = block_first + static_cast<long long>(warp) * kPermutePairsPerWarp;
+#pragma unroll 1
+  for (int step = 0; step < kSteps; ++step) {
+    const long long p = first + step * 32 + lane;
+    int e = -1;
+    if (p < R) {
+      e = idx[p];
+      if (e < 0 || e >= E) {
+        set_status(status, GG_ERR_DEVICE_BAD_EXPERT_ID);
+        e = -1;
+      }
+    }
+    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+    if (e >= 0 && (peers & lanemask_lt()) == 0) h[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+__global__ void __launch_bounds__(kPermuteBlockThreads)
+permute_count_kernel(const int32_t* __restrict__ idx, long long R, int E,
+                     int32_t* __restrict__ block_hist, int32_t* status) {
+  extern __shared__ int hist[];  // [kWarps][E]
+  for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const long long first = static_cast<long long>(blockIdx.x) * kPermutePairsPerBlock;
+  warp_histogram(idx, R, E, first, hist, status);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int s = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s += hist[w * E + e];
+    block_hist[static_cast<long long>(blockIdx.x) * E + e] = s;
+  }
+}
+
+// One block: per expert, exclusive prefix of the block histograms (in place),
+// then offsets[] = exclusive prefix of the padded per-expert counts.
+__global__ void __launch_bounds__(1024)
+permute_scan_kernel(int32_t* __restrict__ block_hist, int nb, int E, int P,
+                    int32_t* __restrict__ offsets) {
+  __shared__ int part_sum[1024];
+  __shared__ int warp_tot[32];
+  const int parts = max(1, static_cast<int>(blockDim.x) / E);
+  const int t = threadIdx.x;
+  const int e = t % E;
+  const int part = t / E;
+  const bool active = part < parts && t < parts * E;
+  int b0 = 0, b1 = 0;
+  if (active) {
+    b0 = static_cast<int>((static_cast<long long>(nb) * part) / parts);
+    b1 = static_cast<int>((static_cast<long long>(nb) * (part + 1)) / parts);
+  }
+  // (1) each (expert, part) sums its blocks
+  int s = 0;
+  if (active)
+    for (int b = b0; b < b1; ++b) s += block_hist[static_cast<long long>(b) * E + e];
+  part_sum[t] = active ? s : 0;
+  __syncthreads();
+  // (2) exclusive prefix across parts, then rewrite the blocks in place
+  if (active) {
+    int run = 0;
+    for (int q = 0; q < part; ++q) run += part_sum[q * E + e];
+    for (int b = b0; b < b1; ++b) {
+      const long long i = static_cast<long long>(b) * E + e;
+      const int c = block_hist[i];
+      block_hist[i] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  // (3) padded totals per expert, exclusive scan over experts
+  for (int base = 0; base < E; base += blockDim.x) {
+    const int ee = base + t;
+    int padded = 0;
+    if (ee < E) {
+      int cnt = 0;
+      for (int q = 0; q < parts; ++q) cnt += part_sum[q * E + ee];
+      padded = ((cnt + P - 1) / P) * P;
+    }
+    // block-wide inclusive scan of `padded`
+    int v = padded;
+    const int lane = t & 31, warp = t >> 5;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int n = __shfl_up_sync(0xFFFFFFFFu, v, d);
+      if (lane >= d) v += n;
+    }
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int w = (lane < static_cast<int>(blockDim.x >> 5)) ? warp_tot[lane] : 0;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, w, d);
+        if (lane >= d) w += n;
+      }
+      warp_tot[lane] = w;
+    }
+    __syncthreads();
+    const int carry = (base == 0) ? 0 : offsets[base];
+    const int incl = v + (warp > 0 ? warp_tot[warp - 1] : 0) + carry;
+    if (ee < E) offsets[ee + 1] = incl;
+    if (ee == 0) offsets[0] = 0;
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(kPermuteBlockThreads)
+permute_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict__ prob,
+                       long long R, int E, const int32_t* __restrict__ block_prefix,
+                       const int32_t* __restrict__ offsets, int32_t* __restrict__ row_of_slot,
+                       int32_t* __restrict__ slot_of_row, float* __restrict__ prob_of_row) {
+  extern __shared__ int hist[];  // [kWarps][E]: counts, then running row bases
+  for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const long long first = static_cast<long long>(blockIdx.x) * kPermutePairsPerBlock;
+  warp_histogram(idx, R, E, first, hist, nullptr);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = offsets[e] + block_prefix[static_cast<long long>(blockIdx.x) * E + e];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = hist[w * E + e];
+      hist[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* base = hist + warp * E;
+  const long long wfirst = first + static_cast<long long>(warp) * kPermutePairsPerWarp;
+#pragma unroll 1
+  for (int step = 0; step < kSteps; ++step) {
+    const long long p = wfirst + step * 32 + lane;
+    int e = -1;
+    if (p < R) {
+      e = idx[p];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+    int row = -1;
+    if (e >= 0) row = base[e] + __popc(peers & lanemask_lt());
+    __syncwarp();
+    if (e >= 0 && (peers & lanemask_lt()) == 0) base[e] += __popc(peers);
+    __syncwarp();
+    if (p < R) {
+      row_of_slot[p] = row;
+      if (row >= 0) {
+        slot_of_row[row] = static_cast<int32_t>(p);
+        prob_of_row[row] = prob[p];
+      }
+    }
+  }
+}
+
+// dst[row] = src[slot_of_row[row] / k] (zero where the slot is -1) for rows
+// below offsets[E]; one warp per row, 16-byte vectors, grid-stride.
+__global__ void __launch_bounds__(256)
+gather_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ slot_of_row,
+                   const int32_t* __restrict__ offsets, int E, int k, int vec_per_row,
+                   long long n_src_rows, uint4* __restrict__ dst, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const long long n_rows = offsets[E];
+  const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long r = warp0; r < n_rows; r += nwarps) {
+    const int s = slot_of_row[r];
+    uint4* d = dst + r * vec_per_row;
+    if (s < 0) {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      for (int c = lane; c < vec_per_row; c += 32) d[c] = z;
+      continue;
+    }
+    const long long t = s / k;
+    if (t >= n_src_rows) {
+      if (lane == 0) set_status(status, GG_ERR_DEVICE_BAD_ROW);
+      continue;
+    }
+    const uint4* sp = src + t * vec_per_row;
+    int c = lane;
+    for (; c + 96 < vec_per_row; c += 128) {
+      const uint4 a0 = __ldg(sp + c), a1 = __ldg(sp + c + 32), a2 = __ldg(sp + c + 64),
+                  a3 = __ldg(sp + c + 96);
+      d[c] = a0;
+      d[c + 32] = a1;
+      d[c + 64] = a2;
+      d[c + 96] = a3;
+    }
+    for (; c < vec_per_row; c += 32) d[c] = __ldg(sp + c);
+  }
+}
+
+// out[t] = bf16(sum_j prob[t][j] * Yp[row_of_slot[t*k+j]]), fp32 in slot
+// order; prob == nullptr gives the plain sum. One warp per token.
+__global__ void __launch_bounds__(256)
+combine_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row_of_slot,
+               const float* __restrict__ prob, int T, int k, int vec_per_row, int R_cap,
+               uint4* __restrict__ out, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int warp0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = warp0; t < T; t += nwarps) {
+    int my_row = -1;
+    float my_p = 1.0f;
+    if (lane < k) {
+      my_row = row_of_slot[static_cast<long long>(t) * k + lane];
+      if (prob != nullptr) my_p = prob[static_cast<long long>(t) * k + lane];
+      if (my_row < -1 || my_row >= R_cap) {
+        set_status(status, GG_ERR_DEVICE_BAD_ROW);
+        my_row = -1;
+      }
+    }
+    // The column loop is warp-uniform so that the shuffles below see every lane.
+    for (int c0 = 0; c0 < vec_per_row; c0 += 32) {
+      const int c = c0 + lane;
+      const bool col_ok = c < vec_per_row;
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      for (int j0 = 0; j0 < k; j0 += 8) {
+        uint4 v[8];
+        int rows[8];
+        float ps[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int j = j0 + jj;
+          rows[jj] = __shfl_sync(0xFFFFFFFFu, my_row, j & 31);
+          ps[jj] = __shfl_sync(0xFFFFFFFFu, my_p, j & 31);
+          if (j >= k || !col_ok) rows[jj] = -1;
+          v[jj] = rows[jj] >= 0 ? __ldg(Yp + static_cast<long long>(rows[jj]) * vec_per_row + c)
+                                : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          if (rows[jj] < 0) continue;
+          const uint32_t w[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            acc[2 * q] = __fmaf_rn(ps[jj], bf16_lo(w[q]), acc[2 * q]);
+            acc[2 * q + 1] = __fmaf_rn(ps[jj], bf16_hi(w[q]), acc[2 * q + 1]);
+          }
+        }
+      }
+      if (col_ok) {
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        out[static_cast<long long>(t) * vec_per_row + c] = o;
+      }
+    }
+  }
+}
+
+__global__ void bounded_wait_selftest_kernel(int32_t* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    mbar_fence_init();
+    abort_flag = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // Nothing ever arrives on `bar`: the wait must give up on its own.
+    (void)mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, status, limit_ns);
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* prob, int T, int H,
+                           int k, int E, int P, gg_bf16* Xp, int32_t* offsets,
+                           int32_t* row_of_slot, int32_t* slot_of_row, float* prob_of_row,
+                           int32_t* status, int32_t* block_hist, int sm_count,
+                           cudaStream_t stream) {
+  const long long R = static_cast<long long>(T) * k;
+  const long long R_cap = R + static_cast<long long>(E) * (P - 1);
+  const int nb = permute_blocks(R);
+  const size_t hist_smem = sizeof(int) * kWarps * E;
+  cudaError_t err;
+  if (R == 0) {
+    // No routed pairs: only the offsets (all zero) are written.
+    permute_scan_kernel<<<1, 1024, 0, stream>>>(block_hist, 0, E, P, offsets);
+    count_launch();
+    return cudaGetLastError();
+  }
+  err = cudaMemsetAsync(slot_of_row, 0xFF, sizeof(int32_t) * R_cap, stream);
+  if (err != cudaSuccess) return err;
+  err = cudaMemsetAsync(prob_of_row, 0, sizeof(float) * R_cap, stream);
+  if (err != cudaSuccess) return err;
+  permute_count_kernel<<<nb, kPermuteBlockThreads, hist_smem, stream>>>(idx, R, E, block_hist,
+                                                                        status);
+  count_launch();
+  permute_scan_kernel<<<1, 1024, 0, stream>>>(block_hist, nb, E, P, offsets);
+  count_launch();
+  permute_scatter_kernel<<<nb, kPermuteBlockThreads, hist_smem, stream>>>(
+      idx, prob, R, E, block_hist, offsets, row_of_slot, slot_of_row, prob_of_row);
+  count_launch();
+  err = launch_gather_rows(x, slot_of_row, offsets, H, k, E, static_cast<int>(R_cap), T, Xp,
+                           status, sm_count, stream);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* slot_of_row,
+                               const int32_t* offsets, int H, int k, int E, int R_cap,
+                               long long n_src_rows, gg_bf16* dst, int32_t* status, int sm_count,
+                               cudaStream_t stream) {
+  if (R_cap <= 0) return cudaSuccess;
+  const int vec = H / 8;
+  long long blocks = (static_cast<long long>(R_cap) + 7) / 8;
+  const long long cap = static_cast<long long>(sm_count) * 8;
+  if (blocks > cap) blocks = cap;
+  gather_rows_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+      reinterpret_cast<const uint4*>(src), slot_of_row, offsets, E, k, vec, n_src_rows,
+      reinterpret_cast<uint4*>(dst), status);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const float* prob,
+                           int T, int k, int H, int R_cap, gg_bf16* out, int32_t* status,
+                           int sm_count, cudaStream_t stream) {
+  if (T <= 0) return cudaSuccess;
+  const int vec = H / 8;
+  long long blocks = (static_cast<long long>(T) + 7) / 8;
+  const long long cap = static_cast<long long>(sm_count) * 8;
+  if (blocks > cap) blocks = cap;
+  combine_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+      reinterpret_cast<const uint4*>(Yp), row_of_slot, prob, T, k, vec, R_cap,
+      reinterpret_cast<uint4*>(out), status);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bounded_wait_selftest(int32_t* status, uint64_t limit_ns, cudaStream_t stream) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace gg

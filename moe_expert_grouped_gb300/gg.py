@@ -1,0 +1,296 @@
+"""ctypes binding of libgg.so (the C ABI in include/gg.h).
+
+Argument marshalling only: every step of the expert path runs in the CUDA
+kernels of libgg.so. torch tensors supply device pointers and the current
+stream; outputs that the caller does not pass are allocated with torch (memory
+plumbing, no compute). If libgg.so is missing the import fails loudly; there
+is no CPU fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgg.so")
+
+GG_OK = 0
+GG_EPI_NONE, GG_EPI_SWIGLU, GG_EPI_SWIGLU_BWD = 0, 1, 2
+STATUS_NAMES = {
+    0: "GG_OK", 1: "GG_ERR_INVALID_ARG", 2: "GG_ERR_UNSUPPORTED_SHAPE", 3: "GG_ERR_MISALIGNED",
+    4: "GG_ERR_WORKSPACE_TOO_SMALL", 5: "GG_ERR_UNSUPPORTED_DEVICE", 6: "GG_ERR_CUDA",
+    16: "GG_ERR_DEVICE_BAD_EXPERT_ID", 17: "GG_ERR_DEVICE_BAD_OFFSETS", 18: "GG_ERR_DEVICE_BAD_ROW",
+    19: "GG_ERR_DEVICE_TIMEOUT",
+}
+
+# (name, restype, argtypes) of every exported symbol in include/gg.h
+_P, _I, _Z, _U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint64
+SIGNATURES = [
+    ("gg_status_string", ctypes.c_char_p, [_I]),
+    ("gg_version", ctypes.c_char_p, []),
+    ("gg_launch_count", _U64, []),
+    ("gg_workspace_size", _Z, [_I, _I, _I]),
+    ("gg_clear_status", _I, [_P, _P]),
+    ("gg_read_status", _I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
+    ("gg_permute", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    ("gg_permute_rows", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
+    ("gg_grouped_fwd", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
+    ("gg_swiglu", _I, [_P, _P, _I, _I, _I, _P, _P]),
+    ("gg_grouped_dgrad", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
+    ("gg_unpermute_combine", _I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P]),
+    ("gg_moe_buffers_size", _Z, [_I, _I, _I, _I, _I, _I]),
+    ("gg_moe_buffers_bind", _I, [_P, _Z, _I, _I, _I, _I, _I, _I, _P]),
+    ("gg_moe_mlp_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
+    ("gg_moe_mlp_bwd", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
+    ("gg_selftest_bounded_wait", _I, [_P, _Z, _U64, _P]),
+]
+
+
+class GGBuffers(ctypes.Structure):
+    """Mirror of struct gg_moe_buffers."""
+
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "Xp", "H1", "A", "Yp", "dYp", "dH", "dXp", "offsets", "row_of_slot", "slot_of_row",
+        "prob_of_row", "ws")] + [("ws_bytes", ctypes.c_size_t)]
+
+
+class GGError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)}")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built; run `python -m moe_expert_grouped_gb300.build` "
+            "(the expert path has no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, res, args in SIGNATURES:
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+LIB = _load()
+
+
+def _check(code: int, where: str) -> None:
+    if code != GG_OK:
+        raise GGError(code, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype: torch.dtype, shape, name: str) -> None:
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def launch_count() -> int:
+    return int(LIB.gg_launch_count())
+
+
+def version() -> str:
+    return LIB.gg_version().decode()
+
+
+def status_string(code: int) -> str:
+    return LIB.gg_status_string(int(code)).decode()
+
+
+def workspace(T: int, k: int, E: int, device) -> torch.Tensor:
+    """A zeroed workspace (status word first) for calls on a batch of T tokens."""
+    n = int(LIB.gg_workspace_size(T, k, E))
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def read_status(ws: torch.Tensor) -> int:
+    v = ctypes.c_int32(0)
+    _check(LIB.gg_read_status(_ptr(ws), _stream(ws.device), ctypes.byref(v)), "gg_read_status")
+    return int(v.value)
+
+
+def clear_status(ws: torch.Tensor) -> None:
+    _check(LIB.gg_clear_status(_ptr(ws), _stream(ws.device)), "gg_clear_status")
+
+
+def r_cap(T: int, k: int, E: int, P: int) -> int:
+    return T * k + E * (P - 1)
+
+
+def permute(x, idx, prob, E: int, P: int = 1, ws=None, out=None):
+    """gg_permute: returns dict(Xp, offsets, row_of_slot, slot_of_row, prob_of_row, ws)."""
+    T, H = x.shape
+    k = idx.shape[1]
+    dev = x.device
+    rc = r_cap(T, k, E, P)
+    _need(x, torch.bfloat16, (T, H), "x")
+    _need(idx, torch.int32, (T, k), "idx")
+    _need(prob, torch.float32, (T, k), "prob")
+    o = out or {}
+    Xp = o.get("Xp", torch.empty((rc, H), dtype=torch.bfloat16, device=dev))
+    offsets = o.get("offsets", torch.empty(E + 1, dtype=torch.int32, device=dev))
+    ros = o.get("row_of_slot", torch.empty(T * k, dtype=torch.int32, device=dev))
+    sor = o.get("slot_of_row", torch.empty(rc, dtype=torch.int32, device=dev))
+    por = o.get("prob_of_row", torch.empty(rc, dtype=torch.float32, device=dev))
+    ws = workspace(T, k, E, dev) if ws is None else ws
+    _check(LIB.gg_permute(_ptr(x), _ptr(idx), _ptr(prob), T, H, k, E, P, _ptr(Xp), _ptr(offsets),
+                          _ptr(ros), _ptr(sor), _ptr(por), _ptr(ws), ws.numel(), _stream(dev)),
+           "gg_permute")
+    return dict(Xp=Xp, offsets=offsets, row_of_slot=ros, slot_of_row=sor, prob_of_row=por, ws=ws)
+
+
+def permute_rows(src, slot_of_row, offsets, k: int, E: int, R_cap: int, ws, dst=None):
+    """gg_permute_rows: dst[row] = src[slot_of_row[row] // k] (0 on padding)."""
+    T, H = src.shape
+    dst = torch.empty((R_cap, H), dtype=torch.bfloat16, device=src.device) if dst is None else dst
+    _check(LIB.gg_permute_rows(_ptr(src), _ptr(slot_of_row), _ptr(offsets), T, H, k, E, R_cap,
+                               _ptr(dst), _ptr(ws), ws.numel(), _stream(src.device)),
+           "gg_permute_rows")
+    return dst
+
+
+def grouped_fwd(A, B, offsets, epilogue: int = GG_EPI_NONE, ws=None, C=None, H1_save=None):
+    """gg_grouped_fwd. B is [E, N, K]; returns C ([R_cap, N] or [R_cap, N/2])."""
+    R_cap, K = A.shape
+    E, N, Kb = B.shape
+    if Kb != K:
+        raise ValueError("A and B disagree on K")
+    dev = A.device
+    ncols = N // 2 if epilogue == GG_EPI_SWIGLU else N
+    C = torch.empty((R_cap, ncols), dtype=torch.bfloat16, device=dev) if C is None else C
+    ws = workspace(0, 1, E, dev) if ws is None else ws
+    _check(LIB.gg_grouped_fwd(_ptr(A), _ptr(B), _ptr(offsets), E, R_cap, K, N, epilogue, _ptr(C),
+                              _ptr(H1_save), _ptr(ws), ws.numel(), _stream(dev)),
+           "gg_grouped_fwd")
+    return C
+
+
+def swiglu(H1, offsets, E: int, A=None):
+    """gg_swiglu: A = silu(g) * u on a stored FC1 output."""
+    R_cap, F2 = H1.shape
+    F = F2 // 2
+    A = torch.empty((R_cap, F), dtype=torch.bfloat16, device=H1.device) if A is None else A
+    _check(LIB.gg_swiglu(_ptr(H1), _ptr(offsets), E, R_cap, F, _ptr(A), _stream(H1.device)),
+           "gg_swiglu")
+    return A
+
+
+def grouped_dgrad(dC, B, offsets, epilogue: int = GG_EPI_NONE, H1=None, prob_of_row=None,
+                  ws=None, dA=None):
+    """gg_grouped_dgrad. B is the forward weight [E, N, K]; dC is [R_cap, N]."""
+    R_cap, N = dC.shape
+    E, Nb, K = B.shape
+    if Nb != N:
+        raise ValueError("dC and B disagree on N")
+    dev = dC.device
+    ncols = 2 * K if epilogue == GG_EPI_SWIGLU_BWD else K
+    dA = torch.empty((R_cap, ncols), dtype=torch.bfloat16, device=dev) if dA is None else dA
+    ws = workspace(0, 1, E, dev) if ws is None else ws
+    _check(LIB.gg_grouped_dgrad(_ptr(dC), _ptr(B), _ptr(offsets), E, R_cap, K, N, epilogue,
+                                _ptr(H1), _ptr(prob_of_row), _ptr(dA), _ptr(ws), ws.numel(),
+                                _stream(dev)),
+           "gg_grouped_dgrad")
+    return dA
+
+
+def unpermute_combine(Yp, row_of_slot, prob, T: int, k: int, ws, out=None):
+    """gg_unpermute_combine: probability-weighted (prob) or plain (None) sum of k rows."""
+    R_cap, H = Yp.shape
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=Yp.device) if out is None else out
+    _check(LIB.gg_unpermute_combine(_ptr(Yp), _ptr(row_of_slot), _ptr(prob), T, k, H, R_cap,
+                                    _ptr(out), _ptr(ws), ws.numel(), _stream(Yp.device)),
+           "gg_unpermute_combine")
+    return out
+
+
+def selftest_bounded_wait(ws, limit_ns: int) -> None:
+    _check(LIB.gg_selftest_bounded_wait(_ptr(ws), ws.numel(), int(limit_ns), _stream(ws.device)),
+           "gg_selftest_bounded_wait")
+
+
+class MoeLayer:
+    """The whole expert layer (gg_moe_mlp_fwd / gg_moe_mlp_bwd) over one owned buffer.
+
+    The buffer holds every intermediate (permuted rows, H1, A, Yp and their
+    gradients, row maps, workspace); ``view(name)`` exposes each as a tensor.
+    """
+
+    _SHAPES = {
+        "Xp": ("rc", "H"), "Yp": ("rc", "H"), "dYp": ("rc", "H"), "dXp": ("rc", "H"),
+        "H1": ("rc", "2F"), "dH": ("rc", "2F"), "A": ("rc", "F"), "offsets": ("E1",),
+        "row_of_slot": ("Tk",), "slot_of_row": ("rc",), "prob_of_row": ("rc",), "ws": ("ws",),
+    }
+
+    def __init__(self, T: int, H: int, F: int, k: int, E: int, P: int = 1, device="cuda"):
+        self.T, self.H, self.F, self.k, self.E, self.P = T, H, F, k, E, P
+        self.R_cap = r_cap(T, k, E, P)
+        self.device = torch.device(device)
+        n = int(LIB.gg_moe_buffers_size(T, H, F, k, E, P))
+        if n == 0:
+            raise GGError(1, "gg_moe_buffers_size")
+        self.storage = torch.zeros(n + 256, dtype=torch.uint8, device=self.device)
+        base = self.storage.data_ptr()
+        self._base = base + ((-base) % 256)
+        self.buf = GGBuffers()
+        _check(LIB.gg_moe_buffers_bind(ctypes.c_void_p(self._base), n, T, H, F, k, E, P,
+                                       ctypes.byref(self.buf)), "gg_moe_buffers_bind")
+
+    def view(self, name: str) -> torch.Tensor:
+        """A torch view of one intermediate buffer of the struct."""
+        dims = {"rc": self.R_cap, "H": self.H, "F": self.F, "2F": 2 * self.F, "E1": self.E + 1,
+                "Tk": self.T * self.k, "ws": int(self.buf.ws_bytes)}
+        dtype = {"offsets": torch.int32, "row_of_slot": torch.int32, "slot_of_row": torch.int32,
+                 "prob_of_row": torch.float32, "ws": torch.uint8}.get(name, torch.bfloat16)
+        shape = tuple(dims[d] for d in self._SHAPES[name])
+        count = 1
+        for s in shape:
+            count *= s
+        esize = torch.empty((), dtype=dtype).element_size()
+        off = getattr(self.buf, name) - self.storage.data_ptr()
+        return self.storage[off:off + count * esize].view(dtype).view(shape)
+
+    def forward(self, x, idx, prob, W1, W2, out=None):
+        T, H, F, k, E = self.T, self.H, self.F, self.k, self.E
+        _need(x, torch.bfloat16, (T, H), "x")
+        _need(idx, torch.int32, (T, k), "idx")
+        _need(prob, torch.float32, (T, k), "prob")
+        _need(W1, torch.bfloat16, (E, 2 * F, H), "W1")
+        _need(W2, torch.bfloat16, (E, H, F), "W2")
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=self.device) if out is None else out
+        _check(LIB.gg_moe_mlp_fwd(_ptr(x), _ptr(idx), _ptr(prob), _ptr(W1), _ptr(W2), T, H, F, k,
+                                  E, self.P, _ptr(out), ctypes.byref(self.buf),
+                                  _stream(self.device)), "gg_moe_mlp_fwd")
+        return out
+
+    def backward(self, dOut, W1, W2, dX=None):
+        T, H, F, k, E = self.T, self.H, self.F, self.k, self.E
+        _need(dOut, torch.bfloat16, (T, H), "dOut")
+        dX = torch.empty((T, H), dtype=torch.bfloat16, device=self.device) if dX is None else dX
+        _check(LIB.gg_moe_mlp_bwd(_ptr(dOut), _ptr(W1), _ptr(W2), T, H, F, k, E, self.P,
+                                  _ptr(dX), ctypes.byref(self.buf), _stream(self.device)),
+               "gg_moe_mlp_bwd")
+        return dX
+
+    def status(self) -> int:
+        return read_status(self.view("ws"))

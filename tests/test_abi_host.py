@@ -1,0 +1,128 @@
+"""CPU-only checks of the C ABI: the library builds, loads, exports every symbol
+declared in include/gg.h, and its host-side logic (sizes, buffer carving and
+argument validation that rejects before touching the device) behaves as the
+header documents. No kernel is launched here."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def gg():
+    from moe_expert_grouped_gb300 import build
+
+    build.build()
+    import moe_expert_grouped_gb300.gg as mod
+
+    return mod
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "gg.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gg_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary_calls():
+    names = _declared_functions()
+    for required in ("gg_permute", "gg_grouped_fwd", "gg_swiglu", "gg_grouped_dgrad",
+                     "gg_unpermute_combine", "gg_moe_mlp_fwd", "gg_moe_mlp_bwd",
+                     "gg_workspace_size", "gg_read_status", "gg_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(gg):
+    lib = ctypes.CDLL(gg.LIB_PATH)
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    bound = {n for n, _, _ in gg.SIGNATURES}
+    assert set(_declared_functions()) == bound
+
+
+def test_status_strings_and_version(gg):
+    assert gg.version().startswith("gg ")
+    for code, name in gg.STATUS_NAMES.items():
+        assert gg.status_string(code).startswith(name)
+    assert "unknown" in gg.status_string(12345)
+
+
+def test_workspace_size_grows_with_pairs(gg):
+    L = gg.LIB
+    assert L.gg_workspace_size(0, 8, 128) >= 256
+    assert L.gg_workspace_size(-1, 8, 128) == 0
+    small = L.gg_workspace_size(16384, 8, 128)
+    big = L.gg_workspace_size(131072, 8, 128)
+    assert big > small > 256
+    # one int32 histogram row of E experts per block of 2048 pairs
+    assert small >= 256 + 4 * 128 * (16384 * 8 // 2048)
+
+
+def test_buffers_bind_carves_disjoint_aligned_pieces(gg):
+    T, H, F, k, E, P = 300, 320, 384, 2, 8, 16
+    n = gg.LIB.gg_moe_buffers_size(T, H, F, k, E, P)
+    base = 1 << 40  # never dereferenced: binding is pointer arithmetic only
+    buf = gg.GGBuffers()
+    assert gg.LIB.gg_moe_buffers_bind(ctypes.c_void_p(base), n, T, H, F, k, E, P,
+                                      ctypes.byref(buf)) == 0
+    rc = T * k + E * (P - 1)
+    sizes = {"Xp": rc * H * 2, "Yp": rc * H * 2, "dYp": rc * H * 2, "dXp": rc * H * 2,
+             "H1": rc * 2 * F * 2, "dH": rc * 2 * F * 2, "A": rc * F * 2, "offsets": 4 * (E + 1),
+             "row_of_slot": 4 * T * k, "slot_of_row": 4 * rc, "prob_of_row": 4 * rc,
+             "ws": buf.ws_bytes}
+    spans = sorted((getattr(buf, name), getattr(buf, name) + sz) for name, sz in sizes.items())
+    for (a0, a1), (b0, _) in zip(spans, spans[1:]):
+        assert a1 <= b0
+    assert all(s % 256 == 0 for s, _ in spans)
+    assert spans[0][0] >= base and spans[-1][1] <= base + n
+    assert buf.ws_bytes >= gg.LIB.gg_workspace_size(T, k, E)
+    # too small / misaligned / null
+    assert gg.LIB.gg_moe_buffers_bind(ctypes.c_void_p(base), n - 1, T, H, F, k, E, P,
+                                      ctypes.byref(buf)) == 4
+    assert gg.LIB.gg_moe_buffers_bind(ctypes.c_void_p(base + 16), n, T, H, F, k, E, P,
+                                      ctypes.byref(buf)) == 3
+    assert gg.LIB.gg_moe_buffers_bind(None, n, T, H, F, k, E, P, ctypes.byref(buf)) == 1
+
+
+def test_validation_rejects_before_launch(gg):
+    L = gg.LIB
+    p = ctypes.c_void_p(1 << 40)
+    mis = ctypes.c_void_p((1 << 40) + 8)
+    ws = ctypes.c_void_p(1 << 41)
+    # gg_permute: bad sizes, k > E, k > 32, H not a multiple of 64, misaligned x
+    assert L.gg_permute(p, p, p, 4, 64, 2, 4, 0, p, p, p, p, p, ws, 1 << 20, None) == 1
+    assert L.gg_permute(p, p, p, 4, 64, 5, 4, 1, p, p, p, p, p, ws, 1 << 20, None) == 1
+    assert L.gg_permute(p, p, p, 4, 64, 33, 64, 1, p, p, p, p, p, ws, 1 << 20, None) == 1
+    assert L.gg_permute(p, p, p, 4, 96, 2, 4, 1, p, p, p, p, p, ws, 1 << 20, None) == 2
+    assert L.gg_permute(p, p, p, 4, 64, 2, 2048, 1, p, p, p, p, p, ws, 1 << 30, None) == 2
+    assert L.gg_permute(mis, p, p, 4, 64, 2, 4, 1, p, p, p, p, p, ws, 1 << 20, None) == 3
+    assert L.gg_permute(p, p, p, 4, 64, 2, 4, 1, p, p, p, p, p, ws, 16, None) == 4
+    assert L.gg_permute(p, None, p, 4, 64, 2, 4, 1, p, p, p, p, p, ws, 1 << 20, None) == 1
+    # gg_grouped_fwd: K/N not multiples of 64, wrong epilogue, H1_save with NONE
+    assert L.gg_grouped_fwd(p, p, p, 4, 128, 96, 128, 0, p, None, ws, 1024, None) == 2
+    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 100, 0, p, None, ws, 1024, None) == 2
+    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 128, 2, p, None, ws, 1024, None) == 1
+    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 128, 0, p, p, ws, 1024, None) == 1
+    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 192, 1, p, p, ws, 1024, None) == 2
+    assert L.gg_grouped_fwd(mis, p, p, 4, 128, 64, 128, 0, p, None, ws, 1024, None) == 3
+    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 128, 0, p, None, ws, 16, None) == 4
+    # gg_grouped_dgrad: SwiGLU backward needs H1; NONE must not get H1
+    assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 2, None, None, p, ws, 1024, None) == 1
+    assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 0, p, None, p, ws, 1024, None) == 1
+    assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 1, p, None, p, ws, 1024, None) == 1
+    # gg_unpermute_combine: k > 32, H % 64
+    assert L.gg_unpermute_combine(p, p, p, 4, 33, 64, 128, p, ws, 1024, None) == 1
+    assert L.gg_unpermute_combine(p, p, p, 4, 2, 72, 128, p, ws, 1024, None) == 2
+    # gg_swiglu: F % 64
+    assert L.gg_swiglu(p, p, 4, 128, 96, p, None) == 2
+    # composites need a full buffer set
+    buf = gg.GGBuffers()
+    assert L.gg_moe_mlp_fwd(p, p, p, p, p, 4, 64, 128, 2, 4, 1, p, ctypes.byref(buf), None) == 1
+    assert L.gg_moe_mlp_bwd(p, p, p, 4, 64, 128, 2, 4, 1, p, ctypes.byref(buf), None) == 1
+    assert L.gg_moe_mlp_fwd(p, p, p, p, p, 4, 64, 128, 2, 4, 1, p, None, None) == 1
+    assert L.gg_read_status(None, None, None) == 1
+    assert L.gg_clear_status(None, None) == 1
