@@ -135,25 +135,23 @@ def permute(x, idx, prob, E: int, P: int = 1):
 
 def grouped_linear(Xp: np.ndarray, W, offsets) -> np.ndarray:
     """Y[rows of e] = Xp[rows of e] @ W[e]^T for every expert (nn.Linear)."""
-    Wf = _as_f64(W)
-    E, N, K = Wf.shape
+    E, N, K = np.shape(W)
     Y = np.zeros((Xp.shape[0], N), dtype=np.float64)
     for e in range(E):
         r0, r1 = int(offsets[e]), int(offsets[e + 1])
         if r1 > r0:
-            Y[r0:r1] = Xp[r0:r1] @ Wf[e].T
+            Y[r0:r1] = Xp[r0:r1] @ _as_f64(W[e]).T
     return Y
 
 
 def grouped_linear_t(dY: np.ndarray, W, offsets) -> np.ndarray:
     """Input gradient of ``grouped_linear``: dX[rows of e] = dY[rows of e] @ W[e]."""
-    Wf = _as_f64(W)
-    E, N, K = Wf.shape
+    E, N, K = np.shape(W)
     dX = np.zeros((dY.shape[0], K), dtype=np.float64)
     for e in range(E):
         r0, r1 = int(offsets[e]), int(offsets[e + 1])
         if r1 > r0:
-            dX[r0:r1] = dY[r0:r1] @ Wf[e]
+            dX[r0:r1] = dY[r0:r1] @ _as_f64(W[e])
     return dX
 
 

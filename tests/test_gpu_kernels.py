@@ -1,0 +1,271 @@
+"""GPU parity of each kernel against the fp64 oracle, through the C ABI.
+
+Sizes are small enough for the oracle to finish in seconds but span several
+128-row tiles, several 256-column tiles, ragged tails in both, an empty expert
+and a one-row expert. Index work is compared bit for bit; floating point uses
+the parity bar of ``_helpers`` (rel-L2 <= 5e-3, |err| <= 1e-2|ref| + 1e-3)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _helpers import assert_parity, bits_to_torch, torch_to_bits, torch_to_f64
+from moe_synth import normal_bf16
+
+pytestmark = pytest.mark.gpu
+
+NAN_BF16 = 0x7FC0
+
+
+@pytest.fixture(scope="module")
+def gg():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from moe_expert_grouped_gb300 import build
+
+    build.build()
+    import moe_expert_grouped_gb300.gg as mod
+
+    return mod
+
+
+def _offsets(counts, P=1):
+    padded = [-(-c // P) * P for c in counts]
+    return np.concatenate([[0], np.cumsum(padded)]).astype(np.int32)
+
+
+def _nan_filled(shape):
+    t = torch.full(shape, 0, dtype=torch.int16, device="cuda")
+    t.fill_(NAN_BF16)
+    return t.view(torch.bfloat16)
+
+
+COUNTS = [130, 0, 1, 257, 60]  # ragged, an empty expert, a one-row expert, > 2 row tiles
+
+
+@pytest.mark.parametrize("K,N", [(320, 320), (64, 256), (192, 576)])
+def test_grouped_fwd_plain(gg, K, N):
+    rng = np.random.default_rng(K + N)
+    E = len(COUNTS)
+    off = _offsets(COUNTS)
+    R_cap = int(off[-1]) + 40  # 40 unused rows past offsets[E]
+    A = normal_bf16(rng, (R_cap, K), 1.0)
+    B = normal_bf16(rng, (E, N, K), 0.05)
+    C = _nan_filled((R_cap, N))
+    ws = gg.workspace(0, 1, E, "cuda")
+    gg.grouped_fwd(bits_to_torch(A), bits_to_torch(B), torch.from_numpy(off).cuda(),
+                   gg.GG_EPI_NONE, ws=ws, C=C)
+    torch.cuda.synchronize()
+    assert gg.read_status(ws) == 0
+    ref = oracle.grouped_linear(oracle.bf16_bits_to_f64(A), B, off)
+    n = int(off[-1])
+    assert_parity(torch_to_f64(C[:n]), ref[:n], "C")
+    # rows past offsets[E] are never written
+    assert np.all(torch_to_bits(C[n:]) == NAN_BF16)
+
+
+@pytest.mark.parametrize("F", [384, 320])
+def test_grouped_fwd_swiglu_and_unfused_swiglu(gg, F):
+    rng = np.random.default_rng(F)
+    E, K = len(COUNTS), 192
+    off = _offsets(COUNTS)
+    R_cap = int(off[-1]) + 8
+    X = normal_bf16(rng, (R_cap, K), 1.0)
+    W1 = normal_bf16(rng, (E, 2 * F, K), 0.08)
+    ws = gg.workspace(0, 1, E, "cuda")
+    d_off = torch.from_numpy(off).cuda()
+    H1 = _nan_filled((R_cap, 2 * F))
+    A = _nan_filled((R_cap, F))
+    gg.grouped_fwd(bits_to_torch(X), bits_to_torch(W1), d_off, gg.GG_EPI_SWIGLU, ws=ws, C=A,
+                   H1_save=H1)
+    A2 = _nan_filled((R_cap, F))
+    gg.swiglu(H1, d_off, E, A=A2)
+    torch.cuda.synchronize()
+    assert gg.read_status(ws) == 0
+    n = int(off[-1])
+    h_ref = oracle.grouped_linear(oracle.bf16_bits_to_f64(X), W1, off)
+    assert_parity(torch_to_f64(H1[:n]), h_ref[:n], "H1")
+    assert_parity(torch_to_f64(A[:n]), oracle.swiglu(h_ref)[:n], "A")
+    # fused epilogue and the standalone kernel round alike: bitwise equal
+    np.testing.assert_array_equal(torch_to_bits(A[:n]), torch_to_bits(A2[:n]))
+    assert np.all(torch_to_bits(A[n:]) == NAN_BF16) and np.all(torch_to_bits(H1[n:]) == NAN_BF16)
+
+
+@pytest.mark.parametrize("K,N", [(192, 320), (320, 64)])
+def test_grouped_dgrad_plain_with_row_scale(gg, K, N):
+    rng = np.random.default_rng(7 * K + N)
+    E = len(COUNTS)
+    off = _offsets(COUNTS)
+    R_cap = int(off[-1]) + 16
+    dC = normal_bf16(rng, (R_cap, N), 1.0)
+    B = normal_bf16(rng, (E, N, K), 0.05)
+    scale = rng.uniform(0.0, 1.0, R_cap).astype(np.float32)
+    ws = gg.workspace(0, 1, E, "cuda")
+    dA = _nan_filled((R_cap, K))
+    gg.grouped_dgrad(bits_to_torch(dC), bits_to_torch(B), torch.from_numpy(off).cuda(),
+                     gg.GG_EPI_NONE, prob_of_row=torch.from_numpy(scale).cuda(), ws=ws, dA=dA)
+    torch.cuda.synchronize()
+    assert gg.read_status(ws) == 0
+    n = int(off[-1])
+    ref = scale.astype(np.float64)[:, None] * oracle.grouped_linear_t(oracle.bf16_bits_to_f64(dC),
+                                                                      B, off)
+    assert_parity(torch_to_f64(dA[:n]), ref[:n], "dA")
+    assert np.all(torch_to_bits(dA[n:]) == NAN_BF16)
+
+
+@pytest.mark.parametrize("F,H", [(320, 256), (256, 128)])
+def test_grouped_dgrad_swiglu_backward(gg, F, H):
+    rng = np.random.default_rng(F * 3 + H)
+    E = len(COUNTS)
+    off = _offsets(COUNTS)
+    R_cap = int(off[-1]) + 16
+    dY = normal_bf16(rng, (R_cap, H), 1.0)
+    W2 = normal_bf16(rng, (E, H, F), 0.05)
+    H1 = normal_bf16(rng, (R_cap, 2 * F), 1.5)
+    prob = rng.uniform(0.05, 1.0, R_cap).astype(np.float32)
+    ws = gg.workspace(0, 1, E, "cuda")
+    dH = _nan_filled((R_cap, 2 * F))
+    gg.grouped_dgrad(bits_to_torch(dY), bits_to_torch(W2), torch.from_numpy(off).cuda(),
+                     gg.GG_EPI_SWIGLU_BWD, H1=bits_to_torch(H1),
+                     prob_of_row=torch.from_numpy(prob).cuda(), ws=ws, dA=dH)
+    torch.cuda.synchronize()
+    assert gg.read_status(ws) == 0
+    n = int(off[-1])
+    dA = prob.astype(np.float64)[:, None] * oracle.grouped_linear_t(oracle.bf16_bits_to_f64(dY),
+                                                                    W2, off)
+    ref = oracle.swiglu_backward(dA, oracle.bf16_bits_to_f64(H1))
+    assert_parity(torch_to_f64(dH[:n]), ref[:n], "dH")
+    assert np.all(torch_to_bits(dH[n:]) == NAN_BF16)
+
+
+def _permute_case(T, E, k, seed, skew=None, dup=False):
+    rng = np.random.default_rng(seed)
+    if dup:
+        idx = rng.integers(0, E, size=(T, k))
+    elif skew is not None:
+        idx = np.full((T, k), skew)
+        if k > 1:
+            idx[:, 1:] = (skew + 1 + np.arange(k - 1)) % E
+    else:
+        idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]) if T else \
+            np.zeros((0, k), np.int64)
+    prob = rng.uniform(0, 1, (T, k)).astype(np.float32)
+    return idx.astype(np.int32).reshape(T, k), prob
+
+
+@pytest.mark.parametrize("T,H,E,k,P,extra", [
+    (256, 64, 4, 2, 1, {}), (300, 256, 8, 2, 1, {}), (300, 256, 8, 2, 16, {}),
+    (1, 64, 1, 1, 1, {}), (5000, 128, 16, 1, 1, {"skew": 7}), (3000, 64, 1024, 8, 1, {}),
+    (700, 192, 6, 3, 256, {"dup": True}), (4096, 64, 128, 8, 256, {}),
+])
+def test_permute_bit_exact(gg, T, H, E, k, P, extra):
+    idx, prob = _permute_case(T, E, k, T + E, **extra)
+    x = normal_bf16(np.random.default_rng(1), (T, H), 1.0)
+    out = gg.permute(bits_to_torch(x), torch.from_numpy(idx).cuda(), torch.from_numpy(prob).cuda(),
+                     E, P)
+    torch.cuda.synchronize()
+    assert gg.read_status(out["ws"]) == 0
+    off, ros, sor = oracle.route(idx, E, P)
+    np.testing.assert_array_equal(out["offsets"].cpu().numpy(), off)
+    np.testing.assert_array_equal(out["row_of_slot"].cpu().numpy(), ros)
+    np.testing.assert_array_equal(out["slot_of_row"].cpu().numpy(), sor)
+    por = out["prob_of_row"].cpu().numpy()
+    live = sor >= 0
+    np.testing.assert_array_equal(por[live], prob.reshape(-1)[sor[live]])
+    assert np.all(por[~live] == 0)
+    n = int(off[-1])
+    xp = torch_to_bits(out["Xp"][:n])
+    live_n = sor[:n] >= 0
+    np.testing.assert_array_equal(xp[live_n], x[sor[:n][live_n] // k])
+    assert np.all(xp[~live_n] == 0)
+
+
+def test_permute_empty_batch_writes_zero_offsets(gg):
+    E = 8
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((0, 2), dtype=torch.int32, device="cuda")
+    prob = torch.empty((0, 2), dtype=torch.float32, device="cuda")
+    out = gg.permute(x, idx, prob, E, 4, out={"offsets": torch.full((E + 1,), 7, dtype=torch.int32,
+                                                                     device="cuda")})
+    torch.cuda.synchronize()
+    assert np.all(out["offsets"].cpu().numpy() == 0)
+
+
+@pytest.mark.parametrize("weighted", [True, False])
+def test_combine(gg, weighted):
+    T, H, E, k = 333, 192, 8, 3
+    idx, prob = _permute_case(T, E, k, 5)
+    x = normal_bf16(np.random.default_rng(2), (T, H), 1.0)
+    p = gg.permute(bits_to_torch(x), torch.from_numpy(idx).cuda(), torch.from_numpy(prob).cuda(), E, 4)
+    R_cap = p["Xp"].shape[0]
+    Yp = normal_bf16(np.random.default_rng(3), (R_cap, H), 1.0)
+    out = gg.unpermute_combine(bits_to_torch(Yp), p["row_of_slot"],
+                               torch.from_numpy(prob).cuda() if weighted else None, T, k, p["ws"])
+    torch.cuda.synchronize()
+    assert gg.read_status(p["ws"]) == 0
+    ros = p["row_of_slot"].cpu().numpy()
+    ref = oracle.combine(oracle.bf16_bits_to_f64(Yp), ros, prob if weighted else None, T, k)
+    assert_parity(torch_to_f64(out), ref, "out")
+
+
+def test_permute_rows_gathers_token_gradient(gg):
+    T, H, E, k, P = 400, 128, 8, 2, 8
+    idx, prob = _permute_case(T, E, k, 9)
+    x = normal_bf16(np.random.default_rng(4), (T, H), 1.0)
+    dO = normal_bf16(np.random.default_rng(5), (T, H), 1.0)
+    p = gg.permute(bits_to_torch(x), torch.from_numpy(idx).cuda(), torch.from_numpy(prob).cuda(), E, P)
+    R_cap = p["Xp"].shape[0]
+    dYp = gg.permute_rows(bits_to_torch(dO), p["slot_of_row"], p["offsets"], k, E, R_cap, p["ws"])
+    torch.cuda.synchronize()
+    sor = p["slot_of_row"].cpu().numpy()
+    n = int(p["offsets"][-1].item())
+    got = torch_to_bits(dYp[:n])
+    live = sor[:n] >= 0
+    np.testing.assert_array_equal(got[live], dO[sor[:n][live] // k])
+    assert np.all(got[~live] == 0)
+
+
+def test_device_status_bad_expert_id(gg):
+    T, H, E, k = 64, 64, 4, 2
+    idx = np.tile(np.array([[0, 1]], np.int32), (T, 1))
+    idx[5, 1] = 9   # out of range
+    idx[6, 0] = -2  # out of range
+    prob = np.ones((T, k), np.float32)
+    x = normal_bf16(np.random.default_rng(0), (T, H), 1.0)
+    p = gg.permute(bits_to_torch(x), torch.from_numpy(idx).cuda(), torch.from_numpy(prob).cuda(), E, 1)
+    torch.cuda.synchronize()
+    assert gg.read_status(p["ws"]) == 16
+    ros = p["row_of_slot"].cpu().numpy()
+    assert ros[5 * k + 1] == -1 and ros[6 * k] == -1
+    assert int(p["offsets"][-1].item()) == T * k - 2
+    gg.clear_status(p["ws"])
+    assert gg.read_status(p["ws"]) == 0
+
+
+def test_device_status_bad_offsets_computes_nothing(gg):
+    E, K, N, R_cap = 3, 64, 64, 256
+    A = torch.zeros((R_cap, K), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((E, N, K), dtype=torch.bfloat16, device="cuda")
+    C = _nan_filled((R_cap, N))
+    ws = gg.workspace(0, 1, E, "cuda")
+    bad = torch.tensor([0, 100, 50, 200], dtype=torch.int32, device="cuda")  # not monotone
+    gg.grouped_fwd(A, B, bad, gg.GG_EPI_NONE, ws=ws, C=C)
+    torch.cuda.synchronize()
+    assert gg.read_status(ws) == 17
+    assert np.all(torch_to_bits(C) == NAN_BF16)
+    gg.clear_status(ws)
+    too_far = torch.tensor([0, 100, 200, 300], dtype=torch.int32, device="cuda")  # > R_cap
+    gg.grouped_fwd(A, B, too_far, gg.GG_EPI_NONE, ws=ws, C=C)
+    torch.cuda.synchronize()
+    assert gg.read_status(ws) == 17
+
+
+def test_bounded_wait_times_out_and_context_survives(gg):
+    ws = gg.workspace(0, 1, 1, "cuda")
+    gg.selftest_bounded_wait(ws, 2_000_000)  # 2 ms on a barrier nothing completes
+    torch.cuda.synchronize()
+    assert gg.read_status(ws) == 19
+    # the context is still usable afterwards
+    gg.clear_status(ws)
+    test_grouped_fwd_plain(gg, 64, 256)

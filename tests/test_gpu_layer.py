@@ -1,0 +1,154 @@
+"""GPU parity of the whole expert layer (gg_moe_mlp_fwd / gg_moe_mlp_bwd).
+
+Covers the tiny workload, a mid-size ragged case (several row and column
+tiles, ragged tails, padding), the empty batch, run-to-run bitwise equality,
+CUDA-graph replay, expert relabelling and replacing one expert's weights."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _helpers import assert_parity, bits_to_torch, torch_to_bits, torch_to_f64
+from moe_synth import CONFIGS, MoeShape, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+MID = MoeShape("mid_e8_h320_f384_t300_k2", E=8, H=320, F=384, T=300, k=2, routing="uniform",
+               x_std=1.0, w_std=0.05)
+MID_PAD = MoeShape("mid_e6_h256_f320_t257_k3_pad16", E=6, H=256, F=320, T=257, k=3, P=16,
+                   routing="uniform", x_std=1.0, w_std=0.05)
+
+
+@pytest.fixture(scope="module")
+def gg():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from moe_expert_grouped_gb300 import build
+
+    build.build()
+    import moe_expert_grouped_gb300.gg as mod
+
+    return mod
+
+
+def _dev(inp):
+    return dict(x=bits_to_torch(inp.x), idx=torch.from_numpy(inp.idx).cuda(),
+                prob=torch.from_numpy(inp.prob).cuda(), W1=bits_to_torch(inp.W1),
+                W2=bits_to_torch(inp.W2), dOut=bits_to_torch(inp.dOut))
+
+
+def _run(gg, shape, d):
+    layer = gg.MoeLayer(shape.T, shape.H, shape.F, shape.k, shape.E, shape.P)
+    out = layer.forward(d["x"], d["idx"], d["prob"], d["W1"], d["W2"])
+    dX = layer.backward(d["dOut"], d["W1"], d["W2"])
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    return layer, out, dX
+
+
+@pytest.mark.parametrize("shape,seed", [(CONFIGS[1], 1000), (MID, 77), (MID_PAD, 78)])
+def test_layer_matches_oracle(gg, shape, seed):
+    inp = make_inputs(shape, seed)
+    d = _dev(inp)
+    layer, out, dX = _run(gg, shape, d)
+    fwd = oracle.moe_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, shape.E, shape.P)
+    bwd = oracle.moe_backward(inp.dOut, fwd, inp.W1, inp.W2)
+    assert_parity(torch_to_f64(out), fwd["out"], "out")
+    assert_parity(torch_to_f64(dX), bwd["dX"], "dX")
+    n = int(fwd["offsets"][-1])
+    np.testing.assert_array_equal(layer.view("offsets").cpu().numpy(), fwd["offsets"])
+    np.testing.assert_array_equal(layer.view("row_of_slot").cpu().numpy(), fwd["row_of_slot"])
+    for name in ("H1", "A", "Yp"):
+        assert_parity(torch_to_f64(layer.view(name)[:n]), fwd[name][:n], name)
+    for name in ("dH", "dXp"):
+        assert_parity(torch_to_f64(layer.view(name)[:n]), bwd[name][:n], name)
+
+
+def test_layer_run_to_run_bitwise(gg):
+    inp = make_inputs(MID, 5)
+    d = _dev(inp)
+    _, o1, g1 = _run(gg, MID, d)
+    _, o2, g2 = _run(gg, MID, d)
+    np.testing.assert_array_equal(torch_to_bits(o1), torch_to_bits(o2))
+    np.testing.assert_array_equal(torch_to_bits(g1), torch_to_bits(g2))
+
+
+def test_layer_empty_batch(gg):
+    shape = CONFIGS[1].with_tokens(0)
+    inp = make_inputs(shape, 1000)
+    d = _dev(inp)
+    layer, out, dX = _run(gg, shape, d)
+    assert out.shape == (0, shape.H) and dX.shape == (0, shape.H)
+    assert np.all(layer.view("offsets").cpu().numpy() == 0)
+
+
+def test_cuda_graph_replay_matches_eager(gg):
+    shape = MID
+    inp = make_inputs(shape, 11)
+    d = _dev(inp)
+    _, out_e, dX_e = _run(gg, shape, d)
+    layer = gg.MoeLayer(shape.T, shape.H, shape.F, shape.k, shape.E, shape.P)
+    out = torch.empty_like(out_e)
+    dX = torch.empty_like(dX_e)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up outside capture (first-use set-up)
+        layer.forward(d["x"], d["idx"], d["prob"], d["W1"], d["W2"], out=out)
+        layer.backward(d["dOut"], d["W1"], d["W2"], dX=dX)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    out.zero_()
+    dX.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer.forward(d["x"], d["idx"], d["prob"], d["W1"], d["W2"], out=out)
+        layer.backward(d["dOut"], d["W1"], d["W2"], dX=dX)
+    g.replay()
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(torch_to_bits(out), torch_to_bits(out_e))
+    np.testing.assert_array_equal(torch_to_bits(dX), torch_to_bits(dX_e))
+    # new routing written into the same input buffers is picked up by the replay
+    inp2 = make_inputs(shape, 12)
+    d["idx"].copy_(torch.from_numpy(inp2.idx))
+    g.replay()
+    torch.cuda.synchronize()
+    d2 = dict(d)
+    _, out_e2, dX_e2 = _run(gg, shape, d2)
+    np.testing.assert_array_equal(torch_to_bits(out), torch_to_bits(out_e2))
+    np.testing.assert_array_equal(torch_to_bits(dX), torch_to_bits(dX_e2))
+
+
+def test_expert_relabel_is_bitwise_invariant(gg):
+    shape = MID
+    inp = make_inputs(shape, 21)
+    d = _dev(inp)
+    _, o1, g1 = _run(gg, shape, d)
+    pi = np.random.default_rng(3).permutation(shape.E)
+    d2 = dict(d)
+    d2["idx"] = torch.from_numpy(pi[inp.idx].astype(np.int32)).cuda()
+    W1p = torch.empty_like(d["W1"])
+    W2p = torch.empty_like(d["W2"])
+    W1p[torch.from_numpy(pi).cuda()] = d["W1"]
+    W2p[torch.from_numpy(pi).cuda()] = d["W2"]
+    d2["W1"], d2["W2"] = W1p, W2p
+    _, o2, g2 = _run(gg, shape, d2)
+    np.testing.assert_array_equal(torch_to_bits(o1), torch_to_bits(o2))
+    np.testing.assert_array_equal(torch_to_bits(g1), torch_to_bits(g2))
+
+
+def test_replacing_one_expert_changes_only_its_tokens(gg):
+    shape = MID
+    inp = make_inputs(shape, 31)
+    d = _dev(inp)
+    _, o1, g1 = _run(gg, shape, d)
+    e = 3
+    d["W1"][e].normal_(0, 0.05)
+    d["W2"][e].normal_(0, 0.05)
+    _, o2, g2 = _run(gg, shape, d)
+    touched = np.any(inp.idx == e, axis=1)
+    assert touched.any() and (~touched).any()
+    b1, b2 = torch_to_bits(o1), torch_to_bits(o2)
+    np.testing.assert_array_equal(b1[~touched], b2[~touched])
+    assert np.all(np.any(b1[touched] != b2[touched], axis=1))
+    np.testing.assert_array_equal(torch_to_bits(g1)[~touched], torch_to_bits(g2)[~touched])
