@@ -1,0 +1,441 @@
+"""Benchmark of the grouped expert MLP (forward + input gradient) on GB300.
+
+One step = one pass of the whole expert path over one batch: permute, grouped
+FC1 with fused SwiGLU, grouped FC2, weighted combine, then the output-gradient
+permute, dgrad FC2 with fused SwiGLU backward, dgrad FC1 and the dX combine.
+Default workload: the balanced 128-expert layer (E=128, H=2048, F=768,
+T=16384 tokens, top-8, uniform routing), synthetic seeded data.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gg|reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs an independent
+replica of the step on its own GPU (the path has no exchange step here), and
+rank 0 prints the whole-job line: units of all ranks / max-over-ranks time.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from moe_synth import CONFIGS, make_inputs  # noqa: E402
+
+METRIC = "expert-MLP fwd+dgrad TFLOP/s & tokens/s on 1 GB300; % BF16 tensor peak"
+DEFAULT_CFG = 2
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ multi-rank plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_seconds: float, local_units: float, backend_device=None):
+    """(max seconds over ranks, sum of units over ranks); identity without a process group."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return local_seconds, local_units
+    dev = backend_device if backend_device is not None else torch.device("cpu")
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.window = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(device_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        inside = [s for t, s in self.samples if self.window and self.window[0] <= t <= self.window[1]]
+        used = inside if inside else [s for _, s in self.samples]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(s[0]) for s in used if num(s[0]) is not None]
+        mx = [num(s[1]) for s in used if num(s[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in used for i in range(4) if "Active" in s[4 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples_in_window": len(inside), "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------ oracle timing
+
+def time_oracle(shape, inp, n_tokens: int, steps: int = 1):
+    """Wall time of the fp64 oracle forward + input gradient on a token sample."""
+    import oracle
+
+    sel = np.arange(min(n_tokens, shape.T))
+    W1 = oracle.bf16_bits_to_f64(inp.W1)  # the oracle's documented fp64 weight form
+    W2 = oracle.bf16_bits_to_f64(inp.W2)
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        fwd = oracle.moe_forward(inp.x[sel], inp.idx[sel], inp.prob[sel], W1, W2, shape.E, shape.P)
+        oracle.moe_backward(inp.dOut[sel], fwd, W1, W2)
+        times.append(time.perf_counter() - t0)
+    return times, sel.size
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:  # noqa: BLE001
+        pass
+    return os.cpu_count()
+
+
+# ------------------------------------------------------------------ the gg arm
+
+def run_gg(args, shape, peaks):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    import moe_expert_grouped_gb300.gg as gg
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+    inp = make_inputs(shape, 1000 * args.config + 17 * rank)
+
+    def to_dev(u16):
+        return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    x, dOut = to_dev(inp.x), to_dev(inp.dOut)
+    W1, W2 = to_dev(inp.W1), to_dev(inp.W2)
+    idx = torch.from_numpy(inp.idx).to(dev)
+    prob = torch.from_numpy(inp.prob).to(dev)
+    T, H, F, k, E, P = shape.T, shape.H, shape.F, shape.k, shape.E, shape.P
+    layer = gg.MoeLayer(T, H, F, k, E, P, device=dev)
+    b = {n: layer.view(n) for n in ("Xp", "H1", "A", "Yp", "dYp", "dH", "dXp", "offsets",
+                                    "row_of_slot", "slot_of_row", "prob_of_row", "ws")}
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    dX = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    ws = b["ws"]
+    rc = layer.R_cap
+    stream = torch.cuda.current_stream(dev)
+    ops = ["permute", "fc1_swiglu", "fc2", "combine", "permute_dout", "dgrad_fc2_swiglu_bwd",
+           "dgrad_fc1", "combine_dx"]
+
+    def step(events=None):
+        def mark(i):
+            if events is not None:
+                events[i].record(stream)
+
+        mark(0)
+        gg.permute(x, idx, prob, E, P, ws=ws, out=b)
+        mark(1)
+        gg.grouped_fwd(b["Xp"], W1, b["offsets"], gg.GG_EPI_SWIGLU, ws=ws, C=b["A"], H1_save=b["H1"])
+        mark(2)
+        gg.grouped_fwd(b["A"], W2, b["offsets"], gg.GG_EPI_NONE, ws=ws, C=b["Yp"])
+        mark(3)
+        gg.unpermute_combine(b["Yp"], b["row_of_slot"], prob, T, k, ws, out=out)
+        mark(4)
+        gg.permute_rows(dOut, b["slot_of_row"], b["offsets"], k, E, rc, ws, dst=b["dYp"])
+        mark(5)
+        gg.grouped_dgrad(b["dYp"], W2, b["offsets"], gg.GG_EPI_SWIGLU_BWD, H1=b["H1"],
+                         prob_of_row=b["prob_of_row"], ws=ws, dA=b["dH"])
+        mark(6)
+        gg.grouped_dgrad(b["dH"], W1, b["offsets"], gg.GG_EPI_NONE, ws=ws, dA=b["dXp"])
+        mark(7)
+        gg.unpermute_combine(b["dXp"], b["row_of_slot"], None, T, k, ws, out=dX)
+        mark(8)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if gg.read_status(ws) != 0:
+        raise RuntimeError("device status after warm-up: " + gg.status_string(gg.read_status(ws)))
+
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    if sampler is not None:
+        time.sleep(0.5)  # let nvidia-smi start producing samples
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    n0 = gg.launch_count()
+    wall0 = time.time()
+    start.record(stream)
+    for s in range(args.steps):
+        step(ev[s])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    launches = gg.launch_count() - n0
+    if world > 1:
+        dist.barrier()
+    if sampler is not None:
+        sampler.mark(wall0, wall1)
+    local_s = start.elapsed_time(end) / 1e3
+    status = gg.read_status(ws)
+    if status != 0:
+        raise RuntimeError("device status after timing: " + gg.status_string(status))
+
+    per_op = {op: [ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps)]
+              for i, op in enumerate(ops)}
+    flop_step = shape.flop_fwd() + shape.flop_dgrad()
+    tot_s, tot_flop = aggregate(local_s, flop_step * args.steps,
+                                dev if world > 1 else None)
+    _, tot_tokens = aggregate(local_s, float(T * args.steps), dev if world > 1 else None)
+
+    # ---- end to end through the public API with host buffers (pinned)
+    h_x = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_dO = torch.from_numpy(inp.dOut.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_idx = torch.from_numpy(inp.idx).pin_memory()
+    h_prob = torch.from_numpy(inp.prob).pin_memory()
+    h_out = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    h_dX = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    d_x, d_dO = torch.empty_like(x), torch.empty_like(dOut)
+    d_idx, d_prob = torch.empty_like(idx), torch.empty_like(prob)
+
+    def e2e_step():
+        d_x.copy_(h_x, non_blocking=True)
+        d_idx.copy_(h_idx, non_blocking=True)
+        d_prob.copy_(h_prob, non_blocking=True)
+        d_dO.copy_(h_dO, non_blocking=True)
+        layer.forward(d_x, d_idx, d_prob, W1, W2, out=out)
+        layer.backward(d_dO, W1, W2, dX=dX)
+        h_out.copy_(out, non_blocking=True)
+        h_dX.copy_(dX, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s, _ = aggregate(e0.elapsed_time(e1) / 1e3, 0.0, dev if world > 1 else None)
+    h2d = x.numel() * 2 + dOut.numel() * 2 + idx.numel() * 4 + prob.numel() * 4
+    d2h = out.numel() * 2 + dX.numel() * 2
+
+    clocks = sampler.stop() if sampler is not None else None
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+
+    # ---- roofline of the dominant kernel
+    avg = {op: float(np.mean(v)) for op, v in per_op.items()}
+    total_ms = sum(avg.values())
+    R = shape.R
+    flop_of = {"fc1_swiglu": 4.0 * R * H * F, "fc2": 2.0 * R * H * F,
+               "dgrad_fc2_swiglu_bwd": 2.0 * R * H * F, "dgrad_fc1": 4.0 * R * H * F}
+    dom = max(avg, key=lambda o: avg[o])
+    if dom in flop_of:
+        ach = flop_of[dom] / (avg[dom] / 1e3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 2),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": None,
+                "peak_source": f"{peaks['source']} bf16 burst"}
+    else:
+        byts = {"permute": (T + R) * H * 2 + 8 * R, "permute_dout": (T + R) * H * 2,
+                "combine": (R + T) * H * 2 + 8 * R, "combine_dx": (R + T) * H * 2 + 4 * R}[dom]
+        ach = byts / (avg[dom] / 1e3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
+                "peak_source": f"{peaks['source']} hbm copy"}
+    hbm_ops = {"permute": (T + R) * H * 2 + 8 * R, "combine": (R + T) * H * 2 + 8 * R,
+               "permute_dout": (T + R) * H * 2, "combine_dx": (R + T) * H * 2 + 4 * R}
+    kernels = {}
+    for op in ops:
+        entry = {"ms": round(avg[op], 4), "share": round(avg[op] / total_ms, 4)}
+        if op in flop_of:
+            entry["tflops"] = round(flop_of[op] / (avg[op] / 1e3) / 1e12, 1)
+        else:
+            entry["gbs"] = round(hbm_ops[op] / (avg[op] / 1e3) / 1e9, 1)
+        kernels[op] = entry
+
+    # ---- CPU baseline: the oracle on a bounded token sample (rank 0, N = 1)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        times, n_tok = time_oracle(shape, inp, args.cpu_tokens)
+        sub = shape.with_tokens(n_tok)
+        cpu_val = (sub.flop_fwd() + sub.flop_dgrad()) / times[0] / 1e12
+        cpu = {"value": cpu_val, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{n_tok} of {T} tokens (all k slots), numpy fp64 forward + input "
+                         f"gradient, {times[0]:.2f} s, tokens/s {n_tok / times[0]:.1f}"}
+
+    value = tot_flop / tot_s / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot_s / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": shape.name, "E": E, "H": H, "F": F, "T": T, "k": k, "P": P,
+                   "routing": shape.routing, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (weights 1.2 GB, activations > 1 GB per step)"},
+        "tokens_per_s": round(tot_tokens / tot_s, 1),
+        "pct_bf16_peak": {"vs_2250_tflops": round(value / world / 2250.0, 4),
+                          "vs_measured_burst": round(value / world / peaks["bf16_tflops"], 4),
+                          "vs_measured_sustained": round(
+                              value / world / peaks["bf16_tflops_sustained"], 4)},
+        "roofline": roof, "kernels": kernels,
+        "e2e": {"value": round(tot_flop / e2e_s / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "tokens_per_s": round(T * args.steps * world / e2e_s, 1)},
+        "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return line
+
+
+# ------------------------------------------------------------------ the reference arm
+
+def run_reference(args, shape):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None  # the oracle runs once, on rank 0's host cores
+    inp = make_inputs(shape, 1000 * args.config)
+    import oracle
+
+    W1 = oracle.bf16_bits_to_f64(inp.W1)
+    W2 = oracle.bf16_bits_to_f64(inp.W2)
+    n = min(args.ref_tokens, shape.T)
+    rng = np.random.default_rng(0)
+
+    def step():
+        sel = np.sort(rng.choice(shape.T, size=n, replace=False))
+        fwd = oracle.moe_forward(inp.x[sel], inp.idx[sel], inp.prob[sel], W1, W2, shape.E, shape.P)
+        oracle.moe_backward(inp.dOut[sel], fwd, W1, W2)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    sub = shape.with_tokens(n)
+    flop = (sub.flop_fwd() + sub.flop_dgrad()) * args.steps
+    value = flop / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": shape.name, "E": shape.E, "H": shape.H, "F": shape.F,
+                   "T": shape.T, "k": shape.k, "P": shape.P, "routing": shape.routing,
+                   "parallelism": "host cores"},
+        "tokens_per_s": n * args.steps / dt,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(),
+                         "kind": "oracle",
+                         "sample": f"{n} random tokens of {shape.T} per step (all k slots), "
+                                   "numpy fp64 forward + input gradient"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gg", "reference"], default="gg")
+    ap.add_argument("--config", type=int, default=DEFAULT_CFG, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--tokens", type=int, default=0, help="override T (sweep points)")
+    ap.add_argument("--cpu-tokens", type=int, default=1024)
+    ap.add_argument("--ref-tokens", type=int, default=128)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    shape = CONFIGS[args.config]
+    if args.tokens:
+        shape = shape.with_tokens(args.tokens)
+    if args.impl == "reference":
+        return run_reference(args, shape)
+    return run_gg(args, shape, load_peaks())
+
+
+if __name__ == "__main__":
+    main()

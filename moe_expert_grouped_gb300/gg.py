@@ -148,11 +148,16 @@ def permute(x, idx, prob, E: int, P: int = 1, ws=None, out=None):
     _need(idx, torch.int32, (T, k), "idx")
     _need(prob, torch.float32, (T, k), "prob")
     o = out or {}
-    Xp = o.get("Xp", torch.empty((rc, H), dtype=torch.bfloat16, device=dev))
-    offsets = o.get("offsets", torch.empty(E + 1, dtype=torch.int32, device=dev))
-    ros = o.get("row_of_slot", torch.empty(T * k, dtype=torch.int32, device=dev))
-    sor = o.get("slot_of_row", torch.empty(rc, dtype=torch.int32, device=dev))
-    por = o.get("prob_of_row", torch.empty(rc, dtype=torch.float32, device=dev))
+
+    def buf(name, shape, dtype):
+        t = o.get(name)
+        return torch.empty(shape, dtype=dtype, device=dev) if t is None else t
+
+    Xp = buf("Xp", (rc, H), torch.bfloat16)
+    offsets = buf("offsets", (E + 1,), torch.int32)
+    ros = buf("row_of_slot", (T * k,), torch.int32)
+    sor = buf("slot_of_row", (rc,), torch.int32)
+    por = buf("prob_of_row", (rc,), torch.float32)
     ws = workspace(T, k, E, dev) if ws is None else ws
     _check(LIB.gg_permute(_ptr(x), _ptr(idx), _ptr(prob), T, H, k, E, P, _ptr(Xp), _ptr(offsets),
                           _ptr(ros), _ptr(sor), _ptr(por), _ptr(ws), ws.numel(), _stream(dev)),

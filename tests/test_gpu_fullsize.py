@@ -56,8 +56,12 @@ def _check_sample(inp, shape, out, dX, n_tokens, seed):
     sel = np.sort(rng.choice(shape.T, size=min(n_tokens, shape.T), replace=False))
     fwd = oracle.moe_forward(inp.x[sel], inp.idx[sel], inp.prob[sel], inp.W1, inp.W2, shape.E, 1)
     bwd = oracle.moe_backward(inp.dOut[sel], fwd, inp.W1, inp.W2)
-    assert_parity(torch_to_f64(out[torch.from_numpy(sel).cuda()]), fwd["out"], "out (sampled)")
-    assert_parity(torch_to_f64(dX[torch.from_numpy(sel).cuda()]), bwd["dX"], "dX (sampled)")
+    ffw = oracle.moe_forward(inp.x[sel], inp.idx[sel], inp.prob[sel], inp.W1, inp.W2, shape.E, 1,
+                             faithful=True)
+    fbw = oracle.moe_backward(inp.dOut[sel], ffw, inp.W1, inp.W2, faithful=True)
+    rows = torch.from_numpy(sel).cuda()
+    assert_parity(torch_to_f64(out[rows]), fwd["out"], "out (sampled)", faithful=ffw["out"])
+    assert_parity(torch_to_f64(dX[rows]), bwd["dX"], "dX (sampled)", faithful=fbw["dX"])
 
 
 @pytest.mark.parametrize("cfg", [2, 4])

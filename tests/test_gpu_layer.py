@@ -54,15 +54,20 @@ def test_layer_matches_oracle(gg, shape, seed):
     layer, out, dX = _run(gg, shape, d)
     fwd = oracle.moe_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, shape.E, shape.P)
     bwd = oracle.moe_backward(inp.dOut, fwd, inp.W1, inp.W2)
-    assert_parity(torch_to_f64(out), fwd["out"], "out")
-    assert_parity(torch_to_f64(dX), bwd["dX"], "dX")
+    ffw = oracle.moe_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, shape.E, shape.P,
+                             faithful=True)
+    fbw = oracle.moe_backward(inp.dOut, ffw, inp.W1, inp.W2, faithful=True)
+    assert_parity(torch_to_f64(out), fwd["out"], "out", faithful=ffw["out"])
+    assert_parity(torch_to_f64(dX), bwd["dX"], "dX", faithful=fbw["dX"])
     n = int(fwd["offsets"][-1])
     np.testing.assert_array_equal(layer.view("offsets").cpu().numpy(), fwd["offsets"])
     np.testing.assert_array_equal(layer.view("row_of_slot").cpu().numpy(), fwd["row_of_slot"])
     for name in ("H1", "A", "Yp"):
-        assert_parity(torch_to_f64(layer.view(name)[:n]), fwd[name][:n], name)
+        assert_parity(torch_to_f64(layer.view(name)[:n]), fwd[name][:n], name,
+                      faithful=ffw[name][:n])
     for name in ("dH", "dXp"):
-        assert_parity(torch_to_f64(layer.view(name)[:n]), bwd[name][:n], name)
+        assert_parity(torch_to_f64(layer.view(name)[:n]), bwd[name][:n], name,
+                      faithful=fbw[name][:n])
 
 
 def test_layer_run_to_run_bitwise(gg):
