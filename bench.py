@@ -88,7 +88,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", str(device_index)],
+                 "-lms", "50", "-i", str(device_index)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -125,7 +125,7 @@ class ClockSampler:
         sm = [num(s[0]) for s in used if num(s[0]) is not None]
         mx = [num(s[1]) for s in used if num(s[1]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for s in used for i in range(4) if "Active" in s[4 + i]})
+        reasons = sorted({names[i] for s in used for i in range(4) if s[4 + i] == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
                 "samples_in_window": len(inside), "samples": len(self.samples)}
@@ -418,12 +418,12 @@ def run_reference(args, shape):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gg", "reference"], default="gg")
     ap.add_argument("--config", type=int, default=DEFAULT_CFG, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--tokens", type=int, default=0, help="override T (sweep points)")
-    ap.add_argument("--cpu-tokens", type=int, default=1024)
+    ap.add_argument("--cpu-tokens", type=int, default=8192)
     ap.add_argument("--ref-tokens", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
