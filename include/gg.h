@@ -144,6 +144,38 @@ gg_status gg_permute(const gg_bf16* x, const int32_t* idx, const float* prob,
                      void* ws, size_t ws_bytes, gg_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * gg_permute_noalloc — gg_permute for callers that cannot allocate device
+ * memory (the pages have no counterpart: this is a service of this library).
+ *
+ * Some callers cannot provide a workspace: runtimes whose memory pool owns
+ * the whole GPU after start-up and forbid cudaMalloc on the hot path, plugins
+ * that receive only pre-sized input and output buffers from their host, C
+ * callers without a device allocator. This entry point computes exactly what
+ * gg_permute computes (same arguments, same outputs, bit-identical results)
+ * but takes no `ws`: its scratch (status word + per-block expert histograms)
+ * lives in a fixed 1 MiB array in the library's device image, which every GPU
+ * that loads the library keeps until the process exits. It calls no
+ * cudaMalloc, cudaFree or allocating library routine.
+ *   - Limit: gg_workspace_size(T, k, E) <= 1 MiB, i.e. ceil(T*k/2048) * E <=
+ *     262080 (for E = 128: T*k <= 4,192,256 pairs). Larger batches are
+ *     rejected with GG_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *   - Set-up: the first call on a device (made with that device current)
+ *     looks up the array's device address once; make that first call before
+ *     any stream capture.
+ *   - Every call on a device shares the one array and it keeps the previous
+ *     call's contents; each call clears the status word itself. Calls whose
+ *     work overlaps on the GPU (different streams without ordering between
+ *     them) race on the array and must not be issued.
+ *   - There is no readable status word: an expert id outside [0, E) is
+ *     visible in the outputs as row_of_slot == -1 and offsets[E] < T*k.
+ * ------------------------------------------------------------------------- */
+gg_status gg_permute_noalloc(const gg_bf16* x, const int32_t* idx, const float* prob,
+                             int T, int H, int k, int E, int pad_multiple,
+                             gg_bf16* Xp, int32_t* offsets, int32_t* row_of_slot,
+                             int32_t* slot_of_row, float* prob_of_row,
+                             gg_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * gg_permute_rows — gather of a token-major tensor into the permuted row
  * order of an earlier gg_permute (the combine's backward: the output
  * gradient dOut[T][H] is routed to the rows its token was sent to).

@@ -381,3 +381,84 @@ cudaError_t launch_bounded_wait_selftest(int32_t* status, uint64_t limit_ns, cud
 }
 
 }  // namespace gg
+
+// ---------------------------------------------------------------------------
+// Permute for callers that cannot allocate device memory.
+//
+// Some callers have no way to hand the library a workspace: a runtime whose
+// memory pool owns every byte of the GPU after start-up and forbids cudaMalloc
+// on its hot path, a plugin embedded in a host framework that gives it only
+// pre-sized input and output buffers, or a C caller without any device
+// allocator. For them gg_permute_noalloc keeps the permute's scratch (the
+// status word and the per-block expert histograms) in one fixed array in
+// device memory that is part of this library's image: every GPU that loads
+// the library holds these bytes until the process exits.
+//
+// The array's host-side name is only a stand-in for the symbol, not a device
+// address, so the host fetches the real address once per device with
+// cudaGetSymbolAddress (on the device that is current at the first call) and
+// passes that pointer to the kernels.
+#include <mutex>
+
+namespace gg {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(1) << 20;  // 1 MiB per device
+
+static __device__ __align__(256) uint8_t g_permute_scratch[kStaticScratchBytes];
+
+struct StaticScratchSlot {
+  std::once_flag once;
+  void* ptr = nullptr;
+  cudaError_t err = cudaErrorUnknown;
+};
+StaticScratchSlot g_static_scratch[64];
+
+}  // namespace
+}  // namespace gg
+
+extern "C" gg_status gg_permute_noalloc(const gg_bf16* x, const int32_t* idx, const float* prob,
+                                        int T, int H, int k, int E, int pad_multiple,
+                                        gg_bf16* Xp, int32_t* offsets, int32_t* row_of_slot,
+                                        int32_t* slot_of_row, float* prob_of_row,
+                                        gg_stream_t stream) {
+  using namespace gg;
+  if (T < 0 || H <= 0 || k <= 0 || E <= 0 || pad_multiple <= 0) return GG_ERR_INVALID_ARG;
+  if (k > E || k > 32) return GG_ERR_INVALID_ARG;
+  if (E > kMaxExperts || H % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
+  const long long R_cap = static_cast<long long>(T) * k + static_cast<long long>(E) * (pad_multiple - 1);
+  if (R_cap > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
+  if (offsets == nullptr) return GG_ERR_INVALID_ARG;
+  if (T > 0 && (x == nullptr || idx == nullptr || prob == nullptr || Xp == nullptr ||
+                row_of_slot == nullptr || slot_of_row == nullptr || prob_of_row == nullptr))
+    return GG_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(Xp) & 15u))
+    return GG_ERR_MISALIGNED;
+  // The batch must fit the fixed scratch: status header + one int32 per
+  // (2048-pair block, expert).
+  const size_t need = kWsHeader + sizeof(int32_t) * static_cast<size_t>(permute_blocks(
+                                                        static_cast<long long>(T) * k)) * E;
+  if (need > kStaticScratchBytes) return GG_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo dev;
+  gg_status s = current_device(&dev);
+  if (s != GG_OK) return s;
+  if (dev.cc_major != 10 || dev.cc_minor != 3) return GG_ERR_UNSUPPORTED_DEVICE;
+  StaticScratchSlot& slot = g_static_scratch[dev.device];
+  std::call_once(slot.once, [&slot] {
+    void* p = nullptr;
+    slot.err = cudaGetSymbolAddress(&p, g_permute_scratch);
+    if (slot.err == cudaSuccess) slot.ptr = p;
+  });
+  if (slot.err != cudaSuccess || slot.ptr == nullptr) return GG_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t* status = static_cast<int32_t*>(slot.ptr);
+  // The array keeps the previous call's bytes: the status word must start at
+  // zero; the histograms are fully rewritten before they are read.
+  if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return GG_ERR_CUDA;
+  int32_t* block_hist = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(slot.ptr) + kWsHeader);
+  return launch_permute(x, idx, prob, T, H, k, E, pad_multiple, Xp, offsets, row_of_slot,
+                        slot_of_row, prob_of_row, status, block_hist, dev.sm_count, st) ==
+                 cudaSuccess
+             ? GG_OK
+             : GG_ERR_CUDA;
+}

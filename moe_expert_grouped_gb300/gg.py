@@ -47,6 +47,7 @@ SIGNATURES = [
     ("gg_moe_mlp_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     ("gg_moe_mlp_bwd", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     ("gg_selftest_bounded_wait", _I, [_P, _Z, _U64, _P]),
+    ("gg_permute_noalloc", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
 ]
 
 
@@ -299,3 +300,29 @@ class MoeLayer:
 
     def status(self) -> int:
         return read_status(self.view("ws"))
+
+
+def permute_noalloc(x, idx, prob, E: int, P: int = 1, out=None):
+    """gg_permute_noalloc: the permute for callers that cannot allocate device
+    memory; the library keeps its scratch in a fixed array of its own (batches
+    with gg_workspace_size(T, k, E) > 1 MiB are rejected). Only the outputs
+    the caller does not pass are allocated here, by torch."""
+    T, H = x.shape
+    k = idx.shape[1]
+    dev = x.device
+    rc = r_cap(T, k, E, P)
+    o = out or {}
+
+    def buf(name, shape, dtype):
+        t = o.get(name)
+        return torch.empty(shape, dtype=dtype, device=dev) if t is None else t
+
+    Xp = buf("Xp", (rc, H), torch.bfloat16)
+    offsets = buf("offsets", (E + 1,), torch.int32)
+    ros = buf("row_of_slot", (T * k,), torch.int32)
+    sor = buf("slot_of_row", (rc,), torch.int32)
+    por = buf("prob_of_row", (rc,), torch.float32)
+    _check(LIB.gg_permute_noalloc(_ptr(x), _ptr(idx), _ptr(prob), T, H, k, E, P, _ptr(Xp),
+                                  _ptr(offsets), _ptr(ros), _ptr(sor), _ptr(por), _stream(dev)),
+           "gg_permute_noalloc")
+    return dict(Xp=Xp, offsets=offsets, row_of_slot=ros, slot_of_row=sor, prob_of_row=por)
