@@ -6,14 +6,15 @@
 // counts are read from the device-resident offsets array (NVIDIA/Megatron-LM
 // PR #7333, "Summary": device metadata, no host synchronisation).
 //
-// Design (one CTA per SM, 192 threads, warp-specialised):
+// Design (one CTA per SM, 320 threads, warp-specialised):
 //   warp 0     TMA producer: A tile 128 x 64 and B tile 256 x 64 (BF16,
 //              128-byte swizzle) per stage into a 4-stage shared-memory ring;
 //   warp 1     allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
 //              and one elected lane issues tcgen05.mma (M=128, N=256, K=16);
-//   warps 2-5  epilogue: tcgen05.ld the accumulator (one TMEM lane = one
-//              output row per thread), fused SwiGLU / SwiGLU-backward /
-//              probability scale, BF16 stores masked to the expert's rows.
+//   warps 2-9  epilogue: tcgen05.ld the accumulator (one TMEM lane = one
+//              output row per thread, two warps per lane quadrant splitting
+//              the columns), fused SwiGLU / SwiGLU-backward / probability
+//              scale, BF16 stores masked to the expert's rows.
 // The two accumulators let the epilogue of tile i overlap the MMAs of tile
 // i+1. Tiles are (expert, 128-row block, 256-column block), enumerated
 // expert-major with the column block fastest and dealt round-robin to CTAs.
@@ -44,7 +45,8 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
 constexpr int STAGES = 4;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
 constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KB
 constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
@@ -171,7 +173,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
       }
       for (int a = 0; a < 2; ++a) {
         mbar_init(smem_u32(&st.tfull[a]), 1);
-        mbar_init(smem_u32(&st.tempty[a]), 128);
+        mbar_init(smem_u32(&st.tempty[a]), 32 * kEpiWarps);
       }
       mbar_init(smem_u32(&st.mma_done), 1);
       mbar_fence_init();
@@ -283,8 +285,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
       (void)mbar_wait_bounded(smem_u32(&st.mma_done), 0, nullptr, p.status);
     }
   } else {
-    // -------------------------------------------------- epilogue (128 threads)
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    // -------------------------------------------------- epilogue (kEpiWarps warps)
+    // Warp w may only read TMEM lanes 32*(w%4) .. +31: two warps share each
+    // lane quadrant and split the tile's columns in halves.
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -293,17 +298,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
       decode_tile(tile, st.tiles_before, E, NT, e, mt, nt);
       const long long grow = static_cast<long long>(st.row_start[e]) + mt * BM + r;
       const bool valid = grow < st.row_start[e + 1];
-      if (!mbar_wait_bounded(smem_u32(&st.tfull[acc]), acc_phase, abort_flag, p.status)) break;
-      tc_fence_after();
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
 
       if (MODE == kFwdPlain || MODE == kDgradPlain) {
         float scale = 1.0f;
         if (MODE == kDgradPlain && p.row_scale != nullptr && valid) scale = p.row_scale[grow];
         const int n0 = nt * BN;
+        const int c0 = half * (BN / 2);
         gg_bf16* crow = p.C + grow * p.ldc + n0;
+        if (!mbar_wait_bounded(smem_u32(&st.tfull[acc]), acc_phase, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = c0; c < c0 + BN / 2; c += 32) {
           if (n0 + c >= p.Nout) break;
           float v[32];
           tmem_ld32(tbase + c, v);
@@ -312,10 +318,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
       } else if (MODE == kFwdSwiglu) {
         const int F = p.F;
         const int j0 = nt * (BN / 2);
+        const int c0 = half * (BN / 4);
         gg_bf16* arow = p.C + grow * F + j0;
         gg_bf16* hrow = p.H1_save != nullptr ? p.H1_save + grow * (2LL * F) + j0 : nullptr;
+        if (!mbar_wait_bounded(smem_u32(&st.tfull[acc]), acc_phase, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
 #pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 32) {
+        for (int c = c0; c < c0 + BN / 4; c += 32) {
           if (j0 + c >= F) break;
           float g[32], u[32];
           tmem_ld32(tbase + c, g);
@@ -341,35 +351,45 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         float scale = 1.0f;
         if (p.row_scale != nullptr && valid) scale = p.row_scale[grow];
         const int n0 = nt * BN;
+        const int c0 = half * (BN / 2);
+        const int c_end = min(c0 + BN / 2, F - n0);  // multiple of 32 (F % 64 == 0)
         const gg_bf16* hrow = p.H1 + grow * (2LL * F) + n0;
         gg_bf16* drow = p.C + grow * (2LL * F) + n0;
+        // The saved H1 does not depend on the accumulator: fetch the first
+        // chunk before waiting for the MMAs, then always one chunk ahead.
+        uint4 gw[4], uw[4];
+        auto fetch = [&](int c) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            gw[i] = __ldg(reinterpret_cast<const uint4*>(hrow + c) + i);
+            uw[i] = __ldg(reinterpret_cast<const uint4*>(hrow + F + c) + i);
+          }
+        };
+        if (valid && c0 < c_end) fetch(c0);
+        if (!mbar_wait_bounded(smem_u32(&st.tfull[acc]), acc_phase, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          if (n0 + c >= F) break;
+        for (int c = c0; c < c_end; c += 32) {
           float v[32];
           tmem_ld32(tbase + c, v);
           if (valid) {
-            const uint4* gp = reinterpret_cast<const uint4*>(hrow + c);
-            const uint4* up = reinterpret_cast<const uint4*>(hrow + F + c);
-            uint4 gw[4], uw[4];
+            uint32_t gs[16], us[16];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              gw[i] = __ldg(gp + i);
-              uw[i] = __ldg(up + i);
+              gs[4 * i + 0] = gw[i].x; gs[4 * i + 1] = gw[i].y;
+              gs[4 * i + 2] = gw[i].z; gs[4 * i + 3] = gw[i].w;
+              us[4 * i + 0] = uw[i].x; us[4 * i + 1] = uw[i].y;
+              us[4 * i + 2] = uw[i].z; us[4 * i + 3] = uw[i].w;
             }
+            if (c + 32 < c_end) fetch(c + 32);
             float dg[32], du[32];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint32_t gs[4] = {gw[i].x, gw[i].y, gw[i].z, gw[i].w};
-              const uint32_t us[4] = {uw[i].x, uw[i].y, uw[i].z, uw[i].w};
-#pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                const int i0 = 8 * i + 2 * h;
-                silu_mul_bwd(__fmul_rn(v[i0], scale), bf16_lo(gs[h]), bf16_lo(us[h]), dg[i0],
-                             du[i0]);
-                silu_mul_bwd(__fmul_rn(v[i0 + 1], scale), bf16_hi(gs[h]), bf16_hi(us[h]),
-                             dg[i0 + 1], du[i0 + 1]);
-              }
+            for (int h = 0; h < 16; ++h) {
+              silu_mul_bwd(__fmul_rn(v[2 * h], scale), bf16_lo(gs[h]), bf16_lo(us[h]), dg[2 * h],
+                           du[2 * h]);
+              silu_mul_bwd(__fmul_rn(v[2 * h + 1], scale), bf16_hi(gs[h]), bf16_hi(us[h]),
+                           dg[2 * h + 1], du[2 * h + 1]);
             }
             store_bf16x32(drow + c, dg, 1.0f);
             store_bf16x32(drow + F + c, du, 1.0f);

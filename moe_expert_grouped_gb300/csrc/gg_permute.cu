@@ -216,13 +216,20 @@ gather_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ sl
     }
     const uint4* sp = src + t * vec_per_row;
     int c = lane;
+    // eight independent 16-byte loads in flight per lane before the stores
+    for (; c + 224 < vec_per_row; c += 256) {
+      uint4 a[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a[i] = __ldg(sp + c + 32 * i);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) d[c + 32 * i] = a[i];
+    }
     for (; c + 96 < vec_per_row; c += 128) {
-      const uint4 a0 = __ldg(sp + c), a1 = __ldg(sp + c + 32), a2 = __ldg(sp + c + 64),
-                  a3 = __ldg(sp + c + 96);
-      d[c] = a0;
-      d[c + 32] = a1;
-      d[c + 64] = a2;
-      d[c + 96] = a3;
+      uint4 a[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = __ldg(sp + c + 32 * i);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d[c + 32 * i] = a[i];
     }
     for (; c < vec_per_row; c += 32) d[c] = __ldg(sp + c);
   }
