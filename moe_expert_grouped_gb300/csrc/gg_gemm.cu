@@ -45,7 +45,6 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
 constexpr int STAGES = 4;
-constexpr int kPrefetch = 8;  // L2 prefetch distance in k-blocks
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
 constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KB
@@ -201,39 +200,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
       uint32_t phase = 0;
       uint32_t used = 0, last_phase = 0;
       bool ok = true;
-      // Boxes of one k-block of a tile, as loads into shared memory or as L2
-      // prefetches. Every first touch of a weight or activation block comes
-      // from DRAM, so the producer prefetches kPrefetch k-blocks ahead of its
-      // loads (running on into its next tile) to hide the DRAM latency that
-      // the shared-memory ring alone cannot cover.
-      auto prefetch_kblock = [&](int pe, int prow0, int pnt, int kb) {
-        tma_prefetch_2d(&mapA, kb * BK, prow0);
-        if (MODE == kFwdPlain) {
-          tma_prefetch_3d(&mapB, kb * BK, pnt * BN, pe);
-        } else if (MODE == kFwdSwiglu) {
-          tma_prefetch_3d(&mapB, kb * BK, pnt * (BN / 2), pe);
-          tma_prefetch_3d(&mapB, kb * BK, p.F + pnt * (BN / 2), pe);
-        } else {
-#pragma unroll
-          for (int j = 0; j < BN / 64; ++j) tma_prefetch_3d(&mapB, pnt * BN + 64 * j, kb * BK, pe);
-        }
-      };
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         int e, mt, nt;
         decode_tile(tile, st.tiles_before, E, NT, e, mt, nt);
         const int row0 = st.row_start[e] + mt * BM;
-        const int next = tile + static_cast<int>(gridDim.x);
-        int ne = 0, nmt = 0, nnt = 0;
-        if (next < total) decode_tile(next, st.tiles_before, E, NT, ne, nmt, nnt);
-        const int nrow0 = next < total ? st.row_start[ne] + nmt * BM : 0;
-        if (tile == static_cast<int>(blockIdx.x))
-          for (int kb = 0; kb < min(kPrefetch, KB); ++kb) prefetch_kblock(e, row0, nt, kb);
         for (int kb = 0; kb < KB; ++kb) {
-          const int pk = kb + kPrefetch;
-          if (pk < KB)
-            prefetch_kblock(e, row0, nt, pk);
-          else if (next < total && pk - KB < KB)
-            prefetch_kblock(ne, nrow0, nnt, pk - KB);
           if (!mbar_wait_bounded(smem_u32(&st.empty[stage]), phase ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
