@@ -6,9 +6,13 @@
 // counts are read from the device-resident offsets array (NVIDIA/Megatron-LM
 // PR #7333, "Summary": device metadata, no host synchronisation).
 //
-// Design (one CTA per SM, 320 threads, warp-specialised):
+// Design (one CTA per SM, clusters of two CTAs, 320 threads, warp-specialised):
 //   warp 0     TMA producer: A tile 128 x 64 and B tile 256 x 64 (BF16,
 //              128-byte swizzle) per stage into a 4-stage shared-memory ring;
+//              the two CTAs of a cluster work on the same expert and column
+//              block with adjacent 128-row blocks, and each loads one half of
+//              the shared B tile and multicasts it to both, so every weight
+//              byte leaves L2 once per pair of row blocks;
 //   warp 1     allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
 //              and one elected lane issues tcgen05.mma (M=128, N=256, K=16);
 //   warps 2-9  epilogue: tcgen05.ld the accumulator (one TMEM lane = one
@@ -16,8 +20,9 @@
 //              the columns), fused SwiGLU / SwiGLU-backward / probability
 //              scale, BF16 stores masked to the expert's rows.
 // The two accumulators let the epilogue of tile i overlap the MMAs of tile
-// i+1. Tiles are (expert, 128-row block, 256-column block), enumerated
-// expert-major with the column block fastest and dealt round-robin to CTAs.
+// i+1. Work items are (expert, 256-row pair of row blocks, 256-column block),
+// enumerated expert-major with the column block fastest and dealt
+// round-robin to clusters; CTA rank r of a cluster takes row block 2*pair+r.
 // A row block that runs past its expert's last row reads the next expert's
 // rows (or TMA zero fill past R_cap) and those rows are simply not stored:
 // every output row depends only on its own input row and its expert's weight
@@ -29,7 +34,8 @@
 //
 // Every wait is bounded (gg_ptx.cuh); a wait that runs out records
 // GG_ERR_DEVICE_TIMEOUT, raises a CTA-wide abort flag, and the CTA drains its
-// in-flight TMA loads and MMAs, frees TMEM and exits.
+// in-flight TMA loads and MMAs, frees TMEM and exits after a final cluster
+// barrier (so no CTA leaves while its peer may still write into it).
 
 #include <cuda_runtime.h>
 
@@ -45,6 +51,8 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
 constexpr int STAGES = 4;
+constexpr int kCluster = 2;  // CTAs sharing one B tile
+constexpr uint16_t kClusterMask = 0x3;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
 constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KB
@@ -142,7 +150,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         const int o0 = p.offsets[e];
         const int o1 = p.offsets[e + 1];
         if (o1 < o0) bad = true;
-        tiles = o1 > o0 ? ((o1 - o0 + BM - 1) / BM) * NT : 0;
+        const int mtiles = (o1 - o0 + BM - 1) / BM;
+        tiles = o1 > o0 ? ((mtiles + kCluster - 1) / kCluster) * NT : 0;
         st.row_start[e] = o0;
       }
       int incl = tiles;
@@ -169,7 +178,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) {
         mbar_init(smem_u32(&st.full[s]), 1);
-        mbar_init(smem_u32(&st.empty[s]), 1);
+        mbar_init(smem_u32(&st.empty[s]), kCluster);  // both CTAs' MMAs
       }
       for (int a = 0; a < 2; ++a) {
         mbar_init(smem_u32(&st.tfull[a]), 1);
@@ -186,7 +195,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The peer's barriers must be initialised before any multicast load or
+  // commit can target them.
+  cluster_sync();
 
+  const uint32_t crank = cluster_ctarank();
+  const int cluster_id = static_cast<int>(blockIdx.x) / kCluster;
+  const int n_clusters = static_cast<int>(gridDim.x) / kCluster;
   const uint32_t tmem_base = st.tmem_base;
   const int total = st.total_tiles;
   volatile int* abort_flag = &st.abort_flag;
@@ -200,10 +215,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
       uint32_t phase = 0;
       uint32_t used = 0, last_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        int e, mt, nt;
-        decode_tile(tile, st.tiles_before, E, NT, e, mt, nt);
-        const int row0 = st.row_start[e] + mt * BM;
+      for (int tile = cluster_id; tile < total && ok; tile += n_clusters) {
+        int e, mp, nt;
+        decode_tile(tile, st.tiles_before, E, NT, e, mp, nt);
+        const int row0 = st.row_start[e] + (mp * kCluster + static_cast<int>(crank)) * BM;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&st.empty[stage]), phase ^ 1u, abort_flag, p.status)) {
             ok = false;
@@ -214,16 +229,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
           const uint32_t sa = sbase + stage * A_BYTES;
           const uint32_t sb = sbase + STAGES * A_BYTES + stage * B_BYTES;
           tma_load_2d(sa, &mapA, fb, kb * BK, row0);
+          // This CTA's half of the B tile, multicast into both CTAs; the
+          // barrier above expects the full tile (own half + peer's half).
+          const int h = static_cast<int>(crank);
           if (MODE == kFwdPlain) {
-            tma_load_3d(sb, &mapB, fb, kb * BK, nt * BN, e);
+            tma_load_3d_mc(sb + h * (B_BYTES / 2), &mapB, fb, kb * BK, nt * BN + h * (BN / 2), e,
+                           kClusterMask);
           } else if (MODE == kFwdSwiglu) {
-            const int j0 = nt * (BN / 2);
-            tma_load_3d(sb, &mapB, fb, kb * BK, j0, e);
-            tma_load_3d(sb + B_BYTES / 2, &mapB, fb, kb * BK, p.F + j0, e);
+            // half 0: gate rows j0.., half 1: up rows F + j0..
+            tma_load_3d_mc(sb + h * (B_BYTES / 2), &mapB, fb, kb * BK, h * p.F + nt * (BN / 2), e,
+                           kClusterMask);
           } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_3d(sb + j * (B_BYTES / 4), &mapB, fb, nt * BN + 64 * j, kb * BK, e);
+            for (int j = 2 * h; j < 2 * h + 2; ++j)
+              tma_load_3d_mc(sb + j * (B_BYTES / 4), &mapB, fb, nt * BN + 64 * j, kb * BK, e,
+                             kClusterMask);
           }
           used |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
@@ -233,11 +253,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
           }
         }
       }
-      // Every issued load must have landed before the CTA may exit.
+      // Every load issued into this CTA (own and the peer's multicast half)
+      // must have landed, and both CTAs' MMAs must have released every stage
+      // (their commits arrive on this CTA's barriers), before the CTA exits.
       for (int s = 0; s < STAGES; ++s)
-        if (used & (1u << s))
+        if (used & (1u << s)) {
           (void)mbar_wait_bounded(smem_u32(&st.full[s]), (last_phase >> s) & 1u, nullptr,
                                   p.status);
+          (void)mbar_wait_bounded(smem_u32(&st.empty[s]), (last_phase >> s) & 1u, nullptr,
+                                  p.status);
+        }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -249,7 +274,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = cluster_id; tile < total && ok; tile += n_clusters) {
         if (!mbar_wait_bounded(smem_u32(&st.tempty[acc]), acc_phase ^ 1u, abort_flag, p.status))
           break;
         tc_fence_after();
@@ -269,7 +294,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                                        : make_sdesc(sb + kk * 32, 16, 1024);
             tc_mma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          tc_commit(smem_u32(&st.empty[stage]));
+          // the stage is free once both CTAs' MMAs have read it
+          tc_commit_mc(smem_u32(&st.empty[stage]), kClusterMask);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -293,9 +319,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     const int r = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      int e, mt, nt;
-      decode_tile(tile, st.tiles_before, E, NT, e, mt, nt);
+    for (int tile = cluster_id; tile < total; tile += n_clusters) {
+      int e, mp, nt;
+      decode_tile(tile, st.tiles_before, E, NT, e, mp, nt);
+      const int mt = mp * kCluster + static_cast<int>(crank);
       const long long grow = static_cast<long long>(st.row_start[e]) + mt * BM + r;
       const bool valid = grow < st.row_start[e + 1];
 
@@ -409,6 +436,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
+  cluster_sync();
 }
 
 // Standalone SwiGLU over rows [0, offsets[E]) — same arithmetic as the fused
@@ -472,17 +500,37 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, int rank, const cuuint6
 template <int MODE>
 cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& kp,
                         const DeviceInfo& dev, cudaStream_t stream) {
-  static int configured_for[64] = {0};
+  // Per device: the shared-memory opt-in and the number of clusters that can
+  // be resident at once (the grid is persistent: one cluster per SM pair).
+  static int clusters_for[64] = {0};
   const int d = dev.device & 63;
-  if (!configured_for[d]) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (clusters_for[d] == 0) {
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    configured_for[d] = 1;
+    int n = 0;
+    cfg.gridDim = dim3(static_cast<unsigned>((dev.sm_count / kCluster) * kCluster), 1, 1);
+    e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<MODE>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorInvalidConfiguration;
+    clusters_for[d] = n < dev.sm_count / kCluster ? n : dev.sm_count / kCluster;
   }
-  grouped_gemm_kernel<MODE><<<dev.sm_count, kThreads, kSmemBytes, stream>>>(ma, mb, kp);
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters_for[d] * kCluster), 1, 1);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, ma, mb, kp);
   count_launch();
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -506,8 +554,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaSt
                                 static_cast<cuuint64_t>(a.E)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.Kw) * 2,
                                    static_cast<cuuint64_t>(a.Kw) * a.Nw * 2};
-    cuuint32_t box[3] = {BK, BN, 1};
-    if (a.mode == kFwdSwiglu) box[1] = BN / 2;
+    cuuint32_t box[3] = {BK, BN / 2, 1};  // each CTA of a pair loads half of B
     if (a.mode == kDgradPlain || a.mode == kDgradSwigluBwd) box[1] = 64;
     if (!encode_bf16_map(&mb, a.B, 3, dims, strides, box)) {
       *host_err = GG_ERR_CUDA;
