@@ -6,27 +6,32 @@
 // counts are read from the device-resident offsets array (NVIDIA/Megatron-LM
 // PR #7333, "Summary": device metadata, no host synchronisation).
 //
-// Design (one CTA per SM, clusters of two CTAs, 320 threads, warp-specialised):
-//   warp 0     TMA producer: A tile 128 x 64 and B tile 256 x 64 (BF16,
-//              128-byte swizzle) per stage into a 4-stage shared-memory ring;
-//              the two CTAs of a cluster work on the same expert and column
-//              block with adjacent 128-row blocks, and each loads one half of
-//              the shared B tile and multicasts it to both, so every weight
-//              byte leaves L2 once per pair of row blocks;
-//   warp 1     allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
-//              and one elected lane issues tcgen05.mma (M=128, N=256, K=16);
-//   warps 2-9  epilogue: tcgen05.ld the accumulator (one TMEM lane = one
-//              output row per thread, two warps per lane quadrant splitting
-//              the columns), fused SwiGLU / SwiGLU-backward / probability
-//              scale, BF16 stores masked to the expert's rows.
+// Design (one CTA per SM, clusters of two CTAs = one tcgen05 MMA pair,
+// 320 threads per CTA, warp-specialised):
+//   warp 0     TMA producer in each CTA: its own 128 rows of A (128 x 64) and
+//              its half of the B tile (128 x 64 of 256 x 64), BF16 with
+//              128-byte swizzle, into a 6-stage ring (32 KB per stage); the
+//              loads of both CTAs complete on the even CTA's barrier;
+//   warp 1     allocates 512 TMEM columns in both CTAs (two 128 x 256 fp32
+//              accumulators each); in the even CTA one lane issues
+//              tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16) over the
+//              pair's shared memory and multicasts its commits to both CTAs;
+//   warps 2-9  epilogue in each CTA: tcgen05.ld of its 128 accumulator rows
+//              (one TMEM lane = one output row per thread, two warps per lane
+//              quadrant splitting the columns), fused SwiGLU / SwiGLU-backward
+//              / probability scale, BF16 stores masked to the expert's rows;
+//              then each warp reports the accumulator free to the even CTA.
+// Per SM and 64-deep K step the pair moves 32 KB into shared memory for a
+// 128 x 256 x 64 product (a single-CTA 128 x 256 tile needs 48 KB), which
+// halves the per-SM weight traffic and leaves room for a deeper ring.
 // The two accumulators let the epilogue of tile i overlap the MMAs of tile
 // i+1. Work items are (expert, 256-row pair of row blocks, 256-column block),
 // enumerated expert-major with the column block fastest and dealt
-// round-robin to clusters; CTA rank r of a cluster takes row block 2*pair+r.
-// A row block that runs past its expert's last row reads the next expert's
-// rows (or TMA zero fill past R_cap) and those rows are simply not stored:
-// every output row depends only on its own input row and its expert's weight
-// (bitwise batch invariance).
+// round-robin to clusters; CTA rank r takes row block 2*pair+r. A row block
+// that runs past its expert's last row reads the next expert's rows (or TMA
+// zero fill past R_cap) and those rows are simply not stored: every output
+// row depends only on its own input row and its expert's weight (bitwise
+// batch invariance).
 //
 // The dgrad variants read the forward weight [E][N][K] as an N-contiguous
 // ("MN-major") B operand straight from its forward layout, so no transposed
@@ -50,14 +55,14 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr int kCluster = 2;  // CTAs sharing one B tile
+constexpr int STAGES = 6;
+constexpr int kCluster = 2;  // the two CTAs of one MMA pair
 constexpr uint16_t kClusterMask = 0x3;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
-constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KB
-constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KB
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t A_BYTES = BM * BK * 2;               // 16 KB: this CTA's A rows
+constexpr uint32_t B_HALF_BYTES = (BN / 2) * BK * 2;     // 16 KB: this CTA's half of B
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_HALF_BYTES;  // per CTA and stage
 constexpr uint32_t TMEM_COLS = 512;
 
 struct SmemTail {
@@ -138,6 +143,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
   const int E = p.E;
   const int NT = p.NT;
   const int KB = p.Kred / BK;
+  const uint32_t crank = cluster_ctarank();
+  const bool leader = crank == 0;
 
   // ---- tile table from the device offsets (warp 0), TMEM (warp 1)
   if (warp == 0) {
@@ -177,29 +184,28 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
       if (bad && blockIdx.x == 0) set_status(p.status, GG_ERR_DEVICE_BAD_OFFSETS);
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) {
-        mbar_init(smem_u32(&st.full[s]), 1);
-        mbar_init(smem_u32(&st.empty[s]), kCluster);  // both CTAs' MMAs
+        mbar_init(smem_u32(&st.full[s]), 1);   // even CTA: its producer's expect_tx
+        mbar_init(smem_u32(&st.empty[s]), 1);  // the pair's MMA commit
       }
       for (int a = 0; a < 2; ++a) {
         mbar_init(smem_u32(&st.tfull[a]), 1);
-        mbar_init(smem_u32(&st.tempty[a]), 32 * kEpiWarps);
+        mbar_init(smem_u32(&st.tempty[a]), kCluster * kEpiWarps);  // every epilogue warp
       }
       mbar_init(smem_u32(&st.mma_done), 1);
       mbar_fence_init();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
   } else if (warp == 1) {
-    tmem_alloc(smem_u32(&st.tmem_base), TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(&st.tmem_base), TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // The peer's barriers must be initialised before any multicast load or
-  // commit can target them.
+  // Both CTAs' barriers must be initialised before any load, commit or
+  // arrive of the pair can target them.
   cluster_sync();
 
-  const uint32_t crank = cluster_ctarank();
   const int cluster_id = static_cast<int>(blockIdx.x) / kCluster;
   const int n_clusters = static_cast<int>(gridDim.x) / kCluster;
   const uint32_t tmem_base = st.tmem_base;
@@ -208,9 +214,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
 
   if (warp == 0) {
     if (lane == 0) {
-      // ------------------------------------------------ TMA producer
+      // ------------------------------------------------ TMA producer (both CTAs)
       tma_prefetch_desc(&mapA);
       tma_prefetch_desc(&mapB);
+      const int h = static_cast<int>(crank);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t used = 0, last_phase = 0;
@@ -218,32 +225,28 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
       for (int tile = cluster_id; tile < total && ok; tile += n_clusters) {
         int e, mp, nt;
         decode_tile(tile, st.tiles_before, E, NT, e, mp, nt);
-        const int row0 = st.row_start[e] + (mp * kCluster + static_cast<int>(crank)) * BM;
+        const int row0 = st.row_start[e] + (mp * kCluster + h) * BM;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&st.empty[stage]), phase ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
           }
-          const uint32_t fb = smem_u32(&st.full[stage]);
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          const uint32_t sa = sbase + stage * A_BYTES;
-          const uint32_t sb = sbase + STAGES * A_BYTES + stage * B_BYTES;
-          tma_load_2d(sa, &mapA, fb, kb * BK, row0);
-          // This CTA's half of the B tile, multicast into both CTAs; the
-          // barrier above expects the full tile (own half + peer's half).
-          const int h = static_cast<int>(crank);
+          // the even CTA's barrier counts the bytes of both CTAs' loads
+          if (leader) mbar_arrive_expect_tx(smem_u32(&st.full[stage]), kCluster * STAGE_BYTES);
+          const uint32_t fb = mapa_shared(smem_u32(&st.full[stage]), 0);
+          const uint32_t sa = sbase + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          tma_load_2d_pair(sa, &mapA, fb, kb * BK, row0);
           if (MODE == kFwdPlain) {
-            tma_load_3d_mc(sb + h * (B_BYTES / 2), &mapB, fb, kb * BK, nt * BN + h * (BN / 2), e,
-                           kClusterMask);
+            tma_load_3d_pair(sb, &mapB, fb, kb * BK, nt * BN + h * (BN / 2), e);
           } else if (MODE == kFwdSwiglu) {
             // half 0: gate rows j0.., half 1: up rows F + j0..
-            tma_load_3d_mc(sb + h * (B_BYTES / 2), &mapB, fb, kb * BK, h * p.F + nt * (BN / 2), e,
-                           kClusterMask);
+            tma_load_3d_pair(sb, &mapB, fb, kb * BK, h * p.F + nt * (BN / 2), e);
           } else {
 #pragma unroll
-            for (int j = 2 * h; j < 2 * h + 2; ++j)
-              tma_load_3d_mc(sb + j * (B_BYTES / 4), &mapB, fb, nt * BN + 64 * j, kb * BK, e,
-                             kClusterMask);
+            for (int j = 0; j < 2; ++j)
+              tma_load_3d_pair(sb + j * (B_HALF_BYTES / 2), &mapB, fb,
+                               nt * BN + h * (BN / 2) + 64 * j, kb * BK, e);
           }
           used |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
@@ -253,22 +256,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
           }
         }
       }
-      // Every load issued into this CTA (own and the peer's multicast half)
-      // must have landed, and both CTAs' MMAs must have released every stage
-      // (their commits arrive on this CTA's barriers), before the CTA exits.
+      // Before the CTA may exit, the pair's MMAs must have consumed (and so
+      // the loads must have landed in) every stage this producer filled.
       for (int s = 0; s < STAGES; ++s)
         if (used & (1u << s)) {
-          (void)mbar_wait_bounded(smem_u32(&st.full[s]), (last_phase >> s) & 1u, nullptr,
-                                  p.status);
+          if (leader)
+            (void)mbar_wait_bounded(smem_u32(&st.full[s]), (last_phase >> s) & 1u, nullptr,
+                                    p.status);
           (void)mbar_wait_bounded(smem_u32(&st.empty[s]), (last_phase >> s) & 1u, nullptr,
                                   p.status);
         }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------ MMA issuer
+    if (lane == 0 && leader) {
+      // ------------------------------------------------ MMA issuer (even CTA)
       constexpr bool kMN = (MODE == kDgradPlain || MODE == kDgradSwigluBwd);
-      constexpr uint32_t idesc = make_idesc_bf16(BM, BN, kMN);
+      constexpr uint32_t idesc = make_idesc_bf16(kCluster * BM, BN, kMN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -285,29 +288,29 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             break;
           }
           tc_fence_after();
-          const uint32_t sa = sbase + stage * A_BYTES;
-          const uint32_t sb = sbase + STAGES * A_BYTES + stage * B_BYTES;
+          const uint32_t sa = sbase + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t adesc = make_sdesc(sa + kk * 32, 16, 1024);
-            const uint64_t bdesc = kMN ? make_sdesc(sb + kk * 2048, B_BYTES / 4, 1024)
+            const uint64_t bdesc = kMN ? make_sdesc(sb + kk * 2048, B_HALF_BYTES / 2, 1024)
                                        : make_sdesc(sb + kk * 32, 16, 1024);
-            tc_mma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+            tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          // the stage is free once both CTAs' MMAs have read it
-          tc_commit_mc(smem_u32(&st.empty[stage]), kClusterMask);
+          // the stage is free in both CTAs once these MMAs have read it
+          tc_commit_pair_mc(smem_u32(&st.empty[stage]), kClusterMask);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(smem_u32(&st.tfull[acc]));
+        tc_commit_pair_mc(smem_u32(&st.tfull[acc]), kClusterMask);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
-      // All MMAs of this thread must retire before TMEM is freed.
-      tc_commit(smem_u32(&st.mma_done));
+      // All MMAs of the pair must retire before TMEM is freed.
+      tc_commit_pair(smem_u32(&st.mma_done));
       (void)mbar_wait_bounded(smem_u32(&st.mma_done), 0, nullptr, p.status);
     }
   } else {
@@ -325,7 +328,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
       const int mt = mp * kCluster + static_cast<int>(crank);
       const long long grow = static_cast<long long>(st.row_start[e]) + mt * BM + r;
       const bool valid = grow < st.row_start[e + 1];
-
       if (MODE == kFwdPlain || MODE == kDgradPlain) {
         float scale = 1.0f;
         if (MODE == kDgradPlain && p.row_scale != nullptr && valid) scale = p.row_scale[grow];
@@ -424,7 +426,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         }
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&st.tempty[acc]));
+      __syncwarp();
+      // this warp's share of the accumulator is free: tell the MMA issuer
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&st.tempty[acc]), 0));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -434,7 +438,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
   cluster_sync();
 }
