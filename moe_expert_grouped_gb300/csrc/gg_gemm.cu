@@ -79,7 +79,11 @@ struct SmemTail {
   int row_start[kMaxExperts + 1];
 };
 
-constexpr size_t kSmemBytes = 1024 + STAGES * STAGE_BYTES + sizeof(SmemTail);
+// Each epilogue warp owns a 2 KB staging buffer (32 rows x 32 BF16) used to
+// turn row-per-lane results into row-contiguous global stores and loads.
+constexpr uint32_t kWarpStagingBytes = 32 * 64;
+constexpr uint32_t kStagingBytes = kEpiWarps * kWarpStagingBytes;
+constexpr size_t kSmemBytes = 1024 + STAGES * STAGE_BYTES + kStagingBytes + sizeof(SmemTail);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 struct KParams {
@@ -114,17 +118,69 @@ __device__ __forceinline__ void decode_tile(int tile, const int* tb, int E, int 
   nt = local - mt * NT;
 }
 
-__device__ __forceinline__ void store_bf16x32(gg_bf16* dst, const float (&v)[32], float scale) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+__device__ __forceinline__ void pack_bf16x32(const float (&v)[32], float scale, uint4 (&w)[4]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint4 o;
-    o.x = pack_bf16x2(__fmul_rn(v[8 * i + 0], scale), __fmul_rn(v[8 * i + 1], scale));
-    o.y = pack_bf16x2(__fmul_rn(v[8 * i + 2], scale), __fmul_rn(v[8 * i + 3], scale));
-    o.z = pack_bf16x2(__fmul_rn(v[8 * i + 4], scale), __fmul_rn(v[8 * i + 5], scale));
-    o.w = pack_bf16x2(__fmul_rn(v[8 * i + 6], scale), __fmul_rn(v[8 * i + 7], scale));
-    d[i] = o;
+    w[i].x = pack_bf16x2(v[8 * i + 0] * scale, v[8 * i + 1] * scale);
+    w[i].y = pack_bf16x2(v[8 * i + 2] * scale, v[8 * i + 3] * scale);
+    w[i].z = pack_bf16x2(v[8 * i + 4] * scale, v[8 * i + 5] * scale);
+    w[i].w = pack_bf16x2(v[8 * i + 6] * scale, v[8 * i + 7] * scale);
   }
+}
+
+// 16-byte slot of column group c (0..3) of row r (0..31) in a warp's staging
+// buffer; the XOR spreads every 8-lane shared-memory phase over all banks.
+__device__ __forceinline__ int stage_slot(int r, int c) { return r * 4 + (c ^ ((r >> 1) & 3)); }
+
+// Warp-collective store of a 32-row x 32-column BF16 chunk. Lane i holds row
+// i in w[]; `dst` is its row pointer at the chunk's first column and rows with
+// valid == false are skipped. Through the staging buffer four lanes write
+// each 64-byte row segment, so every store instruction writes 8 whole row
+// segments instead of 32 scattered 16-byte pieces.
+__device__ __forceinline__ void store_chunk(uint4* stg, const uint4 (&w)[4], gg_bf16* dst,
+                                            bool valid) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) stg[stage_slot(lane, c)] = w[c];
+  __syncwarp();
+  const unsigned long long mine = reinterpret_cast<unsigned long long>(dst);
+  const int ok_mine = valid ? 1 : 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = 8 * j + (lane >> 2);
+    const int c = lane & 3;
+    const uint4 v = stg[stage_slot(r, c)];
+    const unsigned long long p = __shfl_sync(0xFFFFFFFFu, mine, r);
+    if (__shfl_sync(0xFFFFFFFFu, ok_mine, r)) reinterpret_cast<uint4*>(p)[c] = v;
+  }
+  __syncwarp();
+}
+
+// Warp-collective coalesced fetch of a 32-row x 32-column BF16 chunk: lane L
+// loads column group L%4 of rows 8j + L/4 (raw layout); rows with valid ==
+// false read as zero. transpose_chunk() then hands each lane its own row.
+__device__ __forceinline__ void load_chunk_raw(uint4 (&raw)[4], const gg_bf16* src, bool valid) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long mine = reinterpret_cast<unsigned long long>(src);
+  const int ok_mine = valid ? 1 : 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = 8 * j + (lane >> 2);
+    const unsigned long long p = __shfl_sync(0xFFFFFFFFu, mine, r);
+    raw[j] = __shfl_sync(0xFFFFFFFFu, ok_mine, r)
+                 ? __ldg(reinterpret_cast<const uint4*>(p) + (lane & 3))
+                 : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+__device__ __forceinline__ void transpose_chunk(uint4* stg, const uint4 (&raw)[4], uint4 (&w)[4]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) stg[stage_slot(8 * j + (lane >> 2), lane & 3)] = raw[j];
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < 4; ++c) w[c] = stg[stage_slot(lane, c)];
+  __syncwarp();
 }
 
 template <int MODE>
@@ -136,7 +192,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
   const uint32_t sbase = raw_addr + pad;  // 1024-aligned: required by the 128B swizzle
-  SmemTail& st = *reinterpret_cast<SmemTail*>(smem + STAGES * STAGE_BYTES);
+  SmemTail& st = *reinterpret_cast<SmemTail*>(smem + STAGES * STAGE_BYTES + kStagingBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -328,6 +384,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
       const int mt = mp * kCluster + static_cast<int>(crank);
       const long long grow = static_cast<long long>(st.row_start[e]) + mt * BM + r;
       const bool valid = grow < st.row_start[e + 1];
+      uint4* stg = reinterpret_cast<uint4*>(smem + STAGES * STAGE_BYTES +
+                                            (warp - 2) * kWarpStagingBytes);
       if (MODE == kFwdPlain || MODE == kDgradPlain) {
         float scale = 1.0f;
         if (MODE == kDgradPlain && p.row_scale != nullptr && valid) scale = p.row_scale[grow];
@@ -342,14 +400,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
           if (n0 + c >= p.Nout) break;
           float v[32];
           tmem_ld32(tbase + c, v);
-          if (valid) store_bf16x32(crow + c, v, scale);
+          uint4 w[4];
+          pack_bf16x32(v, scale, w);
+          store_chunk(stg, w, crow + c, valid);
         }
       } else if (MODE == kFwdSwiglu) {
         const int F = p.F;
         const int j0 = nt * (BN / 2);
         const int c0 = half * (BN / 4);
         gg_bf16* arow = p.C + grow * F + j0;
-        gg_bf16* hrow = p.H1_save != nullptr ? p.H1_save + grow * (2LL * F) + j0 : nullptr;
+        gg_bf16* hrow = p.H1_save + grow * (2LL * F) + j0;
         if (!mbar_wait_bounded(smem_u32(&st.tfull[acc]), acc_phase, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
@@ -359,21 +419,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
           float g[32], u[32];
           tmem_ld32(tbase + c, g);
           tmem_ld32(tbase + BN / 2 + c, u);
-          if (valid) {
+          uint4 w[4];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              g[i] = round_bf16(g[i]);
-              u[i] = round_bf16(u[i]);
-            }
-            if (hrow != nullptr) {
-              store_bf16x32(hrow + c, g, 1.0f);
-              store_bf16x32(hrow + F + c, u, 1.0f);
-            }
-            float a[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] = silu_mul(g[i], u[i]);
-            store_bf16x32(arow + c, a, 1.0f);
+          for (int i = 0; i < 32; ++i) {
+            g[i] = round_bf16(g[i]);
+            u[i] = round_bf16(u[i]);
           }
+          if (p.H1_save != nullptr) {
+            pack_bf16x32(g, 1.0f, w);
+            store_chunk(stg, w, hrow + c, valid);
+            pack_bf16x32(u, 1.0f, w);
+            store_chunk(stg, w, hrow + F + c, valid);
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) g[i] = silu_mul(g[i], u[i]);
+          pack_bf16x32(g, 1.0f, w);
+          store_chunk(stg, w, arow + c, valid);
         }
       } else {  // kDgradSwigluBwd: F = Nout, output row [dg | du] of width 2F
         const int F = p.Nout;
@@ -386,15 +447,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         gg_bf16* drow = p.C + grow * (2LL * F) + n0;
         // The saved H1 does not depend on the accumulator: fetch the first
         // chunk before waiting for the MMAs, then always one chunk ahead.
-        uint4 gw[4], uw[4];
-        auto fetch = [&](int c) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            gw[i] = __ldg(reinterpret_cast<const uint4*>(hrow + c) + i);
-            uw[i] = __ldg(reinterpret_cast<const uint4*>(hrow + F + c) + i);
-          }
-        };
-        if (valid && c0 < c_end) fetch(c0);
+        uint4 graw[4], uraw[4];
+        if (c0 < c_end) {
+          load_chunk_raw(graw, hrow + c0, valid);
+          load_chunk_raw(uraw, hrow + F + c0, valid);
+        }
         if (!mbar_wait_bounded(smem_u32(&st.tfull[acc]), acc_phase, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
@@ -402,27 +459,33 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         for (int c = c0; c < c_end; c += 32) {
           float v[32];
           tmem_ld32(tbase + c, v);
-          if (valid) {
-            uint32_t gs[16], us[16];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              gs[4 * i + 0] = gw[i].x; gs[4 * i + 1] = gw[i].y;
-              gs[4 * i + 2] = gw[i].z; gs[4 * i + 3] = gw[i].w;
-              us[4 * i + 0] = uw[i].x; us[4 * i + 1] = uw[i].y;
-              us[4 * i + 2] = uw[i].z; us[4 * i + 3] = uw[i].w;
-            }
-            if (c + 32 < c_end) fetch(c + 32);
-            float dg[32], du[32];
-#pragma unroll
-            for (int h = 0; h < 16; ++h) {
-              silu_mul_bwd(__fmul_rn(v[2 * h], scale), bf16_lo(gs[h]), bf16_lo(us[h]), dg[2 * h],
-                           du[2 * h]);
-              silu_mul_bwd(__fmul_rn(v[2 * h + 1], scale), bf16_hi(gs[h]), bf16_hi(us[h]),
-                           dg[2 * h + 1], du[2 * h + 1]);
-            }
-            store_bf16x32(drow + c, dg, 1.0f);
-            store_bf16x32(drow + F + c, du, 1.0f);
+          uint4 gw[4], uw[4];
+          transpose_chunk(stg, graw, gw);
+          transpose_chunk(stg, uraw, uw);
+          if (c + 32 < c_end) {
+            load_chunk_raw(graw, hrow + c + 32, valid);
+            load_chunk_raw(uraw, hrow + F + c + 32, valid);
           }
+          uint32_t gs[16], us[16];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            gs[4 * i + 0] = gw[i].x; gs[4 * i + 1] = gw[i].y;
+            gs[4 * i + 2] = gw[i].z; gs[4 * i + 3] = gw[i].w;
+            us[4 * i + 0] = uw[i].x; us[4 * i + 1] = uw[i].y;
+            us[4 * i + 2] = uw[i].z; us[4 * i + 3] = uw[i].w;
+          }
+          float dg[32], du[32];
+#pragma unroll
+          for (int h = 0; h < 16; ++h) {
+            silu_mul_bwd(v[2 * h] * scale, bf16_lo(gs[h]), bf16_lo(us[h]), dg[2 * h], du[2 * h]);
+            silu_mul_bwd(v[2 * h + 1] * scale, bf16_hi(gs[h]), bf16_hi(us[h]), dg[2 * h + 1],
+                         du[2 * h + 1]);
+          }
+          uint4 w[4];
+          pack_bf16x32(dg, 1.0f, w);
+          store_chunk(stg, w, drow + c, valid);
+          pack_bf16x32(du, 1.0f, w);
+          store_chunk(stg, w, drow + F + c, valid);
         }
       }
       tc_fence_before();
