@@ -131,7 +131,9 @@ gg_status gg_read_status(const void* ws, gg_stream_t stream, int32_t* host_statu
  *   prob_of_row[R_cap] fp32, prob[t][j] of the row's pair, 0 on padding and
  *                     on rows >= offsets[E];
  *   Xp[R_cap][H]      BF16, Xp[row] = x[t]; zero on padding rows; rows
- *                     >= offsets[E] are left untouched.
+ *                     >= offsets[E] are left untouched. Xp may be NULL:
+ *                     then only the row maps and offsets are produced (the
+ *                     gathered GEMMs below read the token rows themselves).
  * Inputs: x[T][H] BF16, idx[T][k] int32 expert ids, prob[T][k] fp32; k <= 32.
  * Indices are bit-exact and independent of scheduling. T = 0 only writes
  * offsets (all zero). An id outside [0, E) sets GG_ERR_DEVICE_BAD_EXPERT_ID
@@ -247,6 +249,31 @@ gg_status gg_grouped_dgrad(const gg_bf16* dC, const gg_bf16* B, const int32_t* o
                            void* ws, size_t ws_bytes, gg_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * gg_grouped_fwd_gather / gg_grouped_dgrad_gather — the same GEMMs with the
+ * permuted operand gathered on the fly instead of read from a materialised
+ * buffer ([P3] "Summary": per-expert metadata on the device; the permute
+ * only has to produce row maps):
+ *   A[r] = src[slot_of_row[r] / k] for slot_of_row[r] >= 0, zero otherwise,
+ * with src token-major [T][K] (fwd: x; dgrad: dOut, then [T][N]) and
+ * slot_of_row / k from gg_permute. Every other argument, output and error is
+ * as in gg_grouped_fwd / gg_grouped_dgrad, and the results are bitwise equal
+ * to running them on the gathered buffer (gg_permute's Xp, or
+ * gg_permute_rows' output). The tensor core's A tiles are loaded by TMA
+ * four-row gathers, so the permuted copy never touches HBM.
+ * ------------------------------------------------------------------------- */
+gg_status gg_grouped_fwd_gather(const gg_bf16* src, int T, const int32_t* slot_of_row, int k,
+                                const gg_bf16* B, const int32_t* offsets,
+                                int E, int R_cap, int K, int N, gg_epilogue epi,
+                                gg_bf16* C, gg_bf16* H1_save,
+                                void* ws, size_t ws_bytes, gg_stream_t stream);
+
+gg_status gg_grouped_dgrad_gather(const gg_bf16* src, int T, const int32_t* slot_of_row, int k,
+                                  const gg_bf16* B, const int32_t* offsets,
+                                  int E, int R_cap, int K, int N, gg_epilogue epi,
+                                  const gg_bf16* H1, const float* prob_of_row, gg_bf16* dA,
+                                  void* ws, size_t ws_bytes, gg_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * gg_unpermute_combine — probability-weighted combine ([P4] "What does this
  * PR do?": the probability boundary; [P1]: the all-to-all combine side):
  *   out[t] = bf16( sum_{j<k} prob[t][j] * Yp[row_of_slot[t*k+j]] )
@@ -265,11 +292,9 @@ gg_status gg_unpermute_combine(const gg_bf16* Yp, const int32_t* row_of_slot,
  * intermediate; gg_moe_buffers_bind() carves it (256-byte aligned pieces).
  * ------------------------------------------------------------------------- */
 typedef struct gg_moe_buffers {
-  gg_bf16* Xp;          /* [R_cap][H]  permuted input                     */
   gg_bf16* H1;          /* [R_cap][2F] FC1 output (BF16), kept for dgrad  */
   gg_bf16* A;           /* [R_cap][F]  SwiGLU output                      */
   gg_bf16* Yp;          /* [R_cap][H]  FC2 output                         */
-  gg_bf16* dYp;         /* [R_cap][H]  permuted output gradient           */
   gg_bf16* dH;          /* [R_cap][2F] gradient w.r.t. FC1 output         */
   gg_bf16* dXp;         /* [R_cap][H]  gradient w.r.t. permuted input     */
   int32_t* offsets;     /* [E+1]                                          */
@@ -288,17 +313,17 @@ size_t gg_moe_buffers_size(int T, int H, int F, int k, int E, int pad_multiple);
 gg_status gg_moe_buffers_bind(void* base, size_t bytes, int T, int H, int F, int k,
                               int E, int pad_multiple, gg_moe_buffers* out);
 
-/* Forward: permute -> grouped FC1 + fused SwiGLU (H1 kept) -> grouped FC2
- * -> probability-weighted combine into out[T][H]. Four stages, all on
- * `stream`, no host synchronisation. */
+/* Forward: permute (row maps only) -> grouped FC1 on the gathered token rows
+ * + fused SwiGLU (H1 kept) -> grouped FC2 -> probability-weighted combine
+ * into out[T][H]. All on `stream`, no host synchronisation. */
 gg_status gg_moe_mlp_fwd(const gg_bf16* x, const int32_t* idx, const float* prob,
                          const gg_bf16* W1, const gg_bf16* W2,
                          int T, int H, int F, int k, int E, int pad_multiple,
                          gg_bf16* out, const gg_moe_buffers* buf, gg_stream_t stream);
 
 /* Input gradient of gg_moe_mlp_fwd (same buffers, after the forward):
- * permute dOut -> dgrad FC2 with probability scale and fused SwiGLU
- * backward -> dgrad FC1 -> unweighted combine into dX[T][H]. */
+ * dgrad FC2 on the gathered dOut rows with probability scale and fused
+ * SwiGLU backward -> dgrad FC1 -> unweighted combine into dX[T][H]. */
 gg_status gg_moe_mlp_bwd(const gg_bf16* dOut, const gg_bf16* W1, const gg_bf16* W2,
                          int T, int H, int F, int k, int E, int pad_multiple,
                          gg_bf16* dX, const gg_moe_buffers* buf, gg_stream_t stream);

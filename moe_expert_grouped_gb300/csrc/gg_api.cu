@@ -142,9 +142,10 @@ gg_status gg_permute(const gg_bf16* x, const int32_t* idx, const float* prob, in
   if (E > kMaxExperts || H % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
   if (r_cap_of(T, k, E, pad_multiple) > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
   if (offsets == nullptr) return GG_ERR_INVALID_ARG;
-  if (T > 0 && (x == nullptr || idx == nullptr || prob == nullptr || Xp == nullptr ||
-                row_of_slot == nullptr || slot_of_row == nullptr || prob_of_row == nullptr))
+  if (T > 0 && (idx == nullptr || prob == nullptr || row_of_slot == nullptr ||
+                slot_of_row == nullptr || prob_of_row == nullptr))
     return GG_ERR_INVALID_ARG;
+  if (T > 0 && Xp != nullptr && x == nullptr) return GG_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(Xp)) return GG_ERR_MISALIGNED;
   gg_status s = check_ws(ws, ws_bytes, gg_workspace_size(T, k, E));
   if (s != GG_OK) return s;
@@ -265,6 +266,91 @@ gg_status gg_grouped_dgrad(const gg_bf16* dC, const gg_bf16* B, const int32_t* o
   return from_cuda(e);
 }
 
+static gg_status gather_checks(const gg_bf16* src, int T, const int32_t* slot_of_row, int k) {
+  if (T < 0 || k <= 0 || src == nullptr || slot_of_row == nullptr) return GG_ERR_INVALID_ARG;
+  if (!aligned16(src)) return GG_ERR_MISALIGNED;
+  return GG_OK;
+}
+
+gg_status gg_grouped_fwd_gather(const gg_bf16* src, int T, const int32_t* slot_of_row, int k,
+                                const gg_bf16* B, const int32_t* offsets, int E, int R_cap, int K,
+                                int N, gg_epilogue epi, gg_bf16* C, gg_bf16* H1_save, void* ws,
+                                size_t ws_bytes, gg_stream_t stream) {
+  gg_status s = gather_checks(src, T, slot_of_row, k);
+  if (s != GG_OK) return s;
+  // the source stands in for A in the common checks
+  s = gemm_common_checks(src, B, offsets, E, R_cap, K, N, C, ws, ws_bytes);
+  if (s != GG_OK) return s;
+  if (epi != GG_EPI_NONE && epi != GG_EPI_SWIGLU) return GG_ERR_INVALID_ARG;
+  if (epi == GG_EPI_NONE && H1_save != nullptr) return GG_ERR_INVALID_ARG;
+  if (epi == GG_EPI_SWIGLU && N % 128 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(H1_save)) return GG_ERR_MISALIGNED;
+  DeviceInfo dev;
+  if ((s = device_ok(&dev)) != GG_OK) return s;
+  if (R_cap == 0 || T == 0) return GG_OK;
+  GemmArgs a{};
+  a.mode = epi == GG_EPI_SWIGLU ? kFwdSwiglu : kFwdPlain;
+  a.B = B;
+  a.offsets = offsets;
+  a.E = E;
+  a.R_cap = R_cap;
+  a.Kred = K;
+  a.Nout = N;
+  a.Nw = N;
+  a.Kw = K;
+  a.C = C;
+  a.H1_save = H1_save;
+  a.status = status_ptr(ws);
+  a.gather_src = src;
+  a.slot_of_row = slot_of_row;
+  a.gather_k = k;
+  a.gather_rows = T;
+  gg_status he = GG_OK;
+  cudaError_t e = launch_grouped_gemm(a, dev, reinterpret_cast<cudaStream_t>(stream), &he);
+  if (he != GG_OK) return he;
+  return from_cuda(e);
+}
+
+gg_status gg_grouped_dgrad_gather(const gg_bf16* src, int T, const int32_t* slot_of_row, int k,
+                                  const gg_bf16* B, const int32_t* offsets, int E, int R_cap,
+                                  int K, int N, gg_epilogue epi, const gg_bf16* H1,
+                                  const float* prob_of_row, gg_bf16* dA, void* ws,
+                                  size_t ws_bytes, gg_stream_t stream) {
+  gg_status s = gather_checks(src, T, slot_of_row, k);
+  if (s != GG_OK) return s;
+  s = gemm_common_checks(src, B, offsets, E, R_cap, K, N, dA, ws, ws_bytes);
+  if (s != GG_OK) return s;
+  if (epi != GG_EPI_NONE && epi != GG_EPI_SWIGLU_BWD) return GG_ERR_INVALID_ARG;
+  if (epi == GG_EPI_NONE && H1 != nullptr) return GG_ERR_INVALID_ARG;
+  if (epi == GG_EPI_SWIGLU_BWD && H1 == nullptr) return GG_ERR_INVALID_ARG;
+  if (!aligned16(H1)) return GG_ERR_MISALIGNED;
+  DeviceInfo dev;
+  if ((s = device_ok(&dev)) != GG_OK) return s;
+  if (R_cap == 0 || T == 0) return GG_OK;
+  GemmArgs a{};
+  a.mode = epi == GG_EPI_SWIGLU_BWD ? kDgradSwigluBwd : kDgradPlain;
+  a.B = B;
+  a.offsets = offsets;
+  a.E = E;
+  a.R_cap = R_cap;
+  a.Kred = N;
+  a.Nout = K;
+  a.Nw = N;
+  a.Kw = K;
+  a.C = dA;
+  a.H1 = H1;
+  a.row_scale = prob_of_row;
+  a.status = status_ptr(ws);
+  a.gather_src = src;
+  a.slot_of_row = slot_of_row;
+  a.gather_k = k;
+  a.gather_rows = T;
+  gg_status he = GG_OK;
+  cudaError_t e = launch_grouped_gemm(a, dev, reinterpret_cast<cudaStream_t>(stream), &he);
+  if (he != GG_OK) return he;
+  return from_cuda(e);
+}
+
 gg_status gg_unpermute_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const float* prob,
                                int T, int k, int H, int R_cap, gg_bf16* out, void* ws,
                                size_t ws_bytes, gg_stream_t stream) {
@@ -288,7 +374,7 @@ size_t gg_moe_buffers_size(int T, int H, int F, int k, int E, int pad_multiple) 
   const size_t R_cap = static_cast<size_t>(r_cap_of(T, k, E, pad_multiple));
   const size_t b2 = sizeof(gg_bf16);
   size_t n = 0;
-  n += align256(R_cap * H * b2) * 4;         // Xp, Yp, dYp, dXp
+  n += align256(R_cap * H * b2) * 2;         // Yp, dXp
   n += align256(R_cap * 2 * F * b2) * 2;     // H1, dH
   n += align256(R_cap * F * b2);             // A
   n += align256(sizeof(int32_t) * (E + 1));  // offsets
@@ -315,9 +401,7 @@ gg_status gg_moe_buffers_bind(void* base, size_t bytes, int T, int H, int F, int
   };
   const size_t b2 = sizeof(gg_bf16);
   std::memset(out, 0, sizeof(*out));
-  out->Xp = reinterpret_cast<gg_bf16*>(take(R_cap * H * b2));
   out->Yp = reinterpret_cast<gg_bf16*>(take(R_cap * H * b2));
-  out->dYp = reinterpret_cast<gg_bf16*>(take(R_cap * H * b2));
   out->dXp = reinterpret_cast<gg_bf16*>(take(R_cap * H * b2));
   out->H1 = reinterpret_cast<gg_bf16*>(take(R_cap * 2 * F * b2));
   out->dH = reinterpret_cast<gg_bf16*>(take(R_cap * 2 * F * b2));
@@ -334,8 +418,8 @@ gg_status gg_moe_buffers_bind(void* base, size_t bytes, int T, int H, int F, int
 
 static gg_status check_buffers(const gg_moe_buffers* b, int T, int k, int E) {
   if (b == nullptr) return GG_ERR_INVALID_ARG;
-  if (b->Xp == nullptr || b->H1 == nullptr || b->A == nullptr || b->Yp == nullptr ||
-      b->dYp == nullptr || b->dH == nullptr || b->dXp == nullptr || b->offsets == nullptr ||
+  if (b->H1 == nullptr || b->A == nullptr || b->Yp == nullptr || b->dH == nullptr ||
+      b->dXp == nullptr || b->offsets == nullptr ||
       b->row_of_slot == nullptr || b->slot_of_row == nullptr || b->prob_of_row == nullptr)
     return GG_ERR_INVALID_ARG;
   return check_ws(b->ws, b->ws_bytes, gg_workspace_size(T, k, E));
@@ -354,11 +438,14 @@ gg_status gg_moe_mlp_fwd(const gg_bf16* x, const int32_t* idx, const float* prob
   const long long rc = r_cap_of(T, k, E, pad_multiple);
   if (rc > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
   const int R_cap = static_cast<int>(rc);
-  s = gg_permute(x, idx, prob, T, H, k, E, pad_multiple, buf->Xp, buf->offsets, buf->row_of_slot,
+  if (T > 0 && x == nullptr) return GG_ERR_INVALID_ARG;
+  // Row maps only: FC1 gathers the token rows itself, so the permuted copy
+  // of x is never written.
+  s = gg_permute(x, idx, prob, T, H, k, E, pad_multiple, nullptr, buf->offsets, buf->row_of_slot,
                  buf->slot_of_row, buf->prob_of_row, buf->ws, buf->ws_bytes, stream);
   if (s != GG_OK || T == 0) return s;
-  s = gg_grouped_fwd(buf->Xp, W1, buf->offsets, E, R_cap, H, 2 * F, GG_EPI_SWIGLU, buf->A,
-                     buf->H1, buf->ws, buf->ws_bytes, stream);
+  s = gg_grouped_fwd_gather(x, T, buf->slot_of_row, k, W1, buf->offsets, E, R_cap, H, 2 * F,
+                            GG_EPI_SWIGLU, buf->A, buf->H1, buf->ws, buf->ws_bytes, stream);
   if (s != GG_OK) return s;
   s = gg_grouped_fwd(buf->A, W2, buf->offsets, E, R_cap, F, H, GG_EPI_NONE, buf->Yp, nullptr,
                      buf->ws, buf->ws_bytes, stream);
@@ -381,12 +468,11 @@ gg_status gg_moe_mlp_bwd(const gg_bf16* dOut, const gg_bf16* W1, const gg_bf16* 
   const long long rc = r_cap_of(T, k, E, pad_multiple);
   if (rc > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
   const int R_cap = static_cast<int>(rc);
-  s = gg_permute_rows(dOut, buf->slot_of_row, buf->offsets, T, H, k, E, R_cap, buf->dYp, buf->ws,
-                      buf->ws_bytes, stream);
-  if (s != GG_OK) return s;
-  // dH = SwiGLU'(H1) applied to prob_of_row * (dYp @ W2_e); W2 is [E][H][F]
-  s = gg_grouped_dgrad(buf->dYp, W2, buf->offsets, E, R_cap, F, H, GG_EPI_SWIGLU_BWD, buf->H1,
-                       buf->prob_of_row, buf->dH, buf->ws, buf->ws_bytes, stream);
+  // dH = SwiGLU'(H1) applied to prob_of_row * (dYp @ W2_e), W2 being [E][H][F];
+  // dYp (dOut routed to the permuted rows) is gathered inside the GEMM.
+  s = gg_grouped_dgrad_gather(dOut, T, buf->slot_of_row, k, W2, buf->offsets, E, R_cap, F, H,
+                              GG_EPI_SWIGLU_BWD, buf->H1, buf->prob_of_row, buf->dH, buf->ws,
+                              buf->ws_bytes, stream);
   if (s != GG_OK) return s;
   // dXp = dH @ W1_e; W1 is [E][2F][H]
   s = gg_grouped_dgrad(buf->dH, W1, buf->offsets, E, R_cap, H, 2 * F, GG_EPI_NONE, nullptr,

@@ -100,6 +100,9 @@ struct KParams {
   const gg_bf16* H1;
   const float* row_scale;
   int32_t* status;
+  const int32_t* slot_of_row;  // gathered A: source row of every permuted row
+  int gather_k;
+  int gather_rows;             // rows of the gather source; this index reads zeros
 };
 
 __device__ __forceinline__ void decode_tile(int tile, const int* tb, int E, int NT, int& e,
@@ -183,7 +186,7 @@ __device__ __forceinline__ void transpose_chunk(uint4* stg, const uint4 (&raw)[4
   __syncwarp();
 }
 
-template <int MODE>
+template <int MODE, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     const __grid_constant__ CUtensorMap mapB, const KParams p) {
@@ -269,30 +272,52 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
   volatile int* abort_flag = &st.abort_flag;
 
   if (warp == 0) {
+    // ------------------------------------------------ TMA producer (both CTAs)
+    // Lane 0 waits for free stages, arms the barrier and loads B; A is loaded
+    // by lane 0 as one box, or, when gathered, by all 32 lanes as four-row
+    // gathers of the token rows each permuted row stands for.
     if (lane == 0) {
-      // ------------------------------------------------ TMA producer (both CTAs)
       tma_prefetch_desc(&mapA);
       tma_prefetch_desc(&mapB);
-      const int h = static_cast<int>(crank);
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t used = 0, last_phase = 0;
-      bool ok = true;
-      for (int tile = cluster_id; tile < total && ok; tile += n_clusters) {
-        int e, mp, nt;
-        decode_tile(tile, st.tiles_before, E, NT, e, mp, nt);
-        const int row0 = st.row_start[e] + (mp * kCluster + h) * BM;
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&st.empty[stage]), phase ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
+    }
+    const int h = static_cast<int>(crank);
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t used = 0, last_phase = 0;
+    bool ok = true;
+    for (int tile = cluster_id; tile < total && ok; tile += n_clusters) {
+      int e, mp, nt;
+      decode_tile(tile, st.tiles_before, E, NT, e, mp, nt);
+      const int row0 = st.row_start[e] + (mp * kCluster + h) * BM;
+      int src[4] = {0, 0, 0, 0};
+      if (GATHER) {
+        const int row_end = st.row_start[e + 1];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = row0 + 4 * lane + i;
+          const int slot = r < row_end ? p.slot_of_row[r] : -1;
+          src[i] = slot >= 0 ? slot / p.gather_k : p.gather_rows;  // past the end: zero fill
+        }
+      }
+      if (!GATHER && lane != 0) continue;
+      for (int kb = 0; kb < KB; ++kb) {
+        int free_ok = 1;
+        if (lane == 0)
+          free_ok = mbar_wait_bounded(smem_u32(&st.empty[stage]), phase ^ 1u, abort_flag, p.status)
+                        ? 1
+                        : 0;
+        if (GATHER) free_ok = __shfl_sync(0xFFFFFFFFu, free_ok, 0);
+        if (!free_ok) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = mapa_shared(smem_u32(&st.full[stage]), 0);
+        const uint32_t sa = sbase + stage * STAGE_BYTES;
+        const uint32_t sb = sa + A_BYTES;
+        if (lane == 0) {
           // the even CTA's barrier counts the bytes of both CTAs' loads
           if (leader) mbar_arrive_expect_tx(smem_u32(&st.full[stage]), kCluster * STAGE_BYTES);
-          const uint32_t fb = mapa_shared(smem_u32(&st.full[stage]), 0);
-          const uint32_t sa = sbase + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
-          tma_load_2d_pair(sa, &mapA, fb, kb * BK, row0);
+          if (!GATHER) tma_load_2d_pair(sa, &mapA, fb, kb * BK, row0);
           if (MODE == kFwdPlain) {
             tma_load_3d_pair(sb, &mapB, fb, kb * BK, nt * BN + h * (BN / 2), e);
           } else if (MODE == kFwdSwiglu) {
@@ -304,16 +329,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
               tma_load_3d_pair(sb + j * (B_HALF_BYTES / 2), &mapB, fb,
                                nt * BN + h * (BN / 2) + 64 * j, kb * BK, e);
           }
-          used |= 1u << stage;
-          last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+        }
+        if (GATHER) {
+          __syncwarp();  // the barrier is armed before any lane's gather lands
+          tma_gather4_pair(sa + lane * 4 * 128, &mapA, fb, kb * BK, src[0], src[1], src[2],
+                           src[3]);
+        }
+        used |= 1u << stage;
+        last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      // Before the CTA may exit, the pair's MMAs must have consumed (and so
-      // the loads must have landed in) every stage this producer filled.
+    }
+    // Before the CTA may exit, the pair's MMAs must have consumed (and so
+    // the loads must have landed in) every stage this producer filled.
+    if (lane == 0)
       for (int s = 0; s < STAGES; ++s)
         if (used & (1u << s)) {
           if (leader)
@@ -322,7 +354,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
           (void)mbar_wait_bounded(smem_u32(&st.empty[s]), (last_phase >> s) & 1u, nullptr,
                                   p.status);
         }
-    }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------ MMA issuer (even CTA)
@@ -564,7 +595,7 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, int rank, const cuuint6
   return r == CUDA_SUCCESS;
 }
 
-template <int MODE>
+template <int MODE, bool GATHER>
 cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& kp,
                         const DeviceInfo& dev, cudaStream_t stream) {
   // Per device: the shared-memory opt-in and the number of clusters that can
@@ -583,19 +614,19 @@ cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const KPar
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (clusters_for[d] == 0) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, GATHER>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     int n = 0;
     cfg.gridDim = dim3(static_cast<unsigned>((dev.sm_count / kCluster) * kCluster), 1, 1);
-    e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<MODE>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<MODE, GATHER>, &cfg);
     if (e != cudaSuccess) return e;
     if (n <= 0) return cudaErrorInvalidConfiguration;
     clusters_for[d] = n < dev.sm_count / kCluster ? n : dev.sm_count / kCluster;
   }
   cfg.gridDim = dim3(static_cast<unsigned>(clusters_for[d] * kCluster), 1, 1);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, ma, mb, kp);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE, GATHER>, ma, mb, kp);
   count_launch();
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -607,11 +638,15 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaSt
                                 gg_status* host_err) {
   *host_err = GG_OK;
   CUtensorMap ma, mb;
+  const bool gather = a.gather_src != nullptr;
   {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.Kred), static_cast<cuuint64_t>(a.R_cap)};
+    // Direct: box of 128 rows over A[R_cap][Kred]. Gathered: one-row box over
+    // the token-major source, loaded four rows at a time.
+    const cuuint64_t rows = gather ? static_cast<cuuint64_t>(a.gather_rows) : a.R_cap;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.Kred), rows};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.Kred) * 2};
-    const cuuint32_t box[2] = {BK, BM};
-    if (!encode_bf16_map(&ma, a.A, 2, dims, strides, box)) {
+    const cuuint32_t box[2] = {BK, gather ? 1u : static_cast<cuuint32_t>(BM)};
+    if (!encode_bf16_map(&ma, gather ? a.gather_src : a.A, 2, dims, strides, box)) {
       *host_err = GG_ERR_CUDA;
       return cudaErrorInvalidValue;
     }
@@ -639,27 +674,34 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaSt
   kp.H1 = a.H1;
   kp.row_scale = a.row_scale;
   kp.status = a.status;
+  kp.slot_of_row = a.slot_of_row;
+  kp.gather_k = a.gather_k;
+  kp.gather_rows = a.gather_rows;
   switch (a.mode) {
     case kFwdPlain:
       kp.F = 0;
       kp.NT = (a.Nout + BN - 1) / BN;
       kp.ldc = a.Nout;
-      return launch_mode<kFwdPlain>(ma, mb, kp, dev, stream);
+      return gather ? launch_mode<kFwdPlain, true>(ma, mb, kp, dev, stream)
+                    : launch_mode<kFwdPlain, false>(ma, mb, kp, dev, stream);
     case kFwdSwiglu:
       kp.F = a.Nout / 2;
       kp.NT = (kp.F + BN / 2 - 1) / (BN / 2);
       kp.ldc = kp.F;
-      return launch_mode<kFwdSwiglu>(ma, mb, kp, dev, stream);
+      return gather ? launch_mode<kFwdSwiglu, true>(ma, mb, kp, dev, stream)
+                    : launch_mode<kFwdSwiglu, false>(ma, mb, kp, dev, stream);
     case kDgradPlain:
       kp.F = 0;
       kp.NT = (a.Nout + BN - 1) / BN;
       kp.ldc = a.Nout;
-      return launch_mode<kDgradPlain>(ma, mb, kp, dev, stream);
+      return gather ? launch_mode<kDgradPlain, true>(ma, mb, kp, dev, stream)
+                    : launch_mode<kDgradPlain, false>(ma, mb, kp, dev, stream);
     case kDgradSwigluBwd:
       kp.F = a.Nout;
       kp.NT = (a.Nout + BN - 1) / BN;
       kp.ldc = 2LL * a.Nout;
-      return launch_mode<kDgradSwigluBwd>(ma, mb, kp, dev, stream);
+      return gather ? launch_mode<kDgradSwigluBwd, true>(ma, mb, kp, dev, stream)
+                    : launch_mode<kDgradSwigluBwd, false>(ma, mb, kp, dev, stream);
   }
   *host_err = GG_ERR_INVALID_ARG;
   return cudaErrorInvalidValue;

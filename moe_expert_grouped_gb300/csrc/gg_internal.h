@@ -35,6 +35,7 @@ struct DeviceInfo {
 gg_status current_device(DeviceInfo* out);
 
 // ------------------------------------------------------------------ gg_permute.cu
+// Xp may be null: then only the row maps and offsets are produced.
 cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* prob, int T, int H,
                            int k, int E, int P, gg_bf16* Xp, int32_t* offsets,
                            int32_t* row_of_slot, int32_t* slot_of_row, float* prob_of_row,
@@ -74,6 +75,12 @@ struct GemmArgs {
   const gg_bf16* H1;       // dgrad SwiGLU backward: [R_cap][2F]
   const float* row_scale;  // dgrad: prob_of_row or null
   int32_t* status;
+  // Gathered A operand: row r of A is gather_src[slot_of_row[r] / gather_k]
+  // (zero where the slot is -1); gather_src is token-major [gather_rows][Kred].
+  const gg_bf16* gather_src = nullptr;
+  const int32_t* slot_of_row = nullptr;
+  int gather_k = 1;
+  int gather_rows = 0;
 };
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t stream,

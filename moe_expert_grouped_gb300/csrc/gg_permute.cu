@@ -344,9 +344,11 @@ cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* pr
   permute_scatter_kernel<<<nb, kPermuteBlockThreads, hist_smem, stream>>>(
       idx, prob, R, E, block_hist, offsets, row_of_slot, slot_of_row, prob_of_row);
   count_launch();
-  err = launch_gather_rows(x, slot_of_row, offsets, H, k, E, static_cast<int>(R_cap), T, Xp,
-                           status, sm_count, stream);
-  if (err != cudaSuccess) return err;
+  if (Xp != nullptr) {
+    err = launch_gather_rows(x, slot_of_row, offsets, H, k, E, static_cast<int>(R_cap), T, Xp,
+                             status, sm_count, stream);
+    if (err != cudaSuccess) return err;
+  }
   return cudaGetLastError();
 }
 

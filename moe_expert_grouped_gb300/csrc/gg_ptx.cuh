@@ -121,6 +121,20 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
+// Gather of four rows (r0..r3) of a 2-D tensor, columns [c0, c0 + box width),
+// into four consecutive box rows at dst; completion is counted on an mbarrier
+// of either CTA of the MMA pair. The tensor map's box is one row high.
+__device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t cluster_bar, int c0, int r0, int r1,
+                                                 int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4"
+      ".mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(cluster_bar)
+      : "memory");
+}
+
 // ----------------------------------------------------------------- tcgen05
 
 // Shared-memory matrix descriptor (64 bit):

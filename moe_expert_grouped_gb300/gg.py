@@ -48,6 +48,9 @@ SIGNATURES = [
     ("gg_moe_mlp_bwd", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     ("gg_selftest_bounded_wait", _I, [_P, _Z, _U64, _P]),
     ("gg_permute_noalloc", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    ("gg_grouped_fwd_gather", _I, [_P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
+    ("gg_grouped_dgrad_gather", _I,
+     [_P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
 ]
 
 
@@ -55,8 +58,8 @@ class GGBuffers(ctypes.Structure):
     """Mirror of struct gg_moe_buffers."""
 
     _fields_ = [(n, ctypes.c_void_p) for n in (
-        "Xp", "H1", "A", "Yp", "dYp", "dH", "dXp", "offsets", "row_of_slot", "slot_of_row",
-        "prob_of_row", "ws")] + [("ws_bytes", ctypes.c_size_t)]
+        "H1", "A", "Yp", "dH", "dXp", "offsets", "row_of_slot", "slot_of_row", "prob_of_row",
+        "ws")] + [("ws_bytes", ctypes.c_size_t)]
 
 
 class GGError(RuntimeError):
@@ -154,7 +157,7 @@ def permute(x, idx, prob, E: int, P: int = 1, ws=None, out=None):
         t = o.get(name)
         return torch.empty(shape, dtype=dtype, device=dev) if t is None else t
 
-    Xp = buf("Xp", (rc, H), torch.bfloat16)
+    Xp = None if "Xp" in o and o["Xp"] is None else buf("Xp", (rc, H), torch.bfloat16)
     offsets = buf("offsets", (E + 1,), torch.int32)
     ros = buf("row_of_slot", (T * k,), torch.int32)
     sor = buf("slot_of_row", (rc,), torch.int32)
@@ -190,6 +193,44 @@ def grouped_fwd(A, B, offsets, epilogue: int = GG_EPI_NONE, ws=None, C=None, H1_
                               _ptr(H1_save), _ptr(ws), ws.numel(), _stream(dev)),
            "gg_grouped_fwd")
     return C
+
+
+def grouped_fwd_gather(src, slot_of_row, k: int, B, offsets, epilogue: int = GG_EPI_NONE,
+                       ws=None, C=None, H1_save=None):
+    """gg_grouped_fwd_gather: A rows gathered from token-major src [T, K]."""
+    T, K = src.shape
+    E, N, Kb = B.shape
+    if Kb != K:
+        raise ValueError("src and B disagree on K")
+    R_cap = slot_of_row.shape[0]
+    dev = src.device
+    ncols = N // 2 if epilogue == GG_EPI_SWIGLU else N
+    C = torch.empty((R_cap, ncols), dtype=torch.bfloat16, device=dev) if C is None else C
+    ws = workspace(0, 1, E, dev) if ws is None else ws
+    _check(LIB.gg_grouped_fwd_gather(_ptr(src), T, _ptr(slot_of_row), k, _ptr(B), _ptr(offsets),
+                                     E, R_cap, K, N, epilogue, _ptr(C), _ptr(H1_save), _ptr(ws),
+                                     ws.numel(), _stream(dev)),
+           "gg_grouped_fwd_gather")
+    return C
+
+
+def grouped_dgrad_gather(src, slot_of_row, k: int, B, offsets, epilogue: int = GG_EPI_NONE,
+                         H1=None, prob_of_row=None, ws=None, dA=None):
+    """gg_grouped_dgrad_gather: dC rows gathered from token-major src [T, N]."""
+    T, N = src.shape
+    E, Nb, K = B.shape
+    if Nb != N:
+        raise ValueError("src and B disagree on N")
+    R_cap = slot_of_row.shape[0]
+    dev = src.device
+    ncols = 2 * K if epilogue == GG_EPI_SWIGLU_BWD else K
+    dA = torch.empty((R_cap, ncols), dtype=torch.bfloat16, device=dev) if dA is None else dA
+    ws = workspace(0, 1, E, dev) if ws is None else ws
+    _check(LIB.gg_grouped_dgrad_gather(_ptr(src), T, _ptr(slot_of_row), k, _ptr(B), _ptr(offsets),
+                                       E, R_cap, K, N, epilogue, _ptr(H1), _ptr(prob_of_row),
+                                       _ptr(dA), _ptr(ws), ws.numel(), _stream(dev)),
+           "gg_grouped_dgrad_gather")
+    return dA
 
 
 def swiglu(H1, offsets, E: int, A=None):
@@ -243,7 +284,7 @@ class MoeLayer:
     """
 
     _SHAPES = {
-        "Xp": ("rc", "H"), "Yp": ("rc", "H"), "dYp": ("rc", "H"), "dXp": ("rc", "H"),
+        "Yp": ("rc", "H"), "dXp": ("rc", "H"),
         "H1": ("rc", "2F"), "dH": ("rc", "2F"), "A": ("rc", "F"), "offsets": ("E1",),
         "row_of_slot": ("Tk",), "slot_of_row": ("rc",), "prob_of_row": ("rc",), "ws": ("ws",),
     }

@@ -270,3 +270,48 @@ def test_bounded_wait_times_out_and_context_survives(gg):
     # the context is still usable afterwards
     gg.clear_status(ws)
     test_grouped_fwd_plain(gg, 64, 256)
+
+
+@pytest.mark.parametrize("P,T,E,k,H,F", [(1, 300, 8, 2, 256, 320), (16, 257, 6, 3, 320, 384),
+                                         (256, 700, 5, 2, 192, 256)])
+def test_gathered_gemms_equal_materialised_path(gg, P, T, E, k, H, F):
+    # FC1 on the gathered x rows == FC1 on gg_permute's Xp; dgrad FC2 on the
+    # gathered dOut rows == dgrad FC2 on gg_permute_rows' dYp: bit for bit,
+    # including zero padding rows and the rows of empty experts.
+    idx, prob = _permute_case(T, E, k, 17 + P)
+    idx[idx == 1] = 0  # expert 1 gets no tokens
+    rng = np.random.default_rng(P + T)
+    x = bits_to_torch(normal_bf16(rng, (T, H), 1.0))
+    dO = bits_to_torch(normal_bf16(rng, (T, H), 1.0))
+    W1 = bits_to_torch(normal_bf16(rng, (E, 2 * F, H), 0.05))
+    W2 = bits_to_torch(normal_bf16(rng, (E, H, F), 0.05))
+    p = gg.permute(x, torch.from_numpy(idx).cuda(), torch.from_numpy(prob).cuda(), E, P)
+    R_cap = p["Xp"].shape[0]
+    n = int(p["offsets"][-1].item())
+    ws = p["ws"]
+    for epi in (gg.GG_EPI_SWIGLU, gg.GG_EPI_NONE):
+        H1a = _nan_filled((R_cap, 2 * F)) if epi == gg.GG_EPI_SWIGLU else None
+        H1b = _nan_filled((R_cap, 2 * F)) if epi == gg.GG_EPI_SWIGLU else None
+        ncols = F if epi == gg.GG_EPI_SWIGLU else 2 * F
+        Ca, Cb = _nan_filled((R_cap, ncols)), _nan_filled((R_cap, ncols))
+        gg.grouped_fwd(p["Xp"], W1, p["offsets"], epi, ws=ws, C=Ca, H1_save=H1a)
+        gg.grouped_fwd_gather(x, p["slot_of_row"], k, W1, p["offsets"], epi, ws=ws, C=Cb,
+                              H1_save=H1b)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(torch_to_bits(Ca), torch_to_bits(Cb))
+        if H1a is not None:
+            np.testing.assert_array_equal(torch_to_bits(H1a), torch_to_bits(H1b))
+    H1 = bits_to_torch(normal_bf16(rng, (R_cap, 2 * F), 1.0))
+    dYp = gg.permute_rows(dO, p["slot_of_row"], p["offsets"], k, E, R_cap, ws)
+    for epi in (gg.GG_EPI_SWIGLU_BWD, gg.GG_EPI_NONE):
+        # dgrad through W2 [E][H][F]: [R][2F] with the SwiGLU backward, else [R][F]
+        ncols = 2 * F if epi == gg.GG_EPI_SWIGLU_BWD else F
+        da, db = _nan_filled((R_cap, ncols)), _nan_filled((R_cap, ncols))
+        h1 = H1 if epi == gg.GG_EPI_SWIGLU_BWD else None
+        gg.grouped_dgrad(dYp, W2, p["offsets"], epi, H1=h1, prob_of_row=p["prob_of_row"], ws=ws,
+                         dA=da)
+        gg.grouped_dgrad_gather(dO, p["slot_of_row"], k, W2, p["offsets"], epi, H1=h1,
+                                prob_of_row=p["prob_of_row"], ws=ws, dA=db)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(torch_to_bits(da[:n]), torch_to_bits(db[:n]))
+    assert gg.read_status(ws) == 0
