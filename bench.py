@@ -188,16 +188,15 @@ def run_gg(args, shape, peaks):
     prob = torch.from_numpy(inp.prob).to(dev)
     T, H, F, k, E, P = shape.T, shape.H, shape.F, shape.k, shape.E, shape.P
     layer = gg.MoeLayer(T, H, F, k, E, P, device=dev)
-    b = {n: layer.view(n) for n in ("H1", "A", "Yp", "dH", "dXp", "offsets", "row_of_slot",
-                                    "slot_of_row", "prob_of_row", "ws")}
-    b["Xp"] = None  # row maps only: the GEMMs gather the token rows themselves
+    b = {n: layer.view(n) for n in ("Xp", "H1", "A", "Yp", "dYp", "dH", "dXp", "offsets",
+                                    "row_of_slot", "slot_of_row", "prob_of_row", "ws")}
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     dX = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     ws = b["ws"]
     rc = layer.R_cap
     stream = torch.cuda.current_stream(dev)
-    ops = ["permute", "fc1_swiglu", "fc2", "combine", "dgrad_fc2_swiglu_bwd", "dgrad_fc1",
-           "combine_dx"]
+    ops = ["permute", "fc1_swiglu", "fc2", "combine", "permute_dout", "dgrad_fc2_swiglu_bwd",
+           "dgrad_fc1", "combine_dx"]
 
     def step(events=None):
         # the same calls, in the same order, as gg_moe_mlp_fwd + gg_moe_mlp_bwd
@@ -208,20 +207,22 @@ def run_gg(args, shape, peaks):
         mark(0)
         gg.permute(x, idx, prob, E, P, ws=ws, out=b)
         mark(1)
-        gg.grouped_fwd_gather(x, b["slot_of_row"], k, W1, b["offsets"], gg.GG_EPI_SWIGLU, ws=ws,
-                              C=b["A"], H1_save=b["H1"])
+        gg.grouped_fwd(b["Xp"], W1, b["offsets"], gg.GG_EPI_SWIGLU, ws=ws, C=b["A"],
+                       H1_save=b["H1"])
         mark(2)
         gg.grouped_fwd(b["A"], W2, b["offsets"], gg.GG_EPI_NONE, ws=ws, C=b["Yp"])
         mark(3)
         gg.unpermute_combine(b["Yp"], b["row_of_slot"], prob, T, k, ws, out=out)
         mark(4)
-        gg.grouped_dgrad_gather(dOut, b["slot_of_row"], k, W2, b["offsets"], gg.GG_EPI_SWIGLU_BWD,
-                                H1=b["H1"], prob_of_row=b["prob_of_row"], ws=ws, dA=b["dH"])
+        gg.permute_rows(dOut, b["slot_of_row"], b["offsets"], k, E, rc, ws, dst=b["dYp"])
         mark(5)
-        gg.grouped_dgrad(b["dH"], W1, b["offsets"], gg.GG_EPI_NONE, ws=ws, dA=b["dXp"])
+        gg.grouped_dgrad(b["dYp"], W2, b["offsets"], gg.GG_EPI_SWIGLU_BWD, H1=b["H1"],
+                         prob_of_row=b["prob_of_row"], ws=ws, dA=b["dH"])
         mark(6)
-        gg.unpermute_combine(b["dXp"], b["row_of_slot"], None, T, k, ws, out=dX)
+        gg.grouped_dgrad(b["dH"], W1, b["offsets"], gg.GG_EPI_NONE, ws=ws, dA=b["dXp"])
         mark(7)
+        gg.unpermute_combine(b["dXp"], b["row_of_slot"], None, T, k, ws, out=dX)
+        mark(8)
 
     for _ in range(args.warmup):
         step()
@@ -308,7 +309,8 @@ def run_gg(args, shape, peaks):
     def hbm_bytes(op):
         # algorithmic bytes: permute reads idx/prob and writes the row maps;
         # the combines read k rows per token (+ row map, prob) and write one
-        return {"permute": 8 * R + 4 * R + 8 * rc + 4 * (E + 1),
+        return {"permute": (T + R) * H * 2 + 8 * R + 4 * R + 8 * rc,
+                "permute_dout": (T + R) * H * 2 + 4 * rc,
                 "combine": (R + T) * H * 2 + 8 * R,
                 "combine_dx": (R + T) * H * 2 + 4 * R}[op]
 
@@ -330,7 +332,7 @@ def run_gg(args, shape, peaks):
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
                 "peak_source": f"{peaks['source']} hbm copy"}
-    hbm_ops = {op: hbm_bytes(op) for op in ("permute", "combine", "combine_dx")}
+    hbm_ops = {op: hbm_bytes(op) for op in ("permute", "permute_dout", "combine", "combine_dx")}
     kernels = {}
     for op in ops:
         entry = {"ms": round(avg[op], 4), "share": round(avg[op] / total_ms, 4)}

@@ -259,7 +259,10 @@ gg_status gg_grouped_dgrad(const gg_bf16* dC, const gg_bf16* B, const int32_t* o
  * as in gg_grouped_fwd / gg_grouped_dgrad, and the results are bitwise equal
  * to running them on the gathered buffer (gg_permute's Xp, or
  * gg_permute_rows' output). The tensor core's A tiles are loaded by TMA
- * four-row gathers, so the permuted copy never touches HBM.
+ * four-row gathers, so the permuted copy never exists: this saves its
+ * R_cap x K x 2 bytes of memory, at a throughput cost (each A row is gathered
+ * once per 256-column block, and many small TMA requests run well below the
+ * tile-load rate), so the whole-layer calls use the materialised path.
  * ------------------------------------------------------------------------- */
 gg_status gg_grouped_fwd_gather(const gg_bf16* src, int T, const int32_t* slot_of_row, int k,
                                 const gg_bf16* B, const int32_t* offsets,
@@ -292,9 +295,11 @@ gg_status gg_unpermute_combine(const gg_bf16* Yp, const int32_t* row_of_slot,
  * intermediate; gg_moe_buffers_bind() carves it (256-byte aligned pieces).
  * ------------------------------------------------------------------------- */
 typedef struct gg_moe_buffers {
+  gg_bf16* Xp;          /* [R_cap][H]  permuted input                     */
   gg_bf16* H1;          /* [R_cap][2F] FC1 output (BF16), kept for dgrad  */
   gg_bf16* A;           /* [R_cap][F]  SwiGLU output                      */
   gg_bf16* Yp;          /* [R_cap][H]  FC2 output                         */
+  gg_bf16* dYp;         /* [R_cap][H]  permuted output gradient           */
   gg_bf16* dH;          /* [R_cap][2F] gradient w.r.t. FC1 output         */
   gg_bf16* dXp;         /* [R_cap][H]  gradient w.r.t. permuted input     */
   int32_t* offsets;     /* [E+1]                                          */
@@ -313,17 +318,17 @@ size_t gg_moe_buffers_size(int T, int H, int F, int k, int E, int pad_multiple);
 gg_status gg_moe_buffers_bind(void* base, size_t bytes, int T, int H, int F, int k,
                               int E, int pad_multiple, gg_moe_buffers* out);
 
-/* Forward: permute (row maps only) -> grouped FC1 on the gathered token rows
- * + fused SwiGLU (H1 kept) -> grouped FC2 -> probability-weighted combine
- * into out[T][H]. All on `stream`, no host synchronisation. */
+/* Forward: permute -> grouped FC1 + fused SwiGLU (H1 kept) -> grouped FC2
+ * -> probability-weighted combine into out[T][H]. All on `stream`, no host
+ * synchronisation. */
 gg_status gg_moe_mlp_fwd(const gg_bf16* x, const int32_t* idx, const float* prob,
                          const gg_bf16* W1, const gg_bf16* W2,
                          int T, int H, int F, int k, int E, int pad_multiple,
                          gg_bf16* out, const gg_moe_buffers* buf, gg_stream_t stream);
 
 /* Input gradient of gg_moe_mlp_fwd (same buffers, after the forward):
- * dgrad FC2 on the gathered dOut rows with probability scale and fused
- * SwiGLU backward -> dgrad FC1 -> unweighted combine into dX[T][H]. */
+ * permute dOut -> dgrad FC2 with probability scale and fused SwiGLU
+ * backward -> dgrad FC1 -> unweighted combine into dX[T][H]. */
 gg_status gg_moe_mlp_bwd(const gg_bf16* dOut, const gg_bf16* W1, const gg_bf16* W2,
                          int T, int H, int F, int k, int E, int pad_multiple,
                          gg_bf16* dX, const gg_moe_buffers* buf, gg_stream_t stream);

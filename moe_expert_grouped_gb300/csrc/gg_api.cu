@@ -374,7 +374,7 @@ size_t gg_moe_buffers_size(int T, int H, int F, int k, int E, int pad_multiple) 
   const size_t R_cap = static_cast<size_t>(r_cap_of(T, k, E, pad_multiple));
   const size_t b2 = sizeof(gg_bf16);
   size_t n = 0;
-  n += align256(R_cap * H * b2) * 2;         // Yp, dXp
+  n += align256(R_cap * H * b2) * 4;         // Xp, Yp, dYp, dXp
   n += align256(R_cap * 2 * F * b2) * 2;     // H1, dH
   n += align256(R_cap * F * b2);             // A
   n += align256(sizeof(int32_t) * (E + 1));  // offsets
@@ -401,7 +401,9 @@ gg_status gg_moe_buffers_bind(void* base, size_t bytes, int T, int H, int F, int
   };
   const size_t b2 = sizeof(gg_bf16);
   std::memset(out, 0, sizeof(*out));
+  out->Xp = reinterpret_cast<gg_bf16*>(take(R_cap * H * b2));
   out->Yp = reinterpret_cast<gg_bf16*>(take(R_cap * H * b2));
+  out->dYp = reinterpret_cast<gg_bf16*>(take(R_cap * H * b2));
   out->dXp = reinterpret_cast<gg_bf16*>(take(R_cap * H * b2));
   out->H1 = reinterpret_cast<gg_bf16*>(take(R_cap * 2 * F * b2));
   out->dH = reinterpret_cast<gg_bf16*>(take(R_cap * 2 * F * b2));
@@ -418,8 +420,8 @@ gg_status gg_moe_buffers_bind(void* base, size_t bytes, int T, int H, int F, int
 
 static gg_status check_buffers(const gg_moe_buffers* b, int T, int k, int E) {
   if (b == nullptr) return GG_ERR_INVALID_ARG;
-  if (b->H1 == nullptr || b->A == nullptr || b->Yp == nullptr || b->dH == nullptr ||
-      b->dXp == nullptr || b->offsets == nullptr ||
+  if (b->Xp == nullptr || b->H1 == nullptr || b->A == nullptr || b->Yp == nullptr ||
+      b->dYp == nullptr || b->dH == nullptr || b->dXp == nullptr || b->offsets == nullptr ||
       b->row_of_slot == nullptr || b->slot_of_row == nullptr || b->prob_of_row == nullptr)
     return GG_ERR_INVALID_ARG;
   return check_ws(b->ws, b->ws_bytes, gg_workspace_size(T, k, E));
@@ -439,13 +441,15 @@ gg_status gg_moe_mlp_fwd(const gg_bf16* x, const int32_t* idx, const float* prob
   if (rc > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
   const int R_cap = static_cast<int>(rc);
   if (T > 0 && x == nullptr) return GG_ERR_INVALID_ARG;
-  // Row maps only: FC1 gathers the token rows itself, so the permuted copy
-  // of x is never written.
-  s = gg_permute(x, idx, prob, T, H, k, E, pad_multiple, nullptr, buf->offsets, buf->row_of_slot,
+  // The permuted copy of x is written once by a bandwidth-bound gather and
+  // read by FC1's tile loads: on GB300 this is several times cheaper than
+  // four-row TMA gathers inside FC1 (gg_grouped_fwd_gather), which re-gather
+  // every A row once per column block.
+  s = gg_permute(x, idx, prob, T, H, k, E, pad_multiple, buf->Xp, buf->offsets, buf->row_of_slot,
                  buf->slot_of_row, buf->prob_of_row, buf->ws, buf->ws_bytes, stream);
   if (s != GG_OK || T == 0) return s;
-  s = gg_grouped_fwd_gather(x, T, buf->slot_of_row, k, W1, buf->offsets, E, R_cap, H, 2 * F,
-                            GG_EPI_SWIGLU, buf->A, buf->H1, buf->ws, buf->ws_bytes, stream);
+  s = gg_grouped_fwd(buf->Xp, W1, buf->offsets, E, R_cap, H, 2 * F, GG_EPI_SWIGLU, buf->A,
+                     buf->H1, buf->ws, buf->ws_bytes, stream);
   if (s != GG_OK) return s;
   s = gg_grouped_fwd(buf->A, W2, buf->offsets, E, R_cap, F, H, GG_EPI_NONE, buf->Yp, nullptr,
                      buf->ws, buf->ws_bytes, stream);
@@ -468,11 +472,12 @@ gg_status gg_moe_mlp_bwd(const gg_bf16* dOut, const gg_bf16* W1, const gg_bf16* 
   const long long rc = r_cap_of(T, k, E, pad_multiple);
   if (rc > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
   const int R_cap = static_cast<int>(rc);
-  // dH = SwiGLU'(H1) applied to prob_of_row * (dYp @ W2_e), W2 being [E][H][F];
-  // dYp (dOut routed to the permuted rows) is gathered inside the GEMM.
-  s = gg_grouped_dgrad_gather(dOut, T, buf->slot_of_row, k, W2, buf->offsets, E, R_cap, F, H,
-                              GG_EPI_SWIGLU_BWD, buf->H1, buf->prob_of_row, buf->dH, buf->ws,
-                              buf->ws_bytes, stream);
+  s = gg_permute_rows(dOut, buf->slot_of_row, buf->offsets, T, H, k, E, R_cap, buf->dYp, buf->ws,
+                      buf->ws_bytes, stream);
+  if (s != GG_OK) return s;
+  // dH = SwiGLU'(H1) applied to prob_of_row * (dYp @ W2_e), W2 being [E][H][F]
+  s = gg_grouped_dgrad(buf->dYp, W2, buf->offsets, E, R_cap, F, H, GG_EPI_SWIGLU_BWD, buf->H1,
+                       buf->prob_of_row, buf->dH, buf->ws, buf->ws_bytes, stream);
   if (s != GG_OK) return s;
   // dXp = dH @ W1_e; W1 is [E][2F][H]
   s = gg_grouped_dgrad(buf->dH, W1, buf->offsets, E, R_cap, H, 2 * F, GG_EPI_NONE, nullptr,

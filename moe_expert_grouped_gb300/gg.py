@@ -58,8 +58,8 @@ class GGBuffers(ctypes.Structure):
     """Mirror of struct gg_moe_buffers."""
 
     _fields_ = [(n, ctypes.c_void_p) for n in (
-        "H1", "A", "Yp", "dH", "dXp", "offsets", "row_of_slot", "slot_of_row", "prob_of_row",
-        "ws")] + [("ws_bytes", ctypes.c_size_t)]
+        "Xp", "H1", "A", "Yp", "dYp", "dH", "dXp", "offsets", "row_of_slot", "slot_of_row",
+        "prob_of_row", "ws")] + [("ws_bytes", ctypes.c_size_t)]
 
 
 class GGError(RuntimeError):
@@ -284,7 +284,7 @@ class MoeLayer:
     """
 
     _SHAPES = {
-        "Yp": ("rc", "H"), "dXp": ("rc", "H"),
+        "Xp": ("rc", "H"), "Yp": ("rc", "H"), "dYp": ("rc", "H"), "dXp": ("rc", "H"),
         "H1": ("rc", "2F"), "dH": ("rc", "2F"), "A": ("rc", "F"), "offsets": ("E1",),
         "row_of_slot": ("Tk",), "slot_of_row": ("rc",), "prob_of_row": ("rc",), "ws": ("ws",),
     }

@@ -70,7 +70,7 @@ def test_buffers_bind_carves_disjoint_aligned_pieces(gg):
     assert gg.LIB.gg_moe_buffers_bind(ctypes.c_void_p(base), n, T, H, F, k, E, P,
                                       ctypes.byref(buf)) == 0
     rc = T * k + E * (P - 1)
-    sizes = {"Yp": rc * H * 2, "dXp": rc * H * 2,
+    sizes = {"Xp": rc * H * 2, "Yp": rc * H * 2, "dYp": rc * H * 2, "dXp": rc * H * 2,
              "H1": rc * 2 * F * 2, "dH": rc * 2 * F * 2, "A": rc * F * 2, "offsets": 4 * (E + 1),
              "row_of_slot": 4 * T * k, "slot_of_row": 4 * rc, "prob_of_row": 4 * rc,
              "ws": buf.ws_bytes}
