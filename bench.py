@@ -48,6 +48,46 @@ def load_peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+# ------------------------------------------------------------------ captured DRAM traffic
+
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_dram_traffic_balanced_e128_t16384.md")
+GEMM_SOURCES = [os.path.join(ROOT, "moe_expert_grouped_gb300", "csrc", f)
+                for f in ("gg_gemm.cu", "gg_ptx.cuh", "gg_internal.h")]
+
+
+def gemm_sources_sha256() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def captured_traffic(op: str, workload: str):
+    """DRAM bytes (read + write) per launch of `op` from the committed ncu
+    summary, or None when there is none for this workload or the GEMM sources
+    changed since it was captured."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    fields = {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            line = line.strip().lstrip("-").strip()
+            if ":" in line:
+                key, _, val = line.partition(":")
+                fields[key.strip().strip("`")] = val.strip().strip("`")
+    if fields.get("sources_sha256") != gemm_sources_sha256():
+        return None
+    if fields.get("workload") != workload:
+        return None
+    try:
+        return int(fields[f"{op}_dram_bytes"])
+    except (KeyError, ValueError):
+        return None
+
+
 # ------------------------------------------------------------------ multi-rank plumbing
 
 def dist_env():
@@ -324,13 +364,15 @@ def run_gg(args, shape, peaks):
         ach = flop_of[dom] / (avg[dom] / 1e3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 2),
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": None,
+                "frac": round(ach / peaks["bf16_tflops"], 4),
+                "traffic": captured_traffic(dom, shape.name),
                 "peak_source": f"{peaks['source']} bf16 burst"}
     else:
         byts = hbm_bytes(dom)
         ach = byts / (avg[dom] / 1e3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
+                "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+                "traffic": captured_traffic(dom, shape.name),
                 "peak_source": f"{peaks['source']} hbm copy"}
     hbm_ops = {op: hbm_bytes(op) for op in ("permute", "permute_dout", "combine", "combine_dx")}
     kernels = {}
