@@ -254,7 +254,8 @@ def run_gg(args, shape, peaks):
         mark(3)
         gg.unpermute_combine(b["Yp"], b["row_of_slot"], prob, T, k, ws, out=out)
         mark(4)
-        gg.permute_rows(dOut, b["slot_of_row"], b["offsets"], k, E, rc, ws, dst=b["dYp"])
+        gg.permute_rows(dOut, b["row_of_slot"], b["slot_of_row"], b["offsets"], k, E, P, rc, ws,
+                        dst=b["dYp"])
         mark(5)
         gg.grouped_dgrad(b["dYp"], W2, b["offsets"], gg.GG_EPI_SWIGLU_BWD, H1=b["H1"],
                          prob_of_row=b["prob_of_row"], ws=ws, dA=b["dH"])

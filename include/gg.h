@@ -180,16 +180,19 @@ gg_status gg_permute_noalloc(const gg_bf16* x, const int32_t* idx, const float* 
 /* ---------------------------------------------------------------------------
  * gg_permute_rows — gather of a token-major tensor into the permuted row
  * order of an earlier gg_permute (the combine's backward: the output
- * gradient dOut[T][H] is routed to the rows its token was sent to).
- *   dst[row] = src[slot_of_row[row] / k] for rows < offsets[E] with a valid
- *   slot, zero on padding rows; rows >= offsets[E] are left untouched.
- * src[T][H], dst[R_cap][H] BF16. The probability is NOT applied here; the
- * dgrad FC2 epilogue applies it (prob_of_row) because FC2 is linear.
+ * gradient dOut[T][H] is routed to the rows its token was sent to), using
+ * that permute's row maps and padding multiple:
+ *   dst[row_of_slot[t*k+j]] = src[t] for every pair with a row, and (when
+ *   pad_multiple > 1) zero on the padding rows below offsets[E] (slot -1);
+ *   rows >= offsets[E] are left untouched.
+ * src[T][H], dst[R_cap][H] BF16; k <= 32. The probability is NOT applied
+ * here; the dgrad FC2 epilogue applies it (prob_of_row) because FC2 is
+ * linear. A row map entry outside [-1, R_cap) sets GG_ERR_DEVICE_BAD_ROW.
  * ------------------------------------------------------------------------- */
-gg_status gg_permute_rows(const gg_bf16* src, const int32_t* slot_of_row,
-                          const int32_t* offsets, int T, int H, int k, int E,
-                          int R_cap, gg_bf16* dst, void* ws, size_t ws_bytes,
-                          gg_stream_t stream);
+gg_status gg_permute_rows(const gg_bf16* src, const int32_t* row_of_slot,
+                          const int32_t* slot_of_row, const int32_t* offsets,
+                          int T, int H, int k, int E, int pad_multiple, int R_cap,
+                          gg_bf16* dst, void* ws, size_t ws_bytes, gg_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * gg_grouped_fwd — grouped GEMM over all experts in one persistent launch

@@ -158,21 +158,24 @@ gg_status gg_permute(const gg_bf16* x, const int32_t* idx, const float* prob, in
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
-gg_status gg_permute_rows(const gg_bf16* src, const int32_t* slot_of_row, const int32_t* offsets,
-                          int T, int H, int k, int E, int R_cap, gg_bf16* dst, void* ws,
+gg_status gg_permute_rows(const gg_bf16* src, const int32_t* row_of_slot,
+                          const int32_t* slot_of_row, const int32_t* offsets, int T, int H, int k,
+                          int E, int pad_multiple, int R_cap, gg_bf16* dst, void* ws,
                           size_t ws_bytes, gg_stream_t stream) {
-  if (T < 0 || H <= 0 || k <= 0 || E <= 0 || R_cap < 0) return GG_ERR_INVALID_ARG;
+  if (T < 0 || H <= 0 || k <= 0 || k > 32 || E <= 0 || R_cap < 0 || pad_multiple <= 0)
+    return GG_ERR_INVALID_ARG;
   if (E > kMaxExperts || H % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
   if (offsets == nullptr || ws == nullptr) return GG_ERR_INVALID_ARG;
-  if (R_cap > 0 && (src == nullptr || slot_of_row == nullptr || dst == nullptr))
+  if (R_cap > 0 && T > 0 &&
+      (src == nullptr || row_of_slot == nullptr || slot_of_row == nullptr || dst == nullptr))
     return GG_ERR_INVALID_ARG;
   if (!aligned16(src) || !aligned16(dst)) return GG_ERR_MISALIGNED;
   gg_status s = check_ws(ws, ws_bytes, kWsHeader);
   if (s != GG_OK) return s;
   DeviceInfo dev;
   if ((s = device_ok(&dev)) != GG_OK) return s;
-  return from_cuda(launch_gather_rows(src, slot_of_row, offsets, H, k, E, R_cap, T, dst,
-                                      status_ptr(ws), dev.sm_count,
+  return from_cuda(launch_gather_rows(src, row_of_slot, slot_of_row, offsets, H, k, E, R_cap, T,
+                                      pad_multiple > 1, dst, status_ptr(ws), dev.sm_count,
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -472,8 +475,8 @@ gg_status gg_moe_mlp_bwd(const gg_bf16* dOut, const gg_bf16* W1, const gg_bf16* 
   const long long rc = r_cap_of(T, k, E, pad_multiple);
   if (rc > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
   const int R_cap = static_cast<int>(rc);
-  s = gg_permute_rows(dOut, buf->slot_of_row, buf->offsets, T, H, k, E, R_cap, buf->dYp, buf->ws,
-                      buf->ws_bytes, stream);
+  s = gg_permute_rows(dOut, buf->row_of_slot, buf->slot_of_row, buf->offsets, T, H, k, E,
+                      pad_multiple, R_cap, buf->dYp, buf->ws, buf->ws_bytes, stream);
   if (s != GG_OK) return s;
   // dH = SwiGLU'(H1) applied to prob_of_row * (dYp @ W2_e), W2 being [E][H][F]
   s = gg_grouped_dgrad(buf->dYp, W2, buf->offsets, E, R_cap, F, H, GG_EPI_SWIGLU_BWD, buf->H1,

@@ -42,10 +42,12 @@ cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* pr
                            int32_t* status, int32_t* block_hist, int sm_count,
                            cudaStream_t stream);
 
-cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* slot_of_row,
-                               const int32_t* offsets, int H, int k, int E, int R_cap,
-                               long long n_src_rows, gg_bf16* dst, int32_t* status, int sm_count,
-                               cudaStream_t stream);
+// dst[row_of_slot[t*k+j]] = src[t]; with has_padding, rows below offsets[E]
+// whose slot_of_row is -1 are zeroed.
+cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* row_of_slot,
+                               const int32_t* slot_of_row, const int32_t* offsets, int H, int k,
+                               int E, int R_cap, int T, bool has_padding, gg_bf16* dst,
+                               int32_t* status, int sm_count, cudaStream_t stream);
 
 cudaError_t launch_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const float* prob,
                            int T, int k, int H, int R_cap, gg_bf16* out, int32_t* status,

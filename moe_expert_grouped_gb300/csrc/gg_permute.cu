@@ -191,52 +191,75 @@ permute_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict_
   }
 }
 
-// dst[row] = src[slot_of_row[row] / k] (zero where the slot is -1) for rows
-// below offsets[E]; one warp per row, 16-byte vectors, grid-stride.
+// dst[row_of_slot[t*k+j]] = src[t] for every pair (t, j) with a row: one warp
+// per token reads the token's row once and writes its k copies (reading the
+// source in order and writing whole 16-byte-vector rows runs at copy speed;
+// the destination-ordered form re-reads source rows through L2 in random
+// order). Stores are streaming: the permuted buffer is far larger than L2.
 __global__ void __launch_bounds__(256)
-gather_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ slot_of_row,
-                   const int32_t* __restrict__ offsets, int E, int k, int vec_per_row,
-                   long long n_src_rows, uint4* __restrict__ dst, int32_t* status) {
+scatter_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ row_of_slot,
+                    int T, int k, int vec_per_row, int R_cap, uint4* __restrict__ dst,
+                    int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long t = warp0; t < T; t += nwarps) {
+    int my_row = -1;
+    if (lane < k) {
+      my_row = row_of_slot[t * k + lane];
+      if (my_row < -1 || my_row >= R_cap) {
+        set_status(status, GG_ERR_DEVICE_BAD_ROW);
+        my_row = -1;
+      }
+    }
+    const uint4* sp = src + t * vec_per_row;
+    for (int c0 = 0; c0 < vec_per_row; c0 += 256) {
+      uint4 a[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = c0 + lane + 32 * i;
+        a[i] = c < vec_per_row ? __ldg(sp + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int row = __shfl_sync(0xFFFFFFFFu, my_row, j & 31);
+        if (row < 0) continue;
+        uint4* d = dst + static_cast<long long>(row) * vec_per_row;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c = c0 + lane + 32 * i;
+          if (c < vec_per_row) __stcs(d + c, a[i]);
+        }
+      }
+    }
+  }
+}
+
+// Zero the padding rows (slot -1) below offsets[E]: each warp checks 32
+// consecutive rows and clears the padding ones together.
+__global__ void __launch_bounds__(256)
+zero_pad_rows_kernel(const int32_t* __restrict__ slot_of_row, const int32_t* __restrict__ offsets,
+                     int E, int vec_per_row, uint4* __restrict__ dst) {
   const int lane = threadIdx.x & 31;
   const long long n_rows = offsets[E];
   const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-  for (long long r = warp0; r < n_rows; r += nwarps) {
-    const int s = slot_of_row[r];
-    uint4* d = dst + r * vec_per_row;
-    if (s < 0) {
-      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      for (int c = lane; c < vec_per_row; c += 32) d[c] = z;
-      continue;
+  for (long long base = warp0 * 32; base < n_rows; base += nwarps * 32) {
+    const long long r = base + lane;
+    const bool pad = r < n_rows && slot_of_row[r] < 0;
+    uint32_t mask = __ballot_sync(0xFFFFFFFFu, pad);
+    while (mask != 0) {
+      const int b = __ffs(mask) - 1;
+      mask &= mask - 1;
+      uint4* d = dst + (base + b) * vec_per_row;
+      for (int c = lane; c < vec_per_row; c += 32) __stcs(d + c, make_uint4(0u, 0u, 0u, 0u));
     }
-    const long long t = s / k;
-    if (t >= n_src_rows) {
-      if (lane == 0) set_status(status, GG_ERR_DEVICE_BAD_ROW);
-      continue;
-    }
-    const uint4* sp = src + t * vec_per_row;
-    int c = lane;
-    // eight independent 16-byte loads in flight per lane before the stores
-    for (; c + 224 < vec_per_row; c += 256) {
-      uint4 a[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) a[i] = __ldg(sp + c + 32 * i);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) d[c + 32 * i] = a[i];
-    }
-    for (; c + 96 < vec_per_row; c += 128) {
-      uint4 a[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = __ldg(sp + c + 32 * i);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) d[c + 32 * i] = a[i];
-    }
-    for (; c < vec_per_row; c += 32) d[c] = __ldg(sp + c);
   }
 }
 
 // out[t] = bf16(sum_j prob[t][j] * Yp[row_of_slot[t*k+j]]), fp32 in slot
-// order; prob == nullptr gives the plain sum. One warp per token.
+// order; prob == nullptr gives the plain sum. One warp per token; per pass a
+// lane holds two 16-byte column groups of up to 8 slots in flight (16
+// independent streaming loads) before accumulating them in slot order.
 __global__ void __launch_bounds__(256)
 combine_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row_of_slot,
                const float* __restrict__ prob, int T, int k, int vec_per_row, int R_cap,
@@ -256,14 +279,14 @@ combine_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row_of_
       }
     }
     // The column loop is warp-uniform so that the shuffles below see every lane.
-    for (int c0 = 0; c0 < vec_per_row; c0 += 32) {
-      const int c = c0 + lane;
-      const bool col_ok = c < vec_per_row;
-      float acc[8];
+    for (int c0 = 0; c0 < vec_per_row; c0 += 64) {
+      const int ca = c0 + lane, cb = c0 + 32 + lane;
+      const bool oka = ca < vec_per_row, okb = cb < vec_per_row;
+      float acc[2][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      for (int i = 0; i < 8; ++i) acc[0][i] = acc[1][i] = 0.0f;
       for (int j0 = 0; j0 < k; j0 += 8) {
-        uint4 v[8];
+        uint4 va[8], vb[8];
         int rows[8];
         float ps[8];
 #pragma unroll
@@ -271,29 +294,32 @@ combine_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row_of_
           const int j = j0 + jj;
           rows[jj] = __shfl_sync(0xFFFFFFFFu, my_row, j & 31);
           ps[jj] = __shfl_sync(0xFFFFFFFFu, my_p, j & 31);
-          if (j >= k || !col_ok) rows[jj] = -1;
-          v[jj] = rows[jj] >= 0 ? __ldg(Yp + static_cast<long long>(rows[jj]) * vec_per_row + c)
-                                : make_uint4(0u, 0u, 0u, 0u);
+          if (j >= k) rows[jj] = -1;
+          const uint4* rp = Yp + static_cast<long long>(rows[jj]) * vec_per_row;
+          va[jj] = rows[jj] >= 0 && oka ? __ldcs(rp + ca) : make_uint4(0u, 0u, 0u, 0u);
+          vb[jj] = rows[jj] >= 0 && okb ? __ldcs(rp + cb) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
           if (rows[jj] < 0) continue;
-          const uint32_t w[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
+          const uint32_t wa[4] = {va[jj].x, va[jj].y, va[jj].z, va[jj].w};
+          const uint32_t wb[4] = {vb[jj].x, vb[jj].y, vb[jj].z, vb[jj].w};
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            acc[2 * q] = __fmaf_rn(ps[jj], bf16_lo(w[q]), acc[2 * q]);
-            acc[2 * q + 1] = __fmaf_rn(ps[jj], bf16_hi(w[q]), acc[2 * q + 1]);
+            acc[0][2 * q] = __fmaf_rn(ps[jj], bf16_lo(wa[q]), acc[0][2 * q]);
+            acc[0][2 * q + 1] = __fmaf_rn(ps[jj], bf16_hi(wa[q]), acc[0][2 * q + 1]);
+            acc[1][2 * q] = __fmaf_rn(ps[jj], bf16_lo(wb[q]), acc[1][2 * q]);
+            acc[1][2 * q + 1] = __fmaf_rn(ps[jj], bf16_hi(wb[q]), acc[1][2 * q + 1]);
           }
         }
       }
-      if (col_ok) {
-        uint4 o;
-        o.x = pack_bf16x2(acc[0], acc[1]);
-        o.y = pack_bf16x2(acc[2], acc[3]);
-        o.z = pack_bf16x2(acc[4], acc[5]);
-        o.w = pack_bf16x2(acc[6], acc[7]);
-        out[static_cast<long long>(t) * vec_per_row + c] = o;
-      }
+      uint4* op = out + static_cast<long long>(t) * vec_per_row;
+      if (oka)
+        __stcs(op + ca, make_uint4(pack_bf16x2(acc[0][0], acc[0][1]), pack_bf16x2(acc[0][2], acc[0][3]),
+                                   pack_bf16x2(acc[0][4], acc[0][5]), pack_bf16x2(acc[0][6], acc[0][7])));
+      if (okb)
+        __stcs(op + cb, make_uint4(pack_bf16x2(acc[1][0], acc[1][1]), pack_bf16x2(acc[1][2], acc[1][3]),
+                                   pack_bf16x2(acc[1][4], acc[1][5]), pack_bf16x2(acc[1][6], acc[1][7])));
     }
   }
 }
@@ -345,26 +371,33 @@ cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* pr
       idx, prob, R, E, block_hist, offsets, row_of_slot, slot_of_row, prob_of_row);
   count_launch();
   if (Xp != nullptr) {
-    err = launch_gather_rows(x, slot_of_row, offsets, H, k, E, static_cast<int>(R_cap), T, Xp,
-                             status, sm_count, stream);
+    err = launch_gather_rows(x, row_of_slot, slot_of_row, offsets, H, k, E,
+                             static_cast<int>(R_cap), T, P > 1, Xp, status, sm_count, stream);
     if (err != cudaSuccess) return err;
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* slot_of_row,
-                               const int32_t* offsets, int H, int k, int E, int R_cap,
-                               long long n_src_rows, gg_bf16* dst, int32_t* status, int sm_count,
-                               cudaStream_t stream) {
-  if (R_cap <= 0) return cudaSuccess;
+cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* row_of_slot,
+                               const int32_t* slot_of_row, const int32_t* offsets, int H, int k,
+                               int E, int R_cap, int T, bool has_padding, gg_bf16* dst,
+                               int32_t* status, int sm_count, cudaStream_t stream) {
+  if (R_cap <= 0 || T <= 0) return cudaSuccess;
   const int vec = H / 8;
-  long long blocks = (static_cast<long long>(R_cap) + 7) / 8;
+  long long blocks = (static_cast<long long>(T) + 7) / 8;
   const long long cap = static_cast<long long>(sm_count) * 8;
   if (blocks > cap) blocks = cap;
-  gather_rows_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
-      reinterpret_cast<const uint4*>(src), slot_of_row, offsets, E, k, vec, n_src_rows,
+  scatter_rows_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+      reinterpret_cast<const uint4*>(src), row_of_slot, T, k, vec, R_cap,
       reinterpret_cast<uint4*>(dst), status);
   count_launch();
+  if (has_padding) {
+    long long pb = (static_cast<long long>(R_cap) + 255) / 256;
+    if (pb > cap) pb = cap;
+    zero_pad_rows_kernel<<<static_cast<int>(pb), 256, 0, stream>>>(slot_of_row, offsets, E, vec,
+                                                                    reinterpret_cast<uint4*>(dst));
+    count_launch();
+  }
   return cudaGetLastError();
 }
 

@@ -37,7 +37,7 @@ SIGNATURES = [
     ("gg_clear_status", _I, [_P, _P]),
     ("gg_read_status", _I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     ("gg_permute", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P]),
-    ("gg_permute_rows", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
+    ("gg_permute_rows", _I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
     ("gg_grouped_fwd", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
     ("gg_swiglu", _I, [_P, _P, _I, _I, _I, _P, _P]),
     ("gg_grouped_dgrad", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
@@ -169,12 +169,14 @@ def permute(x, idx, prob, E: int, P: int = 1, ws=None, out=None):
     return dict(Xp=Xp, offsets=offsets, row_of_slot=ros, slot_of_row=sor, prob_of_row=por, ws=ws)
 
 
-def permute_rows(src, slot_of_row, offsets, k: int, E: int, R_cap: int, ws, dst=None):
-    """gg_permute_rows: dst[row] = src[slot_of_row[row] // k] (0 on padding)."""
+def permute_rows(src, row_of_slot, slot_of_row, offsets, k: int, E: int, P: int, R_cap: int, ws,
+                 dst=None):
+    """gg_permute_rows: dst[row_of_slot[t*k+j]] = src[t] (0 on padding rows)."""
     T, H = src.shape
     dst = torch.empty((R_cap, H), dtype=torch.bfloat16, device=src.device) if dst is None else dst
-    _check(LIB.gg_permute_rows(_ptr(src), _ptr(slot_of_row), _ptr(offsets), T, H, k, E, R_cap,
-                               _ptr(dst), _ptr(ws), ws.numel(), _stream(src.device)),
+    _check(LIB.gg_permute_rows(_ptr(src), _ptr(row_of_slot), _ptr(slot_of_row), _ptr(offsets), T,
+                               H, k, E, P, R_cap, _ptr(dst), _ptr(ws), ws.numel(),
+                               _stream(src.device)),
            "gg_permute_rows")
     return dst
 

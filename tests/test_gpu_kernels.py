@@ -217,7 +217,8 @@ def test_permute_rows_gathers_token_gradient(gg):
     dO = normal_bf16(np.random.default_rng(5), (T, H), 1.0)
     p = gg.permute(bits_to_torch(x), torch.from_numpy(idx).cuda(), torch.from_numpy(prob).cuda(), E, P)
     R_cap = p["Xp"].shape[0]
-    dYp = gg.permute_rows(bits_to_torch(dO), p["slot_of_row"], p["offsets"], k, E, R_cap, p["ws"])
+    dYp = gg.permute_rows(bits_to_torch(dO), p["row_of_slot"], p["slot_of_row"], p["offsets"], k,
+                          E, P, R_cap, p["ws"])
     torch.cuda.synchronize()
     sor = p["slot_of_row"].cpu().numpy()
     n = int(p["offsets"][-1].item())
@@ -302,7 +303,7 @@ def test_gathered_gemms_equal_materialised_path(gg, P, T, E, k, H, F):
         if H1a is not None:
             np.testing.assert_array_equal(torch_to_bits(H1a), torch_to_bits(H1b))
     H1 = bits_to_torch(normal_bf16(rng, (R_cap, 2 * F), 1.0))
-    dYp = gg.permute_rows(dO, p["slot_of_row"], p["offsets"], k, E, R_cap, ws)
+    dYp = gg.permute_rows(dO, p["row_of_slot"], p["slot_of_row"], p["offsets"], k, E, P, R_cap, ws)
     for epi in (gg.GG_EPI_SWIGLU_BWD, gg.GG_EPI_NONE):
         # dgrad through W2 [E][H][F]: [R][2F] with the SwiGLU backward, else [R][F]
         ncols = 2 * F if epi == gg.GG_EPI_SWIGLU_BWD else F
