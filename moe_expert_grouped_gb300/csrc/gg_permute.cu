@@ -258,8 +258,8 @@ zero_pad_rows_kernel(const int32_t* __restrict__ slot_of_row, const int32_t* __r
 
 // out[t] = bf16(sum_j prob[t][j] * Yp[row_of_slot[t*k+j]]), fp32 in slot
 // order; prob == nullptr gives the plain sum. One warp per token; per pass a
-// lane holds two 16-byte column groups of up to 8 slots in flight (16
-// independent streaming loads) before accumulating them in slot order.
+// lane accumulates two 16-byte column groups over the k slots (streaming
+// loads, unrolled so that several slots' loads are in flight).
 __global__ void __launch_bounds__(256)
 combine_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row_of_slot,
                const float* __restrict__ prob, int T, int k, int vec_per_row, int R_cap,
@@ -285,32 +285,22 @@ combine_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row_of_
       float acc[2][8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[0][i] = acc[1][i] = 0.0f;
-      for (int j0 = 0; j0 < k; j0 += 8) {
-        uint4 va[8], vb[8];
-        int rows[8];
-        float ps[8];
+#pragma unroll 8
+      for (int j = 0; j < k; ++j) {
+        const int row = __shfl_sync(0xFFFFFFFFu, my_row, j & 31);
+        const float pj = __shfl_sync(0xFFFFFFFFu, my_p, j & 31);
+        if (row < 0) continue;  // warp-uniform: every lane holds the same row
+        const uint4* rp = Yp + static_cast<long long>(row) * vec_per_row;
+        const uint4 va = oka ? __ldcs(rp + ca) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 vb = okb ? __ldcs(rp + cb) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
+        const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          const int j = j0 + jj;
-          rows[jj] = __shfl_sync(0xFFFFFFFFu, my_row, j & 31);
-          ps[jj] = __shfl_sync(0xFFFFFFFFu, my_p, j & 31);
-          if (j >= k) rows[jj] = -1;
-          const uint4* rp = Yp + static_cast<long long>(rows[jj]) * vec_per_row;
-          va[jj] = rows[jj] >= 0 && oka ? __ldcs(rp + ca) : make_uint4(0u, 0u, 0u, 0u);
-          vb[jj] = rows[jj] >= 0 && okb ? __ldcs(rp + cb) : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          if (rows[jj] < 0) continue;
-          const uint32_t wa[4] = {va[jj].x, va[jj].y, va[jj].z, va[jj].w};
-          const uint32_t wb[4] = {vb[jj].x, vb[jj].y, vb[jj].z, vb[jj].w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            acc[0][2 * q] = __fmaf_rn(ps[jj], bf16_lo(wa[q]), acc[0][2 * q]);
-            acc[0][2 * q + 1] = __fmaf_rn(ps[jj], bf16_hi(wa[q]), acc[0][2 * q + 1]);
-            acc[1][2 * q] = __fmaf_rn(ps[jj], bf16_lo(wb[q]), acc[1][2 * q]);
-            acc[1][2 * q + 1] = __fmaf_rn(ps[jj], bf16_hi(wb[q]), acc[1][2 * q + 1]);
-          }
+        for (int q = 0; q < 4; ++q) {
+          acc[0][2 * q] = __fmaf_rn(pj, bf16_lo(wa[q]), acc[0][2 * q]);
+          acc[0][2 * q + 1] = __fmaf_rn(pj, bf16_hi(wa[q]), acc[0][2 * q + 1]);
+          acc[1][2 * q] = __fmaf_rn(pj, bf16_lo(wb[q]), acc[1][2 * q]);
+          acc[1][2 * q + 1] = __fmaf_rn(pj, bf16_hi(wb[q]), acc[1][2 * q + 1]);
         }
       }
       uint4* op = out + static_cast<long long>(t) * vec_per_row;
