@@ -289,18 +289,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
       int e, mp, nt;
       decode_tile(tile, st.tiles_before, E, NT, e, mp, nt);
       const int row0 = st.row_start[e] + (mp * kCluster + h) * BM;
-      // L2 prefetch of this cluster's next work item, spread over this one's
-      // k-loop: every cluster of a wave first-touches its experts' data at
-      // the same moment, so a block fetched now is an L2 hit when the next
-      // wave asks for it. Each block is prefetched once: the A rows by the
-      // cluster on column block 0 of that row pair, a weight slice by the
-      // cluster on row pair 0 of that expert (each CTA takes its own half).
-      const int next = tile + n_clusters;
-      int ne = 0, nmp = 0, nnt = 0;
-      if (next < total) decode_tile(next, st.tiles_before, E, NT, ne, nmp, nnt);
-      const bool pf_a = !GATHER && next < total && nnt == 0;
-      const bool pf_b = next < total && nmp == 0;
-      const int nrow0 = next < total ? st.row_start[ne] + (nmp * kCluster + h) * BM : 0;
       int src[4] = {0, 0, 0, 0};
       if (GATHER) {
         const int row_end = st.row_start[e + 1];
@@ -340,20 +328,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             for (int j = 0; j < 2; ++j)
               tma_load_3d_pair(sb + j * (B_HALF_BYTES / 2), &mapB, fb,
                                nt * BN + h * (BN / 2) + 64 * j, kb * BK, e);
-          }
-        }
-        if (lane == 0 && (pf_a || pf_b)) {
-          if (pf_a) tma_prefetch_2d(&mapA, kb * BK, nrow0);
-          if (pf_b) {
-            if (MODE == kFwdPlain) {
-              tma_prefetch_3d(&mapB, kb * BK, nnt * BN + h * (BN / 2), ne);
-            } else if (MODE == kFwdSwiglu) {
-              tma_prefetch_3d(&mapB, kb * BK, h * p.F + nnt * (BN / 2), ne);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 2; ++j)
-                tma_prefetch_3d(&mapB, nnt * BN + h * (BN / 2) + 64 * j, kb * BK, ne);
-            }
           }
         }
         if (GATHER) {
