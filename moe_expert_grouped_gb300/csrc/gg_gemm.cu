@@ -476,29 +476,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         const int c_end = min(c0 + BN / 2, F - n0);  // multiple of 32 (F % 64 == 0)
         const gg_bf16* hrow = p.H1 + grow * (2LL * F) + n0;
         gg_bf16* drow = p.C + grow * (2LL * F) + n0;
-        // H1 comes from DRAM: pull this lane's row of the cluster's next work
-        // item (this warp's column half of g and of u, 4 x 128 bytes) into L2
-        // now, so that its reads a tile from now do not wait on DRAM.
-        {
-          const int next = tile + n_clusters;
-          if (next < total) {
-            int ne, nmp, nnt;
-            decode_tile(next, st.tiles_before, E, NT, ne, nmp, nnt);
-            const long long ng =
-                static_cast<long long>(st.row_start[ne]) + (nmp * kCluster + static_cast<int>(crank)) * BM + r;
-            const int nc0 = nnt * BN + c0;
-            if (ng < st.row_start[ne + 1] && nc0 < F) {
-              const gg_bf16* nh = p.H1 + ng * (2LL * F) + nc0;
-              const bool two = nc0 + 64 < F;
-              prefetch_l2(nh);
-              prefetch_l2(nh + F);
-              if (two) {
-                prefetch_l2(nh + 64);
-                prefetch_l2(nh + F + 64);
-              }
-            }
-          }
-        }
         // The saved H1 does not depend on the accumulator: fetch the first
         // chunk before waiting for the MMAs, then always one chunk ahead.
         uint4 graw[4], uraw[4];
