@@ -476,34 +476,26 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         const int c_end = min(c0 + BN / 2, F - n0);  // multiple of 32 (F % 64 == 0)
         const gg_bf16* hrow = p.H1 + grow * (2LL * F) + n0;
         gg_bf16* drow = p.C + grow * (2LL * F) + n0;
-        // The saved H1 does not depend on the accumulator: fetch the first two
-        // chunks before waiting for the MMAs, then keep two chunks in flight.
-        const int nch = (c_end - c0) / 32;  // 0..4 chunks of 32 columns
-        uint4 gr[2][4], ur[2][4];
-        if (nch > 0) {
-          load_chunk_raw(gr[0], hrow + c0, valid);
-          load_chunk_raw(ur[0], hrow + F + c0, valid);
-        }
-        if (nch > 1) {
-          load_chunk_raw(gr[1], hrow + c0 + 32, valid);
-          load_chunk_raw(ur[1], hrow + F + c0 + 32, valid);
+        // The saved H1 does not depend on the accumulator: fetch the first
+        // chunk before waiting for the MMAs, then always one chunk ahead.
+        uint4 graw[4], uraw[4];
+        if (c0 < c_end) {
+          load_chunk_raw(graw, hrow + c0, valid);
+          load_chunk_raw(uraw, hrow + F + c0, valid);
         }
         if (!mbar_wait_bounded(smem_u32(&st.tfull[acc]), acc_phase, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-#pragma unroll
-        for (int ci = 0; ci < BN / 2 / 32; ++ci) {
-          if (ci >= nch) break;
-          const int c = c0 + 32 * ci;
-          const int slot = ci & 1;
+#pragma unroll 1
+        for (int c = c0; c < c_end; c += 32) {
           float v[32];
           tmem_ld32(tbase + c, v);
           uint4 gw[4], uw[4];
-          transpose_chunk(stg, gr[slot], gw);
-          transpose_chunk(stg, ur[slot], uw);
-          if (ci + 2 < nch) {
-            load_chunk_raw(gr[slot], hrow + c + 64, valid);
-            load_chunk_raw(ur[slot], hrow + F + c + 64, valid);
+          transpose_chunk(stg, graw, gw);
+          transpose_chunk(stg, uraw, uw);
+          if (c + 32 < c_end) {
+            load_chunk_raw(graw, hrow + c + 32, valid);
+            load_chunk_raw(uraw, hrow + F + c + 32, valid);
           }
           uint32_t gs[16], us[16];
 #pragma unroll
@@ -513,15 +505,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             us[4 * i + 0] = uw[i].x; us[4 * i + 1] = uw[i].y;
             us[4 * i + 2] = uw[i].z; us[4 * i + 3] = uw[i].w;
           }
-          float du[32];
+          float dg[32], du[32];
 #pragma unroll
-          for (int h = 0; h < 16; ++h) {  // dg overwrites v in place
-            silu_mul_bwd(v[2 * h] * scale, bf16_lo(gs[h]), bf16_lo(us[h]), v[2 * h], du[2 * h]);
-            silu_mul_bwd(v[2 * h + 1] * scale, bf16_hi(gs[h]), bf16_hi(us[h]), v[2 * h + 1],
+          for (int h = 0; h < 16; ++h) {
+            silu_mul_bwd(v[2 * h] * scale, bf16_lo(gs[h]), bf16_lo(us[h]), dg[2 * h], du[2 * h]);
+            silu_mul_bwd(v[2 * h + 1] * scale, bf16_hi(gs[h]), bf16_hi(us[h]), dg[2 * h + 1],
                          du[2 * h + 1]);
           }
           uint4 w[4];
-          pack_bf16x32(v, 1.0f, w);
+          pack_bf16x32(dg, 1.0f, w);
           store_chunk(stg, w, drow + c, valid);
           pack_bf16x32(du, 1.0f, w);
           store_chunk(stg, w, drow + F + c, valid);
