@@ -300,13 +300,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         }
       }
       if (!GATHER && lane != 0) continue;
-      // K blocks in rotated order, starting at a point set by the column
-      // block (see the MMA loop), so that clusters sharing the same A rows do
-      // not request the same blocks at the same time.
-      const int k_start = (nt * KB) / NT;
-      for (int kq = 0; kq < KB; ++kq) {
-        int kb = kq + k_start;
-        if (kb >= KB) kb -= KB;
+      for (int kb = 0; kb < KB; ++kb) {
         int free_ok = 1;
         if (lane == 0)
           free_ok = mbar_wait_bounded(smem_u32(&st.empty[stage]), phase ^ 1u, abort_flag, p.status)
@@ -375,10 +369,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        // Stages arrive in the producer's rotated K order; the order depends
-        // only on the column block, never on a row's position, so every row
-        // is summed in the same order in every batch (batch invariance).
-        for (int kq = 0; kq < KB; ++kq) {
+        for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&st.full[stage]), phase, abort_flag, p.status)) {
             ok = false;
             break;
@@ -391,7 +382,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             const uint64_t adesc = make_sdesc(sa + kk * 32, 16, 1024);
             const uint64_t bdesc = kMN ? make_sdesc(sb + kk * 2048, B_HALF_BYTES / 2, 1024)
                                        : make_sdesc(sb + kk * 32, 16, 1024);
-            tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kq | kk) != 0 ? 1u : 0u);
+            tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           // the stage is free in both CTAs once these MMAs have read it
           tc_commit_pair_mc(smem_u32(&st.empty[stage]), kClusterMask);
