@@ -306,35 +306,64 @@ def run_gg(args, shape, peaks):
     _, tot_tokens = aggregate(local_s, float(T * args.steps), dev if world > 1 else None)
 
     # ---- end to end through the public API with host buffers (pinned)
+    # Every step copies its inputs host->device and its results device->host
+    # inside the timed region. The copies run on two copy streams with two
+    # device buffer sets, so step s+1's inputs arrive and step s-1's results
+    # leave while step s computes (a streaming caller's pipeline).
     h_x = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).pin_memory()
     h_dO = torch.from_numpy(inp.dOut.view(np.int16)).view(torch.bfloat16).pin_memory()
     h_idx = torch.from_numpy(inp.idx).pin_memory()
     h_prob = torch.from_numpy(inp.prob).pin_memory()
-    h_out = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    h_dX = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    d_x, d_dO = torch.empty_like(x), torch.empty_like(dOut)
-    d_idx, d_prob = torch.empty_like(idx), torch.empty_like(prob)
+    h_out = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    h_dX = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    d_in = [(torch.empty_like(x), torch.empty_like(idx), torch.empty_like(prob),
+             torch.empty_like(dOut)) for _ in range(2)]
+    d_res = [(torch.empty_like(out), torch.empty_like(dX)) for _ in range(2)]
+    s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of set i landed
+    ev_used = [torch.cuda.Event() for _ in range(2)]   # compute done with set i
+    ev_out = [torch.cuda.Event() for _ in range(2)]    # results of set i copied out
 
-    def e2e_step():
-        d_x.copy_(h_x, non_blocking=True)
-        d_idx.copy_(h_idx, non_blocking=True)
-        d_prob.copy_(h_prob, non_blocking=True)
-        d_dO.copy_(h_dO, non_blocking=True)
-        layer.forward(d_x, d_idx, d_prob, W1, W2, out=out)
-        layer.backward(d_dO, W1, W2, dX=dX)
-        h_out.copy_(out, non_blocking=True)
-        h_dX.copy_(dX, non_blocking=True)
+    def e2e_run(n_steps):
+        for i in range(2):
+            ev_used[i].record(stream)
+            ev_out[i].record(stream)
+        for s in range(n_steps):
+            i = s & 1
+            dx_, didx_, dprob_, ddO_ = d_in[i]
+            with torch.cuda.stream(s_h2d):
+                s_h2d.wait_event(ev_used[i])
+                dx_.copy_(h_x, non_blocking=True)
+                didx_.copy_(h_idx, non_blocking=True)
+                dprob_.copy_(h_prob, non_blocking=True)
+                ddO_.copy_(h_dO, non_blocking=True)
+                ev_in[i].record(s_h2d)
+            o_, dX_ = d_res[i]
+            stream.wait_event(ev_in[i])
+            stream.wait_event(ev_out[i])
+            layer.forward(dx_, didx_, dprob_, W1, W2, out=o_)
+            layer.backward(ddO_, W1, W2, dX=dX_)
+            ev_used[i].record(stream)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(ev_used[i])
+                h_out[i].copy_(o_, non_blocking=True)
+                h_dX[i].copy_(dX_, non_blocking=True)
+                ev_out[i].record(s_d2h)
+        for i in range(2):
+            stream.wait_event(ev_out[i])
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+    e2e_run(max(1, args.warmup))
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    e2e_run(args.steps)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_s, _ = aggregate(e0.elapsed_time(e1) / 1e3, 0.0, dev if world > 1 else None)
+    if gg.read_status(layer.view("ws")) != 0:
+        raise RuntimeError("device status after the end-to-end run")
+    if not (torch.equal(h_out[0], out.cpu()) and torch.equal(h_dX[0], dX.cpu())):
+        raise RuntimeError("end-to-end results differ from the device-resident step")
     h2d = x.numel() * 2 + dOut.numel() * 2 + idx.numel() * 4 + prob.numel() * 4
     d2h = out.numel() * 2 + dX.numel() * 2
 
