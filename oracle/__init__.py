@@ -15,8 +15,10 @@ from .moe_oracle import (  # noqa: F401
     swiglu,
     swiglu_backward,
     combine,
+    prob_grad,
     moe_forward,
     moe_backward,
     token_forward,
     token_backward,
+    token_prob_grad,
 )

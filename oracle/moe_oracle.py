@@ -197,6 +197,25 @@ def combine(Yp: np.ndarray, row_of_slot, prob, T: int, k: int) -> np.ndarray:
 
 # ---------------------------------------------------------------- full layer
 
+def prob_grad(dOut: np.ndarray, Yp: np.ndarray, row_of_slot, T: int, k: int) -> np.ndarray:
+    """Gradient of the combine w.r.t. the routing probabilities.
+
+    out_t = sum_j prob[t, j] * Yp[row(t, j)] is linear in each prob[t, j], so
+    dL/dprob[t, j] = <dOut_t, Yp[row(t, j)]> (0 for a slot without a row).
+    The probabilities are taken as given: the router that produced them is
+    outside the layer.
+    """
+    dO = _as_f64(dOut)
+    rows = np.asarray(row_of_slot, dtype=np.int64).reshape(T, k)
+    dp = np.zeros((T, k), dtype=np.float64)
+    for t in range(T):
+        for j in range(k):
+            r = rows[t, j]
+            if r >= 0:
+                dp[t, j] = float(np.dot(dO[t], Yp[r]))
+    return dp
+
+
 def moe_forward(x, idx, prob, W1, W2, E: int, P: int = 1, faithful: bool = False):
     """Forward of the expert layer. Returns a dict of every intermediate.
 
@@ -223,8 +242,9 @@ def moe_backward(dOut, fwd: dict, W1, W2, faithful: bool = False):
     dYp[r] = dOut[t] for the pair (t, j) of row r (0 on padding); the pair's
     probability scales FC2's input gradient: dA = p_r * (dYp @ W2_e);
     dH = SwiGLU'(H1) applied to dA; dXp = dH @ W1_e; dX[t] = sum_j dXp[row(t, j)].
-    With ``faithful`` the values are rounded to BF16 where the GPU path stores
-    BF16 (dH, dXp, dX).
+    Also the routing-probability gradient dprob[t, j] = <dOut_t, Yp[row(t, j)]>
+    (``prob_grad``). With ``faithful`` the values are rounded to BF16 where the
+    GPU path stores BF16 (dH, dXp, dX); dprob is kept in fp32 there.
     """
     rnd = round_to_bf16 if faithful else (lambda v: v)
     dO = _as_f64(dOut)
@@ -238,7 +258,8 @@ def moe_backward(dOut, fwd: dict, W1, W2, faithful: bool = False):
     dH = rnd(swiglu_backward(dA, fwd["H1"]))
     dXp = rnd(grouped_linear_t(dH, W1, offsets))
     dX = rnd(combine(dXp, fwd["row_of_slot"], None, T, k))
-    return dict(dYp=dYp, dH=dH, dXp=dXp, dX=dX)
+    dprob = prob_grad(dO, fwd["Yp"], fwd["row_of_slot"], T, k)
+    return dict(dYp=dYp, dH=dH, dXp=dXp, dX=dX, dprob=dprob)
 
 
 # ---------------------------------------------------------------- one token
@@ -277,3 +298,18 @@ def token_backward(x_t, dout_t, experts, probs, W1, W2) -> np.ndarray:
         dh = np.concatenate([da * u * s * (1.0 + g * (1.0 - s)), da * g * s])
         dx += dh @ w1
     return dx
+
+
+def token_prob_grad(x_t, dout_t, experts, W1, W2) -> np.ndarray:
+    """dL/dprob of one token's k slots: <dOut_t, FC2(SwiGLU(FC1 x_t))> per expert."""
+    xt = _as_f64(x_t).reshape(-1)
+    do = _as_f64(dout_t).reshape(-1)
+    out = []
+    for e in np.asarray(experts).reshape(-1):
+        w1 = _as_f64(W1[int(e)])
+        w2 = _as_f64(W2[int(e)])
+        h = w1 @ xt
+        F = h.size // 2
+        a = h[:F] * _sigmoid(h[:F]) * h[F:]
+        out.append(float(np.dot(do, w2 @ a)))
+    return np.asarray(out)

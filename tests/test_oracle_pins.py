@@ -214,6 +214,9 @@ def test_identity_weights_closed_form():
     dsilu = sig + xv * sig * (1 - sig)
     # d/dx [x * silu(x)] = silu(x) + x * silu'(x)
     np.testing.assert_allclose(bwd["dX"], psum * dv * (xv * sig + xv * dsilu), rtol=1e-12, atol=1e-300)
+    # every routed slot's expert output is x * silu(x): dprob[t, j] = <dOut_t, x_t silu(x_t)>
+    closed = np.sum(dv * xv * (xv * sig), axis=1, keepdims=True) * np.ones_like(bwd["dprob"])
+    np.testing.assert_allclose(bwd["dprob"], closed, rtol=1e-12, atol=1e-300)
 
 
 def test_one_hot_rows_closed_form():
@@ -348,15 +351,19 @@ def test_backward_matches_torch_autograd():
     fwd = oracle.moe_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, shape.E, 2)
     bwd = oracle.moe_backward(inp.dOut, fwd, inp.W1, inp.W2)
     x = torch.from_numpy(_val(inp.x)).requires_grad_(True)
-    out = _torch_forward(x, inp.idx, torch.from_numpy(inp.prob.astype(np.float64)),
-                         torch.from_numpy(_val(inp.W1)), torch.from_numpy(_val(inp.W2)))
+    p = torch.from_numpy(inp.prob.astype(np.float64)).requires_grad_(True)
+    out = _torch_forward(x, inp.idx, p, torch.from_numpy(_val(inp.W1)),
+                         torch.from_numpy(_val(inp.W2)))
     np.testing.assert_allclose(fwd["out"], out.detach().numpy(), rtol=1e-11, atol=1e-14)
     out.backward(torch.from_numpy(_val(inp.dOut)))
     np.testing.assert_allclose(bwd["dX"], x.grad.numpy(), rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(bwd["dprob"], p.grad.numpy(), rtol=1e-10, atol=1e-13)
     # the per-token backward agrees as well
     for t in (0, 5, 23):
         dx = oracle.token_backward(inp.x[t], inp.dOut[t], inp.idx[t], inp.prob[t], inp.W1, inp.W2)
         np.testing.assert_allclose(dx, x.grad.numpy()[t], rtol=1e-10, atol=1e-13)
+        dp = oracle.token_prob_grad(inp.x[t], inp.dOut[t], inp.idx[t], inp.W1, inp.W2)
+        np.testing.assert_allclose(dp, p.grad.numpy()[t], rtol=1e-10, atol=1e-13)
 
 
 def test_backward_matches_finite_differences():
@@ -381,6 +388,19 @@ def test_backward_matches_finite_differences():
             fm = oracle.moe_forward(xm, idx, prob, W1, W2, E, 1)["out"]
             num[t, c] = np.sum(dOut * (fp - fm)) / (2 * eps)
     np.testing.assert_allclose(dX, num, rtol=1e-6, atol=1e-8)
+    # and w.r.t. each routing probability (padding P = 4 leaves it unchanged)
+    fwd4 = oracle.moe_forward(x, idx, prob, W1, W2, E, 4)
+    dprob = oracle.moe_backward(dOut, fwd4, W1, W2)["dprob"]
+    num_p = np.zeros_like(prob)
+    for t in range(T):
+        for j in range(k):
+            pp, pm = prob.copy(), prob.copy()
+            pp[t, j] += eps
+            pm[t, j] -= eps
+            fp = oracle.moe_forward(x, idx, pp, W1, W2, E, 1)["out"]
+            fm = oracle.moe_forward(x, idx, pm, W1, W2, E, 1)["out"]
+            num_p[t, j] = np.sum(dOut * (fp - fm)) / (2 * eps)
+    np.testing.assert_allclose(dprob, num_p, rtol=1e-6, atol=1e-8)
 
 
 def test_swiglu_backward_matches_finite_differences():
