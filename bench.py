@@ -174,7 +174,8 @@ class ClockSampler:
 # ------------------------------------------------------------------ oracle timing
 
 def time_oracle(shape, inp, n_tokens: int, steps: int = 1):
-    """Wall time of the fp64 oracle forward + input gradient on a token sample."""
+    """Wall time of the fp64 oracle forward + input and probability gradients on a
+    token sample."""
     import oracle
 
     sel = np.arange(min(n_tokens, shape.T))
@@ -229,9 +230,10 @@ def run_gg(args, shape, peaks):
     T, H, F, k, E, P = shape.T, shape.H, shape.F, shape.k, shape.E, shape.P
     layer = gg.MoeLayer(T, H, F, k, E, P, device=dev)
     b = {n: layer.view(n) for n in ("Xp", "H1", "A", "Yp", "dYp", "dH", "dXp", "offsets",
-                                    "row_of_slot", "slot_of_row", "prob_of_row", "ws")}
+                                    "row_of_slot", "slot_of_row", "prob_of_row", "rowdot", "ws")}
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     dX = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    dprob = torch.empty((T, k), dtype=torch.float32, device=dev)
     ws = b["ws"]
     rc = layer.R_cap
     stream = torch.cuda.current_stream(dev)
@@ -258,11 +260,12 @@ def run_gg(args, shape, peaks):
                         dst=b["dYp"])
         mark(5)
         gg.grouped_dgrad(b["dYp"], W2, b["offsets"], gg.GG_EPI_SWIGLU_BWD, H1=b["H1"],
-                         prob_of_row=b["prob_of_row"], ws=ws, dA=b["dH"])
+                         prob_of_row=b["prob_of_row"], ws=ws, dA=b["dH"], rowdot=b["rowdot"])
         mark(6)
         gg.grouped_dgrad(b["dH"], W1, b["offsets"], gg.GG_EPI_NONE, ws=ws, dA=b["dXp"])
         mark(7)
-        gg.unpermute_combine(b["dXp"], b["row_of_slot"], None, T, k, ws, out=dX)
+        gg.unpermute_combine(b["dXp"], b["row_of_slot"], None, T, k, ws, out=dX,
+                             rowdot=b["rowdot"], dprob=dprob, n_rowdot=gg.rowdot_blocks(F))
         mark(8)
 
     for _ in range(args.warmup):
@@ -316,9 +319,11 @@ def run_gg(args, shape, peaks):
     h_prob = torch.from_numpy(inp.prob).pin_memory()
     h_out = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     h_dX = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    h_dp = [torch.empty((T, k), dtype=torch.float32).pin_memory() for _ in range(2)]
     d_in = [(torch.empty_like(x), torch.empty_like(idx), torch.empty_like(prob),
              torch.empty_like(dOut)) for _ in range(2)]
-    d_res = [(torch.empty_like(out), torch.empty_like(dX)) for _ in range(2)]
+    d_res = [(torch.empty_like(out), torch.empty_like(dX), torch.empty_like(dprob))
+             for _ in range(2)]
     s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of set i landed
     ev_used = [torch.cuda.Event() for _ in range(2)]   # compute done with set i
@@ -338,16 +343,17 @@ def run_gg(args, shape, peaks):
                 dprob_.copy_(h_prob, non_blocking=True)
                 ddO_.copy_(h_dO, non_blocking=True)
                 ev_in[i].record(s_h2d)
-            o_, dX_ = d_res[i]
+            o_, dX_, dp_ = d_res[i]
             stream.wait_event(ev_in[i])
             stream.wait_event(ev_out[i])
             layer.forward(dx_, didx_, dprob_, W1, W2, out=o_)
-            layer.backward(ddO_, W1, W2, dX=dX_)
+            layer.backward(ddO_, W1, W2, dX=dX_, dprob=dp_)
             ev_used[i].record(stream)
             with torch.cuda.stream(s_d2h):
                 s_d2h.wait_event(ev_used[i])
                 h_out[i].copy_(o_, non_blocking=True)
                 h_dX[i].copy_(dX_, non_blocking=True)
+                h_dp[i].copy_(dp_, non_blocking=True)
                 ev_out[i].record(s_d2h)
         for i in range(2):
             stream.wait_event(ev_out[i])
@@ -362,10 +368,11 @@ def run_gg(args, shape, peaks):
     e2e_s, _ = aggregate(e0.elapsed_time(e1) / 1e3, 0.0, dev if world > 1 else None)
     if gg.read_status(layer.view("ws")) != 0:
         raise RuntimeError("device status after the end-to-end run")
-    if not (torch.equal(h_out[0], out.cpu()) and torch.equal(h_dX[0], dX.cpu())):
+    if not (torch.equal(h_out[0], out.cpu()) and torch.equal(h_dX[0], dX.cpu())
+            and torch.equal(h_dp[0], dprob.cpu())):
         raise RuntimeError("end-to-end results differ from the device-resident step")
     h2d = x.numel() * 2 + dOut.numel() * 2 + idx.numel() * 4 + prob.numel() * 4
-    d2h = out.numel() * 2 + dX.numel() * 2
+    d2h = out.numel() * 2 + dX.numel() * 2 + dprob.numel() * 4
 
     clocks = sampler.stop() if sampler is not None else None
     if rank != 0:
@@ -422,7 +429,8 @@ def run_gg(args, shape, peaks):
         cpu_val = (sub.flop_fwd() + sub.flop_dgrad()) / times[0] / 1e12
         cpu = {"value": cpu_val, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
                "sample": f"{n_tok} of {T} tokens (all k slots), numpy fp64 forward + input "
-                         f"gradient, {times[0]:.2f} s, tokens/s {n_tok / times[0]:.1f}"}
+                         f"and probability gradients, {times[0]:.2f} s, "
+                         f"tokens/s {n_tok / times[0]:.1f}"}
 
     value = tot_flop / tot_s / 1e12
     line = {
@@ -432,6 +440,7 @@ def run_gg(args, shape, peaks):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": shape.name, "E": E, "H": H, "F": F, "T": T, "k": k, "P": P,
                    "routing": shape.routing, "parallelism": f"replicas x{world}",
+                   "outputs": "out, dX, dprob",
                    "l2": "inputs larger than L2 (weights 1.2 GB, activations > 1 GB per step)"},
         "tokens_per_s": round(tot_tokens / tot_s, 1),
         "pct_bf16_peak": {"vs_2250_tflops": round(value / world / 2250.0, 4),
@@ -486,12 +495,12 @@ def run_reference(args, shape):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": shape.name, "E": shape.E, "H": shape.H, "F": shape.F,
                    "T": shape.T, "k": shape.k, "P": shape.P, "routing": shape.routing,
-                   "parallelism": "host cores"},
+                   "parallelism": "host cores", "outputs": "out, dX, dprob"},
         "tokens_per_s": n * args.steps / dt,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(),
                          "kind": "oracle",
                          "sample": f"{n} random tokens of {shape.T} per step (all k slots), "
-                                   "numpy fp64 forward + input gradient"},
+                                   "numpy fp64 forward + input and probability gradients"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

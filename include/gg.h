@@ -244,12 +244,32 @@ gg_status gg_swiglu(const gg_bf16* H1, const int32_t* offsets, int E, int R_cap,
  *                    dA[r][j]     = bf16(acc * u * s * (1 + g * (1 - s)))
  *                    dA[r][F + j] = bf16(acc * g * s)
  *                  so dA is [R_cap][2F] (the gradient w.r.t. FC1's output).
+ *   rowdot (nullable, GG_EPI_SWIGLU_BWD only): partial sums for the routing-
+ *                  probability gradient ([P4] "What does this PR do?": the
+ *                  probability multiplies the expert output at the combine,
+ *                  so its gradient is <dOut_t, Yp[r]> = <dC[r] * W_e, A[r]>
+ *                  for the FC2 weight W_e and SwiGLU output A). With a[r][j]
+ *                  = bf16(silu(g) * u) (the forward's A, same arithmetic) and
+ *                  the accumulator taken BEFORE the prob_of_row scale:
+ *                    rowdot[r][b] = sum_{128b <= j < min(128b + 128, F)} acc[r][j] * a[r][j]
+ *                  in fp32 (any order), for b < gg_rowdot_blocks(K); layout
+ *                  [R_cap][gg_rowdot_stride(K)] fp32 (one 32-byte-aligned
+ *                  group per row; entries b >= gg_rowdot_blocks(K) are not
+ *                  written), 32-byte aligned. The blocks' sum
+ *                  (gg_unpermute_combine's dprob) is the gradient.
  * Rows outside [0, offsets[E]) are never written.
  * ------------------------------------------------------------------------- */
 gg_status gg_grouped_dgrad(const gg_bf16* dC, const gg_bf16* B, const int32_t* offsets,
                            int E, int R_cap, int K, int N, gg_epilogue epi,
                            const gg_bf16* H1, const float* prob_of_row, gg_bf16* dA,
-                           void* ws, size_t ws_bytes, gg_stream_t stream);
+                           float* rowdot, void* ws, size_t ws_bytes, gg_stream_t stream);
+
+/* Number of fp32 partial sums per permuted row written to `rowdot` by the
+ * SwiGLU-backward dgrad with F = K: 2 * ceil(F / 256) (0 if F <= 0), and the
+ * row stride of `rowdot` in floats: gg_rowdot_blocks(F) rounded up to a
+ * multiple of 8. */
+int gg_rowdot_blocks(int F);
+int gg_rowdot_stride(int F);
 
 /* ---------------------------------------------------------------------------
  * gg_grouped_fwd_gather / gg_grouped_dgrad_gather — the same GEMMs with the
@@ -277,7 +297,8 @@ gg_status gg_grouped_dgrad_gather(const gg_bf16* src, int T, const int32_t* slot
                                   const gg_bf16* B, const int32_t* offsets,
                                   int E, int R_cap, int K, int N, gg_epilogue epi,
                                   const gg_bf16* H1, const float* prob_of_row, gg_bf16* dA,
-                                  void* ws, size_t ws_bytes, gg_stream_t stream);
+                                  float* rowdot, void* ws, size_t ws_bytes,
+                                  gg_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * gg_unpermute_combine — probability-weighted combine ([P4] "What does this
@@ -287,10 +308,17 @@ gg_status gg_grouped_dgrad_gather(const gg_bf16* src, int T, const int32_t* slot
  * gives the unweighted sum (the input-gradient combine). Pairs whose row is
  * -1 contribute nothing. Yp[R_cap][H], out[T][H] BF16; k <= 32. A row outside
  * [-1, R_cap) sets GG_ERR_DEVICE_BAD_ROW and is skipped.
+ * dprob (nullable): the routing-probability gradient from the partial sums
+ * of gg_grouped_dgrad's `rowdot` ([R_cap][stride] fp32 with stride =
+ * n_rowdot rounded up to a multiple of 8, n_rowdot >= 1, 32-byte aligned):
+ *   dprob[t*k+j] = sum_{b < n_rowdot} rowdot[row_of_slot[t*k+j]][b]
+ * in fp32, b ascending; 0 for a pair without a row. rowdot must be non-NULL
+ * when dprob is; both NULL (n_rowdot ignored) skips it.
  * ------------------------------------------------------------------------- */
 gg_status gg_unpermute_combine(const gg_bf16* Yp, const int32_t* row_of_slot,
                                const float* prob, int T, int k, int H, int R_cap,
-                               gg_bf16* out, void* ws, size_t ws_bytes,
+                               gg_bf16* out, const float* rowdot, int n_rowdot,
+                               float* dprob, void* ws, size_t ws_bytes,
                                gg_stream_t stream);
 
 /* ---------------------------------------------------------------------------
@@ -309,6 +337,7 @@ typedef struct gg_moe_buffers {
   int32_t* row_of_slot; /* [T*k]                                          */
   int32_t* slot_of_row; /* [R_cap]                                        */
   float* prob_of_row;   /* [R_cap]                                        */
+  float* rowdot;        /* [R_cap][gg_rowdot_stride(F)] dprob partial sums */
   void* ws;             /* gg_workspace_size(T, k, E) bytes, status first */
   size_t ws_bytes;
 } gg_moe_buffers;
@@ -331,10 +360,14 @@ gg_status gg_moe_mlp_fwd(const gg_bf16* x, const int32_t* idx, const float* prob
 
 /* Input gradient of gg_moe_mlp_fwd (same buffers, after the forward):
  * permute dOut -> dgrad FC2 with probability scale and fused SwiGLU
- * backward -> dgrad FC1 -> unweighted combine into dX[T][H]. */
+ * backward -> dgrad FC1 -> unweighted combine into dX[T][H]. With dprob
+ * (nullable) also the routing-probability gradient dprob[T][k] fp32,
+ * dprob[t][j] = <dOut[t], FC2 output of pair (t, j)>, from partial sums the
+ * SwiGLU-backward epilogue accumulates and the dX combine adds up. */
 gg_status gg_moe_mlp_bwd(const gg_bf16* dOut, const gg_bf16* W1, const gg_bf16* W2,
                          int T, int H, int F, int k, int E, int pad_multiple,
-                         gg_bf16* dX, const gg_moe_buffers* buf, gg_stream_t stream);
+                         gg_bf16* dX, float* dprob, const gg_moe_buffers* buf,
+                         gg_stream_t stream);
 
 /* Test hook for the bounded waits: one CTA waits on a barrier that nothing
  * completes, gives up after `limit_ns` nanoseconds (clamped to 1 s), writes

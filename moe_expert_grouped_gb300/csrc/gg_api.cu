@@ -108,7 +108,11 @@ const char* gg_status_string(int status) {
   }
 }
 
-const char* gg_version(void) { return "gg 0.1 sm_103a"; }
+const char* gg_version(void) { return "gg 0.2 sm_103a"; }
+
+int gg_rowdot_blocks(int F) { return F > 0 ? 2 * ((F + 255) / 256) : 0; }
+
+int gg_rowdot_stride(int F) { return (gg_rowdot_blocks(F) + 7) / 8 * 8; }
 
 uint64_t gg_launch_count(void) { return g_launches.load(); }
 
@@ -235,16 +239,21 @@ gg_status gg_swiglu(const gg_bf16* H1, const int32_t* offsets, int E, int R_cap,
                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static gg_status dgrad_epilogue_checks(gg_epilogue epi, const gg_bf16* H1, const float* rowdot) {
+  if (epi != GG_EPI_NONE && epi != GG_EPI_SWIGLU_BWD) return GG_ERR_INVALID_ARG;
+  if (epi == GG_EPI_NONE && (H1 != nullptr || rowdot != nullptr)) return GG_ERR_INVALID_ARG;
+  if (epi == GG_EPI_SWIGLU_BWD && H1 == nullptr) return GG_ERR_INVALID_ARG;
+  if (!aligned16(H1) || (reinterpret_cast<uintptr_t>(rowdot) & 31u) != 0) return GG_ERR_MISALIGNED;
+  return GG_OK;
+}
+
 gg_status gg_grouped_dgrad(const gg_bf16* dC, const gg_bf16* B, const int32_t* offsets, int E,
                            int R_cap, int K, int N, gg_epilogue epi, const gg_bf16* H1,
-                           const float* prob_of_row, gg_bf16* dA, void* ws, size_t ws_bytes,
-                           gg_stream_t stream) {
+                           const float* prob_of_row, gg_bf16* dA, float* rowdot, void* ws,
+                           size_t ws_bytes, gg_stream_t stream) {
   gg_status s = gemm_common_checks(dC, B, offsets, E, R_cap, K, N, dA, ws, ws_bytes);
   if (s != GG_OK) return s;
-  if (epi != GG_EPI_NONE && epi != GG_EPI_SWIGLU_BWD) return GG_ERR_INVALID_ARG;
-  if (epi == GG_EPI_NONE && H1 != nullptr) return GG_ERR_INVALID_ARG;
-  if (epi == GG_EPI_SWIGLU_BWD && H1 == nullptr) return GG_ERR_INVALID_ARG;
-  if (!aligned16(H1)) return GG_ERR_MISALIGNED;
+  if ((s = dgrad_epilogue_checks(epi, H1, rowdot)) != GG_OK) return s;
   DeviceInfo dev;
   if ((s = device_ok(&dev)) != GG_OK) return s;
   if (R_cap == 0) return GG_OK;
@@ -262,6 +271,7 @@ gg_status gg_grouped_dgrad(const gg_bf16* dC, const gg_bf16* B, const int32_t* o
   a.C = dA;
   a.H1 = H1;
   a.row_scale = prob_of_row;
+  a.rowdot = rowdot;
   a.status = status_ptr(ws);
   gg_status he = GG_OK;
   cudaError_t e = launch_grouped_gemm(a, dev, reinterpret_cast<cudaStream_t>(stream), &he);
@@ -317,16 +327,13 @@ gg_status gg_grouped_fwd_gather(const gg_bf16* src, int T, const int32_t* slot_o
 gg_status gg_grouped_dgrad_gather(const gg_bf16* src, int T, const int32_t* slot_of_row, int k,
                                   const gg_bf16* B, const int32_t* offsets, int E, int R_cap,
                                   int K, int N, gg_epilogue epi, const gg_bf16* H1,
-                                  const float* prob_of_row, gg_bf16* dA, void* ws,
+                                  const float* prob_of_row, gg_bf16* dA, float* rowdot, void* ws,
                                   size_t ws_bytes, gg_stream_t stream) {
   gg_status s = gather_checks(src, T, slot_of_row, k);
   if (s != GG_OK) return s;
   s = gemm_common_checks(src, B, offsets, E, R_cap, K, N, dA, ws, ws_bytes);
   if (s != GG_OK) return s;
-  if (epi != GG_EPI_NONE && epi != GG_EPI_SWIGLU_BWD) return GG_ERR_INVALID_ARG;
-  if (epi == GG_EPI_NONE && H1 != nullptr) return GG_ERR_INVALID_ARG;
-  if (epi == GG_EPI_SWIGLU_BWD && H1 == nullptr) return GG_ERR_INVALID_ARG;
-  if (!aligned16(H1)) return GG_ERR_MISALIGNED;
+  if ((s = dgrad_epilogue_checks(epi, H1, rowdot)) != GG_OK) return s;
   DeviceInfo dev;
   if ((s = device_ok(&dev)) != GG_OK) return s;
   if (R_cap == 0 || T == 0) return GG_OK;
@@ -343,6 +350,7 @@ gg_status gg_grouped_dgrad_gather(const gg_bf16* src, int T, const int32_t* slot
   a.C = dA;
   a.H1 = H1;
   a.row_scale = prob_of_row;
+  a.rowdot = rowdot;
   a.status = status_ptr(ws);
   a.gather_src = src;
   a.slot_of_row = slot_of_row;
@@ -355,18 +363,23 @@ gg_status gg_grouped_dgrad_gather(const gg_bf16* src, int T, const int32_t* slot
 }
 
 gg_status gg_unpermute_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const float* prob,
-                               int T, int k, int H, int R_cap, gg_bf16* out, void* ws,
-                               size_t ws_bytes, gg_stream_t stream) {
+                               int T, int k, int H, int R_cap, gg_bf16* out, const float* rowdot,
+                               int n_rowdot, float* dprob, void* ws, size_t ws_bytes,
+                               gg_stream_t stream) {
   if (T < 0 || k <= 0 || k > 32 || H <= 0 || R_cap < 0) return GG_ERR_INVALID_ARG;
   if (H % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
   if (T > 0 && (Yp == nullptr || row_of_slot == nullptr || out == nullptr))
     return GG_ERR_INVALID_ARG;
+  if (dprob != nullptr && (rowdot == nullptr || n_rowdot <= 0)) return GG_ERR_INVALID_ARG;
+  if (dprob == nullptr && rowdot != nullptr) return GG_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(rowdot) & 31u) != 0) return GG_ERR_MISALIGNED;
   if (!aligned16(Yp) || !aligned16(out)) return GG_ERR_MISALIGNED;
   gg_status s = check_ws(ws, ws_bytes, kWsHeader);
   if (s != GG_OK) return s;
   DeviceInfo dev;
   if ((s = device_ok(&dev)) != GG_OK) return s;
-  return from_cuda(launch_combine(Yp, row_of_slot, prob, T, k, H, R_cap, out, status_ptr(ws),
+  return from_cuda(launch_combine(Yp, row_of_slot, prob, T, k, H, R_cap, out, rowdot,
+                                  dprob != nullptr ? n_rowdot : 0, dprob, status_ptr(ws),
                                   dev.sm_count, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -384,6 +397,7 @@ size_t gg_moe_buffers_size(int T, int H, int F, int k, int E, int pad_multiple) 
   n += align256(sizeof(int32_t) * static_cast<size_t>(T) * k);  // row_of_slot
   n += align256(sizeof(int32_t) * R_cap);    // slot_of_row
   n += align256(sizeof(float) * R_cap);      // prob_of_row
+  n += align256(sizeof(float) * R_cap * gg_rowdot_stride(F));  // rowdot
   n += align256(gg_workspace_size(T, k, E)); // workspace (status first)
   return n;
 }
@@ -416,6 +430,7 @@ gg_status gg_moe_buffers_bind(void* base, size_t bytes, int T, int H, int F, int
       reinterpret_cast<int32_t*>(take(sizeof(int32_t) * static_cast<size_t>(T) * k));
   out->slot_of_row = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * R_cap));
   out->prob_of_row = reinterpret_cast<float*>(take(sizeof(float) * R_cap));
+  out->rowdot = reinterpret_cast<float*>(take(sizeof(float) * R_cap * gg_rowdot_stride(F)));
   out->ws_bytes = align256(gg_workspace_size(T, k, E));
   out->ws = take(out->ws_bytes);
   return GG_OK;
@@ -425,7 +440,8 @@ static gg_status check_buffers(const gg_moe_buffers* b, int T, int k, int E) {
   if (b == nullptr) return GG_ERR_INVALID_ARG;
   if (b->Xp == nullptr || b->H1 == nullptr || b->A == nullptr || b->Yp == nullptr ||
       b->dYp == nullptr || b->dH == nullptr || b->dXp == nullptr || b->offsets == nullptr ||
-      b->row_of_slot == nullptr || b->slot_of_row == nullptr || b->prob_of_row == nullptr)
+      b->row_of_slot == nullptr || b->slot_of_row == nullptr || b->prob_of_row == nullptr ||
+      b->rowdot == nullptr)
     return GG_ERR_INVALID_ARG;
   return check_ws(b->ws, b->ws_bytes, gg_workspace_size(T, k, E));
 }
@@ -457,12 +473,12 @@ gg_status gg_moe_mlp_fwd(const gg_bf16* x, const int32_t* idx, const float* prob
   s = gg_grouped_fwd(buf->A, W2, buf->offsets, E, R_cap, F, H, GG_EPI_NONE, buf->Yp, nullptr,
                      buf->ws, buf->ws_bytes, stream);
   if (s != GG_OK) return s;
-  return gg_unpermute_combine(buf->Yp, buf->row_of_slot, prob, T, k, H, R_cap, out, buf->ws,
-                              buf->ws_bytes, stream);
+  return gg_unpermute_combine(buf->Yp, buf->row_of_slot, prob, T, k, H, R_cap, out, nullptr, 0,
+                              nullptr, buf->ws, buf->ws_bytes, stream);
 }
 
 gg_status gg_moe_mlp_bwd(const gg_bf16* dOut, const gg_bf16* W1, const gg_bf16* W2, int T, int H,
-                         int F, int k, int E, int pad_multiple, gg_bf16* dX,
+                         int F, int k, int E, int pad_multiple, gg_bf16* dX, float* dprob,
                          const gg_moe_buffers* buf, gg_stream_t stream) {
   if (T < 0 || H <= 0 || k <= 0 || E <= 0 || pad_multiple <= 0 || F <= 0)
     return GG_ERR_INVALID_ARG;
@@ -472,6 +488,7 @@ gg_status gg_moe_mlp_bwd(const gg_bf16* dOut, const gg_bf16* W1, const gg_bf16* 
   if (F % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
   if (T == 0) return GG_OK;
   if (dOut == nullptr || dX == nullptr) return GG_ERR_INVALID_ARG;
+  float* rowdot = dprob != nullptr ? buf->rowdot : nullptr;
   const long long rc = r_cap_of(T, k, E, pad_multiple);
   if (rc > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
   const int R_cap = static_cast<int>(rc);
@@ -480,14 +497,14 @@ gg_status gg_moe_mlp_bwd(const gg_bf16* dOut, const gg_bf16* W1, const gg_bf16* 
   if (s != GG_OK) return s;
   // dH = SwiGLU'(H1) applied to prob_of_row * (dYp @ W2_e), W2 being [E][H][F]
   s = gg_grouped_dgrad(buf->dYp, W2, buf->offsets, E, R_cap, F, H, GG_EPI_SWIGLU_BWD, buf->H1,
-                       buf->prob_of_row, buf->dH, buf->ws, buf->ws_bytes, stream);
+                       buf->prob_of_row, buf->dH, rowdot, buf->ws, buf->ws_bytes, stream);
   if (s != GG_OK) return s;
   // dXp = dH @ W1_e; W1 is [E][2F][H]
   s = gg_grouped_dgrad(buf->dH, W1, buf->offsets, E, R_cap, H, 2 * F, GG_EPI_NONE, nullptr,
-                       nullptr, buf->dXp, buf->ws, buf->ws_bytes, stream);
+                       nullptr, buf->dXp, nullptr, buf->ws, buf->ws_bytes, stream);
   if (s != GG_OK) return s;
-  return gg_unpermute_combine(buf->dXp, buf->row_of_slot, nullptr, T, k, H, R_cap, dX, buf->ws,
-                              buf->ws_bytes, stream);
+  return gg_unpermute_combine(buf->dXp, buf->row_of_slot, nullptr, T, k, H, R_cap, dX, rowdot,
+                              gg_rowdot_blocks(F), dprob, buf->ws, buf->ws_bytes, stream);
 }
 
 gg_status gg_selftest_bounded_wait(void* ws, size_t ws_bytes, uint64_t limit_ns,

@@ -99,6 +99,8 @@ struct KParams {
   gg_bf16* H1_save;
   const gg_bf16* H1;
   const float* row_scale;
+  float* rowdot;               // dgrad SwiGLU backward: [R_cap][rowdot_stride] partial <acc, a>
+  int rowdot_stride;
   int32_t* status;
   const int32_t* slot_of_row;  // gathered A: source row of every permuted row
   int gather_k;
@@ -486,6 +488,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         if (!mbar_wait_bounded(smem_u32(&st.tfull[acc]), acc_phase, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+        float rdot = 0.0f;  // this row's <acc, a> over this warp's columns
+        const bool want_dot = p.rowdot != nullptr;
 #pragma unroll 1
         for (int c = c0; c < c_end; c += 32) {
           float v[32];
@@ -506,11 +510,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             us[4 * i + 2] = uw[i].z; us[4 * i + 3] = uw[i].w;
           }
           float dg[32], du[32];
+          if (want_dot) {
 #pragma unroll
-          for (int h = 0; h < 16; ++h) {
-            silu_mul_bwd(v[2 * h] * scale, bf16_lo(gs[h]), bf16_lo(us[h]), dg[2 * h], du[2 * h]);
-            silu_mul_bwd(v[2 * h + 1] * scale, bf16_hi(gs[h]), bf16_hi(us[h]), dg[2 * h + 1],
-                         du[2 * h + 1]);
+            for (int h = 0; h < 16; ++h) {
+              silu_mul_bwd<true>(v[2 * h], scale, bf16_lo(gs[h]), bf16_lo(us[h]), dg[2 * h],
+                                 du[2 * h], rdot);
+              silu_mul_bwd<true>(v[2 * h + 1], scale, bf16_hi(gs[h]), bf16_hi(us[h]),
+                                 dg[2 * h + 1], du[2 * h + 1], rdot);
+            }
+          } else {
+#pragma unroll
+            for (int h = 0; h < 16; ++h) {
+              silu_mul_bwd<false>(v[2 * h], scale, bf16_lo(gs[h]), bf16_lo(us[h]), dg[2 * h],
+                                  du[2 * h], rdot);
+              silu_mul_bwd<false>(v[2 * h + 1], scale, bf16_hi(gs[h]), bf16_hi(us[h]),
+                                  dg[2 * h + 1], du[2 * h + 1], rdot);
+            }
           }
           uint4 w[4];
           pack_bf16x32(dg, 1.0f, w);
@@ -518,6 +533,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
           pack_bf16x32(du, 1.0f, w);
           store_chunk(stg, w, drow + F + c, valid);
         }
+        if (p.rowdot != nullptr && valid)
+          p.rowdot[grow * p.rowdot_stride + nt * 2 + half] = rdot;
       }
       tc_fence_before();
       __syncwarp();
@@ -673,6 +690,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaSt
   kp.H1_save = a.H1_save;
   kp.H1 = a.H1;
   kp.row_scale = a.row_scale;
+  kp.rowdot = a.rowdot;
+  kp.rowdot_stride = (2 * ((a.Nout + BN - 1) / BN) + 7) / 8 * 8;
   kp.status = a.status;
   kp.slot_of_row = a.slot_of_row;
   kp.gather_k = a.gather_k;

@@ -49,9 +49,12 @@ cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* row_of_slot,
                                int E, int R_cap, int T, bool has_padding, gg_bf16* dst,
                                int32_t* status, int sm_count, cudaStream_t stream);
 
+// dprob (nullable): dprob[t*k+j] = sum_b rowdot[row_of_slot[t*k+j]][b], rows of
+// rowdot (n_rowdot + 7) / 8 * 8 floats apart.
 cudaError_t launch_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const float* prob,
-                           int T, int k, int H, int R_cap, gg_bf16* out, int32_t* status,
-                           int sm_count, cudaStream_t stream);
+                           int T, int k, int H, int R_cap, gg_bf16* out, const float* rowdot,
+                           int n_rowdot, float* dprob, int32_t* status, int sm_count,
+                           cudaStream_t stream);
 
 cudaError_t launch_bounded_wait_selftest(int32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
@@ -76,6 +79,7 @@ struct GemmArgs {
   gg_bf16* H1_save;        // fwd SwiGLU: [R_cap][2F] or null
   const gg_bf16* H1;       // dgrad SwiGLU backward: [R_cap][2F]
   const float* row_scale;  // dgrad: prob_of_row or null
+  float* rowdot = nullptr; // dgrad SwiGLU backward: [R_cap][stride] partials, or null
   int32_t* status;
   // Gathered A operand: row r of A is gather_src[slot_of_row[r] / gather_k]
   // (zero where the slot is -1); gather_src is token-major [gather_rows][Kred].

@@ -314,6 +314,89 @@ combine_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row_of_
   }
 }
 
+// combine_kernel plus the routing-probability gradient: lane j < k also adds
+// up the n_rowdot partial sums of its pair's row (the first eight as one
+// aligned 32-byte group, loaded before the column loop and added after it, in
+// fp32 in ascending order). A separate kernel so that the plain combine keeps
+// its own code.
+__global__ void __launch_bounds__(256, 4)
+combine_dprob_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row_of_slot,
+                     const float* __restrict__ prob, int T, int k, int vec_per_row, int R_cap,
+                     uint4* __restrict__ out, const float* __restrict__ rowdot, int n_rowdot,
+                     float* __restrict__ dprob, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int warp0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = warp0; t < T; t += nwarps) {
+    int my_row = -1;
+    float my_p = 1.0f;
+    if (lane < k) {
+      my_row = row_of_slot[static_cast<long long>(t) * k + lane];
+      if (prob != nullptr) my_p = prob[static_cast<long long>(t) * k + lane];
+      if (my_row < -1 || my_row >= R_cap) {
+        set_status(status, GG_ERR_DEVICE_BAD_ROW);
+        my_row = -1;
+      }
+    }
+    const int rd_stride = (n_rowdot + 7) / 8 * 8;
+    float4 part0 = make_float4(0.f, 0.f, 0.f, 0.f), part1 = part0;
+    if (lane < k && my_row >= 0) {
+      const float4* rd =
+          reinterpret_cast<const float4*>(rowdot + static_cast<long long>(my_row) * rd_stride);
+      part0 = __ldg(rd);
+      part1 = __ldg(rd + 1);
+    }
+    // The column loop is warp-uniform so that the shuffles below see every lane.
+    for (int c0 = 0; c0 < vec_per_row; c0 += 64) {
+      const int ca = c0 + lane, cb = c0 + 32 + lane;
+      const bool oka = ca < vec_per_row, okb = cb < vec_per_row;
+      float acc[2][8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[0][i] = acc[1][i] = 0.0f;
+#pragma unroll 8
+      for (int j = 0; j < k; ++j) {
+        const int row = __shfl_sync(0xFFFFFFFFu, my_row, j & 31);
+        const float pj = __shfl_sync(0xFFFFFFFFu, my_p, j & 31);
+        if (row < 0) continue;  // warp-uniform: every lane holds the same row
+        const uint4* rp = Yp + static_cast<long long>(row) * vec_per_row;
+        const uint4 va = oka ? __ldcs(rp + ca) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 vb = okb ? __ldcs(rp + cb) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
+        const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[0][2 * q] = __fmaf_rn(pj, bf16_lo(wa[q]), acc[0][2 * q]);
+          acc[0][2 * q + 1] = __fmaf_rn(pj, bf16_hi(wa[q]), acc[0][2 * q + 1]);
+          acc[1][2 * q] = __fmaf_rn(pj, bf16_lo(wb[q]), acc[1][2 * q]);
+          acc[1][2 * q + 1] = __fmaf_rn(pj, bf16_hi(wb[q]), acc[1][2 * q + 1]);
+        }
+      }
+      uint4* op = out + static_cast<long long>(t) * vec_per_row;
+      if (oka)
+        __stcs(op + ca, make_uint4(pack_bf16x2(acc[0][0], acc[0][1]), pack_bf16x2(acc[0][2], acc[0][3]),
+                                   pack_bf16x2(acc[0][4], acc[0][5]), pack_bf16x2(acc[0][6], acc[0][7])));
+      if (okb)
+        __stcs(op + cb, make_uint4(pack_bf16x2(acc[1][0], acc[1][1]), pack_bf16x2(acc[1][2], acc[1][3]),
+                                   pack_bf16x2(acc[1][4], acc[1][5]), pack_bf16x2(acc[1][6], acc[1][7])));
+    }
+    if (lane < k) {
+      float dp = 0.0f;
+      if (n_rowdot > 0) dp += part0.x;
+      if (n_rowdot > 1) dp += part0.y;
+      if (n_rowdot > 2) dp += part0.z;
+      if (n_rowdot > 3) dp += part0.w;
+      if (n_rowdot > 4) dp += part1.x;
+      if (n_rowdot > 5) dp += part1.y;
+      if (n_rowdot > 6) dp += part1.z;
+      if (n_rowdot > 7) dp += part1.w;
+      if (my_row >= 0)
+        for (int b = 8; b < n_rowdot; ++b)
+          dp += __ldg(rowdot + static_cast<long long>(my_row) * rd_stride + b);
+      dprob[static_cast<long long>(t) * k + lane] = dp;
+    }
+  }
+}
+
 __global__ void bounded_wait_selftest_kernel(int32_t* status, uint64_t limit_ns) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
@@ -375,6 +458,9 @@ cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* row_of_slot,
   if (R_cap <= 0 || T <= 0) return cudaSuccess;
   const int vec = H / 8;
   long long blocks = (static_cast<long long>(T) + 7) / 8;
+  // 8 blocks per SM: more than fit at once; the blocks of the second wave
+  // start as the first ones finish, which balances tokens whose rows load
+  // slowly (measured faster than one exactly resident wave).
   const long long cap = static_cast<long long>(sm_count) * 8;
   if (blocks > cap) blocks = cap;
   scatter_rows_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
@@ -392,16 +478,22 @@ cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* row_of_slot,
 }
 
 cudaError_t launch_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const float* prob,
-                           int T, int k, int H, int R_cap, gg_bf16* out, int32_t* status,
-                           int sm_count, cudaStream_t stream) {
+                           int T, int k, int H, int R_cap, gg_bf16* out, const float* rowdot,
+                           int n_rowdot, float* dprob, int32_t* status, int sm_count,
+                           cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
   const int vec = H / 8;
   long long blocks = (static_cast<long long>(T) + 7) / 8;
-  const long long cap = static_cast<long long>(sm_count) * 8;
+  const long long cap = static_cast<long long>(sm_count) * 8;  // as for the row copy
   if (blocks > cap) blocks = cap;
-  combine_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
-      reinterpret_cast<const uint4*>(Yp), row_of_slot, prob, T, k, vec, R_cap,
-      reinterpret_cast<uint4*>(out), status);
+  if (dprob != nullptr)
+    combine_dprob_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+        reinterpret_cast<const uint4*>(Yp), row_of_slot, prob, T, k, vec, R_cap,
+        reinterpret_cast<uint4*>(out), rowdot, n_rowdot, dprob, status);
+  else
+    combine_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+        reinterpret_cast<const uint4*>(Yp), row_of_slot, prob, T, k, vec, R_cap,
+        reinterpret_cast<uint4*>(out), status);
   count_launch();
   return cudaGetLastError();
 }

@@ -287,13 +287,24 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return (g * s) * u;
 }
 
-// Backward of silu(g) * u given dA: returns (dg, du).
-//   d silu / dg = s * (1 + g * (1 - s)),  s = sigmoid(g)
-__device__ __forceinline__ void silu_mul_bwd(float dA, float g, float u, float& dg, float& du) {
+__device__ __forceinline__ float round_bf16(float x);
+
+// Backward of silu(g) * u at dA = acc * scale: dg = dA * u * silu'(g),
+// du = dA * silu(g), silu'(g) = s * (1 + g * (1 - s)) with s = sigmoid(g).
+// With kDot also dot += acc * bf16(silu(g) * u): the SwiGLU output of the
+// forward pass (same sigmoid and products as silu_mul, so the same BF16
+// value) against the unscaled accumulator, for the routing-probability
+// gradient.
+template <bool kDot>
+__device__ __forceinline__ void silu_mul_bwd(float acc, float scale, float g, float u, float& dg,
+                                             float& du, float& dot) {
+  const float dA = acc * scale;
   const float s = __fdividef(1.0f, 1.0f + __expf(-g));
   const float dsilu = s * (1.0f + g * (1.0f - s));
+  const float gs = g * s;
   dg = (dA * u) * dsilu;
-  du = dA * (g * s);
+  du = dA * gs;
+  if (kDot) dot = fmaf(acc, round_bf16(gs * u), dot);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

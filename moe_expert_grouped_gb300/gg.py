@@ -40,17 +40,19 @@ SIGNATURES = [
     ("gg_permute_rows", _I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
     ("gg_grouped_fwd", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
     ("gg_swiglu", _I, [_P, _P, _I, _I, _I, _P, _P]),
-    ("gg_grouped_dgrad", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
-    ("gg_unpermute_combine", _I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P]),
+    ("gg_grouped_dgrad", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
+    ("gg_rowdot_blocks", _I, [_I]),
+    ("gg_rowdot_stride", _I, [_I]),
+    ("gg_unpermute_combine", _I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _Z, _P]),
     ("gg_moe_buffers_size", _Z, [_I, _I, _I, _I, _I, _I]),
     ("gg_moe_buffers_bind", _I, [_P, _Z, _I, _I, _I, _I, _I, _I, _P]),
     ("gg_moe_mlp_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
-    ("gg_moe_mlp_bwd", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
+    ("gg_moe_mlp_bwd", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     ("gg_selftest_bounded_wait", _I, [_P, _Z, _U64, _P]),
     ("gg_permute_noalloc", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     ("gg_grouped_fwd_gather", _I, [_P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
     ("gg_grouped_dgrad_gather", _I,
-     [_P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
+     [_P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
 ]
 
 
@@ -59,7 +61,7 @@ class GGBuffers(ctypes.Structure):
 
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "Xp", "H1", "A", "Yp", "dYp", "dH", "dXp", "offsets", "row_of_slot", "slot_of_row",
-        "prob_of_row", "ws")] + [("ws_bytes", ctypes.c_size_t)]
+        "prob_of_row", "rowdot", "ws")] + [("ws_bytes", ctypes.c_size_t)]
 
 
 class GGError(RuntimeError):
@@ -216,8 +218,18 @@ def grouped_fwd_gather(src, slot_of_row, k: int, B, offsets, epilogue: int = GG_
     return C
 
 
+def rowdot_blocks(F: int) -> int:
+    """gg_rowdot_blocks: partial sums per row of the dprob epilogue output."""
+    return int(LIB.gg_rowdot_blocks(int(F)))
+
+
+def rowdot_stride(F: int) -> int:
+    """gg_rowdot_stride: floats per row of the rowdot array [R_cap, stride]."""
+    return int(LIB.gg_rowdot_stride(int(F)))
+
+
 def grouped_dgrad_gather(src, slot_of_row, k: int, B, offsets, epilogue: int = GG_EPI_NONE,
-                         H1=None, prob_of_row=None, ws=None, dA=None):
+                         H1=None, prob_of_row=None, ws=None, dA=None, rowdot=None):
     """gg_grouped_dgrad_gather: dC rows gathered from token-major src [T, N]."""
     T, N = src.shape
     E, Nb, K = B.shape
@@ -230,7 +242,8 @@ def grouped_dgrad_gather(src, slot_of_row, k: int, B, offsets, epilogue: int = G
     ws = workspace(0, 1, E, dev) if ws is None else ws
     _check(LIB.gg_grouped_dgrad_gather(_ptr(src), T, _ptr(slot_of_row), k, _ptr(B), _ptr(offsets),
                                        E, R_cap, K, N, epilogue, _ptr(H1), _ptr(prob_of_row),
-                                       _ptr(dA), _ptr(ws), ws.numel(), _stream(dev)),
+                                       _ptr(dA), _ptr(rowdot), _ptr(ws), ws.numel(),
+                                       _stream(dev)),
            "gg_grouped_dgrad_gather")
     return dA
 
@@ -246,8 +259,10 @@ def swiglu(H1, offsets, E: int, A=None):
 
 
 def grouped_dgrad(dC, B, offsets, epilogue: int = GG_EPI_NONE, H1=None, prob_of_row=None,
-                  ws=None, dA=None):
-    """gg_grouped_dgrad. B is the forward weight [E, N, K]; dC is [R_cap, N]."""
+                  ws=None, dA=None, rowdot=None):
+    """gg_grouped_dgrad. B is the forward weight [E, N, K]; dC is [R_cap, N]. With
+    GG_EPI_SWIGLU_BWD, rowdot [R_cap, rowdot_stride(K)] fp32 receives the dprob
+    partial sums (the first rowdot_blocks(K) of each row)."""
     R_cap, N = dC.shape
     E, Nb, K = B.shape
     if Nb != N:
@@ -257,20 +272,32 @@ def grouped_dgrad(dC, B, offsets, epilogue: int = GG_EPI_NONE, H1=None, prob_of_
     dA = torch.empty((R_cap, ncols), dtype=torch.bfloat16, device=dev) if dA is None else dA
     ws = workspace(0, 1, E, dev) if ws is None else ws
     _check(LIB.gg_grouped_dgrad(_ptr(dC), _ptr(B), _ptr(offsets), E, R_cap, K, N, epilogue,
-                                _ptr(H1), _ptr(prob_of_row), _ptr(dA), _ptr(ws), ws.numel(),
-                                _stream(dev)),
+                                _ptr(H1), _ptr(prob_of_row), _ptr(dA), _ptr(rowdot), _ptr(ws),
+                                ws.numel(), _stream(dev)),
            "gg_grouped_dgrad")
     return dA
 
 
-def unpermute_combine(Yp, row_of_slot, prob, T: int, k: int, ws, out=None):
-    """gg_unpermute_combine: probability-weighted (prob) or plain (None) sum of k rows."""
+def unpermute_combine(Yp, row_of_slot, prob, T: int, k: int, ws, out=None, rowdot=None,
+                      dprob=None, n_rowdot=None):
+    """gg_unpermute_combine: probability-weighted (prob) or plain (None) sum of k rows;
+    with rowdot [R_cap, stride] (and n_rowdot partials per row, default all but
+    the padding of the last 8-group: pass n_rowdot when it differs) also
+    dprob [T, k] = the sum of each pair's row partials."""
     R_cap, H = Yp.shape
     out = torch.empty((T, H), dtype=torch.bfloat16, device=Yp.device) if out is None else out
+    if rowdot is not None:
+        if n_rowdot is None:
+            raise ValueError("n_rowdot (rowdot_blocks(F)) is required with rowdot")
+        if (n_rowdot + 7) // 8 * 8 != rowdot.shape[1]:
+            raise ValueError("rowdot rows must hold n_rowdot rounded up to 8 floats")
+        if dprob is None:
+            dprob = torch.empty((T, k), dtype=torch.float32, device=Yp.device)
     _check(LIB.gg_unpermute_combine(_ptr(Yp), _ptr(row_of_slot), _ptr(prob), T, k, H, R_cap,
-                                    _ptr(out), _ptr(ws), ws.numel(), _stream(Yp.device)),
+                                    _ptr(out), _ptr(rowdot), n_rowdot or 0, _ptr(dprob), _ptr(ws),
+                                    ws.numel(), _stream(Yp.device)),
            "gg_unpermute_combine")
-    return out
+    return out if rowdot is None else (out, dprob)
 
 
 def selftest_bounded_wait(ws, limit_ns: int) -> None:
@@ -288,7 +315,8 @@ class MoeLayer:
     _SHAPES = {
         "Xp": ("rc", "H"), "Yp": ("rc", "H"), "dYp": ("rc", "H"), "dXp": ("rc", "H"),
         "H1": ("rc", "2F"), "dH": ("rc", "2F"), "A": ("rc", "F"), "offsets": ("E1",),
-        "row_of_slot": ("Tk",), "slot_of_row": ("rc",), "prob_of_row": ("rc",), "ws": ("ws",),
+        "row_of_slot": ("Tk",), "slot_of_row": ("rc",), "prob_of_row": ("rc",),
+        "rowdot": ("rc", "nbs"), "ws": ("ws",),
     }
 
     def __init__(self, T: int, H: int, F: int, k: int, E: int, P: int = 1, device="cuda"):
@@ -308,9 +336,11 @@ class MoeLayer:
     def view(self, name: str) -> torch.Tensor:
         """A torch view of one intermediate buffer of the struct."""
         dims = {"rc": self.R_cap, "H": self.H, "F": self.F, "2F": 2 * self.F, "E1": self.E + 1,
-                "Tk": self.T * self.k, "ws": int(self.buf.ws_bytes)}
+                "Tk": self.T * self.k, "ws": int(self.buf.ws_bytes),
+                "nbs": rowdot_stride(self.F)}
         dtype = {"offsets": torch.int32, "row_of_slot": torch.int32, "slot_of_row": torch.int32,
-                 "prob_of_row": torch.float32, "ws": torch.uint8}.get(name, torch.bfloat16)
+                 "prob_of_row": torch.float32, "rowdot": torch.float32,
+                 "ws": torch.uint8}.get(name, torch.bfloat16)
         shape = tuple(dims[d] for d in self._SHAPES[name])
         count = 1
         for s in shape:
@@ -332,14 +362,22 @@ class MoeLayer:
                                   _stream(self.device)), "gg_moe_mlp_fwd")
         return out
 
-    def backward(self, dOut, W1, W2, dX=None):
+    def backward(self, dOut, W1, W2, dX=None, dprob=None):
+        """dX [T, H]; with dprob ([T, k] fp32 tensor, or True to allocate one) also
+        the routing-probability gradient, returned as (dX, dprob)."""
         T, H, F, k, E = self.T, self.H, self.F, self.k, self.E
         _need(dOut, torch.bfloat16, (T, H), "dOut")
         dX = torch.empty((T, H), dtype=torch.bfloat16, device=self.device) if dX is None else dX
+        want = dprob is not None and dprob is not False
+        if dprob is True:
+            dprob = torch.empty((T, k), dtype=torch.float32, device=self.device)
+        if want:
+            _need(dprob, torch.float32, (T, k), "dprob")
         _check(LIB.gg_moe_mlp_bwd(_ptr(dOut), _ptr(W1), _ptr(W2), T, H, F, k, E, self.P,
-                                  _ptr(dX), ctypes.byref(self.buf), _stream(self.device)),
+                                  _ptr(dX), _ptr(dprob) if want else None,
+                                  ctypes.byref(self.buf), _stream(self.device)),
                "gg_moe_mlp_bwd")
-        return dX
+        return (dX, dprob) if want else dX
 
     def status(self) -> int:
         return read_status(self.view("ws"))

@@ -73,7 +73,7 @@ def test_buffers_bind_carves_disjoint_aligned_pieces(gg):
     sizes = {"Xp": rc * H * 2, "Yp": rc * H * 2, "dYp": rc * H * 2, "dXp": rc * H * 2,
              "H1": rc * 2 * F * 2, "dH": rc * 2 * F * 2, "A": rc * F * 2, "offsets": 4 * (E + 1),
              "row_of_slot": 4 * T * k, "slot_of_row": 4 * rc, "prob_of_row": 4 * rc,
-             "ws": buf.ws_bytes}
+             "rowdot": 4 * rc * gg.LIB.gg_rowdot_stride(F), "ws": buf.ws_bytes}
     spans = sorted((getattr(buf, name), getattr(buf, name) + sz) for name, sz in sizes.items())
     for (a0, a1), (b0, _) in zip(spans, spans[1:]):
         assert a1 <= b0
@@ -110,19 +110,34 @@ def test_validation_rejects_before_launch(gg):
     assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 192, 1, p, p, ws, 1024, None) == 2
     assert L.gg_grouped_fwd(mis, p, p, 4, 128, 64, 128, 0, p, None, ws, 1024, None) == 3
     assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 128, 0, p, None, ws, 16, None) == 4
-    # gg_grouped_dgrad: SwiGLU backward needs H1; NONE must not get H1
-    assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 2, None, None, p, ws, 1024, None) == 1
-    assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 0, p, None, p, ws, 1024, None) == 1
-    assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 1, p, None, p, ws, 1024, None) == 1
-    # gg_unpermute_combine: k > 32, H % 64
-    assert L.gg_unpermute_combine(p, p, p, 4, 33, 64, 128, p, ws, 1024, None) == 1
-    assert L.gg_unpermute_combine(p, p, p, 4, 2, 72, 128, p, ws, 1024, None) == 2
+    # gg_grouped_dgrad: SwiGLU backward needs H1; NONE must not get H1 or rowdot
+    assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 2, None, None, p, None, ws, 1024,
+                              None) == 1
+    assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 0, p, None, p, None, ws, 1024, None) == 1
+    assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 0, None, None, p, p, ws, 1024, None) == 1
+    assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 1, p, None, p, None, ws, 1024, None) == 1
+    assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 2, p, None, p, mis, ws, 1024, None) == 3
+    assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 2, p, None, p,
+                              ctypes.c_void_p((1 << 40) + 16), ws, 1024, None) == 3
+    # gg_unpermute_combine: k > 32, H % 64, dprob without partial sums (or the reverse)
+    assert L.gg_unpermute_combine(p, p, p, 4, 33, 64, 128, p, None, 0, None, ws, 1024, None) == 1
+    assert L.gg_unpermute_combine(p, p, p, 4, 2, 72, 128, p, None, 0, None, ws, 1024, None) == 2
+    assert L.gg_unpermute_combine(p, p, p, 4, 2, 64, 128, p, None, 2, p, ws, 1024, None) == 1
+    assert L.gg_unpermute_combine(p, p, p, 4, 2, 64, 128, p, p, 0, p, ws, 1024, None) == 1
+    assert L.gg_unpermute_combine(p, p, p, 4, 2, 64, 128, p, p, 2, None, ws, 1024, None) == 1
+    assert L.gg_rowdot_blocks(768) == 6 and L.gg_rowdot_blocks(64) == 2
+    assert L.gg_rowdot_blocks(256) == 2 and L.gg_rowdot_blocks(0) == 0
+    assert L.gg_rowdot_stride(768) == 8 and L.gg_rowdot_stride(1280) == 16
+    assert L.gg_rowdot_stride(0) == 0
+    # rowdot must be 32-byte aligned
+    mis32 = ctypes.c_void_p((1 << 40) + 16)
+    assert L.gg_unpermute_combine(p, p, p, 4, 2, 64, 128, p, mis32, 2, p, ws, 1024, None) == 3
     # gg_swiglu: F % 64
     assert L.gg_swiglu(p, p, 4, 128, 96, p, None) == 2
     # composites need a full buffer set
     buf = gg.GGBuffers()
     assert L.gg_moe_mlp_fwd(p, p, p, p, p, 4, 64, 128, 2, 4, 1, p, ctypes.byref(buf), None) == 1
-    assert L.gg_moe_mlp_bwd(p, p, p, 4, 64, 128, 2, 4, 1, p, ctypes.byref(buf), None) == 1
+    assert L.gg_moe_mlp_bwd(p, p, p, 4, 64, 128, 2, 4, 1, p, None, ctypes.byref(buf), None) == 1
     assert L.gg_moe_mlp_fwd(p, p, p, p, p, 4, 64, 128, 2, 4, 1, p, None, None) == 1
     assert L.gg_read_status(None, None, None) == 1
     assert L.gg_clear_status(None, None) == 1

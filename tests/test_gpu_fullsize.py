@@ -37,10 +37,10 @@ def _run(gg, shape, inp):
              W2=bits_to_torch(inp.W2), dOut=bits_to_torch(inp.dOut))
     layer = gg.MoeLayer(shape.T, shape.H, shape.F, shape.k, shape.E, shape.P)
     out = layer.forward(d["x"], d["idx"], d["prob"], d["W1"], d["W2"])
-    dX = layer.backward(d["dOut"], d["W1"], d["W2"])
+    dX, dprob = layer.backward(d["dOut"], d["W1"], d["W2"], dprob=True)
     torch.cuda.synchronize()
     assert layer.status() == 0
-    return layer, out, dX
+    return layer, out, (dX, dprob)
 
 
 def _check_indices(layer, inp, shape):
@@ -51,7 +51,8 @@ def _check_indices(layer, inp, shape):
     return off
 
 
-def _check_sample(inp, shape, out, dX, n_tokens, seed):
+def _check_sample(inp, shape, out, grads, n_tokens, seed):
+    dX, dprob = grads
     rng = np.random.default_rng(seed)
     sel = np.sort(rng.choice(shape.T, size=min(n_tokens, shape.T), replace=False))
     fwd = oracle.moe_forward(inp.x[sel], inp.idx[sel], inp.prob[sel], inp.W1, inp.W2, shape.E, 1)
@@ -62,6 +63,8 @@ def _check_sample(inp, shape, out, dX, n_tokens, seed):
     rows = torch.from_numpy(sel).cuda()
     assert_parity(torch_to_f64(out[rows]), fwd["out"], "out (sampled)", faithful=ffw["out"])
     assert_parity(torch_to_f64(dX[rows]), bwd["dX"], "dX (sampled)", faithful=fbw["dX"])
+    assert_parity(dprob[rows].cpu().numpy().astype(np.float64), bwd["dprob"], "dprob (sampled)",
+                  faithful=fbw["dprob"])
 
 
 @pytest.mark.parametrize("cfg", [2, 4])
@@ -72,7 +75,8 @@ def test_fullsize_sampled_parity(gg, cfg):
     _check_indices(layer, inp, shape)
     _check_sample(inp, shape, out, dX, 96, cfg)
     # every routed row was produced (no unwritten row survives in the output)
-    assert torch.isfinite(out.float()).all() and torch.isfinite(dX.float()).all()
+    assert torch.isfinite(out.float()).all() and torch.isfinite(dX[0].float()).all()
+    assert torch.isfinite(dX[1]).all()
 
 
 @pytest.mark.parametrize("rows", [SWEEP_ROWS[0], SWEEP_ROWS[-1]])
@@ -96,6 +100,7 @@ def test_skewed_padded_batch_invariance(gg):
     assert np.all(np.diff(off_a) % shape.P == 0)
     rows_a = slice(int(off_a[e_star]), int(off_a[e_star]) + int(counts[e_star]))
     snap = {n: torch_to_bits(la.view(n)[rows_a]) for n in ("H1", "A", "Yp", "dH", "dXp")}
+    snap_rd = la.view("rowdot")[rows_a].cpu().numpy()
     _check_sample(a, shape, out_a, dX_a, 96, 3)
     del la
     lb, out_b, dX_b = _run(gg, shape, b)
@@ -104,3 +109,4 @@ def test_skewed_padded_batch_invariance(gg):
     rows_b = slice(int(off_b[e_star]), int(off_b[e_star]) + int(counts[e_star]))
     for n, bits in snap.items():
         np.testing.assert_array_equal(torch_to_bits(lb.view(n)[rows_b]), bits, err_msg=n)
+    np.testing.assert_array_equal(lb.view("rowdot")[rows_b].cpu().numpy(), snap_rd)

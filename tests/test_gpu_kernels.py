@@ -127,17 +127,29 @@ def test_grouped_dgrad_swiglu_backward(gg, F, H):
     prob = rng.uniform(0.05, 1.0, R_cap).astype(np.float32)
     ws = gg.workspace(0, 1, E, "cuda")
     dH = _nan_filled((R_cap, 2 * F))
+    nb, nbs = gg.rowdot_blocks(F), gg.rowdot_stride(F)
+    rowdot = torch.full((R_cap, nbs), float("nan"), dtype=torch.float32, device="cuda")
     gg.grouped_dgrad(bits_to_torch(dY), bits_to_torch(W2), torch.from_numpy(off).cuda(),
                      gg.GG_EPI_SWIGLU_BWD, H1=bits_to_torch(H1),
-                     prob_of_row=torch.from_numpy(prob).cuda(), ws=ws, dA=dH)
+                     prob_of_row=torch.from_numpy(prob).cuda(), ws=ws, dA=dH, rowdot=rowdot)
     torch.cuda.synchronize()
     assert gg.read_status(ws) == 0
     n = int(off[-1])
-    dA = prob.astype(np.float64)[:, None] * oracle.grouped_linear_t(oracle.bf16_bits_to_f64(dY),
-                                                                    W2, off)
-    ref = oracle.swiglu_backward(dA, oracle.bf16_bits_to_f64(H1))
+    acc = oracle.grouped_linear_t(oracle.bf16_bits_to_f64(dY), W2, off)
+    dA = prob.astype(np.float64)[:, None] * acc
+    h1 = oracle.bf16_bits_to_f64(H1)
+    ref = oracle.swiglu_backward(dA, h1)
     assert_parity(torch_to_f64(dH[:n]), ref[:n], "dH", faithful=oracle.round_to_bf16(ref[:n]))
     assert np.all(torch_to_bits(dH[n:]) == NAN_BF16)
+    # dprob partial sums: block b = columns [128 b, 128 b + 128) of the unscaled
+    # accumulator against the forward's BF16 SwiGLU output
+    a = oracle.round_to_bf16(oracle.swiglu(h1))
+    prod = acc * a
+    ref_rd = np.stack([prod[:, 128 * b:128 * (b + 1)].sum(axis=1) for b in range(nb)], axis=1)
+    got_rd = rowdot.cpu().numpy().astype(np.float64)
+    assert_parity(got_rd[:n, :nb], ref_rd[:n], "rowdot")
+    assert np.all(np.isnan(got_rd[n:]))  # rows past offsets[E] are not written
+    assert np.all(np.isnan(got_rd[:, nb:]))  # nor the padding of each row's group
 
 
 def _permute_case(T, E, k, seed, skew=None, dup=False):
@@ -208,6 +220,34 @@ def test_combine(gg, weighted):
     ros = p["row_of_slot"].cpu().numpy()
     ref = oracle.combine(oracle.bf16_bits_to_f64(Yp), ros, prob if weighted else None, T, k)
     assert_parity(torch_to_f64(out), ref, "out", faithful=oracle.round_to_bf16(ref))
+
+
+def test_combine_prob_gradient_sums_partials_in_order(gg):
+    # dprob[t, j] = sum_b rowdot[b][row(t, j)] in fp32, b ascending: bit-exact
+    # against the same fp32 sum on the host; a pair without a row gives 0.
+    T, k, H, R_cap = 300, 3, 64, 1000
+    rng = np.random.default_rng(41)
+    rows = rng.permutation(R_cap)[:T * k].astype(np.int32)
+    rows[[5, 77, 301]] = -1
+    Yp = normal_bf16(rng, (R_cap, H), 1.0)
+    ws = gg.workspace(T, k, 1, "cuda")
+    for nb in (6, 8, 11):  # one group of 8 with padding, exactly one, a second group
+        nbs = (nb + 7) // 8 * 8
+        rowdot = np.full((R_cap, nbs), np.nan, np.float32)
+        rowdot[:, :nb] = rng.standard_normal((R_cap, nb))
+        out, dprob = gg.unpermute_combine(bits_to_torch(Yp), torch.from_numpy(rows).cuda(), None,
+                                          T, k, ws, rowdot=torch.from_numpy(rowdot).cuda(),
+                                          n_rowdot=nb)
+        torch.cuda.synchronize()
+        assert gg.read_status(ws) == 0
+        want = np.zeros(T * k, np.float32)
+        for b in range(nb):
+            want = np.where(rows >= 0, want + rowdot[np.maximum(rows, 0), b], want)
+            want = want.astype(np.float32)
+        np.testing.assert_array_equal(dprob.cpu().numpy().reshape(-1), want)
+    # the combine itself is unchanged by the extra output
+    out2 = gg.unpermute_combine(bits_to_torch(Yp), torch.from_numpy(rows).cuda(), None, T, k, ws)
+    np.testing.assert_array_equal(torch_to_bits(out), torch_to_bits(out2))
 
 
 def test_permute_rows_gathers_token_gradient(gg):

@@ -38,20 +38,23 @@ def _dev(inp):
                 W2=bits_to_torch(inp.W2), dOut=bits_to_torch(inp.dOut))
 
 
-def _run(gg, shape, d):
+def _run(gg, shape, d, with_dprob=False):
     layer = gg.MoeLayer(shape.T, shape.H, shape.F, shape.k, shape.E, shape.P)
     out = layer.forward(d["x"], d["idx"], d["prob"], d["W1"], d["W2"])
-    dX = layer.backward(d["dOut"], d["W1"], d["W2"])
+    if with_dprob:
+        dX, dprob = layer.backward(d["dOut"], d["W1"], d["W2"], dprob=True)
+    else:
+        dX = layer.backward(d["dOut"], d["W1"], d["W2"])
     torch.cuda.synchronize()
     assert layer.status() == 0
-    return layer, out, dX
+    return (layer, out, dX, dprob) if with_dprob else (layer, out, dX)
 
 
 @pytest.mark.parametrize("shape,seed", [(CONFIGS[1], 1000), (MID, 77), (MID_PAD, 78)])
 def test_layer_matches_oracle(gg, shape, seed):
     inp = make_inputs(shape, seed)
     d = _dev(inp)
-    layer, out, dX = _run(gg, shape, d)
+    layer, out, dX, dprob = _run(gg, shape, d, with_dprob=True)
     fwd = oracle.moe_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, shape.E, shape.P)
     bwd = oracle.moe_backward(inp.dOut, fwd, inp.W1, inp.W2)
     ffw = oracle.moe_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, shape.E, shape.P,
@@ -59,6 +62,8 @@ def test_layer_matches_oracle(gg, shape, seed):
     fbw = oracle.moe_backward(inp.dOut, ffw, inp.W1, inp.W2, faithful=True)
     assert_parity(torch_to_f64(out), fwd["out"], "out", faithful=ffw["out"])
     assert_parity(torch_to_f64(dX), bwd["dX"], "dX", faithful=fbw["dX"])
+    assert_parity(dprob.cpu().numpy().astype(np.float64), bwd["dprob"], "dprob",
+                  faithful=fbw["dprob"])
     n = int(fwd["offsets"][-1])
     np.testing.assert_array_equal(layer.view("offsets").cpu().numpy(), fwd["offsets"])
     np.testing.assert_array_equal(layer.view("row_of_slot").cpu().numpy(), fwd["row_of_slot"])
@@ -73,10 +78,14 @@ def test_layer_matches_oracle(gg, shape, seed):
 def test_layer_run_to_run_bitwise(gg):
     inp = make_inputs(MID, 5)
     d = _dev(inp)
-    _, o1, g1 = _run(gg, MID, d)
-    _, o2, g2 = _run(gg, MID, d)
+    _, o1, g1, p1 = _run(gg, MID, d, with_dprob=True)
+    _, o2, g2, p2 = _run(gg, MID, d, with_dprob=True)
+    _, o3, g3 = _run(gg, MID, d)
     np.testing.assert_array_equal(torch_to_bits(o1), torch_to_bits(o2))
     np.testing.assert_array_equal(torch_to_bits(g1), torch_to_bits(g2))
+    np.testing.assert_array_equal(p1.cpu().numpy(), p2.cpu().numpy())
+    # asking for dprob leaves dX untouched
+    np.testing.assert_array_equal(torch_to_bits(g1), torch_to_bits(g3))
 
 
 def test_layer_empty_batch(gg):
