@@ -12,6 +12,10 @@ from .moe_oracle import (  # noqa: F401
     permute,
     grouped_linear,
     grouped_linear_t,
+    GLU_ALPHA,
+    PROB_MODES,
+    glu,
+    glu_backward,
     swiglu,
     swiglu_backward,
     combine,

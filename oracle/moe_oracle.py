@@ -156,26 +156,48 @@ def grouped_linear_t(dY: np.ndarray, W, offsets) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- activation
+#
+# Gated activations of "[Main] Support paged stash with device-initiated
+# GroupedLinear" (NVIDIA/Megatron-LM PR #6828, "What does this PR do?"): fused
+# SwiGLU or QuickGeGLU with GLU interleaving disabled. Both are
+# act(g) * u with act(g) = g * sigmoid(alpha * g): alpha = 1 is SiLU; the
+# page names QuickGeGLU without defining it, read here as the QuickGELU gate
+# x * sigmoid(1.702 x) of the usual definition.
 
-def swiglu(H1: np.ndarray) -> np.ndarray:
-    """A = silu(g) * u with g the first and u the second half of FC1's output."""
+GLU_ALPHA = {"swiglu": 1.0, "qgeglu": 1.702}
+
+
+def glu(H1: np.ndarray, activation: str = "swiglu") -> np.ndarray:
+    """A = g * sigmoid(alpha g) * u, g the first and u the second half of FC1's output."""
+    a = GLU_ALPHA[activation]
     F = H1.shape[1] // 2
     g, u = H1[:, :F], H1[:, F:]
-    return g * _sigmoid(g) * u
+    return g * _sigmoid(a * g) * u
+
+
+def glu_backward(dA: np.ndarray, H1: np.ndarray, activation: str = "swiglu") -> np.ndarray:
+    """Gradient of ``glu`` w.r.t. its input [g, u], given dA.
+
+    d/dg [g * s] = s + a*g*s*(1-s) = s*(1 + a*g*(1-s)) with s = sigmoid(a*g);
+    dL/dg = dA * u * s*(1 + a*g*(1-s)),  dL/du = dA * g*s.
+    """
+    a = GLU_ALPHA[activation]
+    F = H1.shape[1] // 2
+    g, u = H1[:, :F], H1[:, F:]
+    s = _sigmoid(a * g)
+    dg = dA * u * s * (1.0 + a * g * (1.0 - s))
+    du = dA * g * s
+    return np.concatenate([dg, du], axis=1)
+
+
+def swiglu(H1: np.ndarray) -> np.ndarray:
+    """A = silu(g) * u (``glu`` with SiLU)."""
+    return glu(H1, "swiglu")
 
 
 def swiglu_backward(dA: np.ndarray, H1: np.ndarray) -> np.ndarray:
-    """Gradient of ``swiglu`` w.r.t. its input [g, u], given dA.
-
-    d silu(g)/dg = s + g*s*(1-s) = s*(1 + g*(1-s)) with s = sigmoid(g);
-    dL/dg = dA * u * s*(1 + g*(1-s)),  dL/du = dA * g*s.
-    """
-    F = H1.shape[1] // 2
-    g, u = H1[:, :F], H1[:, F:]
-    s = _sigmoid(g)
-    dg = dA * u * s * (1.0 + g * (1.0 - s))
-    du = dA * g * s
-    return np.concatenate([dg, du], axis=1)
+    """Gradient of ``swiglu`` w.r.t. [g, u] (``glu_backward`` with SiLU)."""
+    return glu_backward(dA, H1, "swiglu")
 
 
 # ---------------------------------------------------------------- combine
@@ -203,7 +225,8 @@ def prob_grad(dOut: np.ndarray, Yp: np.ndarray, row_of_slot, T: int, k: int) -> 
     out_t = sum_j prob[t, j] * Yp[row(t, j)] is linear in each prob[t, j], so
     dL/dprob[t, j] = <dOut_t, Yp[row(t, j)]> (0 for a slot without a row).
     The probabilities are taken as given: the router that produced them is
-    outside the layer.
+    outside the layer. (The same pairing of a token-major row with a permuted
+    row gives the pre-FC1 form <x_t, dXp[row(t, j)]>.)
     """
     dO = _as_f64(dOut)
     rows = np.asarray(row_of_slot, dtype=np.int64).reshape(T, k)
@@ -216,100 +239,149 @@ def prob_grad(dOut: np.ndarray, Yp: np.ndarray, row_of_slot, T: int, k: int) -> 
     return dp
 
 
-def moe_forward(x, idx, prob, W1, W2, E: int, P: int = 1, faithful: bool = False):
+PROB_MODES = ("combine", "activation", "pre_fc1")
+
+
+def moe_forward(x, idx, prob, W1, W2, E: int, P: int = 1, faithful: bool = False,
+                activation: str = "swiglu", prob_mode: str = "combine"):
     """Forward of the expert layer. Returns a dict of every intermediate.
 
-    Steps: permute -> FC1 (grouped) -> SwiGLU -> FC2 (grouped) -> weighted
-    combine. With ``faithful`` the values are rounded to BF16 where the GPU
-    path stores BF16 (H1, A, Yp, out).
+    Steps: permute -> FC1 (grouped) -> gated activation -> FC2 (grouped) ->
+    combine, with the routing probability p of each (token, slot) pair applied
+    at one of the three places PR #6828 ("What does this PR do?") names:
+      "combine":    out_t = sum_j p * Yp[row]          (A = act, Yp = FC2(A));
+      "activation": A = p * act(H1) (the weighted gated activation), the
+                    combine sums Yp unweighted; FC2 is linear and bias-free, so
+                    this is the same function as "combine";
+      "pre_fc1":    Xp[row] = p * x_t before FC1 (a different function), the
+                    combine sums unweighted.
+    With ``faithful`` the values are rounded to BF16 where the GPU path stores
+    BF16 (Xp, H1, A, Yp, out).
     """
+    if prob_mode not in PROB_MODES:
+        raise ValueError(prob_mode)
     rnd = round_to_bf16 if faithful else (lambda v: v)
     idx = np.asarray(idx)
     T = _as_f64(x).shape[0]
     k = idx.shape[1] if idx.ndim == 2 else 1
     Xp, offsets, row_of_slot, slot_of_row, prob_of_row = permute(x, idx, prob, E, P)
+    if prob_mode == "pre_fc1":
+        Xp = rnd(prob_of_row[:, None] * Xp)
     H1 = rnd(grouped_linear(Xp, W1, offsets))
-    A = rnd(swiglu(H1))
+    act = glu(H1, activation)
+    A = rnd(prob_of_row[:, None] * act if prob_mode == "activation" else act)
     Yp = rnd(grouped_linear(A, W2, offsets))
-    out = rnd(combine(Yp, row_of_slot, prob, T, k))
+    out = rnd(combine(Yp, row_of_slot, prob if prob_mode == "combine" else None, T, k))
     return dict(Xp=Xp, offsets=offsets, row_of_slot=row_of_slot, slot_of_row=slot_of_row,
-                prob_of_row=prob_of_row, H1=H1, A=A, Yp=Yp, out=out, T=T, k=k, E=E, P=P)
+                prob_of_row=prob_of_row, H1=H1, A=A, Yp=Yp, out=out, T=T, k=k, E=E, P=P,
+                x=_as_f64(x), prob=np.asarray(prob, dtype=np.float64).reshape(T, k),
+                activation=activation, prob_mode=prob_mode)
 
 
 def moe_backward(dOut, fwd: dict, W1, W2, faithful: bool = False):
-    """Input gradient dX of ``moe_forward`` (weights are frozen: no dW).
+    """Input gradient dX of ``moe_forward`` (weights are frozen: no dW), and the
+    routing-probability gradient dprob.
 
-    dYp[r] = dOut[t] for the pair (t, j) of row r (0 on padding); the pair's
-    probability scales FC2's input gradient: dA = p_r * (dYp @ W2_e);
-    dH = SwiGLU'(H1) applied to dA; dXp = dH @ W1_e; dX[t] = sum_j dXp[row(t, j)].
-    Also the routing-probability gradient dprob[t, j] = <dOut_t, Yp[row(t, j)]>
-    (``prob_grad``). With ``faithful`` the values are rounded to BF16 where the
-    GPU path stores BF16 (dH, dXp, dX); dprob is kept in fp32 there.
+    dYp[r] = dOut[t] for the pair (t, j) of row r (0 on padding). The gradient
+    w.r.t. the activation output is dA = p_r * (dYp @ W2_e) ("combine" and
+    "activation": the probability multiplies the activation or the FC2 output)
+    or dYp @ W2_e ("pre_fc1"); dH = act'(H1) applied to dA; dXp = dH @ W1_e;
+    dX[t] = sum_j dXp[row(t, j)], weighted by p for "pre_fc1".
+    dprob[t, j] = <dOut_t, FC2(act(H1))[row]> for "combine" / "activation"
+    (``prob_grad``: the FC2 output is linear in p) and <x_t, dXp[row]> for
+    "pre_fc1" (Xp[row] = p * x_t). With ``faithful`` the values are rounded to
+    BF16 where the GPU path stores BF16 (dH, dXp, dX); dprob stays fp32.
     """
     rnd = round_to_bf16 if faithful else (lambda v: v)
     dO = _as_f64(dOut)
     T, k = fwd["T"], fwd["k"]
+    act_name, mode = fwd["activation"], fwd["prob_mode"]
     slot_of_row = fwd["slot_of_row"]
     offsets = fwd["offsets"]
+    p_row = fwd["prob_of_row"][:, None]
     live = slot_of_row >= 0
     dYp = np.zeros((slot_of_row.size, dO.shape[1]), dtype=np.float64)
     dYp[live] = dO[slot_of_row[live] // k]
-    dA = fwd["prob_of_row"][:, None] * grouped_linear_t(dYp, W2, offsets)
-    dH = rnd(swiglu_backward(dA, fwd["H1"]))
+    # gradient w.r.t. the activation output act(H1): p * (dYp @ W2_e) unless p
+    # was applied before FC1
+    dact = grouped_linear_t(dYp, W2, offsets)
+    dA = dact if mode == "pre_fc1" else p_row * dact
+    dH = rnd(glu_backward(dA, fwd["H1"], act_name))
     dXp = rnd(grouped_linear_t(dH, W1, offsets))
-    dX = rnd(combine(dXp, fwd["row_of_slot"], None, T, k))
-    dprob = prob_grad(dO, fwd["Yp"], fwd["row_of_slot"], T, k)
+    if mode == "pre_fc1":
+        # Xp[row] = p * x_t: dX_t = sum_j p * dXp[row], dprob = <x_t, dXp[row]>
+        dX = rnd(combine(dXp, fwd["row_of_slot"], fwd["prob"], T, k))
+        dprob = prob_grad(fwd["x"], dXp, fwd["row_of_slot"], T, k)
+    else:
+        dX = rnd(combine(dXp, fwd["row_of_slot"], None, T, k))
+        # dprob = <dOut_t, FC2 output of the unweighted activation>
+        Yu = fwd["Yp"] if mode == "combine" else grouped_linear(glu(fwd["H1"], act_name), W2,
+                                                                offsets)
+        dprob = prob_grad(dO, Yu, fwd["row_of_slot"], T, k)
     return dict(dYp=dYp, dH=dH, dXp=dXp, dX=dX, dprob=dprob)
 
 
 # ---------------------------------------------------------------- one token
 
-def token_forward(x_t, experts, probs, W1, W2) -> np.ndarray:
-    """Output of one token: sum over its routed experts of p * FC2(SwiGLU(FC1 x)).
+def token_forward(x_t, experts, probs, W1, W2, activation: str = "swiglu",
+                  prob_mode: str = "combine") -> np.ndarray:
+    """Output of one token: sum over its routed experts of FC2(act(FC1 x)) with
+    the probability p applied per ``prob_mode`` (see ``moe_forward``).
 
     ``W1``/``W2`` may be the full [E, ...] BF16 arrays (uint16 bits); only the
     routed experts are converted. Used for sampled checks at full size.
     """
+    al = GLU_ALPHA[activation]
     xt = _as_f64(x_t).reshape(-1)
     y = np.zeros_like(xt)
     for e, p in zip(np.asarray(experts).reshape(-1), np.asarray(probs, dtype=np.float64).reshape(-1)):
         w1 = _as_f64(W1[int(e)])
         w2 = _as_f64(W2[int(e)])
-        h = w1 @ xt
+        h = w1 @ (p * xt if prob_mode == "pre_fc1" else xt)
         F = h.size // 2
-        a = h[:F] * _sigmoid(h[:F]) * h[F:]
-        y += p * (w2 @ a)
+        a = h[:F] * _sigmoid(al * h[:F]) * h[F:]
+        y += (w2 @ a) if prob_mode == "pre_fc1" else p * (w2 @ a)
     return y
 
 
-def token_backward(x_t, dout_t, experts, probs, W1, W2) -> np.ndarray:
+def _token_expert_grads(xt, do, p, w1, w2, al, prob_mode):
+    """For one routed expert of one token: (gradient w.r.t. x_t, dprob)."""
+    xin = p * xt if prob_mode == "pre_fc1" else xt
+    h = w1 @ xin
+    F = h.size // 2
+    g, u = h[:F], h[F:]
+    s = _sigmoid(al * g)
+    dact = do @ w2
+    da = dact if prob_mode == "pre_fc1" else p * dact
+    dh = np.concatenate([da * u * s * (1.0 + al * g * (1.0 - s)), da * g * s])
+    dxin = dh @ w1
+    if prob_mode == "pre_fc1":
+        return p * dxin, float(np.dot(xt, dxin))
+    return dxin, float(np.dot(dact, g * s * u))
+
+
+def token_backward(x_t, dout_t, experts, probs, W1, W2, activation: str = "swiglu",
+                   prob_mode: str = "combine") -> np.ndarray:
     """Input gradient of ``token_forward`` for one token, given dOut[t]."""
     xt = _as_f64(x_t).reshape(-1)
     do = _as_f64(dout_t).reshape(-1)
     dx = np.zeros_like(xt)
     for e, p in zip(np.asarray(experts).reshape(-1), np.asarray(probs, dtype=np.float64).reshape(-1)):
-        w1 = _as_f64(W1[int(e)])
-        w2 = _as_f64(W2[int(e)])
-        h = w1 @ xt
-        F = h.size // 2
-        g, u = h[:F], h[F:]
-        s = _sigmoid(g)
-        da = p * (do @ w2)
-        dh = np.concatenate([da * u * s * (1.0 + g * (1.0 - s)), da * g * s])
-        dx += dh @ w1
+        dx += _token_expert_grads(xt, do, p, _as_f64(W1[int(e)]), _as_f64(W2[int(e)]),
+                                  GLU_ALPHA[activation], prob_mode)[0]
     return dx
 
 
-def token_prob_grad(x_t, dout_t, experts, W1, W2) -> np.ndarray:
-    """dL/dprob of one token's k slots: <dOut_t, FC2(SwiGLU(FC1 x_t))> per expert."""
+def token_prob_grad(x_t, dout_t, experts, W1, W2, activation: str = "swiglu",
+                    prob_mode: str = "combine", probs=None) -> np.ndarray:
+    """dL/dprob of one token's k slots: <dOut_t, FC2(act(FC1 x_t))> per expert, or
+    for "pre_fc1" <x_t, d/dXp> at Xp = p * x_t (``probs`` required there)."""
     xt = _as_f64(x_t).reshape(-1)
     do = _as_f64(dout_t).reshape(-1)
-    out = []
-    for e in np.asarray(experts).reshape(-1):
-        w1 = _as_f64(W1[int(e)])
-        w2 = _as_f64(W2[int(e)])
-        h = w1 @ xt
-        F = h.size // 2
-        a = h[:F] * _sigmoid(h[:F]) * h[F:]
-        out.append(float(np.dot(do, w2 @ a)))
-    return np.asarray(out)
+    ex = np.asarray(experts).reshape(-1)
+    ps = np.ones(ex.size) if probs is None else np.asarray(probs, dtype=np.float64).reshape(-1)
+    if prob_mode == "pre_fc1" and probs is None:
+        raise ValueError("pre_fc1 needs the probabilities")
+    return np.asarray([_token_expert_grads(xt, do, p, _as_f64(W1[int(e)]), _as_f64(W2[int(e)]),
+                                           GLU_ALPHA[activation], prob_mode)[1]
+                       for e, p in zip(ex, ps)])

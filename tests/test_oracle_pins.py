@@ -326,8 +326,10 @@ def test_replacing_one_expert_changes_only_its_tokens():
 
 # ------------------------------------------------------------------ backward
 
-def _torch_forward(x, idx, prob, W1, W2):
-    """The same layer in torch float64 ops, token by token (autograd reference)."""
+def _torch_forward(x, idx, prob, W1, W2, activation="swiglu", prob_mode="combine"):
+    """The same layer in torch float64 ops, token by token (autograd reference).
+    The gate uses torch's own silu for SwiGLU and x * sigmoid(1.702 x) for
+    QuickGeGLU."""
     T, k = idx.shape
     F = W1.shape[1] // 2
     outs = []
@@ -335,9 +337,15 @@ def _torch_forward(x, idx, prob, W1, W2):
         acc = torch.zeros(x.shape[1], dtype=torch.float64)
         for j in range(k):
             e = int(idx[t, j])
-            h = W1[e] @ x[t]
-            a = torch.nn.functional.silu(h[:F]) * h[F:]
-            acc = acc + prob[t, j] * (W2[e] @ a)
+            p = prob[t, j]
+            h = W1[e] @ (p * x[t] if prob_mode == "pre_fc1" else x[t])
+            gate = (torch.nn.functional.silu(h[:F]) if activation == "swiglu"
+                    else h[:F] * torch.sigmoid(1.702 * h[:F]))
+            a = gate * h[F:]
+            if prob_mode == "activation":
+                a = p * a
+            y = W2[e] @ a
+            acc = acc + (p * y if prob_mode == "combine" else y)
         outs.append(acc)
     return torch.stack(outs)
 
@@ -432,3 +440,122 @@ def test_faithful_mode_error_budget_config1():
         rel = np.linalg.norm(a - b) / np.linalg.norm(b)
         assert rel < 5e-3, rel
         assert np.all(np.abs(a - b) <= 1e-2 * np.abs(b) + 1e-3)
+
+
+# ------------------------------------------------------------------ activation and
+# probability variants (QuickGeGLU; probability at the activation or before FC1)
+
+@pytest.mark.parametrize("activation", ["swiglu", "qgeglu"])
+@pytest.mark.parametrize("prob_mode", ["combine", "activation", "pre_fc1"])
+def test_variants_match_torch_autograd(activation, prob_mode):
+    shape = CONFIGS[1].with_tokens(16)
+    inp = make_inputs(shape, 1000)
+    inp.W1[:] = normal_bf16(np.random.default_rng(5), inp.W1.shape, 0.2)
+    inp.W2[:] = normal_bf16(np.random.default_rng(6), inp.W2.shape, 0.2)
+    inp.x[:] = normal_bf16(np.random.default_rng(8), inp.x.shape, 1.0)
+    fwd = oracle.moe_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, shape.E, 2,
+                             activation=activation, prob_mode=prob_mode)
+    bwd = oracle.moe_backward(inp.dOut, fwd, inp.W1, inp.W2)
+    x = torch.from_numpy(_val(inp.x)).requires_grad_(True)
+    p = torch.from_numpy(inp.prob.astype(np.float64)).requires_grad_(True)
+    out = _torch_forward(x, inp.idx, p, torch.from_numpy(_val(inp.W1)),
+                         torch.from_numpy(_val(inp.W2)), activation, prob_mode)
+    np.testing.assert_allclose(fwd["out"], out.detach().numpy(), rtol=1e-11, atol=1e-14)
+    out.backward(torch.from_numpy(_val(inp.dOut)))
+    np.testing.assert_allclose(bwd["dX"], x.grad.numpy(), rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(bwd["dprob"], p.grad.numpy(), rtol=1e-10, atol=1e-13)
+    for t in (0, 7, 15):
+        y = oracle.token_forward(inp.x[t], inp.idx[t], inp.prob[t], inp.W1, inp.W2, activation,
+                                 prob_mode)
+        np.testing.assert_allclose(y, out.detach().numpy()[t], rtol=1e-11, atol=1e-14)
+        dx = oracle.token_backward(inp.x[t], inp.dOut[t], inp.idx[t], inp.prob[t], inp.W1,
+                                   inp.W2, activation, prob_mode)
+        np.testing.assert_allclose(dx, x.grad.numpy()[t], rtol=1e-10, atol=1e-13)
+        dp = oracle.token_prob_grad(inp.x[t], inp.dOut[t], inp.idx[t], inp.W1, inp.W2,
+                                    activation, prob_mode, probs=inp.prob[t])
+        np.testing.assert_allclose(dp, p.grad.numpy()[t], rtol=1e-10, atol=1e-13)
+
+
+@pytest.mark.parametrize("activation", ["swiglu", "qgeglu"])
+def test_probability_at_activation_is_the_combine_function(activation):
+    # FC2 is linear and bias-free: p * FC2(act) = FC2(p * act), so both
+    # placements give the same output and gradients (exact arithmetic).
+    shape = CONFIGS[1]
+    inp = make_inputs(shape, 1000)
+    res = []
+    for mode in ("combine", "activation"):
+        f = oracle.moe_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, shape.E, 1,
+                               activation=activation, prob_mode=mode)
+        b = oracle.moe_backward(inp.dOut, f, inp.W1, inp.W2)
+        res.append((f["out"], b["dX"], b["dprob"]))
+    for a, b in zip(*res):  # equal up to fp64 rounding order
+        np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-12 * np.max(np.abs(b)))
+
+
+def test_qgeglu_identity_weights_closed_form():
+    shape = CONFIGS[1]
+    inp = make_inputs(shape, 1000, with_weights=False)
+    W1, W2, F = _identity_weights(shape.E, shape.H)
+    fwd = oracle.moe_forward(inp.x, inp.idx, inp.prob, W1, W2, shape.E, 1, activation="qgeglu")
+    xv = _val(inp.x)
+    sig = 1.0 / (1.0 + np.exp(-1.702 * xv))
+    psum = inp.prob.astype(np.float64).sum(axis=1, keepdims=True)
+    np.testing.assert_allclose(fwd["out"], psum * xv * sig * xv, rtol=1e-13, atol=0)
+    bwd = oracle.moe_backward(inp.dOut, fwd, W1, W2)
+    dv = _val(inp.dOut)
+    # d/dx [x * sigmoid(1.702 x) * x] = 2 x s + 1.702 x^2 s (1 - s)
+    deriv = 2 * xv * sig + 1.702 * xv * xv * sig * (1 - sig)
+    np.testing.assert_allclose(bwd["dX"], psum * dv * deriv, rtol=1e-12, atol=1e-300)
+
+
+def test_qgeglu_backward_matches_finite_differences():
+    rng = np.random.default_rng(13)
+    H1 = rng.standard_normal((3, 8)) * 2
+    dA = rng.standard_normal((3, 4))
+    ana = oracle.glu_backward(dA, H1, "qgeglu")
+    eps = 1e-6
+    num = np.zeros_like(H1)
+    for i in range(H1.shape[0]):
+        for j in range(H1.shape[1]):
+            hp, hm = H1.copy(), H1.copy()
+            hp[i, j] += eps
+            hm[i, j] -= eps
+            num[i, j] = np.sum(dA * (oracle.glu(hp, "qgeglu") - oracle.glu(hm, "qgeglu"))) / (2 * eps)
+    np.testing.assert_allclose(ana, num, rtol=1e-7, atol=1e-9)
+    # a planted wrong slope (SiLU's derivative on the QuickGELU gate) is caught
+    assert not np.allclose(oracle.glu_backward(dA, H1, "swiglu"), num, rtol=1e-3)
+
+
+def test_pre_fc1_gradients_match_finite_differences():
+    E, H, F, T, k = 3, 5, 3, 4, 2
+    rng = np.random.default_rng(17)
+    x = rng.standard_normal((T, H))
+    W1 = rng.standard_normal((E, 2 * F, H)) * 0.7
+    W2 = rng.standard_normal((E, H, F)) * 0.7
+    idx = np.array([[0, 2], [1, 0], [2, 1], [0, 1]], np.int32)
+    prob = rng.uniform(0.2, 1.0, (T, k))
+    dOut = rng.standard_normal((T, H))
+    kw = dict(activation="qgeglu", prob_mode="pre_fc1")
+    fwd = oracle.moe_forward(x, idx, prob, W1, W2, E, 1, **kw)
+    bwd = oracle.moe_backward(dOut, fwd, W1, W2)
+    eps = 1e-6
+
+    def loss(xx, pp):
+        return np.sum(dOut * oracle.moe_forward(xx, idx, pp, W1, W2, E, 1, **kw)["out"])
+
+    num_x = np.zeros_like(x)
+    for t in range(T):
+        for c in range(H):
+            xp, xm = x.copy(), x.copy()
+            xp[t, c] += eps
+            xm[t, c] -= eps
+            num_x[t, c] = (loss(xp, prob) - loss(xm, prob)) / (2 * eps)
+    num_p = np.zeros_like(prob)
+    for t in range(T):
+        for j in range(k):
+            pp, pm = prob.copy(), prob.copy()
+            pp[t, j] += eps
+            pm[t, j] -= eps
+            num_p[t, j] = (loss(x, pp) - loss(x, pm)) / (2 * eps)
+    np.testing.assert_allclose(bwd["dX"], num_x, rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(bwd["dprob"], num_p, rtol=1e-6, atol=1e-8)
