@@ -87,10 +87,16 @@ typedef enum gg_status {
   GG_ERR_DEVICE_TIMEOUT = 19         /* a bounded in-kernel wait gave up */
 } gg_status;
 
+/* Epilogues. The gated activations ([P4] "What does this PR do?": fused
+ * SwiGLU or QuickGeGLU, GLU interleaving disabled) are act(g) * u with
+ * act(g) = g * sigmoid(alpha * g): alpha = 1 (SwiGLU) or 1.702 (QuickGeGLU,
+ * the QuickGELU gate; the page names it without a formula). */
 typedef enum gg_epilogue {
   GG_EPI_NONE = 0,        /* store the BF16-rounded accumulator */
   GG_EPI_SWIGLU = 1,      /* gg_grouped_fwd only: fused SwiGLU, see below */
-  GG_EPI_SWIGLU_BWD = 2   /* gg_grouped_dgrad only: fused SwiGLU backward */
+  GG_EPI_SWIGLU_BWD = 2,  /* gg_grouped_dgrad only: fused SwiGLU backward */
+  GG_EPI_QGEGLU = 3,      /* gg_grouped_fwd only: fused QuickGeGLU */
+  GG_EPI_QGEGLU_BWD = 4   /* gg_grouped_dgrad only: fused QuickGeGLU backward */
 } gg_epilogue;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -185,14 +191,17 @@ gg_status gg_permute_noalloc(const gg_bf16* x, const int32_t* idx, const float* 
  *   dst[row_of_slot[t*k+j]] = src[t] for every pair with a row, and (when
  *   pad_multiple > 1) zero on the padding rows below offsets[E] (slot -1);
  *   rows >= offsets[E] are left untouched.
- * src[T][H], dst[R_cap][H] BF16; k <= 32. The probability is NOT applied
- * here; the dgrad FC2 epilogue applies it (prob_of_row) because FC2 is
- * linear. A row map entry outside [-1, R_cap) sets GG_ERR_DEVICE_BAD_ROW.
+ * src[T][H], dst[R_cap][H] BF16; k <= 32. With prob NULL the probability
+ * is not applied (the dgrad FC2 epilogue applies it, FC2 being linear); with
+ * prob[T][k] fp32 each copy is scaled, dst[row] = bf16(prob[t][j] * src[t])
+ * in fp32 — the optional pre-FC1 probability multiply ([P4] "What does this
+ * PR do?"). A row map entry outside [-1, R_cap) sets GG_ERR_DEVICE_BAD_ROW.
  * ------------------------------------------------------------------------- */
 gg_status gg_permute_rows(const gg_bf16* src, const int32_t* row_of_slot,
                           const int32_t* slot_of_row, const int32_t* offsets,
                           int T, int H, int k, int E, int pad_multiple, int R_cap,
-                          gg_bf16* dst, void* ws, size_t ws_bytes, gg_stream_t stream);
+                          const float* prob, gg_bf16* dst, void* ws, size_t ws_bytes,
+                          gg_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * gg_grouped_fwd — grouped GEMM over all experts in one persistent launch
@@ -210,6 +219,10 @@ gg_status gg_permute_rows(const gg_bf16* src, const int32_t* row_of_slot,
  *                  computed in fp32 from the rounded g and u, and, when
  *                  H1_save is not NULL, H1_save[R_cap][2F] = [g, u] (kept
  *                  for the backward pass).
+ *   GG_EPI_QGEGLU: the same with g * sigmoid(1.702 g) in place of silu(g).
+ *   prob_of_row (nullable, gated epilogues only): the weighted activation
+ *                  ([P4]: the probability at the fused-activation boundary),
+ *                  C[r][j] = bf16(prob_of_row[r] * act(g) * u) in fp32.
  * Rows outside [0, offsets[E]) are never written. Results of a row depend
  * only on that row and its expert's weights (bitwise batch invariance).
  * Offsets that are not monotone, do not start at 0 or end past R_cap set
@@ -217,7 +230,7 @@ gg_status gg_permute_rows(const gg_bf16* src, const int32_t* row_of_slot,
  * ------------------------------------------------------------------------- */
 gg_status gg_grouped_fwd(const gg_bf16* A, const gg_bf16* B, const int32_t* offsets,
                          int E, int R_cap, int K, int N, gg_epilogue epi,
-                         gg_bf16* C, gg_bf16* H1_save,
+                         gg_bf16* C, gg_bf16* H1_save, const float* prob_of_row,
                          void* ws, size_t ws_bytes, gg_stream_t stream);
 
 /* ---------------------------------------------------------------------------
@@ -228,6 +241,13 @@ gg_status gg_grouped_fwd(const gg_bf16* A, const gg_bf16* B, const int32_t* offs
  * ------------------------------------------------------------------------- */
 gg_status gg_swiglu(const gg_bf16* H1, const int32_t* offsets, int E, int R_cap,
                     int F, gg_bf16* A, gg_stream_t stream);
+
+/* gg_glu — the unfused gated activation of either kind (epi = GG_EPI_SWIGLU
+ * or GG_EPI_QGEGLU), optionally weighted by prob_of_row (nullable), bitwise
+ * identical to the matching gg_grouped_fwd epilogue:
+ *   A[r][j] = bf16([prob_of_row[r] *] act(H1[r][j]) * H1[r][F + j]). */
+gg_status gg_glu(const gg_bf16* H1, const int32_t* offsets, int E, int R_cap, int F,
+                 gg_epilogue epi, const float* prob_of_row, gg_bf16* A, gg_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * gg_grouped_dgrad — input gradient of gg_grouped_fwd through the same
@@ -244,12 +264,16 @@ gg_status gg_swiglu(const gg_bf16* H1, const int32_t* offsets, int E, int R_cap,
  *                    dA[r][j]     = bf16(acc * u * s * (1 + g * (1 - s)))
  *                    dA[r][F + j] = bf16(acc * g * s)
  *                  so dA is [R_cap][2F] (the gradient w.r.t. FC1's output).
- *   rowdot (nullable, GG_EPI_SWIGLU_BWD only): partial sums for the routing-
+ *   GG_EPI_QGEGLU_BWD: the same with s = sigmoid(1.702 g) and the gate
+ *                  derivative s * (1 + 1.702 * g * (1 - s)).
+ *   rowdot (nullable, gated backward epilogues only): partial sums for the routing-
  *                  probability gradient ([P4] "What does this PR do?": the
  *                  probability multiplies the expert output at the combine,
  *                  so its gradient is <dOut_t, Yp[r]> = <dC[r] * W_e, A[r]>
- *                  for the FC2 weight W_e and SwiGLU output A). With a[r][j]
- *                  = bf16(silu(g) * u) (the forward's A, same arithmetic) and
+ *                  for the FC2 weight W_e and activation output A). With
+ *                  a[r][j] = bf16(act(g) * u) (the forward's unweighted A,
+ *                  same arithmetic; also right when the forward weighted the
+ *                  activation, whose output is linear in the probability) and
  *                  the accumulator taken BEFORE the prob_of_row scale:
  *                    rowdot[r][b] = sum_{128b <= j < min(128b + 128, F)} acc[r][j] * a[r][j]
  *                  in fp32 (any order), for b < gg_rowdot_blocks(K); layout
@@ -290,7 +314,7 @@ int gg_rowdot_stride(int F);
 gg_status gg_grouped_fwd_gather(const gg_bf16* src, int T, const int32_t* slot_of_row, int k,
                                 const gg_bf16* B, const int32_t* offsets,
                                 int E, int R_cap, int K, int N, gg_epilogue epi,
-                                gg_bf16* C, gg_bf16* H1_save,
+                                gg_bf16* C, gg_bf16* H1_save, const float* prob_of_row,
                                 void* ws, size_t ws_bytes, gg_stream_t stream);
 
 gg_status gg_grouped_dgrad_gather(const gg_bf16* src, int T, const int32_t* slot_of_row, int k,
@@ -308,18 +332,23 @@ gg_status gg_grouped_dgrad_gather(const gg_bf16* src, int T, const int32_t* slot
  * gives the unweighted sum (the input-gradient combine). Pairs whose row is
  * -1 contribute nothing. Yp[R_cap][H], out[T][H] BF16; k <= 32. A row outside
  * [-1, R_cap) sets GG_ERR_DEVICE_BAD_ROW and is skipped.
- * dprob (nullable): the routing-probability gradient from the partial sums
- * of gg_grouped_dgrad's `rowdot` ([R_cap][stride] fp32 with stride =
- * n_rowdot rounded up to a multiple of 8, n_rowdot >= 1, 32-byte aligned):
- *   dprob[t*k+j] = sum_{b < n_rowdot} rowdot[row_of_slot[t*k+j]][b]
- * in fp32, b ascending; 0 for a pair without a row. rowdot must be non-NULL
- * when dprob is; both NULL (n_rowdot ignored) skips it.
+ * dprob (nullable): the routing-probability gradient, from exactly one of
+ *   rowdot (the partial sums of gg_grouped_dgrad's `rowdot`, [R_cap][stride]
+ *     fp32 with stride = n_rowdot rounded up to a multiple of 8,
+ *     n_rowdot >= 1, 32-byte aligned):
+ *       dprob[t*k+j] = sum_{b < n_rowdot} rowdot[row_of_slot[t*k+j]][b]
+ *     in fp32, b ascending;
+ *   dot_src (token-major [T][H] BF16, the pre-FC1 form: Xp = prob * x):
+ *       dprob[t*k+j] = <dot_src[t], Yp[row_of_slot[t*k+j]]>
+ *     in fp32 (fixed order);
+ * and 0 for a pair without a row. dprob NULL requires rowdot and dot_src
+ * NULL (n_rowdot ignored).
  * ------------------------------------------------------------------------- */
 gg_status gg_unpermute_combine(const gg_bf16* Yp, const int32_t* row_of_slot,
                                const float* prob, int T, int k, int H, int R_cap,
                                gg_bf16* out, const float* rowdot, int n_rowdot,
-                               float* dprob, void* ws, size_t ws_bytes,
-                               gg_stream_t stream);
+                               const gg_bf16* dot_src, float* dprob, void* ws,
+                               size_t ws_bytes, gg_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Whole expert layer. The caller owns one device buffer that holds every
@@ -368,6 +397,41 @@ gg_status gg_moe_mlp_bwd(const gg_bf16* dOut, const gg_bf16* W1, const gg_bf16* 
                          int T, int H, int F, int k, int E, int pad_multiple,
                          gg_bf16* dX, float* dprob, const gg_moe_buffers* buf,
                          gg_stream_t stream);
+
+/* Layer options ([P4] "What does this PR do?"): the gated activation and the
+ * place where the routing probability p of a (token, slot) pair is applied. */
+typedef enum gg_activation {
+  GG_ACT_SWIGLU = 0,      /* silu(g) * u                                   */
+  GG_ACT_QGEGLU = 1       /* g * sigmoid(1.702 g) * u                      */
+} gg_activation;
+typedef enum gg_prob_mode {
+  GG_PROB_COMBINE = 0,    /* out_t = sum_j p * FC2(act): gg_moe_mlp_fwd     */
+  GG_PROB_ACTIVATION = 1, /* A = p * act (weighted activation), out_t =
+                             sum_j FC2(A): the same function, rounded once
+                             more inside FC2's input                       */
+  GG_PROB_PRE_FC1 = 2     /* Xp = p * x before FC1, out_t = sum_j FC2(act):
+                             a different function                          */
+} gg_prob_mode;
+typedef struct gg_moe_options {
+  int activation;         /* gg_activation */
+  int prob_mode;          /* gg_prob_mode  */
+} gg_moe_options;
+
+/* gg_moe_mlp_fwd / gg_moe_mlp_bwd with options (NULL = SwiGLU, probability
+ * at the combine: the calls above). The backward needs the forward's x and
+ * prob for GG_PROB_PRE_FC1 (dX_t = sum_j p * dXp[row], dprob = <x_t,
+ * dXp[row]>); they are ignored (may be NULL) otherwise. Returns
+ * GG_ERR_INVALID_ARG for an unknown activation or mode. */
+gg_status gg_moe_mlp_fwd_ex(const gg_bf16* x, const int32_t* idx, const float* prob,
+                            const gg_bf16* W1, const gg_bf16* W2,
+                            int T, int H, int F, int k, int E, int pad_multiple,
+                            const gg_moe_options* opt, gg_bf16* out,
+                            const gg_moe_buffers* buf, gg_stream_t stream);
+gg_status gg_moe_mlp_bwd_ex(const gg_bf16* dOut, const gg_bf16* x, const float* prob,
+                            const gg_bf16* W1, const gg_bf16* W2,
+                            int T, int H, int F, int k, int E, int pad_multiple,
+                            const gg_moe_options* opt, gg_bf16* dX, float* dprob,
+                            const gg_moe_buffers* buf, gg_stream_t stream);
 
 /* Test hook for the bounded waits: one CTA waits on a barrier that nothing
  * completes, gives up after `limit_ns` nanoseconds (clamped to 1 s), writes

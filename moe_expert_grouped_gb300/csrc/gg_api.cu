@@ -164,8 +164,8 @@ gg_status gg_permute(const gg_bf16* x, const int32_t* idx, const float* prob, in
 
 gg_status gg_permute_rows(const gg_bf16* src, const int32_t* row_of_slot,
                           const int32_t* slot_of_row, const int32_t* offsets, int T, int H, int k,
-                          int E, int pad_multiple, int R_cap, gg_bf16* dst, void* ws,
-                          size_t ws_bytes, gg_stream_t stream) {
+                          int E, int pad_multiple, int R_cap, const float* prob, gg_bf16* dst,
+                          void* ws, size_t ws_bytes, gg_stream_t stream) {
   if (T < 0 || H <= 0 || k <= 0 || k > 32 || E <= 0 || R_cap < 0 || pad_multiple <= 0)
     return GG_ERR_INVALID_ARG;
   if (E > kMaxExperts || H % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
@@ -179,7 +179,7 @@ gg_status gg_permute_rows(const gg_bf16* src, const int32_t* row_of_slot,
   DeviceInfo dev;
   if ((s = device_ok(&dev)) != GG_OK) return s;
   return from_cuda(launch_gather_rows(src, row_of_slot, slot_of_row, offsets, H, k, E, R_cap, T,
-                                      pad_multiple > 1, dst, status_ptr(ws), dev.sm_count,
+                                      pad_multiple > 1, prob, dst, status_ptr(ws), dev.sm_count,
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -194,20 +194,31 @@ static gg_status gemm_common_checks(const gg_bf16* A, const gg_bf16* B, const in
   return check_ws(ws, ws_bytes, kWsHeader);
 }
 
+static gg_status fwd_epilogue_checks(gg_epilogue epi, int N, const gg_bf16* H1_save,
+                                     const float* prob_of_row) {
+  const bool gated = epi == GG_EPI_SWIGLU || epi == GG_EPI_QGEGLU;
+  if (epi != GG_EPI_NONE && !gated) return GG_ERR_INVALID_ARG;
+  if (!gated && (H1_save != nullptr || prob_of_row != nullptr)) return GG_ERR_INVALID_ARG;
+  if (gated && N % 128 != 0) return GG_ERR_UNSUPPORTED_SHAPE;  // F % 64
+  if (!aligned16(H1_save)) return GG_ERR_MISALIGNED;
+  return GG_OK;
+}
+
 gg_status gg_grouped_fwd(const gg_bf16* A, const gg_bf16* B, const int32_t* offsets, int E,
                          int R_cap, int K, int N, gg_epilogue epi, gg_bf16* C, gg_bf16* H1_save,
-                         void* ws, size_t ws_bytes, gg_stream_t stream) {
+                         const float* prob_of_row, void* ws, size_t ws_bytes,
+                         gg_stream_t stream) {
   gg_status s = gemm_common_checks(A, B, offsets, E, R_cap, K, N, C, ws, ws_bytes);
   if (s != GG_OK) return s;
-  if (epi != GG_EPI_NONE && epi != GG_EPI_SWIGLU) return GG_ERR_INVALID_ARG;
-  if (epi == GG_EPI_NONE && H1_save != nullptr) return GG_ERR_INVALID_ARG;
-  if (epi == GG_EPI_SWIGLU && N % 128 != 0) return GG_ERR_UNSUPPORTED_SHAPE;  // F % 64
-  if (!aligned16(H1_save)) return GG_ERR_MISALIGNED;
+  if ((s = fwd_epilogue_checks(epi, N, H1_save, prob_of_row)) != GG_OK) return s;
   DeviceInfo dev;
   if ((s = device_ok(&dev)) != GG_OK) return s;
   if (R_cap == 0) return GG_OK;
   GemmArgs a{};
-  a.mode = epi == GG_EPI_SWIGLU ? kFwdSwiglu : kFwdPlain;
+  a.mode = epi == GG_EPI_NONE     ? kFwdPlain
+           : epi == GG_EPI_QGEGLU ? kFwdQgeglu
+                                  : kFwdSwiglu;
+  a.row_scale = prob_of_row;
   a.A = A;
   a.B = B;
   a.offsets = offsets;
@@ -228,21 +239,29 @@ gg_status gg_grouped_fwd(const gg_bf16* A, const gg_bf16* B, const int32_t* offs
 
 gg_status gg_swiglu(const gg_bf16* H1, const int32_t* offsets, int E, int R_cap, int F,
                     gg_bf16* A, gg_stream_t stream) {
+  return gg_glu(H1, offsets, E, R_cap, F, GG_EPI_SWIGLU, nullptr, A, stream);
+}
+
+gg_status gg_glu(const gg_bf16* H1, const int32_t* offsets, int E, int R_cap, int F,
+                 gg_epilogue epi, const float* prob_of_row, gg_bf16* A, gg_stream_t stream) {
   if (E <= 0 || R_cap < 0 || F <= 0) return GG_ERR_INVALID_ARG;
+  if (epi != GG_EPI_SWIGLU && epi != GG_EPI_QGEGLU) return GG_ERR_INVALID_ARG;
   if (H1 == nullptr || offsets == nullptr || A == nullptr) return GG_ERR_INVALID_ARG;
   if (E > kMaxExperts || F % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(H1) || !aligned16(A)) return GG_ERR_MISALIGNED;
   DeviceInfo dev;
   gg_status s = device_ok(&dev);
   if (s != GG_OK) return s;
-  return from_cuda(launch_swiglu(H1, offsets, E, R_cap, F, A, dev.sm_count,
+  return from_cuda(launch_swiglu(H1, offsets, E, R_cap, F, glu_alpha(epi), prob_of_row, A,
+                                 dev.sm_count,
                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
 static gg_status dgrad_epilogue_checks(gg_epilogue epi, const gg_bf16* H1, const float* rowdot) {
-  if (epi != GG_EPI_NONE && epi != GG_EPI_SWIGLU_BWD) return GG_ERR_INVALID_ARG;
-  if (epi == GG_EPI_NONE && (H1 != nullptr || rowdot != nullptr)) return GG_ERR_INVALID_ARG;
-  if (epi == GG_EPI_SWIGLU_BWD && H1 == nullptr) return GG_ERR_INVALID_ARG;
+  const bool gated = epi == GG_EPI_SWIGLU_BWD || epi == GG_EPI_QGEGLU_BWD;
+  if (epi != GG_EPI_NONE && !gated) return GG_ERR_INVALID_ARG;
+  if (!gated && (H1 != nullptr || rowdot != nullptr)) return GG_ERR_INVALID_ARG;
+  if (gated && H1 == nullptr) return GG_ERR_INVALID_ARG;
   if (!aligned16(H1) || (reinterpret_cast<uintptr_t>(rowdot) & 31u) != 0) return GG_ERR_MISALIGNED;
   return GG_OK;
 }
@@ -258,7 +277,9 @@ gg_status gg_grouped_dgrad(const gg_bf16* dC, const gg_bf16* B, const int32_t* o
   if ((s = device_ok(&dev)) != GG_OK) return s;
   if (R_cap == 0) return GG_OK;
   GemmArgs a{};
-  a.mode = epi == GG_EPI_SWIGLU_BWD ? kDgradSwigluBwd : kDgradPlain;
+  a.mode = epi == GG_EPI_NONE         ? kDgradPlain
+           : epi == GG_EPI_QGEGLU_BWD ? kDgradQgegluBwd
+                                      : kDgradSwigluBwd;
   a.A = dC;
   a.B = B;
   a.offsets = offsets;
@@ -287,22 +308,23 @@ static gg_status gather_checks(const gg_bf16* src, int T, const int32_t* slot_of
 
 gg_status gg_grouped_fwd_gather(const gg_bf16* src, int T, const int32_t* slot_of_row, int k,
                                 const gg_bf16* B, const int32_t* offsets, int E, int R_cap, int K,
-                                int N, gg_epilogue epi, gg_bf16* C, gg_bf16* H1_save, void* ws,
-                                size_t ws_bytes, gg_stream_t stream) {
+                                int N, gg_epilogue epi, gg_bf16* C, gg_bf16* H1_save,
+                                const float* prob_of_row, void* ws, size_t ws_bytes,
+                                gg_stream_t stream) {
   gg_status s = gather_checks(src, T, slot_of_row, k);
   if (s != GG_OK) return s;
   // the source stands in for A in the common checks
   s = gemm_common_checks(src, B, offsets, E, R_cap, K, N, C, ws, ws_bytes);
   if (s != GG_OK) return s;
-  if (epi != GG_EPI_NONE && epi != GG_EPI_SWIGLU) return GG_ERR_INVALID_ARG;
-  if (epi == GG_EPI_NONE && H1_save != nullptr) return GG_ERR_INVALID_ARG;
-  if (epi == GG_EPI_SWIGLU && N % 128 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned16(H1_save)) return GG_ERR_MISALIGNED;
+  if ((s = fwd_epilogue_checks(epi, N, H1_save, prob_of_row)) != GG_OK) return s;
   DeviceInfo dev;
   if ((s = device_ok(&dev)) != GG_OK) return s;
   if (R_cap == 0 || T == 0) return GG_OK;
   GemmArgs a{};
-  a.mode = epi == GG_EPI_SWIGLU ? kFwdSwiglu : kFwdPlain;
+  a.mode = epi == GG_EPI_NONE     ? kFwdPlain
+           : epi == GG_EPI_QGEGLU ? kFwdQgeglu
+                                  : kFwdSwiglu;
+  a.row_scale = prob_of_row;
   a.B = B;
   a.offsets = offsets;
   a.E = E;
@@ -338,7 +360,9 @@ gg_status gg_grouped_dgrad_gather(const gg_bf16* src, int T, const int32_t* slot
   if ((s = device_ok(&dev)) != GG_OK) return s;
   if (R_cap == 0 || T == 0) return GG_OK;
   GemmArgs a{};
-  a.mode = epi == GG_EPI_SWIGLU_BWD ? kDgradSwigluBwd : kDgradPlain;
+  a.mode = epi == GG_EPI_NONE         ? kDgradPlain
+           : epi == GG_EPI_QGEGLU_BWD ? kDgradQgegluBwd
+                                      : kDgradSwigluBwd;
   a.B = B;
   a.offsets = offsets;
   a.E = E;
@@ -364,14 +388,17 @@ gg_status gg_grouped_dgrad_gather(const gg_bf16* src, int T, const int32_t* slot
 
 gg_status gg_unpermute_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const float* prob,
                                int T, int k, int H, int R_cap, gg_bf16* out, const float* rowdot,
-                               int n_rowdot, float* dprob, void* ws, size_t ws_bytes,
-                               gg_stream_t stream) {
+                               int n_rowdot, const gg_bf16* dot_src, float* dprob, void* ws,
+                               size_t ws_bytes, gg_stream_t stream) {
   if (T < 0 || k <= 0 || k > 32 || H <= 0 || R_cap < 0) return GG_ERR_INVALID_ARG;
   if (H % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
   if (T > 0 && (Yp == nullptr || row_of_slot == nullptr || out == nullptr))
     return GG_ERR_INVALID_ARG;
-  if (dprob != nullptr && (rowdot == nullptr || n_rowdot <= 0)) return GG_ERR_INVALID_ARG;
-  if (dprob == nullptr && rowdot != nullptr) return GG_ERR_INVALID_ARG;
+  // dprob needs exactly one source: the partial sums or the token-major rows
+  if (dprob != nullptr && (rowdot != nullptr) == (dot_src != nullptr)) return GG_ERR_INVALID_ARG;
+  if (dprob != nullptr && rowdot != nullptr && n_rowdot <= 0) return GG_ERR_INVALID_ARG;
+  if (dprob == nullptr && (rowdot != nullptr || dot_src != nullptr)) return GG_ERR_INVALID_ARG;
+  if (!aligned16(dot_src)) return GG_ERR_MISALIGNED;
   if ((reinterpret_cast<uintptr_t>(rowdot) & 31u) != 0) return GG_ERR_MISALIGNED;
   if (!aligned16(Yp) || !aligned16(out)) return GG_ERR_MISALIGNED;
   gg_status s = check_ws(ws, ws_bytes, kWsHeader);
@@ -379,8 +406,9 @@ gg_status gg_unpermute_combine(const gg_bf16* Yp, const int32_t* row_of_slot, co
   DeviceInfo dev;
   if ((s = device_ok(&dev)) != GG_OK) return s;
   return from_cuda(launch_combine(Yp, row_of_slot, prob, T, k, H, R_cap, out, rowdot,
-                                  dprob != nullptr ? n_rowdot : 0, dprob, status_ptr(ws),
-                                  dev.sm_count, reinterpret_cast<cudaStream_t>(stream)));
+                                  rowdot != nullptr ? n_rowdot : 0, dot_src, dprob,
+                                  status_ptr(ws), dev.sm_count,
+                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
 // ------------------------------------------------------------------ composite
@@ -446,13 +474,28 @@ static gg_status check_buffers(const gg_moe_buffers* b, int T, int k, int E) {
   return check_ws(b->ws, b->ws_bytes, gg_workspace_size(T, k, E));
 }
 
-gg_status gg_moe_mlp_fwd(const gg_bf16* x, const int32_t* idx, const float* prob,
-                         const gg_bf16* W1, const gg_bf16* W2, int T, int H, int F, int k, int E,
-                         int pad_multiple, gg_bf16* out, const gg_moe_buffers* buf,
-                         gg_stream_t stream) {
+static gg_status read_options(const gg_moe_options* opt, gg_epilogue* fwd_epi,
+                              gg_epilogue* bwd_epi, int* mode) {
+  const int act = opt != nullptr ? opt->activation : GG_ACT_SWIGLU;
+  *mode = opt != nullptr ? opt->prob_mode : GG_PROB_COMBINE;
+  if (act != GG_ACT_SWIGLU && act != GG_ACT_QGEGLU) return GG_ERR_INVALID_ARG;
+  if (*mode != GG_PROB_COMBINE && *mode != GG_PROB_ACTIVATION && *mode != GG_PROB_PRE_FC1)
+    return GG_ERR_INVALID_ARG;
+  *fwd_epi = act == GG_ACT_QGEGLU ? GG_EPI_QGEGLU : GG_EPI_SWIGLU;
+  *bwd_epi = act == GG_ACT_QGEGLU ? GG_EPI_QGEGLU_BWD : GG_EPI_SWIGLU_BWD;
+  return GG_OK;
+}
+
+gg_status gg_moe_mlp_fwd_ex(const gg_bf16* x, const int32_t* idx, const float* prob,
+                            const gg_bf16* W1, const gg_bf16* W2, int T, int H, int F, int k,
+                            int E, int pad_multiple, const gg_moe_options* opt, gg_bf16* out,
+                            const gg_moe_buffers* buf, gg_stream_t stream) {
   if (T < 0 || H <= 0 || k <= 0 || E <= 0 || pad_multiple <= 0) return GG_ERR_INVALID_ARG;
-  gg_status s = check_buffers(buf, T, k, E);
+  gg_epilogue fepi, bepi;
+  int mode;
+  gg_status s = read_options(opt, &fepi, &bepi, &mode);
   if (s != GG_OK) return s;
+  if ((s = check_buffers(buf, T, k, E)) != GG_OK) return s;
   if (W1 == nullptr || W2 == nullptr || F <= 0) return GG_ERR_INVALID_ARG;
   if (F % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
   if (T > 0 && out == nullptr) return GG_ERR_INVALID_ARG;
@@ -460,51 +503,90 @@ gg_status gg_moe_mlp_fwd(const gg_bf16* x, const int32_t* idx, const float* prob
   if (rc > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
   const int R_cap = static_cast<int>(rc);
   if (T > 0 && x == nullptr) return GG_ERR_INVALID_ARG;
-  // The permuted copy of x is written once by a bandwidth-bound gather and
+  // The permuted copy of x is written once by a bandwidth-bound row copy and
   // read by FC1's tile loads: on GB300 this is several times cheaper than
   // four-row TMA gathers inside FC1 (gg_grouped_fwd_gather), which re-gather
-  // every A row once per column block.
-  s = gg_permute(x, idx, prob, T, H, k, E, pad_multiple, buf->Xp, buf->offsets, buf->row_of_slot,
-                 buf->slot_of_row, buf->prob_of_row, buf->ws, buf->ws_bytes, stream);
+  // every A row once per column block. Before FC1 the copy takes the
+  // probability along (GG_PROB_PRE_FC1).
+  const bool pre = mode == GG_PROB_PRE_FC1;
+  s = gg_permute(x, idx, prob, T, H, k, E, pad_multiple, pre ? nullptr : buf->Xp, buf->offsets,
+                 buf->row_of_slot, buf->slot_of_row, buf->prob_of_row, buf->ws, buf->ws_bytes,
+                 stream);
   if (s != GG_OK || T == 0) return s;
-  s = gg_grouped_fwd(buf->Xp, W1, buf->offsets, E, R_cap, H, 2 * F, GG_EPI_SWIGLU, buf->A,
-                     buf->H1, buf->ws, buf->ws_bytes, stream);
+  if (pre) {
+    s = gg_permute_rows(x, buf->row_of_slot, buf->slot_of_row, buf->offsets, T, H, k, E,
+                        pad_multiple, R_cap, prob, buf->Xp, buf->ws, buf->ws_bytes, stream);
+    if (s != GG_OK) return s;
+  }
+  s = gg_grouped_fwd(buf->Xp, W1, buf->offsets, E, R_cap, H, 2 * F, fepi, buf->A, buf->H1,
+                     mode == GG_PROB_ACTIVATION ? buf->prob_of_row : nullptr, buf->ws,
+                     buf->ws_bytes, stream);
   if (s != GG_OK) return s;
   s = gg_grouped_fwd(buf->A, W2, buf->offsets, E, R_cap, F, H, GG_EPI_NONE, buf->Yp, nullptr,
-                     buf->ws, buf->ws_bytes, stream);
+                     nullptr, buf->ws, buf->ws_bytes, stream);
   if (s != GG_OK) return s;
-  return gg_unpermute_combine(buf->Yp, buf->row_of_slot, prob, T, k, H, R_cap, out, nullptr, 0,
-                              nullptr, buf->ws, buf->ws_bytes, stream);
+  return gg_unpermute_combine(buf->Yp, buf->row_of_slot, mode == GG_PROB_COMBINE ? prob : nullptr,
+                              T, k, H, R_cap, out, nullptr, 0, nullptr, nullptr, buf->ws,
+                              buf->ws_bytes, stream);
 }
 
-gg_status gg_moe_mlp_bwd(const gg_bf16* dOut, const gg_bf16* W1, const gg_bf16* W2, int T, int H,
-                         int F, int k, int E, int pad_multiple, gg_bf16* dX, float* dprob,
-                         const gg_moe_buffers* buf, gg_stream_t stream) {
+gg_status gg_moe_mlp_fwd(const gg_bf16* x, const int32_t* idx, const float* prob,
+                         const gg_bf16* W1, const gg_bf16* W2, int T, int H, int F, int k, int E,
+                         int pad_multiple, gg_bf16* out, const gg_moe_buffers* buf,
+                         gg_stream_t stream) {
+  return gg_moe_mlp_fwd_ex(x, idx, prob, W1, W2, T, H, F, k, E, pad_multiple, nullptr, out, buf,
+                           stream);
+}
+
+gg_status gg_moe_mlp_bwd_ex(const gg_bf16* dOut, const gg_bf16* x, const float* prob,
+                            const gg_bf16* W1, const gg_bf16* W2, int T, int H, int F, int k,
+                            int E, int pad_multiple, const gg_moe_options* opt, gg_bf16* dX,
+                            float* dprob, const gg_moe_buffers* buf, gg_stream_t stream) {
   if (T < 0 || H <= 0 || k <= 0 || E <= 0 || pad_multiple <= 0 || F <= 0)
     return GG_ERR_INVALID_ARG;
-  gg_status s = check_buffers(buf, T, k, E);
+  gg_epilogue fepi, bepi;
+  int mode;
+  gg_status s = read_options(opt, &fepi, &bepi, &mode);
   if (s != GG_OK) return s;
+  if ((s = check_buffers(buf, T, k, E)) != GG_OK) return s;
   if (W1 == nullptr || W2 == nullptr) return GG_ERR_INVALID_ARG;
   if (F % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
   if (T == 0) return GG_OK;
   if (dOut == nullptr || dX == nullptr) return GG_ERR_INVALID_ARG;
-  float* rowdot = dprob != nullptr ? buf->rowdot : nullptr;
+  const bool pre = mode == GG_PROB_PRE_FC1;
+  if (pre && (prob == nullptr || (dprob != nullptr && x == nullptr))) return GG_ERR_INVALID_ARG;
   const long long rc = r_cap_of(T, k, E, pad_multiple);
   if (rc > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
   const int R_cap = static_cast<int>(rc);
+  float* rowdot = dprob != nullptr && !pre ? buf->rowdot : nullptr;
   s = gg_permute_rows(dOut, buf->row_of_slot, buf->slot_of_row, buf->offsets, T, H, k, E,
-                      pad_multiple, R_cap, buf->dYp, buf->ws, buf->ws_bytes, stream);
+                      pad_multiple, R_cap, nullptr, buf->dYp, buf->ws, buf->ws_bytes, stream);
   if (s != GG_OK) return s;
-  // dH = SwiGLU'(H1) applied to prob_of_row * (dYp @ W2_e), W2 being [E][H][F]
-  s = gg_grouped_dgrad(buf->dYp, W2, buf->offsets, E, R_cap, F, H, GG_EPI_SWIGLU_BWD, buf->H1,
-                       buf->prob_of_row, buf->dH, rowdot, buf->ws, buf->ws_bytes, stream);
+  // dH = act'(H1) applied to [prob_of_row *] (dYp @ W2_e), W2 being [E][H][F]:
+  // the probability scales the activation's gradient unless it was applied
+  // before FC1
+  s = gg_grouped_dgrad(buf->dYp, W2, buf->offsets, E, R_cap, F, H, bepi, buf->H1,
+                       pre ? nullptr : buf->prob_of_row, buf->dH, rowdot, buf->ws,
+                       buf->ws_bytes, stream);
   if (s != GG_OK) return s;
   // dXp = dH @ W1_e; W1 is [E][2F][H]
   s = gg_grouped_dgrad(buf->dH, W1, buf->offsets, E, R_cap, H, 2 * F, GG_EPI_NONE, nullptr,
                        nullptr, buf->dXp, nullptr, buf->ws, buf->ws_bytes, stream);
   if (s != GG_OK) return s;
+  if (pre)  // Xp = prob * x: dX = sum_j prob * dXp[row], dprob = <x_t, dXp[row]>
+    return gg_unpermute_combine(buf->dXp, buf->row_of_slot, prob, T, k, H, R_cap, dX, nullptr, 0,
+                                dprob != nullptr ? x : nullptr, dprob, buf->ws, buf->ws_bytes,
+                                stream);
   return gg_unpermute_combine(buf->dXp, buf->row_of_slot, nullptr, T, k, H, R_cap, dX, rowdot,
-                              gg_rowdot_blocks(F), dprob, buf->ws, buf->ws_bytes, stream);
+                              gg_rowdot_blocks(F), nullptr, dprob, buf->ws, buf->ws_bytes,
+                              stream);
+}
+
+gg_status gg_moe_mlp_bwd(const gg_bf16* dOut, const gg_bf16* W1, const gg_bf16* W2, int T, int H,
+                         int F, int k, int E, int pad_multiple, gg_bf16* dX, float* dprob,
+                         const gg_moe_buffers* buf, gg_stream_t stream) {
+  return gg_moe_mlp_bwd_ex(dOut, nullptr, nullptr, W1, W2, T, H, F, k, E, pad_multiple, nullptr,
+                           dX, dprob, buf, stream);
 }
 
 gg_status gg_selftest_bounded_wait(void* ws, size_t ws_bytes, uint64_t limit_ns,

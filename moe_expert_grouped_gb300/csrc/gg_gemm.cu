@@ -192,6 +192,11 @@ template <int MODE, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     const __grid_constant__ CUtensorMap mapB, const KParams p) {
+  // gated epilogues: act(g) * u with act(g) = g * sigmoid(kAlpha * g)
+  constexpr bool kGatedFwd = MODE == kFwdSwiglu || MODE == kFwdQgeglu;
+  constexpr bool kGatedBwd = MODE == kDgradSwigluBwd || MODE == kDgradQgegluBwd;
+  constexpr bool kDgrad = MODE == kDgradPlain || kGatedBwd;
+  constexpr float kAlpha = (MODE == kFwdQgeglu || MODE == kDgradQgegluBwd) ? 1.702f : 1.0f;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -322,7 +327,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
           if (!GATHER) tma_load_2d_pair(sa, &mapA, fb, kb * BK, row0);
           if (MODE == kFwdPlain) {
             tma_load_3d_pair(sb, &mapB, fb, kb * BK, nt * BN + h * (BN / 2), e);
-          } else if (MODE == kFwdSwiglu) {
+          } else if (kGatedFwd) {
             // half 0: gate rows j0.., half 1: up rows F + j0..
             tma_load_3d_pair(sb, &mapB, fb, kb * BK, h * p.F + nt * (BN / 2), e);
           } else {
@@ -359,7 +364,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------ MMA issuer (even CTA)
-      constexpr bool kMN = (MODE == kDgradPlain || MODE == kDgradSwigluBwd);
+      constexpr bool kMN = kDgrad;
       constexpr uint32_t idesc = make_idesc_bf16(kCluster * BM, BN, kMN);
       int stage = 0;
       uint32_t phase = 0;
@@ -437,8 +442,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
           pack_bf16x32(v, scale, w);
           store_chunk(stg, w, crow + c, valid);
         }
-      } else if (MODE == kFwdSwiglu) {
+      } else if (kGatedFwd) {
         const int F = p.F;
+        constexpr float alpha = kAlpha;
+        const bool scaled = p.row_scale != nullptr;  // weighted activation
+        const float prow = scaled && valid ? p.row_scale[grow] : 1.0f;
         const int j0 = nt * (BN / 2);
         const int c0 = half * (BN / 4);
         gg_bf16* arow = p.C + grow * F + j0;
@@ -465,11 +473,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             store_chunk(stg, w, hrow + F + c, valid);
           }
 #pragma unroll
-          for (int i = 0; i < 32; ++i) g[i] = silu_mul(g[i], u[i]);
+          for (int i = 0; i < 32; ++i) g[i] = glu_mul(g[i], u[i], alpha, scaled, prow);
           pack_bf16x32(g, 1.0f, w);
           store_chunk(stg, w, arow + c, valid);
         }
-      } else {  // kDgradSwigluBwd: F = Nout, output row [dg | du] of width 2F
+      } else {  // gated backward: F = Nout, output row [dg | du] of width 2F
         const int F = p.Nout;
         float scale = 1.0f;
         if (p.row_scale != nullptr && valid) scale = p.row_scale[grow];
@@ -490,6 +498,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
         float rdot = 0.0f;  // this row's <acc, a> over this warp's columns
         const bool want_dot = p.rowdot != nullptr;
+        constexpr float alpha = kAlpha;
 #pragma unroll 1
         for (int c = c0; c < c_end; c += 32) {
           float v[32];
@@ -513,18 +522,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
           if (want_dot) {
 #pragma unroll
             for (int h = 0; h < 16; ++h) {
-              silu_mul_bwd<true>(v[2 * h], scale, bf16_lo(gs[h]), bf16_lo(us[h]), dg[2 * h],
-                                 du[2 * h], rdot);
-              silu_mul_bwd<true>(v[2 * h + 1], scale, bf16_hi(gs[h]), bf16_hi(us[h]),
-                                 dg[2 * h + 1], du[2 * h + 1], rdot);
+              glu_mul_bwd<true>(v[2 * h], scale, bf16_lo(gs[h]), bf16_lo(us[h]), alpha,
+                                dg[2 * h], du[2 * h], rdot);
+              glu_mul_bwd<true>(v[2 * h + 1], scale, bf16_hi(gs[h]), bf16_hi(us[h]), alpha,
+                                dg[2 * h + 1], du[2 * h + 1], rdot);
             }
           } else {
 #pragma unroll
             for (int h = 0; h < 16; ++h) {
-              silu_mul_bwd<false>(v[2 * h], scale, bf16_lo(gs[h]), bf16_lo(us[h]), dg[2 * h],
-                                  du[2 * h], rdot);
-              silu_mul_bwd<false>(v[2 * h + 1], scale, bf16_hi(gs[h]), bf16_hi(us[h]),
-                                  dg[2 * h + 1], du[2 * h + 1], rdot);
+              glu_mul_bwd<false>(v[2 * h], scale, bf16_lo(gs[h]), bf16_lo(us[h]), alpha,
+                                 dg[2 * h], du[2 * h], rdot);
+              glu_mul_bwd<false>(v[2 * h + 1], scale, bf16_hi(gs[h]), bf16_hi(us[h]), alpha,
+                                 dg[2 * h + 1], du[2 * h + 1], rdot);
             }
           }
           uint4 w[4];
@@ -554,11 +563,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
   cluster_sync();
 }
 
-// Standalone SwiGLU over rows [0, offsets[E]) — same arithmetic as the fused
-// FC1 epilogue (silu_mul on the BF16 values of g and u).
+// Standalone gated activation over rows [0, offsets[E]) — same arithmetic as
+// the fused FC1 epilogue (glu_mul on the BF16 values of g and u).
 __global__ void __launch_bounds__(256)
 swiglu_kernel(const uint4* __restrict__ H1, const int32_t* __restrict__ offsets, int E, int F,
-              uint4* __restrict__ A) {
+              float alpha, const float* __restrict__ row_scale, uint4* __restrict__ A) {
+  const bool scaled = row_scale != nullptr;
   const long long rows = offsets[E];
   const int vec = F / 8;
   const long long n = rows * vec;
@@ -570,11 +580,12 @@ swiglu_kernel(const uint4* __restrict__ H1, const int32_t* __restrict__ offsets,
     const uint4 uw = __ldg(H1 + r * (2LL * vec) + vec + c);
     const uint32_t gs[4] = {gw.x, gw.y, gw.z, gw.w};
     const uint32_t us[4] = {uw.x, uw.y, uw.z, uw.w};
+    const float pr = scaled ? row_scale[r] : 1.0f;
     uint32_t o[4];
 #pragma unroll
     for (int h = 0; h < 4; ++h)
-      o[h] = pack_bf16x2(silu_mul(bf16_lo(gs[h]), bf16_lo(us[h])),
-                         silu_mul(bf16_hi(gs[h]), bf16_hi(us[h])));
+      o[h] = pack_bf16x2(glu_mul(bf16_lo(gs[h]), bf16_lo(us[h]), alpha, scaled, pr),
+                         glu_mul(bf16_hi(gs[h]), bf16_hi(us[h]), alpha, scaled, pr));
     A[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
@@ -674,7 +685,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaSt
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.Kw) * 2,
                                    static_cast<cuuint64_t>(a.Kw) * a.Nw * 2};
     cuuint32_t box[3] = {BK, BN / 2, 1};  // each CTA of a pair loads half of B
-    if (a.mode == kDgradPlain || a.mode == kDgradSwigluBwd) box[1] = 64;
+    if (a.mode == kDgradPlain || a.mode == kDgradSwigluBwd || a.mode == kDgradQgegluBwd)
+      box[1] = 64;
     if (!encode_bf16_map(&mb, a.B, 3, dims, strides, box)) {
       *host_err = GG_ERR_CUDA;
       return cudaErrorInvalidValue;
@@ -704,9 +716,13 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaSt
       return gather ? launch_mode<kFwdPlain, true>(ma, mb, kp, dev, stream)
                     : launch_mode<kFwdPlain, false>(ma, mb, kp, dev, stream);
     case kFwdSwiglu:
+    case kFwdQgeglu:
       kp.F = a.Nout / 2;
       kp.NT = (kp.F + BN / 2 - 1) / (BN / 2);
       kp.ldc = kp.F;
+      if (a.mode == kFwdQgeglu)
+        return gather ? launch_mode<kFwdQgeglu, true>(ma, mb, kp, dev, stream)
+                      : launch_mode<kFwdQgeglu, false>(ma, mb, kp, dev, stream);
       return gather ? launch_mode<kFwdSwiglu, true>(ma, mb, kp, dev, stream)
                     : launch_mode<kFwdSwiglu, false>(ma, mb, kp, dev, stream);
     case kDgradPlain:
@@ -716,9 +732,13 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaSt
       return gather ? launch_mode<kDgradPlain, true>(ma, mb, kp, dev, stream)
                     : launch_mode<kDgradPlain, false>(ma, mb, kp, dev, stream);
     case kDgradSwigluBwd:
+    case kDgradQgegluBwd:
       kp.F = a.Nout;
       kp.NT = (a.Nout + BN - 1) / BN;
       kp.ldc = 2LL * a.Nout;
+      if (a.mode == kDgradQgegluBwd)
+        return gather ? launch_mode<kDgradQgegluBwd, true>(ma, mb, kp, dev, stream)
+                      : launch_mode<kDgradQgegluBwd, false>(ma, mb, kp, dev, stream);
       return gather ? launch_mode<kDgradSwigluBwd, true>(ma, mb, kp, dev, stream)
                     : launch_mode<kDgradSwigluBwd, false>(ma, mb, kp, dev, stream);
   }
@@ -727,14 +747,16 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaSt
 }
 
 cudaError_t launch_swiglu(const gg_bf16* H1, const int32_t* offsets, int E, int R_cap, int F,
-                          gg_bf16* A, int sm_count, cudaStream_t stream) {
+                          float alpha, const float* row_scale, gg_bf16* A, int sm_count,
+                          cudaStream_t stream) {
   if (R_cap <= 0) return cudaSuccess;
   const long long n = static_cast<long long>(R_cap) * (F / 8);
   long long blocks = (n + 255) / 256;
   const long long cap = static_cast<long long>(sm_count) * 8;
   if (blocks > cap) blocks = cap;
   swiglu_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
-      reinterpret_cast<const uint4*>(H1), offsets, E, F, reinterpret_cast<uint4*>(A));
+      reinterpret_cast<const uint4*>(H1), offsets, E, F, alpha, row_scale,
+      reinterpret_cast<uint4*>(A));
   count_launch();
   return cudaGetLastError();
 }

@@ -42,19 +42,21 @@ cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* pr
                            int32_t* status, int32_t* block_hist, int sm_count,
                            cudaStream_t stream);
 
-// dst[row_of_slot[t*k+j]] = src[t]; with has_padding, rows below offsets[E]
-// whose slot_of_row is -1 are zeroed.
+// dst[row_of_slot[t*k+j]] = src[t] (times prob[t*k+j] when prob is not
+// null); with has_padding, rows below offsets[E] whose slot_of_row is -1 are
+// zeroed.
 cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* row_of_slot,
                                const int32_t* slot_of_row, const int32_t* offsets, int H, int k,
-                               int E, int R_cap, int T, bool has_padding, gg_bf16* dst,
-                               int32_t* status, int sm_count, cudaStream_t stream);
+                               int E, int R_cap, int T, bool has_padding, const float* prob,
+                               gg_bf16* dst, int32_t* status, int sm_count, cudaStream_t stream);
 
 // dprob (nullable): dprob[t*k+j] = sum_b rowdot[row_of_slot[t*k+j]][b], rows of
 // rowdot (n_rowdot + 7) / 8 * 8 floats apart.
+// With dot_src (and dprob): dprob[t*k+j] = <dot_src[t], Yp[row_of_slot[t*k+j]]>.
 cudaError_t launch_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const float* prob,
                            int T, int k, int H, int R_cap, gg_bf16* out, const float* rowdot,
-                           int n_rowdot, float* dprob, int32_t* status, int sm_count,
-                           cudaStream_t stream);
+                           int n_rowdot, const gg_bf16* dot_src, float* dprob, int32_t* status,
+                           int sm_count, cudaStream_t stream);
 
 cudaError_t launch_bounded_wait_selftest(int32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
@@ -64,6 +66,8 @@ enum GemmMode : int {
   kFwdSwiglu = 1,
   kDgradPlain = 2,
   kDgradSwigluBwd = 3,
+  kFwdQgeglu = 4,       // kFwdSwiglu with the QuickGELU gate
+  kDgradQgegluBwd = 5,  // kDgradSwigluBwd with the QuickGELU gate
 };
 
 struct GemmArgs {
@@ -78,7 +82,8 @@ struct GemmArgs {
   gg_bf16* C;              // output
   gg_bf16* H1_save;        // fwd SwiGLU: [R_cap][2F] or null
   const gg_bf16* H1;       // dgrad SwiGLU backward: [R_cap][2F]
-  const float* row_scale;  // dgrad: prob_of_row or null
+  const float* row_scale;  // dgrad: prob_of_row; fwd gated epilogue: the weighted
+                           // activation's prob_of_row; or null
   float* rowdot = nullptr; // dgrad SwiGLU backward: [R_cap][stride] partials, or null
   int32_t* status;
   // Gathered A operand: row r of A is gather_src[slot_of_row[r] / gather_k]
@@ -93,6 +98,22 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaSt
                                 gg_status* host_err);
 
 cudaError_t launch_swiglu(const gg_bf16* H1, const int32_t* offsets, int E, int R_cap, int F,
-                          gg_bf16* A, int sm_count, cudaStream_t stream);
+                          float alpha, const float* row_scale, gg_bf16* A, int sm_count,
+                          cudaStream_t stream);
+
+// alpha of the gated activation of a gg_epilogue (1 for SwiGLU, 1.702 for
+// QuickGeGLU), 0 for epilogues without one.
+inline float glu_alpha(gg_epilogue epi) {
+  switch (epi) {
+    case GG_EPI_SWIGLU:
+    case GG_EPI_SWIGLU_BWD:
+      return 1.0f;
+    case GG_EPI_QGEGLU:
+    case GG_EPI_QGEGLU_BWD:
+      return 1.702f;
+    default:
+      return 0.0f;
+  }
+}
 
 }  // namespace gg

@@ -234,6 +234,56 @@ scatter_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ r
   }
 }
 
+// scatter_rows_kernel with the pre-FC1 probability multiply: the copy of
+// token t for pair (t, j) is bf16(prob[t*k+j] * src[t]), the product in fp32.
+__global__ void __launch_bounds__(256)
+scatter_rows_scaled_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ row_of_slot,
+                           const float* __restrict__ prob, int T, int k, int vec_per_row,
+                           int R_cap, uint4* __restrict__ dst, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long t = warp0; t < T; t += nwarps) {
+    int my_row = -1;
+    float my_p = 0.0f;
+    if (lane < k) {
+      my_row = row_of_slot[t * k + lane];
+      my_p = prob[t * k + lane];
+      if (my_row < -1 || my_row >= R_cap) {
+        set_status(status, GG_ERR_DEVICE_BAD_ROW);
+        my_row = -1;
+      }
+    }
+    const uint4* sp = src + t * vec_per_row;
+    for (int c0 = 0; c0 < vec_per_row; c0 += 256) {
+      uint4 a[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = c0 + lane + 32 * i;
+        a[i] = c < vec_per_row ? __ldg(sp + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int row = __shfl_sync(0xFFFFFFFFu, my_row, j & 31);
+        const float pj = __shfl_sync(0xFFFFFFFFu, my_p, j & 31);
+        if (row < 0) continue;
+        uint4* d = dst + static_cast<long long>(row) * vec_per_row;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c = c0 + lane + 32 * i;
+          if (c < vec_per_row) {
+            const uint32_t w[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              o[q] = pack_bf16x2(pj * bf16_lo(w[q]), pj * bf16_hi(w[q]));
+            __stcs(d + c, make_uint4(o[0], o[1], o[2], o[3]));
+          }
+        }
+      }
+    }
+  }
+}
+
 // Zero the padding rows (slot -1) below offsets[E]: each warp checks 32
 // consecutive rows and clears the padding ones together.
 __global__ void __launch_bounds__(256)
@@ -397,6 +447,82 @@ combine_dprob_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ r
   }
 }
 
+// combine_kernel plus the pre-FC1 probability gradient: with Xp[row] =
+// prob * dot_src[t], dprob[t*k+j] = <dot_src[t], Yp[row(t, j)]>. Each lane
+// keeps one partial dot per slot over its columns (x chunk loaded once per
+// pass), reduced across the warp in a fixed butterfly order at the end.
+__global__ void __launch_bounds__(256)
+combine_dot_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row_of_slot,
+                   const float* __restrict__ prob, int T, int k, int vec_per_row, int R_cap,
+                   uint4* __restrict__ out, const uint4* __restrict__ dot_src,
+                   float* __restrict__ dprob, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int warp0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = warp0; t < T; t += nwarps) {
+    int my_row = -1;
+    float my_p = 1.0f;
+    if (lane < k) {
+      my_row = row_of_slot[static_cast<long long>(t) * k + lane];
+      if (prob != nullptr) my_p = prob[static_cast<long long>(t) * k + lane];
+      if (my_row < -1 || my_row >= R_cap) {
+        set_status(status, GG_ERR_DEVICE_BAD_ROW);
+        my_row = -1;
+      }
+    }
+    float dotp[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) dotp[j] = 0.0f;
+    const uint4* xs = dot_src + static_cast<long long>(t) * vec_per_row;
+    for (int c0 = 0; c0 < vec_per_row; c0 += 64) {
+      const int ca = c0 + lane, cb = c0 + 32 + lane;
+      const bool oka = ca < vec_per_row, okb = cb < vec_per_row;
+      const uint4 xa = oka ? __ldg(xs + ca) : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 xb = okb ? __ldg(xs + cb) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      float acc[2][8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[0][i] = acc[1][i] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (j >= k) break;
+        const int row = __shfl_sync(0xFFFFFFFFu, my_row, j);
+        const float pj = __shfl_sync(0xFFFFFFFFu, my_p, j);
+        if (row < 0) continue;  // warp-uniform
+        const uint4* rp = Yp + static_cast<long long>(row) * vec_per_row;
+        const uint4 va = oka ? __ldcs(rp + ca) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 vb = okb ? __ldcs(rp + cb) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t yw[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float ylo = bf16_lo(yw[q]), yhi = bf16_hi(yw[q]);
+          acc[q >> 2][2 * (q & 3)] = __fmaf_rn(pj, ylo, acc[q >> 2][2 * (q & 3)]);
+          acc[q >> 2][2 * (q & 3) + 1] = __fmaf_rn(pj, yhi, acc[q >> 2][2 * (q & 3) + 1]);
+          dotp[j] = __fmaf_rn(bf16_lo(xw[q]), ylo, dotp[j]);
+          dotp[j] = __fmaf_rn(bf16_hi(xw[q]), yhi, dotp[j]);
+        }
+      }
+      uint4* op = out + static_cast<long long>(t) * vec_per_row;
+      if (oka)
+        __stcs(op + ca, make_uint4(pack_bf16x2(acc[0][0], acc[0][1]), pack_bf16x2(acc[0][2], acc[0][3]),
+                                   pack_bf16x2(acc[0][4], acc[0][5]), pack_bf16x2(acc[0][6], acc[0][7])));
+      if (okb)
+        __stcs(op + cb, make_uint4(pack_bf16x2(acc[1][0], acc[1][1]), pack_bf16x2(acc[1][2], acc[1][3]),
+                                   pack_bf16x2(acc[1][4], acc[1][5]), pack_bf16x2(acc[1][6], acc[1][7])));
+    }
+    float mine = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j >= k) break;
+      float v = dotp[j];
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, m);
+      if (lane == j) mine = v;
+    }
+    if (lane < k) dprob[static_cast<long long>(t) * k + lane] = my_row >= 0 ? mine : 0.0f;
+  }
+}
+
 __global__ void bounded_wait_selftest_kernel(int32_t* status, uint64_t limit_ns) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
@@ -445,7 +571,8 @@ cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* pr
   count_launch();
   if (Xp != nullptr) {
     err = launch_gather_rows(x, row_of_slot, slot_of_row, offsets, H, k, E,
-                             static_cast<int>(R_cap), T, P > 1, Xp, status, sm_count, stream);
+                             static_cast<int>(R_cap), T, P > 1, nullptr, Xp, status, sm_count,
+                             stream);
     if (err != cudaSuccess) return err;
   }
   return cudaGetLastError();
@@ -453,8 +580,9 @@ cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* pr
 
 cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* row_of_slot,
                                const int32_t* slot_of_row, const int32_t* offsets, int H, int k,
-                               int E, int R_cap, int T, bool has_padding, gg_bf16* dst,
-                               int32_t* status, int sm_count, cudaStream_t stream) {
+                               int E, int R_cap, int T, bool has_padding, const float* prob,
+                               gg_bf16* dst, int32_t* status, int sm_count,
+                               cudaStream_t stream) {
   if (R_cap <= 0 || T <= 0) return cudaSuccess;
   const int vec = H / 8;
   long long blocks = (static_cast<long long>(T) + 7) / 8;
@@ -463,9 +591,14 @@ cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* row_of_slot,
   // slowly (measured faster than one exactly resident wave).
   const long long cap = static_cast<long long>(sm_count) * 8;
   if (blocks > cap) blocks = cap;
-  scatter_rows_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
-      reinterpret_cast<const uint4*>(src), row_of_slot, T, k, vec, R_cap,
-      reinterpret_cast<uint4*>(dst), status);
+  if (prob != nullptr)
+    scatter_rows_scaled_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+        reinterpret_cast<const uint4*>(src), row_of_slot, prob, T, k, vec, R_cap,
+        reinterpret_cast<uint4*>(dst), status);
+  else
+    scatter_rows_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+        reinterpret_cast<const uint4*>(src), row_of_slot, T, k, vec, R_cap,
+        reinterpret_cast<uint4*>(dst), status);
   count_launch();
   if (has_padding) {
     long long pb = (static_cast<long long>(R_cap) + 255) / 256;
@@ -479,14 +612,18 @@ cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* row_of_slot,
 
 cudaError_t launch_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const float* prob,
                            int T, int k, int H, int R_cap, gg_bf16* out, const float* rowdot,
-                           int n_rowdot, float* dprob, int32_t* status, int sm_count,
-                           cudaStream_t stream) {
+                           int n_rowdot, const gg_bf16* dot_src, float* dprob, int32_t* status,
+                           int sm_count, cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
   const int vec = H / 8;
   long long blocks = (static_cast<long long>(T) + 7) / 8;
   const long long cap = static_cast<long long>(sm_count) * 8;  // as for the row copy
   if (blocks > cap) blocks = cap;
-  if (dprob != nullptr)
+  if (dprob != nullptr && dot_src != nullptr)
+    combine_dot_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+        reinterpret_cast<const uint4*>(Yp), row_of_slot, prob, T, k, vec, R_cap,
+        reinterpret_cast<uint4*>(out), reinterpret_cast<const uint4*>(dot_src), dprob, status);
+  else if (dprob != nullptr)
     combine_dprob_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
         reinterpret_cast<const uint4*>(Yp), row_of_slot, prob, T, k, vec, R_cap,
         reinterpret_cast<uint4*>(out), rowdot, n_rowdot, dprob, status);

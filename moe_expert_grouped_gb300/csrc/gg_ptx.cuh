@@ -277,32 +277,35 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 
 // ----------------------------------------------------------------- math
 
-// silu(g) * u in fp32, shared by the fused FC1 epilogue and the standalone
-// SwiGLU kernel (same translation unit, same instructions), so both round
-// alike. The sigmoid uses the fast exponential and divide intrinsics: their
-// relative error (a few fp32 ulp) is far below the BF16 rounding applied to
-// every result.
-__device__ __forceinline__ float silu_mul(float g, float u) {
-  const float s = __fdividef(1.0f, 1.0f + __expf(-g));
-  return (g * s) * u;
+// Gated activation act(g) * u = (g * sigmoid(alpha * g)) * u in fp32, times
+// the row's probability when `scaled` (the weighted activation). alpha = 1 is
+// SwiGLU (alpha * g is then exactly g), 1.702 QuickGeGLU. Shared by the fused
+// FC1 epilogue and the standalone kernel (same translation unit, same
+// instructions), so both round alike. The sigmoid uses the fast exponential
+// and divide intrinsics: their relative error (a few fp32 ulp) is far below
+// the BF16 rounding applied to every result.
+__device__ __forceinline__ float glu_mul(float g, float u, float alpha, bool scaled, float p) {
+  const float s = __fdividef(1.0f, 1.0f + __expf(-(alpha * g)));
+  const float v = (g * s) * u;
+  return scaled ? v * p : v;
 }
 
 __device__ __forceinline__ float round_bf16(float x);
 
-// Backward of silu(g) * u at dA = acc * scale: dg = dA * u * silu'(g),
-// du = dA * silu(g), silu'(g) = s * (1 + g * (1 - s)) with s = sigmoid(g).
-// With kDot also dot += acc * bf16(silu(g) * u): the SwiGLU output of the
-// forward pass (same sigmoid and products as silu_mul, so the same BF16
-// value) against the unscaled accumulator, for the routing-probability
-// gradient.
+// Backward of act(g) * u at dA = acc * scale, act(g) = g * s with
+// s = sigmoid(alpha * g): dg = dA * u * s * (1 + alpha * g * (1 - s)),
+// du = dA * g * s. With kDot also dot += acc * bf16(act(g) * u): the
+// unweighted activation output of the forward pass (same sigmoid and
+// products as glu_mul, so the same BF16 value) against the unscaled
+// accumulator, for the routing-probability gradient.
 template <bool kDot>
-__device__ __forceinline__ void silu_mul_bwd(float acc, float scale, float g, float u, float& dg,
-                                             float& du, float& dot) {
+__device__ __forceinline__ void glu_mul_bwd(float acc, float scale, float g, float u, float alpha,
+                                            float& dg, float& du, float& dot) {
   const float dA = acc * scale;
-  const float s = __fdividef(1.0f, 1.0f + __expf(-g));
-  const float dsilu = s * (1.0f + g * (1.0f - s));
+  const float s = __fdividef(1.0f, 1.0f + __expf(-(alpha * g)));
+  const float dact = s * (1.0f + (alpha * g) * (1.0f - s));
   const float gs = g * s;
-  dg = (dA * u) * dsilu;
+  dg = (dA * u) * dact;
   du = dA * gs;
   if (kDot) dot = fmaf(acc, round_bf16(gs * u), dot);
 }

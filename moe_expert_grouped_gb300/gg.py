@@ -19,7 +19,11 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgg.so")
 
 GG_OK = 0
-GG_EPI_NONE, GG_EPI_SWIGLU, GG_EPI_SWIGLU_BWD = 0, 1, 2
+GG_EPI_NONE, GG_EPI_SWIGLU, GG_EPI_SWIGLU_BWD, GG_EPI_QGEGLU, GG_EPI_QGEGLU_BWD = 0, 1, 2, 3, 4
+GG_ACT_SWIGLU, GG_ACT_QGEGLU = 0, 1
+GG_PROB_COMBINE, GG_PROB_ACTIVATION, GG_PROB_PRE_FC1 = 0, 1, 2
+_GATED_FWD = (GG_EPI_SWIGLU, GG_EPI_QGEGLU)
+_GATED_BWD = (GG_EPI_SWIGLU_BWD, GG_EPI_QGEGLU_BWD)
 STATUS_NAMES = {
     0: "GG_OK", 1: "GG_ERR_INVALID_ARG", 2: "GG_ERR_UNSUPPORTED_SHAPE", 3: "GG_ERR_MISALIGNED",
     4: "GG_ERR_WORKSPACE_TOO_SMALL", 5: "GG_ERR_UNSUPPORTED_DEVICE", 6: "GG_ERR_CUDA",
@@ -37,20 +41,24 @@ SIGNATURES = [
     ("gg_clear_status", _I, [_P, _P]),
     ("gg_read_status", _I, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     ("gg_permute", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P]),
-    ("gg_permute_rows", _I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
-    ("gg_grouped_fwd", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
+    ("gg_permute_rows", _I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
+    ("gg_grouped_fwd", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     ("gg_swiglu", _I, [_P, _P, _I, _I, _I, _P, _P]),
+    ("gg_glu", _I, [_P, _P, _I, _I, _I, _I, _P, _P, _P]),
     ("gg_grouped_dgrad", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
     ("gg_rowdot_blocks", _I, [_I]),
     ("gg_rowdot_stride", _I, [_I]),
-    ("gg_unpermute_combine", _I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _Z, _P]),
+    ("gg_unpermute_combine", _I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _Z, _P]),
     ("gg_moe_buffers_size", _Z, [_I, _I, _I, _I, _I, _I]),
     ("gg_moe_buffers_bind", _I, [_P, _Z, _I, _I, _I, _I, _I, _I, _P]),
     ("gg_moe_mlp_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     ("gg_moe_mlp_bwd", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    ("gg_moe_mlp_fwd_ex", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    ("gg_moe_mlp_bwd_ex", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     ("gg_selftest_bounded_wait", _I, [_P, _Z, _U64, _P]),
     ("gg_permute_noalloc", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
-    ("gg_grouped_fwd_gather", _I, [_P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
+    ("gg_grouped_fwd_gather", _I,
+     [_P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     ("gg_grouped_dgrad_gather", _I,
      [_P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
 ]
@@ -62,6 +70,12 @@ class GGBuffers(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "Xp", "H1", "A", "Yp", "dYp", "dH", "dXp", "offsets", "row_of_slot", "slot_of_row",
         "prob_of_row", "rowdot", "ws")] + [("ws_bytes", ctypes.c_size_t)]
+
+
+class GGOptions(ctypes.Structure):
+    """Mirror of struct gg_moe_options."""
+
+    _fields_ = [("activation", ctypes.c_int), ("prob_mode", ctypes.c_int)]
 
 
 class GGError(RuntimeError):
@@ -172,35 +186,39 @@ def permute(x, idx, prob, E: int, P: int = 1, ws=None, out=None):
 
 
 def permute_rows(src, row_of_slot, slot_of_row, offsets, k: int, E: int, P: int, R_cap: int, ws,
-                 dst=None):
-    """gg_permute_rows: dst[row_of_slot[t*k+j]] = src[t] (0 on padding rows)."""
+                 dst=None, prob=None):
+    """gg_permute_rows: dst[row_of_slot[t*k+j]] = src[t] (times prob[t, j] when given;
+    0 on padding rows)."""
     T, H = src.shape
     dst = torch.empty((R_cap, H), dtype=torch.bfloat16, device=src.device) if dst is None else dst
     _check(LIB.gg_permute_rows(_ptr(src), _ptr(row_of_slot), _ptr(slot_of_row), _ptr(offsets), T,
-                               H, k, E, P, R_cap, _ptr(dst), _ptr(ws), ws.numel(),
+                               H, k, E, P, R_cap, _ptr(prob), _ptr(dst), _ptr(ws), ws.numel(),
                                _stream(src.device)),
            "gg_permute_rows")
     return dst
 
 
-def grouped_fwd(A, B, offsets, epilogue: int = GG_EPI_NONE, ws=None, C=None, H1_save=None):
-    """gg_grouped_fwd. B is [E, N, K]; returns C ([R_cap, N] or [R_cap, N/2])."""
+def grouped_fwd(A, B, offsets, epilogue: int = GG_EPI_NONE, ws=None, C=None, H1_save=None,
+                prob_of_row=None):
+    """gg_grouped_fwd. B is [E, N, K]; returns C ([R_cap, N] or, gated, [R_cap, N/2]);
+    prob_of_row weights a gated activation."""
     R_cap, K = A.shape
     E, N, Kb = B.shape
     if Kb != K:
         raise ValueError("A and B disagree on K")
     dev = A.device
-    ncols = N // 2 if epilogue == GG_EPI_SWIGLU else N
+    ncols = N // 2 if epilogue in _GATED_FWD else N
     C = torch.empty((R_cap, ncols), dtype=torch.bfloat16, device=dev) if C is None else C
     ws = workspace(0, 1, E, dev) if ws is None else ws
     _check(LIB.gg_grouped_fwd(_ptr(A), _ptr(B), _ptr(offsets), E, R_cap, K, N, epilogue, _ptr(C),
-                              _ptr(H1_save), _ptr(ws), ws.numel(), _stream(dev)),
+                              _ptr(H1_save), _ptr(prob_of_row), _ptr(ws), ws.numel(),
+                              _stream(dev)),
            "gg_grouped_fwd")
     return C
 
 
 def grouped_fwd_gather(src, slot_of_row, k: int, B, offsets, epilogue: int = GG_EPI_NONE,
-                       ws=None, C=None, H1_save=None):
+                       ws=None, C=None, H1_save=None, prob_of_row=None):
     """gg_grouped_fwd_gather: A rows gathered from token-major src [T, K]."""
     T, K = src.shape
     E, N, Kb = B.shape
@@ -208,12 +226,12 @@ def grouped_fwd_gather(src, slot_of_row, k: int, B, offsets, epilogue: int = GG_
         raise ValueError("src and B disagree on K")
     R_cap = slot_of_row.shape[0]
     dev = src.device
-    ncols = N // 2 if epilogue == GG_EPI_SWIGLU else N
+    ncols = N // 2 if epilogue in _GATED_FWD else N
     C = torch.empty((R_cap, ncols), dtype=torch.bfloat16, device=dev) if C is None else C
     ws = workspace(0, 1, E, dev) if ws is None else ws
     _check(LIB.gg_grouped_fwd_gather(_ptr(src), T, _ptr(slot_of_row), k, _ptr(B), _ptr(offsets),
-                                     E, R_cap, K, N, epilogue, _ptr(C), _ptr(H1_save), _ptr(ws),
-                                     ws.numel(), _stream(dev)),
+                                     E, R_cap, K, N, epilogue, _ptr(C), _ptr(H1_save),
+                                     _ptr(prob_of_row), _ptr(ws), ws.numel(), _stream(dev)),
            "gg_grouped_fwd_gather")
     return C
 
@@ -237,7 +255,7 @@ def grouped_dgrad_gather(src, slot_of_row, k: int, B, offsets, epilogue: int = G
         raise ValueError("src and B disagree on N")
     R_cap = slot_of_row.shape[0]
     dev = src.device
-    ncols = 2 * K if epilogue == GG_EPI_SWIGLU_BWD else K
+    ncols = 2 * K if epilogue in _GATED_BWD else K
     dA = torch.empty((R_cap, ncols), dtype=torch.bfloat16, device=dev) if dA is None else dA
     ws = workspace(0, 1, E, dev) if ws is None else ws
     _check(LIB.gg_grouped_dgrad_gather(_ptr(src), T, _ptr(slot_of_row), k, _ptr(B), _ptr(offsets),
@@ -246,6 +264,17 @@ def grouped_dgrad_gather(src, slot_of_row, k: int, B, offsets, epilogue: int = G
                                        _stream(dev)),
            "gg_grouped_dgrad_gather")
     return dA
+
+
+def glu(H1, offsets, E: int, epilogue: int = GG_EPI_SWIGLU, prob_of_row=None, A=None):
+    """gg_glu: the unfused gated activation (SwiGLU or QuickGeGLU), optionally weighted."""
+    R_cap, F2 = H1.shape
+    F = F2 // 2
+    A = torch.empty((R_cap, F), dtype=torch.bfloat16, device=H1.device) if A is None else A
+    _check(LIB.gg_glu(_ptr(H1), _ptr(offsets), E, R_cap, F, epilogue, _ptr(prob_of_row), _ptr(A),
+                      _stream(H1.device)),
+           "gg_glu")
+    return A
 
 
 def swiglu(H1, offsets, E: int, A=None):
@@ -268,7 +297,7 @@ def grouped_dgrad(dC, B, offsets, epilogue: int = GG_EPI_NONE, H1=None, prob_of_
     if Nb != N:
         raise ValueError("dC and B disagree on N")
     dev = dC.device
-    ncols = 2 * K if epilogue == GG_EPI_SWIGLU_BWD else K
+    ncols = 2 * K if epilogue in _GATED_BWD else K
     dA = torch.empty((R_cap, ncols), dtype=torch.bfloat16, device=dev) if dA is None else dA
     ws = workspace(0, 1, E, dev) if ws is None else ws
     _check(LIB.gg_grouped_dgrad(_ptr(dC), _ptr(B), _ptr(offsets), E, R_cap, K, N, epilogue,
@@ -279,13 +308,15 @@ def grouped_dgrad(dC, B, offsets, epilogue: int = GG_EPI_NONE, H1=None, prob_of_
 
 
 def unpermute_combine(Yp, row_of_slot, prob, T: int, k: int, ws, out=None, rowdot=None,
-                      dprob=None, n_rowdot=None):
+                      dprob=None, n_rowdot=None, dot_src=None):
     """gg_unpermute_combine: probability-weighted (prob) or plain (None) sum of k rows;
     with rowdot [R_cap, stride] (and n_rowdot partials per row, default all but
     the padding of the last 8-group: pass n_rowdot when it differs) also
     dprob [T, k] = the sum of each pair's row partials."""
     R_cap, H = Yp.shape
     out = torch.empty((T, H), dtype=torch.bfloat16, device=Yp.device) if out is None else out
+    if dot_src is not None and dprob is None:
+        dprob = torch.empty((T, k), dtype=torch.float32, device=Yp.device)
     if rowdot is not None:
         if n_rowdot is None:
             raise ValueError("n_rowdot (rowdot_blocks(F)) is required with rowdot")
@@ -294,10 +325,10 @@ def unpermute_combine(Yp, row_of_slot, prob, T: int, k: int, ws, out=None, rowdo
         if dprob is None:
             dprob = torch.empty((T, k), dtype=torch.float32, device=Yp.device)
     _check(LIB.gg_unpermute_combine(_ptr(Yp), _ptr(row_of_slot), _ptr(prob), T, k, H, R_cap,
-                                    _ptr(out), _ptr(rowdot), n_rowdot or 0, _ptr(dprob), _ptr(ws),
-                                    ws.numel(), _stream(Yp.device)),
+                                    _ptr(out), _ptr(rowdot), n_rowdot or 0, _ptr(dot_src),
+                                    _ptr(dprob), _ptr(ws), ws.numel(), _stream(Yp.device)),
            "gg_unpermute_combine")
-    return out if rowdot is None else (out, dprob)
+    return out if dprob is None else (out, dprob)
 
 
 def selftest_bounded_wait(ws, limit_ns: int) -> None:
@@ -319,8 +350,11 @@ class MoeLayer:
         "rowdot": ("rc", "nbs"), "ws": ("ws",),
     }
 
-    def __init__(self, T: int, H: int, F: int, k: int, E: int, P: int = 1, device="cuda"):
+    def __init__(self, T: int, H: int, F: int, k: int, E: int, P: int = 1, device="cuda",
+                 activation: int = GG_ACT_SWIGLU, prob_mode: int = GG_PROB_COMBINE):
         self.T, self.H, self.F, self.k, self.E, self.P = T, H, F, k, E, P
+        self.opt = GGOptions(activation, prob_mode)
+        self._saved = None  # the forward's (x, prob): the pre-FC1 backward needs them
         self.R_cap = r_cap(T, k, E, P)
         self.device = torch.device(device)
         n = int(LIB.gg_moe_buffers_size(T, H, F, k, E, P))
@@ -357,9 +391,11 @@ class MoeLayer:
         _need(W1, torch.bfloat16, (E, 2 * F, H), "W1")
         _need(W2, torch.bfloat16, (E, H, F), "W2")
         out = torch.empty((T, H), dtype=torch.bfloat16, device=self.device) if out is None else out
-        _check(LIB.gg_moe_mlp_fwd(_ptr(x), _ptr(idx), _ptr(prob), _ptr(W1), _ptr(W2), T, H, F, k,
-                                  E, self.P, _ptr(out), ctypes.byref(self.buf),
-                                  _stream(self.device)), "gg_moe_mlp_fwd")
+        _check(LIB.gg_moe_mlp_fwd_ex(_ptr(x), _ptr(idx), _ptr(prob), _ptr(W1), _ptr(W2), T, H, F,
+                                     k, E, self.P, ctypes.byref(self.opt), _ptr(out),
+                                     ctypes.byref(self.buf), _stream(self.device)),
+               "gg_moe_mlp_fwd_ex")
+        self._saved = (x, prob)
         return out
 
     def backward(self, dOut, W1, W2, dX=None, dprob=None):
@@ -373,10 +409,12 @@ class MoeLayer:
             dprob = torch.empty((T, k), dtype=torch.float32, device=self.device)
         if want:
             _need(dprob, torch.float32, (T, k), "dprob")
-        _check(LIB.gg_moe_mlp_bwd(_ptr(dOut), _ptr(W1), _ptr(W2), T, H, F, k, E, self.P,
-                                  _ptr(dX), _ptr(dprob) if want else None,
-                                  ctypes.byref(self.buf), _stream(self.device)),
-               "gg_moe_mlp_bwd")
+        x, prob = self._saved if self._saved is not None else (None, None)
+        _check(LIB.gg_moe_mlp_bwd_ex(_ptr(dOut), _ptr(x), _ptr(prob), _ptr(W1), _ptr(W2), T, H, F,
+                                     k, E, self.P, ctypes.byref(self.opt), _ptr(dX),
+                                     _ptr(dprob) if want else None, ctypes.byref(self.buf),
+                                     _stream(self.device)),
+               "gg_moe_mlp_bwd_ex")
         return (dX, dprob) if want else dX
 
     def status(self) -> int:

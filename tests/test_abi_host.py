@@ -102,42 +102,73 @@ def test_validation_rejects_before_launch(gg):
     assert L.gg_permute(mis, p, p, 4, 64, 2, 4, 1, p, p, p, p, p, ws, 1 << 20, None) == 3
     assert L.gg_permute(p, p, p, 4, 64, 2, 4, 1, p, p, p, p, p, ws, 16, None) == 4
     assert L.gg_permute(p, None, p, 4, 64, 2, 4, 1, p, p, p, p, p, ws, 1 << 20, None) == 1
-    # gg_grouped_fwd: K/N not multiples of 64, wrong epilogue, H1_save with NONE
-    assert L.gg_grouped_fwd(p, p, p, 4, 128, 96, 128, 0, p, None, ws, 1024, None) == 2
-    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 100, 0, p, None, ws, 1024, None) == 2
-    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 128, 2, p, None, ws, 1024, None) == 1
-    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 128, 0, p, p, ws, 1024, None) == 1
-    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 192, 1, p, p, ws, 1024, None) == 2
-    assert L.gg_grouped_fwd(mis, p, p, 4, 128, 64, 128, 0, p, None, ws, 1024, None) == 3
-    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 128, 0, p, None, ws, 16, None) == 4
+    # gg_grouped_fwd: K/N not multiples of 64, wrong epilogue, H1_save or prob with NONE
+    assert L.gg_grouped_fwd(p, p, p, 4, 128, 96, 128, 0, p, None, None, ws, 1024, None) == 2
+    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 100, 0, p, None, None, ws, 1024, None) == 2
+    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 128, 2, p, None, None, ws, 1024, None) == 1
+    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 128, 4, p, None, None, ws, 1024, None) == 1
+    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 128, 5, p, None, None, ws, 1024, None) == 1
+    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 128, 0, p, p, None, ws, 1024, None) == 1
+    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 128, 0, p, None, p, ws, 1024, None) == 1
+    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 192, 1, p, p, None, ws, 1024, None) == 2
+    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 192, 3, p, p, None, ws, 1024, None) == 2
+    assert L.gg_grouped_fwd(mis, p, p, 4, 128, 64, 128, 0, p, None, None, ws, 1024, None) == 3
+    assert L.gg_grouped_fwd(p, p, p, 4, 128, 64, 128, 0, p, None, None, ws, 16, None) == 4
     # gg_grouped_dgrad: SwiGLU backward needs H1; NONE must not get H1 or rowdot
     assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 2, None, None, p, None, ws, 1024,
                               None) == 1
     assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 0, p, None, p, None, ws, 1024, None) == 1
     assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 0, None, None, p, p, ws, 1024, None) == 1
     assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 1, p, None, p, None, ws, 1024, None) == 1
+    assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 3, p, None, p, None, ws, 1024, None) == 1
+    assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 4, None, None, p, None, ws, 1024,
+                              None) == 1
     assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 2, p, None, p, mis, ws, 1024, None) == 3
     assert L.gg_grouped_dgrad(p, p, p, 4, 128, 64, 128, 2, p, None, p,
                               ctypes.c_void_p((1 << 40) + 16), ws, 1024, None) == 3
-    # gg_unpermute_combine: k > 32, H % 64, dprob without partial sums (or the reverse)
-    assert L.gg_unpermute_combine(p, p, p, 4, 33, 64, 128, p, None, 0, None, ws, 1024, None) == 1
-    assert L.gg_unpermute_combine(p, p, p, 4, 2, 72, 128, p, None, 0, None, ws, 1024, None) == 2
-    assert L.gg_unpermute_combine(p, p, p, 4, 2, 64, 128, p, None, 2, p, ws, 1024, None) == 1
-    assert L.gg_unpermute_combine(p, p, p, 4, 2, 64, 128, p, p, 0, p, ws, 1024, None) == 1
-    assert L.gg_unpermute_combine(p, p, p, 4, 2, 64, 128, p, p, 2, None, ws, 1024, None) == 1
+    # gg_unpermute_combine: k > 32, H % 64; dprob needs exactly one of the partial
+    # sums or the token-major rows, and neither may come without dprob
+    C = L.gg_unpermute_combine
+    assert C(p, p, p, 4, 33, 64, 128, p, None, 0, None, None, ws, 1024, None) == 1
+    assert C(p, p, p, 4, 2, 72, 128, p, None, 0, None, None, ws, 1024, None) == 2
+    assert C(p, p, p, 4, 2, 64, 128, p, None, 2, None, p, ws, 1024, None) == 1
+    assert C(p, p, p, 4, 2, 64, 128, p, p, 0, None, p, ws, 1024, None) == 1
+    assert C(p, p, p, 4, 2, 64, 128, p, p, 2, None, None, ws, 1024, None) == 1
+    assert C(p, p, p, 4, 2, 64, 128, p, None, 0, p, None, ws, 1024, None) == 1
+    assert C(p, p, p, 4, 2, 64, 128, p, p, 2, p, p, ws, 1024, None) == 1
+    assert C(p, p, p, 4, 2, 64, 128, p, None, 0, mis, p, ws, 1024, None) == 3
     assert L.gg_rowdot_blocks(768) == 6 and L.gg_rowdot_blocks(64) == 2
     assert L.gg_rowdot_blocks(256) == 2 and L.gg_rowdot_blocks(0) == 0
     assert L.gg_rowdot_stride(768) == 8 and L.gg_rowdot_stride(1280) == 16
     assert L.gg_rowdot_stride(0) == 0
     # rowdot must be 32-byte aligned
     mis32 = ctypes.c_void_p((1 << 40) + 16)
-    assert L.gg_unpermute_combine(p, p, p, 4, 2, 64, 128, p, mis32, 2, p, ws, 1024, None) == 3
-    # gg_swiglu: F % 64
+    assert C(p, p, p, 4, 2, 64, 128, p, mis32, 2, None, p, ws, 1024, None) == 3
+    # gg_swiglu / gg_glu: F % 64, only the gated forward epilogues
     assert L.gg_swiglu(p, p, 4, 128, 96, p, None) == 2
+    assert L.gg_glu(p, p, 4, 128, 96, 1, None, p, None) == 2
+    assert L.gg_glu(p, p, 4, 128, 128, 2, None, p, None) == 1
+    assert L.gg_glu(p, p, 4, 128, 128, 0, None, p, None) == 1
     # composites need a full buffer set
     buf = gg.GGBuffers()
     assert L.gg_moe_mlp_fwd(p, p, p, p, p, 4, 64, 128, 2, 4, 1, p, ctypes.byref(buf), None) == 1
     assert L.gg_moe_mlp_bwd(p, p, p, 4, 64, 128, 2, 4, 1, p, None, ctypes.byref(buf), None) == 1
+    # options: unknown activation / probability mode; the pre-FC1 backward needs prob
+    good = gg.GGBuffers()
+    n = L.gg_moe_buffers_size(4, 64, 128, 2, 4, 1)
+    assert L.gg_moe_buffers_bind(ctypes.c_void_p(1 << 40), n, 4, 64, 128, 2, 4, 1,
+                                 ctypes.byref(good)) == 0
+    for act, mode in ((2, 0), (0, 3), (-1, 0)):
+        opt = gg.GGOptions(act, mode)
+        assert L.gg_moe_mlp_fwd_ex(p, p, p, p, p, 4, 64, 128, 2, 4, 1, ctypes.byref(opt), p,
+                                   ctypes.byref(good), None) == 1
+        assert L.gg_moe_mlp_bwd_ex(p, p, p, p, p, 4, 64, 128, 2, 4, 1, ctypes.byref(opt), p, p,
+                                   ctypes.byref(good), None) == 1
+    pre = gg.GGOptions(0, 2)
+    assert L.gg_moe_mlp_bwd_ex(p, p, None, p, p, 4, 64, 128, 2, 4, 1, ctypes.byref(pre), p, None,
+                               ctypes.byref(good), None) == 1
+    assert L.gg_moe_mlp_bwd_ex(p, None, p, p, p, 4, 64, 128, 2, 4, 1, ctypes.byref(pre), p, p,
+                               ctypes.byref(good), None) == 1
     assert L.gg_moe_mlp_fwd(p, p, p, p, p, 4, 64, 128, 2, 4, 1, p, None, None) == 1
     assert L.gg_read_status(None, None, None) == 1
     assert L.gg_clear_status(None, None) == 1

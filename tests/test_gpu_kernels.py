@@ -356,3 +356,124 @@ def test_gathered_gemms_equal_materialised_path(gg, P, T, E, k, H, F):
         torch.cuda.synchronize()
         np.testing.assert_array_equal(torch_to_bits(da[:n]), torch_to_bits(db[:n]))
     assert gg.read_status(ws) == 0
+
+
+# ------------------------------------------------------------------ activation and
+# probability variants: QuickGeGLU, the weighted activation, the pre-FC1 multiply
+
+@pytest.mark.parametrize("epi,act", [(1, "swiglu"), (3, "qgeglu")])
+def test_gated_forward_variants(gg, epi, act):
+    F, K = 320, 192
+    rng = np.random.default_rng(91 + epi)
+    E = len(COUNTS)
+    off = _offsets(COUNTS)
+    R_cap = int(off[-1]) + 8
+    X = normal_bf16(rng, (R_cap, K), 1.0)
+    W1 = normal_bf16(rng, (E, 2 * F, K), 0.08)
+    prob = rng.uniform(0.05, 1.0, R_cap).astype(np.float32)
+    ws = gg.workspace(0, 1, E, "cuda")
+    d_off = torch.from_numpy(off).cuda()
+    d_prob = torch.from_numpy(prob).cuda()
+    n = int(off[-1])
+    h_ref = oracle.grouped_linear(oracle.bf16_bits_to_f64(X), W1, off)
+    h_faith = oracle.round_to_bf16(h_ref)
+    for weighted in (False, True):
+        H1 = _nan_filled((R_cap, 2 * F))
+        A = _nan_filled((R_cap, F))
+        gg.grouped_fwd(bits_to_torch(X), bits_to_torch(W1), d_off, epi, ws=ws, C=A, H1_save=H1,
+                       prob_of_row=d_prob if weighted else None)
+        A2 = gg.glu(H1, d_off, E, epi, prob_of_row=d_prob if weighted else None,
+                    A=_nan_filled((R_cap, F)))
+        torch.cuda.synchronize()
+        assert gg.read_status(ws) == 0
+        p = prob.astype(np.float64)[:, None] if weighted else 1.0
+        assert_parity(torch_to_f64(H1[:n]), h_ref[:n], "H1", faithful=h_faith[:n])
+        ref = (p * oracle.glu(h_ref, act))[:n]
+        assert_parity(torch_to_f64(A[:n]), ref, "A",
+                      faithful=oracle.round_to_bf16(p * oracle.glu(h_faith, act))[:n])
+        # fused epilogue and the standalone kernel round alike: bitwise equal
+        np.testing.assert_array_equal(torch_to_bits(A[:n]), torch_to_bits(A2[:n]))
+        assert np.all(torch_to_bits(A[n:]) == NAN_BF16)
+
+
+@pytest.mark.parametrize("epi,act", [(2, "swiglu"), (4, "qgeglu")])
+def test_gated_backward_variants(gg, epi, act):
+    F, H = 320, 256
+    rng = np.random.default_rng(97 + epi)
+    E = len(COUNTS)
+    off = _offsets(COUNTS)
+    R_cap = int(off[-1]) + 16
+    dY = normal_bf16(rng, (R_cap, H), 1.0)
+    W2 = normal_bf16(rng, (E, H, F), 0.05)
+    H1 = normal_bf16(rng, (R_cap, 2 * F), 1.5)
+    prob = rng.uniform(0.05, 1.0, R_cap).astype(np.float32)
+    ws = gg.workspace(0, 1, E, "cuda")
+    nb, nbs = gg.rowdot_blocks(F), gg.rowdot_stride(F)
+    rowdot = torch.full((R_cap, nbs), float("nan"), dtype=torch.float32, device="cuda")
+    dH = _nan_filled((R_cap, 2 * F))
+    gg.grouped_dgrad(bits_to_torch(dY), bits_to_torch(W2), torch.from_numpy(off).cuda(), epi,
+                     H1=bits_to_torch(H1), prob_of_row=torch.from_numpy(prob).cuda(), ws=ws,
+                     dA=dH, rowdot=rowdot)
+    torch.cuda.synchronize()
+    assert gg.read_status(ws) == 0
+    n = int(off[-1])
+    acc = oracle.grouped_linear_t(oracle.bf16_bits_to_f64(dY), W2, off)
+    h1 = oracle.bf16_bits_to_f64(H1)
+    ref = oracle.glu_backward(prob.astype(np.float64)[:, None] * acc, h1, act)
+    assert_parity(torch_to_f64(dH[:n]), ref[:n], "dH", faithful=oracle.round_to_bf16(ref[:n]))
+    prod = acc * oracle.round_to_bf16(oracle.glu(h1, act))
+    ref_rd = np.stack([prod[:, 128 * b:128 * (b + 1)].sum(axis=1) for b in range(nb)], axis=1)
+    assert_parity(rowdot.cpu().numpy().astype(np.float64)[:n, :nb], ref_rd[:n], "rowdot")
+
+
+def test_permute_rows_scaled_by_probability(gg):
+    # the pre-FC1 multiply: dst[row] = bf16(prob * x) with the product in fp32,
+    # bit-exact against the same fp32 product rounded on the host
+    T, H, E, k, P = 300, 256, 8, 3, 16
+    idx, prob = _permute_case(T, E, k, 33)
+    rng = np.random.default_rng(5)
+    x = normal_bf16(rng, (T, H), 1.0)
+    p = gg.permute(bits_to_torch(x), torch.from_numpy(idx).cuda(), torch.from_numpy(prob).cuda(),
+                   E, P)
+    R_cap = p["Xp"].shape[0]
+    dst = _nan_filled((R_cap, H))
+    gg.permute_rows(bits_to_torch(x), p["row_of_slot"], p["slot_of_row"], p["offsets"], k, E, P,
+                    R_cap, p["ws"], dst=dst, prob=torch.from_numpy(prob).cuda())
+    torch.cuda.synchronize()
+    assert gg.read_status(p["ws"]) == 0
+    xv = oracle.bf16_bits_to_f64(x).astype(np.float32)
+    ros = p["row_of_slot"].cpu().numpy().reshape(T, k)
+    got = torch_to_f64(dst)
+    for t in range(T):
+        for j in range(k):
+            want = oracle.round_to_bf16((np.float32(prob[t, j]) * xv[t]).astype(np.float64))
+            np.testing.assert_array_equal(got[ros[t, j]], want)
+    n = int(p["offsets"][-1].item())
+    pad = p["slot_of_row"].cpu().numpy()[:n] < 0
+    assert np.all(got[:n][pad] == 0)
+
+
+def test_combine_dot_probability_gradient(gg):
+    # dprob[t, j] = <dot_src[t], Yp[row(t, j)]>; the weighted sum itself is
+    # bitwise the plain weighted combine
+    T, k, H, R_cap = 300, 3, 320, 1000
+    rng = np.random.default_rng(43)
+    rows = rng.permutation(R_cap)[:T * k].astype(np.int32)
+    rows[[5, 77, 301]] = -1
+    Yp = normal_bf16(rng, (R_cap, H), 1.0)
+    xs = normal_bf16(rng, (T, H), 1.0)
+    prob = rng.uniform(0, 1, (T, k)).astype(np.float32)
+    ws = gg.workspace(T, k, 1, "cuda")
+    d_rows = torch.from_numpy(rows).cuda()
+    d_prob = torch.from_numpy(prob).cuda()
+    out, dprob = gg.unpermute_combine(bits_to_torch(Yp), d_rows, d_prob, T, k, ws,
+                                      dot_src=bits_to_torch(xs))
+    out2 = gg.unpermute_combine(bits_to_torch(Yp), d_rows, d_prob, T, k, ws)
+    torch.cuda.synchronize()
+    assert gg.read_status(ws) == 0
+    np.testing.assert_array_equal(torch_to_bits(out), torch_to_bits(out2))
+    y = oracle.bf16_bits_to_f64(Yp)
+    ref = oracle.prob_grad(oracle.bf16_bits_to_f64(xs), y, rows, T, k)
+    got = dprob.cpu().numpy().astype(np.float64)
+    assert np.all(got.reshape(-1)[rows < 0] == 0)
+    assert_parity(got, ref, "dprob (dot)")

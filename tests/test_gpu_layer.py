@@ -38,8 +38,9 @@ def _dev(inp):
                 W2=bits_to_torch(inp.W2), dOut=bits_to_torch(inp.dOut))
 
 
-def _run(gg, shape, d, with_dprob=False):
-    layer = gg.MoeLayer(shape.T, shape.H, shape.F, shape.k, shape.E, shape.P)
+def _run(gg, shape, d, with_dprob=False, activation=0, prob_mode=0):
+    layer = gg.MoeLayer(shape.T, shape.H, shape.F, shape.k, shape.E, shape.P,
+                        activation=activation, prob_mode=prob_mode)
     out = layer.forward(d["x"], d["idx"], d["prob"], d["W1"], d["W2"])
     if with_dprob:
         dX, dprob = layer.backward(d["dOut"], d["W1"], d["W2"], dprob=True)
@@ -166,3 +167,30 @@ def test_replacing_one_expert_changes_only_its_tokens(gg):
     np.testing.assert_array_equal(b1[~touched], b2[~touched])
     assert np.all(np.any(b1[touched] != b2[touched], axis=1))
     np.testing.assert_array_equal(torch_to_bits(g1)[~touched], torch_to_bits(g2)[~touched])
+
+
+ACT_NAMES = {0: "swiglu", 1: "qgeglu"}
+MODE_NAMES = {0: "combine", 1: "activation", 2: "pre_fc1"}
+
+
+@pytest.mark.parametrize("activation,prob_mode", [(1, 0), (0, 1), (1, 1), (0, 2), (1, 2)])
+@pytest.mark.parametrize("shape,seed", [(CONFIGS[1], 1000), (MID_PAD, 79)])
+def test_layer_variants_match_oracle(gg, shape, seed, activation, prob_mode):
+    inp = make_inputs(shape, seed)
+    d = _dev(inp)
+    layer, out, dX, dprob = _run(gg, shape, d, with_dprob=True, activation=activation,
+                                 prob_mode=prob_mode)
+    kw = dict(activation=ACT_NAMES[activation], prob_mode=MODE_NAMES[prob_mode])
+    fwd = oracle.moe_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, shape.E, shape.P, **kw)
+    bwd = oracle.moe_backward(inp.dOut, fwd, inp.W1, inp.W2)
+    ffw = oracle.moe_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, shape.E, shape.P,
+                             faithful=True, **kw)
+    fbw = oracle.moe_backward(inp.dOut, ffw, inp.W1, inp.W2, faithful=True)
+    assert_parity(torch_to_f64(out), fwd["out"], "out", faithful=ffw["out"])
+    assert_parity(torch_to_f64(dX), bwd["dX"], "dX", faithful=fbw["dX"])
+    assert_parity(dprob.cpu().numpy().astype(np.float64), bwd["dprob"], "dprob",
+                  faithful=fbw["dprob"])
+    n = int(fwd["offsets"][-1])
+    for name in ("Xp", "H1", "A", "Yp"):
+        assert_parity(torch_to_f64(layer.view(name)[:n]), fwd[name][:n], name,
+                      faithful=ffw[name][:n])
