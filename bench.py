@@ -173,7 +173,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ oracle timing
 
-def time_oracle(shape, inp, n_tokens: int, steps: int = 1):
+def time_oracle(shape, inp, n_tokens: int, steps: int = 1, **variant):
     """Wall time of the fp64 oracle forward + input and probability gradients on a
     token sample."""
     import oracle
@@ -184,7 +184,8 @@ def time_oracle(shape, inp, n_tokens: int, steps: int = 1):
     times = []
     for _ in range(steps):
         t0 = time.perf_counter()
-        fwd = oracle.moe_forward(inp.x[sel], inp.idx[sel], inp.prob[sel], W1, W2, shape.E, shape.P)
+        fwd = oracle.moe_forward(inp.x[sel], inp.idx[sel], inp.prob[sel], W1, W2, shape.E, shape.P,
+                                 **variant)
         oracle.moe_backward(inp.dOut[sel], fwd, W1, W2)
         times.append(time.perf_counter() - t0)
     return times, sel.size
@@ -228,7 +229,13 @@ def run_gg(args, shape, peaks):
     idx = torch.from_numpy(inp.idx).to(dev)
     prob = torch.from_numpy(inp.prob).to(dev)
     T, H, F, k, E, P = shape.T, shape.H, shape.F, shape.k, shape.E, shape.P
-    layer = gg.MoeLayer(T, H, F, k, E, P, device=dev)
+    act = {"swiglu": gg.GG_ACT_SWIGLU, "qgeglu": gg.GG_ACT_QGEGLU}[args.activation]
+    mode = {"combine": gg.GG_PROB_COMBINE, "activation": gg.GG_PROB_ACTIVATION,
+            "pre_fc1": gg.GG_PROB_PRE_FC1}[args.prob_mode]
+    epi_f = gg.GG_EPI_QGEGLU if act == gg.GG_ACT_QGEGLU else gg.GG_EPI_SWIGLU
+    epi_b = gg.GG_EPI_QGEGLU_BWD if act == gg.GG_ACT_QGEGLU else gg.GG_EPI_SWIGLU_BWD
+    pre = mode == gg.GG_PROB_PRE_FC1
+    layer = gg.MoeLayer(T, H, F, k, E, P, device=dev, activation=act, prob_mode=mode)
     b = {n: layer.view(n) for n in ("Xp", "H1", "A", "Yp", "dYp", "dH", "dXp", "offsets",
                                     "row_of_slot", "slot_of_row", "prob_of_row", "rowdot", "ws")}
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
@@ -247,25 +254,36 @@ def run_gg(args, shape, peaks):
                 events[i].record(stream)
 
         mark(0)
-        gg.permute(x, idx, prob, E, P, ws=ws, out=b)
+        if pre:  # row maps, then the copy that takes the probability along
+            gg.permute(x, idx, prob, E, P, ws=ws, out=dict(b, Xp=None))
+            gg.permute_rows(x, b["row_of_slot"], b["slot_of_row"], b["offsets"], k, E, P, rc, ws,
+                            dst=b["Xp"], prob=prob)
+        else:
+            gg.permute(x, idx, prob, E, P, ws=ws, out=b)
         mark(1)
-        gg.grouped_fwd(b["Xp"], W1, b["offsets"], gg.GG_EPI_SWIGLU, ws=ws, C=b["A"],
-                       H1_save=b["H1"])
+        gg.grouped_fwd(b["Xp"], W1, b["offsets"], epi_f, ws=ws, C=b["A"], H1_save=b["H1"],
+                       prob_of_row=b["prob_of_row"] if mode == gg.GG_PROB_ACTIVATION else None)
         mark(2)
         gg.grouped_fwd(b["A"], W2, b["offsets"], gg.GG_EPI_NONE, ws=ws, C=b["Yp"])
         mark(3)
-        gg.unpermute_combine(b["Yp"], b["row_of_slot"], prob, T, k, ws, out=out)
+        gg.unpermute_combine(b["Yp"], b["row_of_slot"], prob if mode == gg.GG_PROB_COMBINE else None,
+                             T, k, ws, out=out)
         mark(4)
         gg.permute_rows(dOut, b["row_of_slot"], b["slot_of_row"], b["offsets"], k, E, P, rc, ws,
                         dst=b["dYp"])
         mark(5)
-        gg.grouped_dgrad(b["dYp"], W2, b["offsets"], gg.GG_EPI_SWIGLU_BWD, H1=b["H1"],
-                         prob_of_row=b["prob_of_row"], ws=ws, dA=b["dH"], rowdot=b["rowdot"])
+        gg.grouped_dgrad(b["dYp"], W2, b["offsets"], epi_b, H1=b["H1"],
+                         prob_of_row=None if pre else b["prob_of_row"], ws=ws, dA=b["dH"],
+                         rowdot=None if pre else b["rowdot"])
         mark(6)
         gg.grouped_dgrad(b["dH"], W1, b["offsets"], gg.GG_EPI_NONE, ws=ws, dA=b["dXp"])
         mark(7)
-        gg.unpermute_combine(b["dXp"], b["row_of_slot"], None, T, k, ws, out=dX,
-                             rowdot=b["rowdot"], dprob=dprob, n_rowdot=gg.rowdot_blocks(F))
+        if pre:
+            gg.unpermute_combine(b["dXp"], b["row_of_slot"], prob, T, k, ws, out=dX, dprob=dprob,
+                                 dot_src=x)
+        else:
+            gg.unpermute_combine(b["dXp"], b["row_of_slot"], None, T, k, ws, out=dX,
+                                 rowdot=b["rowdot"], dprob=dprob, n_rowdot=gg.rowdot_blocks(F))
         mark(8)
 
     for _ in range(args.warmup):
@@ -424,7 +442,8 @@ def run_gg(args, shape, peaks):
     # ---- CPU baseline: the oracle on a bounded token sample (rank 0, N = 1)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        times, n_tok = time_oracle(shape, inp, args.cpu_tokens)
+        times, n_tok = time_oracle(shape, inp, args.cpu_tokens, activation=args.activation,
+                                   prob_mode=args.prob_mode)
         sub = shape.with_tokens(n_tok)
         cpu_val = (sub.flop_fwd() + sub.flop_dgrad()) / times[0] / 1e12
         cpu = {"value": cpu_val, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
@@ -440,7 +459,8 @@ def run_gg(args, shape, peaks):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": shape.name, "E": E, "H": H, "F": F, "T": T, "k": k, "P": P,
                    "routing": shape.routing, "parallelism": f"replicas x{world}",
-                   "outputs": "out, dX, dprob",
+                   "outputs": "out, dX, dprob", "activation": args.activation,
+                   "prob_mode": args.prob_mode,
                    "l2": "inputs larger than L2 (weights 1.2 GB, activations > 1 GB per step)"},
         "tokens_per_s": round(tot_tokens / tot_s, 1),
         "pct_bf16_peak": {"vs_2250_tflops": round(value / world / 2250.0, 4),
@@ -476,7 +496,8 @@ def run_reference(args, shape):
 
     def step():
         sel = np.sort(rng.choice(shape.T, size=n, replace=False))
-        fwd = oracle.moe_forward(inp.x[sel], inp.idx[sel], inp.prob[sel], W1, W2, shape.E, shape.P)
+        fwd = oracle.moe_forward(inp.x[sel], inp.idx[sel], inp.prob[sel], W1, W2, shape.E, shape.P,
+                                 activation=args.activation, prob_mode=args.prob_mode)
         oracle.moe_backward(inp.dOut[sel], fwd, W1, W2)
 
     for _ in range(args.warmup):
@@ -495,7 +516,8 @@ def run_reference(args, shape):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": shape.name, "E": shape.E, "H": shape.H, "F": shape.F,
                    "T": shape.T, "k": shape.k, "P": shape.P, "routing": shape.routing,
-                   "parallelism": "host cores", "outputs": "out, dX, dprob"},
+                   "parallelism": "host cores", "outputs": "out, dX, dprob",
+                   "activation": args.activation, "prob_mode": args.prob_mode},
         "tokens_per_s": n * args.steps / dt,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(),
                          "kind": "oracle",
@@ -519,6 +541,9 @@ def main(argv=None):
     ap.add_argument("--cpu-tokens", type=int, default=8192)
     ap.add_argument("--ref-tokens", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--activation", choices=["swiglu", "qgeglu"], default="swiglu")
+    ap.add_argument("--prob-mode", choices=["combine", "activation", "pre_fc1"],
+                    default="combine", help="where the routing probability is applied")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

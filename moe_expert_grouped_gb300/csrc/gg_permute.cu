@@ -450,7 +450,9 @@ combine_dprob_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ r
 // combine_kernel plus the pre-FC1 probability gradient: with Xp[row] =
 // prob * dot_src[t], dprob[t*k+j] = <dot_src[t], Yp[row(t, j)]>. Each lane
 // keeps one partial dot per slot over its columns (x chunk loaded once per
-// pass), reduced across the warp in a fixed butterfly order at the end.
+// pass), reduced across the warp in a fixed butterfly order at the end;
+// kMaxK (8 or 32) bounds k and the partials held in registers.
+template <int kMaxK>
 __global__ void __launch_bounds__(256)
 combine_dot_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row_of_slot,
                    const float* __restrict__ prob, int T, int k, int vec_per_row, int R_cap,
@@ -470,9 +472,9 @@ combine_dot_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row
         my_row = -1;
       }
     }
-    float dotp[32];
+    float dotp[kMaxK];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) dotp[j] = 0.0f;
+    for (int j = 0; j < kMaxK; ++j) dotp[j] = 0.0f;
     const uint4* xs = dot_src + static_cast<long long>(t) * vec_per_row;
     for (int c0 = 0; c0 < vec_per_row; c0 += 64) {
       const int ca = c0 + lane, cb = c0 + 32 + lane;
@@ -484,7 +486,7 @@ combine_dot_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[0][i] = acc[1][i] = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int j = 0; j < kMaxK; ++j) {
         if (j >= k) break;
         const int row = __shfl_sync(0xFFFFFFFFu, my_row, j);
         const float pj = __shfl_sync(0xFFFFFFFFu, my_p, j);
@@ -512,7 +514,7 @@ combine_dot_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row
     }
     float mine = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+    for (int j = 0; j < kMaxK; ++j) {
       if (j >= k) break;
       float v = dotp[j];
 #pragma unroll
@@ -619,8 +621,12 @@ cudaError_t launch_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const 
   long long blocks = (static_cast<long long>(T) + 7) / 8;
   const long long cap = static_cast<long long>(sm_count) * 8;  // as for the row copy
   if (blocks > cap) blocks = cap;
-  if (dprob != nullptr && dot_src != nullptr)
-    combine_dot_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+  if (dprob != nullptr && dot_src != nullptr && k <= 8)
+    combine_dot_kernel<8><<<static_cast<int>(blocks), 256, 0, stream>>>(
+        reinterpret_cast<const uint4*>(Yp), row_of_slot, prob, T, k, vec, R_cap,
+        reinterpret_cast<uint4*>(out), reinterpret_cast<const uint4*>(dot_src), dprob, status);
+  else if (dprob != nullptr && dot_src != nullptr)
+    combine_dot_kernel<32><<<static_cast<int>(blocks), 256, 0, stream>>>(
         reinterpret_cast<const uint4*>(Yp), row_of_slot, prob, T, k, vec, R_cap,
         reinterpret_cast<uint4*>(out), reinterpret_cast<const uint4*>(dot_src), dprob, status);
   else if (dprob != nullptr)

@@ -31,11 +31,12 @@ def gg():
     return mod
 
 
-def _run(gg, shape, inp):
+def _run(gg, shape, inp, activation=0, prob_mode=0):
     d = dict(x=bits_to_torch(inp.x), idx=torch.from_numpy(inp.idx).cuda(),
              prob=torch.from_numpy(inp.prob).cuda(), W1=bits_to_torch(inp.W1),
              W2=bits_to_torch(inp.W2), dOut=bits_to_torch(inp.dOut))
-    layer = gg.MoeLayer(shape.T, shape.H, shape.F, shape.k, shape.E, shape.P)
+    layer = gg.MoeLayer(shape.T, shape.H, shape.F, shape.k, shape.E, shape.P,
+                        activation=activation, prob_mode=prob_mode)
     out = layer.forward(d["x"], d["idx"], d["prob"], d["W1"], d["W2"])
     dX, dprob = layer.backward(d["dOut"], d["W1"], d["W2"], dprob=True)
     torch.cuda.synchronize()
@@ -51,14 +52,15 @@ def _check_indices(layer, inp, shape):
     return off
 
 
-def _check_sample(inp, shape, out, grads, n_tokens, seed):
+def _check_sample(inp, shape, out, grads, n_tokens, seed, **variant):
     dX, dprob = grads
     rng = np.random.default_rng(seed)
     sel = np.sort(rng.choice(shape.T, size=min(n_tokens, shape.T), replace=False))
-    fwd = oracle.moe_forward(inp.x[sel], inp.idx[sel], inp.prob[sel], inp.W1, inp.W2, shape.E, 1)
+    fwd = oracle.moe_forward(inp.x[sel], inp.idx[sel], inp.prob[sel], inp.W1, inp.W2, shape.E, 1,
+                             **variant)
     bwd = oracle.moe_backward(inp.dOut[sel], fwd, inp.W1, inp.W2)
     ffw = oracle.moe_forward(inp.x[sel], inp.idx[sel], inp.prob[sel], inp.W1, inp.W2, shape.E, 1,
-                             faithful=True)
+                             faithful=True, **variant)
     fbw = oracle.moe_backward(inp.dOut[sel], ffw, inp.W1, inp.W2, faithful=True)
     rows = torch.from_numpy(sel).cuda()
     assert_parity(torch_to_f64(out[rows]), fwd["out"], "out (sampled)", faithful=ffw["out"])
@@ -77,6 +79,19 @@ def test_fullsize_sampled_parity(gg, cfg):
     # every routed row was produced (no unwritten row survives in the output)
     assert torch.isfinite(out.float()).all() and torch.isfinite(dX[0].float()).all()
     assert torch.isfinite(dX[1]).all()
+
+
+@pytest.mark.parametrize("activation,prob_mode", [(1, 1), (0, 2)])
+def test_fullsize_variants_sampled_parity(gg, activation, prob_mode):
+    # the balanced layer with QuickGeGLU and the weighted activation, and with
+    # SwiGLU and the pre-FC1 probability multiply
+    shape = CONFIGS[2]
+    inp = make_inputs(shape, 2000)
+    layer, out, grads = _run(gg, shape, inp, activation, prob_mode)
+    _check_indices(layer, inp, shape)
+    _check_sample(inp, shape, out, grads, 48, 7 + prob_mode,
+                  activation=("swiglu", "qgeglu")[activation],
+                  prob_mode=("combine", "activation", "pre_fc1")[prob_mode])
 
 
 @pytest.mark.parametrize("rows", [SWEEP_ROWS[0], SWEEP_ROWS[-1]])

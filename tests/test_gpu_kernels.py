@@ -453,10 +453,11 @@ def test_permute_rows_scaled_by_probability(gg):
     assert np.all(got[:n][pad] == 0)
 
 
-def test_combine_dot_probability_gradient(gg):
+@pytest.mark.parametrize("k", [3, 12])  # both register bounds of the kernel (8 and 32 slots)
+def test_combine_dot_probability_gradient(gg, k):
     # dprob[t, j] = <dot_src[t], Yp[row(t, j)]>; the weighted sum itself is
     # bitwise the plain weighted combine
-    T, k, H, R_cap = 300, 3, 320, 1000
+    T, H, R_cap = 300, 320, 4000
     rng = np.random.default_rng(43)
     rows = rng.permutation(R_cap)[:T * k].astype(np.int32)
     rows[[5, 77, 301]] = -1
