@@ -235,7 +235,9 @@ def run_gg(args, shape, peaks):
     epi_f = gg.GG_EPI_QGEGLU if act == gg.GG_ACT_QGEGLU else gg.GG_EPI_SWIGLU
     epi_b = gg.GG_EPI_QGEGLU_BWD if act == gg.GG_ACT_QGEGLU else gg.GG_EPI_SWIGLU_BWD
     pre = mode == gg.GG_PROB_PRE_FC1
-    layer = gg.MoeLayer(T, H, F, k, E, P, device=dev, activation=act, prob_mode=mode)
+    rec = args.recompute_h1
+    layer = gg.MoeLayer(T, H, F, k, E, P, device=dev, activation=act, prob_mode=mode,
+                        recompute_h1=rec)
     b = {n: layer.view(n) for n in ("Xp", "H1", "A", "Yp", "dYp", "dH", "dXp", "offsets",
                                     "row_of_slot", "slot_of_row", "prob_of_row", "rowdot", "ws")}
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
@@ -246,6 +248,8 @@ def run_gg(args, shape, peaks):
     stream = torch.cuda.current_stream(dev)
     ops = ["permute", "fc1_swiglu", "fc2", "combine", "permute_dout", "dgrad_fc2_swiglu_bwd",
            "dgrad_fc1", "combine_dx"]
+    if rec:
+        ops.insert(4, "fc1_recompute")
 
     def step(events=None):
         # the same calls, in the same order, as gg_moe_mlp_fwd + gg_moe_mlp_bwd
@@ -261,7 +265,8 @@ def run_gg(args, shape, peaks):
         else:
             gg.permute(x, idx, prob, E, P, ws=ws, out=b)
         mark(1)
-        gg.grouped_fwd(b["Xp"], W1, b["offsets"], epi_f, ws=ws, C=b["A"], H1_save=b["H1"],
+        gg.grouped_fwd(b["Xp"], W1, b["offsets"], epi_f, ws=ws, C=b["A"],
+                       H1_save=None if rec else b["H1"],
                        prob_of_row=b["prob_of_row"] if mode == gg.GG_PROB_ACTIVATION else None)
         mark(2)
         gg.grouped_fwd(b["A"], W2, b["offsets"], gg.GG_EPI_NONE, ws=ws, C=b["Yp"])
@@ -269,22 +274,27 @@ def run_gg(args, shape, peaks):
         gg.unpermute_combine(b["Yp"], b["row_of_slot"], prob if mode == gg.GG_PROB_COMBINE else None,
                              T, k, ws, out=out)
         mark(4)
+        i = 4
+        if rec:  # the backward's recompute of FC1's output (a plain grouped FC1)
+            gg.grouped_fwd(b["Xp"], W1, b["offsets"], gg.GG_EPI_NONE, ws=ws, C=b["H1"])
+            i += 1
+            mark(i)
         gg.permute_rows(dOut, b["row_of_slot"], b["slot_of_row"], b["offsets"], k, E, P, rc, ws,
                         dst=b["dYp"])
-        mark(5)
+        mark(i + 1)
         gg.grouped_dgrad(b["dYp"], W2, b["offsets"], epi_b, H1=b["H1"],
                          prob_of_row=None if pre else b["prob_of_row"], ws=ws, dA=b["dH"],
                          rowdot=None if pre else b["rowdot"])
-        mark(6)
+        mark(i + 2)
         gg.grouped_dgrad(b["dH"], W1, b["offsets"], gg.GG_EPI_NONE, ws=ws, dA=b["dXp"])
-        mark(7)
+        mark(i + 3)
         if pre:
             gg.unpermute_combine(b["dXp"], b["row_of_slot"], prob, T, k, ws, out=dX, dprob=dprob,
                                  dot_src=x)
         else:
             gg.unpermute_combine(b["dXp"], b["row_of_slot"], None, T, k, ws, out=dX,
                                  rowdot=b["rowdot"], dprob=dprob, n_rowdot=gg.rowdot_blocks(F))
-        mark(8)
+        mark(i + 4)
 
     for _ in range(args.warmup):
         step()
@@ -412,8 +422,11 @@ def run_gg(args, shape, peaks):
     avg = {op: float(np.mean(v)) for op, v in per_op.items()}
     total_ms = sum(avg.values())
     R = shape.R
+    # (with --recompute-h1 the backward's FC1 recompute is extra work the
+    # metric does not count: `value` stays 12·R·H·F per step)
     flop_of = {"fc1_swiglu": 4.0 * R * H * F, "fc2": 2.0 * R * H * F,
-               "dgrad_fc2_swiglu_bwd": 2.0 * R * H * F, "dgrad_fc1": 4.0 * R * H * F}
+               "dgrad_fc2_swiglu_bwd": 2.0 * R * H * F, "dgrad_fc1": 4.0 * R * H * F,
+               "fc1_recompute": 4.0 * R * H * F}
     dom = max(avg, key=lambda o: avg[o])
     if dom in flop_of:
         ach = flop_of[dom] / (avg[dom] / 1e3) / 1e12
@@ -460,7 +473,7 @@ def run_gg(args, shape, peaks):
         "config": {"workload": shape.name, "E": E, "H": H, "F": F, "T": T, "k": k, "P": P,
                    "routing": shape.routing, "parallelism": f"replicas x{world}",
                    "outputs": "out, dX, dprob", "activation": args.activation,
-                   "prob_mode": args.prob_mode,
+                   "prob_mode": args.prob_mode, "recompute_h1": rec,
                    "l2": "inputs larger than L2 (weights 1.2 GB, activations > 1 GB per step)"},
         "tokens_per_s": round(tot_tokens / tot_s, 1),
         "pct_bf16_peak": {"vs_2250_tflops": round(value / world / 2250.0, 4),
@@ -542,6 +555,8 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--activation", choices=["swiglu", "qgeglu"], default="swiglu")
+    ap.add_argument("--recompute-h1", action="store_true",
+                    help="do not keep FC1's output for the backward; recompute it there")
     ap.add_argument("--prob-mode", choices=["combine", "activation", "pre_fc1"],
                     default="combine", help="where the routing probability is applied")
     args = ap.parse_args(argv)

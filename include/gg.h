@@ -415,6 +415,14 @@ typedef enum gg_prob_mode {
 typedef struct gg_moe_options {
   int activation;         /* gg_activation */
   int prob_mode;          /* gg_prob_mode  */
+  int recompute_h1;       /* 0: the forward stores FC1's output H1 for the
+                             backward; 1: the forward does not store it and
+                             the backward recomputes it (a plain grouped FC1
+                             on the kept Xp, same bits: "save vs recompute"
+                             of [P1] "Scope deliberately omitted" /
+                             expert_fc1_act). The H1 region of the buffers is
+                             then scratch of the backward call only, free for
+                             the caller between forward and backward. */
 } gg_moe_options;
 
 /* gg_moe_mlp_fwd / gg_moe_mlp_bwd with options (NULL = SwiGLU, probability

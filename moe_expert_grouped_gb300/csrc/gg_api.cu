@@ -475,9 +475,12 @@ static gg_status check_buffers(const gg_moe_buffers* b, int T, int k, int E) {
 }
 
 static gg_status read_options(const gg_moe_options* opt, gg_epilogue* fwd_epi,
-                              gg_epilogue* bwd_epi, int* mode) {
+                              gg_epilogue* bwd_epi, int* mode, bool* recompute) {
   const int act = opt != nullptr ? opt->activation : GG_ACT_SWIGLU;
   *mode = opt != nullptr ? opt->prob_mode : GG_PROB_COMBINE;
+  *recompute = opt != nullptr && opt->recompute_h1 != 0;
+  if (opt != nullptr && opt->recompute_h1 != 0 && opt->recompute_h1 != 1)
+    return GG_ERR_INVALID_ARG;
   if (act != GG_ACT_SWIGLU && act != GG_ACT_QGEGLU) return GG_ERR_INVALID_ARG;
   if (*mode != GG_PROB_COMBINE && *mode != GG_PROB_ACTIVATION && *mode != GG_PROB_PRE_FC1)
     return GG_ERR_INVALID_ARG;
@@ -493,7 +496,8 @@ gg_status gg_moe_mlp_fwd_ex(const gg_bf16* x, const int32_t* idx, const float* p
   if (T < 0 || H <= 0 || k <= 0 || E <= 0 || pad_multiple <= 0) return GG_ERR_INVALID_ARG;
   gg_epilogue fepi, bepi;
   int mode;
-  gg_status s = read_options(opt, &fepi, &bepi, &mode);
+  bool recompute;
+  gg_status s = read_options(opt, &fepi, &bepi, &mode, &recompute);
   if (s != GG_OK) return s;
   if ((s = check_buffers(buf, T, k, E)) != GG_OK) return s;
   if (W1 == nullptr || W2 == nullptr || F <= 0) return GG_ERR_INVALID_ARG;
@@ -518,7 +522,8 @@ gg_status gg_moe_mlp_fwd_ex(const gg_bf16* x, const int32_t* idx, const float* p
                         pad_multiple, R_cap, prob, buf->Xp, buf->ws, buf->ws_bytes, stream);
     if (s != GG_OK) return s;
   }
-  s = gg_grouped_fwd(buf->Xp, W1, buf->offsets, E, R_cap, H, 2 * F, fepi, buf->A, buf->H1,
+  s = gg_grouped_fwd(buf->Xp, W1, buf->offsets, E, R_cap, H, 2 * F, fepi, buf->A,
+                     recompute ? nullptr : buf->H1,
                      mode == GG_PROB_ACTIVATION ? buf->prob_of_row : nullptr, buf->ws,
                      buf->ws_bytes, stream);
   if (s != GG_OK) return s;
@@ -546,7 +551,8 @@ gg_status gg_moe_mlp_bwd_ex(const gg_bf16* dOut, const gg_bf16* x, const float* 
     return GG_ERR_INVALID_ARG;
   gg_epilogue fepi, bepi;
   int mode;
-  gg_status s = read_options(opt, &fepi, &bepi, &mode);
+  bool recompute;
+  gg_status s = read_options(opt, &fepi, &bepi, &mode, &recompute);
   if (s != GG_OK) return s;
   if ((s = check_buffers(buf, T, k, E)) != GG_OK) return s;
   if (W1 == nullptr || W2 == nullptr) return GG_ERR_INVALID_ARG;
@@ -559,6 +565,11 @@ gg_status gg_moe_mlp_bwd_ex(const gg_bf16* dOut, const gg_bf16* x, const float* 
   if (rc > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
   const int R_cap = static_cast<int>(rc);
   float* rowdot = dprob != nullptr && !pre ? buf->rowdot : nullptr;
+  if (recompute) {  // H1 = bf16(Xp_e @ W1_e^T), the bits the forward's epilogue would store
+    s = gg_grouped_fwd(buf->Xp, W1, buf->offsets, E, R_cap, H, 2 * F, GG_EPI_NONE, buf->H1,
+                       nullptr, nullptr, buf->ws, buf->ws_bytes, stream);
+    if (s != GG_OK) return s;
+  }
   s = gg_permute_rows(dOut, buf->row_of_slot, buf->slot_of_row, buf->offsets, T, H, k, E,
                       pad_multiple, R_cap, nullptr, buf->dYp, buf->ws, buf->ws_bytes, stream);
   if (s != GG_OK) return s;

@@ -75,7 +75,8 @@ class GGBuffers(ctypes.Structure):
 class GGOptions(ctypes.Structure):
     """Mirror of struct gg_moe_options."""
 
-    _fields_ = [("activation", ctypes.c_int), ("prob_mode", ctypes.c_int)]
+    _fields_ = [("activation", ctypes.c_int), ("prob_mode", ctypes.c_int),
+                ("recompute_h1", ctypes.c_int)]
 
 
 class GGError(RuntimeError):
@@ -351,9 +352,10 @@ class MoeLayer:
     }
 
     def __init__(self, T: int, H: int, F: int, k: int, E: int, P: int = 1, device="cuda",
-                 activation: int = GG_ACT_SWIGLU, prob_mode: int = GG_PROB_COMBINE):
+                 activation: int = GG_ACT_SWIGLU, prob_mode: int = GG_PROB_COMBINE,
+                 recompute_h1: bool = False):
         self.T, self.H, self.F, self.k, self.E, self.P = T, H, F, k, E, P
-        self.opt = GGOptions(activation, prob_mode)
+        self.opt = GGOptions(activation, prob_mode, 1 if recompute_h1 else 0)
         self._saved = None  # the forward's (x, prob): the pre-FC1 backward needs them
         self.R_cap = r_cap(T, k, E, P)
         self.device = torch.device(device)

@@ -158,13 +158,13 @@ def test_validation_rejects_before_launch(gg):
     n = L.gg_moe_buffers_size(4, 64, 128, 2, 4, 1)
     assert L.gg_moe_buffers_bind(ctypes.c_void_p(1 << 40), n, 4, 64, 128, 2, 4, 1,
                                  ctypes.byref(good)) == 0
-    for act, mode in ((2, 0), (0, 3), (-1, 0)):
-        opt = gg.GGOptions(act, mode)
+    for act, mode, rec in ((2, 0, 0), (0, 3, 0), (-1, 0, 0), (0, 0, 2)):
+        opt = gg.GGOptions(act, mode, rec)
         assert L.gg_moe_mlp_fwd_ex(p, p, p, p, p, 4, 64, 128, 2, 4, 1, ctypes.byref(opt), p,
                                    ctypes.byref(good), None) == 1
         assert L.gg_moe_mlp_bwd_ex(p, p, p, p, p, 4, 64, 128, 2, 4, 1, ctypes.byref(opt), p, p,
                                    ctypes.byref(good), None) == 1
-    pre = gg.GGOptions(0, 2)
+    pre = gg.GGOptions(0, 2, 0)
     assert L.gg_moe_mlp_bwd_ex(p, p, None, p, p, 4, 64, 128, 2, 4, 1, ctypes.byref(pre), p, None,
                                ctypes.byref(good), None) == 1
     assert L.gg_moe_mlp_bwd_ex(p, None, p, p, p, 4, 64, 128, 2, 4, 1, ctypes.byref(pre), p, p,

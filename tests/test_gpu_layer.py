@@ -194,3 +194,32 @@ def test_layer_variants_match_oracle(gg, shape, seed, activation, prob_mode):
     for name in ("Xp", "H1", "A", "Yp"):
         assert_parity(torch_to_f64(layer.view(name)[:n]), fwd[name][:n], name,
                       faithful=ffw[name][:n])
+
+
+@pytest.mark.parametrize("activation,prob_mode", [(0, 0), (1, 1), (0, 2)])
+def test_recompute_h1_equals_saved_h1(gg, activation, prob_mode):
+    # The backward that recomputes FC1's output with a plain grouped FC1 gives
+    # the same bits as the one that reads the forward's saved H1.
+    shape = MID_PAD
+    inp = make_inputs(shape, 81)
+    d = _dev(inp)
+    res = []
+    for recompute in (False, True):
+        layer = gg.MoeLayer(shape.T, shape.H, shape.F, shape.k, shape.E, shape.P,
+                            activation=activation, prob_mode=prob_mode, recompute_h1=recompute)
+        out = layer.forward(d["x"], d["idx"], d["prob"], d["W1"], d["W2"])
+        torch.cuda.synchronize()
+        h1_after_fwd = torch_to_bits(layer.view("H1"))
+        dX, dprob = layer.backward(d["dOut"], d["W1"], d["W2"], dprob=True)
+        torch.cuda.synchronize()
+        assert layer.status() == 0
+        n = int(layer.view("offsets")[-1].item())
+        res.append((torch_to_bits(out), torch_to_bits(dX), dprob.cpu().numpy(),
+                    torch_to_bits(layer.view("H1")[:n]), h1_after_fwd[:n]))
+    saved, recomputed = res
+    for a, b in zip(saved[:4], recomputed[:4]):
+        np.testing.assert_array_equal(a, b)
+    # without recompute the forward stored H1; with it the forward left the
+    # (zero-initialised) region alone and the backward filled it
+    np.testing.assert_array_equal(saved[4], saved[3])
+    assert np.all(recomputed[4] == 0)
