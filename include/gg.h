@@ -111,7 +111,8 @@ uint64_t gg_launch_count(void);
 
 /* Bytes of workspace every call below needs for a batch of T tokens with
  * top-k routing over E experts. The first 256 bytes hold the status word;
- * the rest is scratch for the permute's per-block expert histograms. */
+ * the rest is scratch for the permute's per-block expert histograms (one
+ * int32 per expert and 256-pair block). */
 size_t gg_workspace_size(int T, int k, int E);
 
 /* Zero the status word at the start of `ws` (stream-ordered). */
@@ -161,11 +162,11 @@ gg_status gg_permute(const gg_bf16* x, const int32_t* idx, const float* prob,
  * callers without a device allocator. This entry point computes exactly what
  * gg_permute computes (same arguments, same outputs, bit-identical results)
  * but takes no `ws`: its scratch (status word + per-block expert histograms)
- * lives in a fixed 1 MiB array in the library's device image, which every GPU
+ * lives in a fixed 8 MiB array in the library's device image, which every GPU
  * that loads the library keeps until the process exits. It calls no
  * cudaMalloc, cudaFree or allocating library routine.
- *   - Limit: gg_workspace_size(T, k, E) <= 1 MiB, i.e. ceil(T*k/2048) * E <=
- *     262080 (for E = 128: T*k <= 4,192,256 pairs). Larger batches are
+ *   - Limit: gg_workspace_size(T, k, E) <= 8 MiB, i.e. ceil(T*k/256) * E <=
+ *     2097088 (for E = 128: T*k <= 4,194,048 pairs). Larger batches are
  *     rejected with GG_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
  *   - Set-up: the first call on a device (made with that device current)
  *     looks up the array's device address once; make that first call before

@@ -14,7 +14,7 @@ namespace gg {
 // per-block expert histograms (int32 [n_blocks][E]).
 constexpr size_t kWsHeader = 256;
 constexpr int kPermuteBlockThreads = 256;
-constexpr int kPermutePairsPerWarp = 256;  // 8 steps of 32 pairs
+constexpr int kPermutePairsPerWarp = 32;  // one step of 32 pairs
 constexpr int kPermutePairsPerBlock = kPermutePairsPerWarp * (kPermuteBlockThreads / 32);
 constexpr int kMaxExperts = 1024;
 

@@ -56,7 +56,16 @@ __device__ __forceinline__ void warp_histogram(const int32_t* __restrict__ idx, 
 
 __global__ void __launch_bounds__(kPermuteBlockThreads)
 permute_count_kernel(const int32_t* __restrict__ idx, long long R, int E,
-                     int32_t* __restrict__ block_hist, int32_t* status) {
+                     int32_t* __restrict__ block_hist, int32_t* status,
+                     int32_t* __restrict__ slot_of_row, float* __restrict__ prob_of_row,
+                     long long R_cap) {
+  // every row starts as padding (slot -1, probability 0); the scatter kernel
+  // fills in the routed rows
+  for (long long r = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; r < R_cap;
+       r += static_cast<long long>(gridDim.x) * blockDim.x) {
+    slot_of_row[r] = -1;
+    prob_of_row[r] = 0.0f;
+  }
   extern __shared__ int hist[];  // [kWarps][E]
   for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
@@ -559,12 +568,8 @@ cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* pr
     count_launch();
     return cudaGetLastError();
   }
-  err = cudaMemsetAsync(slot_of_row, 0xFF, sizeof(int32_t) * R_cap, stream);
-  if (err != cudaSuccess) return err;
-  err = cudaMemsetAsync(prob_of_row, 0, sizeof(float) * R_cap, stream);
-  if (err != cudaSuccess) return err;
-  permute_count_kernel<<<nb, kPermuteBlockThreads, hist_smem, stream>>>(idx, R, E, block_hist,
-                                                                        status);
+  permute_count_kernel<<<nb, kPermuteBlockThreads, hist_smem, stream>>>(
+      idx, R, E, block_hist, status, slot_of_row, prob_of_row, R_cap);
   count_launch();
   permute_scan_kernel<<<1, 1024, 0, stream>>>(block_hist, nb, E, P, offsets);
   count_launch();
@@ -670,7 +675,7 @@ cudaError_t launch_bounded_wait_selftest(int32_t* status, uint64_t limit_ns, cud
 namespace gg {
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(1) << 20;  // 1 MiB per device
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB per device
 
 static __device__ __align__(256) uint8_t g_permute_scratch[kStaticScratchBytes];
 
@@ -702,7 +707,7 @@ extern "C" gg_status gg_permute_noalloc(const gg_bf16* x, const int32_t* idx, co
   if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(Xp) & 15u))
     return GG_ERR_MISALIGNED;
   // The batch must fit the fixed scratch: status header + one int32 per
-  // (2048-pair block, expert).
+  // (256-pair block, expert).
   const size_t need = kWsHeader + sizeof(int32_t) * static_cast<size_t>(permute_blocks(
                                                         static_cast<long long>(T) * k)) * E;
   if (need > kStaticScratchBytes) return GG_ERR_WORKSPACE_TOO_SMALL;

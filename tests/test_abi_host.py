@@ -58,8 +58,8 @@ def test_workspace_size_grows_with_pairs(gg):
     small = L.gg_workspace_size(16384, 8, 128)
     big = L.gg_workspace_size(131072, 8, 128)
     assert big > small > 256
-    # one int32 histogram row of E experts per block of 2048 pairs
-    assert small >= 256 + 4 * 128 * (16384 * 8 // 2048)
+    # one int32 histogram row of E experts per block of 256 pairs
+    assert small >= 256 + 4 * 128 * (16384 * 8 // 256)
 
 
 def test_buffers_bind_carves_disjoint_aligned_pieces(gg):
