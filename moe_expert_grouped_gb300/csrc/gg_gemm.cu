@@ -547,8 +547,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
       }
       tc_fence_before();
       __syncwarp();
-      // this warp's share of the accumulator is free: tell the MMA issuer
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&st.tempty[acc]), 0));
+      // this warp's share of the accumulator is free: tell the MMA issuer. The
+      // arrive is relaxed: a release would first wait for this warp's
+      // output stores (measured 3.5 % of FC2 and dgrad FC2), and the barrier
+      // only has to order the completed TMEM reads.
+      if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&st.tempty[acc]), 0));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }

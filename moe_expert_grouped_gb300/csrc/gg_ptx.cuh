@@ -235,6 +235,16 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
                : "memory");
 }
 
+// The same arrive without release semantics: it does not wait for this
+// thread's earlier global stores to become visible. For barriers that only
+// order tcgen05 accesses (the TMEM reads of the epilogue, already complete
+// after tcgen05.wait::ld and ordered by tcgen05.fence::before_thread_sync)
+// and pass no data through memory.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+
 // Loads into this CTA's shared memory whose completion is counted on an
 // mbarrier of either CTA of the MMA pair (`cluster_bar` from mapa_shared).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
