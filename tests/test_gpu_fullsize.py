@@ -125,3 +125,19 @@ def test_skewed_padded_batch_invariance(gg):
     for n, bits in snap.items():
         np.testing.assert_array_equal(torch_to_bits(lb.view(n)[rows_b]), bits, err_msg=n)
     np.testing.assert_array_equal(lb.view("rowdot")[rows_b].cpu().numpy(), snap_rd)
+
+
+def test_skewed_padded_variant_parity(gg):
+    # Zipf loads, 16 empty experts and 256-row padding with QuickGeGLU and the
+    # probability applied before FC1
+    shape = CONFIGS[3]
+    inp = make_inputs(shape, 3000)
+    layer, out, grads = _run(gg, shape, inp, activation=1, prob_mode=2)
+    off = _check_indices(layer, inp, shape)
+    assert np.all(np.diff(off) % shape.P == 0)
+    _check_sample(inp, shape, out, grads, 64, 11, activation="qgeglu", prob_mode="pre_fc1")
+    # padding rows of the pre-FC1 copy are zero
+    n = int(off[-1])
+    pad = layer.view("slot_of_row").cpu().numpy()[:n] < 0
+    assert pad.any()
+    assert np.all(torch_to_bits(layer.view("Xp")[:n])[pad] == 0)

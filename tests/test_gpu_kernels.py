@@ -330,10 +330,11 @@ def test_gathered_gemms_equal_materialised_path(gg, P, T, E, k, H, F):
     R_cap = p["Xp"].shape[0]
     n = int(p["offsets"][-1].item())
     ws = p["ws"]
-    for epi in (gg.GG_EPI_SWIGLU, gg.GG_EPI_NONE):
-        H1a = _nan_filled((R_cap, 2 * F)) if epi == gg.GG_EPI_SWIGLU else None
-        H1b = _nan_filled((R_cap, 2 * F)) if epi == gg.GG_EPI_SWIGLU else None
-        ncols = F if epi == gg.GG_EPI_SWIGLU else 2 * F
+    for epi in (gg.GG_EPI_SWIGLU, gg.GG_EPI_QGEGLU, gg.GG_EPI_NONE):
+        gated = epi != gg.GG_EPI_NONE
+        H1a = _nan_filled((R_cap, 2 * F)) if gated else None
+        H1b = _nan_filled((R_cap, 2 * F)) if gated else None
+        ncols = F if gated else 2 * F
         Ca, Cb = _nan_filled((R_cap, ncols)), _nan_filled((R_cap, ncols))
         gg.grouped_fwd(p["Xp"], W1, p["offsets"], epi, ws=ws, C=Ca, H1_save=H1a)
         gg.grouped_fwd_gather(x, p["slot_of_row"], k, W1, p["offsets"], epi, ws=ws, C=Cb,
@@ -344,11 +345,12 @@ def test_gathered_gemms_equal_materialised_path(gg, P, T, E, k, H, F):
             np.testing.assert_array_equal(torch_to_bits(H1a), torch_to_bits(H1b))
     H1 = bits_to_torch(normal_bf16(rng, (R_cap, 2 * F), 1.0))
     dYp = gg.permute_rows(dO, p["row_of_slot"], p["slot_of_row"], p["offsets"], k, E, P, R_cap, ws)
-    for epi in (gg.GG_EPI_SWIGLU_BWD, gg.GG_EPI_NONE):
-        # dgrad through W2 [E][H][F]: [R][2F] with the SwiGLU backward, else [R][F]
-        ncols = 2 * F if epi == gg.GG_EPI_SWIGLU_BWD else F
+    for epi in (gg.GG_EPI_SWIGLU_BWD, gg.GG_EPI_QGEGLU_BWD, gg.GG_EPI_NONE):
+        # dgrad through W2 [E][H][F]: [R][2F] with a gated backward, else [R][F]
+        gated = epi != gg.GG_EPI_NONE
+        ncols = 2 * F if gated else F
         da, db = _nan_filled((R_cap, ncols)), _nan_filled((R_cap, ncols))
-        h1 = H1 if epi == gg.GG_EPI_SWIGLU_BWD else None
+        h1 = H1 if gated else None
         gg.grouped_dgrad(dYp, W2, p["offsets"], epi, H1=h1, prob_of_row=p["prob_of_row"], ws=ws,
                          dA=da)
         gg.grouped_dgrad_gather(dO, p["slot_of_row"], k, W2, p["offsets"], epi, H1=h1,

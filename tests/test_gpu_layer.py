@@ -223,3 +223,38 @@ def test_recompute_h1_equals_saved_h1(gg, activation, prob_mode):
     # (zero-initialised) region alone and the backward filled it
     np.testing.assert_array_equal(saved[4], saved[3])
     assert np.all(recomputed[4] == 0)
+
+
+@pytest.mark.parametrize("activation,prob_mode,recompute", [(1, 2, True), (1, 1, False)])
+def test_cuda_graph_replay_of_variants(gg, activation, prob_mode, recompute):
+    # the option paths (QuickGeGLU, probability at the activation or before
+    # FC1, H1 recompute) capture into a CUDA graph and replay bitwise
+    shape = MID_PAD
+    inp = make_inputs(shape, 83)
+    d = _dev(inp)
+    kw = dict(activation=activation, prob_mode=prob_mode, recompute_h1=recompute)
+    eager = gg.MoeLayer(shape.T, shape.H, shape.F, shape.k, shape.E, shape.P, **kw)
+    out_e = eager.forward(d["x"], d["idx"], d["prob"], d["W1"], d["W2"])
+    dX_e, dp_e = eager.backward(d["dOut"], d["W1"], d["W2"], dprob=True)
+    layer = gg.MoeLayer(shape.T, shape.H, shape.F, shape.k, shape.E, shape.P, **kw)
+    out, dX = torch.empty_like(out_e), torch.empty_like(dX_e)
+    dp = torch.empty_like(dp_e)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.forward(d["x"], d["idx"], d["prob"], d["W1"], d["W2"], out=out)
+        layer.backward(d["dOut"], d["W1"], d["W2"], dX=dX, dprob=dp)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    for t in (out, dX, dp):
+        t.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer.forward(d["x"], d["idx"], d["prob"], d["W1"], d["W2"], out=out)
+        layer.backward(d["dOut"], d["W1"], d["W2"], dX=dX, dprob=dp)
+    g.replay()
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    np.testing.assert_array_equal(torch_to_bits(out), torch_to_bits(out_e))
+    np.testing.assert_array_equal(torch_to_bits(dX), torch_to_bits(dX_e))
+    np.testing.assert_array_equal(dp.cpu().numpy(), dp_e.cpu().numpy())
