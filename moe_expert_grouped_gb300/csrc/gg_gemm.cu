@@ -138,43 +138,39 @@ __device__ __forceinline__ void pack_bf16x32(const float (&v)[32], float scale, 
 __device__ __forceinline__ int stage_slot(int r, int c) { return r * 4 + (c ^ ((r >> 1) & 3)); }
 
 // Warp-collective store of a 32-row x 32-column BF16 chunk. Lane i holds row
-// i in w[]; `dst` is its row pointer at the chunk's first column and rows with
-// valid == false are skipped. Through the staging buffer four lanes write
-// each 64-byte row segment, so every store instruction writes 8 whole row
-// segments instead of 32 scattered 16-byte pieces.
-__device__ __forceinline__ void store_chunk(uint4* stg, const uint4 (&w)[4], gg_bf16* dst,
-                                            bool valid) {
+// i in w[]; row r of the chunk starts at row0 + r * ld (the warp's 32 rows
+// are consecutive) and only rows r < nvalid are written. Through the staging
+// buffer four lanes write each 64-byte row segment, so every store
+// instruction writes 8 whole row segments instead of 32 scattered 16-byte
+// pieces.
+__device__ __forceinline__ void store_chunk(uint4* stg, const uint4 (&w)[4], gg_bf16* row0,
+                                            long long ld, int nvalid) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int c = 0; c < 4; ++c) stg[stage_slot(lane, c)] = w[c];
   __syncwarp();
-  const unsigned long long mine = reinterpret_cast<unsigned long long>(dst);
-  const int ok_mine = valid ? 1 : 0;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int r = 8 * j + (lane >> 2);
     const int c = lane & 3;
     const uint4 v = stg[stage_slot(r, c)];
-    const unsigned long long p = __shfl_sync(0xFFFFFFFFu, mine, r);
-    if (__shfl_sync(0xFFFFFFFFu, ok_mine, r)) reinterpret_cast<uint4*>(p)[c] = v;
+    if (r < nvalid) reinterpret_cast<uint4*>(row0 + r * ld)[c] = v;
   }
   __syncwarp();
 }
 
-// Warp-collective coalesced fetch of a 32-row x 32-column BF16 chunk: lane L
-// loads column group L%4 of rows 8j + L/4 (raw layout); rows with valid ==
-// false read as zero. transpose_chunk() then hands each lane its own row.
-__device__ __forceinline__ void load_chunk_raw(uint4 (&raw)[4], const gg_bf16* src, bool valid) {
+// Warp-collective coalesced fetch of a 32-row x 32-column BF16 chunk (rows
+// row0 + r * ld): lane L loads column group L%4 of rows 8j + L/4 (raw
+// layout); rows r >= nvalid read as zero. transpose_chunk() then hands each
+// lane its own row.
+__device__ __forceinline__ void load_chunk_raw(uint4 (&raw)[4], const gg_bf16* row0, long long ld,
+                                               int nvalid) {
   const int lane = threadIdx.x & 31;
-  const unsigned long long mine = reinterpret_cast<unsigned long long>(src);
-  const int ok_mine = valid ? 1 : 0;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int r = 8 * j + (lane >> 2);
-    const unsigned long long p = __shfl_sync(0xFFFFFFFFu, mine, r);
-    raw[j] = __shfl_sync(0xFFFFFFFFu, ok_mine, r)
-                 ? __ldg(reinterpret_cast<const uint4*>(p) + (lane & 3))
-                 : make_uint4(0u, 0u, 0u, 0u);
+    raw[j] = r < nvalid ? __ldg(reinterpret_cast<const uint4*>(row0 + r * ld) + (lane & 3))
+                        : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -422,6 +418,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
       const int mt = mp * kCluster + static_cast<int>(crank);
       const long long grow = static_cast<long long>(st.row_start[e]) + mt * BM + r;
       const bool valid = grow < st.row_start[e + 1];
+      // the warp's 32 rows are consecutive: row 0 is grow0, rows < nvalid exist
+      const long long grow0 = grow - lane;
+      const int nvalid = static_cast<int>(
+          max(0LL, min(32LL, static_cast<long long>(st.row_start[e + 1]) - grow0)));
       uint4* stg = reinterpret_cast<uint4*>(smem + STAGES * STAGE_BYTES +
                                             (warp - 2) * kWarpStagingBytes);
       if (MODE == kFwdPlain || MODE == kDgradPlain) {
@@ -429,7 +429,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         if (MODE == kDgradPlain && p.row_scale != nullptr && valid) scale = p.row_scale[grow];
         const int n0 = nt * BN;
         const int c0 = half * (BN / 2);
-        gg_bf16* crow = p.C + grow * p.ldc + n0;
+        gg_bf16* crow0 = p.C + grow0 * p.ldc + n0;
         if (!mbar_wait_bounded(smem_u32(&st.tfull[acc]), acc_phase, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
@@ -440,7 +440,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
           tmem_ld32(tbase + c, v);
           uint4 w[4];
           pack_bf16x32(v, scale, w);
-          store_chunk(stg, w, crow + c, valid);
+          store_chunk(stg, w, crow0 + c, p.ldc, nvalid);
         }
       } else if (kGatedFwd) {
         const int F = p.F;
@@ -449,8 +449,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         const float prow = scaled && valid ? p.row_scale[grow] : 1.0f;
         const int j0 = nt * (BN / 2);
         const int c0 = half * (BN / 4);
-        gg_bf16* arow = p.C + grow * F + j0;
-        gg_bf16* hrow = p.H1_save + grow * (2LL * F) + j0;
+        gg_bf16* arow0 = p.C + grow0 * F + j0;
+        gg_bf16* hrow0 = p.H1_save + grow0 * (2LL * F) + j0;
         if (!mbar_wait_bounded(smem_u32(&st.tfull[acc]), acc_phase, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
@@ -468,14 +468,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
           }
           if (p.H1_save != nullptr) {
             pack_bf16x32(g, 1.0f, w);
-            store_chunk(stg, w, hrow + c, valid);
+            store_chunk(stg, w, hrow0 + c, 2LL * F, nvalid);
             pack_bf16x32(u, 1.0f, w);
-            store_chunk(stg, w, hrow + F + c, valid);
+            store_chunk(stg, w, hrow0 + F + c, 2LL * F, nvalid);
           }
 #pragma unroll
           for (int i = 0; i < 32; ++i) g[i] = glu_mul(g[i], u[i], alpha, scaled, prow);
           pack_bf16x32(g, 1.0f, w);
-          store_chunk(stg, w, arow + c, valid);
+          store_chunk(stg, w, arow0 + c, F, nvalid);
         }
       } else {  // gated backward: F = Nout, output row [dg | du] of width 2F
         const int F = p.Nout;
@@ -484,14 +484,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         const int n0 = nt * BN;
         const int c0 = half * (BN / 2);
         const int c_end = min(c0 + BN / 2, F - n0);  // multiple of 32 (F % 64 == 0)
-        const gg_bf16* hrow = p.H1 + grow * (2LL * F) + n0;
-        gg_bf16* drow = p.C + grow * (2LL * F) + n0;
+        const gg_bf16* hrow0 = p.H1 + grow0 * (2LL * F) + n0;
+        gg_bf16* drow0 = p.C + grow0 * (2LL * F) + n0;
         // The saved H1 does not depend on the accumulator: fetch the first
         // chunk before waiting for the MMAs, then always one chunk ahead.
         uint4 graw[4], uraw[4];
         if (c0 < c_end) {
-          load_chunk_raw(graw, hrow + c0, valid);
-          load_chunk_raw(uraw, hrow + F + c0, valid);
+          load_chunk_raw(graw, hrow0 + c0, 2LL * F, nvalid);
+          load_chunk_raw(uraw, hrow0 + F + c0, 2LL * F, nvalid);
         }
         if (!mbar_wait_bounded(smem_u32(&st.tfull[acc]), acc_phase, abort_flag, p.status)) break;
         tc_fence_after();
@@ -507,8 +507,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
           transpose_chunk(stg, graw, gw);
           transpose_chunk(stg, uraw, uw);
           if (c + 32 < c_end) {
-            load_chunk_raw(graw, hrow + c + 32, valid);
-            load_chunk_raw(uraw, hrow + F + c + 32, valid);
+            load_chunk_raw(graw, hrow0 + c + 32, 2LL * F, nvalid);
+            load_chunk_raw(uraw, hrow0 + F + c + 32, 2LL * F, nvalid);
           }
           uint32_t gs[16], us[16];
 #pragma unroll
@@ -538,9 +538,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
           }
           uint4 w[4];
           pack_bf16x32(dg, 1.0f, w);
-          store_chunk(stg, w, drow + c, valid);
+          store_chunk(stg, w, drow0 + c, 2LL * F, nvalid);
           pack_bf16x32(du, 1.0f, w);
-          store_chunk(stg, w, drow + F + c, valid);
+          store_chunk(stg, w, drow0 + F + c, 2LL * F, nvalid);
         }
         if (p.rowdot != nullptr && valid)
           p.rowdot[grow * p.rowdot_stride + nt * 2 + half] = rdot;
