@@ -74,7 +74,7 @@ typedef struct CUstream_st* gg_stream_t;  /* same handle as cudaStream_t */
 
 typedef enum gg_status {
   GG_OK = 0,
-  GG_ERR_INVALID_ARG = 1,          /* null pointer, negative size, k > E, ... */
+  GG_ERR_INVALID_ARG = 1,          /* null pointer, negative size, k > 32, ... */
   GG_ERR_UNSUPPORTED_SHAPE = 2,    /* H or F not a multiple of 64, E > 1024, ... */
   GG_ERR_MISALIGNED = 3,           /* a matrix pointer is not 16-byte aligned */
   GG_ERR_WORKSPACE_TOO_SMALL = 4,

@@ -142,7 +142,7 @@ gg_status gg_permute(const gg_bf16* x, const int32_t* idx, const float* prob, in
                      int32_t* row_of_slot, int32_t* slot_of_row, float* prob_of_row, void* ws,
                      size_t ws_bytes, gg_stream_t stream) {
   if (T < 0 || H <= 0 || k <= 0 || E <= 0 || pad_multiple <= 0) return GG_ERR_INVALID_ARG;
-  if (k > E || k > 32) return GG_ERR_INVALID_ARG;
+  if (k > 32) return GG_ERR_INVALID_ARG;  // k > E is legal: duplicate ids share an expert
   if (E > kMaxExperts || H % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
   if (r_cap_of(T, k, E, pad_multiple) > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
   if (offsets == nullptr) return GG_ERR_INVALID_ARG;

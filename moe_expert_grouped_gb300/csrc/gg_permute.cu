@@ -696,7 +696,7 @@ extern "C" gg_status gg_permute_noalloc(const gg_bf16* x, const int32_t* idx, co
                                         gg_stream_t stream) {
   using namespace gg;
   if (T < 0 || H <= 0 || k <= 0 || E <= 0 || pad_multiple <= 0) return GG_ERR_INVALID_ARG;
-  if (k > E || k > 32) return GG_ERR_INVALID_ARG;
+  if (k > 32) return GG_ERR_INVALID_ARG;
   if (E > kMaxExperts || H % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
   const long long R_cap = static_cast<long long>(T) * k + static_cast<long long>(E) * (pad_multiple - 1);
   if (R_cap > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;

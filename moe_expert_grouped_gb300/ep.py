@@ -1,0 +1,134 @@
+"""Expert parallelism around the grouped expert layer.
+
+Each of W ranks owns E / W experts (rank r: experts [r*El, (r+1)*El)) and their
+weights. A rank's routed (token, slot) pairs are grouped by the rank that owns
+their expert, the rows are exchanged with one all-to-all (counts first, then
+rows and local expert ids), every rank runs the grouped expert MLP on the rows
+it received (one slot per row, no probability), the outputs travel back with
+the reverse all-to-all and the sending rank combines them with the routing
+probabilities. The backward mirrors it: the output gradient goes out in the
+same order, the input-gradient rows and the per-row probability gradients
+come back, and the sender sums the rows weighted by the probabilities
+("perf(moe): add frozen grouped GEMM for adapter training",
+AlignmentResearch/Megatron-LM PR #3, "B200 throughput evidence": ordinary
+all-to-all dispatch around the local grouped GEMM).
+
+The exchange uses torch.distributed (NCCL between GPUs, gloo on CPU); the
+rank-local steps come from an ``ops`` object: ``GgOps`` runs them with this
+library's kernels on the rank's GPU. Counts are read on the host once per
+exchange (uneven all-to-all splits need them).
+"""
+
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+import torch.distributed as dist
+
+
+def _a2a(x: torch.Tensor, out_counts, in_counts, group) -> torch.Tensor:
+    """Uneven all-to-all along dim 0 (identity on one rank)."""
+    if group is None and not dist.is_initialized():
+        return x
+    out = x.new_empty((int(sum(out_counts)),) + tuple(x.shape[1:]))
+    dist.all_to_all_single(out, x.contiguous(), list(out_counts), list(in_counts), group=group)
+    return out
+
+
+def _exchange_counts(send_counts: torch.Tensor, group) -> torch.Tensor:
+    if group is None and not dist.is_initialized():
+        return send_counts.clone()
+    recv = torch.empty_like(send_counts)
+    dist.all_to_all_single(recv, send_counts.contiguous(), group=group)
+    return recv
+
+
+class GgOps:
+    """Rank-local steps with the library's kernels (CUDA tensors)."""
+
+    def __init__(self, H: int, F: int, El: int, activation: int = 0):
+        from . import gg  # the CUDA library: loaded only when these ops are used
+
+        self.gg = gg
+        self.H, self.F, self.El, self.activation = H, F, El, activation
+        self._layer = None
+
+    def group_by_rank(self, x, dest, prob, world: int) -> dict:
+        # the stable counting sort of the pairs by destination rank is the
+        # permute with the ranks as "experts"
+        return self.gg.permute(x, dest, prob, world, 1)
+
+    def to_send_order(self, src, maps: dict, k: int, world: int) -> torch.Tensor:
+        n = src.shape[0] * k
+        return self.gg.permute_rows(src, maps["row_of_slot"], maps["slot_of_row"],
+                                    maps["offsets"], k, world, 1, n, maps["ws"])
+
+    def local_forward(self, rows, local_eid, W1, W2) -> torch.Tensor:
+        n = rows.shape[0]
+        self._layer = self.gg.MoeLayer(n, self.H, self.F, 1, self.El, 1, device=rows.device,
+                                       activation=self.activation)
+        ones = torch.ones((n, 1), dtype=torch.float32, device=rows.device)
+        return self._layer.forward(rows, local_eid.view(n, 1), ones, W1, W2)
+
+    def local_backward(self, d_rows, W1, W2):
+        dX, dprob = self._layer.backward(d_rows, W1, W2, dprob=True)
+        return dX, dprob.view(-1)
+
+    def combine(self, rows, maps: dict, prob, T: int, k: int) -> torch.Tensor:
+        return self.gg.unpermute_combine(rows, maps["row_of_slot"], prob, T, k, maps["ws"])
+
+
+class ExpertParallelLayer:
+    """The expert layer over ``E`` experts spread evenly over the ranks of
+    ``group`` (one rank when torch.distributed is not initialised).
+
+    forward(x [T, H], idx [T, k] global expert ids, prob [T, k], W1_local
+    [E/W, 2F, H], W2_local [E/W, H, F]) -> out [T, H]; backward(dOut) ->
+    (dX [T, H], dprob [T, k]) after a forward, the probability applied at the
+    combine.
+    """
+
+    def __init__(self, H: int, F: int, k: int, E: int, group=None, ops=None):
+        self.group = group
+        distributed = group is not None or dist.is_initialized()
+        self.world = dist.get_world_size(group) if distributed else 1
+        self.rank = dist.get_rank(group) if distributed else 0
+        if E % self.world != 0:
+            raise ValueError(f"{E} experts do not split evenly over {self.world} ranks")
+        self.H, self.F, self.k, self.E = H, F, k, E
+        self.El = E // self.world
+        self.ops = ops if ops is not None else GgOps(H, F, self.El)
+        self._ctx: Optional[tuple] = None
+
+    def forward(self, x, idx, prob, W1_local, W2_local):
+        T, k, W, El = x.shape[0], self.k, self.world, self.El
+        dest = torch.div(idx, El, rounding_mode="floor").to(torch.int32)
+        maps = self.ops.group_by_rank(x, dest, prob, W)
+        n = T * k
+        send = (maps["offsets"][1:] - maps["offsets"][:-1]).to(torch.int64)
+        recv = _exchange_counts(send, self.group)
+        send_l, recv_l = send.tolist(), recv.tolist()
+        # local expert id of every sent row (row r carries pair slot_of_row[r])
+        eid = torch.remainder(idx.reshape(-1), El).to(torch.int32)[maps["slot_of_row"][:n].long()]
+        rows = _a2a(maps["Xp"][:n], recv_l, send_l, self.group)
+        eids = _a2a(eid, recv_l, send_l, self.group)
+        y = self.ops.local_forward(rows, eids, W1_local, W2_local)
+        y_back = _a2a(y, send_l, recv_l, self.group)
+        self._ctx = (maps, send_l, recv_l, prob, T)
+        return self.ops.combine(y_back, maps, prob, T, k)
+
+    def backward(self, dOut, W1_local, W2_local):
+        if self._ctx is None:
+            raise RuntimeError("backward needs a forward first")
+        maps, send_l, recv_l, prob, T = self._ctx
+        k, n = self.k, T * self.k
+        d_send = self.ops.to_send_order(dOut, maps, k, self.world)[:n]
+        d_rows = _a2a(d_send, recv_l, send_l, self.group)
+        dx_rows, dp_rows = self.ops.local_backward(d_rows, W1_local, W2_local)
+        dx_back = _a2a(dx_rows, send_l, recv_l, self.group)
+        dp_back = _a2a(dp_rows, send_l, recv_l, self.group)
+        # the remote rows carry no probability: weight them in the sum
+        dX = self.ops.combine(dx_back, maps, prob, T, k)
+        dprob = dp_back[maps["row_of_slot"].long()].view(T, k)
+        return dX, dprob

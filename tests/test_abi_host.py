@@ -93,9 +93,9 @@ def test_validation_rejects_before_launch(gg):
     p = ctypes.c_void_p(1 << 40)
     mis = ctypes.c_void_p((1 << 40) + 8)
     ws = ctypes.c_void_p(1 << 41)
-    # gg_permute: bad sizes, k > E, k > 32, H not a multiple of 64, misaligned x
+    # gg_permute: bad sizes, k > 32, H not a multiple of 64, misaligned x (k > E is
+    # legal: a token may name one expert in several slots)
     assert L.gg_permute(p, p, p, 4, 64, 2, 4, 0, p, p, p, p, p, ws, 1 << 20, None) == 1
-    assert L.gg_permute(p, p, p, 4, 64, 5, 4, 1, p, p, p, p, p, ws, 1 << 20, None) == 1
     assert L.gg_permute(p, p, p, 4, 64, 33, 64, 1, p, p, p, p, p, ws, 1 << 20, None) == 1
     assert L.gg_permute(p, p, p, 4, 96, 2, 4, 1, p, p, p, p, p, ws, 1 << 20, None) == 2
     assert L.gg_permute(p, p, p, 4, 64, 2, 2048, 1, p, p, p, p, p, ws, 1 << 30, None) == 2

@@ -171,6 +171,8 @@ def _permute_case(T, E, k, seed, skew=None, dup=False):
     (256, 64, 4, 2, 1, {}), (300, 256, 8, 2, 1, {}), (300, 256, 8, 2, 16, {}),
     (1, 64, 1, 1, 1, {}), (5000, 128, 16, 1, 1, {"skew": 7}), (3000, 64, 1024, 8, 1, {}),
     (700, 192, 6, 3, 256, {"dup": True}), (4096, 64, 128, 8, 256, {}),
+    # more slots than experts (the grouping by rank of expert parallelism)
+    (600, 64, 2, 8, 1, {"dup": True}), (300, 128, 4, 8, 16, {"dup": True}),
 ])
 def test_permute_bit_exact(gg, T, H, E, k, P, extra):
     idx, prob = _permute_case(T, E, k, T + E, **extra)
