@@ -50,35 +50,44 @@ def load_peaks():
 
 # ------------------------------------------------------------------ captured DRAM traffic
 
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_dram_traffic_balanced_e128_t16384.md")
-GEMM_SOURCES = [os.path.join(ROOT, "moe_expert_grouped_gb300", "csrc", f)
-                for f in ("gg_gemm.cu", "gg_ptx.cuh", "gg_internal.h")]
+_CSRC = os.path.join(ROOT, "moe_expert_grouped_gb300", "csrc")
+TRAFFIC_FILES = {
+    "bf16": os.path.join(ROOT, "profiles", "gemm_dram_traffic_balanced_e128_t16384.md"),
+    "mxfp8": os.path.join(ROOT, "profiles", "gemm_mx_dram_traffic_balanced_e128_t16384.md"),
+}
+GEMM_SOURCES = {
+    "bf16": [os.path.join(_CSRC, f) for f in ("gg_gemm.cu", "gg_epilogue.cuh", "gg_ptx.cuh",
+                                              "gg_internal.h")],
+    "mxfp8": [os.path.join(_CSRC, f) for f in ("gg_gemm_mx.cu", "gg_mx.cuh", "gg_epilogue.cuh",
+                                               "gg_ptx.cuh", "gg_internal.h")],
+}
 
 
-def gemm_sources_sha256() -> str:
+def gemm_sources_sha256(precision: str = "bf16") -> str:
     import hashlib
 
     h = hashlib.sha256()
-    for f in GEMM_SOURCES:
+    for f in GEMM_SOURCES[precision]:
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
 
-def captured_traffic(op: str, workload: str):
+def captured_traffic(op: str, workload: str, precision: str = "bf16"):
     """DRAM bytes (read + write) per launch of `op` from the committed ncu
     summary, or None when there is none for this workload or the GEMM sources
     changed since it was captured."""
-    if not os.path.exists(TRAFFIC_FILE):
+    path = TRAFFIC_FILES[precision]
+    if not os.path.exists(path):
         return None
     fields = {}
-    with open(TRAFFIC_FILE) as f:
+    with open(path) as f:
         for line in f:
             line = line.strip().lstrip("-").strip()
             if ":" in line:
                 key, _, val = line.partition(":")
                 fields[key.strip().strip("`")] = val.strip().strip("`")
-    if fields.get("sources_sha256") != gemm_sources_sha256():
+    if fields.get("sources_sha256") != gemm_sources_sha256(precision):
         return None
     if fields.get("workload") != workload:
         return None
@@ -236,20 +245,82 @@ def run_gg(args, shape, peaks):
     epi_b = gg.GG_EPI_QGEGLU_BWD if act == gg.GG_ACT_QGEGLU else gg.GG_EPI_SWIGLU_BWD
     pre = mode == gg.GG_PROB_PRE_FC1
     rec = args.recompute_h1
-    layer = gg.MoeLayer(T, H, F, k, E, P, device=dev, activation=act, prob_mode=mode,
-                        recompute_h1=rec)
-    b = {n: layer.view(n) for n in ("Xp", "H1", "A", "Yp", "dYp", "dH", "dXp", "offsets",
-                                    "row_of_slot", "slot_of_row", "prob_of_row", "rowdot", "ws")}
+    mx = args.precision == "mxfp8"
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     dX = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     dprob = torch.empty((T, k), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    if mx:
+        # the frozen weights are quantised once, outside the timed region
+        mxw, _ = gg.mx_prepare_weights(W1, W2)
+        layer = gg.MxMoeLayer(T, H, F, k, E, P, device=dev, activation=act, prob_mode=mode)
+        b = {n: layer.view(n) for n in gg.MxMoeLayer._SHAPES}
+        ops = ["permute", "quant_x", "fc1_swiglu", "fc2", "combine", "quant_dout",
+               "dgrad_fc2_swiglu_bwd", "dgrad_fc1", "combine_dx"]
+
+        def run_layer(x_, idx_, prob_, dO_, o_, dX_, dp_):
+            layer.forward(x_, idx_, prob_, mxw, out=o_)
+            layer.backward(dO_, mxw, dX=dX_, dprob=dp_)
+    else:
+        layer = gg.MoeLayer(T, H, F, k, E, P, device=dev, activation=act, prob_mode=mode,
+                            recompute_h1=rec)
+        b = {n: layer.view(n) for n in ("Xp", "H1", "A", "Yp", "dYp", "dH", "dXp", "offsets",
+                                        "row_of_slot", "slot_of_row", "prob_of_row", "rowdot",
+                                        "ws")}
+        ops = ["permute", "fc1_swiglu", "fc2", "combine", "permute_dout",
+               "dgrad_fc2_swiglu_bwd", "dgrad_fc1", "combine_dx"]
+        if rec:
+            ops.insert(4, "fc1_recompute")
+
+        def run_layer(x_, idx_, prob_, dO_, o_, dX_, dp_):
+            layer.forward(x_, idx_, prob_, W1, W2, out=o_)
+            layer.backward(dO_, W1, W2, dX=dX_, dprob=dp_)
     ws = b["ws"]
     rc = layer.R_cap
-    stream = torch.cuda.current_stream(dev)
-    ops = ["permute", "fc1_swiglu", "fc2", "combine", "permute_dout", "dgrad_fc2_swiglu_bwd",
-           "dgrad_fc1", "combine_dx"]
-    if rec:
-        ops.insert(4, "fc1_recompute")
+
+    def step_mx(events=None):
+        # the same calls, in the same order, as gg_moe_mlp_fwd_mx + gg_moe_mlp_bwd_mx
+        def mark(i):
+            if events is not None:
+                events[i].record(stream)
+
+        por = b["prob_of_row"]
+        nt = int(layer.buf.n_tiles)
+        mark(0)
+        gg.permute(x, idx, prob, E, P, ws=ws, out=dict(b, Xp=None))
+        mark(1)
+        gg.mx_quantize_rows(x, b["slot_of_row"], b["offsets"], k, E, rc, ws,
+                            prob_of_row=por if pre else None, n_tiles=nt,
+                            out=dict(Q=b["Xq"], S=b["Xs"], tiles_before=b["tiles_before"]))
+        mark(2)
+        gg.mx_grouped_gemm(gg.GG_MX_FC1, b["Xq"], b["Xs"], mxw, b["offsets"], E, rc, H, F, ws,
+                           activation=act, Cq=b["Aq"], Cs=b["As"], H1=b["H1"],
+                           row_scale=por if mode == gg.GG_PROB_ACTIVATION else None)
+        mark(3)
+        gg.mx_grouped_gemm(gg.GG_MX_FC2, b["Aq"], b["As"], mxw, b["offsets"], E, rc, H, F, ws,
+                           activation=act, C=b["Yp"])
+        mark(4)
+        gg.unpermute_combine(b["Yp"], b["row_of_slot"], prob if mode == gg.GG_PROB_COMBINE else None,
+                             T, k, ws, out=out)
+        mark(5)
+        gg.mx_quantize_rows(dOut, b["slot_of_row"], b["offsets"], k, E, rc, ws, n_tiles=nt,
+                            out=dict(Q=b["dYq"], S=b["dYs"], tiles_before=b["tiles_before"]))
+        mark(6)
+        gg.mx_grouped_gemm(gg.GG_MX_DGRAD_FC2, b["dYq"], b["dYs"], mxw, b["offsets"], E, rc, H, F,
+                           ws, activation=act, Cq=b["dHq"], Cs=b["dHs"], H1=b["H1"],
+                           row_scale=None if pre else por, rowdot=None if pre else b["rowdot"])
+        mark(7)
+        gg.mx_grouped_gemm(gg.GG_MX_DGRAD_FC1, b["dHq"], b["dHs"], mxw, b["offsets"], E, rc, H, F,
+                           ws, activation=act, C=b["dXp"])
+        mark(8)
+        if pre:
+            gg.unpermute_combine(b["dXp"], b["row_of_slot"], prob, T, k, ws, out=dX, dprob=dprob,
+                                 dot_src=x)
+        else:
+            gg.unpermute_combine(b["dXp"], b["row_of_slot"], None, T, k, ws, out=dX,
+                                 rowdot=b["rowdot"], dprob=dprob,
+                                 n_rowdot=gg.mx_rowdot_blocks(F))
+        mark(9)
 
     def step(events=None):
         # the same calls, in the same order, as gg_moe_mlp_fwd + gg_moe_mlp_bwd
@@ -296,6 +367,8 @@ def run_gg(args, shape, peaks):
                                  rowdot=b["rowdot"], dprob=dprob, n_rowdot=gg.rowdot_blocks(F))
         mark(i + 4)
 
+    if mx:
+        step = step_mx  # noqa: F811
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -374,8 +447,7 @@ def run_gg(args, shape, peaks):
             o_, dX_, dp_ = d_res[i]
             stream.wait_event(ev_in[i])
             stream.wait_event(ev_out[i])
-            layer.forward(dx_, didx_, dprob_, W1, W2, out=o_)
-            layer.backward(ddO_, W1, W2, dX=dX_, dprob=dp_)
+            run_layer(dx_, didx_, dprob_, ddO_, o_, dX_, dp_)
             ev_used[i].record(stream)
             with torch.cuda.stream(s_d2h):
                 s_d2h.wait_event(ev_used[i])
@@ -414,8 +486,12 @@ def run_gg(args, shape, peaks):
     def hbm_bytes(op):
         # algorithmic bytes: permute reads idx/prob and writes the row maps;
         # the combines read k rows per token (+ row map, prob) and write one
-        return {"permute": (T + R) * H * 2 + 8 * R + 4 * R + 8 * rc,
+        # (MXFP8: the permute writes the row maps only, the row quantisers
+        # read each token row once and write one E4M3 row + scales per pair)
+        quant = T * H * 2 + R * H + R * H // 32 + 4 * rc
+        return {"permute": (8 * R + 4 * R + 8 * rc) + (0 if mx else (T + R) * H * 2),
                 "permute_dout": (T + R) * H * 2 + 4 * rc,
+                "quant_x": quant, "quant_dout": quant,
                 "combine": (R + T) * H * 2 + 8 * R,
                 "combine_dx": (R + T) * H * 2 + 4 * R}[op]
 
@@ -428,21 +504,24 @@ def run_gg(args, shape, peaks):
                "dgrad_fc2_swiglu_bwd": 2.0 * R * H * F, "dgrad_fc1": 4.0 * R * H * F,
                "fc1_recompute": 4.0 * R * H * F}
     dom = max(avg, key=lambda o: avg[o])
+    # MXFP8 contractions run at twice the BF16 rate (nominal 4.5 vs 2.25 PFLOP/s
+    # dense): their peak is the measured BF16 burst times that ratio
+    tensor_peak = peaks["bf16_tflops"] * (2.0 if mx else 1.0)
+    tensor_src = f"{peaks['source']} bf16 burst" + (" x 2 (nominal fp8/bf16 ratio)" if mx else "")
     if dom in flop_of:
         ach = flop_of[dom] / (avg[dom] / 1e3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 2),
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(ach / peaks["bf16_tflops"], 4),
-                "traffic": captured_traffic(dom, shape.name),
-                "peak_source": f"{peaks['source']} bf16 burst"}
+                "peak": round(tensor_peak, 1), "unit": "TFLOP/s",
+                "frac": round(ach / tensor_peak, 4),
+                "traffic": captured_traffic(dom, shape.name, args.precision),
+                "peak_source": tensor_src}
     else:
         byts = hbm_bytes(dom)
         ach = byts / (avg[dom] / 1e3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
-                "traffic": captured_traffic(dom, shape.name),
-                "peak_source": f"{peaks['source']} hbm copy"}
-    hbm_ops = {op: hbm_bytes(op) for op in ("permute", "permute_dout", "combine", "combine_dx")}
+                "traffic": None, "peak_source": f"{peaks['source']} hbm copy"}
+    hbm_ops = {op: hbm_bytes(op) for op in ops if op not in flop_of}
     kernels = {}
     for op in ops:
         entry = {"ms": round(avg[op], 4), "share": round(avg[op] / total_ms, 4)}
@@ -454,7 +533,7 @@ def run_gg(args, shape, peaks):
 
     # ---- CPU baseline: the oracle on a bounded token sample (rank 0, N = 1)
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not mx:
         times, n_tok = time_oracle(shape, inp, args.cpu_tokens, activation=args.activation,
                                    prob_mode=args.prob_mode)
         sub = shape.with_tokens(n_tok)
@@ -469,11 +548,13 @@ def run_gg(args, shape, peaks):
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tot_s / args.steps * 1e3, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8" if mx else "bf16",
+        "data": "synthetic",
         "config": {"workload": shape.name, "E": E, "H": H, "F": F, "T": T, "k": k, "P": P,
                    "routing": shape.routing, "parallelism": f"replicas x{world}",
                    "outputs": "out, dX, dprob", "activation": args.activation,
                    "prob_mode": args.prob_mode, "recompute_h1": rec,
+                   "precision": args.precision,
                    "l2": "inputs larger than L2 (weights 1.2 GB, activations > 1 GB per step)"},
         "tokens_per_s": round(tot_tokens / tot_s, 1),
         "pct_bf16_peak": {"vs_2250_tflops": round(value / world / 2250.0, 4),
@@ -487,6 +568,12 @@ def run_gg(args, shape, peaks):
         "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
         "launches_per_step": int(launches) // max(1, args.steps),
     }
+    if mx:
+        line["pct_fp8_peak"] = {"vs_4500_tflops": round(value / world / 4500.0, 4),
+                                "vs_measured_bf16_burst_x2": round(
+                                    value / world / (2 * peaks["bf16_tflops"]), 4)}
+        line["cpu_baseline_note"] = ("the oracle's MXFP8 layer quantises every expert's weights "
+                                     "in fp64; the timed CPU baseline is on the BF16 line")
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -559,9 +646,14 @@ def main(argv=None):
                     help="do not keep FC1's output for the backward; recompute it there")
     ap.add_argument("--prob-mode", choices=["combine", "activation", "pre_fc1"],
                     default="combine", help="where the routing probability is applied")
+    ap.add_argument("--precision", choices=["bf16", "mxfp8"], default="bf16",
+                    help="bf16: the frozen BF16 weights; mxfp8: MXFP8 operands on the "
+                         "block-scaled tensor cores (weights quantised once, untimed)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.precision == "mxfp8" and args.recompute_h1:
+        ap.error("--recompute-h1 is a BF16 option")
     shape = CONFIGS[args.config]
     if args.tokens:
         shape = shape.with_tokens(args.tokens)

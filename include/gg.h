@@ -442,6 +442,149 @@ gg_status gg_moe_mlp_bwd_ex(const gg_bf16* dOut, const gg_bf16* x, const float* 
                             const gg_moe_options* opt, gg_bf16* dX, float* dprob,
                             const gg_moe_buffers* buf, gg_stream_t stream);
 
+/* -------------------------------------------------------------------------
+ * MXFP8 expert layer. [P3] "Validation": routed expert projections only in
+ * MXFP8, other modules BF16; [P4] "End-to-end GB300 validation": MXFP8 on
+ * GB300. The pages do not define the encoding; it is read as the OCP
+ * microscaling format with E4M3 elements: one E8M0 scale 2^e per 32
+ * consecutive elements along each GEMM's reduction dimension, e the smallest
+ * exponent with max|v| / 2^e <= 448 (clamped to [-127, 127]; -127 for an
+ * all-zero block), elements v * 2^-e rounded to nearest-even E4M3. Both
+ * operands of every GEMM are MXFP8 (block-scaled tcgen05 MMAs, FP32
+ * accumulation). Results pass between GEMMs as BF16 values that the next
+ * GEMM's quantiser reads: H1 (kept for the backward) and the activation
+ * bf16(act(H1)) before it is quantised for FC2, and likewise dH1 before the
+ * second input-gradient GEMM.
+ *
+ * Shapes: H and F multiples of 128, E <= 1024. The weights are quantised once
+ * (gg_mx_prepare_weights): along their input dimension for the forward and,
+ * transposed, along their output dimension for the input gradient.
+ *
+ * Scale tiles (bytes holding E8M0 codes e + 127):
+ *  - activation operands: per expert-local 128-row tile t of expert e, tile
+ *    index tiles_before[e] + t (tiles_before = exclusive prefix sum of
+ *    ceil(rows_e / 128)); for K = 128 * KG columns a tile holds KG blocks of
+ *    512 bytes, byte (r % 32) * 16 + (r / 32) * 4 + b of block kg holding the
+ *    scale of row r of the tile, 32-column block 4 * kg + b. Rows of a tile
+ *    past the expert's end hold code 0. Every activation scale buffer holds
+ *    gg_mx_row_tiles() tiles.
+ *  - weight operands: per expert and 192-column tile of the GEMM that reads
+ *    them (FC1: 96 gate rows followed by the 96 matching up rows, FC1 tile j
+ *    covering gate rows 96j..), KG blocks of 1024 bytes, byte
+ *    (n / 128) * 512 + ((n % 128) % 32) * 16 + ((n % 128) / 32) * 4 + b for
+ *    column n of the tile; columns past the weight's rows hold code 0.
+ * ------------------------------------------------------------------------- */
+
+/* Row-scale tiles of one activation operand: ceil(R_cap / 128) + E. */
+int gg_mx_row_tiles(int T, int k, int E, int pad_multiple);
+
+/* Byte offsets of the prepared weights inside the buffer of
+ * gg_mx_prepare_weights (each piece 256-byte aligned). */
+typedef struct gg_mx_weights_layout {
+  size_t w1, w1_scales;   /* FC1: E4M3 [E][2F][H], along H; scale tiles
+                             [E][ceil(F/96)][H/128]                        */
+  size_t w2, w2_scales;   /* FC2: E4M3 [E][H][F], along F;
+                             [E][ceil(H/192)][F/128]                       */
+  size_t w2t, w2t_scales; /* input gradient of FC2: E4M3 [E][F][H] = W2
+                             transposed, along H; [E][ceil(F/192)][H/128]  */
+  size_t w1t, w1t_scales; /* input gradient of FC1: E4M3 [E][H][2F] = W1
+                             transposed, along 2F; [E][ceil(H/192)][2F/128] */
+  size_t bytes;           /* total                                         */
+} gg_mx_weights_layout;
+
+/* Host only. GG_ERR_UNSUPPORTED_SHAPE unless H % 128 == 0, F % 128 == 0 and
+ * 0 < E <= 1024. */
+gg_status gg_mx_weights_layout_of(int E, int H, int F, gg_mx_weights_layout* out);
+
+/* Quantise the frozen BF16 weights W1 [E][2F][H] and W2 [E][H][F] into the
+ * four MXFP8 operands at `mxw` (device, 256-byte aligned, `bytes` >= the
+ * layout's total). Run once per weight set; the layer calls read `mxw` only. */
+gg_status gg_mx_prepare_weights(const gg_bf16* W1, const gg_bf16* W2, int E, int H, int F,
+                                void* mxw, size_t bytes, gg_stream_t stream);
+
+/* Permuted MXFP8 activation operand. Writes tiles_before[E+1] from offsets,
+ * then for every row r < offsets[E]: Q[r] = the E4M3 codes of
+ * src[slot_of_row[r] / k] (times prob_of_row[r], rounded to BF16, when
+ * prob_of_row is not NULL), zeros where slot_of_row[r] is -1; scales into S
+ * (n_tiles tiles of K/128 blocks). src [T][K] BF16, Q [R_cap][K], K a
+ * multiple of 128. */
+gg_status gg_mx_quantize_rows(const gg_bf16* src, int T, int K, int k,
+                              const int32_t* slot_of_row, const int32_t* offsets,
+                              const float* prob_of_row, int E, int R_cap, int n_tiles,
+                              int32_t* tiles_before, uint8_t* Q, uint8_t* S, void* ws,
+                              size_t ws_bytes, gg_stream_t stream);
+
+/* The four MXFP8 grouped GEMMs of the layer, with the weights of `mxw`:
+ *  GG_MX_FC1        A = Xq [R_cap][H]: H1 = bf16(A W1^T) stored to H1 (may
+ *                   be NULL), a = bf16(act(H1) [* row_scale]) quantised to
+ *                   Cq [R_cap][F] + Cs;
+ *  GG_MX_FC2        A = Aq [R_cap][F]: C = bf16(A W2^T) [R_cap][H];
+ *  GG_MX_DGRAD_FC2  A = dYq [R_cap][H]: dA = (A W2) [* row_scale], dH1 =
+ *                   bf16(act'(H1) applied to dA) quantised to Cq [R_cap][2F]
+ *                   + Cs; rowdot (may be NULL) gets per-row partial sums of
+ *                   <A W2, act(H1)>, gg_mx_rowdot_blocks(F) of them,
+ *                   gg_mx_rowdot_stride(F) floats apart;
+ *  GG_MX_DGRAD_FC1  A = dHq [R_cap][2F]: C = bf16(A W1) [R_cap][H].
+ * `activation` is a gg_activation; As, Cs hold n_tiles row-scale tiles. */
+typedef enum gg_mx_gemm {
+  GG_MX_FC1 = 0,
+  GG_MX_FC2 = 1,
+  GG_MX_DGRAD_FC2 = 2,
+  GG_MX_DGRAD_FC1 = 3
+} gg_mx_gemm;
+int gg_mx_rowdot_blocks(int F);
+int gg_mx_rowdot_stride(int F);
+gg_status gg_mx_grouped_gemm(int which, int activation, const uint8_t* Aq, const uint8_t* As,
+                             const void* mxw, const int32_t* offsets, int E, int R_cap, int H,
+                             int F, int n_tiles, gg_bf16* C, uint8_t* Cq, uint8_t* Cs,
+                             gg_bf16* H1, const float* row_scale, float* rowdot, void* ws,
+                             size_t ws_bytes, gg_stream_t stream);
+
+/* Buffers of the MXFP8 layer, carved by gg_mx_buffers_bind(). */
+typedef struct gg_mx_buffers {
+  uint8_t* Xq;          /* [R_cap][H]  permuted input, E4M3               */
+  uint8_t* Xs;          /* its row-scale tiles                            */
+  gg_bf16* H1;          /* [R_cap][2F] FC1 output, kept for the backward  */
+  uint8_t* Aq;          /* [R_cap][F]  activation, E4M3                   */
+  uint8_t* As;
+  gg_bf16* Yp;          /* [R_cap][H]  FC2 output                         */
+  uint8_t* dYq;         /* [R_cap][H]  permuted output gradient, E4M3     */
+  uint8_t* dYs;
+  uint8_t* dHq;         /* [R_cap][2F] gradient of H1, E4M3               */
+  uint8_t* dHs;
+  gg_bf16* dXp;         /* [R_cap][H]  gradient of the permuted input     */
+  int32_t* offsets;     /* [E+1]                                          */
+  int32_t* row_of_slot; /* [T*k]                                          */
+  int32_t* slot_of_row; /* [R_cap]                                        */
+  float* prob_of_row;   /* [R_cap]                                        */
+  int32_t* tiles_before;/* [E+1]                                          */
+  float* rowdot;        /* [R_cap][gg_mx_rowdot_stride(F)]                */
+  int n_tiles;          /* gg_mx_row_tiles(T, k, E, pad_multiple)         */
+  void* ws;             /* gg_workspace_size(T, k, E) bytes, status first */
+  size_t ws_bytes;
+} gg_mx_buffers;
+
+size_t gg_mx_buffers_size(int T, int H, int F, int k, int E, int pad_multiple);
+gg_status gg_mx_buffers_bind(void* base, size_t bytes, int T, int H, int F, int k, int E,
+                             int pad_multiple, gg_mx_buffers* out);
+
+/* The MXFP8 layer: forward (permute -> quantise rows -> FC1 + activation +
+ * quantise -> FC2 -> combine into out[T][H]) and backward (quantise dOut
+ * rows -> input gradient of FC2 + activation backward + quantise -> input
+ * gradient of FC1 -> combine into dX[T][H], dprob[T][k] when not NULL).
+ * Options as gg_moe_mlp_fwd_ex except recompute_h1, which must be 0
+ * (GG_ERR_INVALID_ARG). dprob is the gradient where the probability meets
+ * the activation: sum over the row of (A W2) * act(H1) for the combine and
+ * weighted-activation modes, <x_t, dXp[row]> for the pre-FC1 mode. */
+gg_status gg_moe_mlp_fwd_mx(const gg_bf16* x, const int32_t* idx, const float* prob,
+                            const void* mxw, int T, int H, int F, int k, int E,
+                            int pad_multiple, const gg_moe_options* opt, gg_bf16* out,
+                            const gg_mx_buffers* buf, gg_stream_t stream);
+gg_status gg_moe_mlp_bwd_mx(const gg_bf16* dOut, const gg_bf16* x, const float* prob,
+                            const void* mxw, int T, int H, int F, int k, int E,
+                            int pad_multiple, const gg_moe_options* opt, gg_bf16* dX,
+                            float* dprob, const gg_mx_buffers* buf, gg_stream_t stream);
+
 /* Test hook for the bounded waits: one CTA waits on a barrier that nothing
  * completes, gives up after `limit_ns` nanoseconds (clamped to 1 s), writes
  * GG_ERR_DEVICE_TIMEOUT into the status word and returns normally. */

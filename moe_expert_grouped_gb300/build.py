@@ -19,7 +19,7 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libgg.so")
-SOURCES = ["gg_api.cu", "gg_permute.cu", "gg_gemm.cu"]
+SOURCES = ["gg_api.cu", "gg_permute.cu", "gg_gemm.cu", "gg_gemm_mx.cu", "gg_mx_quant.cu"]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -600,6 +600,336 @@ gg_status gg_moe_mlp_bwd(const gg_bf16* dOut, const gg_bf16* W1, const gg_bf16* 
                            dX, dprob, buf, stream);
 }
 
+// ------------------------------------------------------------------ MXFP8
+
+static bool mx_shape_ok(int E, int H, int F) {
+  return E > 0 && E <= kMaxExperts && H > 0 && F > 0 && H % 128 == 0 && F % 128 == 0;
+}
+
+int gg_mx_row_tiles(int T, int k, int E, int pad_multiple) {
+  if (T < 0 || k <= 0 || E <= 0 || pad_multiple <= 0) return 0;
+  const long long rc = r_cap_of(T, k, E, pad_multiple);
+  const long long n = (rc + 127) / 128 + E;
+  return n > 0x7FFFFFFFLL ? 0 : static_cast<int>(n);
+}
+
+int gg_mx_rowdot_blocks(int F) { return F > 0 ? 2 * ((F + 191) / 192) : 0; }
+
+int gg_mx_rowdot_stride(int F) { return (gg_mx_rowdot_blocks(F) + 7) / 8 * 8; }
+
+gg_status gg_mx_weights_layout_of(int E, int H, int F, gg_mx_weights_layout* out) {
+  if (out == nullptr) return GG_ERR_INVALID_ARG;
+  if (!mx_shape_ok(E, H, F)) return GG_ERR_UNSUPPORTED_SHAPE;
+  const size_t e = static_cast<size_t>(E), h = static_cast<size_t>(H), f = static_cast<size_t>(F);
+  const size_t sfb = 1024;
+  size_t at = 0;
+  auto take = [&at](size_t n) {
+    const size_t q = at;
+    at += align256(n);
+    return q;
+  };
+  out->w1 = take(e * 2 * f * h);
+  out->w1_scales = take(e * ((f + 95) / 96) * (h / 128) * sfb);
+  out->w2 = take(e * h * f);
+  out->w2_scales = take(e * ((h + 191) / 192) * (f / 128) * sfb);
+  out->w2t = take(e * f * h);
+  out->w2t_scales = take(e * ((f + 191) / 192) * (h / 128) * sfb);
+  out->w1t = take(e * h * 2 * f);
+  out->w1t_scales = take(e * ((h + 191) / 192) * (2 * f / 128) * sfb);
+  out->bytes = at;
+  return GG_OK;
+}
+
+gg_status gg_mx_prepare_weights(const gg_bf16* W1, const gg_bf16* W2, int E, int H, int F,
+                                void* mxw, size_t bytes, gg_stream_t stream) {
+  gg_mx_weights_layout L;
+  gg_status s = gg_mx_weights_layout_of(E, H, F, &L);
+  if (s != GG_OK) return s;
+  if (W1 == nullptr || W2 == nullptr || mxw == nullptr) return GG_ERR_INVALID_ARG;
+  if (!aligned16(W1) || !aligned16(W2) || (reinterpret_cast<uintptr_t>(mxw) & 255u) != 0)
+    return GG_ERR_MISALIGNED;
+  if (bytes < L.bytes) return GG_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo dev;
+  if ((s = device_ok(&dev)) != GG_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(mxw);
+  // scale bytes of columns past a weight's rows stay 0
+  const size_t scale_regions[4][2] = {{L.w1_scales, L.w2 - L.w1_scales},
+                                      {L.w2_scales, L.w2t - L.w2_scales},
+                                      {L.w2t_scales, L.w1t - L.w2t_scales},
+                                      {L.w1t_scales, L.bytes - L.w1t_scales}};
+  for (const auto& r : scale_regions) {
+    cudaError_t e = cudaMemsetAsync(base + r[0], 0, r[1], st);
+    if (e != cudaSuccess) return GG_ERR_CUDA;
+  }
+  cudaError_t e;
+  if ((e = launch_mx_prepare_weight(W1, E, 2 * F, H, false, F, (F + 95) / 96, base + L.w1,
+                                    base + L.w1_scales, st)) != cudaSuccess ||
+      (e = launch_mx_prepare_weight(W2, E, H, F, false, 0, (H + 191) / 192, base + L.w2,
+                                    base + L.w2_scales, st)) != cudaSuccess ||
+      (e = launch_mx_prepare_weight(W2, E, F, H, true, 0, (F + 191) / 192, base + L.w2t,
+                                    base + L.w2t_scales, st)) != cudaSuccess ||
+      (e = launch_mx_prepare_weight(W1, E, H, 2 * F, true, 0, (H + 191) / 192, base + L.w1t,
+                                    base + L.w1t_scales, st)) != cudaSuccess)
+    return GG_ERR_CUDA;
+  return GG_OK;
+}
+
+gg_status gg_mx_quantize_rows(const gg_bf16* src, int T, int K, int k,
+                              const int32_t* slot_of_row, const int32_t* offsets,
+                              const float* prob_of_row, int E, int R_cap, int n_tiles,
+                              int32_t* tiles_before, uint8_t* Q, uint8_t* S, void* ws,
+                              size_t ws_bytes, gg_stream_t stream) {
+  if (T < 0 || K <= 0 || k <= 0 || k > 32 || E <= 0 || R_cap < 0 || n_tiles < 0)
+    return GG_ERR_INVALID_ARG;
+  if (E > kMaxExperts || K % 128 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
+  if (offsets == nullptr || tiles_before == nullptr) return GG_ERR_INVALID_ARG;
+  if (R_cap > 0 && (slot_of_row == nullptr || Q == nullptr || S == nullptr ||
+                    (T > 0 && src == nullptr)))
+    return GG_ERR_INVALID_ARG;
+  if (n_tiles < (R_cap + 127) / 128 + E) return GG_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(src) || !aligned16(Q)) return GG_ERR_MISALIGNED;
+  gg_status s = check_ws(ws, ws_bytes, kWsHeader);
+  if (s != GG_OK) return s;
+  DeviceInfo dev;
+  if ((s = device_ok(&dev)) != GG_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_mx_tile_prefix(offsets, E, tiles_before, st);
+  if (e != cudaSuccess || R_cap == 0) return from_cuda(e);
+  return from_cuda(launch_mx_quantize_rows(src, T, K, k, slot_of_row, offsets, tiles_before, E,
+                                           R_cap, n_tiles, prob_of_row, Q, S, status_ptr(ws),
+                                           dev.sm_count, st));
+}
+
+gg_status gg_mx_grouped_gemm(int which, int activation, const uint8_t* Aq, const uint8_t* As,
+                             const void* mxw, const int32_t* offsets, int E, int R_cap, int H,
+                             int F, int n_tiles, gg_bf16* C, uint8_t* Cq, uint8_t* Cs,
+                             gg_bf16* H1, const float* row_scale, float* rowdot, void* ws,
+                             size_t ws_bytes, gg_stream_t stream) {
+  if (R_cap < 0 || n_tiles < 0) return GG_ERR_INVALID_ARG;
+  if (activation != GG_ACT_SWIGLU && activation != GG_ACT_QGEGLU) return GG_ERR_INVALID_ARG;
+  gg_mx_weights_layout L;
+  gg_status s = gg_mx_weights_layout_of(E, H, F, &L);
+  if (s != GG_OK) return s;
+  if (n_tiles < (R_cap + 127) / 128 + E) return GG_ERR_WORKSPACE_TOO_SMALL;
+  if (Aq == nullptr || As == nullptr || mxw == nullptr || offsets == nullptr)
+    return GG_ERR_INVALID_ARG;
+  const bool qg = activation == GG_ACT_QGEGLU;
+  const uint8_t* w = static_cast<const uint8_t*>(mxw);
+  MxGemmArgs a{};
+  a.A = Aq;
+  a.As = As;
+  a.sf_tiles = n_tiles;
+  a.offsets = offsets;
+  a.E = E;
+  a.R_cap = R_cap;
+  a.C = C;
+  a.Cq = Cq;
+  a.Cs = Cs;
+  a.row_scale = row_scale;
+  switch (which) {
+    case GG_MX_FC1:
+      if (Cq == nullptr || Cs == nullptr || rowdot != nullptr) return GG_ERR_INVALID_ARG;
+      a.mode = qg ? kFwdQgeglu : kFwdSwiglu;
+      a.K = H, a.Nout = 2 * F, a.Nw = 2 * F, a.Kq = F;
+      a.B = w + L.w1, a.Bs = w + L.w1_scales;
+      a.H1_save = H1;
+      break;
+    case GG_MX_FC2:
+      if (C == nullptr || row_scale != nullptr || rowdot != nullptr) return GG_ERR_INVALID_ARG;
+      a.mode = kFwdPlain;
+      a.K = F, a.Nout = H, a.Nw = H;
+      a.B = w + L.w2, a.Bs = w + L.w2_scales;
+      break;
+    case GG_MX_DGRAD_FC2:
+      if (Cq == nullptr || Cs == nullptr || H1 == nullptr) return GG_ERR_INVALID_ARG;
+      a.mode = qg ? kDgradQgegluBwd : kDgradSwigluBwd;
+      a.K = H, a.Nout = F, a.Nw = F, a.Kq = 2 * F;
+      a.B = w + L.w2t, a.Bs = w + L.w2t_scales;
+      a.H1 = H1;
+      a.rowdot = rowdot;
+      break;
+    case GG_MX_DGRAD_FC1:
+      if (C == nullptr || rowdot != nullptr) return GG_ERR_INVALID_ARG;
+      a.mode = kDgradPlain;
+      a.K = 2 * F, a.Nout = H, a.Nw = H;
+      a.B = w + L.w1t, a.Bs = w + L.w1t_scales;
+      break;
+    default:
+      return GG_ERR_INVALID_ARG;
+  }
+  if (!aligned16(Aq) || !aligned16(As) || !aligned16(C) || !aligned16(Cq) || !aligned16(H1) ||
+      (reinterpret_cast<uintptr_t>(mxw) & 255u) != 0)
+    return GG_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(rowdot) & 31u) != 0) return GG_ERR_MISALIGNED;
+  if ((s = check_ws(ws, ws_bytes, kWsHeader)) != GG_OK) return s;
+  if (R_cap == 0) return GG_OK;
+  DeviceInfo dev;
+  if ((s = device_ok(&dev)) != GG_OK) return s;
+  a.status = status_ptr(ws);
+  gg_status he = GG_OK;
+  const cudaError_t e =
+      launch_grouped_gemm_mx(a, dev, reinterpret_cast<cudaStream_t>(stream), &he);
+  if (he != GG_OK) return he;
+  return from_cuda(e);
+}
+
+size_t gg_mx_buffers_size(int T, int H, int F, int k, int E, int pad_multiple) {
+  if (T < 0 || k <= 0 || pad_multiple <= 0 || !mx_shape_ok(E, H, F)) return 0;
+  const size_t R_cap = static_cast<size_t>(r_cap_of(T, k, E, pad_multiple));
+  const size_t nt = static_cast<size_t>(gg_mx_row_tiles(T, k, E, pad_multiple));
+  const size_t h = static_cast<size_t>(H), f = static_cast<size_t>(F);
+  size_t n = 0;
+  n += align256(R_cap * h) * 2 + align256(nt * (h / 128) * 512) * 2;   // Xq, dYq + scales
+  n += align256(R_cap * f) + align256(nt * (f / 128) * 512);            // Aq + scales
+  n += align256(R_cap * 2 * f) + align256(nt * (2 * f / 128) * 512);    // dHq + scales
+  n += align256(R_cap * 2 * f * 2);                                     // H1
+  n += align256(R_cap * h * 2) * 2;                                     // Yp, dXp
+  n += align256(sizeof(int32_t) * (E + 1)) * 2;                         // offsets, tiles_before
+  n += align256(sizeof(int32_t) * static_cast<size_t>(T) * k);          // row_of_slot
+  n += align256(sizeof(int32_t) * R_cap) + align256(sizeof(float) * R_cap);
+  n += align256(sizeof(float) * R_cap * gg_mx_rowdot_stride(F));        // rowdot
+  n += align256(gg_workspace_size(T, k, E));
+  return n;
+}
+
+gg_status gg_mx_buffers_bind(void* base, size_t bytes, int T, int H, int F, int k, int E,
+                             int pad_multiple, gg_mx_buffers* out) {
+  if (base == nullptr || out == nullptr) return GG_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(base) & 255u) return GG_ERR_MISALIGNED;
+  const size_t need = gg_mx_buffers_size(T, H, F, k, E, pad_multiple);
+  if (need == 0) return GG_ERR_INVALID_ARG;
+  if (bytes < need) return GG_ERR_WORKSPACE_TOO_SMALL;
+  const size_t R_cap = static_cast<size_t>(r_cap_of(T, k, E, pad_multiple));
+  const size_t nt = static_cast<size_t>(gg_mx_row_tiles(T, k, E, pad_multiple));
+  const size_t h = static_cast<size_t>(H), f = static_cast<size_t>(F);
+  uint8_t* p = static_cast<uint8_t*>(base);
+  auto take = [&p](size_t n) {
+    uint8_t* q = p;
+    p += align256(n);
+    return q;
+  };
+  std::memset(out, 0, sizeof(*out));
+  out->Xq = take(R_cap * h);
+  out->Xs = take(nt * (h / 128) * 512);
+  out->dYq = take(R_cap * h);
+  out->dYs = take(nt * (h / 128) * 512);
+  out->Aq = take(R_cap * f);
+  out->As = take(nt * (f / 128) * 512);
+  out->dHq = take(R_cap * 2 * f);
+  out->dHs = take(nt * (2 * f / 128) * 512);
+  out->H1 = reinterpret_cast<gg_bf16*>(take(R_cap * 2 * f * 2));
+  out->Yp = reinterpret_cast<gg_bf16*>(take(R_cap * h * 2));
+  out->dXp = reinterpret_cast<gg_bf16*>(take(R_cap * h * 2));
+  out->offsets = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (E + 1)));
+  out->tiles_before = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (E + 1)));
+  out->row_of_slot =
+      reinterpret_cast<int32_t*>(take(sizeof(int32_t) * static_cast<size_t>(T) * k));
+  out->slot_of_row = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * R_cap));
+  out->prob_of_row = reinterpret_cast<float*>(take(sizeof(float) * R_cap));
+  out->rowdot = reinterpret_cast<float*>(take(sizeof(float) * R_cap * gg_mx_rowdot_stride(F)));
+  out->n_tiles = static_cast<int>(nt);
+  out->ws_bytes = align256(gg_workspace_size(T, k, E));
+  out->ws = take(out->ws_bytes);
+  return GG_OK;
+}
+
+static gg_status check_mx_buffers(const gg_mx_buffers* b, int T, int k, int E, int P) {
+  if (b == nullptr) return GG_ERR_INVALID_ARG;
+  if (b->Xq == nullptr || b->Xs == nullptr || b->H1 == nullptr || b->Aq == nullptr ||
+      b->As == nullptr || b->Yp == nullptr || b->dYq == nullptr || b->dYs == nullptr ||
+      b->dHq == nullptr || b->dHs == nullptr || b->dXp == nullptr || b->offsets == nullptr ||
+      b->row_of_slot == nullptr || b->slot_of_row == nullptr || b->prob_of_row == nullptr ||
+      b->tiles_before == nullptr || b->rowdot == nullptr)
+    return GG_ERR_INVALID_ARG;
+  if (b->n_tiles < gg_mx_row_tiles(T, k, E, P)) return GG_ERR_WORKSPACE_TOO_SMALL;
+  return check_ws(b->ws, b->ws_bytes, gg_workspace_size(T, k, E));
+}
+
+static gg_status mx_layer_checks(int T, int H, int F, int k, int E, int P,
+                                 const gg_moe_options* opt, const void* mxw,
+                                 const gg_mx_buffers* buf, int* act, int* mode, int* R_cap) {
+  if (T < 0 || k <= 0 || E <= 0 || P <= 0 || H <= 0 || F <= 0) return GG_ERR_INVALID_ARG;
+  gg_epilogue fepi, bepi;
+  bool recompute;
+  gg_status s = read_options(opt, &fepi, &bepi, mode, &recompute);
+  if (s != GG_OK) return s;
+  if (recompute) return GG_ERR_INVALID_ARG;
+  if (!mx_shape_ok(E, H, F)) return GG_ERR_UNSUPPORTED_SHAPE;
+  if ((s = check_mx_buffers(buf, T, k, E, P)) != GG_OK) return s;
+  if (mxw == nullptr) return GG_ERR_INVALID_ARG;
+  const long long rc = r_cap_of(T, k, E, P);
+  if (rc > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
+  *R_cap = static_cast<int>(rc);
+  *act = fepi == GG_EPI_QGEGLU ? GG_ACT_QGEGLU : GG_ACT_SWIGLU;
+  return GG_OK;
+}
+
+gg_status gg_moe_mlp_fwd_mx(const gg_bf16* x, const int32_t* idx, const float* prob,
+                            const void* mxw, int T, int H, int F, int k, int E,
+                            int pad_multiple, const gg_moe_options* opt, gg_bf16* out,
+                            const gg_mx_buffers* buf, gg_stream_t stream) {
+  int act, mode, R_cap;
+  gg_status s = mx_layer_checks(T, H, F, k, E, pad_multiple, opt, mxw, buf, &act, &mode, &R_cap);
+  if (s != GG_OK) return s;
+  if (T > 0 && (x == nullptr || out == nullptr)) return GG_ERR_INVALID_ARG;
+  // row maps only: the permuted copy is the quantised one below
+  s = gg_permute(x, idx, prob, T, H, k, E, pad_multiple, nullptr, buf->offsets, buf->row_of_slot,
+                 buf->slot_of_row, buf->prob_of_row, buf->ws, buf->ws_bytes, stream);
+  if (s != GG_OK || T == 0) return s;
+  const bool pre = mode == GG_PROB_PRE_FC1;
+  s = gg_mx_quantize_rows(x, T, H, k, buf->slot_of_row, buf->offsets,
+                          pre ? buf->prob_of_row : nullptr, E, R_cap, buf->n_tiles,
+                          buf->tiles_before, buf->Xq, buf->Xs, buf->ws, buf->ws_bytes, stream);
+  if (s != GG_OK) return s;
+  s = gg_mx_grouped_gemm(GG_MX_FC1, act, buf->Xq, buf->Xs, mxw, buf->offsets, E, R_cap, H, F,
+                         buf->n_tiles, nullptr, buf->Aq, buf->As, buf->H1,
+                         mode == GG_PROB_ACTIVATION ? buf->prob_of_row : nullptr, nullptr,
+                         buf->ws, buf->ws_bytes, stream);
+  if (s != GG_OK) return s;
+  s = gg_mx_grouped_gemm(GG_MX_FC2, act, buf->Aq, buf->As, mxw, buf->offsets, E, R_cap, H, F,
+                         buf->n_tiles, buf->Yp, nullptr, nullptr, nullptr, nullptr, nullptr,
+                         buf->ws, buf->ws_bytes, stream);
+  if (s != GG_OK) return s;
+  return gg_unpermute_combine(buf->Yp, buf->row_of_slot, mode == GG_PROB_COMBINE ? prob : nullptr,
+                              T, k, H, R_cap, out, nullptr, 0, nullptr, nullptr, buf->ws,
+                              buf->ws_bytes, stream);
+}
+
+gg_status gg_moe_mlp_bwd_mx(const gg_bf16* dOut, const gg_bf16* x, const float* prob,
+                            const void* mxw, int T, int H, int F, int k, int E,
+                            int pad_multiple, const gg_moe_options* opt, gg_bf16* dX,
+                            float* dprob, const gg_mx_buffers* buf, gg_stream_t stream) {
+  int act, mode, R_cap;
+  gg_status s = mx_layer_checks(T, H, F, k, E, pad_multiple, opt, mxw, buf, &act, &mode, &R_cap);
+  if (s != GG_OK) return s;
+  if (T == 0) return GG_OK;
+  if (dOut == nullptr || dX == nullptr) return GG_ERR_INVALID_ARG;
+  const bool pre = mode == GG_PROB_PRE_FC1;
+  if (pre && (prob == nullptr || (dprob != nullptr && x == nullptr))) return GG_ERR_INVALID_ARG;
+  float* rowdot = dprob != nullptr && !pre ? buf->rowdot : nullptr;
+  s = gg_mx_quantize_rows(dOut, T, H, k, buf->slot_of_row, buf->offsets, nullptr, E, R_cap,
+                          buf->n_tiles, buf->tiles_before, buf->dYq, buf->dYs, buf->ws,
+                          buf->ws_bytes, stream);
+  if (s != GG_OK) return s;
+  s = gg_mx_grouped_gemm(GG_MX_DGRAD_FC2, act, buf->dYq, buf->dYs, mxw, buf->offsets, E, R_cap,
+                         H, F, buf->n_tiles, nullptr, buf->dHq, buf->dHs, buf->H1,
+                         pre ? nullptr : buf->prob_of_row, rowdot, buf->ws, buf->ws_bytes,
+                         stream);
+  if (s != GG_OK) return s;
+  s = gg_mx_grouped_gemm(GG_MX_DGRAD_FC1, act, buf->dHq, buf->dHs, mxw, buf->offsets, E, R_cap,
+                         H, F, buf->n_tiles, buf->dXp, nullptr, nullptr, nullptr, nullptr,
+                         nullptr, buf->ws, buf->ws_bytes, stream);
+  if (s != GG_OK) return s;
+  if (pre)
+    return gg_unpermute_combine(buf->dXp, buf->row_of_slot, prob, T, k, H, R_cap, dX, nullptr, 0,
+                                dprob != nullptr ? x : nullptr, dprob, buf->ws, buf->ws_bytes,
+                                stream);
+  return gg_unpermute_combine(buf->dXp, buf->row_of_slot, nullptr, T, k, H, R_cap, dX, rowdot,
+                              gg_mx_rowdot_blocks(F), nullptr, dprob, buf->ws, buf->ws_bytes,
+                              stream);
+}
+
 gg_status gg_selftest_bounded_wait(void* ws, size_t ws_bytes, uint64_t limit_ns,
                                    gg_stream_t stream) {
   gg_status s = check_ws(ws, ws_bytes, kWsHeader);

@@ -46,6 +46,7 @@
 
 #include <mutex>
 
+#include "gg_epilogue.cuh"
 #include "gg_internal.h"
 #include "gg_ptx.cuh"
 
@@ -106,83 +107,6 @@ struct KParams {
   int gather_k;
   int gather_rows;             // rows of the gather source; this index reads zeros
 };
-
-__device__ __forceinline__ void decode_tile(int tile, const int* tb, int E, int NT, int& e,
-                                            int& mt, int& nt) {
-  int lo = 0, hi = E;  // tb[lo] <= tile < tb[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (tb[mid] <= tile)
-      lo = mid;
-    else
-      hi = mid;
-  }
-  e = lo;
-  const int local = tile - tb[lo];
-  mt = local / NT;
-  nt = local - mt * NT;
-}
-
-__device__ __forceinline__ void pack_bf16x32(const float (&v)[32], float scale, uint4 (&w)[4]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    w[i].x = pack_bf16x2(v[8 * i + 0] * scale, v[8 * i + 1] * scale);
-    w[i].y = pack_bf16x2(v[8 * i + 2] * scale, v[8 * i + 3] * scale);
-    w[i].z = pack_bf16x2(v[8 * i + 4] * scale, v[8 * i + 5] * scale);
-    w[i].w = pack_bf16x2(v[8 * i + 6] * scale, v[8 * i + 7] * scale);
-  }
-}
-
-// 16-byte slot of column group c (0..3) of row r (0..31) in a warp's staging
-// buffer; the XOR spreads every 8-lane shared-memory phase over all banks.
-__device__ __forceinline__ int stage_slot(int r, int c) { return r * 4 + (c ^ ((r >> 1) & 3)); }
-
-// Warp-collective store of a 32-row x 32-column BF16 chunk. Lane i holds row
-// i in w[]; row r of the chunk starts at row0 + r * ld (the warp's 32 rows
-// are consecutive) and only rows r < nvalid are written. Through the staging
-// buffer four lanes write each 64-byte row segment, so every store
-// instruction writes 8 whole row segments instead of 32 scattered 16-byte
-// pieces.
-__device__ __forceinline__ void store_chunk(uint4* stg, const uint4 (&w)[4], gg_bf16* row0,
-                                            long long ld, int nvalid) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) stg[stage_slot(lane, c)] = w[c];
-  __syncwarp();
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int r = 8 * j + (lane >> 2);
-    const int c = lane & 3;
-    const uint4 v = stg[stage_slot(r, c)];
-    if (r < nvalid) reinterpret_cast<uint4*>(row0 + r * ld)[c] = v;
-  }
-  __syncwarp();
-}
-
-// Warp-collective coalesced fetch of a 32-row x 32-column BF16 chunk (rows
-// row0 + r * ld): lane L loads column group L%4 of rows 8j + L/4 (raw
-// layout); rows r >= nvalid read as zero. transpose_chunk() then hands each
-// lane its own row.
-__device__ __forceinline__ void load_chunk_raw(uint4 (&raw)[4], const gg_bf16* row0, long long ld,
-                                               int nvalid) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int r = 8 * j + (lane >> 2);
-    raw[j] = r < nvalid ? __ldg(reinterpret_cast<const uint4*>(row0 + r * ld) + (lane & 3))
-                        : make_uint4(0u, 0u, 0u, 0u);
-  }
-}
-
-__device__ __forceinline__ void transpose_chunk(uint4* stg, const uint4 (&raw)[4], uint4 (&w)[4]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) stg[stage_slot(8 * j + (lane >> 2), lane & 3)] = raw[j];
-  __syncwarp();
-#pragma unroll
-  for (int c = 0; c < 4; ++c) w[c] = stg[stage_slot(lane, c)];
-  __syncwarp();
-}
 
 template <int MODE, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -595,28 +519,9 @@ swiglu_kernel(const uint4* __restrict__ H1, const int32_t* __restrict__ offsets,
 
 // ------------------------------------------------------------------ host side
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
 bool encode_bf16_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
                      const cuuint64_t* strides_bytes, const cuuint32_t* box) {
-  EncodeTiledFn fn = encode_fn();
+  EncodeTiledFn fn = encode_tiled_fn();
   if (fn == nullptr) return false;
   cuuint32_t elem_strides[3] = {1, 1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
@@ -664,6 +569,20 @@ cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const KPar
 }
 
 }  // namespace
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t stream,
                                 gg_status* host_err) {

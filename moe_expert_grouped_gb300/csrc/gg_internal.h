@@ -97,9 +97,72 @@ struct GemmArgs {
 cudaError_t launch_grouped_gemm(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t stream,
                                 gg_status* host_err);
 
+// cuTensorMapEncodeTiled, fetched once through the runtime's driver entry point.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
 cudaError_t launch_swiglu(const gg_bf16* H1, const int32_t* offsets, int E, int R_cap, int F,
                           float alpha, const float* row_scale, gg_bf16* A, int sm_count,
                           cudaStream_t stream);
+
+// ------------------------------------------------------------------ gg_gemm_mx.cu
+// MXFP8 grouped GEMM (layouts in gg_mx.cuh). C[r][n] = sum_k A[r][k] B[e][n][k]
+// with both operands E4M3 + E8M0 scales; modes as GemmMode, the dgrad modes
+// reading pre-transposed weights (B is always [E][Nw][K], K-major).
+struct MxGemmArgs {
+  GemmMode mode;
+  const uint8_t* A;        // [R_cap][K] E4M3
+  const uint8_t* As;       // A scale tiles: sf_tiles x (K/128) x 512 B
+  int sf_tiles;            // scale tiles the A-scale buffer holds
+  const uint8_t* B;        // [E][Nw][K] E4M3
+  const uint8_t* Bs;       // weight scale tiles [E][NT][K/128][1024 B]
+  const int32_t* offsets;  // [E+1]
+  int E, R_cap, K, Nout, Nw;
+  gg_bf16* C;              // plain modes: BF16 [R_cap][Nout]
+  uint8_t* Cq;             // gated modes: E4M3 [R_cap][Kq] (fwd: A, Kq = F; bwd: dH1, Kq = 2F)
+  uint8_t* Cs;             // and its scale tiles
+  int Kq;
+  gg_bf16* H1_save;        // gated fwd: [R_cap][2F] or null
+  const gg_bf16* H1;       // gated bwd: [R_cap][2F]
+  const float* row_scale;  // as GemmArgs
+  float* rowdot;           // gated bwd: [R_cap][roundup8(2 NT)] partials, or null
+  int32_t* status;
+};
+
+// Column tiles per row-tile pair of a mode (gated fwd: 96 gate + 96 up
+// columns; otherwise 192 columns).
+int mx_column_tiles(GemmMode mode, int Nout);
+
+cudaError_t launch_grouped_gemm_mx(const MxGemmArgs& a, const DeviceInfo& dev, cudaStream_t stream,
+                                   gg_status* host_err);
+
+// ------------------------------------------------------------------ gg_mx_quant.cu
+// tiles_before[e] = sum over e' < e of ceil(rows of e' / 128), e in [0, E].
+cudaError_t launch_mx_tile_prefix(const int32_t* offsets, int E, int32_t* tiles_before,
+                                  cudaStream_t stream);
+
+// Permuted MXFP8 A operand: row r < offsets[E] of Q is the quantised
+// src[slot_of_row[r] / k] (times prob_of_row[r], rounded to BF16, when
+// prob_of_row is not null); padding rows are zeros. Scales go to the 128-row
+// tiles of each expert (tile tiles_before[e] + t); rows of a tile past the
+// expert's end get code 0. S holds sf_tiles_cap tiles of K/128 x 512 bytes.
+cudaError_t launch_mx_quantize_rows(const gg_bf16* src, int T, int K, int k,
+                                    const int32_t* slot_of_row, const int32_t* offsets,
+                                    const int32_t* tiles_before, int E, int R_cap,
+                                    int sf_tiles_cap, const float* prob_of_row, uint8_t* Q,
+                                    uint8_t* S, int32_t* status, int sm_count,
+                                    cudaStream_t stream);
+
+// One weight operand: Wq[e][n][k] = E4M3 of W[e][n][k] (transpose = false,
+// W [E][N][K]) or of W[e][k][n] (transpose = true, W [E][K][N]), quantised
+// along k; scales into the weight scale tiles of the GEMM that reads it
+// (gated_F > 0: FC1's gate/up column tiles).
+cudaError_t launch_mx_prepare_weight(const gg_bf16* W, int E, int N, int K, bool transpose,
+                                     int gated_F, int NT, uint8_t* Wq, uint8_t* S,
+                                     cudaStream_t stream);
 
 // alpha of the gated activation of a gg_epilogue (1 for SwiGLU, 1.702 for
 // QuickGeGLU), 0 for epilogues without one.

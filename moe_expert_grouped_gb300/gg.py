@@ -61,7 +61,22 @@ SIGNATURES = [
      [_P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     ("gg_grouped_dgrad_gather", _I,
      [_P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
+    ("gg_mx_row_tiles", _I, [_I, _I, _I, _I]),
+    ("gg_mx_weights_layout_of", _I, [_I, _I, _I, _P]),
+    ("gg_mx_prepare_weights", _I, [_P, _P, _I, _I, _I, _P, _Z, _P]),
+    ("gg_mx_quantize_rows", _I,
+     [_P, _I, _I, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
+    ("gg_mx_rowdot_blocks", _I, [_I]),
+    ("gg_mx_rowdot_stride", _I, [_I]),
+    ("gg_mx_grouped_gemm", _I,
+     [_I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    ("gg_mx_buffers_size", _Z, [_I, _I, _I, _I, _I, _I]),
+    ("gg_mx_buffers_bind", _I, [_P, _Z, _I, _I, _I, _I, _I, _I, _P]),
+    ("gg_moe_mlp_fwd_mx", _I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    ("gg_moe_mlp_bwd_mx", _I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
 ]
+
+GG_MX_FC1, GG_MX_FC2, GG_MX_DGRAD_FC2, GG_MX_DGRAD_FC1 = 0, 1, 2, 3
 
 
 class GGBuffers(ctypes.Structure):
@@ -77,6 +92,22 @@ class GGOptions(ctypes.Structure):
 
     _fields_ = [("activation", ctypes.c_int), ("prob_mode", ctypes.c_int),
                 ("recompute_h1", ctypes.c_int)]
+
+
+class GGMxWeightsLayout(ctypes.Structure):
+    """Mirror of struct gg_mx_weights_layout (byte offsets)."""
+
+    _fields_ = [(n, ctypes.c_size_t) for n in (
+        "w1", "w1_scales", "w2", "w2_scales", "w2t", "w2t_scales", "w1t", "w1t_scales", "bytes")]
+
+
+class GGMxBuffers(ctypes.Structure):
+    """Mirror of struct gg_mx_buffers."""
+
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "Xq", "Xs", "H1", "Aq", "As", "Yp", "dYq", "dYs", "dHq", "dHs", "dXp", "offsets",
+        "row_of_slot", "slot_of_row", "prob_of_row", "tiles_before", "rowdot")] + [
+        ("n_tiles", ctypes.c_int), ("ws", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t)]
 
 
 class GGError(RuntimeError):
@@ -447,3 +478,173 @@ def permute_noalloc(x, idx, prob, E: int, P: int = 1, out=None):
                                   _ptr(offsets), _ptr(ros), _ptr(sor), _ptr(por), _stream(dev)),
            "gg_permute_noalloc")
     return dict(Xp=Xp, offsets=offsets, row_of_slot=ros, slot_of_row=sor, prob_of_row=por)
+
+
+# ---------------------------------------------------------------- MXFP8 path
+
+def mx_row_tiles(T: int, k: int, E: int, P: int = 1) -> int:
+    return int(LIB.gg_mx_row_tiles(T, k, E, P))
+
+
+def mx_rowdot_blocks(F: int) -> int:
+    return int(LIB.gg_mx_rowdot_blocks(F))
+
+
+def mx_rowdot_stride(F: int) -> int:
+    return int(LIB.gg_mx_rowdot_stride(F))
+
+
+def mx_weights_layout(E: int, H: int, F: int) -> dict:
+    """gg_mx_weights_layout_of as a dict of byte offsets (and 'bytes')."""
+    L = GGMxWeightsLayout()
+    _check(LIB.gg_mx_weights_layout_of(E, H, F, ctypes.byref(L)), "gg_mx_weights_layout_of")
+    return {n: int(getattr(L, n)) for n, _ in GGMxWeightsLayout._fields_}
+
+
+def mx_prepare_weights(W1, W2):
+    """gg_mx_prepare_weights: the four MXFP8 weight operands in one uint8
+    device tensor (256-byte aligned start); returns (tensor, layout)."""
+    E, F2, H = W1.shape
+    F = F2 // 2
+    _need(W1, torch.bfloat16, (E, 2 * F, H), "W1")
+    _need(W2, torch.bfloat16, (E, H, F), "W2")
+    L = mx_weights_layout(E, H, F)
+    raw = torch.empty(L["bytes"] + 256, dtype=torch.uint8, device=W1.device)
+    off = (-raw.data_ptr()) % 256
+    mxw = raw[off:off + L["bytes"]]
+    _check(LIB.gg_mx_prepare_weights(_ptr(W1), _ptr(W2), E, H, F, _ptr(mxw), L["bytes"],
+                                     _stream(W1.device)), "gg_mx_prepare_weights")
+    return mxw, L
+
+
+def mx_quantize_rows(src, slot_of_row, offsets, k: int, E: int, R_cap: int, ws,
+                     prob_of_row=None, n_tiles=None, out=None):
+    """gg_mx_quantize_rows: returns dict(Q [R_cap, K] uint8, S scale tiles
+    [n_tiles, K/128, 512] uint8, tiles_before [E+1] int32)."""
+    T, K = src.shape
+    dev = src.device
+    if n_tiles is None:
+        n_tiles = (R_cap + 127) // 128 + E
+    o = out or {}
+    Q = o.get("Q")
+    Q = torch.empty((R_cap, K), dtype=torch.uint8, device=dev) if Q is None else Q
+    S = o.get("S")
+    S = torch.zeros((n_tiles, K // 128, 512), dtype=torch.uint8, device=dev) if S is None else S
+    tb = o.get("tiles_before")
+    tb = torch.empty((E + 1,), dtype=torch.int32, device=dev) if tb is None else tb
+    _check(LIB.gg_mx_quantize_rows(_ptr(src), T, K, k, _ptr(slot_of_row), _ptr(offsets),
+                                   _ptr(prob_of_row), E, R_cap, n_tiles, _ptr(tb), _ptr(Q),
+                                   _ptr(S), _ptr(ws), ws.numel(), _stream(dev)),
+           "gg_mx_quantize_rows")
+    return dict(Q=Q, S=S, tiles_before=tb)
+
+
+def mx_grouped_gemm(which: int, Aq, As, mxw, offsets, E: int, R_cap: int, H: int, F: int, ws,
+                    activation: int = GG_ACT_SWIGLU, C=None, Cq=None, Cs=None, H1=None,
+                    row_scale=None, rowdot=None):
+    """gg_mx_grouped_gemm. Outputs the caller does not pass are allocated:
+    FC1 -> (Cq [R_cap, F], Cs, H1 [R_cap, 2F]); FC2 / DGRAD_FC1 -> C [R_cap, H];
+    DGRAD_FC2 -> (Cq [R_cap, 2F], Cs) (H1 is an input there)."""
+    dev = Aq.device
+    n_tiles = As.shape[0]
+    if which == GG_MX_FC1:
+        Cq = torch.empty((R_cap, F), dtype=torch.uint8, device=dev) if Cq is None else Cq
+        Cs = torch.zeros((n_tiles, F // 128, 512), dtype=torch.uint8, device=dev) \
+            if Cs is None else Cs
+        H1 = torch.empty((R_cap, 2 * F), dtype=torch.bfloat16, device=dev) if H1 is None else H1
+    elif which == GG_MX_DGRAD_FC2:
+        Cq = torch.empty((R_cap, 2 * F), dtype=torch.uint8, device=dev) if Cq is None else Cq
+        Cs = torch.zeros((n_tiles, 2 * F // 128, 512), dtype=torch.uint8, device=dev) \
+            if Cs is None else Cs
+    else:
+        C = torch.empty((R_cap, H), dtype=torch.bfloat16, device=dev) if C is None else C
+    _check(LIB.gg_mx_grouped_gemm(which, activation, _ptr(Aq), _ptr(As), _ptr(mxw),
+                                  _ptr(offsets), E, R_cap, H, F, n_tiles, _ptr(C), _ptr(Cq),
+                                  _ptr(Cs), _ptr(H1), _ptr(row_scale), _ptr(rowdot), _ptr(ws),
+                                  ws.numel(), _stream(dev)), "gg_mx_grouped_gemm")
+    if which == GG_MX_FC1:
+        return Cq, Cs, H1
+    if which == GG_MX_DGRAD_FC2:
+        return Cq, Cs
+    return C
+
+
+class MxMoeLayer:
+    """The MXFP8 expert layer (gg_moe_mlp_fwd_mx / gg_moe_mlp_bwd_mx) over one
+    owned buffer, with weights prepared once by gg_mx_prepare_weights."""
+
+    _SHAPES = {
+        "Xq": ("rc", "H"), "dYq": ("rc", "H"), "Aq": ("rc", "F"), "dHq": ("rc", "2F"),
+        "Xs": ("nt", "Hb", "512"), "dYs": ("nt", "Hb", "512"), "As": ("nt", "Fb", "512"),
+        "dHs": ("nt", "F2b", "512"), "H1": ("rc", "2F"), "Yp": ("rc", "H"), "dXp": ("rc", "H"),
+        "offsets": ("E1",), "tiles_before": ("E1",), "row_of_slot": ("Tk",),
+        "slot_of_row": ("rc",), "prob_of_row": ("rc",), "rowdot": ("rc", "nbs"), "ws": ("ws",),
+    }
+    _DTYPES = {"H1": torch.bfloat16, "Yp": torch.bfloat16, "dXp": torch.bfloat16,
+               "offsets": torch.int32, "tiles_before": torch.int32, "row_of_slot": torch.int32,
+               "slot_of_row": torch.int32, "prob_of_row": torch.float32,
+               "rowdot": torch.float32}
+
+    def __init__(self, T: int, H: int, F: int, k: int, E: int, P: int = 1, device="cuda",
+                 activation: int = GG_ACT_SWIGLU, prob_mode: int = GG_PROB_COMBINE):
+        self.T, self.H, self.F, self.k, self.E, self.P = T, H, F, k, E, P
+        self.opt = GGOptions(activation, prob_mode, 0)
+        self._saved = None
+        self.R_cap = r_cap(T, k, E, P)
+        self.device = torch.device(device)
+        n = int(LIB.gg_mx_buffers_size(T, H, F, k, E, P))
+        if n == 0:
+            raise GGError(2, "gg_mx_buffers_size")
+        self.storage = torch.zeros(n + 256, dtype=torch.uint8, device=self.device)
+        base = self.storage.data_ptr()
+        self._base = base + ((-base) % 256)
+        self.buf = GGMxBuffers()
+        _check(LIB.gg_mx_buffers_bind(ctypes.c_void_p(self._base), n, T, H, F, k, E, P,
+                                      ctypes.byref(self.buf)), "gg_mx_buffers_bind")
+
+    def view(self, name: str) -> torch.Tensor:
+        dims = {"rc": self.R_cap, "H": self.H, "F": self.F, "2F": 2 * self.F,
+                "E1": self.E + 1, "Tk": self.T * self.k, "ws": int(self.buf.ws_bytes),
+                "nbs": mx_rowdot_stride(self.F), "nt": int(self.buf.n_tiles),
+                "Hb": self.H // 128, "Fb": self.F // 128, "F2b": 2 * self.F // 128, "512": 512}
+        dtype = self._DTYPES.get(name, torch.uint8)
+        shape = tuple(dims[d] for d in self._SHAPES[name])
+        count = 1
+        for s in shape:
+            count *= s
+        esize = torch.empty((), dtype=dtype).element_size()
+        off = getattr(self.buf, name) - self.storage.data_ptr()
+        return self.storage[off:off + count * esize].view(dtype).view(shape)
+
+    def forward(self, x, idx, prob, mxw, out=None):
+        T, H, F, k, E = self.T, self.H, self.F, self.k, self.E
+        _need(x, torch.bfloat16, (T, H), "x")
+        _need(idx, torch.int32, (T, k), "idx")
+        _need(prob, torch.float32, (T, k), "prob")
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=self.device) if out is None else out
+        _check(LIB.gg_moe_mlp_fwd_mx(_ptr(x), _ptr(idx), _ptr(prob), _ptr(mxw), T, H, F, k, E,
+                                     self.P, ctypes.byref(self.opt), _ptr(out),
+                                     ctypes.byref(self.buf), _stream(self.device)),
+               "gg_moe_mlp_fwd_mx")
+        self._saved = (x, prob)
+        return out
+
+    def backward(self, dOut, mxw, dX=None, dprob=None):
+        T, H, F, k, E = self.T, self.H, self.F, self.k, self.E
+        _need(dOut, torch.bfloat16, (T, H), "dOut")
+        dX = torch.empty((T, H), dtype=torch.bfloat16, device=self.device) if dX is None else dX
+        want = dprob is not None and dprob is not False
+        if dprob is True:
+            dprob = torch.empty((T, k), dtype=torch.float32, device=self.device)
+        if want:
+            _need(dprob, torch.float32, (T, k), "dprob")
+        x, prob = self._saved if self._saved is not None else (None, None)
+        _check(LIB.gg_moe_mlp_bwd_mx(_ptr(dOut), _ptr(x), _ptr(prob), _ptr(mxw), T, H, F, k, E,
+                                     self.P, ctypes.byref(self.opt), _ptr(dX),
+                                     _ptr(dprob) if want else None, ctypes.byref(self.buf),
+                                     _stream(self.device)),
+               "gg_moe_mlp_bwd_mx")
+        return (dX, dprob) if want else dX
+
+    def status(self) -> int:
+        return read_status(self.view("ws"))

@@ -155,13 +155,15 @@ def mx_weights(W1, W2):
 # ---------------------------------------------------------------- the layer
 
 def mx_forward(x, idx, prob, W1, W2, E: int, P: int = 1, activation: str = "swiglu",
-               prob_mode: str = "combine") -> dict:
+               prob_mode: str = "combine", faithful: bool = False) -> dict:
     """MXFP8 expert layer, forward (readings in the module docstring).
 
     Xq = mx(x rows), H1 = bf16(Xq W1f^T), A = bf16(act(H1)) (times the
     probability in ``activation`` mode), Yp = mx(A) W2f^T exactly, out =
     the probability-weighted (``combine``) or plain sum of the k rows. The
-    pre-FC1 probability mode scales x before its quantisation."""
+    pre-FC1 probability mode scales x before its quantisation. With
+    ``faithful``, Yp and out are also rounded to BF16 (where the GPU path
+    stores them); that only sizes the error budget of a parity test."""
     if prob_mode not in ("combine", "activation", "pre_fc1"):
         raise ValueError(prob_mode)
     x = _mo._as_f64(x)
@@ -185,27 +187,33 @@ def mx_forward(x, idx, prob, W1, W2, E: int, P: int = 1, activation: str = "swig
         A = A * pr[:, None]
     A = _mo.round_to_bf16(A)
     Aq = mx(A)
-    Yp = _mo.grouped_linear(Aq, W["W2f"], offsets)
+    rnd = _mo.round_to_bf16 if faithful else (lambda v: v)
+    Yp = rnd(_mo.grouped_linear(Aq, W["W2f"], offsets))
     if prob_mode == "combine":
-        out = _mo.combine(Yp, row_of_slot, prob, T, k)
+        out = rnd(_mo.combine(Yp, row_of_slot, prob, T, k))
     else:
-        out = _mo.combine(Yp, row_of_slot, None, T, k)
+        out = rnd(_mo.combine(Yp, row_of_slot, None, T, k))
     return dict(out=out, offsets=offsets, row_of_slot=row_of_slot, slot_of_row=slot_of_row,
                 Xq=Xq, H1=H1, A=A, Aq=Aq, Yp=Yp, W=W, x=x, prob=prob, pr=pr,
-                activation=activation, prob_mode=prob_mode, k=k)
+                activation=activation, prob_mode=prob_mode, k=k, faithful=faithful)
 
 
 def mx_backward(dOut, fwd: dict) -> dict:
     """MXFP8 expert layer, input gradient and probability gradient.
 
     dYq = mx(dOut rows) (each row of the permuted gradient is its token's
-    dOut), dA = (dYq W2d) times the probability in ``combine`` mode,
-    dH1 = bf16(act'(H1) applied to dA) (times the probability in
-    ``activation`` mode, applied to dA before the activation's backward),
-    dXp = mx(dH1) W1d, dX = the plain sum of the k rows (times the probability
-    in ``pre_fc1`` mode). dprob follows the BF16 layer's definition with this
-    layer's saved tensors: <dOut_t, Yp> (combine), <dA_unscaled, act(H1)>
-    (activation), <x_t, dXp_unscaled> (pre_fc1)."""
+    dOut), dA0 = dYq W2d, dA = dA0 times the probability (``combine`` and
+    ``activation`` modes: the probability scales the activation's output, or
+    equivalently FC2's), dH1 = bf16(act'(H1) applied to dA), dXp = mx(dH1)
+    W1d, dX = the plain sum of the k rows (probability-weighted in
+    ``pre_fc1`` mode). The quantisers pass gradients straight through.
+
+    dprob is the gradient where the probability meets the activation: the row
+    sum of dA0 * act(H1) (``combine`` and ``activation``; in exact arithmetic
+    it equals <dOut_t, Yp>, but here FC2's forward and backward see
+    differently quantised operands), <x_t, dXp> in ``pre_fc1`` mode. With a
+    ``faithful`` forward, dXp, dX and the activation in the dprob sum are
+    rounded to BF16 as well."""
     dOut = _mo._as_f64(dOut)
     k = fwd["k"]
     T = dOut.shape[0]
@@ -219,23 +227,21 @@ def mx_backward(dOut, fwd: dict) -> dict:
     dYp[valid] = dOut[sor[valid] // k]
     dA0 = _mo.grouped_linear_t(mx(dYp), W["W2d"], offsets)
     dprob_rows = np.zeros(R_cap)
-    if mode == "combine":
+    rnd = _mo.round_to_bf16 if fwd.get("faithful") else (lambda v: v)
+    if mode in ("combine", "activation"):
         dA = dA0 * pr[:, None]
-        dprob_rows[valid] = np.sum(dYp[valid] * fwd["Yp"][valid], axis=1)
-    elif mode == "activation":
-        dA = dA0 * pr[:, None]
-        act = _mo.glu(fwd["H1"], fwd["activation"])
+        act = rnd(_mo.glu(fwd["H1"], fwd["activation"]))
         dprob_rows[valid] = np.sum(dA0[valid] * act[valid], axis=1)
     else:
         dA = dA0
     dH1 = _mo.round_to_bf16(_mo.glu_backward(dA, fwd["H1"], fwd["activation"]))
-    dXp = _mo.grouped_linear_t(mx(dH1), W["W1d"], offsets)
+    dXp = rnd(_mo.grouped_linear_t(mx(dH1), W["W1d"], offsets))
     if mode == "pre_fc1":
         x = fwd["x"]
         dprob_rows[valid] = np.sum(x[sor[valid] // k] * dXp[valid], axis=1)
-        dX = _mo.combine(dXp, ros, fwd["prob"], T, k)
+        dX = rnd(_mo.combine(dXp, ros, fwd["prob"], T, k))
     else:
-        dX = _mo.combine(dXp, ros, None, T, k)
+        dX = rnd(_mo.combine(dXp, ros, None, T, k))
     dprob = np.zeros(T * k)
     dprob[sor[valid]] = dprob_rows[valid]
     return dict(dX=dX, dprob=dprob.reshape(T, k), dYp=dYp, dA=dA, dH1=dH1, dXp=dXp)

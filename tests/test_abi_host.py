@@ -172,3 +172,87 @@ def test_validation_rejects_before_launch(gg):
     assert L.gg_moe_mlp_fwd(p, p, p, p, p, 4, 64, 128, 2, 4, 1, p, None, None) == 1
     assert L.gg_read_status(None, None, None) == 1
     assert L.gg_clear_status(None, None) == 1
+
+
+def test_mx_layout_and_validation(gg):
+    L = gg.LIB
+    p = ctypes.c_void_p(1 << 40)
+    mis = ctypes.c_void_p((1 << 40) + 8)
+    ws = ctypes.c_void_p(1 << 41)
+    E, H, F = 4, 256, 384
+    lay = gg.mx_weights_layout(E, H, F)
+    # four E4M3 operands and their scale tiles, in order, 256-byte aligned, disjoint
+    sizes = {"w1": E * 2 * F * H, "w1_scales": E * (F // 96) * (H // 128) * 1024,
+             "w2": E * H * F, "w2_scales": E * 2 * (F // 128) * 1024,
+             "w2t": E * F * H, "w2t_scales": E * 2 * (H // 128) * 1024,
+             "w1t": E * H * 2 * F, "w1t_scales": E * 2 * (2 * F // 128) * 1024}
+    spans = sorted((lay[n], lay[n] + sz) for n, sz in sizes.items())
+    for (a0, a1), (b0, _) in zip(spans, spans[1:]):
+        assert a1 <= b0
+    assert all(s % 256 == 0 for s, _ in spans) and spans[-1][1] <= lay["bytes"]
+    # shapes: H, F multiples of 128, 0 < E <= 1024
+    for bad in ((E, 192, F), (E, H, 320), (0, H, F), (1025, H, F)):
+        with pytest.raises(gg.GGError):
+            gg.mx_weights_layout(*bad)
+    assert L.gg_mx_row_tiles(300, 3, 6, 16) == (300 * 3 + 6 * 15 + 127) // 128 + 6
+    assert L.gg_mx_row_tiles(-1, 3, 6, 1) == 0
+    assert L.gg_mx_rowdot_blocks(768) == 8 and L.gg_mx_rowdot_blocks(384) == 4
+    assert L.gg_mx_rowdot_blocks(640) == 8 and L.gg_mx_rowdot_stride(640) == 8
+    assert L.gg_mx_rowdot_stride(1536) == 16 and L.gg_mx_rowdot_blocks(0) == 0
+    # prepare: misaligned buffer, too small
+    assert L.gg_mx_prepare_weights(p, p, E, H, F, mis, lay["bytes"], None) == 3
+    assert L.gg_mx_prepare_weights(p, p, E, H, F, p, lay["bytes"] - 1, None) == 4
+    assert L.gg_mx_prepare_weights(None, p, E, H, F, p, lay["bytes"], None) == 1
+    # quantize rows: K % 128, scale capacity, alignment
+    R_cap, nt = 900, (900 + 127) // 128 + E
+    Q = L.gg_mx_quantize_rows
+    assert Q(p, 300, 192, 3, p, p, None, E, R_cap, nt, p, p, p, ws, 1024, None) == 2
+    assert Q(p, 300, 256, 3, p, p, None, E, R_cap, nt - 1, p, p, p, ws, 1024, None) == 4
+    assert Q(mis, 300, 256, 3, p, p, None, E, R_cap, nt, p, p, p, ws, 1024, None) == 3
+    assert Q(p, 300, 256, 33, p, p, None, E, R_cap, nt, p, p, p, ws, 1024, None) == 1
+    # grouped gemm: outputs each kind needs, activation, capacity, alignment
+    G = L.gg_mx_grouped_gemm
+    args = (p, p, p, p, E, R_cap, H, F, nt)
+    assert G(0, 0, *args, None, None, p, p, None, None, ws, 1024, None) == 1      # FC1 w/o Cq
+    assert G(0, 2, *args, None, p, p, p, None, None, ws, 1024, None) == 1         # activation
+    assert G(1, 0, *args, None, None, None, None, None, None, ws, 1024, None) == 1  # FC2 w/o C
+    assert G(1, 0, *args, p, None, None, None, p, None, ws, 1024, None) == 1      # FC2 + scale
+    assert G(2, 0, *args, None, p, p, None, p, None, ws, 1024, None) == 1         # no H1
+    assert G(3, 0, *args, p, None, None, None, None, p, ws, 1024, None) == 1      # rowdot
+    assert G(4, 0, *args, p, None, None, None, None, None, ws, 1024, None) == 1   # kind
+    assert G(1, 0, p, p, p, p, E, R_cap, H, F, nt - 1, p, None, None, None, None, None, ws,
+             1024, None) == 4
+    assert G(1, 0, mis, p, p, p, E, R_cap, H, F, nt, p, None, None, None, None, None, ws,
+             1024, None) == 3
+    assert G(2, 0, *args, None, p, p, p, p, ctypes.c_void_p((1 << 40) + 16), ws, 1024,
+             None) == 3
+    # buffers: disjoint aligned pieces; the layer rejects recompute_h1 and bad shapes
+    T, k, P = 300, 3, 16
+    n = L.gg_mx_buffers_size(T, H, F, k, E, P)
+    buf = gg.GGMxBuffers()
+    assert L.gg_mx_buffers_bind(p, n, T, H, F, k, E, P, ctypes.byref(buf)) == 0
+    rc = T * k + E * (P - 1)
+    ntl = L.gg_mx_row_tiles(T, k, E, P)
+    assert buf.n_tiles == ntl
+    sizes = {"Xq": rc * H, "Xs": ntl * (H // 128) * 512, "dYq": rc * H,
+             "dYs": ntl * (H // 128) * 512, "Aq": rc * F, "As": ntl * (F // 128) * 512,
+             "dHq": rc * 2 * F, "dHs": ntl * (2 * F // 128) * 512, "H1": rc * 4 * F,
+             "Yp": rc * H * 2, "dXp": rc * H * 2, "offsets": 4 * (E + 1),
+             "tiles_before": 4 * (E + 1), "row_of_slot": 4 * T * k, "slot_of_row": 4 * rc,
+             "prob_of_row": 4 * rc, "rowdot": 4 * rc * L.gg_mx_rowdot_stride(F),
+             "ws": buf.ws_bytes}
+    spans = sorted((getattr(buf, name), getattr(buf, name) + sz) for name, sz in sizes.items())
+    for (a0, a1), (b0, _) in zip(spans, spans[1:]):
+        assert a1 <= b0
+    assert all(s % 256 == 0 for s, _ in spans) and spans[-1][1] <= (1 << 40) + n
+    assert L.gg_mx_buffers_size(T, 192, F, k, E, P) == 0
+    for act, mode, rec in ((0, 0, 1), (2, 0, 0), (0, 3, 0)):
+        opt = gg.GGOptions(act, mode, rec)
+        assert L.gg_moe_mlp_fwd_mx(p, p, p, p, T, H, F, k, E, P, ctypes.byref(opt), p,
+                                   ctypes.byref(buf), None) == 1
+        assert L.gg_moe_mlp_bwd_mx(p, p, p, p, T, H, F, k, E, P, ctypes.byref(opt), p, p,
+                                   ctypes.byref(buf), None) == 1
+    assert L.gg_moe_mlp_fwd_mx(p, p, p, p, T, H, 320, k, E, P, None, p, ctypes.byref(buf),
+                               None) == 2
+    assert L.gg_moe_mlp_fwd_mx(p, p, p, None, T, H, F, k, E, P, None, p, ctypes.byref(buf),
+                               None) == 1
