@@ -289,8 +289,7 @@ def run_gg(args, shape, peaks):
         mark(0)
         gg.permute(x, idx, prob, E, P, ws=ws, out=dict(b, Xp=None))
         mark(1)
-        gg.mx_quantize_rows(x, b["slot_of_row"], b["offsets"], k, E, rc, ws,
-                            prob_of_row=por if pre else None, n_tiles=nt,
+        gg.mx_quantize_rows(x, b, k, E, P, ws, prob=prob if pre else None, n_tiles=nt,
                             out=dict(Q=b["Xq"], S=b["Xs"], tiles_before=b["tiles_before"]))
         mark(2)
         gg.mx_grouped_gemm(gg.GG_MX_FC1, b["Xq"], b["Xs"], mxw, b["offsets"], E, rc, H, F, ws,
@@ -303,7 +302,7 @@ def run_gg(args, shape, peaks):
         gg.unpermute_combine(b["Yp"], b["row_of_slot"], prob if mode == gg.GG_PROB_COMBINE else None,
                              T, k, ws, out=out)
         mark(5)
-        gg.mx_quantize_rows(dOut, b["slot_of_row"], b["offsets"], k, E, rc, ws, n_tiles=nt,
+        gg.mx_quantize_rows(dOut, b, k, E, P, ws, n_tiles=nt,
                             out=dict(Q=b["dYq"], S=b["dYs"], tiles_before=b["tiles_before"]))
         mark(6)
         gg.mx_grouped_gemm(gg.GG_MX_DGRAD_FC2, b["dYq"], b["dYs"], mxw, b["offsets"], E, rc, H, F,
@@ -488,7 +487,7 @@ def run_gg(args, shape, peaks):
         # the combines read k rows per token (+ row map, prob) and write one
         # (MXFP8: the permute writes the row maps only, the row quantisers
         # read each token row once and write one E4M3 row + scales per pair)
-        quant = T * H * 2 + R * H + R * H // 32 + 4 * rc
+        quant = T * H * 2 + R * H + R * H // 32 + 4 * R
         return {"permute": (8 * R + 4 * R + 8 * rc) + (0 if mx else (T + R) * H * 2),
                 "permute_dout": (T + R) * H * 2 + 4 * rc,
                 "quant_x": quant, "quant_dout": quant,

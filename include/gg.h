@@ -502,17 +502,20 @@ gg_status gg_mx_weights_layout_of(int E, int H, int F, gg_mx_weights_layout* out
 gg_status gg_mx_prepare_weights(const gg_bf16* W1, const gg_bf16* W2, int E, int H, int F,
                                 void* mxw, size_t bytes, gg_stream_t stream);
 
-/* Permuted MXFP8 activation operand. Writes tiles_before[E+1] from offsets,
- * then for every row r < offsets[E]: Q[r] = the E4M3 codes of
- * src[slot_of_row[r] / k] (times prob_of_row[r], rounded to BF16, when
- * prob_of_row is not NULL), zeros where slot_of_row[r] is -1; scales into S
- * (n_tiles tiles of K/128 blocks). src [T][K] BF16, Q [R_cap][K], K a
- * multiple of 128. */
+/* Permuted MXFP8 activation operand, from the permute's maps. Writes
+ * tiles_before[E+1] from offsets, clears S (n_tiles tiles of K/128 blocks),
+ * then for every (token t, slot j) with a row r = row_of_slot[t*k+j]:
+ * Q[r] = the E4M3 codes of src[t] (times prob[t*k+j], rounded to BF16, when
+ * prob is not NULL) and its scales into the tiles of the expert whose rows
+ * contain r. Rows that no pair reaches keep code 0; padding rows
+ * (pad_multiple > 1, slot -1) of Q are zeroed. src [T][K] BF16,
+ * Q [R_cap][K], K a multiple of 128. A row outside [0, R_cap) is skipped
+ * and reported as GG_ERR_DEVICE_BAD_ROW. */
 gg_status gg_mx_quantize_rows(const gg_bf16* src, int T, int K, int k,
-                              const int32_t* slot_of_row, const int32_t* offsets,
-                              const float* prob_of_row, int E, int R_cap, int n_tiles,
-                              int32_t* tiles_before, uint8_t* Q, uint8_t* S, void* ws,
-                              size_t ws_bytes, gg_stream_t stream);
+                              const int32_t* row_of_slot, const int32_t* slot_of_row,
+                              const int32_t* offsets, const float* prob, int E,
+                              int pad_multiple, int n_tiles, int32_t* tiles_before, uint8_t* Q,
+                              uint8_t* S, void* ws, size_t ws_bytes, gg_stream_t stream);
 
 /* The four MXFP8 grouped GEMMs of the layer, with the weights of `mxw`:
  *  GG_MX_FC1        A = Xq [R_cap][H]: H1 = bf16(A W1^T) stored to H1 (may

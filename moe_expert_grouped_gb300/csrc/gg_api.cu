@@ -676,29 +676,32 @@ gg_status gg_mx_prepare_weights(const gg_bf16* W1, const gg_bf16* W2, int E, int
 }
 
 gg_status gg_mx_quantize_rows(const gg_bf16* src, int T, int K, int k,
-                              const int32_t* slot_of_row, const int32_t* offsets,
-                              const float* prob_of_row, int E, int R_cap, int n_tiles,
-                              int32_t* tiles_before, uint8_t* Q, uint8_t* S, void* ws,
-                              size_t ws_bytes, gg_stream_t stream) {
-  if (T < 0 || K <= 0 || k <= 0 || k > 32 || E <= 0 || R_cap < 0 || n_tiles < 0)
+                              const int32_t* row_of_slot, const int32_t* slot_of_row,
+                              const int32_t* offsets, const float* prob, int E,
+                              int pad_multiple, int n_tiles, int32_t* tiles_before, uint8_t* Q,
+                              uint8_t* S, void* ws, size_t ws_bytes, gg_stream_t stream) {
+  if (T < 0 || K <= 0 || k <= 0 || k > 32 || E <= 0 || pad_multiple <= 0 || n_tiles < 0)
     return GG_ERR_INVALID_ARG;
   if (E > kMaxExperts || K % 128 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
-  if (offsets == nullptr || tiles_before == nullptr) return GG_ERR_INVALID_ARG;
-  if (R_cap > 0 && (slot_of_row == nullptr || Q == nullptr || S == nullptr ||
-                    (T > 0 && src == nullptr)))
+  const long long rc = r_cap_of(T, k, E, pad_multiple);
+  if (rc > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
+  const int R_cap = static_cast<int>(rc);
+  if (offsets == nullptr || tiles_before == nullptr || S == nullptr) return GG_ERR_INVALID_ARG;
+  if (T > 0 && (src == nullptr || row_of_slot == nullptr || slot_of_row == nullptr ||
+                Q == nullptr))
     return GG_ERR_INVALID_ARG;
   if (n_tiles < (R_cap + 127) / 128 + E) return GG_ERR_WORKSPACE_TOO_SMALL;
-  if (!aligned16(src) || !aligned16(Q)) return GG_ERR_MISALIGNED;
+  if (!aligned16(src) || !aligned16(Q) || !aligned16(S)) return GG_ERR_MISALIGNED;
   gg_status s = check_ws(ws, ws_bytes, kWsHeader);
   if (s != GG_OK) return s;
   DeviceInfo dev;
   if ((s = device_ok(&dev)) != GG_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = launch_mx_tile_prefix(offsets, E, tiles_before, st);
-  if (e != cudaSuccess || R_cap == 0) return from_cuda(e);
-  return from_cuda(launch_mx_quantize_rows(src, T, K, k, slot_of_row, offsets, tiles_before, E,
-                                           R_cap, n_tiles, prob_of_row, Q, S, status_ptr(ws),
-                                           dev.sm_count, st));
+  if (e != cudaSuccess) return GG_ERR_CUDA;
+  return from_cuda(launch_mx_quantize_rows(src, T, K, k, row_of_slot, slot_of_row, offsets,
+                                           tiles_before, E, R_cap, pad_multiple > 1, n_tiles,
+                                           prob, Q, S, status_ptr(ws), dev.sm_count, st));
 }
 
 gg_status gg_mx_grouped_gemm(int which, int activation, const uint8_t* Aq, const uint8_t* As,
@@ -878,9 +881,9 @@ gg_status gg_moe_mlp_fwd_mx(const gg_bf16* x, const int32_t* idx, const float* p
                  buf->slot_of_row, buf->prob_of_row, buf->ws, buf->ws_bytes, stream);
   if (s != GG_OK || T == 0) return s;
   const bool pre = mode == GG_PROB_PRE_FC1;
-  s = gg_mx_quantize_rows(x, T, H, k, buf->slot_of_row, buf->offsets,
-                          pre ? buf->prob_of_row : nullptr, E, R_cap, buf->n_tiles,
-                          buf->tiles_before, buf->Xq, buf->Xs, buf->ws, buf->ws_bytes, stream);
+  s = gg_mx_quantize_rows(x, T, H, k, buf->row_of_slot, buf->slot_of_row, buf->offsets,
+                          pre ? prob : nullptr, E, pad_multiple, buf->n_tiles, buf->tiles_before,
+                          buf->Xq, buf->Xs, buf->ws, buf->ws_bytes, stream);
   if (s != GG_OK) return s;
   s = gg_mx_grouped_gemm(GG_MX_FC1, act, buf->Xq, buf->Xs, mxw, buf->offsets, E, R_cap, H, F,
                          buf->n_tiles, nullptr, buf->Aq, buf->As, buf->H1,
@@ -908,9 +911,9 @@ gg_status gg_moe_mlp_bwd_mx(const gg_bf16* dOut, const gg_bf16* x, const float* 
   const bool pre = mode == GG_PROB_PRE_FC1;
   if (pre && (prob == nullptr || (dprob != nullptr && x == nullptr))) return GG_ERR_INVALID_ARG;
   float* rowdot = dprob != nullptr && !pre ? buf->rowdot : nullptr;
-  s = gg_mx_quantize_rows(dOut, T, H, k, buf->slot_of_row, buf->offsets, nullptr, E, R_cap,
-                          buf->n_tiles, buf->tiles_before, buf->dYq, buf->dYs, buf->ws,
-                          buf->ws_bytes, stream);
+  s = gg_mx_quantize_rows(dOut, T, H, k, buf->row_of_slot, buf->slot_of_row, buf->offsets,
+                          nullptr, E, pad_multiple, buf->n_tiles, buf->tiles_before, buf->dYq,
+                          buf->dYs, buf->ws, buf->ws_bytes, stream);
   if (s != GG_OK) return s;
   s = gg_mx_grouped_gemm(GG_MX_DGRAD_FC2, act, buf->dYq, buf->dYs, mxw, buf->offsets, E, R_cap,
                          H, F, buf->n_tiles, nullptr, buf->dHq, buf->dHs, buf->H1,

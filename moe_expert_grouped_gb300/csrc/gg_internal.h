@@ -58,6 +58,12 @@ cudaError_t launch_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const 
                            int n_rowdot, const gg_bf16* dot_src, float* dprob, int32_t* status,
                            int sm_count, cudaStream_t stream);
 
+// Zeroes row r (vec_per_row 16-byte vectors of dst) for every r < offsets[E]
+// whose slot_of_row is -1 (the padding rows).
+cudaError_t launch_zero_pad_rows(const int32_t* slot_of_row, const int32_t* offsets, int E,
+                                 int R_cap, int vec_per_row, void* dst, int sm_count,
+                                 cudaStream_t stream);
+
 cudaError_t launch_bounded_wait_selftest(int32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
 // ------------------------------------------------------------------ gg_gemm.cu
@@ -144,17 +150,19 @@ cudaError_t launch_grouped_gemm_mx(const MxGemmArgs& a, const DeviceInfo& dev, c
 cudaError_t launch_mx_tile_prefix(const int32_t* offsets, int E, int32_t* tiles_before,
                                   cudaStream_t stream);
 
-// Permuted MXFP8 A operand: row r < offsets[E] of Q is the quantised
-// src[slot_of_row[r] / k] (times prob_of_row[r], rounded to BF16, when
-// prob_of_row is not null); padding rows are zeros. Scales go to the 128-row
-// tiles of each expert (tile tiles_before[e] + t); rows of a tile past the
-// expert's end get code 0. S holds sf_tiles_cap tiles of K/128 x 512 bytes.
+// Permuted MXFP8 A operand, token-ordered: every pair (t, j) with a row
+// gets Q[row_of_slot[t*k+j]] = the E4M3 codes of src[t] (times prob[t*k+j],
+// rounded to BF16, when prob is not null) and its scales in the 128-row tile
+// of the expert e whose rows contain it (tile tiles_before[e] + local row /
+// 128). S (sf_tiles_cap tiles of K/128 x 512 bytes) is cleared first, so rows
+// no pair reaches hold code 0; with has_padding the padding rows of Q are
+// zeroed.
 cudaError_t launch_mx_quantize_rows(const gg_bf16* src, int T, int K, int k,
-                                    const int32_t* slot_of_row, const int32_t* offsets,
-                                    const int32_t* tiles_before, int E, int R_cap,
-                                    int sf_tiles_cap, const float* prob_of_row, uint8_t* Q,
-                                    uint8_t* S, int32_t* status, int sm_count,
-                                    cudaStream_t stream);
+                                    const int32_t* row_of_slot, const int32_t* slot_of_row,
+                                    const int32_t* offsets, const int32_t* tiles_before, int E,
+                                    int R_cap, bool has_padding, int sf_tiles_cap,
+                                    const float* prob, uint8_t* Q, uint8_t* S, int32_t* status,
+                                    int sm_count, cudaStream_t stream);
 
 // One weight operand: Wq[e][n][k] = E4M3 of W[e][n][k] (transpose = false,
 // W [E][N][K]) or of W[e][k][n] (transpose = true, W [E][K][N]), quantised

@@ -52,76 +52,88 @@ __device__ __forceinline__ void unpack_bf16x8(uint4 w, float* v) {
   v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
 }
 
-// One warp per row of every expert's 128-row tiles; lane b handles the
-// 32-element blocks b, b + 32, ... of the row (64 contiguous source bytes in,
-// 32 bytes out per block).
+// One warp per token: the token's row is read once and each 32-element
+// block is quantised once (once per pair when the pairs scale it by their
+// probability) and written to the permuted row of every pair of the token,
+// its scale byte into the 128-row tile of the expert whose rows contain it.
+// Lane b0 + l owns block b0 + l; lane j < k first resolves pair j's row, its
+// expert (binary search of the offsets) and its scale position.
 __global__ void __launch_bounds__(256)
-quantize_rows_kernel(const gg_bf16* __restrict__ src, int T, int K, int k,
-                     const int32_t* __restrict__ slot_of_row, const int32_t* __restrict__ offsets,
-                     const int32_t* __restrict__ tb, int E, int R_cap, int sf_tiles_cap,
-                     const float* __restrict__ prob_of_row, uint8_t* __restrict__ Q,
-                     uint8_t* __restrict__ S, int32_t* status) {
+quantize_scatter_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ row_of_slot,
+                        const float* __restrict__ prob,
+                        const int32_t* __restrict__ offsets, const int32_t* __restrict__ tb,
+                        int T, int k, int K, int E, int R_cap, int sf_tiles_cap,
+                        uint8_t* __restrict__ Q, uint8_t* __restrict__ S, int32_t* status) {
   const int lane = threadIdx.x & 31;
-  const long long warp_id = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const long long n_warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-  int total_tiles = tb[E];
-  if (total_tiles > sf_tiles_cap) {
-    if (warp_id == 0 && lane == 0) set_status(status, GG_ERR_DEVICE_BAD_OFFSETS);
-    total_tiles = sf_tiles_cap;
-  }
-  const int KG = K / mx::kKStep;
+  const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   const int nblk = K / mx::kBlock;
-  const long long pairs = static_cast<long long>(T) * k;
-  for (long long w = warp_id; w < static_cast<long long>(total_tiles) * mx::kRowTile;
-       w += n_warps) {
-    const int tile = static_cast<int>(w / mx::kRowTile);
-    const int r = static_cast<int>(w % mx::kRowTile);
-    int lo = 0, hi = E;  // tb[lo] <= tile < tb[lo + 1]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (tb[mid] <= tile)
-        lo = mid;
-      else
-        hi = mid;
-    }
-    const int e = lo;
-    const long long grow =
-        static_cast<long long>(offsets[e]) + static_cast<long long>(tile - tb[e]) * mx::kRowTile + r;
-    const bool in_expert = grow < offsets[e + 1] && grow < R_cap;
-    long long src_row = -1;
-    float p = 1.0f;
-    if (in_expert) {
-      const int slot = slot_of_row[grow];
-      if (slot >= pairs) {
-        if (lane == 0) set_status(status, GG_ERR_DEVICE_BAD_ROW);
-      } else if (slot >= 0) {
-        src_row = slot / k;
+  const long long tile_bytes = static_cast<long long>(K / mx::kKStep) * mx::kSfaBytes;
+  for (long long t = warp0; t < T; t += nwarps) {
+    int my_row = -1;
+    long long my_sf = 0;  // byte of block 0 of this pair's row in S
+    float my_p = 1.0f;
+    if (lane < k) {
+      const int row = row_of_slot[t * k + lane];
+      int e = 0, hi = E;  // the expert whose rows contain `row`: offsets[e] <= row
+      while (hi - e > 1) {
+        const int mid = (e + hi) >> 1;
+        if (offsets[mid] <= row)
+          e = mid;
+        else
+          hi = mid;
       }
-      if (prob_of_row != nullptr) p = prob_of_row[grow];
+      const int local = row - offsets[e];
+      const long long tile = static_cast<long long>(tb[e]) + (local >> 7);
+      if (row >= 0 && row < R_cap && local >= 0 && row < offsets[e + 1] && tile < sf_tiles_cap) {
+        my_row = row;
+        my_sf = tile * tile_bytes + mx::sf_byte(local & 127, 0);
+      } else if (row != -1) {
+        set_status(status, GG_ERR_DEVICE_BAD_ROW);
+      }
+      if (prob != nullptr) my_p = prob[t * k + lane];
     }
-    const uint4* srow = reinterpret_cast<const uint4*>(src + (src_row >= 0 ? src_row : 0) * K);
-    for (int b = lane; b < nblk; b += 32) {
-      float v[32];
-      if (src_row >= 0) {
+    const uint4* sp = src + t * (K / 8);
+    // two blocks per lane and pass: their eight 16-byte loads are in flight together
+    for (int b0 = 0; b0 < nblk; b0 += 64) {
+      uint4 raw[2][4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) unpack_bf16x8(__ldg(srow + 4 * b + j), v + 8 * j);
-        if (prob_of_row != nullptr) {
+      for (int h = 0; h < 2; ++h) {
+        const int b = b0 + 32 * h + lane;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = round_bf16(v[i] * p);
+        for (int j = 0; j < 4; ++j)
+          raw[h][j] = b < nblk ? __ldg(sp + 4 * b + j) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int b = b0 + 32 * h + lane;
+        const bool live = b < nblk;
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) unpack_bf16x8(raw[h][j], v + 8 * j);
+        const long long sf_b = (b >> 2) * static_cast<long long>(mx::kSfaBytes) + (b & 3);
+        uint32_t q[8];
+        uint32_t code = prob == nullptr ? mx::quantize32(v, q) : 0u;
+        for (int j = 0; j < k; ++j) {
+          const int row = __shfl_sync(0xFFFFFFFFu, my_row, j);
+          const long long sfo = __shfl_sync(0xFFFFFFFFu, my_sf, j);
+          const float pj = __shfl_sync(0xFFFFFFFFu, my_p, j);
+          if (row < 0) continue;
+          if (prob != nullptr) {
+            float w[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) w[i] = round_bf16(v[i] * pj);
+            code = mx::quantize32(w, q);
+          }
+          if (live) {
+            uint4* d =
+                reinterpret_cast<uint4*>(Q + static_cast<long long>(row) * K + b * mx::kBlock);
+            __stcs(d, make_uint4(q[0], q[1], q[2], q[3]));
+            __stcs(d + 1, make_uint4(q[4], q[5], q[6], q[7]));
+            S[sfo + sf_b] = static_cast<uint8_t>(code);
+          }
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
       }
-      uint32_t q[8];
-      const uint32_t code = mx::quantize32(v, q);
-      if (in_expert) {
-        uint4* d = reinterpret_cast<uint4*>(Q + grow * K + b * mx::kBlock);
-        d[0] = make_uint4(q[0], q[1], q[2], q[3]);
-        d[1] = make_uint4(q[4], q[5], q[6], q[7]);
-      }
-      S[(static_cast<long long>(tile) * KG + (b >> 2)) * mx::kSfaBytes + mx::sf_byte(r, b & 3)] =
-          static_cast<uint8_t>(in_expert ? code : 0u);
     }
   }
 }
@@ -191,21 +203,26 @@ cudaError_t launch_mx_tile_prefix(const int32_t* offsets, int E, int32_t* tiles_
 }
 
 cudaError_t launch_mx_quantize_rows(const gg_bf16* src, int T, int K, int k,
-                                    const int32_t* slot_of_row, const int32_t* offsets,
-                                    const int32_t* tiles_before, int E, int R_cap,
-                                    int sf_tiles_cap, const float* prob_of_row, uint8_t* Q,
-                                    uint8_t* S, int32_t* status, int sm_count,
-                                    cudaStream_t stream) {
-  if (sf_tiles_cap <= 0) return cudaSuccess;
-  const long long rows = static_cast<long long>(sf_tiles_cap) * mx::kRowTile;
-  long long blocks = (rows + 7) / 8;  // 8 warps per block
+                                    const int32_t* row_of_slot, const int32_t* slot_of_row,
+                                    const int32_t* offsets, const int32_t* tiles_before, int E,
+                                    int R_cap, bool has_padding, int sf_tiles_cap,
+                                    const float* prob, uint8_t* Q, uint8_t* S, int32_t* status,
+                                    int sm_count, cudaStream_t stream) {
+  // code 0 wherever no pair lands: rows past an expert's end, padding rows
+  cudaError_t e = cudaMemsetAsync(
+      S, 0, static_cast<size_t>(sf_tiles_cap) * (K / mx::kKStep) * mx::kSfaBytes, stream);
+  if (e != cudaSuccess || T <= 0) return e;
+  long long blocks = (static_cast<long long>(T) + 7) / 8;  // 8 warps per block
   const long long cap = static_cast<long long>(sm_count) * 8;
   if (blocks > cap) blocks = cap;
-  quantize_rows_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
-      src, T, K, k, slot_of_row, offsets, tiles_before, E, R_cap, sf_tiles_cap, prob_of_row, Q, S,
-      status);
+  quantize_scatter_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+      reinterpret_cast<const uint4*>(src), row_of_slot, prob, offsets, tiles_before, T, k, K, E,
+      R_cap, sf_tiles_cap, Q, S, status);
   count_launch();
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (has_padding)  // E4M3 zeros on the padding rows (K bytes = K/16 vectors)
+    return launch_zero_pad_rows(slot_of_row, offsets, E, R_cap, K / 16, Q, sm_count, stream);
+  return cudaSuccess;
 }
 
 cudaError_t launch_mx_prepare_weight(const gg_bf16* W, int E, int N, int K, bool transpose,

@@ -617,6 +617,20 @@ cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* row_of_slot,
   return cudaGetLastError();
 }
 
+cudaError_t launch_zero_pad_rows(const int32_t* slot_of_row, const int32_t* offsets, int E,
+                                 int R_cap, int vec_per_row, void* dst, int sm_count,
+                                 cudaStream_t stream) {
+  if (R_cap <= 0) return cudaSuccess;
+  long long pb = (static_cast<long long>(R_cap) + 255) / 256;
+  const long long cap = static_cast<long long>(sm_count) * 8;
+  if (pb > cap) pb = cap;
+  zero_pad_rows_kernel<<<static_cast<int>(pb), 256, 0, stream>>>(slot_of_row, offsets, E,
+                                                                  vec_per_row,
+                                                                  static_cast<uint4*>(dst));
+  count_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t launch_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const float* prob,
                            int T, int k, int H, int R_cap, gg_bf16* out, const float* rowdot,
                            int n_rowdot, const gg_bf16* dot_src, float* dprob, int32_t* status,

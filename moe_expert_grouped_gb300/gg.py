@@ -65,7 +65,7 @@ SIGNATURES = [
     ("gg_mx_weights_layout_of", _I, [_I, _I, _I, _P]),
     ("gg_mx_prepare_weights", _I, [_P, _P, _I, _I, _I, _P, _Z, _P]),
     ("gg_mx_quantize_rows", _I,
-     [_P, _I, _I, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
+     [_P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     ("gg_mx_rowdot_blocks", _I, [_I]),
     ("gg_mx_rowdot_stride", _I, [_I]),
     ("gg_mx_grouped_gemm", _I,
@@ -517,25 +517,26 @@ def mx_prepare_weights(W1, W2):
     return mxw, L
 
 
-def mx_quantize_rows(src, slot_of_row, offsets, k: int, E: int, R_cap: int, ws,
-                     prob_of_row=None, n_tiles=None, out=None):
-    """gg_mx_quantize_rows: returns dict(Q [R_cap, K] uint8, S scale tiles
-    [n_tiles, K/128, 512] uint8, tiles_before [E+1] int32)."""
+def mx_quantize_rows(src, maps, k: int, E: int, P: int, ws, prob=None, n_tiles=None, out=None):
+    """gg_mx_quantize_rows from the permute's maps (dict with row_of_slot,
+    slot_of_row, offsets); prob [T, k] scales each pair's copy. Returns
+    dict(Q [R_cap, K] uint8, S [n_tiles, K/128, 512] uint8, tiles_before [E+1])."""
     T, K = src.shape
     dev = src.device
+    rc = r_cap(T, k, E, P)
     if n_tiles is None:
-        n_tiles = (R_cap + 127) // 128 + E
+        n_tiles = (rc + 127) // 128 + E
     o = out or {}
     Q = o.get("Q")
-    Q = torch.empty((R_cap, K), dtype=torch.uint8, device=dev) if Q is None else Q
+    Q = torch.empty((rc, K), dtype=torch.uint8, device=dev) if Q is None else Q
     S = o.get("S")
-    S = torch.zeros((n_tiles, K // 128, 512), dtype=torch.uint8, device=dev) if S is None else S
+    S = torch.empty((n_tiles, K // 128, 512), dtype=torch.uint8, device=dev) if S is None else S
     tb = o.get("tiles_before")
     tb = torch.empty((E + 1,), dtype=torch.int32, device=dev) if tb is None else tb
-    _check(LIB.gg_mx_quantize_rows(_ptr(src), T, K, k, _ptr(slot_of_row), _ptr(offsets),
-                                   _ptr(prob_of_row), E, R_cap, n_tiles, _ptr(tb), _ptr(Q),
-                                   _ptr(S), _ptr(ws), ws.numel(), _stream(dev)),
-           "gg_mx_quantize_rows")
+    _check(LIB.gg_mx_quantize_rows(_ptr(src), T, K, k, _ptr(maps["row_of_slot"]),
+                                   _ptr(maps["slot_of_row"]), _ptr(maps["offsets"]), _ptr(prob),
+                                   E, P, n_tiles, _ptr(tb), _ptr(Q), _ptr(S), _ptr(ws),
+                                   ws.numel(), _stream(dev)), "gg_mx_quantize_rows")
     return dict(Q=Q, S=S, tiles_before=tb)
 
 

@@ -205,11 +205,13 @@ def test_mx_layout_and_validation(gg):
     assert L.gg_mx_prepare_weights(None, p, E, H, F, p, lay["bytes"], None) == 1
     # quantize rows: K % 128, scale capacity, alignment
     R_cap, nt = 900, (900 + 127) // 128 + E
-    Q = L.gg_mx_quantize_rows
-    assert Q(p, 300, 192, 3, p, p, None, E, R_cap, nt, p, p, p, ws, 1024, None) == 2
-    assert Q(p, 300, 256, 3, p, p, None, E, R_cap, nt - 1, p, p, p, ws, 1024, None) == 4
-    assert Q(mis, 300, 256, 3, p, p, None, E, R_cap, nt, p, p, p, ws, 1024, None) == 3
-    assert Q(p, 300, 256, 33, p, p, None, E, R_cap, nt, p, p, p, ws, 1024, None) == 1
+    Q = L.gg_mx_quantize_rows  # T = 300, k = 3, P = 1: R_cap = 900
+    assert Q(p, 300, 192, 3, p, p, p, None, E, 1, nt, p, p, p, ws, 1024, None) == 2
+    assert Q(p, 300, 256, 3, p, p, p, None, E, 1, nt - 1, p, p, p, ws, 1024, None) == 4
+    assert Q(mis, 300, 256, 3, p, p, p, None, E, 1, nt, p, p, p, ws, 1024, None) == 3
+    assert Q(p, 300, 256, 33, p, p, p, None, E, 1, nt, p, p, p, ws, 1024, None) == 1
+    assert Q(p, 300, 256, 3, None, p, p, None, E, 1, nt, p, p, p, ws, 1024, None) == 1
+    assert Q(p, 300, 256, 3, p, p, p, None, E, 0, nt, p, p, p, ws, 1024, None) == 1
     # grouped gemm: outputs each kind needs, activation, capacity, alignment
     G = L.gg_mx_grouped_gemm
     args = (p, p, p, p, E, R_cap, H, F, nt)

@@ -138,8 +138,7 @@ def test_quantize_rows_bit_exact(gg, shape, scaled):
     m, off, sor = _maps(gg, d, s)
     rc = gg.r_cap(s.T, s.k, s.E, s.P)
     ws = m["ws"]
-    res = gg.mx_quantize_rows(d["x"], m["slot_of_row"], m["offsets"], s.k, s.E, rc, ws,
-                              prob_of_row=m["prob_of_row"] if scaled else None)
+    res = gg.mx_quantize_rows(d["x"], m, s.k, s.E, s.P, ws, prob=d["prob"] if scaled else None)
     torch.cuda.synchronize()
     assert gg.read_status(ws) == 0
     n = int(off[-1])
@@ -212,7 +211,7 @@ def test_grouped_gemms_match_oracle(gg, shape, act):
     ws = m["ws"]
     mxw, _ = gg.mx_prepare_weights(d["W1"], d["W2"])
     W = mxo.mx_weights(inp.W1, inp.W2)
-    xq = gg.mx_quantize_rows(d["x"], m["slot_of_row"], m["offsets"], s.k, s.E, rc, ws)
+    xq = gg.mx_quantize_rows(d["x"], m, s.k, s.E, s.P, ws)
     por_t = m["prob_of_row"]
     # FC1 (+ the weighted activation)
     Aq, As, H1 = gg.mx_grouped_gemm(gg.GG_MX_FC1, xq["Q"], xq["S"], mxw, m["offsets"], s.E, rc,
@@ -221,7 +220,7 @@ def test_grouped_gemms_match_oracle(gg, shape, act):
     Yp = gg.mx_grouped_gemm(gg.GG_MX_FC2, Aq, As, mxw, m["offsets"], s.E, rc, s.H, s.F, ws,
                             activation=act)
     # input gradient: dOut rows quantised, FC2's input gradient + activation backward
-    dyq = gg.mx_quantize_rows(d["dOut"], m["slot_of_row"], m["offsets"], s.k, s.E, rc, ws)
+    dyq = gg.mx_quantize_rows(d["dOut"], m, s.k, s.E, s.P, ws)
     rowdot = torch.zeros((rc, gg.mx_rowdot_stride(s.F)), dtype=torch.float32, device="cuda")
     dHq, dHs = gg.mx_grouped_gemm(gg.GG_MX_DGRAD_FC2, dyq["Q"], dyq["S"], mxw, m["offsets"],
                                   s.E, rc, s.H, s.F, ws, activation=act, H1=H1,
