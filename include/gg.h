@@ -468,9 +468,9 @@ gg_status gg_moe_mlp_bwd_ex(const gg_bf16* dOut, const gg_bf16* x, const float* 
  *    scale of row r of the tile, 32-column block 4 * kg + b. Rows of a tile
  *    past the expert's end hold code 0. Every activation scale buffer holds
  *    gg_mx_row_tiles() tiles.
- *  - weight operands: per expert and 192-column tile of the GEMM that reads
- *    them (FC1: 96 gate rows followed by the 96 matching up rows, FC1 tile j
- *    covering gate rows 96j..), KG blocks of 1024 bytes, byte
+ *  - weight operands: per expert and 256-column tile of the GEMM that reads
+ *    them (FC1: 128 gate rows followed by the 128 matching up rows, FC1 tile
+ *    j covering gate rows 128j..), KG blocks of 1024 bytes, byte
  *    (n / 128) * 512 + ((n % 128) % 32) * 16 + ((n % 128) / 32) * 4 + b for
  *    column n of the tile; columns past the weight's rows hold code 0.
  * ------------------------------------------------------------------------- */
@@ -482,13 +482,13 @@ int gg_mx_row_tiles(int T, int k, int E, int pad_multiple);
  * gg_mx_prepare_weights (each piece 256-byte aligned). */
 typedef struct gg_mx_weights_layout {
   size_t w1, w1_scales;   /* FC1: E4M3 [E][2F][H], along H; scale tiles
-                             [E][ceil(F/96)][H/128]                        */
+                             [E][F/128][H/128]                             */
   size_t w2, w2_scales;   /* FC2: E4M3 [E][H][F], along F;
-                             [E][ceil(H/192)][F/128]                       */
+                             [E][ceil(H/256)][F/128]                       */
   size_t w2t, w2t_scales; /* input gradient of FC2: E4M3 [E][F][H] = W2
-                             transposed, along H; [E][ceil(F/192)][H/128]  */
+                             transposed, along H; [E][ceil(F/256)][H/128]  */
   size_t w1t, w1t_scales; /* input gradient of FC1: E4M3 [E][H][2F] = W1
-                             transposed, along 2F; [E][ceil(H/192)][2F/128] */
+                             transposed, along 2F; [E][ceil(H/256)][2F/128] */
   size_t bytes;           /* total                                         */
 } gg_mx_weights_layout;
 

@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "gg_internal.h"
+#include "gg_mx.cuh"
 
 namespace gg {
 
@@ -613,7 +614,7 @@ int gg_mx_row_tiles(int T, int k, int E, int pad_multiple) {
   return n > 0x7FFFFFFFLL ? 0 : static_cast<int>(n);
 }
 
-int gg_mx_rowdot_blocks(int F) { return F > 0 ? 2 * ((F + 191) / 192) : 0; }
+int gg_mx_rowdot_blocks(int F) { return F > 0 ? 2 * ((F + mx::kTileN - 1) / mx::kTileN) : 0; }
 
 int gg_mx_rowdot_stride(int F) { return (gg_mx_rowdot_blocks(F) + 7) / 8 * 8; }
 
@@ -621,7 +622,8 @@ gg_status gg_mx_weights_layout_of(int E, int H, int F, gg_mx_weights_layout* out
   if (out == nullptr) return GG_ERR_INVALID_ARG;
   if (!mx_shape_ok(E, H, F)) return GG_ERR_UNSUPPORTED_SHAPE;
   const size_t e = static_cast<size_t>(E), h = static_cast<size_t>(H), f = static_cast<size_t>(F);
-  const size_t sfb = 1024;
+  const size_t sfb = mx::kSfbBytes;
+  const size_t tn = mx::kTileN, th = mx::kTileNHalf;
   size_t at = 0;
   auto take = [&at](size_t n) {
     const size_t q = at;
@@ -629,13 +631,13 @@ gg_status gg_mx_weights_layout_of(int E, int H, int F, gg_mx_weights_layout* out
     return q;
   };
   out->w1 = take(e * 2 * f * h);
-  out->w1_scales = take(e * ((f + 95) / 96) * (h / 128) * sfb);
+  out->w1_scales = take(e * ((f + th - 1) / th) * (h / 128) * sfb);
   out->w2 = take(e * h * f);
-  out->w2_scales = take(e * ((h + 191) / 192) * (f / 128) * sfb);
+  out->w2_scales = take(e * ((h + tn - 1) / tn) * (f / 128) * sfb);
   out->w2t = take(e * f * h);
-  out->w2t_scales = take(e * ((f + 191) / 192) * (h / 128) * sfb);
+  out->w2t_scales = take(e * ((f + tn - 1) / tn) * (h / 128) * sfb);
   out->w1t = take(e * h * 2 * f);
-  out->w1t_scales = take(e * ((h + 191) / 192) * (2 * f / 128) * sfb);
+  out->w1t_scales = take(e * ((h + tn - 1) / tn) * (2 * f / 128) * sfb);
   out->bytes = at;
   return GG_OK;
 }
@@ -663,13 +665,14 @@ gg_status gg_mx_prepare_weights(const gg_bf16* W1, const gg_bf16* W2, int E, int
     if (e != cudaSuccess) return GG_ERR_CUDA;
   }
   cudaError_t e;
-  if ((e = launch_mx_prepare_weight(W1, E, 2 * F, H, false, F, (F + 95) / 96, base + L.w1,
+  const int tn = mx::kTileN, th = mx::kTileNHalf;
+  if ((e = launch_mx_prepare_weight(W1, E, 2 * F, H, false, F, (F + th - 1) / th, base + L.w1,
                                     base + L.w1_scales, st)) != cudaSuccess ||
-      (e = launch_mx_prepare_weight(W2, E, H, F, false, 0, (H + 191) / 192, base + L.w2,
+      (e = launch_mx_prepare_weight(W2, E, H, F, false, 0, (H + tn - 1) / tn, base + L.w2,
                                     base + L.w2_scales, st)) != cudaSuccess ||
-      (e = launch_mx_prepare_weight(W2, E, F, H, true, 0, (F + 191) / 192, base + L.w2t,
+      (e = launch_mx_prepare_weight(W2, E, F, H, true, 0, (F + tn - 1) / tn, base + L.w2t,
                                     base + L.w2t_scales, st)) != cudaSuccess ||
-      (e = launch_mx_prepare_weight(W1, E, H, 2 * F, true, 0, (H + 191) / 192, base + L.w1t,
+      (e = launch_mx_prepare_weight(W1, E, H, 2 * F, true, 0, (H + tn - 1) / tn, base + L.w1t,
                                     base + L.w1t_scales, st)) != cudaSuccess)
     return GG_ERR_CUDA;
   return GG_OK;

@@ -13,24 +13,27 @@
 // producer, one thread of the even CTA issues the MMAs, 8 epilogue warps per
 // CTA drain TMEM. Differences:
 //   * a k-step is 128 E4M3 elements (one 128-byte swizzle row): the pair's
-//     A tile (2 x 128 x 128 B) and B tile (2 x 96 x 128 B) plus their scale
+//     A tile (2 x 128 x 128 B) and B tile (2 x 128 x 128 B) plus their scale
 //     tiles (512 B of A scales per CTA, 1 KB of B scales) land on one
 //     barrier; 6 stages;
 //   * the scale tiles go from shared memory to TMEM with tcgen05.cp (ordered
 //     before the MMAs of the same thread), then four MMAs of K = 32 each
 //     pick their 32-element block with the instruction's scale ids;
-//   * the tile is 256 x 192 (two 192-column accumulators at TMEM columns 0
-//     and 256; the scale cells of the 6 stages use columns 192-255 and
-//     448-511), so the stage scales fit next to a double-buffered
-//     accumulator;
+//   * the MMA is 256 x 256 x 32 (a 192-column MMA costs 137 clocks against
+//     128 for 256 columns, measured): one 256-column accumulator at TMEM
+//     columns 0-255, the scale cells of the stages at 256 + 16 s. With a
+//     single accumulator the epilogue first moves its share of it into
+//     registers as BF16 (every GEMM result of the layer is BF16), releases it
+//     to the MMA issuer, and only then does the activation, quantisation and
+//     stores while the next tile's MMAs run;
 //   * the B operand is always K-major: the input-gradient GEMMs read weights
 //     that were transposed and quantised along their output dimension once
 //     (gg_mx_prepare_weights);
 //   * the gated epilogues quantise what they hand to the next GEMM: FC1
 //     writes H1 (BF16, for the backward) and the activation as E4M3 + scales;
 //     the SwiGLU-backward epilogue writes dH1 as E4M3 + scales. A thread owns
-//     one row and 32 consecutive columns per TMEM load, exactly one scale
-//     block, so the block maximum needs no exchange between threads.
+//     one row and 32 consecutive columns per chunk, exactly one scale block,
+//     so the block maximum needs no exchange between threads.
 // Every wait is bounded like the BF16 kernel's.
 
 #include <cuda_runtime.h>
@@ -54,29 +57,28 @@ constexpr uint16_t kClusterMask = 0x3;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t A_BYTES = BM * kKStep;               // 16 KB
-constexpr uint32_t B_BYTES = kTileNHalf * kKStep;       // 12 KB
-constexpr uint32_t AB_STAGE = A_BYTES + B_BYTES;        // 28 KB, 1024-aligned
+constexpr uint32_t B_BYTES = kTileNHalf * kKStep;       // 16 KB
+constexpr uint32_t AB_STAGE = A_BYTES + B_BYTES;        // 32 KB, 1024-aligned
 constexpr uint32_t SF_STAGE = mx::kSfaBytes + mx::kSfbBytes;
 constexpr uint32_t TX_BYTES = AB_STAGE + SF_STAGE;      // per CTA and stage
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t kAccStride = 256;                    // accumulator a at column a * 256
 
-__device__ __forceinline__ uint32_t sf_col(int stage) {
-  return stage < 4 ? 192u + 16u * stage : 448u + 16u * (stage - 4);
-}
+// TMEM columns of stage s's scale cells: A scales in 4, B scales in 8
+__device__ __forceinline__ uint32_t sf_col(int stage) { return 256u + 16u * stage; }
 
+// The expert row starts are read from the offsets in global memory (two
+// cached loads per tile), which leaves room for a sixth stage.
 struct SmemTail {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t tfull;
+  uint64_t tempty;
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
   int total_tiles;
   int pad_;
   int tiles_before[kMaxExperts + 1];
-  int row_start[kMaxExperts + 1];
   int sf_before[kMaxExperts + 1];  // first 128-row scale tile of each expert
 };
 
@@ -85,7 +87,7 @@ constexpr uint32_t kStagingBytes = kEpiWarps * kWarpStagingBytes;
 constexpr size_t kSmemBytes =
     1024 + STAGES * (AB_STAGE + SF_STAGE) + kStagingBytes + sizeof(SmemTail);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-static_assert(STAGES <= 8, "scale cells: four stages per TMEM column range");
+static_assert(256 + 16 * STAGES <= TMEM_COLS, "scale cells next to the accumulator");
 
 struct MxParams {
   const int32_t* offsets;
@@ -136,6 +138,7 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
                        const __grid_constant__ CUtensorMap mapSA,
                        const __grid_constant__ CUtensorMap mapSB, const MxParams p) {
   constexpr bool kGatedFwd = MODE == kFwdSwiglu || MODE == kFwdQgeglu;
+  constexpr bool kGatedBwd = MODE == kDgradSwigluBwd || MODE == kDgradQgegluBwd;
   constexpr float kAlpha = (MODE == kFwdQgeglu || MODE == kDgradQgegluBwd) ? 1.702f : 1.0f;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -167,7 +170,6 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
         const int mtiles = o1 > o0 ? (o1 - o0 + BM - 1) / BM : 0;
         tiles = ((mtiles + kCluster - 1) / kCluster) * NT;
         sft = mtiles;
-        st.row_start[e] = o0;
       }
       int incl = tiles, incl_sf = sft;
 #pragma unroll
@@ -190,7 +192,6 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
       const int o_first = p.offsets[0];
       const int o_last = p.offsets[E];
       if (o_first != 0 || o_last > p.R_cap || o_last < 0) bad = true;
-      st.row_start[E] = o_last;
       st.tiles_before[E] = carry;
       st.sf_before[E] = carry_sf;
     }
@@ -204,10 +205,8 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
         mbar_init(smem_u32(&st.full[s]), 1);
         mbar_init(smem_u32(&st.empty[s]), 1);
       }
-      for (int a = 0; a < 2; ++a) {
-        mbar_init(smem_u32(&st.tfull[a]), 1);
-        mbar_init(smem_u32(&st.tempty[a]), kCluster * kEpiWarps);
-      }
+      mbar_init(smem_u32(&st.tfull), 1);
+      mbar_init(smem_u32(&st.tempty), kCluster * kEpiWarps);
       mbar_init(smem_u32(&st.mma_done), 1);
       mbar_fence_init();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -243,7 +242,7 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
         int e, mp, nt;
         decode_tile(tile, st.tiles_before, E, NT, e, mp, nt);
         const int mt = mp * kCluster + h;
-        const int row0 = st.row_start[e] + mt * BM;
+        const int row0 = __ldg(p.offsets + e) + mt * BM;
         const int sf_row = (st.sf_before[e] + mt) * KB;
         const int b_row = kGatedFwd ? h * p.F + nt * kTileNHalf : nt * kTileN + h * kTileNHalf;
         const int sfb_row = (e * NT + nt) * KB;
@@ -284,14 +283,12 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
       // ------------------------------------------------ MMA issuer (even CTA)
       int stage = 0;
       uint32_t phase = 0;
-      int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int tile = cluster_id; tile < total && ok; tile += n_clusters) {
-        if (!mbar_wait_bounded(smem_u32(&st.tempty[acc]), acc_phase ^ 1u, abort_flag, p.status))
-          break;
+        // the epilogue has moved the previous tile's accumulator out of TMEM
+        if (!mbar_wait_bounded(smem_u32(&st.tempty), acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * kAccStride;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&st.full[stage]), phase, abort_flag, p.status)) {
             ok = false;
@@ -311,8 +308,9 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
           for (int kk = 0; kk < kKStep / 32; ++kk) {
             const uint64_t adesc = make_sdesc(sa + kk * 32, 16, 1024);
             const uint64_t bdesc = make_sdesc(sb + kk * 32, 16, 1024);
-            mx::mma_mx_pair(d_tmem, adesc, bdesc, mx::make_idesc_mx(kCluster * BM, kTileN, kk, kk),
-                            tsa, tsb, (kb | kk) != 0 ? 1u : 0u);
+            mx::mma_mx_pair(tmem_base, adesc, bdesc,
+                            mx::make_idesc_mx(kCluster * BM, kTileN, kk, kk), tsa, tsb,
+                            (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit_pair_mc(smem_u32(&st.empty[stage]), kClusterMask);
           if (++stage == STAGES) {
@@ -321,28 +319,31 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
           }
         }
         if (!ok) break;
-        tc_commit_pair_mc(smem_u32(&st.tfull[acc]), kClusterMask);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        tc_commit_pair_mc(smem_u32(&st.tfull), kClusterMask);
+        acc_phase ^= 1u;
       }
       tc_commit_pair(smem_u32(&st.mma_done));
       (void)mbar_wait_bounded(smem_u32(&st.mma_done), 0, nullptr, p.status);
     }
   } else {
     // -------------------------------------------------- epilogue (kEpiWarps warps)
+    // Warp w reads TMEM lanes 32*(w%4) .. +31 (its rows); the two warps of a
+    // lane quadrant take half of the 256 columns each. The warp's share goes
+    // to registers as BF16 (acc[16] = 4 chunks of 32 columns), the warp
+    // reports the accumulator free, then works from registers.
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const int r = q * 32 + lane;
-    int acc = 0;
     uint32_t acc_phase = 0;
     uint4* stg = reinterpret_cast<uint4*>(staging + (warp - 2) * kWarpStagingBytes);
+    const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     for (int tile = cluster_id; tile < total; tile += n_clusters) {
       int e, mp, nt;
       decode_tile(tile, st.tiles_before, E, NT, e, mp, nt);
       const int mt = mp * kCluster + static_cast<int>(crank);
-      const long long tile_row0 = static_cast<long long>(st.row_start[e]) + mt * BM;
+      const long long tile_row0 = static_cast<long long>(__ldg(p.offsets + e)) + mt * BM;
       const long long grow = tile_row0 + r;
-      const long long row_end = st.row_start[e + 1];
+      const long long row_end = __ldg(p.offsets + e + 1);
       const bool valid = grow < row_end;
       const long long grow0 = grow - lane;
       const int nvalid = static_cast<int>(max(0LL, min(32LL, row_end - grow0)));
@@ -350,62 +351,80 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
       // every row of it, code 0 for the rows past the expert's end
       const bool owns_sf = tile_row0 < row_end;
       const long long sf_tile = st.sf_before[e] + mt;
-      const uint32_t tbase =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccStride;
+      // the four 32-column chunks of this warp: plain and backward modes take
+      // columns [128 half, +128); FC1 takes gate [64 half, +64) and the
+      // matching up columns [128 + 64 half, +64)
+      float scale = 1.0f;
+      if (MODE == kDgradPlain && p.row_scale != nullptr && valid) scale = p.row_scale[grow];
+      // the saved H1 does not depend on the accumulator: fetch the first
+      // chunk of the backward before waiting for the MMAs
+      const int Fb = p.Nout;
+      const int n0 = nt * kTileN;
+      const int cb0 = half * (kTileN / 2);
+      const gg_bf16* hrow0 = kGatedBwd ? p.H1 + grow0 * (2LL * Fb) + n0 : nullptr;
+      uint4 graw[4], uraw[4];
+      if (kGatedBwd && n0 + cb0 < Fb) {
+        load_chunk_raw(graw, hrow0 + cb0, 2LL * Fb, nvalid);
+        load_chunk_raw(uraw, hrow0 + Fb + cb0, 2LL * Fb, nvalid);
+      }
+      if (!mbar_wait_bounded(smem_u32(&st.tfull), acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      uint4 acc[4][4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int col = kGatedFwd ? (j < 2 ? 64 * half + 32 * j : 128 + 64 * half + 32 * (j - 2))
+                                  : cb0 + 32 * j;
+        float v[32];
+        tmem_ld32(tq + col, v);
+        pack_bf16x32(v, scale, acc[j]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      // this warp's share of the accumulator is in registers: the MMAs of the
+      // next tile may overwrite it (relaxed arrive: only the completed TMEM
+      // reads need ordering)
+      if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&st.tempty), 0));
+      acc_phase ^= 1u;
+
       if (MODE == kFwdPlain || MODE == kDgradPlain) {
-        float scale = 1.0f;
-        if (MODE == kDgradPlain && p.row_scale != nullptr && valid) scale = p.row_scale[grow];
-        const int n0 = nt * kTileN;
-        const int c0 = half * (kTileN / 2);
         gg_bf16* crow0 = p.C + grow0 * p.ldc + n0;
-        if (!mbar_wait_bounded(smem_u32(&st.tfull[acc]), acc_phase, abort_flag, p.status)) break;
-        tc_fence_after();
-#pragma unroll 1
-        for (int c = c0; c < c0 + kTileN / 2; c += 32) {
-          if (n0 + c >= p.Nout) break;
-          float v[32];
-          tmem_ld32(tbase + c, v);
-          uint4 w[4];
-          pack_bf16x32(v, scale, w);
-          store_chunk(stg, w, crow0 + c, p.ldc, nvalid);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = cb0 + 32 * j;
+          if (n0 + c < p.Nout) store_chunk(stg, acc[j], crow0 + c, p.ldc, nvalid);
         }
       } else if (kGatedFwd) {
-        // columns [0, 96) of the tile are gate outputs j0 + c, [96, 192) the
-        // matching up outputs; chunks 0 and 1 go to the first warp of a lane
-        // quadrant, chunk 2 to the second
         const int F = p.F;
         const bool scaled = p.row_scale != nullptr;
         const float prow = scaled && valid ? p.row_scale[grow] : 1.0f;
         const int j0 = nt * kTileNHalf;
         const int KGq = p.Kq / kKStep;
-        const int c_lo = half == 0 ? 0 : 64;
-        const int c_hi = half == 0 ? 64 : 96;
-        gg_bf16* hrow0 = p.H1_save + grow0 * (2LL * F) + j0;
+        gg_bf16* hrow = p.H1_save + grow0 * (2LL * F) + j0;
         uint8_t* arow0 = p.Cq + grow0 * p.Kq + j0;
-        if (!mbar_wait_bounded(smem_u32(&st.tfull[acc]), acc_phase, abort_flag, p.status)) break;
-        tc_fence_after();
-#pragma unroll 1
-        for (int c = c_lo; c < c_hi; c += 32) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int c = 64 * half + 32 * j;  // gate column in the tile's 128
           if (j0 + c >= F) break;
-          float g[32], u[32];
-          tmem_ld32(tbase + c, g);
-          tmem_ld32(tbase + kTileNHalf + c, u);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            g[i] = round_bf16(g[i]);
-            u[i] = round_bf16(u[i]);
-          }
-          uint4 w[4];
           if (p.H1_save != nullptr) {
-            pack_bf16x32(g, 1.0f, w);
-            store_chunk(stg, w, hrow0 + c, 2LL * F, nvalid);
-            pack_bf16x32(u, 1.0f, w);
-            store_chunk(stg, w, hrow0 + F + c, 2LL * F, nvalid);
+            store_chunk(stg, acc[j], hrow + c, 2LL * F, nvalid);
+            store_chunk(stg, acc[j + 2], hrow + F + c, 2LL * F, nvalid);
           }
+          float a[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) g[i] = round_bf16(glu_mul(g[i], u[i], kAlpha, scaled, prow));
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t gw[4] = {acc[j][i].x, acc[j][i].y, acc[j][i].z, acc[j][i].w};
+            const uint32_t uw[4] = {acc[j + 2][i].x, acc[j + 2][i].y, acc[j + 2][i].z,
+                                    acc[j + 2][i].w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              a[8 * i + 2 * w] =
+                  round_bf16(glu_mul(bf16_lo(gw[w]), bf16_lo(uw[w]), kAlpha, scaled, prow));
+              a[8 * i + 2 * w + 1] =
+                  round_bf16(glu_mul(bf16_hi(gw[w]), bf16_hi(uw[w]), kAlpha, scaled, prow));
+            }
+          }
           uint32_t qv[8];
-          const uint32_t code = mx::quantize32(g, qv);
+          const uint32_t code = mx::quantize32(a, qv);
           store_chunk8(stg, qv, arow0 + c, p.Kq, nvalid);
           if (owns_sf) {
             const int col = j0 + c;
@@ -413,29 +432,19 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
                 static_cast<uint8_t>(valid ? code : 0u);
           }
         }
-      } else {  // gated backward: dA columns n0.., output [dg | du] quantised, K = 2F
-        const int F = p.Nout;
-        float scale = 1.0f;
-        if (p.row_scale != nullptr && valid) scale = p.row_scale[grow];
-        const int n0 = nt * kTileN;
-        const int c0 = half * (kTileN / 2);
-        const int c_end = min(c0 + kTileN / 2, F - n0);  // multiple of 32
+      } else {  // gated backward: dA columns n0 + cb0.., output [dg | du] quantised, K = 2F
+        const int F = Fb;
+        float prs = 1.0f;
+        if (p.row_scale != nullptr && valid) prs = p.row_scale[grow];
+        const int c_end = min(cb0 + kTileN / 2, F - n0);  // multiple of 32
         const int KGq = p.Kq / kKStep;
-        const gg_bf16* hrow0 = p.H1 + grow0 * (2LL * F) + n0;
         uint8_t* drow0 = p.Cq + grow0 * p.Kq + n0;
-        uint4 graw[4], uraw[4];
-        if (c0 < c_end) {
-          load_chunk_raw(graw, hrow0 + c0, 2LL * F, nvalid);
-          load_chunk_raw(uraw, hrow0 + F + c0, 2LL * F, nvalid);
-        }
-        if (!mbar_wait_bounded(smem_u32(&st.tfull[acc]), acc_phase, abort_flag, p.status)) break;
-        tc_fence_after();
         float rdot = 0.0f;
         const bool want_dot = p.rowdot != nullptr;
-#pragma unroll 1
-        for (int c = c0; c < c_end; c += 32) {
-          float v[32];
-          tmem_ld32(tbase + c, v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = cb0 + 32 * j;
+          if (c >= c_end) break;
           uint4 gw[4], uw[4];
           transpose_chunk(stg, graw, gw);
           transpose_chunk(stg, uraw, uw);
@@ -443,9 +452,11 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
             load_chunk_raw(graw, hrow0 + c + 32, 2LL * F, nvalid);
             load_chunk_raw(uraw, hrow0 + F + c + 32, 2LL * F, nvalid);
           }
-          uint32_t gs[16], us[16];
+          uint32_t as[16], gs[16], us[16];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
+            as[4 * i + 0] = acc[j][i].x; as[4 * i + 1] = acc[j][i].y;
+            as[4 * i + 2] = acc[j][i].z; as[4 * i + 3] = acc[j][i].w;
             gs[4 * i + 0] = gw[i].x; gs[4 * i + 1] = gw[i].y;
             gs[4 * i + 2] = gw[i].z; gs[4 * i + 3] = gw[i].w;
             us[4 * i + 0] = uw[i].x; us[4 * i + 1] = uw[i].y;
@@ -455,17 +466,17 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
           if (want_dot) {
 #pragma unroll
             for (int hh = 0; hh < 16; ++hh) {
-              glu_mul_bwd<true>(v[2 * hh], scale, bf16_lo(gs[hh]), bf16_lo(us[hh]), kAlpha,
+              glu_mul_bwd<true>(bf16_lo(as[hh]), prs, bf16_lo(gs[hh]), bf16_lo(us[hh]), kAlpha,
                                 dg[2 * hh], du[2 * hh], rdot);
-              glu_mul_bwd<true>(v[2 * hh + 1], scale, bf16_hi(gs[hh]), bf16_hi(us[hh]), kAlpha,
+              glu_mul_bwd<true>(bf16_hi(as[hh]), prs, bf16_hi(gs[hh]), bf16_hi(us[hh]), kAlpha,
                                 dg[2 * hh + 1], du[2 * hh + 1], rdot);
             }
           } else {
 #pragma unroll
             for (int hh = 0; hh < 16; ++hh) {
-              glu_mul_bwd<false>(v[2 * hh], scale, bf16_lo(gs[hh]), bf16_lo(us[hh]), kAlpha,
+              glu_mul_bwd<false>(bf16_lo(as[hh]), prs, bf16_lo(gs[hh]), bf16_lo(us[hh]), kAlpha,
                                  dg[2 * hh], du[2 * hh], rdot);
-              glu_mul_bwd<false>(v[2 * hh + 1], scale, bf16_hi(gs[hh]), bf16_hi(us[hh]), kAlpha,
+              glu_mul_bwd<false>(bf16_hi(as[hh]), prs, bf16_hi(gs[hh]), bf16_hi(us[hh]), kAlpha,
                                  dg[2 * hh + 1], du[2 * hh + 1], rdot);
             }
           }
@@ -490,11 +501,6 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
         if (p.rowdot != nullptr && valid)
           p.rowdot[grow * p.rowdot_stride + nt * 2 + half] = rdot;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&st.tempty[acc]), 0));
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
     }
   }
 

@@ -22,8 +22,8 @@
 // kept per expert-local 128-row tile: tile t of expert e is scale block
 // tiles_before(e) + t, and block `blk` of a K = 128*KG operand starts at
 // byte (blk * KG + kg) * 512. B-operand (weight) scales are kept per GEMM
-// column tile: [E][NT][KG][1024 bytes], columns 0..127 of the tile in the
-// first 512 bytes and 128..191 in the second.
+// column tile: [E][NT][KG][1024 bytes], columns 0..127 of the 256-column
+// tile in the first 512 bytes and 128..255 in the second.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -39,14 +39,14 @@ namespace mx {
 constexpr int kBlock = 32;        // elements per scale
 constexpr int kRowTile = 128;     // rows per A-operand scale tile
 constexpr int kKStep = 128;       // K elements (bytes) per GEMM k-step = 4 scale blocks
-constexpr int kTileN = 192;       // output columns per CTA-pair tile
-constexpr int kTileNHalf = 96;    // weight rows per CTA
+constexpr int kTileN = 256;       // output columns per CTA-pair tile
+constexpr int kTileNHalf = 128;   // weight rows per CTA
 constexpr int kSfaBytes = 512;    // one 128-row scale tile of one k-step
-constexpr int kSfbBytes = 1024;   // the 192-column scale tile of one k-step
+constexpr int kSfbBytes = 1024;   // the 256-column scale tile of one k-step
 
 __host__ __device__ constexpr int sf_byte(int r, int b) { return (r & 31) * 16 + (r >> 5) * 4 + b; }
 
-// Byte of column n (0..191) of a weight scale tile.
+// Byte of column n (0..255) of a weight scale tile.
 __host__ __device__ constexpr int sfb_byte(int n, int b) { return (n >> 7) * 512 + sf_byte(n & 127, b); }
 
 // Quantise one 32-element block. Returns the E8M0 byte (e + 127) and packs the

@@ -27,13 +27,15 @@ taken here (each also listed in the design notes):
   reduction dimension and accumulates exactly; the weights therefore exist in
   two quantisations: along their input dimension for the forward and along
   their output dimension for the input gradient.
-* The tensors a GEMM hands to the next one are BF16 before they are
-  quantised: FC1's output H1 is rounded to BF16 (it is also what the backward
-  reads), the gated activation is applied to those BF16 values and its result
-  rounded to BF16, and only then quantised for FC2; the same holds for the
-  SwiGLU gradient dH1 before the second input-gradient GEMM. The quantised
-  codes are decided on these BF16 values, which both this oracle and the
-  kernels compute.
+* Every GEMM's result is BF16, and the tensors one GEMM hands to the next are
+  BF16 before they are quantised: FC1's output H1 is rounded to BF16 (it is
+  also what the backward reads), the gated activation is applied to those
+  BF16 values and its result rounded to BF16, and only then quantised for
+  FC2; the input gradient of FC2 (the activation's output gradient) is
+  rounded to BF16 before the activation's backward, whose result dH1 is
+  rounded to BF16 before it is quantised for the second input-gradient GEMM.
+  The quantised codes are decided on these BF16 values, which both this
+  oracle and the kernels compute.
 
 Shapes follow ``moe_oracle``: W1[E, 2F, H], W2[E, H, F], x[T, H].
 """
@@ -202,7 +204,7 @@ def mx_backward(dOut, fwd: dict) -> dict:
     """MXFP8 expert layer, input gradient and probability gradient.
 
     dYq = mx(dOut rows) (each row of the permuted gradient is its token's
-    dOut), dA0 = dYq W2d, dA = dA0 times the probability (``combine`` and
+    dOut), dA0 = bf16(dYq W2d), dA = dA0 times the probability (``combine`` and
     ``activation`` modes: the probability scales the activation's output, or
     equivalently FC2's), dH1 = bf16(act'(H1) applied to dA), dXp = mx(dH1)
     W1d, dX = the plain sum of the k rows (probability-weighted in
@@ -225,7 +227,7 @@ def mx_backward(dOut, fwd: dict) -> dict:
     valid = sor >= 0
     dYp = np.zeros((R_cap, dOut.shape[1]))
     dYp[valid] = dOut[sor[valid] // k]
-    dA0 = _mo.grouped_linear_t(mx(dYp), W["W2d"], offsets)
+    dA0 = _mo.round_to_bf16(_mo.grouped_linear_t(mx(dYp), W["W2d"], offsets))
     dprob_rows = np.zeros(R_cap)
     rnd = _mo.round_to_bf16 if fwd.get("faithful") else (lambda v: v)
     if mode in ("combine", "activation"):

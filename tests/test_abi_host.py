@@ -182,10 +182,10 @@ def test_mx_layout_and_validation(gg):
     E, H, F = 4, 256, 384
     lay = gg.mx_weights_layout(E, H, F)
     # four E4M3 operands and their scale tiles, in order, 256-byte aligned, disjoint
-    sizes = {"w1": E * 2 * F * H, "w1_scales": E * (F // 96) * (H // 128) * 1024,
-             "w2": E * H * F, "w2_scales": E * 2 * (F // 128) * 1024,
+    sizes = {"w1": E * 2 * F * H, "w1_scales": E * (F // 128) * (H // 128) * 1024,
+             "w2": E * H * F, "w2_scales": E * 1 * (F // 128) * 1024,
              "w2t": E * F * H, "w2t_scales": E * 2 * (H // 128) * 1024,
-             "w1t": E * H * 2 * F, "w1t_scales": E * 2 * (2 * F // 128) * 1024}
+             "w1t": E * H * 2 * F, "w1t_scales": E * 1 * (2 * F // 128) * 1024}
     spans = sorted((lay[n], lay[n] + sz) for n, sz in sizes.items())
     for (a0, a1), (b0, _) in zip(spans, spans[1:]):
         assert a1 <= b0
@@ -196,9 +196,9 @@ def test_mx_layout_and_validation(gg):
             gg.mx_weights_layout(*bad)
     assert L.gg_mx_row_tiles(300, 3, 6, 16) == (300 * 3 + 6 * 15 + 127) // 128 + 6
     assert L.gg_mx_row_tiles(-1, 3, 6, 1) == 0
-    assert L.gg_mx_rowdot_blocks(768) == 8 and L.gg_mx_rowdot_blocks(384) == 4
-    assert L.gg_mx_rowdot_blocks(640) == 8 and L.gg_mx_rowdot_stride(640) == 8
-    assert L.gg_mx_rowdot_stride(1536) == 16 and L.gg_mx_rowdot_blocks(0) == 0
+    assert L.gg_mx_rowdot_blocks(768) == 6 and L.gg_mx_rowdot_blocks(384) == 4
+    assert L.gg_mx_rowdot_blocks(640) == 6 and L.gg_mx_rowdot_stride(640) == 8
+    assert L.gg_mx_rowdot_stride(2304) == 24 and L.gg_mx_rowdot_blocks(0) == 0
     # prepare: misaligned buffer, too small
     assert L.gg_mx_prepare_weights(p, p, E, H, F, mis, lay["bytes"], None) == 3
     assert L.gg_mx_prepare_weights(p, p, E, H, F, p, lay["bytes"] - 1, None) == 4

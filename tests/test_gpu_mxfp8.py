@@ -24,8 +24,9 @@ from oracle import mxfp8 as mxo
 
 pytestmark = pytest.mark.gpu
 
-# H, F multiples of 128; F = 256 gives a ragged last FC1 tile (96 + 96 + 64
-# gate columns), H = 384 two full FC2 tiles of 192, P = 16 padding rows
+# H, F multiples of 128; H = 384 gives a ragged last FC2 / input-gradient
+# tile (256 + 128 columns), F = 384 a ragged SwiGLU-backward tile, P = 16
+# padding rows
 MX_MID = MoeShape("mx_e8_h384_f256_t300_k2", E=8, H=384, F=256, T=300, k=2, routing="uniform",
                   x_std=1.0, w_std=0.05)
 MX_PAD = MoeShape("mx_e6_h256_f384_t257_k3_pad16", E=6, H=256, F=384, T=257, k=3, P=16,
@@ -98,9 +99,9 @@ def _weight_tiles(codes, NT, K, gated_F=0):
         if gated_F:
             up = n >= gated_F
             j = n - gated_F if up else n
-            nt, col = j // 96, j % 96 + (96 if up else 0)
+            nt, col = j // 128, j % 128 + (128 if up else 0)
         else:
-            nt, col = n // 192, n % 192
+            nt, col = n // 256, n % 256
         for blk in range(K // 32):
             S[:, nt, blk // 4, (col // 128) * 512 + _sf_byte(col % 128, blk % 4)] = codes[:, n, blk]
     return S
@@ -169,9 +170,9 @@ def test_prepare_weights_bit_exact(gg, E, H, F):
     mxw, L = gg.mx_prepare_weights(tb(W1), tb(W2))
     torch.cuda.synchronize()
     got = mxw.cpu().numpy()
-    ops = {"w1": (W1, (F + 95) // 96, F), "w2": (W2, (H + 191) // 192, 0),
-           "w2t": (np.swapaxes(W2, 1, 2), (F + 191) // 192, 0),
-           "w1t": (np.swapaxes(W1, 1, 2), (H + 191) // 192, 0)}
+    ops = {"w1": (W1, F // 128, F), "w2": (W2, (H + 255) // 256, 0),
+           "w2t": (np.swapaxes(W2, 1, 2), (F + 255) // 256, 0),
+           "w1t": (np.swapaxes(W1, 1, 2), (H + 255) // 256, 0)}
     for name, (Wop, NT, gF) in ops.items():
         Ex, N, K = Wop.shape
         bits, codes = _quant_bits(Wop)
@@ -253,7 +254,8 @@ def test_grouped_gemms_match_oracle(gg, shape, act):
     Yp_ref = oracle.grouped_linear(rows(Aq, As, s.F), W["W2f"], off)[:n]
     assert_parity(torch_to_f64(Yp)[:n], Yp_ref, "Yp", faithful=oracle.round_to_bf16(Yp_ref))
     # dgrad FC2 + activation backward from the kernel's dYq and H1
-    dA0 = oracle.grouped_linear_t(rows(dyq["Q"], dyq["S"], s.H), W["W2d"], off)[:n]
+    dA0 = oracle.round_to_bf16(
+        oracle.grouped_linear_t(rows(dyq["Q"], dyq["S"], s.H), W["W2d"], off)[:n])
     dq_ref, dc_ref = _quant_bits(oracle.round_to_bf16(oracle.glu_backward(dA0 * por, H1k, name)))
     _assert_codes_close(*codes(dHq, dHs, 2 * s.F), dq_ref, dc_ref, "dH1")
     rd = rowdot.cpu().numpy()[:n, :gg.mx_rowdot_blocks(s.F)].astype(np.float64).sum(axis=1)

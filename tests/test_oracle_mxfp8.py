@@ -136,9 +136,10 @@ def test_layer_reduces_to_bf16_oracle_on_representable_inputs():
         mb = mxo.mx_backward(dOut, mf)
         bb = oracle.moe_backward(dOut, oracle.moe_forward(x, idx, prob, W1, W2, E, 1,
                                                           prob_mode=mode), W1, W2)
-        # the activation gradient before the SwiGLU backward is exact here
-        dA_ref = oracle.grouped_linear_t(bb["dYp"], W2, mf["offsets"]) * mf["pr"][:, None]
-        np.testing.assert_allclose(mb["dA"], dA_ref, rtol=1e-12, atol=1e-12)
+        # the activation gradient before the SwiGLU backward: the exact product
+        # (the quantisations are the identity here), rounded once to BF16
+        dA_ref = oracle.round_to_bf16(oracle.grouped_linear_t(bb["dYp"], W2, mf["offsets"]))
+        np.testing.assert_array_equal(mb["dA"], dA_ref * mf["pr"][:, None])
         rel = np.linalg.norm(mb["dX"] - bb["dX"]) / np.linalg.norm(bb["dX"])
         assert rel < 0.05, rel
         rel = np.linalg.norm(mb["dprob"] - bb["dprob"]) / np.linalg.norm(bb["dprob"])
