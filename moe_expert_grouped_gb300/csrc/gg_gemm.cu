@@ -420,7 +420,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         if (!mbar_wait_bounded(smem_u32(&st.tfull[acc]), acc_phase, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-        float rdot = 0.0f;  // this row's <acc, a> over this warp's columns
+        // this row's <acc, a> over this warp's columns, in four independent
+        // partial sums (a single 32-long chain per chunk would serialise)
+        float rd[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         const bool want_dot = p.rowdot != nullptr;
         constexpr float alpha = kAlpha;
 #pragma unroll 1
@@ -447,17 +449,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
 #pragma unroll
             for (int h = 0; h < 16; ++h) {
               glu_mul_bwd<true>(v[2 * h], scale, bf16_lo(gs[h]), bf16_lo(us[h]), alpha,
-                                dg[2 * h], du[2 * h], rdot);
+                                dg[2 * h], du[2 * h], rd[h & 1]);
               glu_mul_bwd<true>(v[2 * h + 1], scale, bf16_hi(gs[h]), bf16_hi(us[h]), alpha,
-                                dg[2 * h + 1], du[2 * h + 1], rdot);
+                                dg[2 * h + 1], du[2 * h + 1], rd[2 + (h & 1)]);
             }
           } else {
 #pragma unroll
             for (int h = 0; h < 16; ++h) {
               glu_mul_bwd<false>(v[2 * h], scale, bf16_lo(gs[h]), bf16_lo(us[h]), alpha,
-                                 dg[2 * h], du[2 * h], rdot);
+                                 dg[2 * h], du[2 * h], rd[h & 1]);
               glu_mul_bwd<false>(v[2 * h + 1], scale, bf16_hi(gs[h]), bf16_hi(us[h]), alpha,
-                                 dg[2 * h + 1], du[2 * h + 1], rdot);
+                                 dg[2 * h + 1], du[2 * h + 1], rd[2 + (h & 1)]);
             }
           }
           uint4 w[4];
@@ -467,7 +469,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
           store_chunk(stg, w, drow0 + F + c, 2LL * F, nvalid);
         }
         if (p.rowdot != nullptr && valid)
-          p.rowdot[grow * p.rowdot_stride + nt * 2 + half] = rdot;
+          p.rowdot[grow * p.rowdot_stride + nt * 2 + half] = (rd[0] + rd[1]) + (rd[2] + rd[3]);
       }
       tc_fence_before();
       __syncwarp();

@@ -439,7 +439,7 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
         const int c_end = min(cb0 + kTileN / 2, F - n0);  // multiple of 32
         const int KGq = p.Kq / kKStep;
         uint8_t* drow0 = p.Cq + grow0 * p.Kq + n0;
-        float rdot = 0.0f;
+        float rd[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four independent partial sums
         const bool want_dot = p.rowdot != nullptr;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -467,17 +467,17 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
 #pragma unroll
             for (int hh = 0; hh < 16; ++hh) {
               glu_mul_bwd<true>(bf16_lo(as[hh]), prs, bf16_lo(gs[hh]), bf16_lo(us[hh]), kAlpha,
-                                dg[2 * hh], du[2 * hh], rdot);
+                                dg[2 * hh], du[2 * hh], rd[hh & 1]);
               glu_mul_bwd<true>(bf16_hi(as[hh]), prs, bf16_hi(gs[hh]), bf16_hi(us[hh]), kAlpha,
-                                dg[2 * hh + 1], du[2 * hh + 1], rdot);
+                                dg[2 * hh + 1], du[2 * hh + 1], rd[2 + (hh & 1)]);
             }
           } else {
 #pragma unroll
             for (int hh = 0; hh < 16; ++hh) {
               glu_mul_bwd<false>(bf16_lo(as[hh]), prs, bf16_lo(gs[hh]), bf16_lo(us[hh]), kAlpha,
-                                 dg[2 * hh], du[2 * hh], rdot);
+                                 dg[2 * hh], du[2 * hh], rd[hh & 1]);
               glu_mul_bwd<false>(bf16_hi(as[hh]), prs, bf16_hi(gs[hh]), bf16_hi(us[hh]), kAlpha,
-                                 dg[2 * hh + 1], du[2 * hh + 1], rdot);
+                                 dg[2 * hh + 1], du[2 * hh + 1], rd[2 + (hh & 1)]);
             }
           }
 #pragma unroll
@@ -499,7 +499,7 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
           }
         }
         if (p.rowdot != nullptr && valid)
-          p.rowdot[grow * p.rowdot_stride + nt * 2 + half] = rdot;
+          p.rowdot[grow * p.rowdot_stride + nt * 2 + half] = (rd[0] + rd[1]) + (rd[2] + rd[3]);
       }
     }
   }

@@ -56,9 +56,16 @@ __host__ __device__ constexpr int sfb_byte(int n, int b) { return (n >> 7) * 512
 // A zero or subnormal maximum takes e = -127. Multiplying by 2^-e is exact;
 // the conversion rounds to nearest even and saturates at 448.
 __device__ __forceinline__ uint32_t quantize32(const float (&v)[32], uint32_t (&q)[8]) {
-  float amax = 0.0f;
+  // block maximum as a 5-level tree (a 32-long chain would serialise)
+  float m[16];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  for (int i = 0; i < 16; ++i) m[i] = fmaxf(fabsf(v[i]), fabsf(v[i + 16]));
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1) {
+#pragma unroll
+    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+  }
+  const float amax = m[0];
   const uint32_t bits = __float_as_uint(amax);
   const int biased = static_cast<int>(bits >> 23);
   int e = biased == 0 ? -127 : biased - 135 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
