@@ -43,8 +43,13 @@ Shapes follow ``moe_oracle``: W1[E, 2F, H], W2[E, H, F], x[T, H].
 from __future__ import annotations
 
 import numpy as np
+import torch
 
 from . import moe_oracle as _mo
+
+# The elementwise steps below run as plain PyTorch CPU ops on views of the
+# numpy arrays (same arithmetic, fp64; PyTorch spreads them over the host
+# cores, which matters for the full-size weights).
 
 BLOCK = 32
 E4M3_MAX = 448.0
@@ -58,14 +63,14 @@ def e4m3_round(v: np.ndarray) -> np.ndarray:
 
     Normal E4M3 numbers 2^E * (1 + m/8) cover exponents E in [-6, 8]; below
     2^-6 the grid is the subnormal step 2^-9."""
-    v = np.asarray(v, dtype=np.float64)
-    a = np.abs(v)
-    _, p = np.frexp(a)                      # a = f * 2^p, f in [0.5, 1)
-    E = np.maximum(p - 1, -6)               # binade of a; subnormals share E = -6
-    step = np.ldexp(1.0, E - 3)             # 3 mantissa bits
-    q = np.rint(a / step) * step            # np.rint rounds half to even
-    q = np.minimum(q, E4M3_MAX)
-    return np.copysign(q, v)
+    v = torch.from_numpy(np.ascontiguousarray(v, dtype=np.float64))
+    a = v.abs()
+    _, p = torch.frexp(a)                   # a = f * 2^p, f in [0.5, 1)
+    E = torch.clamp(p - 1, min=-6)          # binade of a; subnormals share E = -6
+    step = torch.ldexp(torch.ones_like(a), E - 3)   # 3 mantissa bits
+    q = torch.round(a / step) * step        # torch.round rounds half to even
+    q = torch.clamp(q, max=E4M3_MAX)
+    return torch.copysign(q, v).numpy()
 
 
 def e4m3_bits(q: np.ndarray) -> np.ndarray:
@@ -103,12 +108,12 @@ def block_exponent(amax: np.ndarray) -> np.ndarray:
 
     With amax = (1 + f) * 2^q, 448 = 1.75 * 2^8: e = q - 8 when 1 + f <= 1.75,
     else q - 7."""
-    amax = np.asarray(amax, dtype=np.float64)
-    f, p = np.frexp(amax)                   # amax = f * 2^p, f in [0.5, 1)
-    q = p - 1
-    e = q - 8 + (2.0 * f > 1.75)
-    e = np.where(amax > 0, e, -E8M0_BIAS)
-    return np.clip(e, -E8M0_BIAS, E8M0_BIAS).astype(np.int64)
+    amax = torch.from_numpy(np.ascontiguousarray(amax, dtype=np.float64))
+    f, p = torch.frexp(amax)                # amax = f * 2^p, f in [0.5, 1)
+    q = p.to(torch.int64) - 1
+    e = q - 8 + (2.0 * f > 1.75).to(torch.int64)
+    e = torch.where(amax > 0, e, torch.full_like(e, -E8M0_BIAS))
+    return torch.clamp(e, -E8M0_BIAS, E8M0_BIAS).numpy()
 
 
 def quantize(v: np.ndarray):
@@ -120,18 +125,21 @@ def quantize(v: np.ndarray):
     K = v.shape[-1]
     if K % BLOCK:
         raise ValueError("the quantised axis must be a multiple of 32")
-    blocks = v.reshape(v.shape[:-1] + (K // BLOCK, BLOCK))
-    e = block_exponent(np.max(np.abs(blocks), axis=-1))
-    q = e4m3_round(blocks / np.ldexp(1.0, e)[..., None])
+    blocks = torch.from_numpy(np.ascontiguousarray(v)).reshape(v.shape[:-1] + (K // BLOCK, BLOCK))
+    e = block_exponent(blocks.abs().amax(dim=-1).numpy())
+    scale = torch.ldexp(torch.ones(e.shape, dtype=torch.float64), torch.from_numpy(e))
+    q = e4m3_round((blocks / scale[..., None]).numpy())
     return q.reshape(v.shape), e
 
 
 def dequantize(q: np.ndarray, e: np.ndarray) -> np.ndarray:
     """Exact value of MXFP8 data: element times its block's 2^e."""
-    q = np.asarray(q, dtype=np.float64)
+    q = torch.from_numpy(np.ascontiguousarray(q, dtype=np.float64))
     K = q.shape[-1]
     blocks = q.reshape(q.shape[:-1] + (K // BLOCK, BLOCK))
-    return (blocks * np.ldexp(1.0, np.asarray(e))[..., None]).reshape(q.shape)
+    e = torch.from_numpy(np.ascontiguousarray(e, dtype=np.int64))
+    scale = torch.ldexp(torch.ones(e.shape, dtype=torch.float64), e)
+    return (blocks * scale[..., None]).reshape(q.shape).numpy()
 
 
 def mx(v: np.ndarray) -> np.ndarray:
@@ -157,7 +165,7 @@ def mx_weights(W1, W2):
 # ---------------------------------------------------------------- the layer
 
 def mx_forward(x, idx, prob, W1, W2, E: int, P: int = 1, activation: str = "swiglu",
-               prob_mode: str = "combine", faithful: bool = False) -> dict:
+               prob_mode: str = "combine", faithful: bool = False, weights=None) -> dict:
     """MXFP8 expert layer, forward (readings in the module docstring).
 
     Xq = mx(x rows), H1 = bf16(Xq W1f^T), A = bf16(act(H1)) (times the
@@ -165,14 +173,15 @@ def mx_forward(x, idx, prob, W1, W2, E: int, P: int = 1, activation: str = "swig
     the probability-weighted (``combine``) or plain sum of the k rows. The
     pre-FC1 probability mode scales x before its quantisation. With
     ``faithful``, Yp and out are also rounded to BF16 (where the GPU path
-    stores them); that only sizes the error budget of a parity test."""
+    stores them); that only sizes the error budget of a parity test.
+    ``weights`` may pass the result of ``mx_weights(W1, W2)`` to reuse it."""
     if prob_mode not in ("combine", "activation", "pre_fc1"):
         raise ValueError(prob_mode)
     x = _mo._as_f64(x)
     idx = np.asarray(idx)
     prob = np.asarray(prob, dtype=np.float64)
     T, k = idx.shape
-    W = mx_weights(W1, W2)
+    W = mx_weights(W1, W2) if weights is None else weights
     offsets, row_of_slot, slot_of_row = _mo.route(idx, E, P)
     R_cap = slot_of_row.shape[0]
     pr = np.zeros(R_cap)

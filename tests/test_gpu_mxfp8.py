@@ -350,3 +350,32 @@ def test_layer_empty_batch_and_zero_token_experts(gg):
     g = empty.backward(d["dOut"][:0], mxw)
     torch.cuda.synchronize()
     assert o.shape == (0, s.H) and g.shape == (0, s.H)
+
+
+def test_layer_fullsize_sampled_parity(gg):
+    """The balanced 128-expert layer at full size (the benchmark's workload and
+    launch configuration); outputs and gradients of a seeded token sample
+    against the MXFP8 oracle run on that sub-batch (rows are independent, the
+    weights' quantisation does not depend on the batch)."""
+    from moe_synth import CONFIGS
+
+    s = CONFIGS[2]
+    inp = make_inputs(s, 2000 + 17)
+    d = _dev(inp)
+    mxw, _ = gg.mx_prepare_weights(d["W1"], d["W2"])
+    layer, out, dX, dprob = _layer(gg, s, d, mxw)
+    off, ros, sor = oracle.route(inp.idx, s.E, s.P)
+    np.testing.assert_array_equal(layer.view("offsets").cpu().numpy(), off)
+    np.testing.assert_array_equal(layer.view("row_of_slot").cpu().numpy(), ros)
+    rng = np.random.default_rng(7)
+    sel = np.sort(rng.choice(s.T, size=48, replace=False))
+    W = mxo.mx_weights(inp.W1, inp.W2)
+    f = mxo.mx_forward(inp.x[sel], inp.idx[sel], inp.prob[sel], inp.W1, inp.W2, s.E, 1,
+                       weights=W)
+    ff = mxo.mx_forward(inp.x[sel], inp.idx[sel], inp.prob[sel], inp.W1, inp.W2, s.E, 1,
+                        faithful=True, weights=W)
+    b, fb = mxo.mx_backward(inp.dOut[sel], f), mxo.mx_backward(inp.dOut[sel], ff)
+    assert_parity(torch_to_f64(out)[sel], f["out"], "out", faithful=ff["out"])
+    assert_parity(torch_to_f64(dX)[sel], b["dX"], "dX", faithful=fb["dX"])
+    assert_parity(dprob.cpu().numpy().astype(np.float64)[sel], b["dprob"], "dprob",
+                  faithful=fb["dprob"])
