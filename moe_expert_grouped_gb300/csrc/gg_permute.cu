@@ -398,12 +398,19 @@ combine_dprob_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ r
       }
     }
     const int rd_stride = (n_rowdot + 7) / 8 * 8;
-    float4 part0 = make_float4(0.f, 0.f, 0.f, 0.f), part1 = part0;
+    // a pair's first 8 or 16 partials, loaded before the column loop
+    float4 part[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) part[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (lane < k && my_row >= 0) {
       const float4* rd =
           reinterpret_cast<const float4*>(rowdot + static_cast<long long>(my_row) * rd_stride);
-      part0 = __ldg(rd);
-      part1 = __ldg(rd + 1);
+      part[0] = __ldg(rd);
+      part[1] = __ldg(rd + 1);
+      if (rd_stride >= 16) {
+        part[2] = __ldg(rd + 2);
+        part[3] = __ldg(rd + 3);
+      }
     }
     // The column loop is warp-uniform so that the shuffles below see every lane.
     for (int c0 = 0; c0 < vec_per_row; c0 += 64) {
@@ -440,16 +447,15 @@ combine_dprob_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ r
     }
     if (lane < k) {
       float dp = 0.0f;
-      if (n_rowdot > 0) dp += part0.x;
-      if (n_rowdot > 1) dp += part0.y;
-      if (n_rowdot > 2) dp += part0.z;
-      if (n_rowdot > 3) dp += part0.w;
-      if (n_rowdot > 4) dp += part1.x;
-      if (n_rowdot > 5) dp += part1.y;
-      if (n_rowdot > 6) dp += part1.z;
-      if (n_rowdot > 7) dp += part1.w;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (n_rowdot > 4 * i + 0) dp += part[i].x;
+        if (n_rowdot > 4 * i + 1) dp += part[i].y;
+        if (n_rowdot > 4 * i + 2) dp += part[i].z;
+        if (n_rowdot > 4 * i + 3) dp += part[i].w;
+      }
       if (my_row >= 0)
-        for (int b = 8; b < n_rowdot; ++b)
+        for (int b = 16; b < n_rowdot; ++b)
           dp += __ldg(rowdot + static_cast<long long>(my_row) * rd_stride + b);
       dprob[static_cast<long long>(t) * k + lane] = dp;
     }

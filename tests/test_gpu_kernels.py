@@ -233,7 +233,9 @@ def test_combine_prob_gradient_sums_partials_in_order(gg):
     rows[[5, 77, 301]] = -1
     Yp = normal_bf16(rng, (R_cap, H), 1.0)
     ws = gg.workspace(T, k, 1, "cuda")
-    for nb in (6, 8, 11):  # one group of 8 with padding, exactly one, a second group
+    # one group of 8 with padding, exactly one, two groups (padded, exact),
+    # and partials past the 16 loaded before the column loop
+    for nb in (6, 8, 11, 16, 19):
         nbs = (nb + 7) // 8 * 8
         rowdot = np.full((R_cap, nbs), np.nan, np.float32)
         rowdot[:, :nb] = rng.standard_normal((R_cap, nb))
