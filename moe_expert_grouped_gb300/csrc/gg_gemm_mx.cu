@@ -409,22 +409,20 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
             store_chunk(stg, acc[j], hrow + c, 2LL * F, nvalid);
             store_chunk(stg, acc[j + 2], hrow + F + c, 2LL * F, nvalid);
           }
-          float a[32];
+          uint32_t pa[16];  // the activation as BF16 pairs
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const uint32_t gw[4] = {acc[j][i].x, acc[j][i].y, acc[j][i].z, acc[j][i].w};
             const uint32_t uw[4] = {acc[j + 2][i].x, acc[j + 2][i].y, acc[j + 2][i].z,
                                     acc[j + 2][i].w};
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              a[8 * i + 2 * w] =
-                  round_bf16(glu_mul(bf16_lo(gw[w]), bf16_lo(uw[w]), kAlpha, scaled, prow));
-              a[8 * i + 2 * w + 1] =
-                  round_bf16(glu_mul(bf16_hi(gw[w]), bf16_hi(uw[w]), kAlpha, scaled, prow));
-            }
+            for (int w = 0; w < 4; ++w)
+              pa[4 * i + w] =
+                  pack_bf16x2(glu_mul(bf16_lo(gw[w]), bf16_lo(uw[w]), kAlpha, scaled, prow),
+                              glu_mul(bf16_hi(gw[w]), bf16_hi(uw[w]), kAlpha, scaled, prow));
           }
           uint32_t qv[8];
-          const uint32_t code = mx::quantize32(a, qv);
+          const uint32_t code = mx::quantize32_bf16(pa, qv);
           store_chunk8(stg, qv, arow0 + c, p.Kq, nvalid);
           if (owns_sf) {
             const int col = j0 + c;
@@ -462,33 +460,30 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
             us[4 * i + 0] = uw[i].x; us[4 * i + 1] = uw[i].y;
             us[4 * i + 2] = uw[i].z; us[4 * i + 3] = uw[i].w;
           }
-          float dg[32], du[32];
-          if (want_dot) {
+          // dg and du go to BF16 pairs as soon as they exist (the values the
+          // block quantiser takes), which halves their live registers
+          uint32_t pg[16], pu[16];
 #pragma unroll
-            for (int hh = 0; hh < 16; ++hh) {
+          for (int hh = 0; hh < 16; ++hh) {
+            float g0, g1, u0, u1;
+            if (want_dot) {
               glu_mul_bwd<true>(bf16_lo(as[hh]), prs, bf16_lo(gs[hh]), bf16_lo(us[hh]), kAlpha,
-                                dg[2 * hh], du[2 * hh], rd[hh & 1]);
+                                g0, u0, rd[hh & 1]);
               glu_mul_bwd<true>(bf16_hi(as[hh]), prs, bf16_hi(gs[hh]), bf16_hi(us[hh]), kAlpha,
-                                dg[2 * hh + 1], du[2 * hh + 1], rd[2 + (hh & 1)]);
-            }
-          } else {
-#pragma unroll
-            for (int hh = 0; hh < 16; ++hh) {
+                                g1, u1, rd[2 + (hh & 1)]);
+            } else {
               glu_mul_bwd<false>(bf16_lo(as[hh]), prs, bf16_lo(gs[hh]), bf16_lo(us[hh]), kAlpha,
-                                 dg[2 * hh], du[2 * hh], rd[hh & 1]);
+                                 g0, u0, rd[hh & 1]);
               glu_mul_bwd<false>(bf16_hi(as[hh]), prs, bf16_hi(gs[hh]), bf16_hi(us[hh]), kAlpha,
-                                 dg[2 * hh + 1], du[2 * hh + 1], rd[2 + (hh & 1)]);
+                                 g1, u1, rd[2 + (hh & 1)]);
             }
-          }
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            dg[i] = round_bf16(dg[i]);
-            du[i] = round_bf16(du[i]);
+            pg[hh] = pack_bf16x2(g0, g1);
+            pu[hh] = pack_bf16x2(u0, u1);
           }
           uint32_t qv[8];
-          const uint32_t code_g = mx::quantize32(dg, qv);
+          const uint32_t code_g = mx::quantize32_bf16(pg, qv);
           store_chunk8(stg, qv, drow0 + c, p.Kq, nvalid);
-          const uint32_t code_u = mx::quantize32(du, qv);
+          const uint32_t code_u = mx::quantize32_bf16(pu, qv);
           store_chunk8(stg, qv, drow0 + F + c, p.Kq, nvalid);
           if (owns_sf) {
             const int cg = n0 + c, cu = F + n0 + c;
