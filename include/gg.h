@@ -112,7 +112,8 @@ uint64_t gg_launch_count(void);
 /* Bytes of workspace every call below needs for a batch of T tokens with
  * top-k routing over E experts. The first 256 bytes hold the status word;
  * the rest is scratch for the permute's per-block expert histograms (one
- * int32 per expert and 256-pair block). */
+ * int32 per expert and block; at most 128 blocks, each of a multiple of
+ * 1024 pairs, at least 1024). */
 size_t gg_workspace_size(int T, int k, int E);
 
 /* Zero the status word at the start of `ws` (stream-ordered). */
@@ -162,12 +163,13 @@ gg_status gg_permute(const gg_bf16* x, const int32_t* idx, const float* prob,
  * callers without a device allocator. This entry point computes exactly what
  * gg_permute computes (same arguments, same outputs, bit-identical results)
  * but takes no `ws`: its scratch (status word + per-block expert histograms)
- * lives in a fixed 8 MiB array in the library's device image, which every GPU
- * that loads the library keeps until the process exits. It calls no
- * cudaMalloc, cudaFree or allocating library routine.
- *   - Limit: gg_workspace_size(T, k, E) <= 8 MiB, i.e. ceil(T*k/256) * E <=
- *     2097088 (for E = 128: T*k <= 4,194,048 pairs). Larger batches are
- *     rejected with GG_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ * lives in a fixed 256 KiB (+ 256 bytes) array in the library's device
+ * image, which every GPU that loads the library keeps until the process
+ * exits. It calls no cudaMalloc, cudaFree or allocating library routine.
+ *   - Limit: gg_workspace_size(T, k, E) <= 256 KiB + 256 bytes: any batch for
+ *     E <= 512; for larger E, T*k <= 1024 * floor(65536 / E) pairs (65,536
+ *     at E = 1024). Larger batches are rejected with
+ *     GG_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
  *   - Set-up: the first call on a device (made with that device current)
  *     looks up the array's device address once; make that first call before
  *     any stream capture.

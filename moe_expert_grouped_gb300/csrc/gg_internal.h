@@ -13,13 +13,22 @@ namespace gg {
 // Workspace layout: [0, 256) status word + reserved; then the permute's
 // per-block expert histograms (int32 [n_blocks][E]).
 constexpr size_t kWsHeader = 256;
-constexpr int kPermuteBlockThreads = 256;
-constexpr int kPermutePairsPerWarp = 32;  // one step of 32 pairs
-constexpr int kPermutePairsPerBlock = kPermutePairsPerWarp * (kPermuteBlockThreads / 32);
+constexpr int kPermuteBlockThreads = 1024;
+constexpr int kPermuteMaxBlocks = 128;  // histogram rows every scatter block reads
 constexpr int kMaxExperts = 1024;
 
+// The permute splits its R pairs into at most kPermuteMaxBlocks blocks of a
+// whole number of 1024-pair steps (one 32-pair step per warp).
+inline long long permute_pairs_per_block(long long pairs) {
+  const long long per = (pairs + kPermuteMaxBlocks - 1) / kPermuteMaxBlocks;
+  const long long step = kPermuteBlockThreads;
+  const long long ppb = (per + step - 1) / step * step;
+  return ppb > step ? ppb : step;
+}
+
 inline int permute_blocks(long long pairs) {
-  return static_cast<int>((pairs + kPermutePairsPerBlock - 1) / kPermutePairsPerBlock);
+  const long long ppb = permute_pairs_per_block(pairs);
+  return static_cast<int>((pairs + ppb - 1) / ppb);
 }
 
 void count_launch(int n = 1);

@@ -21,7 +21,6 @@ namespace gg {
 namespace {
 
 constexpr int kWarps = kPermuteBlockThreads / 32;
-constexpr int kSteps = kPermutePairsPerWarp / 32;
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t m;
@@ -29,168 +28,179 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
-// Per-warp expert histogram of this block's pairs, into hist[warp][E].
-// Pairs with an id outside [0, E) are ignored (and reported).
-__device__ __forceinline__ void warp_histogram(const int32_t* __restrict__ idx, long long R, int E,
-                                               long long block_first, int* hist,
-                                               int32_t* status) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int* h = hist + warp * E;
-  const long long first = block_first + static_cast<long long>(warp) * kPermutePairsPerWarp;
-#pragma unroll 1
-  for (int step = 0; step < kSteps; ++step) {
-    const long long p = first + step * 32 + lane;
-    int e = -1;
-    if (p < R) {
-      e = idx[p];
-      if (e < 0 || e >= E) {
-        set_status(status, GG_ERR_DEVICE_BAD_EXPERT_ID);
-        e = -1;
-      }
-    }
-    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
-    if (e >= 0 && (peers & lanemask_lt()) == 0) h[e] += __popc(peers);
-    __syncwarp();
+// Expert of pair p, or -1 for p >= R and for an id outside [0, E) (reported
+// when status is not null).
+__device__ __forceinline__ int pair_expert(const int32_t* __restrict__ idx, long long p,
+                                           long long R, int E, int32_t* status) {
+  if (p >= R) return -1;
+  const int e = idx[p];
+  if (e < 0 || e >= E) {
+    if (status != nullptr) set_status(status, GG_ERR_DEVICE_BAD_EXPERT_ID);
+    return -1;
   }
+  return e;
 }
 
+// Block b counts the experts of pairs [b ppb, (b + 1) ppb) into
+// block_hist[b][E]. It also marks every row as padding (slot -1, probability
+// 0); the scatter kernel fills in the routed rows.
 __global__ void __launch_bounds__(kPermuteBlockThreads)
-permute_count_kernel(const int32_t* __restrict__ idx, long long R, int E,
+permute_count_kernel(const int32_t* __restrict__ idx, long long R, int E, long long ppb,
                      int32_t* __restrict__ block_hist, int32_t* status,
                      int32_t* __restrict__ slot_of_row, float* __restrict__ prob_of_row,
                      long long R_cap) {
-  // every row starts as padding (slot -1, probability 0); the scatter kernel
-  // fills in the routed rows
   for (long long r = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; r < R_cap;
        r += static_cast<long long>(gridDim.x) * blockDim.x) {
     slot_of_row[r] = -1;
     prob_of_row[r] = 0.0f;
   }
-  extern __shared__ int hist[];  // [kWarps][E]
-  for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
-  const long long first = static_cast<long long>(blockIdx.x) * kPermutePairsPerBlock;
-  warp_histogram(idx, R, E, first, hist, status);
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int s = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) s += hist[w * E + e];
-    block_hist[static_cast<long long>(blockIdx.x) * E + e] = s;
-  }
-}
-
-// One block: per expert, exclusive prefix of the block histograms (in place),
-// then offsets[] = exclusive prefix of the padded per-expert counts.
-__global__ void __launch_bounds__(1024)
-permute_scan_kernel(int32_t* __restrict__ block_hist, int nb, int E, int P,
-                    int32_t* __restrict__ offsets) {
-  __shared__ int part_sum[1024];
-  __shared__ int warp_tot[32];
-  const int parts = max(1, static_cast<int>(blockDim.x) / E);
-  const int t = threadIdx.x;
-  const int e = t % E;
-  const int part = t / E;
-  const bool active = part < parts && t < parts * E;
-  int b0 = 0, b1 = 0;
-  if (active) {
-    b0 = static_cast<int>((static_cast<long long>(nb) * part) / parts);
-    b1 = static_cast<int>((static_cast<long long>(nb) * (part + 1)) / parts);
-  }
-  // (1) each (expert, part) sums its blocks
-  int s = 0;
-  if (active)
-    for (int b = b0; b < b1; ++b) s += block_hist[static_cast<long long>(b) * E + e];
-  part_sum[t] = active ? s : 0;
-  __syncthreads();
-  // (2) exclusive prefix across parts, then rewrite the blocks in place
-  if (active) {
-    int run = 0;
-    for (int q = 0; q < part; ++q) run += part_sum[q * E + e];
-    for (int b = b0; b < b1; ++b) {
-      const long long i = static_cast<long long>(b) * E + e;
-      const int c = block_hist[i];
-      block_hist[i] = run;
-      run += c;
-    }
-  }
-  __syncthreads();
-  // (3) padded totals per expert, exclusive scan over experts
-  for (int base = 0; base < E; base += blockDim.x) {
-    const int ee = base + t;
-    int padded = 0;
-    if (ee < E) {
-      int cnt = 0;
-      for (int q = 0; q < parts; ++q) cnt += part_sum[q * E + ee];
-      padded = ((cnt + P - 1) / P) * P;
-    }
-    // block-wide inclusive scan of `padded`
-    int v = padded;
-    const int lane = t & 31, warp = t >> 5;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int n = __shfl_up_sync(0xFFFFFFFFu, v, d);
-      if (lane >= d) v += n;
-    }
-    if (lane == 31) warp_tot[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-      int w = (lane < static_cast<int>(blockDim.x >> 5)) ? warp_tot[lane] : 0;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int n = __shfl_up_sync(0xFFFFFFFFu, w, d);
-        if (lane >= d) w += n;
-      }
-      warp_tot[lane] = w;
-    }
-    __syncthreads();
-    const int carry = (base == 0) ? 0 : offsets[base];
-    const int incl = v + (warp > 0 ? warp_tot[warp - 1] : 0) + carry;
-    if (ee < E) offsets[ee + 1] = incl;
-    if (ee == 0) offsets[0] = 0;
-    __syncthreads();
-  }
-}
-
-__global__ void __launch_bounds__(kPermuteBlockThreads)
-permute_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict__ prob,
-                       long long R, int E, const int32_t* __restrict__ block_prefix,
-                       const int32_t* __restrict__ offsets, int32_t* __restrict__ row_of_slot,
-                       int32_t* __restrict__ slot_of_row, float* __restrict__ prob_of_row) {
-  extern __shared__ int hist[];  // [kWarps][E]: counts, then running row bases
-  for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
-  const long long first = static_cast<long long>(blockIdx.x) * kPermutePairsPerBlock;
-  warp_histogram(idx, R, E, first, hist, nullptr);
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = offsets[e] + block_prefix[static_cast<long long>(blockIdx.x) * E + e];
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const int c = hist[w * E + e];
-      hist[w * E + e] = run;
-      run += c;
-    }
-  }
+  extern __shared__ int hist[];  // [E]
+  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int* base = hist + warp * E;
-  const long long wfirst = first + static_cast<long long>(warp) * kPermutePairsPerWarp;
+  const long long first = static_cast<long long>(blockIdx.x) * ppb;
+  const long long last = min(R, first + ppb);
 #pragma unroll 1
-  for (int step = 0; step < kSteps; ++step) {
-    const long long p = wfirst + step * 32 + lane;
-    int e = -1;
-    if (p < R) {
-      e = idx[p];
-      if (e < 0 || e >= E) e = -1;
+  for (long long p0 = first + 32LL * warp; p0 < last; p0 += kPermuteBlockThreads) {
+    const int e = pair_expert(idx, p0 + lane, last, E, status);
+    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+    if (e >= 0 && (peers & lanemask_lt()) == 0) atomicAdd(&hist[e], __popc(peers));
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    block_hist[static_cast<long long>(blockIdx.x) * E + e] = hist[e];
+}
+
+// Block b of the scatter (nb = number of count blocks; one block when nb = 0):
+//  (1) from all nb histogram rows, every expert's total count and the count in
+//      the blocks before b (each of the 1024 / E threads of an expert sums a
+//      range of rows with its loads in flight together);
+//  (2) offsets = exclusive prefix of the totals padded to multiples of P
+//      (written by block 0);
+//  (3) the per-warp histograms of its own pairs (warp w owns the contiguous
+//      pairs [b ppb + w ppb / 32, +ppb / 32), 32 at a time), turned into
+//      running row bases: expert e's rows for warp w of block b start at
+//      offsets[e] + (count of e before b) + (count of e in warps < w);
+//  (4) stable rows: each warp walks its pairs in order, a pair's row is its
+//      warp base plus the number of earlier lanes of the step with the same
+//      expert. No order-dependent atomics anywhere: the maps are bit-exact.
+__global__ void __launch_bounds__(kPermuteBlockThreads)
+permute_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict__ prob,
+                       long long R, int E, int P, long long ppb, int nb,
+                       const int32_t* __restrict__ block_hist, int32_t* __restrict__ offsets,
+                       int32_t* __restrict__ row_of_slot, int32_t* __restrict__ slot_of_row,
+                       float* __restrict__ prob_of_row) {
+  extern __shared__ int sm[];
+  int* wb = sm;                          // [kWarps][E]: warp counts, then warp row bases
+  int* part_all = wb + kWarps * E;       // [kPermuteBlockThreads]
+  int* part_below = part_all + kPermuteBlockThreads;
+  int* base_e = part_below + kPermuteBlockThreads;  // [E]: offsets[e] + count before b
+  __shared__ int warp_tot[kWarps];
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int b = blockIdx.x;
+
+  // (1) totals and counts before this block
+  const int parts = max(1, kPermuteBlockThreads / E);
+  {
+    const int e = t % E, part = t / E;
+    int s_all = 0, s_below = 0;
+    if (part < parts && t < parts * E) {
+      const int b0 = static_cast<int>((static_cast<long long>(nb) * part) / parts);
+      const int b1 = static_cast<int>((static_cast<long long>(nb) * (part + 1)) / parts);
+      constexpr int kChunk = 8;
+      for (int r0 = b0; r0 < b1; r0 += kChunk) {
+        int v[kChunk];
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j)
+          v[j] = r0 + j < b1 ? block_hist[static_cast<long long>(r0 + j) * E + e] : 0;
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) {
+          s_all += v[j];
+          if (r0 + j < b) s_below += v[j];
+        }
+      }
     }
+    part_all[t] = s_all;
+    part_below[t] = s_below;
+  }
+  // zero the warp histograms while the partial sums settle
+  for (int i = t; i < kWarps * E; i += kPermuteBlockThreads) wb[i] = 0;
+  __syncthreads();
+
+  // (2) padded exclusive prefix over experts, E <= 1024 = one expert per thread
+  int total = 0, below = 0;
+  if (t < E) {
+    for (int q = 0; q < parts; ++q) {
+      total += part_all[q * E + t];
+      below += part_below[q * E + t];
+    }
+  }
+  const int padded = t < E ? (total + P - 1) / P * P : 0;
+  int incl = padded;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int n = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += n;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_tot[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int n = __shfl_up_sync(0xFFFFFFFFu, w, d);
+      if (lane >= d) w += n;
+    }
+    warp_tot[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int excl = incl - padded + (warp > 0 ? warp_tot[warp - 1] : 0);
+  if (t < E) {
+    base_e[t] = excl + below;
+    if (b == 0) {
+      offsets[t] = excl;
+      if (t == E - 1) offsets[E] = excl + padded;
+    }
+  }
+
+  // (3) per-warp histograms of this block's pairs
+  const long long first = static_cast<long long>(b) * ppb;
+  const long long last = min(R, first + ppb);
+  const long long ppw = ppb / kWarps;
+  const long long wfirst = first + ppw * warp;
+  const long long wlast = min(last, wfirst + ppw);
+  int* hw = wb + warp * E;
+#pragma unroll 1
+  for (long long p0 = wfirst; p0 < wlast; p0 += 32) {
+    const int e = pair_expert(idx, p0 + lane, wlast, E, nullptr);
+    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+    if (e >= 0 && (peers & lanemask_lt()) == 0) hw[e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = t; e < E; e += kPermuteBlockThreads) {
+    int run = base_e[e];
+#pragma unroll 4
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = wb[w * E + e];
+      wb[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+
+  // (4) stable rows
+#pragma unroll 1
+  for (long long p0 = wfirst; p0 < wlast; p0 += 32) {
+    const long long p = p0 + lane;
+    const int e = pair_expert(idx, p, wlast, E, nullptr);
     const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
     int row = -1;
-    if (e >= 0) row = base[e] + __popc(peers & lanemask_lt());
+    if (e >= 0) row = hw[e] + __popc(peers & lanemask_lt());
     __syncwarp();
-    if (e >= 0 && (peers & lanemask_lt()) == 0) base[e] += __popc(peers);
+    if (e >= 0 && (peers & lanemask_lt()) == 0) hw[e] += __popc(peers);
     __syncwarp();
-    if (p < R) {
+    if (p < wlast) {
       row_of_slot[p] = row;
       if (row >= 0) {
         slot_of_row[row] = static_cast<int32_t>(p);
@@ -566,22 +576,35 @@ cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* pr
   const long long R = static_cast<long long>(T) * k;
   const long long R_cap = R + static_cast<long long>(E) * (P - 1);
   const int nb = permute_blocks(R);
-  const size_t hist_smem = sizeof(int) * kWarps * E;
+  const long long ppb = permute_pairs_per_block(R);
+  // scatter: warp histograms, two partial-sum rows, expert bases
+  const size_t scatter_smem = sizeof(int) * (static_cast<size_t>(kWarps) * E +
+                                             2 * kPermuteBlockThreads + E);
+  static bool smem_opt_in[64] = {false};
   cudaError_t err;
-  if (R == 0) {
-    // No routed pairs: only the offsets (all zero) are written.
-    permute_scan_kernel<<<1, 1024, 0, stream>>>(block_hist, 0, E, P, offsets);
-    count_launch();
-    return cudaGetLastError();
+  int dev = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if (!smem_opt_in[dev & 63]) {
+    // up to 32 x 1024 warp counts (128 KB) at E = 1024
+    err = cudaFuncSetAttribute(permute_scatter_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(sizeof(int) * (static_cast<size_t>(kWarps) *
+                                                                   kMaxExperts +
+                                                               2 * kPermuteBlockThreads +
+                                                               kMaxExperts)));
+    if (err != cudaSuccess) return err;
+    smem_opt_in[dev & 63] = true;
   }
-  permute_count_kernel<<<nb, kPermuteBlockThreads, hist_smem, stream>>>(
-      idx, R, E, block_hist, status, slot_of_row, prob_of_row, R_cap);
+  if (nb > 0) {
+    permute_count_kernel<<<nb, kPermuteBlockThreads, sizeof(int) * E, stream>>>(
+        idx, R, E, ppb, block_hist, status, slot_of_row, prob_of_row, R_cap);
+    count_launch();
+  }
+  // with no routed pairs one block writes the offsets (all zero)
+  permute_scatter_kernel<<<nb > 0 ? nb : 1, kPermuteBlockThreads, scatter_smem, stream>>>(
+      idx, prob, R, E, P, ppb, nb, block_hist, offsets, row_of_slot, slot_of_row, prob_of_row);
   count_launch();
-  permute_scan_kernel<<<1, 1024, 0, stream>>>(block_hist, nb, E, P, offsets);
-  count_launch();
-  permute_scatter_kernel<<<nb, kPermuteBlockThreads, hist_smem, stream>>>(
-      idx, prob, R, E, block_hist, offsets, row_of_slot, slot_of_row, prob_of_row);
-  count_launch();
+  if (R == 0) return cudaGetLastError();
   if (Xp != nullptr) {
     err = launch_gather_rows(x, row_of_slot, slot_of_row, offsets, H, k, E,
                              static_cast<int>(R_cap), T, P > 1, nullptr, Xp, status, sm_count,
@@ -695,7 +718,9 @@ cudaError_t launch_bounded_wait_selftest(int32_t* status, uint64_t limit_ns, cud
 namespace gg {
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB per device
+// status header + 128 histogram rows of 512 experts: any batch with E <= 512,
+// T*k <= 1024 * floor(65536 / E) pairs above that (65,536 at E = 1024)
+constexpr size_t kStaticScratchBytes = kWsHeader + (size_t(256) << 10);
 
 static __device__ __align__(256) uint8_t g_permute_scratch[kStaticScratchBytes];
 
@@ -727,7 +752,7 @@ extern "C" gg_status gg_permute_noalloc(const gg_bf16* x, const int32_t* idx, co
   if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(Xp) & 15u))
     return GG_ERR_MISALIGNED;
   // The batch must fit the fixed scratch: status header + one int32 per
-  // (256-pair block, expert).
+  // (histogram block, expert).
   const size_t need = kWsHeader + sizeof(int32_t) * static_cast<size_t>(permute_blocks(
                                                         static_cast<long long>(T) * k)) * E;
   if (need > kStaticScratchBytes) return GG_ERR_WORKSPACE_TOO_SMALL;

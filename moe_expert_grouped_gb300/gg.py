@@ -457,7 +457,7 @@ class MoeLayer:
 def permute_noalloc(x, idx, prob, E: int, P: int = 1, out=None):
     """gg_permute_noalloc: the permute for callers that cannot allocate device
     memory; the library keeps its scratch in a fixed array of its own (batches
-    with gg_workspace_size(T, k, E) > 8 MiB are rejected). Only the outputs
+    with gg_workspace_size(T, k, E) > 256 KiB + 256 bytes are rejected). Only the outputs
     the caller does not pass are allocated here, by torch."""
     T, H = x.shape
     k = idx.shape[1]

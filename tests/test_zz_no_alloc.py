@@ -87,7 +87,8 @@ def test_noalloc_permute_matches_workspace_permute_on_two_calls(gg):
 
 
 def test_noalloc_permute_rejects_batches_beyond_its_scratch(gg):
-    # ceil(70000 * 8 / 256) * 1024 = 2240512 histogram entries > 2097088 that fit in 8 MiB
+    # 70000 * 8 pairs at E = 1024 take 128 histogram rows of 1024 experts
+    # (512 KiB), more than the 256 KiB the fixed scratch holds
     dummy = torch.zeros(64, dtype=torch.float32, device="cuda")
     before = gg.launch_count()
     code = gg.LIB.gg_permute_noalloc(_p(dummy), _p(dummy), _p(dummy), 70000, 64, 8, 1024, 1,
