@@ -527,7 +527,8 @@ gg_status gg_mx_quantize_rows(const gg_bf16* src, int T, int K, int k,
  *  GG_MX_DGRAD_FC2  A = dYq [R_cap][H]: dA = (A W2) [* row_scale], dH1 =
  *                   bf16(act'(H1) applied to dA) quantised to Cq [R_cap][2F]
  *                   + Cs; rowdot (may be NULL) gets per-row partial sums of
- *                   <A W2, act(H1)>, gg_mx_rowdot_blocks(F) of them,
+ *                   <A W2, act(H1)>, gg_mx_rowdot_blocks(F) of them
+ *                   (2 * ceil(F / 128): one per 64 columns),
  *                   gg_mx_rowdot_stride(F) floats apart;
  *  GG_MX_DGRAD_FC1  A = dHq [R_cap][2F]: C = bf16(A W1) [R_cap][H].
  * `activation` is a gg_activation; As, Cs hold n_tiles row-scale tiles. */

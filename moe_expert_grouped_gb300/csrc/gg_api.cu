@@ -614,7 +614,8 @@ int gg_mx_row_tiles(int T, int k, int E, int pad_multiple) {
   return n > 0x7FFFFFFFLL ? 0 : static_cast<int>(n);
 }
 
-int gg_mx_rowdot_blocks(int F) { return F > 0 ? 2 * ((F + mx::kTileN - 1) / mx::kTileN) : 0; }
+// the SwiGLU-backward GEMM runs 128-column tiles: two partials per tile
+int gg_mx_rowdot_blocks(int F) { return F > 0 ? 2 * ((F + 127) / 128) : 0; }
 
 int gg_mx_rowdot_stride(int F) { return (gg_mx_rowdot_blocks(F) + 7) / 8 * 8; }
 

@@ -25,7 +25,10 @@
 //     single accumulator the epilogue first moves its share of it into
 //     registers as BF16 (every GEMM result of the layer is BF16), releases it
 //     to the MMA issuer, and only then does the activation, quantisation and
-//     stores while the next tile's MMAs run;
+//     stores while the next tile's MMAs run. The SwiGLU backward, whose
+//     epilogue bounds its kernel, instead runs 256 x 128 x 32 MMAs into two
+//     128-column accumulators (columns 0-127 and 128-255), so its epilogue
+//     drains half as much per tile while the MMAs fill the other one;
 //   * the B operand is always K-major: the input-gradient GEMMs read weights
 //     that were transposed and quantised along their output dimension once
 //     (gg_mx_prepare_weights);
@@ -60,8 +63,13 @@ constexpr uint32_t A_BYTES = BM * kKStep;               // 16 KB
 constexpr uint32_t B_BYTES = kTileNHalf * kKStep;       // 16 KB
 constexpr uint32_t AB_STAGE = A_BYTES + B_BYTES;        // 32 KB, 1024-aligned
 constexpr uint32_t SF_STAGE = mx::kSfaBytes + mx::kSfbBytes;
-constexpr uint32_t TX_BYTES = AB_STAGE + SF_STAGE;      // per CTA and stage
+constexpr uint32_t TX_BYTES = AB_STAGE + SF_STAGE;      // per CTA and stage (256 columns)
 constexpr uint32_t TMEM_COLS = 512;
+
+__host__ __device__ constexpr bool two_acc_mode(int mode) {
+  return mode == kDgradSwigluBwd || mode == kDgradQgegluBwd;
+}
+__host__ __device__ constexpr int tile_cols(int mode) { return two_acc_mode(mode) ? 128 : 256; }
 
 // TMEM columns of stage s's scale cells: A scales in 4, B scales in 8
 __device__ __forceinline__ uint32_t sf_col(int stage) { return 256u + 16u * stage; }
@@ -71,8 +79,8 @@ __device__ __forceinline__ uint32_t sf_col(int stage) { return 256u + 16u * stag
 struct SmemTail {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
-  uint64_t tfull;
-  uint64_t tempty;
+  uint64_t tfull[2];   // accumulator a holds a finished tile (a = 1: two-accumulator mode)
+  uint64_t tempty[2];  // the epilogue has read accumulator a
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
@@ -97,6 +105,7 @@ struct MxParams {
   int Nout;    // accumulator columns that exist
   int F;       // gated modes
   int NT;      // column tiles per row-tile pair
+  int NTw;     // 256-column tiles of the weight scale layout
   gg_bf16* C;  // plain modes: BF16 [R_cap][ldc]
   long long ldc;
   uint8_t* Cq;     // gated modes: E4M3 output [R_cap][Kq]
@@ -140,6 +149,15 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
   constexpr bool kGatedFwd = MODE == kFwdSwiglu || MODE == kFwdQgeglu;
   constexpr bool kGatedBwd = MODE == kDgradSwigluBwd || MODE == kDgradQgegluBwd;
   constexpr float kAlpha = (MODE == kFwdQgeglu || MODE == kDgradQgegluBwd) ? 1.702f : 1.0f;
+  // The SwiGLU backward, whose epilogue is the slowest stage, uses 128-column
+  // tiles in two accumulators (TMEM columns 0-127 and 128-255): the MMAs of
+  // one tile run while the epilogue works on the other. The other modes use
+  // one 256-column accumulator that the epilogue drains to registers.
+  constexpr bool kTwoAcc = two_acc_mode(MODE);
+  constexpr int kTN = tile_cols(MODE);        // accumulator columns per tile
+  constexpr uint32_t kBRows = kTN / 2;        // weight rows per CTA
+  constexpr uint32_t kTx = A_BYTES + kBRows * kKStep + mx::kSfaBytes + kTN * 4;
+  static_assert(kTwoAcc || kTx == TX_BYTES, "a 256-column stage fills the whole slot");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -205,8 +223,10 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
         mbar_init(smem_u32(&st.full[s]), 1);
         mbar_init(smem_u32(&st.empty[s]), 1);
       }
-      mbar_init(smem_u32(&st.tfull), 1);
-      mbar_init(smem_u32(&st.tempty), kCluster * kEpiWarps);
+      for (int a = 0; a < 2; ++a) {
+        mbar_init(smem_u32(&st.tfull[a]), 1);
+        mbar_init(smem_u32(&st.tempty[a]), kCluster * kEpiWarps);
+      }
       mbar_init(smem_u32(&st.mma_done), 1);
       mbar_fence_init();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -244,8 +264,11 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
         const int mt = mp * kCluster + h;
         const int row0 = __ldg(p.offsets + e) + mt * BM;
         const int sf_row = (st.sf_before[e] + mt) * KB;
-        const int b_row = kGatedFwd ? h * p.F + nt * kTileNHalf : nt * kTileN + h * kTileNHalf;
-        const int sfb_row = (e * NT + nt) * KB;
+        const int b_row = kGatedFwd ? h * p.F + nt * kTileNHalf : nt * kTN + h * kBRows;
+        // weight scales: the 256-column tile holding this tile's columns, and
+        // for a 128-column tile the half (128 words) that covers it
+        const int sfb_row = (e * p.NTw + (kTwoAcc ? nt >> 1 : nt)) * KB;
+        const int sfb_x = kTwoAcc ? (nt & 1) * 128 : 0;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&st.empty[stage]), phase ^ 1u, abort_flag, p.status)) {
             ok = false;
@@ -256,11 +279,11 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
           const uint32_t sb = sa + A_BYTES;
           const uint32_t ssa = sf_base + stage * SF_STAGE;
           const uint32_t ssb = ssa + mx::kSfaBytes;
-          if (leader) mbar_arrive_expect_tx(smem_u32(&st.full[stage]), kCluster * TX_BYTES);
+          if (leader) mbar_arrive_expect_tx(smem_u32(&st.full[stage]), kCluster * kTx);
           tma_load_2d_pair(sa, &mapA, fb, kb * kKStep, row0);
           tma_load_3d_pair(sb, &mapB, fb, kb * kKStep, b_row, e);
           tma_load_2d_pair(ssa, &mapSA, fb, 0, sf_row + kb);
-          tma_load_2d_pair(ssb, &mapSB, fb, 0, sfb_row + kb);
+          tma_load_2d_pair(ssb, &mapSB, fb, sfb_x, sfb_row + kb);
           used |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -283,12 +306,15 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
       // ------------------------------------------------ MMA issuer (even CTA)
       int stage = 0;
       uint32_t phase = 0;
+      int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int tile = cluster_id; tile < total && ok; tile += n_clusters) {
-        // the epilogue has moved the previous tile's accumulator out of TMEM
-        if (!mbar_wait_bounded(smem_u32(&st.tempty), acc_phase ^ 1u, abort_flag, p.status)) break;
+        // the epilogue has read this accumulator's previous tile out of TMEM
+        if (!mbar_wait_bounded(smem_u32(&st.tempty[acc]), acc_phase ^ 1u, abort_flag, p.status))
+          break;
         tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kTN);
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&st.full[stage]), phase, abort_flag, p.status)) {
             ok = false;
@@ -302,14 +328,14 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
           const uint32_t tsa = tmem_base + sf_col(stage);
           const uint32_t tsb = tsa + 4;
           mx::cp_scales_pair(tsa, ssa);
-          mx::cp_scales_pair(tsb, ssb);
-          mx::cp_scales_pair(tsb + 4, ssb + 512);
+          mx::cp_scales_pair(tsb, ssb);  // columns 0-127
+          if (!kTwoAcc) mx::cp_scales_pair(tsb + 4, ssb + 512);  // columns 128-255
 #pragma unroll
           for (int kk = 0; kk < kKStep / 32; ++kk) {
             const uint64_t adesc = make_sdesc(sa + kk * 32, 16, 1024);
             const uint64_t bdesc = make_sdesc(sb + kk * 32, 16, 1024);
-            mx::mma_mx_pair(tmem_base, adesc, bdesc,
-                            mx::make_idesc_mx(kCluster * BM, kTileN, kk, kk), tsa, tsb,
+            mx::mma_mx_pair(d_tmem, adesc, bdesc,
+                            mx::make_idesc_mx(kCluster * BM, kTN, kk, kk), tsa, tsb,
                             (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit_pair_mc(smem_u32(&st.empty[stage]), kClusterMask);
@@ -319,8 +345,9 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
           }
         }
         if (!ok) break;
-        tc_commit_pair_mc(smem_u32(&st.tfull), kClusterMask);
-        acc_phase ^= 1u;
+        tc_commit_pair_mc(smem_u32(&st.tfull[acc]), kClusterMask);
+        if (kTwoAcc) acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
       }
       tc_commit_pair(smem_u32(&st.mma_done));
       (void)mbar_wait_bounded(smem_u32(&st.mma_done), 0, nullptr, p.status);
@@ -334,6 +361,8 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const int r = q * 32 + lane;
+    constexpr int kChunks = kTN / 64;  // 32-column chunks of this warp per tile
+    int eacc = 0;                      // accumulator of the current tile
     uint32_t acc_phase = 0;
     uint4* stg = reinterpret_cast<uint4*>(staging + (warp - 2) * kWarpStagingBytes);
     const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
@@ -359,41 +388,42 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
       // the saved H1 does not depend on the accumulator: fetch the first
       // chunk of the backward before waiting for the MMAs
       const int Fb = p.Nout;
-      const int n0 = nt * kTileN;
-      const int cb0 = half * (kTileN / 2);
+      const int n0 = nt * kTN;
+      const int cb0 = half * (kTN / 2);
       const gg_bf16* hrow0 = kGatedBwd ? p.H1 + grow0 * (2LL * Fb) + n0 : nullptr;
       uint4 graw[4], uraw[4];
       if (kGatedBwd && n0 + cb0 < Fb) {
         load_chunk_raw(graw, hrow0 + cb0, 2LL * Fb, nvalid);
         load_chunk_raw(uraw, hrow0 + Fb + cb0, 2LL * Fb, nvalid);
       }
-      if (!mbar_wait_bounded(smem_u32(&st.tfull), acc_phase, abort_flag, p.status)) break;
+      if (!mbar_wait_bounded(smem_u32(&st.tfull[eacc]), acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
-      uint4 acc[4][4];
+      uint4 acc[kChunks][4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < kChunks; ++j) {
         const int col = kGatedFwd ? (j < 2 ? 64 * half + 32 * j : 128 + 64 * half + 32 * (j - 2))
                                   : cb0 + 32 * j;
         float v[32];
-        tmem_ld32(tq + col, v);
+        tmem_ld32(tq + static_cast<uint32_t>(eacc * kTN + col), v);
         pack_bf16x32(v, scale, acc[j]);
       }
       tc_fence_before();
       __syncwarp();
-      // this warp's share of the accumulator is in registers: the MMAs of the
-      // next tile may overwrite it (relaxed arrive: only the completed TMEM
+      // this warp's share of the accumulator is in registers: the MMAs of a
+      // later tile may overwrite it (relaxed arrive: only the completed TMEM
       // reads need ordering)
-      if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&st.tempty), 0));
-      acc_phase ^= 1u;
+      if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&st.tempty[eacc]), 0));
+      if (kTwoAcc) eacc ^= 1;
+      if (eacc == 0) acc_phase ^= 1u;
 
-      if (MODE == kFwdPlain || MODE == kDgradPlain) {
+      if constexpr (MODE == kFwdPlain || MODE == kDgradPlain) {
         gg_bf16* crow0 = p.C + grow0 * p.ldc + n0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < kChunks; ++j) {
           const int c = cb0 + 32 * j;
           if (n0 + c < p.Nout) store_chunk(stg, acc[j], crow0 + c, p.ldc, nvalid);
         }
-      } else if (kGatedFwd) {
+      } else if constexpr (kGatedFwd) {
         const int F = p.F;
         const bool scaled = p.row_scale != nullptr;
         const float prow = scaled && valid ? p.row_scale[grow] : 1.0f;
@@ -434,13 +464,13 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
         const int F = Fb;
         float prs = 1.0f;
         if (p.row_scale != nullptr && valid) prs = p.row_scale[grow];
-        const int c_end = min(cb0 + kTileN / 2, F - n0);  // multiple of 32
+        const int c_end = min(cb0 + kTN / 2, F - n0);  // multiple of 32
         const int KGq = p.Kq / kKStep;
         uint8_t* drow0 = p.Cq + grow0 * p.Kq + n0;
         float rd[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four independent partial sums
         const bool want_dot = p.rowdot != nullptr;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < kChunks; ++j) {
           const int c = cb0 + 32 * j;
           if (c >= c_end) break;
           uint4 gw[4], uw[4];
@@ -562,7 +592,8 @@ cudaError_t launch_mx_mode(const CUtensorMap (&maps)[4], const MxParams& kp,
 
 int mx_column_tiles(GemmMode mode, int Nout) {
   const bool gated = mode == kFwdSwiglu || mode == kFwdQgeglu;
-  return gated ? (Nout / 2 + kTileNHalf - 1) / kTileNHalf : (Nout + kTileN - 1) / kTileN;
+  const int tn = tile_cols(mode);
+  return gated ? (Nout / 2 + kTileNHalf - 1) / kTileNHalf : (Nout + tn - 1) / tn;
 }
 
 cudaError_t launch_grouped_gemm_mx(const MxGemmArgs& a, const DeviceInfo& dev, cudaStream_t stream,
@@ -571,6 +602,10 @@ cudaError_t launch_grouped_gemm_mx(const MxGemmArgs& a, const DeviceInfo& dev, c
   CUtensorMap maps[4];
   const int KB = a.K / kKStep;
   const int NT = mx_column_tiles(a.mode, a.Nout);
+  // the weight scale tiles are laid out per 256 columns in every mode
+  const bool gated_fwd = a.mode == kFwdSwiglu || a.mode == kFwdQgeglu;
+  const int NTw = gated_fwd ? NT : (a.Nout + kTileN - 1) / kTileN;
+  const bool two_acc = two_acc_mode(a.mode);
   {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.R_cap)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K)};
@@ -586,7 +621,7 @@ cudaError_t launch_grouped_gemm_mx(const MxGemmArgs& a, const DeviceInfo& dev, c
                                 static_cast<cuuint64_t>(a.E)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.K),
                                    static_cast<cuuint64_t>(a.K) * a.Nw};
-    const cuuint32_t box[3] = {kKStep, kTileNHalf, 1};
+    const cuuint32_t box[3] = {kKStep, two_acc ? kTileNHalf / 2u : kTileNHalf, 1};
     if (!encode_map(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, 3, dims, strides, box,
                     CU_TENSOR_MAP_SWIZZLE_128B)) {
       *host_err = GG_ERR_CUDA;
@@ -605,10 +640,11 @@ cudaError_t launch_grouped_gemm_mx(const MxGemmArgs& a, const DeviceInfo& dev, c
     }
   }
   {
-    // B scales: [E * NT * KB] rows of 256 words (1 KB)
-    const cuuint64_t dims[2] = {256, static_cast<cuuint64_t>(a.E) * NT * KB};
+    // B scales: [E * NTw * KB] rows of 256 words (1 KB); a 128-column tile
+    // loads the half that covers it
+    const cuuint64_t dims[2] = {256, static_cast<cuuint64_t>(a.E) * NTw * KB};
     const cuuint64_t strides[1] = {mx::kSfbBytes};
-    const cuuint32_t box[2] = {256, 1};
+    const cuuint32_t box[2] = {two_acc ? 128u : 256u, 1};
     if (!encode_map(&maps[3], CU_TENSOR_MAP_DATA_TYPE_UINT32, a.Bs, 2, dims, strides, box,
                     CU_TENSOR_MAP_SWIZZLE_NONE)) {
       *host_err = GG_ERR_CUDA;
@@ -622,6 +658,7 @@ cudaError_t launch_grouped_gemm_mx(const MxGemmArgs& a, const DeviceInfo& dev, c
   kp.K = a.K;
   kp.Nout = a.Nout;
   kp.NT = NT;
+  kp.NTw = NTw;
   kp.C = a.C;
   kp.Cq = a.Cq;
   kp.Cs = a.Cs;

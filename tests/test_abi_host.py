@@ -198,9 +198,10 @@ def test_mx_layout_and_validation(gg):
             gg.mx_weights_layout(*bad)
     assert L.gg_mx_row_tiles(300, 3, 6, 16) == (300 * 3 + 6 * 15 + 127) // 128 + 6
     assert L.gg_mx_row_tiles(-1, 3, 6, 1) == 0
-    assert L.gg_mx_rowdot_blocks(768) == 6 and L.gg_mx_rowdot_blocks(384) == 4
-    assert L.gg_mx_rowdot_blocks(640) == 6 and L.gg_mx_rowdot_stride(640) == 8
-    assert L.gg_mx_rowdot_stride(2304) == 24 and L.gg_mx_rowdot_blocks(0) == 0
+    # the SwiGLU-backward GEMM runs 128-column tiles, two partials each
+    assert L.gg_mx_rowdot_blocks(768) == 12 and L.gg_mx_rowdot_blocks(384) == 6
+    assert L.gg_mx_rowdot_blocks(640) == 10 and L.gg_mx_rowdot_stride(640) == 16
+    assert L.gg_mx_rowdot_stride(2304) == 40 and L.gg_mx_rowdot_blocks(0) == 0
     # prepare: misaligned buffer, too small
     assert L.gg_mx_prepare_weights(p, p, E, H, F, mis, lay["bytes"], None) == 3
     assert L.gg_mx_prepare_weights(p, p, E, H, F, p, lay["bytes"] - 1, None) == 4
