@@ -57,7 +57,9 @@ __device__ __forceinline__ void unpack_bf16x8(uint4 w, float* v) {
 // probability) and written to the permuted row of every pair of the token,
 // its scale byte into the 128-row tile of the expert whose rows contain it.
 // Lane b0 + l owns block b0 + l; lane j < k first resolves pair j's row, its
-// expert (binary search of the offsets) and its scale position.
+// expert (binary search of the offsets, staged in shared memory with the
+// scale-tile prefix once per block) and its scale position.
+template <bool kScaled>  // prob != nullptr: each pair's copy is scaled by its probability
 __global__ void __launch_bounds__(256)
 quantize_scatter_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ row_of_slot,
                         const float* __restrict__ prob,
@@ -69,6 +71,16 @@ quantize_scatter_kernel(const uint4* __restrict__ src, const int32_t* __restrict
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   const int nblk = K / mx::kBlock;
   const long long tile_bytes = static_cast<long long>(K / mx::kKStep) * mx::kSfaBytes;
+  // offsets and tiles_before in shared memory: the searches below would
+  // otherwise chain seven global loads per token on the way to its stores
+  extern __shared__ int s_tab[];  // [E + 1] offsets, then [E + 1] tiles_before
+  int* s_off = s_tab;
+  int* s_tb = s_tab + E + 1;
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+    s_off[i] = offsets[i];
+    s_tb[i] = tb[i];
+  }
+  __syncthreads();
   for (long long t = warp0; t < T; t += nwarps) {
     int my_row = -1;
     long long my_sf = 0;  // byte of block 0 of this pair's row in S
@@ -78,20 +90,20 @@ quantize_scatter_kernel(const uint4* __restrict__ src, const int32_t* __restrict
       int e = 0, hi = E;  // the expert whose rows contain `row`: offsets[e] <= row
       while (hi - e > 1) {
         const int mid = (e + hi) >> 1;
-        if (offsets[mid] <= row)
+        if (s_off[mid] <= row)
           e = mid;
         else
           hi = mid;
       }
-      const int local = row - offsets[e];
-      const long long tile = static_cast<long long>(tb[e]) + (local >> 7);
-      if (row >= 0 && row < R_cap && local >= 0 && row < offsets[e + 1] && tile < sf_tiles_cap) {
+      const int local = row - s_off[e];
+      const long long tile = static_cast<long long>(s_tb[e]) + (local >> 7);
+      if (row >= 0 && row < R_cap && local >= 0 && row < s_off[e + 1] && tile < sf_tiles_cap) {
         my_row = row;
         my_sf = tile * tile_bytes + mx::sf_byte(local & 127, 0);
       } else if (row != -1) {
         set_status(status, GG_ERR_DEVICE_BAD_ROW);
       }
-      if (prob != nullptr) my_p = prob[t * k + lane];
+      if (kScaled) my_p = prob[t * k + lane];
     }
     const uint4* sp = src + t * (K / 8);
     // two blocks per lane and pass: their eight 16-byte loads are in flight together
@@ -113,13 +125,13 @@ quantize_scatter_kernel(const uint4* __restrict__ src, const int32_t* __restrict
         for (int j = 0; j < 4; ++j) unpack_bf16x8(raw[h][j], v + 8 * j);
         const long long sf_b = (b >> 2) * static_cast<long long>(mx::kSfaBytes) + (b & 3);
         uint32_t q[8];
-        uint32_t code = prob == nullptr ? mx::quantize32(v, q) : 0u;
+        uint32_t code = kScaled ? 0u : mx::quantize32(v, q);
         for (int j = 0; j < k; ++j) {
           const int row = __shfl_sync(0xFFFFFFFFu, my_row, j);
           const long long sfo = __shfl_sync(0xFFFFFFFFu, my_sf, j);
           const float pj = __shfl_sync(0xFFFFFFFFu, my_p, j);
           if (row < 0) continue;
-          if (prob != nullptr) {
+          if (kScaled) {
             float w[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) w[i] = round_bf16(v[i] * pj);
@@ -176,7 +188,7 @@ prepare_weight_kernel(const gg_bf16* __restrict__ W, int N, int K, int transpose
       d[0] = make_uint4(q[0], q[1], q[2], q[3]);
       d[1] = make_uint4(q[4], q[5], q[6], q[7]);
       int nt, col;
-      if (gated_F > 0) {  // FC1: gate rows in columns 0..95 of a tile, up rows in 96..191
+      if (gated_F > 0) {  // FC1: gate rows in columns 0..127 of a tile, up rows in 128..255
         const bool up = n >= gated_F;
         const int j = up ? n - gated_F : n;
         nt = j / mx::kTileNHalf;
@@ -215,9 +227,16 @@ cudaError_t launch_mx_quantize_rows(const gg_bf16* src, int T, int K, int k,
   long long blocks = (static_cast<long long>(T) + 7) / 8;  // 8 warps per block
   const long long cap = static_cast<long long>(sm_count) * 8;
   if (blocks > cap) blocks = cap;
-  quantize_scatter_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
-      reinterpret_cast<const uint4*>(src), row_of_slot, prob, offsets, tiles_before, T, k, K, E,
-      R_cap, sf_tiles_cap, Q, S, status);
+  // E <= kMaxExperts: at most 8 KB of staged tables
+  const size_t tab_bytes = sizeof(int) * 2 * (static_cast<size_t>(E) + 1);
+  if (prob != nullptr)
+    quantize_scatter_kernel<true><<<static_cast<int>(blocks), 256, tab_bytes, stream>>>(
+        reinterpret_cast<const uint4*>(src), row_of_slot, prob, offsets, tiles_before, T, k, K,
+        E, R_cap, sf_tiles_cap, Q, S, status);
+  else
+    quantize_scatter_kernel<false><<<static_cast<int>(blocks), 256, tab_bytes, stream>>>(
+        reinterpret_cast<const uint4*>(src), row_of_slot, prob, offsets, tiles_before, T, k, K,
+        E, R_cap, sf_tiles_cap, Q, S, status);
   count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (has_padding)  // E4M3 zeros on the padding rows (K bytes = K/16 vectors)
