@@ -665,16 +665,15 @@ gg_status gg_mx_prepare_weights(const gg_bf16* W1, const gg_bf16* W2, int E, int
     cudaError_t e = cudaMemsetAsync(base + r[0], 0, r[1], st);
     if (e != cudaSuccess) return GG_ERR_CUDA;
   }
-  cudaError_t e;
   const int tn = mx::kTileN, th = mx::kTileNHalf;
-  if ((e = launch_mx_prepare_weight(W1, E, 2 * F, H, false, F, (F + th - 1) / th, base + L.w1,
-                                    base + L.w1_scales, st)) != cudaSuccess ||
-      (e = launch_mx_prepare_weight(W2, E, H, F, false, 0, (H + tn - 1) / tn, base + L.w2,
-                                    base + L.w2_scales, st)) != cudaSuccess ||
-      (e = launch_mx_prepare_weight(W2, E, F, H, true, 0, (F + tn - 1) / tn, base + L.w2t,
-                                    base + L.w2t_scales, st)) != cudaSuccess ||
-      (e = launch_mx_prepare_weight(W1, E, H, 2 * F, true, 0, (H + tn - 1) / tn, base + L.w1t,
-                                    base + L.w1t_scales, st)) != cudaSuccess)
+  if (launch_mx_prepare_weight(W1, E, 2 * F, H, false, F, (F + th - 1) / th, base + L.w1,
+                               base + L.w1_scales, st) != cudaSuccess ||
+      launch_mx_prepare_weight(W2, E, H, F, false, 0, (H + tn - 1) / tn, base + L.w2,
+                               base + L.w2_scales, st) != cudaSuccess ||
+      launch_mx_prepare_weight(W2, E, F, H, true, 0, (F + tn - 1) / tn, base + L.w2t,
+                               base + L.w2t_scales, st) != cudaSuccess ||
+      launch_mx_prepare_weight(W1, E, H, 2 * F, true, 0, (H + tn - 1) / tn, base + L.w1t,
+                               base + L.w1t_scales, st) != cudaSuccess)
     return GG_ERR_CUDA;
   return GG_OK;
 }
