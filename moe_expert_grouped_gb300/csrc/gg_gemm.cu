@@ -44,6 +44,7 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "gg_epilogue.cuh"
@@ -538,7 +539,8 @@ cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const KPar
                         const DeviceInfo& dev, cudaStream_t stream) {
   // Per device: the shared-memory opt-in and the number of clusters that can
   // be resident at once (the grid is persistent: one cluster per SM pair).
-  static int clusters_for[64] = {0};
+  // (atomic: host threads may launch concurrently; every writer stores the same value)
+  static std::atomic<int> clusters_for[64];
   const int d = dev.device & 63;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -551,7 +553,7 @@ cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const KPar
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (clusters_for[d] == 0) {
+  if (clusters_for[d].load(std::memory_order_relaxed) == 0) {
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, GATHER>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
@@ -561,9 +563,11 @@ cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const KPar
     e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<MODE, GATHER>, &cfg);
     if (e != cudaSuccess) return e;
     if (n <= 0) return cudaErrorInvalidConfiguration;
-    clusters_for[d] = n < dev.sm_count / kCluster ? n : dev.sm_count / kCluster;
+    clusters_for[d].store(n < dev.sm_count / kCluster ? n : dev.sm_count / kCluster,
+                          std::memory_order_relaxed);
   }
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters_for[d] * kCluster), 1, 1);
+  cfg.gridDim = dim3(
+      static_cast<unsigned>(clusters_for[d].load(std::memory_order_relaxed) * kCluster), 1, 1);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE, GATHER>, ma, mb, kp);
   count_launch();
   if (e != cudaSuccess) return e;

@@ -41,6 +41,8 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "gg_epilogue.cuh"
 #include "gg_internal.h"
 #include "gg_mx.cuh"
@@ -555,7 +557,8 @@ bool encode_map(CUtensorMap* map, CUtensorMapDataType type, const void* base, in
 template <int MODE>
 cudaError_t launch_mx_mode(const CUtensorMap (&maps)[4], const MxParams& kp,
                            const DeviceInfo& dev, cudaStream_t stream) {
-  static int clusters_for[64] = {0};
+  // (atomic: host threads may launch concurrently; every writer stores the same value)
+  static std::atomic<int> clusters_for[64];
   const int d = dev.device & 63;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -568,7 +571,7 @@ cudaError_t launch_mx_mode(const CUtensorMap (&maps)[4], const MxParams& kp,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (clusters_for[d] == 0) {
+  if (clusters_for[d].load(std::memory_order_relaxed) == 0) {
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_mx_kernel<MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
@@ -578,9 +581,11 @@ cudaError_t launch_mx_mode(const CUtensorMap (&maps)[4], const MxParams& kp,
     e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_mx_kernel<MODE>, &cfg);
     if (e != cudaSuccess) return e;
     if (n <= 0) return cudaErrorInvalidConfiguration;
-    clusters_for[d] = n < dev.sm_count / kCluster ? n : dev.sm_count / kCluster;
+    clusters_for[d].store(n < dev.sm_count / kCluster ? n : dev.sm_count / kCluster,
+                          std::memory_order_relaxed);
   }
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters_for[d] * kCluster), 1, 1);
+  cfg.gridDim = dim3(
+      static_cast<unsigned>(clusters_for[d].load(std::memory_order_relaxed) * kCluster), 1, 1);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_mx_kernel<MODE>, maps[0], maps[1],
                                            maps[2], maps[3], kp);
   count_launch();

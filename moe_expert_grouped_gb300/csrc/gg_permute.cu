@@ -14,6 +14,8 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "gg_internal.h"
 #include "gg_ptx.cuh"
 
@@ -580,11 +582,11 @@ cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* pr
   // scatter: warp histograms, two partial-sum rows, expert bases
   const size_t scatter_smem = sizeof(int) * (static_cast<size_t>(kWarps) * E +
                                              2 * kPermuteBlockThreads + E);
-  static bool smem_opt_in[64] = {false};
+  static std::atomic<bool> smem_opt_in[64];  // per device; concurrent writers agree
   cudaError_t err;
   int dev = 0;
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-  if (!smem_opt_in[dev & 63]) {
+  if (!smem_opt_in[dev & 63].load(std::memory_order_relaxed)) {
     // up to 32 x 1024 warp counts (128 KB) at E = 1024
     err = cudaFuncSetAttribute(permute_scatter_kernel,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -593,7 +595,7 @@ cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* pr
                                                                2 * kPermuteBlockThreads +
                                                                kMaxExperts)));
     if (err != cudaSuccess) return err;
-    smem_opt_in[dev & 63] = true;
+    smem_opt_in[dev & 63].store(true, std::memory_order_relaxed);
   }
   if (nb > 0) {
     permute_count_kernel<<<nb, kPermuteBlockThreads, sizeof(int) * E, stream>>>(
