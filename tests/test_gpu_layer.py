@@ -2,7 +2,8 @@
 
 Covers the tiny workload, a mid-size ragged case (several row and column
 tiles, ragged tails, padding), the empty batch, run-to-run bitwise equality,
-CUDA-graph replay, expert relabelling and replacing one expert's weights."""
+CUDA-graph replay, expert relabelling, replacing one expert's weights and the
+1024-expert limit."""
 
 import numpy as np
 import pytest
@@ -258,3 +259,29 @@ def test_cuda_graph_replay_of_variants(gg, activation, prob_mode, recompute):
     np.testing.assert_array_equal(torch_to_bits(out), torch_to_bits(out_e))
     np.testing.assert_array_equal(torch_to_bits(dX), torch_to_bits(dX_e))
     np.testing.assert_array_equal(dp.cpu().numpy(), dp_e.cpu().numpy())
+
+
+def test_layer_at_the_expert_limit(gg):
+    """1024 experts, the library's maximum, with tokens on eight of them (the
+    first, middle and last ids): the permute's histogram table and the
+    GEMMs' per-expert tables at their full size, 1016 empty experts."""
+    shape = MoeShape("maxe_e1024_h64_f128_t200_k2", E=1024, H=64, F=128, T=200, k=2,
+                     routing="uniform", x_std=1.0, w_std=0.05)
+    inp = make_inputs(shape, 91)
+    rng = np.random.default_rng(92)
+    live = np.array([0, 1, 2, 511, 512, 700, 1022, 1023])
+    inp.idx[:] = np.stack([rng.choice(live, size=shape.k, replace=False)
+                           for _ in range(shape.T)]).astype(np.int32)
+    d = _dev(inp)
+    layer, out, dX, dprob = _run(gg, shape, d, with_dprob=True)
+    fwd = oracle.moe_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, shape.E, shape.P)
+    bwd = oracle.moe_backward(inp.dOut, fwd, inp.W1, inp.W2)
+    ffw = oracle.moe_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, shape.E, shape.P,
+                             faithful=True)
+    fbw = oracle.moe_backward(inp.dOut, ffw, inp.W1, inp.W2, faithful=True)
+    np.testing.assert_array_equal(layer.view("offsets").cpu().numpy(), fwd["offsets"])
+    np.testing.assert_array_equal(layer.view("row_of_slot").cpu().numpy(), fwd["row_of_slot"])
+    assert_parity(torch_to_f64(out), fwd["out"], "out", faithful=ffw["out"])
+    assert_parity(torch_to_f64(dX), bwd["dX"], "dX", faithful=fbw["dX"])
+    assert_parity(dprob.cpu().numpy().astype(np.float64), bwd["dprob"], "dprob",
+                  faithful=fbw["dprob"])

@@ -379,3 +379,25 @@ def test_layer_fullsize_sampled_parity(gg):
     assert_parity(torch_to_f64(dX)[sel], b["dX"], "dX", faithful=fb["dX"])
     assert_parity(dprob.cpu().numpy().astype(np.float64)[sel], b["dprob"], "dprob",
                   faithful=fb["dprob"])
+
+
+def test_layer_at_the_expert_limit(gg):
+    """The MXFP8 layer with 1024 experts (the maximum), tokens on eight of
+    them: scale-tile prefixes and per-expert tables at full size."""
+    s = MoeShape("mx_maxe_e1024_h128_f128_t160_k2", E=1024, H=128, F=128, T=160, k=2,
+                 routing="uniform", x_std=1.0, w_std=0.05)
+    inp = make_inputs(s, 97)
+    rng = np.random.default_rng(98)
+    live = np.array([0, 1, 2, 511, 512, 700, 1022, 1023])
+    inp.idx[:] = np.stack([rng.choice(live, size=s.k, replace=False)
+                           for _ in range(s.T)]).astype(np.int32)
+    d = _dev(inp)
+    mxw, _ = gg.mx_prepare_weights(d["W1"], d["W2"])
+    _, out, dX, dprob = _layer(gg, s, d, mxw)
+    f = mxo.mx_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, s.E, s.P)
+    ff = mxo.mx_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, s.E, s.P, faithful=True)
+    b, fb = mxo.mx_backward(inp.dOut, f), mxo.mx_backward(inp.dOut, ff)
+    assert_parity(torch_to_f64(out), f["out"], "out", faithful=ff["out"])
+    assert_parity(torch_to_f64(dX), b["dX"], "dX", faithful=fb["dX"])
+    assert_parity(dprob.cpu().numpy().astype(np.float64), b["dprob"], "dprob",
+                  faithful=fb["dprob"])
