@@ -64,6 +64,44 @@ def test_workspace_size_grows_with_pairs(gg):
     assert mid == big == 256 + 4 * 128 * 128
 
 
+def _align256(n):
+    return (n + 255) // 256 * 256
+
+
+def _permute_blocks(R):
+    """The permute's histogram blocks for R pairs: at most 128 blocks, each a
+    whole number of 1024-pair steps (at least one)."""
+    per = -(-R // 128)
+    ppb = max(1024, -(-per // 1024) * 1024)
+    return -(-R // ppb), ppb
+
+
+def test_workspace_size_matches_the_block_model(gg):
+    L = gg.LIB
+    for T in (1, 127, 128, 1000, 4096, 16383, 16384, 30272, 131072, 1 << 20):
+        for k in (1, 2, 8):
+            for E in (1, 8, 128, 1024):
+                R = T * k
+                nb, ppb = _permute_blocks(R)
+                assert 1 <= nb <= 128 and nb * ppb >= R > (nb - 1) * ppb
+                assert L.gg_workspace_size(T, k, E) == 256 + _align256(4 * nb * E), (T, k, E)
+
+
+def test_noalloc_permute_refuses_oversized_batches_on_the_host(gg):
+    # The fixed scratch holds 256 KiB of histogram rows: 128 rows of 512
+    # experts. Larger batches are refused before any device call, so these
+    # never-dereferenced pointers stay untouched.
+    L = gg.LIB
+    p = ctypes.c_void_p(1 << 40)
+    n0 = gg.launch_count()
+    # 65544 pairs at E = 1024: 65 rows of 4 KiB
+    assert L.gg_permute_noalloc(p, p, p, 8193, 64, 8, 1024, 1, p, p, p, p, p, None) == 4
+    assert L.gg_permute_noalloc(p, p, p, 70000, 64, 8, 1024, 1, p, p, p, p, p, None) == 4
+    assert L.gg_permute_noalloc(p, p, p, 4096, 64, 8, 1025, 1, p, p, p, p, p, None) == 2
+    assert L.gg_permute_noalloc(p, p, p, 4096, 64, 33, 8, 1, p, p, p, p, p, None) == 1
+    assert gg.launch_count() == n0
+
+
 def test_buffers_bind_carves_disjoint_aligned_pieces(gg):
     T, H, F, k, E, P = 300, 320, 384, 2, 8, 16
     n = gg.LIB.gg_moe_buffers_size(T, H, F, k, E, P)
