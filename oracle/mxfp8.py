@@ -219,12 +219,18 @@ def mx_backward(dOut, fwd: dict) -> dict:
     W1d, dX = the plain sum of the k rows (probability-weighted in
     ``pre_fc1`` mode). The quantisers pass gradients straight through.
 
-    dprob is the gradient where the probability meets the activation: the row
-    sum of dA0 * act(H1) (``combine`` and ``activation``; in exact arithmetic
-    it equals <dOut_t, Yp>, but here FC2's forward and backward see
-    differently quantised operands), <x_t, dXp> in ``pre_fc1`` mode. With a
-    ``faithful`` forward, dXp, dX and the activation in the dprob sum are
-    rounded to BF16 as well."""
+    dprob is taken where the probability enters the forward:
+      * ``combine``: out_t = sum_j p_tj * Yp[row(t, j)] is linear in p and no
+        quantiser lies between p and out, so dprob_tj = <dOut_t, Yp[row(t, j)]>
+        exactly, with the forward's Yp (the probability gradient at the
+        combine, "[Main] Support paged stash with device-initiated
+        GroupedLinear", "What does this PR do?": the probability boundary);
+      * ``activation``: A = bf16(p * act(H1)) is quantised for FC2, whose
+        quantiser passes the gradient straight through, so dprob is the row
+        sum of dA0 * act(H1), dA0 being the gradient that reaches A;
+      * ``pre_fc1``: <x_t, dXp[row]>.
+    With a ``faithful`` forward (whose Yp is already BF16), dXp, dX and the
+    activation in the ``activation``-mode sum are rounded to BF16 as well."""
     dOut = _mo._as_f64(dOut)
     k = fwd["k"]
     T = dOut.shape[0]
@@ -239,7 +245,10 @@ def mx_backward(dOut, fwd: dict) -> dict:
     dA0 = _mo.round_to_bf16(_mo.grouped_linear_t(mx(dYp), W["W2d"], offsets))
     dprob_rows = np.zeros(R_cap)
     rnd = _mo.round_to_bf16 if fwd.get("faithful") else (lambda v: v)
-    if mode in ("combine", "activation"):
+    if mode == "combine":
+        dA = dA0 * pr[:, None]
+        dprob_rows[valid] = np.sum(dYp[valid] * fwd["Yp"][valid], axis=1)
+    elif mode == "activation":
         dA = dA0 * pr[:, None]
         act = rnd(_mo.glu(fwd["H1"], fwd["activation"]))
         dprob_rows[valid] = np.sum(dA0[valid] * act[valid], axis=1)

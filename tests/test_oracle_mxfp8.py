@@ -12,7 +12,10 @@
   activation gradient must equal the BF16 oracle's (BF16-faithful) values,
   and the later tensors must stay within the format's error;
 * the weight quantisation axes, with blocks that lose their small entries
-  along one axis but not along the other."""
+  along one axis but not along the other;
+* the combine-mode probability gradient against a central finite difference
+  of the forward (exact: out is linear in the probabilities there) and
+  against the closed form of identity weights."""
 
 import numpy as np
 import pytest
@@ -184,3 +187,71 @@ def test_weight_quantisation_axes():
 def test_quantize_rejects_ragged_axis():
     with pytest.raises(ValueError):
         mxo.quantize(np.zeros((2, 48)))
+
+
+def test_combine_mode_prob_grad_is_the_derivative_of_the_forward():
+    # In combine mode out_t = sum_j p_tj * Yp[row(t, j)]: out is linear in
+    # every p_tj and no quantiser sits between p and out, so the central
+    # difference of L = <dOut, out> through mx_forward is the exact
+    # derivative, whatever the step. mx_backward's dprob must equal it.
+    from moe_synth import MoeShape, make_inputs
+
+    s = MoeShape("fd_e4_h64_f64_t16_k2", E=4, H=64, F=64, T=16, k=2, x_std=1.0, w_std=0.1)
+    inp = make_inputs(s, 71)
+    W = mxo.mx_weights(inp.W1, inp.W2)
+    f = mxo.mx_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, s.E, weights=W)
+    dprob = mxo.mx_backward(inp.dOut, f)["dprob"]
+    dOut = oracle.bf16_bits_to_f64(inp.dOut)
+    prob = inp.prob.astype(np.float64)
+    h = 0.25
+    for t, j in [(0, 0), (3, 1), (9, 0), (15, 1)]:
+        loss = []
+        for sgn in (1.0, -1.0):
+            p = prob.copy()
+            p[t, j] += sgn * h
+            out = mxo.mx_forward(inp.x, inp.idx, p, inp.W1, inp.W2, s.E, weights=W)["out"]
+            loss.append(float(np.sum(dOut * out)))
+        fd = (loss[0] - loss[1]) / (2 * h)
+        assert abs(fd - dprob[t, j]) <= 1e-10 * max(1.0, abs(fd)), (t, j, fd, dprob[t, j])
+
+    # The pin has teeth: the route through the input-gradient GEMM (quantised
+    # dOut against the output-dimension quantisation of W2, dotted with the
+    # activation) is a different number once the operands are quantised.
+    dYp = np.zeros_like(f["Yp"])
+    valid = f["slot_of_row"] >= 0
+    dYp[valid] = dOut[f["slot_of_row"][valid] // s.k]
+    dA0 = oracle.round_to_bf16(oracle.grouped_linear_t(mxo.mx(dYp), W["W2d"], f["offsets"]))
+    other_rows = np.sum(dA0 * oracle.glu(f["H1"], "swiglu"), axis=1)
+    other = np.zeros(s.T * s.k)
+    other[f["slot_of_row"][valid]] = other_rows[valid]
+    rel = np.linalg.norm(other - dprob.reshape(-1)) / np.linalg.norm(dprob)
+    assert rel > 1e-3, rel
+
+
+def test_combine_mode_prob_grad_closed_form_on_identity_weights():
+    # Gate and up blocks [I; 0] and W2 = [I 0] are exact in MXFP8, and so are
+    # inputs x on the representable grid. Then H1 = [x, x], A = bf16(x^2
+    # sigmoid(x)) and Yp = mx(A), so in closed form
+    # dprob_tj = <dOut_t, mx(bf16(x_t^2 sigmoid(x_t)))> for every pair.
+    rng = np.random.default_rng(12)
+    E, H, F, T, k = 2, 64, 64, 8, 2
+    W1 = np.zeros((E, 2 * F, H))
+    W1[:, :H, :] = np.eye(H)
+    W1[:, F:F + H, :] = np.eye(H)
+    W2 = np.zeros((E, H, F))
+    W2[:, :, :H] = np.eye(H)
+    x = _representable(rng, (T, H), 1.0)
+    dOut = _representable(rng, (T, H), 0.5)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    prob = rng.uniform(0.1, 1.0, (T, k))
+    f = mxo.mx_forward(x, idx, prob, W1, W2, E)
+    b = mxo.mx_backward(dOut, f)
+    sor = f["slot_of_row"]
+    valid = sor >= 0
+    np.testing.assert_array_equal(f["H1"][valid][:, :H], x[sor[valid] // k])
+    np.testing.assert_array_equal(f["H1"][valid][:, F:], x[sor[valid] // k])
+    y = mxo.mx(oracle.round_to_bf16(x * x / (1.0 + np.exp(-x))))
+    for t in range(T):
+        for j in range(k):
+            np.testing.assert_allclose(b["dprob"][t, j], np.dot(dOut[t], y[t]), rtol=1e-13,
+                                       atol=1e-13)
