@@ -290,7 +290,10 @@ def moe_backward(dOut, fwd: dict, W1, W2, faithful: bool = False):
     dprob[t, j] = <dOut_t, FC2(act(H1))[row]> for "combine" / "activation"
     (``prob_grad``: the FC2 output is linear in p) and <x_t, dXp[row]> for
     "pre_fc1" (Xp[row] = p * x_t). With ``faithful`` the values are rounded to
-    BF16 where the GPU path stores BF16 (dH, dXp, dX); dprob stays fp32.
+    BF16 where the GPU path stores BF16 (dH, dXp, dX); dprob stays fp32 and
+    pairs dOut with the FC2 output of the BF16 activation before that output
+    is rounded (the path forms it from FC2's fp32 accumulation against the
+    stored activation and never reads a rounded Yp for it).
     """
     rnd = round_to_bf16 if faithful else (lambda v: v)
     dO = _as_f64(dOut)
@@ -315,8 +318,12 @@ def moe_backward(dOut, fwd: dict, W1, W2, faithful: bool = False):
     else:
         dX = rnd(combine(dXp, fwd["row_of_slot"], None, T, k))
         # dprob = <dOut_t, FC2 output of the unweighted activation>
-        Yu = fwd["Yp"] if mode == "combine" else grouped_linear(glu(fwd["H1"], act_name), W2,
-                                                                offsets)
+        if mode == "combine" and not faithful:
+            Yu = fwd["Yp"]
+        elif mode == "combine":
+            Yu = grouped_linear(fwd["A"], W2, offsets)
+        else:
+            Yu = grouped_linear(rnd(glu(fwd["H1"], act_name)), W2, offsets)
         dprob = prob_grad(dO, Yu, fwd["row_of_slot"], T, k)
     return dict(dYp=dYp, dH=dH, dXp=dXp, dX=dX, dprob=dprob)
 

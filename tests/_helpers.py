@@ -7,15 +7,28 @@ import numpy as np
 # Parity bar for floating-point results of the expert path against the exact
 # fp64 oracle:
 #   * relative L2 error over the tensor <= 5e-3;
-#   * per element |err| <= 1e-2 * |ref| + floor.
+#   * per element |err_i| <= 1e-2 * |ref_i| + floor_i.
 # The stated floor is 1e-3 for tensors of order-one scale; for a tensor whose
 # magnitude is far below 1 (the 0.02-scale tiny workload produces outputs near
-# 1e-6) it is 1e-3 * max|ref| so that the test is not vacuous. The floor is
-# raised to twice the largest error of the BF16-faithful oracle (exact
-# arithmetic, BF16 rounding exactly where the path stores BF16) when that is
-# larger: the k-way weighted combine cancels terms whose rounding errors scale
-# with the terms, not with their sum, so no BF16-storage implementation can
-# meet 1e-3 on order-one outputs; the faithful oracle measures that floor.
+# 1e-6) it is 1e-3 * max|ref| so that the test is not vacuous. floor_i is
+# raised, token by token, to twice the largest error of the BF16-faithful
+# oracle (exact arithmetic, BF16 rounding exactly where the path stores BF16)
+# within element i's own row (the token's H outputs, or its k probability
+# gradients) where that is larger: the k-way weighted combine cancels terms
+# whose rounding errors scale with the terms, not with their sum, so no
+# BF16-storage implementation can meet 1e-3 on such an element. The floor is
+# per row rather than per element because the kernels accumulate in fp32 and
+# round once, so single BF16 roundings upstream land on the other side of a
+# tie than the exact oracle's: an element's faithful error is one sample of
+# that noise and can sit near zero where the kernel's does not (a CPU model
+# of the kernels' arithmetic fails a strictly per-element 2x floor on 1-37
+# elements per tensor, and a per-row one on none). A cancelling element thus
+# lifts only its own token's bound; every other token keeps its own.
+# The MXFP8 layer's value checks take the floor over the whole tensor
+# (scope="tensor"): its kernels decide E4M3 codes on their own BF16 values,
+# and where those sit one BF16 step from the oracle's at a rounding boundary
+# the code moves by one E4M3 step (12.5 % of the element), which changes
+# whole downstream rows by an amount no per-row faithful error predicts.
 REL_L2 = 5e-3
 REL_ELEM = 1e-2
 ABS_FLOOR = 1e-3
@@ -38,7 +51,7 @@ def torch_to_bits(t) -> np.ndarray:
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def parity_report(got: np.ndarray, ref: np.ndarray, faithful=None):
+def parity_report(got: np.ndarray, ref: np.ndarray, faithful=None, scope: str = "row") -> dict:
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     err = np.abs(got - ref)
@@ -46,25 +59,42 @@ def parity_report(got: np.ndarray, ref: np.ndarray, faithful=None):
     rel = np.linalg.norm(got - ref) / nref if nref > 0 else np.linalg.norm(got - ref)
     scale = float(np.max(np.abs(ref))) if ref.size else 0.0
     floor = ABS_FLOOR if scale >= 1e-1 else ABS_FLOOR * scale
+    stated = REL_ELEM * np.abs(ref) + floor
+    bound = stated
     f_err = 0.0
     if faithful is not None and ref.size:
-        f_err = float(np.max(np.abs(np.asarray(faithful, np.float64) - ref)))
-        floor = max(floor, FAITHFUL_FACTOR * f_err)
-    bound = REL_ELEM * np.abs(ref) + floor
-    n_bad = int(np.sum(err > bound))
-    return rel, n_bad, float(err.max()) if err.size else 0.0, floor, f_err
+        f_err_i = np.abs(np.asarray(faithful, np.float64) - ref)
+        f_err = float(f_err_i.max())
+        if scope == "tensor":
+            row_max = np.full(ref.shape, f_err)
+        elif scope == "row":
+            rows = f_err_i.reshape(f_err_i.shape[0], -1) if f_err_i.ndim >= 2 else f_err_i[:, None]
+            row_max = np.broadcast_to(rows.max(axis=1, keepdims=True),
+                                      rows.shape).reshape(ref.shape)
+        else:
+            raise ValueError(scope)
+        bound = REL_ELEM * np.abs(ref) + np.maximum(floor, FAITHFUL_FACTOR * row_max)
+    return dict(rel=float(rel), n_bad=int(np.sum(err > bound)),
+                max_err=float(err.max()) if err.size else 0.0, floor=floor, f_err=f_err,
+                # elements over the stated bar that pass on their raised floor
+                n_raised=int(np.sum((err > stated) & (err <= bound))), size=int(ref.size))
 
 
-def assert_parity(got, ref, what: str = "", faithful=None) -> None:
+def assert_parity(got, ref, what: str = "", faithful=None, scope: str = "row") -> dict:
     """Parity of `got` with the exact oracle `ref`; `faithful` is the oracle's
-    BF16-faithful value of the same tensor (sets the per-element floor)."""
+    BF16-faithful value of the same tensor (sets each row's floor; rows along
+    the first axis).
+    Returns the report (rel-L2, largest error, elements that needed their
+    raised floor)."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     if ref.size == 0:
-        return
-    rel, n_bad, max_err, floor, f_err = parity_report(got, ref, faithful)
-    assert rel <= REL_L2, f"{what}: rel-L2 {rel:.3e} > {REL_L2}"
-    assert n_bad == 0, (f"{what}: {n_bad} elements over 1e-2*|ref|+{floor:.2e} "
-                        f"(max err {max_err:.3e}, faithful-oracle max err {f_err:.3e})")
+        return dict(rel=0.0, n_bad=0, max_err=0.0, floor=0.0, f_err=0.0, n_raised=0, size=0)
+    r = parity_report(got, ref, faithful, scope)
+    assert r["rel"] <= REL_L2, f"{what}: rel-L2 {r['rel']:.3e} > {REL_L2}"
+    assert r["n_bad"] == 0, (f"{what}: {r['n_bad']} elements over 1e-2*|ref| + "
+                             f"max({r['floor']:.2e}, 2*max over the {scope} |faithful - ref|) (max err "
+                             f"{r['max_err']:.3e}, faithful-oracle max err {r['f_err']:.3e})")
+    return r
