@@ -154,6 +154,7 @@ class ClockSampler:
         self.window = (t0, t1)
 
     def stop(self):
+        """Stop sampling; the summary of the window given to mark()."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -162,8 +163,15 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=2)
-        inside = [s for t, s in self.samples if self.window and self.window[0] <= t <= self.window[1]]
-        used = inside if inside else [s for _, s in self.samples]
+        return self.summary(self.window)
+
+    def summary(self, window):
+        """Median SM clock, max clock and active throttle reasons of the
+        samples inside `window` (all samples when none fell inside it)."""
+        if self.proc is None:
+            return None
+        inside = [s for t, s in list(self.samples) if window and window[0] <= t <= window[1]]
+        used = inside if inside else [s for _, s in list(self.samples)]
 
         def num(x):
             try:
@@ -226,7 +234,6 @@ def run_gg(args, shape, peaks):
     torch.cuda.set_device(dev)
 
     import moe_expert_grouped_gb300.gg as gg
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
 
     inp = make_inputs(shape, 1000 * args.config + 17 * rank)
 
@@ -307,7 +314,8 @@ def run_gg(args, shape, peaks):
         mark(6)
         gg.mx_grouped_gemm(gg.GG_MX_DGRAD_FC2, b["dYq"], b["dYs"], mxw, b["offsets"], E, rc, H, F,
                            ws, activation=act, Cq=b["dHq"], Cs=b["dHs"], H1=b["H1"],
-                           row_scale=None if pre else por, rowdot=None if pre else b["rowdot"])
+                           row_scale=None if pre else por,
+                           rowdot=b["rowdot"] if mode == gg.GG_PROB_ACTIVATION else None)
         mark(7)
         gg.mx_grouped_gemm(gg.GG_MX_DGRAD_FC1, b["dHq"], b["dHs"], mxw, b["offsets"], E, rc, H, F,
                            ws, activation=act, C=b["dXp"])
@@ -315,6 +323,9 @@ def run_gg(args, shape, peaks):
         if pre:
             gg.unpermute_combine(b["dXp"], b["row_of_slot"], prob, T, k, ws, out=dX, dprob=dprob,
                                  dot_src=x)
+        elif mode == gg.GG_PROB_COMBINE:
+            gg.unpermute_combine_dot(b["dXp"], b["row_of_slot"], None, T, k, dOut, b["Yp"], ws,
+                                     out=dX, dprob=dprob)
         else:
             gg.unpermute_combine(b["dXp"], b["row_of_slot"], None, T, k, ws, out=dX,
                                  rowdot=b["rowdot"], dprob=dprob,
@@ -473,7 +484,34 @@ def run_gg(args, shape, peaks):
     h2d = x.numel() * 2 + dOut.numel() * 2 + idx.numel() * 4 + prob.numel() * 4
     d2h = out.numel() * 2 + dX.numel() * 2 + dprob.numel() * 4
 
+    # ---- sustained: at least --sustained-s seconds of back-to-back steps
+    # after the timed region and the end-to-end run, with their own clock
+    # record (a seconds-long training step runs the layer under the power
+    # cap, not as a burst)
+    sus = None
+    if args.sustained_s > 0:
+        n_sus = max(args.steps, int(args.sustained_s / max(local_s / args.steps, 1e-6)) + 1)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        sw0 = time.time()
+        s0.record(stream)
+        for _ in range(n_sus):
+            step()
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        sw1 = time.time()
+        sus_s, _ = aggregate(s0.elapsed_time(s1) / 1e3, 0.0, dev if world > 1 else None)
+        if gg.read_status(ws) != 0:
+            raise RuntimeError("device status after the sustained run")
+        sus = {"steps": n_sus, "seconds": round(sus_s, 3), "window": (sw0, sw1)}
+
+
     clocks = sampler.stop() if sampler is not None else None
+    if sus is not None:
+        sus["clocks"] = sampler.summary(sus.pop("window")) if sampler is not None else None
+        sus.pop("window", None)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -492,7 +530,10 @@ def run_gg(args, shape, peaks):
                 "permute_dout": (T + R) * H * 2 + 4 * rc,
                 "quant_x": quant, "quant_dout": quant,
                 "combine": (R + T) * H * 2 + 8 * R,
-                "combine_dx": (R + T) * H * 2 + 4 * R}[op]
+                # MXFP8 with the probability at the combine: the dX combine also
+                # reads the kept Yp rows and dOut for the probability gradient
+                "combine_dx": (R + T) * H * 2 + 4 * R + (
+                    (R + T) * H * 2 if mx and mode == gg.GG_PROB_COMBINE else 0)}[op]
 
     avg = {op: float(np.mean(v)) for op, v in per_op.items()}
     total_ms = sum(avg.values())
@@ -543,6 +584,21 @@ def run_gg(args, shape, peaks):
                          f"tokens/s {n_tok / times[0]:.1f}"}
 
     value = tot_flop / tot_s / 1e12
+
+    def per_ghz(v, clk):
+        mhz = (clk or {}).get("sm_mhz")
+        return round(v / world / (mhz / 1e3), 2) if mhz else None
+
+    sustained = None
+    if sus is not None:
+        sus_value = flop_step * sus["steps"] * world / sus["seconds"] / 1e12
+        sustained = {"value": round(sus_value, 2), "unit": "TFLOP/s",
+                     "steps": sus["steps"], "seconds": sus["seconds"],
+                     "ms_per_step": round(sus["seconds"] / sus["steps"] * 1e3, 4),
+                     "tokens_per_s": round(T * sus["steps"] * world / sus["seconds"], 1),
+                     "pct_vs_2250_tflops": round(sus_value / world / 2250.0, 4),
+                     "tflops_per_ghz": per_ghz(sus_value, sus["clocks"]),
+                     "clocks": sus["clocks"]}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -566,6 +622,8 @@ def run_gg(args, shape, peaks):
                 "tokens_per_s": round(T * args.steps * world / e2e_s, 1)},
         "gpu_launches": int(launches), "clocks": clocks, "cpu_baseline": cpu,
         "launches_per_step": int(launches) // max(1, args.steps),
+        "tflops_per_ghz": per_ghz(value, clocks),
+        "sustained": sustained,
     }
     if mx:
         line["pct_fp8_peak"] = {"vs_4500_tflops": round(value / world / 4500.0, 4),
@@ -640,6 +698,9 @@ def main(argv=None):
     ap.add_argument("--cpu-tokens", type=int, default=8192)
     ap.add_argument("--ref-tokens", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sustained-s", type=float, default=2.0,
+                    help="seconds of back-to-back steps timed after the timed region "
+                         "(0: none)")
     ap.add_argument("--activation", choices=["swiglu", "qgeglu"], default="swiglu")
     ap.add_argument("--recompute-h1", action="store_true",
                     help="do not keep FC1's output for the backward; recompute it there")

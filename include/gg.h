@@ -170,9 +170,14 @@ gg_status gg_permute(const gg_bf16* x, const int32_t* idx, const float* prob,
  *     E <= 512; for larger E, T*k <= 1024 * floor(65536 / E) pairs (65,536
  *     at E = 1024). Larger batches are rejected with
  *     GG_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *   - Xp may be NULL (row maps, offsets and per-row probabilities only), and
+ *     x is then not read, exactly as for gg_permute.
  *   - Set-up: the first call on a device (made with that device current)
- *     looks up the array's device address once; make that first call before
- *     any stream capture.
+ *     looks up the array's device address; make that first call before any
+ *     stream capture. Only a successful lookup is kept: if it fails the call
+ *     returns GG_ERR_CUDA and the next call on that device tries again.
+ *   - Device ordinals of 64 and above are refused with
+ *     GG_ERR_UNSUPPORTED_DEVICE.
  *   - Every call on a device shares the one array and it keeps the previous
  *     call's contents; each call clears the status word itself. Calls whose
  *     work overlaps on the GPU (different streams without ordering between
@@ -352,6 +357,30 @@ gg_status gg_unpermute_combine(const gg_bf16* Yp, const int32_t* row_of_slot,
                                gg_bf16* out, const float* rowdot, int n_rowdot,
                                const gg_bf16* dot_src, float* dprob, void* ws,
                                size_t ws_bytes, gg_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gg_unpermute_combine_dot — the combine of gg_unpermute_combine together
+ * with a routing-probability gradient that is a dot product of a token row
+ * with a second permuted tensor ([P4] "What does this PR do?": the
+ * probability boundary; with the probability applied at the combine,
+ * out_t = sum_j p_tj * Yp[row(t, j)], so d out / d p_tj = Yp[row(t, j)]):
+ *   out[t]       = bf16( sum_{j<k} [prob[t][j] *] Sp[row_of_slot[t*k+j]] )
+ *                  fp32 in slot order, one rounding (prob NULL: plain sum);
+ *   dprob[t*k+j] = <dot_src[t], dot_rows[row_of_slot[t*k+j]]>
+ *                  fp32, fixed order; 0 for a pair without a row.
+ * The MXFP8 layer's backward calls it with Sp = dXp (out = dX), dot_src =
+ * dOut and dot_rows = the forward's Yp, so that its probability gradient is
+ * formed from its definition rather than from the quantised input-gradient
+ * GEMM. Sp, dot_rows [R_cap][H]; dot_src, out [T][H] BF16 (16-byte
+ * aligned); dprob [T][k] fp32; k <= 32. All pointers are required when
+ * T > 0 (GG_ERR_INVALID_ARG). A row outside [-1, R_cap) sets
+ * GG_ERR_DEVICE_BAD_ROW in the status word of `ws` and is skipped.
+ * ------------------------------------------------------------------------- */
+gg_status gg_unpermute_combine_dot(const gg_bf16* Sp, const int32_t* row_of_slot,
+                                   const float* prob, int T, int k, int H, int R_cap,
+                                   gg_bf16* out, const gg_bf16* dot_src,
+                                   const gg_bf16* dot_rows, float* dprob, void* ws,
+                                   size_t ws_bytes, gg_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Whole expert layer. The caller owns one device buffer that holds every
@@ -579,9 +608,14 @@ gg_status gg_mx_buffers_bind(void* base, size_t bytes, int T, int H, int F, int 
  * rows -> input gradient of FC2 + activation backward + quantise -> input
  * gradient of FC1 -> combine into dX[T][H], dprob[T][k] when not NULL).
  * Options as gg_moe_mlp_fwd_ex except recompute_h1, which must be 0
- * (GG_ERR_INVALID_ARG). dprob is the gradient where the probability meets
- * the activation: sum over the row of (A W2) * act(H1) for the combine and
- * weighted-activation modes, <x_t, dXp[row]> for the pre-FC1 mode. */
+ * (GG_ERR_INVALID_ARG). dprob is the gradient where the probability enters
+ * the forward: <dOut_t, Yp[row]> on the forward's kept Yp when it is applied
+ * at the combine (formed by gg_unpermute_combine_dot; no quantiser lies
+ * between p and out), the row sum of dA0 * act(H1) with the weighted
+ * activation (dA0 the input gradient of FC2, before the probability scale;
+ * the probability sits inside FC2's quantised operand), <x_t, dXp[row]> for
+ * the pre-FC1 mode. The forward's Yp must therefore still hold its values
+ * when the combine-mode backward runs with dprob. */
 gg_status gg_moe_mlp_fwd_mx(const gg_bf16* x, const int32_t* idx, const float* prob,
                             const void* mxw, int T, int H, int F, int k, int E,
                             int pad_multiple, const gg_moe_options* opt, gg_bf16* out,

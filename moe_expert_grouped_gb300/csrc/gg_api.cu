@@ -30,7 +30,7 @@ struct DevCache {
   DeviceInfo info;
   gg_status status = GG_ERR_CUDA;
 };
-DevCache g_dev[64];
+DevCache g_dev[kMaxDevices];
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -63,7 +63,8 @@ void count_launch(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
 
 gg_status current_device(DeviceInfo* out) {
   int d = -1;
-  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return GG_ERR_CUDA;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0) return GG_ERR_CUDA;
+  if (d >= kMaxDevices) return GG_ERR_UNSUPPORTED_DEVICE;
   DevCache& c = g_dev[d];
   std::call_once(c.once, [&c, d] {
     DeviceInfo i;
@@ -159,7 +160,7 @@ gg_status gg_permute(const gg_bf16* x, const int32_t* idx, const float* prob, in
   int32_t* block_hist = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + kWsHeader);
   return from_cuda(launch_permute(x, idx, prob, T, H, k, E, pad_multiple, Xp, offsets,
                                   row_of_slot, slot_of_row, prob_of_row, status_ptr(ws),
-                                  block_hist, dev.sm_count,
+                                  block_hist, dev,
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -407,8 +408,28 @@ gg_status gg_unpermute_combine(const gg_bf16* Yp, const int32_t* row_of_slot, co
   DeviceInfo dev;
   if ((s = device_ok(&dev)) != GG_OK) return s;
   return from_cuda(launch_combine(Yp, row_of_slot, prob, T, k, H, R_cap, out, rowdot,
-                                  rowdot != nullptr ? n_rowdot : 0, dot_src, dprob,
+                                  rowdot != nullptr ? n_rowdot : 0, dot_src, nullptr, dprob,
                                   status_ptr(ws), dev.sm_count,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gg_status gg_unpermute_combine_dot(const gg_bf16* Sp, const int32_t* row_of_slot,
+                                   const float* prob, int T, int k, int H, int R_cap,
+                                   gg_bf16* out, const gg_bf16* dot_src, const gg_bf16* dot_rows,
+                                   float* dprob, void* ws, size_t ws_bytes, gg_stream_t stream) {
+  if (T < 0 || k <= 0 || k > 32 || H <= 0 || R_cap < 0) return GG_ERR_INVALID_ARG;
+  if (H % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
+  if (T > 0 && (Sp == nullptr || row_of_slot == nullptr || out == nullptr ||
+                dot_src == nullptr || dot_rows == nullptr || dprob == nullptr))
+    return GG_ERR_INVALID_ARG;
+  if (!aligned16(Sp) || !aligned16(out) || !aligned16(dot_src) || !aligned16(dot_rows))
+    return GG_ERR_MISALIGNED;
+  gg_status s = check_ws(ws, ws_bytes, kWsHeader);
+  if (s != GG_OK) return s;
+  DeviceInfo dev;
+  if ((s = device_ok(&dev)) != GG_OK) return s;
+  return from_cuda(launch_combine(Sp, row_of_slot, prob, T, k, H, R_cap, out, nullptr, 0,
+                                  dot_src, dot_rows, dprob, status_ptr(ws), dev.sm_count,
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -913,7 +934,13 @@ gg_status gg_moe_mlp_bwd_mx(const gg_bf16* dOut, const gg_bf16* x, const float* 
   if (dOut == nullptr || dX == nullptr) return GG_ERR_INVALID_ARG;
   const bool pre = mode == GG_PROB_PRE_FC1;
   if (pre && (prob == nullptr || (dprob != nullptr && x == nullptr))) return GG_ERR_INVALID_ARG;
-  float* rowdot = dprob != nullptr && !pre ? buf->rowdot : nullptr;
+  // Where the probability meets the forward decides where its gradient is
+  // formed: at the combine (out = sum_j p * Yp, no quantiser in between) it
+  // is <dOut_t, Yp[row]> on the kept Yp, formed in the dX combine; with the
+  // weighted activation the probability sits inside FC2's quantised operand
+  // and its gradient is the row sum of dA0 * act(H1), accumulated by the
+  // SwiGLU-backward epilogue.
+  float* rowdot = dprob != nullptr && mode == GG_PROB_ACTIVATION ? buf->rowdot : nullptr;
   s = gg_mx_quantize_rows(dOut, T, H, k, buf->row_of_slot, buf->slot_of_row, buf->offsets,
                           nullptr, E, pad_multiple, buf->n_tiles, buf->tiles_before, buf->dYq,
                           buf->dYs, buf->ws, buf->ws_bytes, stream);
@@ -931,6 +958,9 @@ gg_status gg_moe_mlp_bwd_mx(const gg_bf16* dOut, const gg_bf16* x, const float* 
     return gg_unpermute_combine(buf->dXp, buf->row_of_slot, prob, T, k, H, R_cap, dX, nullptr, 0,
                                 dprob != nullptr ? x : nullptr, dprob, buf->ws, buf->ws_bytes,
                                 stream);
+  if (dprob != nullptr && mode == GG_PROB_COMBINE)
+    return gg_unpermute_combine_dot(buf->dXp, buf->row_of_slot, nullptr, T, k, H, R_cap, dX,
+                                    dOut, buf->Yp, dprob, buf->ws, buf->ws_bytes, stream);
   return gg_unpermute_combine(buf->dXp, buf->row_of_slot, nullptr, T, k, H, R_cap, dX, rowdot,
                               gg_mx_rowdot_blocks(F), nullptr, dprob, buf->ws, buf->ws_bytes,
                               stream);

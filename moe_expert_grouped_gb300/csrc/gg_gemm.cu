@@ -540,8 +540,9 @@ cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const KPar
   // Per device: the shared-memory opt-in and the number of clusters that can
   // be resident at once (the grid is persistent: one cluster per SM pair).
   // (atomic: host threads may launch concurrently; every writer stores the same value)
-  static std::atomic<int> clusters_for[64];
-  const int d = dev.device & 63;
+  static std::atomic<int> clusters_for[kMaxDevices];
+  if (dev.device < 0 || dev.device >= kMaxDevices) return cudaErrorInvalidDevice;
+  const int d = dev.device;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;

@@ -558,8 +558,9 @@ template <int MODE>
 cudaError_t launch_mx_mode(const CUtensorMap (&maps)[4], const MxParams& kp,
                            const DeviceInfo& dev, cudaStream_t stream) {
   // (atomic: host threads may launch concurrently; every writer stores the same value)
-  static std::atomic<int> clusters_for[64];
-  const int d = dev.device & 63;
+  static std::atomic<int> clusters_for[kMaxDevices];
+  if (dev.device < 0 || dev.device >= kMaxDevices) return cudaErrorInvalidDevice;
+  const int d = dev.device;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;

@@ -16,6 +16,10 @@ constexpr size_t kWsHeader = 256;
 constexpr int kPermuteBlockThreads = 1024;
 constexpr int kPermuteMaxBlocks = 128;  // histogram rows every scatter block reads
 constexpr int kMaxExperts = 1024;
+// Per-device host-side caches (launch attributes, device properties, the
+// no-workspace permute's scratch address) are indexed by the device ordinal;
+// ordinals at or above this are refused with GG_ERR_UNSUPPORTED_DEVICE.
+constexpr int kMaxDevices = 64;
 
 // The permute splits its R pairs into at most kPermuteMaxBlocks blocks of a
 // whole number of 1024-pair steps (one 32-pair step per warp).
@@ -48,7 +52,7 @@ gg_status current_device(DeviceInfo* out);
 cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* prob, int T, int H,
                            int k, int E, int P, gg_bf16* Xp, int32_t* offsets,
                            int32_t* row_of_slot, int32_t* slot_of_row, float* prob_of_row,
-                           int32_t* status, int32_t* block_hist, int sm_count,
+                           int32_t* status, int32_t* block_hist, const DeviceInfo& dev,
                            cudaStream_t stream);
 
 // dst[row_of_slot[t*k+j]] = src[t] (times prob[t*k+j] when prob is not
@@ -61,11 +65,12 @@ cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* row_of_slot,
 
 // dprob (nullable): dprob[t*k+j] = sum_b rowdot[row_of_slot[t*k+j]][b], rows of
 // rowdot (n_rowdot + 7) / 8 * 8 floats apart.
-// With dot_src (and dprob): dprob[t*k+j] = <dot_src[t], Yp[row_of_slot[t*k+j]]>.
+// With dot_src (and dprob): dprob[t*k+j] = <dot_src[t], D[row_of_slot[t*k+j]]>
+// with D = dot_rows, or Yp when dot_rows is null.
 cudaError_t launch_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const float* prob,
                            int T, int k, int H, int R_cap, gg_bf16* out, const float* rowdot,
-                           int n_rowdot, const gg_bf16* dot_src, float* dprob, int32_t* status,
-                           int sm_count, cudaStream_t stream);
+                           int n_rowdot, const gg_bf16* dot_src, const gg_bf16* dot_rows,
+                           float* dprob, int32_t* status, int sm_count, cudaStream_t stream);
 
 // Zeroes row r (vec_per_row 16-byte vectors of dst) for every r < offsets[E]
 // whose slot_of_row is -1 (the padding rows).

@@ -474,17 +474,24 @@ combine_dprob_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ r
   }
 }
 
-// combine_kernel plus the pre-FC1 probability gradient: with Xp[row] =
-// prob * dot_src[t], dprob[t*k+j] = <dot_src[t], Yp[row(t, j)]>. Each lane
-// keeps one partial dot per slot over its columns (x chunk loaded once per
-// pass), reduced across the warp in a fixed butterfly order at the end;
-// kMaxK (8 or 32) bounds k and the partials held in registers.
-template <int kMaxK>
+// combine_kernel plus a probability gradient that is a dot product of the
+// token's row of dot_src with one permuted row per slot:
+//   kDotRows false: dprob[t*k+j] = <dot_src[t], Yp[row(t, j)]> (the pre-FC1
+//     mode: Xp[row] = prob * dot_src[t], dot_src = x, Yp = dXp);
+//   kDotRows true:  dprob[t*k+j] = <dot_src[t], dot_rows[row(t, j)]> (the
+//     probability at the combine: dot_src = dOut, dot_rows = the forward's
+//     Yp, while the sum runs over Yp = dXp).
+// Each lane keeps one partial dot per slot over its columns (the token's
+// chunk loaded once per pass), reduced across the warp in a fixed butterfly
+// order at the end; kMaxK (8 or 32) bounds k and the partials held in
+// registers.
+template <int kMaxK, bool kDotRows>
 __global__ void __launch_bounds__(256)
 combine_dot_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row_of_slot,
                    const float* __restrict__ prob, int T, int k, int vec_per_row, int R_cap,
                    uint4* __restrict__ out, const uint4* __restrict__ dot_src,
-                   float* __restrict__ dprob, int32_t* status) {
+                   const uint4* __restrict__ dot_rows, float* __restrict__ dprob,
+                   int32_t* status) {
   const int lane = threadIdx.x & 31;
   const int warp0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -522,13 +529,24 @@ combine_dot_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row
         const uint4 va = oka ? __ldcs(rp + ca) : make_uint4(0u, 0u, 0u, 0u);
         const uint4 vb = okb ? __ldcs(rp + cb) : make_uint4(0u, 0u, 0u, 0u);
         const uint32_t yw[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+        uint32_t dw[8];
+        if (kDotRows) {
+          const uint4* dp = dot_rows + static_cast<long long>(row) * vec_per_row;
+          const uint4 da = oka ? __ldcs(dp + ca) : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 db = okb ? __ldcs(dp + cb) : make_uint4(0u, 0u, 0u, 0u);
+          dw[0] = da.x; dw[1] = da.y; dw[2] = da.z; dw[3] = da.w;
+          dw[4] = db.x; dw[5] = db.y; dw[6] = db.z; dw[7] = db.w;
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) dw[q] = yw[q];
+        }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const float ylo = bf16_lo(yw[q]), yhi = bf16_hi(yw[q]);
           acc[q >> 2][2 * (q & 3)] = __fmaf_rn(pj, ylo, acc[q >> 2][2 * (q & 3)]);
           acc[q >> 2][2 * (q & 3) + 1] = __fmaf_rn(pj, yhi, acc[q >> 2][2 * (q & 3) + 1]);
-          dotp[j] = __fmaf_rn(bf16_lo(xw[q]), ylo, dotp[j]);
-          dotp[j] = __fmaf_rn(bf16_hi(xw[q]), yhi, dotp[j]);
+          dotp[j] = __fmaf_rn(bf16_lo(xw[q]), bf16_lo(dw[q]), dotp[j]);
+          dotp[j] = __fmaf_rn(bf16_hi(xw[q]), bf16_hi(dw[q]), dotp[j]);
         }
       }
       uint4* op = out + static_cast<long long>(t) * vec_per_row;
@@ -573,7 +591,7 @@ __global__ void bounded_wait_selftest_kernel(int32_t* status, uint64_t limit_ns)
 cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* prob, int T, int H,
                            int k, int E, int P, gg_bf16* Xp, int32_t* offsets,
                            int32_t* row_of_slot, int32_t* slot_of_row, float* prob_of_row,
-                           int32_t* status, int32_t* block_hist, int sm_count,
+                           int32_t* status, int32_t* block_hist, const DeviceInfo& dev,
                            cudaStream_t stream) {
   const long long R = static_cast<long long>(T) * k;
   const long long R_cap = R + static_cast<long long>(E) * (P - 1);
@@ -582,11 +600,10 @@ cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* pr
   // scatter: warp histograms, two partial-sum rows, expert bases
   const size_t scatter_smem = sizeof(int) * (static_cast<size_t>(kWarps) * E +
                                              2 * kPermuteBlockThreads + E);
-  static std::atomic<bool> smem_opt_in[64];  // per device; concurrent writers agree
+  static std::atomic<bool> smem_opt_in[kMaxDevices];  // per device; concurrent writers agree
+  if (dev.device < 0 || dev.device >= kMaxDevices) return cudaErrorInvalidDevice;
   cudaError_t err;
-  int dev = 0;
-  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-  if (!smem_opt_in[dev & 63].load(std::memory_order_relaxed)) {
+  if (!smem_opt_in[dev.device].load(std::memory_order_relaxed)) {
     // up to 32 x 1024 warp counts (128 KB) at E = 1024
     err = cudaFuncSetAttribute(permute_scatter_kernel,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -595,7 +612,7 @@ cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* pr
                                                                2 * kPermuteBlockThreads +
                                                                kMaxExperts)));
     if (err != cudaSuccess) return err;
-    smem_opt_in[dev & 63].store(true, std::memory_order_relaxed);
+    smem_opt_in[dev.device].store(true, std::memory_order_relaxed);
   }
   if (nb > 0) {
     permute_count_kernel<<<nb, kPermuteBlockThreads, sizeof(int) * E, stream>>>(
@@ -609,8 +626,8 @@ cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* pr
   if (R == 0) return cudaGetLastError();
   if (Xp != nullptr) {
     err = launch_gather_rows(x, row_of_slot, slot_of_row, offsets, H, k, E,
-                             static_cast<int>(R_cap), T, P > 1, nullptr, Xp, status, sm_count,
-                             stream);
+                             static_cast<int>(R_cap), T, P > 1, nullptr, Xp, status,
+                             dev.sm_count, stream);
     if (err != cudaSuccess) return err;
   }
   return cudaGetLastError();
@@ -662,24 +679,41 @@ cudaError_t launch_zero_pad_rows(const int32_t* slot_of_row, const int32_t* offs
   return cudaGetLastError();
 }
 
+template <int kMaxK, bool kDotRows>
+void launch_combine_dot(int blocks, const gg_bf16* Yp, const int32_t* row_of_slot,
+                        const float* prob, int T, int k, int vec, int R_cap, gg_bf16* out,
+                        const gg_bf16* dot_src, const gg_bf16* dot_rows, float* dprob,
+                        int32_t* status, cudaStream_t stream) {
+  combine_dot_kernel<kMaxK, kDotRows><<<blocks, 256, 0, stream>>>(
+      reinterpret_cast<const uint4*>(Yp), row_of_slot, prob, T, k, vec, R_cap,
+      reinterpret_cast<uint4*>(out), reinterpret_cast<const uint4*>(dot_src),
+      reinterpret_cast<const uint4*>(dot_rows), dprob, status);
+}
+
 cudaError_t launch_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const float* prob,
                            int T, int k, int H, int R_cap, gg_bf16* out, const float* rowdot,
-                           int n_rowdot, const gg_bf16* dot_src, float* dprob, int32_t* status,
-                           int sm_count, cudaStream_t stream) {
+                           int n_rowdot, const gg_bf16* dot_src, const gg_bf16* dot_rows,
+                           float* dprob, int32_t* status, int sm_count, cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
   const int vec = H / 8;
   long long blocks = (static_cast<long long>(T) + 7) / 8;
   const long long cap = static_cast<long long>(sm_count) * 8;  // as for the row copy
   if (blocks > cap) blocks = cap;
-  if (dprob != nullptr && dot_src != nullptr && k <= 8)
-    combine_dot_kernel<8><<<static_cast<int>(blocks), 256, 0, stream>>>(
-        reinterpret_cast<const uint4*>(Yp), row_of_slot, prob, T, k, vec, R_cap,
-        reinterpret_cast<uint4*>(out), reinterpret_cast<const uint4*>(dot_src), dprob, status);
-  else if (dprob != nullptr && dot_src != nullptr)
-    combine_dot_kernel<32><<<static_cast<int>(blocks), 256, 0, stream>>>(
-        reinterpret_cast<const uint4*>(Yp), row_of_slot, prob, T, k, vec, R_cap,
-        reinterpret_cast<uint4*>(out), reinterpret_cast<const uint4*>(dot_src), dprob, status);
-  else if (dprob != nullptr)
+  const int nb = static_cast<int>(blocks);
+  if (dprob != nullptr && dot_src != nullptr) {
+    if (dot_rows != nullptr && k <= 8)
+      launch_combine_dot<8, true>(nb, Yp, row_of_slot, prob, T, k, vec, R_cap, out, dot_src,
+                                  dot_rows, dprob, status, stream);
+    else if (dot_rows != nullptr)
+      launch_combine_dot<32, true>(nb, Yp, row_of_slot, prob, T, k, vec, R_cap, out, dot_src,
+                                   dot_rows, dprob, status, stream);
+    else if (k <= 8)
+      launch_combine_dot<8, false>(nb, Yp, row_of_slot, prob, T, k, vec, R_cap, out, dot_src,
+                                   nullptr, dprob, status, stream);
+    else
+      launch_combine_dot<32, false>(nb, Yp, row_of_slot, prob, T, k, vec, R_cap, out, dot_src,
+                                    nullptr, dprob, status, stream);
+  } else if (dprob != nullptr)
     combine_dprob_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
         reinterpret_cast<const uint4*>(Yp), row_of_slot, prob, T, k, vec, R_cap,
         reinterpret_cast<uint4*>(out), rowdot, n_rowdot, dprob, status);
@@ -726,12 +760,25 @@ constexpr size_t kStaticScratchBytes = kWsHeader + (size_t(256) << 10);
 
 static __device__ __align__(256) uint8_t g_permute_scratch[kStaticScratchBytes];
 
+// Device address of g_permute_scratch per device ordinal, looked up on the
+// first call made with that device current. Only a successful lookup is
+// kept: a failed one (for instance a sticky error left by earlier work, or a
+// first call made during a stream capture) is retried by the next call.
 struct StaticScratchSlot {
-  std::once_flag once;
+  std::mutex mu;
   void* ptr = nullptr;
-  cudaError_t err = cudaErrorUnknown;
 };
-StaticScratchSlot g_static_scratch[64];
+StaticScratchSlot g_static_scratch[kMaxDevices];
+
+void* static_scratch_address(int device) {
+  StaticScratchSlot& slot = g_static_scratch[device];
+  std::lock_guard<std::mutex> lock(slot.mu);
+  if (slot.ptr == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_permute_scratch) == cudaSuccess) slot.ptr = p;
+  }
+  return slot.ptr;
+}
 
 }  // namespace
 }  // namespace gg
@@ -747,10 +794,13 @@ extern "C" gg_status gg_permute_noalloc(const gg_bf16* x, const int32_t* idx, co
   if (E > kMaxExperts || H % 64 != 0) return GG_ERR_UNSUPPORTED_SHAPE;
   const long long R_cap = static_cast<long long>(T) * k + static_cast<long long>(E) * (pad_multiple - 1);
   if (R_cap > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
+  // the same argument rules as gg_permute: Xp NULL asks for the row maps and
+  // offsets only, and x is needed only when Xp is given
   if (offsets == nullptr) return GG_ERR_INVALID_ARG;
-  if (T > 0 && (x == nullptr || idx == nullptr || prob == nullptr || Xp == nullptr ||
-                row_of_slot == nullptr || slot_of_row == nullptr || prob_of_row == nullptr))
+  if (T > 0 && (idx == nullptr || prob == nullptr || row_of_slot == nullptr ||
+                slot_of_row == nullptr || prob_of_row == nullptr))
     return GG_ERR_INVALID_ARG;
+  if (T > 0 && Xp != nullptr && x == nullptr) return GG_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(Xp) & 15u))
     return GG_ERR_MISALIGNED;
   // The batch must fit the fixed scratch: status header + one int32 per
@@ -761,22 +811,18 @@ extern "C" gg_status gg_permute_noalloc(const gg_bf16* x, const int32_t* idx, co
   DeviceInfo dev;
   gg_status s = current_device(&dev);
   if (s != GG_OK) return s;
+  if (dev.device < 0 || dev.device >= kMaxDevices) return GG_ERR_UNSUPPORTED_DEVICE;
   if (dev.cc_major != 10 || dev.cc_minor != 3) return GG_ERR_UNSUPPORTED_DEVICE;
-  StaticScratchSlot& slot = g_static_scratch[dev.device];
-  std::call_once(slot.once, [&slot] {
-    void* p = nullptr;
-    slot.err = cudaGetSymbolAddress(&p, g_permute_scratch);
-    if (slot.err == cudaSuccess) slot.ptr = p;
-  });
-  if (slot.err != cudaSuccess || slot.ptr == nullptr) return GG_ERR_CUDA;
+  void* scratch = static_scratch_address(dev.device);
+  if (scratch == nullptr) return GG_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  int32_t* status = static_cast<int32_t*>(slot.ptr);
+  int32_t* status = static_cast<int32_t*>(scratch);
   // The array keeps the previous call's bytes: the status word must start at
   // zero; the histograms are fully rewritten before they are read.
   if (cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) return GG_ERR_CUDA;
-  int32_t* block_hist = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(slot.ptr) + kWsHeader);
+  int32_t* block_hist = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(scratch) + kWsHeader);
   return launch_permute(x, idx, prob, T, H, k, E, pad_multiple, Xp, offsets, row_of_slot,
-                        slot_of_row, prob_of_row, status, block_hist, dev.sm_count, st) ==
+                        slot_of_row, prob_of_row, status, block_hist, dev, st) ==
                  cudaSuccess
              ? GG_OK
              : GG_ERR_CUDA;

@@ -66,10 +66,17 @@ class GgOps:
 
     def local_forward(self, rows, local_eid, W1, W2) -> torch.Tensor:
         n = rows.shape[0]
-        self._layer = self.gg.MoeLayer(n, self.H, self.F, 1, self.El, 1, device=rows.device,
-                                       activation=self.activation)
+        # One device buffer serves every forward; it is replaced (by one for
+        # the next power of two rows, at least 1024) only when a batch does
+        # not fit it.
+        L = self._layer
+        if L is None or L.device != rows.device or not L.fits(n):
+            cap = 1 << max(10, (max(n, 1) - 1).bit_length())
+            L = self.gg.MoeLayer(cap, self.H, self.F, 1, self.El, 1, device=rows.device,
+                                 activation=self.activation)
+            self._layer = L
         ones = torch.ones((n, 1), dtype=torch.float32, device=rows.device)
-        return self._layer.forward(rows, local_eid.view(n, 1), ones, W1, W2)
+        return L.forward(rows, local_eid.view(n, 1), ones, W1, W2)
 
     def local_backward(self, d_rows, W1, W2):
         dX, dprob = self._layer.backward(d_rows, W1, W2, dprob=True)

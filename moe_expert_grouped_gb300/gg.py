@@ -49,6 +49,7 @@ SIGNATURES = [
     ("gg_rowdot_blocks", _I, [_I]),
     ("gg_rowdot_stride", _I, [_I]),
     ("gg_unpermute_combine", _I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _Z, _P]),
+    ("gg_unpermute_combine_dot", _I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
     ("gg_moe_buffers_size", _Z, [_I, _I, _I, _I, _I, _I]),
     ("gg_moe_buffers_bind", _I, [_P, _Z, _I, _I, _I, _I, _I, _I, _P]),
     ("gg_moe_mlp_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
@@ -363,6 +364,22 @@ def unpermute_combine(Yp, row_of_slot, prob, T: int, k: int, ws, out=None, rowdo
     return out if dprob is None else (out, dprob)
 
 
+def unpermute_combine_dot(Sp, row_of_slot, prob, T: int, k: int, dot_src, dot_rows, ws,
+                          out=None, dprob=None):
+    """gg_unpermute_combine_dot: out [T, H] = the (probability-weighted when prob
+    is given) sum of each token's k rows of Sp, and dprob [T, k] = <dot_src[t],
+    dot_rows[row of (t, j)]>; returns (out, dprob)."""
+    R_cap, H = Sp.shape
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=Sp.device) if out is None else out
+    if dprob is None:
+        dprob = torch.empty((T, k), dtype=torch.float32, device=Sp.device)
+    _check(LIB.gg_unpermute_combine_dot(_ptr(Sp), _ptr(row_of_slot), _ptr(prob), T, k, H, R_cap,
+                                        _ptr(out), _ptr(dot_src), _ptr(dot_rows), _ptr(dprob),
+                                        _ptr(ws), ws.numel(), _stream(Sp.device)),
+           "gg_unpermute_combine_dot")
+    return out, dprob
+
+
 def selftest_bounded_wait(ws, limit_ns: int) -> None:
     _check(LIB.gg_selftest_bounded_wait(_ptr(ws), ws.numel(), int(limit_ns), _stream(ws.device)),
            "gg_selftest_bounded_wait")
@@ -388,6 +405,7 @@ class MoeLayer:
         self.T, self.H, self.F, self.k, self.E, self.P = T, H, F, k, E, P
         self.opt = GGOptions(activation, prob_mode, 1 if recompute_h1 else 0)
         self._saved = None  # the forward's (x, prob): the pre-FC1 backward needs them
+        self._rows = None   # the forward's batch size
         self.R_cap = r_cap(T, k, E, P)
         self.device = torch.device(device)
         n = int(LIB.gg_moe_buffers_size(T, H, F, k, E, P))
@@ -416,8 +434,19 @@ class MoeLayer:
         off = getattr(self.buf, name) - self.storage.data_ptr()
         return self.storage[off:off + count * esize].view(dtype).view(shape)
 
+    def fits(self, T: int) -> bool:
+        """Whether a batch of T tokens can run on this layer's buffer (T at
+        most the bound size and its permute workspace no larger)."""
+        return 0 <= T <= self.T and int(LIB.gg_workspace_size(T, self.k, self.E)) <= int(
+            self.buf.ws_bytes)
+
     def forward(self, x, idx, prob, W1, W2, out=None):
-        T, H, F, k, E = self.T, self.H, self.F, self.k, self.E
+        """out [T, H] for x [T, H]: T is the bound size or, for a buffer reused
+        across batches, any smaller batch the buffer fits."""
+        T = int(x.shape[0])
+        H, F, k, E = self.H, self.F, self.k, self.E
+        if not self.fits(T):
+            raise GGError(4, f"{T} tokens do not fit a layer bound for {self.T}")
         _need(x, torch.bfloat16, (T, H), "x")
         _need(idx, torch.int32, (T, k), "idx")
         _need(prob, torch.float32, (T, k), "prob")
@@ -429,12 +458,15 @@ class MoeLayer:
                                      ctypes.byref(self.buf), _stream(self.device)),
                "gg_moe_mlp_fwd_ex")
         self._saved = (x, prob)
+        self._rows = T
         return out
 
     def backward(self, dOut, W1, W2, dX=None, dprob=None):
         """dX [T, H]; with dprob ([T, k] fp32 tensor, or True to allocate one) also
-        the routing-probability gradient, returned as (dX, dprob)."""
-        T, H, F, k, E = self.T, self.H, self.F, self.k, self.E
+        the routing-probability gradient, returned as (dX, dprob). T is the
+        last forward's batch."""
+        T = self._rows if self._rows is not None else self.T
+        H, F, k, E = self.H, self.F, self.k, self.E
         _need(dOut, torch.bfloat16, (T, H), "dOut")
         dX = torch.empty((T, H), dtype=torch.bfloat16, device=self.device) if dX is None else dX
         want = dprob is not None and dprob is not False

@@ -184,6 +184,16 @@ def test_validation_rejects_before_launch(gg):
     # rowdot must be 32-byte aligned
     mis32 = ctypes.c_void_p((1 << 40) + 16)
     assert C(p, p, p, 4, 2, 64, 128, p, mis32, 2, None, p, ws, 1024, None) == 3
+    # gg_unpermute_combine_dot: every pointer required, k <= 32, H % 64, alignment
+    D = L.gg_unpermute_combine_dot
+    assert D(p, p, None, 4, 33, 64, 128, p, p, p, p, ws, 1024, None) == 1
+    assert D(p, p, None, 4, 2, 72, 128, p, p, p, p, ws, 1024, None) == 2
+    assert D(p, p, None, 4, 2, 64, 128, p, None, p, p, ws, 1024, None) == 1
+    assert D(p, p, None, 4, 2, 64, 128, p, p, None, p, ws, 1024, None) == 1
+    assert D(p, p, None, 4, 2, 64, 128, p, p, p, None, ws, 1024, None) == 1
+    assert D(p, p, None, 4, 2, 64, 128, p, mis, p, p, ws, 1024, None) == 3
+    assert D(p, p, None, 4, 2, 64, 128, p, p, mis, p, ws, 1024, None) == 3
+    assert D(p, p, None, 4, 2, 64, 128, p, p, p, p, ws, 16, None) == 4
     # gg_swiglu / gg_glu: F % 64, only the gated forward epilogues
     assert L.gg_swiglu(p, p, 4, 128, 96, p, None) == 2
     assert L.gg_glu(p, p, 4, 128, 96, 1, None, p, None) == 2

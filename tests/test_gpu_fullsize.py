@@ -1,10 +1,12 @@
 """GPU parity at the workloads' full sizes, in the launch configuration the
 benchmark times (the whole layer through gg_moe_mlp_fwd / gg_moe_mlp_bwd).
 
-Index outputs are compared in full against the oracle's row map; values are
-compared on a seeded sample of tokens, each with all k of its rows: the expert
-MLP treats rows independently, so the oracle run on the sampled sub-batch gives
-exactly those tokens' outputs and input gradients. The skewed, padded workload
+Index outputs are compared in full against the oracle's row map. On the
+benchmarked balanced 128-expert layer every element of out, dX and dprob is
+compared with the oracle; on the larger workloads values are compared on a
+seeded sample of tokens, each with all k of its rows: the expert MLP treats
+rows independently, so the oracle run on the sampled sub-batch gives exactly
+those tokens' outputs and input gradients. The skewed, padded workload
 also checks batch invariance: two load draws that route identical token rows to
 one expert produce bitwise identical rows of that expert."""
 
@@ -63,13 +65,48 @@ def _check_sample(inp, shape, out, grads, n_tokens, seed, **variant):
                              faithful=True, **variant)
     fbw = oracle.moe_backward(inp.dOut[sel], ffw, inp.W1, inp.W2, faithful=True)
     rows = torch.from_numpy(sel).cuda()
-    assert_parity(torch_to_f64(out[rows]), fwd["out"], "out (sampled)", faithful=ffw["out"])
-    assert_parity(torch_to_f64(dX[rows]), bwd["dX"], "dX (sampled)", faithful=fbw["dX"])
-    assert_parity(dprob[rows].cpu().numpy().astype(np.float64), bwd["dprob"], "dprob (sampled)",
-                  faithful=fbw["dprob"])
+    _report(shape.name + " sampled", {
+        "out": assert_parity(torch_to_f64(out[rows]), fwd["out"], "out (sampled)",
+                             faithful=ffw["out"]),
+        "dX": assert_parity(torch_to_f64(dX[rows]), bwd["dX"], "dX (sampled)",
+                            faithful=fbw["dX"]),
+        "dprob": assert_parity(dprob[rows].cpu().numpy().astype(np.float64), bwd["dprob"],
+                               "dprob (sampled)", faithful=fbw["dprob"])})
 
 
-@pytest.mark.parametrize("cfg", [2, 4])
+def _report(what, reports):
+    # one line per tensor: how close it is and how many elements needed the
+    # floor raised to their BF16-faithful error
+    for name, r in reports.items():
+        print(f"[parity] {what} {name}: rel-L2 {r['rel']:.3e}, max err {r['max_err']:.3e}, "
+              f"raised-floor elements {r['n_raised']} / {r['size']}")
+
+
+def test_balanced_layer_full_tensor_parity(gg):
+    # the benchmarked workload with the benchmark's inputs: every token's
+    # out, dX and dprob against the exact and the BF16-faithful oracle
+    shape = CONFIGS[2]
+    inp = make_inputs(shape, 2000)
+    layer, out, (dX, dprob) = _run(gg, shape, inp)
+    _check_indices(layer, inp, shape)
+    got = dict(out=torch_to_f64(out), dX=torch_to_f64(dX),
+               dprob=dprob.cpu().numpy().astype(np.float64))
+    del layer, out, dX, dprob
+    torch.cuda.empty_cache()
+    ref, faithful = {}, {}
+    for dst, flag in ((ref, False), (faithful, True)):
+        fwd = oracle.moe_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, shape.E, shape.P,
+                                 faithful=flag)
+        dst["out"] = fwd["out"]
+        bwd = oracle.moe_backward(inp.dOut, fwd, inp.W1, inp.W2, faithful=flag)
+        dst["dX"], dst["dprob"] = bwd["dX"], bwd["dprob"]
+        del fwd, bwd
+    _report(shape.name + " full", {
+        name: assert_parity(got[name], ref[name], name + " (all tokens)",
+                            faithful=faithful[name]) for name in ("out", "dX", "dprob")})
+
+
+@pytest.mark.parametrize("cfg", [4])
 def test_fullsize_sampled_parity(gg, cfg):
     shape = CONFIGS[cfg]
     inp = make_inputs(shape, 1000 * cfg)

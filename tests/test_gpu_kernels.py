@@ -484,3 +484,32 @@ def test_combine_dot_probability_gradient(gg, k):
     got = dprob.cpu().numpy().astype(np.float64)
     assert np.all(got.reshape(-1)[rows < 0] == 0)
     assert_parity(got, ref, "dprob (dot)")
+
+
+@pytest.mark.parametrize("k", [8, 12])
+@pytest.mark.parametrize("weighted", [False, True])
+def test_combine_dot_with_separate_dot_rows(gg, k, weighted):
+    # gg_unpermute_combine_dot: the sum runs over Sp while each pair's dot
+    # takes its permuted row from a second tensor, dprob[t, j] =
+    # <dot_src[t], D[row(t, j)]>; the sum is bitwise the plain combine of Sp
+    T, H, R_cap = 300, 320, 4000
+    rng = np.random.default_rng(47 + k)
+    rows = rng.permutation(R_cap)[:T * k].astype(np.int32)
+    rows[[5, 77, 301]] = -1
+    Sp = normal_bf16(rng, (R_cap, H), 1.0)
+    D = normal_bf16(rng, (R_cap, H), 1.0)
+    xs = normal_bf16(rng, (T, H), 1.0)
+    prob = rng.uniform(0, 1, (T, k)).astype(np.float32)
+    ws = gg.workspace(T, k, 1, "cuda")
+    d_rows = torch.from_numpy(rows).cuda()
+    d_prob = torch.from_numpy(prob).cuda() if weighted else None
+    out, dprob = gg.unpermute_combine_dot(bits_to_torch(Sp), d_rows, d_prob, T, k,
+                                          bits_to_torch(xs), bits_to_torch(D), ws)
+    out2 = gg.unpermute_combine(bits_to_torch(Sp), d_rows, d_prob, T, k, ws)
+    torch.cuda.synchronize()
+    assert gg.read_status(ws) == 0
+    np.testing.assert_array_equal(torch_to_bits(out), torch_to_bits(out2))
+    ref = oracle.prob_grad(oracle.bf16_bits_to_f64(xs), oracle.bf16_bits_to_f64(D), rows, T, k)
+    got = dprob.cpu().numpy().astype(np.float64)
+    assert np.all(got.reshape(-1)[rows < 0] == 0)
+    assert_parity(got, ref, "dprob (dot rows)")

@@ -245,14 +245,14 @@ def test_grouped_gemms_match_oracle(gg, shape, act):
 
     # FC1: H1 = bf16(Xq W1f^T)
     H1_ref = oracle.grouped_linear(rows(xq["Q"], xq["S"], s.H), W["W1f"], off)[:n]
-    H1k = torch_to_f64(H1)[:n]
+    H1k = torch_to_f64(H1[:n])
     assert_parity(H1k, H1_ref, "H1", faithful=oracle.round_to_bf16(H1_ref))
     # the activation codes, from the kernel's own H1
     aq_ref, ac_ref = _quant_bits(oracle.round_to_bf16(oracle.glu(H1k, name) * por))
     _assert_codes_close(*codes(Aq, As, s.F), aq_ref, ac_ref, "A")
     # FC2 from the kernel's codes
     Yp_ref = oracle.grouped_linear(rows(Aq, As, s.F), W["W2f"], off)[:n]
-    assert_parity(torch_to_f64(Yp)[:n], Yp_ref, "Yp", faithful=oracle.round_to_bf16(Yp_ref))
+    assert_parity(torch_to_f64(Yp[:n]), Yp_ref, "Yp", faithful=oracle.round_to_bf16(Yp_ref))
     # dgrad FC2 + activation backward from the kernel's dYq and H1
     dA0 = oracle.round_to_bf16(
         oracle.grouped_linear_t(rows(dyq["Q"], dyq["S"], s.H), W["W2d"], off)[:n])
@@ -264,7 +264,7 @@ def test_grouped_gemms_match_oracle(gg, shape, act):
                   faithful=np.sum(dA0 * oracle.round_to_bf16(oracle.glu(H1k, name)), axis=1))
     # dgrad FC1 from the kernel's dH1 codes
     dXp_ref = oracle.grouped_linear_t(rows(dHq, dHs, 2 * s.F), W["W1d"], off)[:n]
-    assert_parity(torch_to_f64(dXp)[:n], dXp_ref, "dXp", faithful=oracle.round_to_bf16(dXp_ref))
+    assert_parity(torch_to_f64(dXp[:n]), dXp_ref, "dXp", faithful=oracle.round_to_bf16(dXp_ref))
 
 
 # ------------------------------------------------------------ the layer
@@ -291,10 +291,10 @@ def test_layer_matches_oracle(gg, shape, act, mode):
     b = mxo.mx_backward(inp.dOut, f)
     ff = mxo.mx_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, s.E, s.P, faithful=True, **kw)
     fb = mxo.mx_backward(inp.dOut, ff)
-    assert_parity(torch_to_f64(out), f["out"], "out", faithful=ff["out"])
-    assert_parity(torch_to_f64(dX), b["dX"], "dX", faithful=fb["dX"])
+    assert_parity(torch_to_f64(out), f["out"], "out", faithful=ff["out"], scope="tensor")
+    assert_parity(torch_to_f64(dX), b["dX"], "dX", faithful=fb["dX"], scope="tensor")
     assert_parity(dprob.cpu().numpy().astype(np.float64), b["dprob"], "dprob",
-                  faithful=fb["dprob"])
+                  faithful=fb["dprob"], scope="tensor")
     n = int(f["offsets"][-1])
     np.testing.assert_array_equal(layer.view("offsets").cpu().numpy(), f["offsets"])
     assert_parity(torch_to_f64(layer.view("H1")[:n]), f["H1"][:n], "H1",
@@ -342,9 +342,9 @@ def test_layer_empty_batch_and_zero_token_experts(gg):
     _, out, dX, dprob = _layer(gg, s, d, mxw)
     f = mxo.mx_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, s.E, s.P)
     ff = mxo.mx_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, s.E, s.P, faithful=True)
-    assert_parity(torch_to_f64(out), f["out"], "out", faithful=ff["out"])
+    assert_parity(torch_to_f64(out), f["out"], "out", faithful=ff["out"], scope="tensor")
     b, fb = mxo.mx_backward(inp.dOut, f), mxo.mx_backward(inp.dOut, ff)
-    assert_parity(torch_to_f64(dX), b["dX"], "dX", faithful=fb["dX"])
+    assert_parity(torch_to_f64(dX), b["dX"], "dX", faithful=fb["dX"], scope="tensor")
     empty = gg.MxMoeLayer(0, s.H, s.F, s.k, s.E, s.P)
     o = empty.forward(d["x"][:0], d["idx"][:0], d["prob"][:0], mxw)
     g = empty.backward(d["dOut"][:0], mxw)
@@ -375,10 +375,10 @@ def test_layer_fullsize_sampled_parity(gg):
     ff = mxo.mx_forward(inp.x[sel], inp.idx[sel], inp.prob[sel], inp.W1, inp.W2, s.E, 1,
                         faithful=True, weights=W)
     b, fb = mxo.mx_backward(inp.dOut[sel], f), mxo.mx_backward(inp.dOut[sel], ff)
-    assert_parity(torch_to_f64(out)[sel], f["out"], "out", faithful=ff["out"])
-    assert_parity(torch_to_f64(dX)[sel], b["dX"], "dX", faithful=fb["dX"])
+    assert_parity(torch_to_f64(out)[sel], f["out"], "out", faithful=ff["out"], scope="tensor")
+    assert_parity(torch_to_f64(dX)[sel], b["dX"], "dX", faithful=fb["dX"], scope="tensor")
     assert_parity(dprob.cpu().numpy().astype(np.float64)[sel], b["dprob"], "dprob",
-                  faithful=fb["dprob"])
+                  faithful=fb["dprob"], scope="tensor")
 
 
 def test_layer_at_the_expert_limit(gg):
@@ -397,7 +397,7 @@ def test_layer_at_the_expert_limit(gg):
     f = mxo.mx_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, s.E, s.P)
     ff = mxo.mx_forward(inp.x, inp.idx, inp.prob, inp.W1, inp.W2, s.E, s.P, faithful=True)
     b, fb = mxo.mx_backward(inp.dOut, f), mxo.mx_backward(inp.dOut, ff)
-    assert_parity(torch_to_f64(out), f["out"], "out", faithful=ff["out"])
-    assert_parity(torch_to_f64(dX), b["dX"], "dX", faithful=fb["dX"])
+    assert_parity(torch_to_f64(out), f["out"], "out", faithful=ff["out"], scope="tensor")
+    assert_parity(torch_to_f64(dX), b["dX"], "dX", faithful=fb["dX"], scope="tensor")
     assert_parity(dprob.cpu().numpy().astype(np.float64), b["dprob"], "dprob",
-                  faithful=fb["dprob"])
+                  faithful=fb["dprob"], scope="tensor")

@@ -96,3 +96,28 @@ def test_noalloc_permute_rejects_batches_beyond_its_scratch(gg):
                                      ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert code == 4  # GG_ERR_WORKSPACE_TOO_SMALL
     assert gg.launch_count() == before
+
+
+def test_noalloc_permute_maps_only(gg):
+    # With Xp (and x) NULL the call produces only the row maps, offsets and
+    # per-row probabilities, as gg_permute does; twice in a row again.
+    shape = MoeShape("maps_e16_h128_t500_k4_pad8", E=16, H=128, F=128, T=500, k=4, P=8)
+    for seed in (17, 18):
+        inp = make_inputs(shape, seed, with_weights=False, with_dout=False)
+        x = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).cuda()
+        idx = torch.from_numpy(inp.idx).cuda()
+        prob = torch.from_numpy(inp.prob).cuda()
+        T, k, E, P, H = shape.T, shape.k, shape.E, shape.P, shape.H
+        mine = _outputs(T, H, k, E, P)
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        code = gg.LIB.gg_permute_noalloc(None, _p(idx), _p(prob), T, H, k, E, P, None,
+                                         _p(mine["offsets"]), _p(mine["row_of_slot"]),
+                                         _p(mine["slot_of_row"]), _p(mine["prob_of_row"]), stream)
+        assert code == gg.GG_OK
+        ref = _outputs(T, H, k, E, P)
+        gg.permute(x, idx, prob, E, P, out=ref)
+        torch.cuda.synchronize()
+        for name in ("offsets", "row_of_slot", "slot_of_row", "prob_of_row"):
+            np.testing.assert_array_equal(_bits(mine[name]), _bits(ref[name]), err_msg=name)
+        # the permuted-row buffer was not touched
+        assert np.all(_bits(mine["Xp"]) == np.int16(SENTINEL_BF16))
