@@ -422,10 +422,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         tc_fence_after();
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
         // this row's <acc, a> over this warp's columns, in four independent
-        // partial sums (a single 32-long chain per chunk would serialise)
-        float rd[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        // partial sums (a single 32-long chain per chunk would serialise):
+        // rd[c & 1] takes column pair c, .x its low and .y its high column
+        float2 rd[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
         const bool want_dot = p.rowdot != nullptr;
         constexpr float alpha = kAlpha;
+        constexpr bool kAlphaOne = kAlpha == 1.0f;
 #pragma unroll 1
         for (int c = c0; c < c_end; c += 32) {
           float v[32];
@@ -445,32 +447,33 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             us[4 * i + 0] = uw[i].x; us[4 * i + 1] = uw[i].y;
             us[4 * i + 2] = uw[i].z; us[4 * i + 3] = uw[i].w;
           }
-          float dg[32], du[32];
+          // column pairs as packed fp32 pairs: half the multiply-add
+          // instructions of the scalar form, the same rounding per column
+          uint32_t dgw[16], duw[16];
           if (want_dot) {
 #pragma unroll
-            for (int h = 0; h < 16; ++h) {
-              glu_mul_bwd<true>(v[2 * h], scale, bf16_lo(gs[h]), bf16_lo(us[h]), alpha,
-                                dg[2 * h], du[2 * h], rd[h & 1]);
-              glu_mul_bwd<true>(v[2 * h + 1], scale, bf16_hi(gs[h]), bf16_hi(us[h]), alpha,
-                                dg[2 * h + 1], du[2 * h + 1], rd[2 + (h & 1)]);
-            }
+            for (int h = 0; h < 16; ++h)
+              glu_mul_bwd2<true, kAlphaOne>(make_float2(v[2 * h], v[2 * h + 1]), scale, gs[h],
+                                            us[h], alpha, dgw[h], duw[h], rd[h & 1]);
           } else {
 #pragma unroll
-            for (int h = 0; h < 16; ++h) {
-              glu_mul_bwd<false>(v[2 * h], scale, bf16_lo(gs[h]), bf16_lo(us[h]), alpha,
-                                 dg[2 * h], du[2 * h], rd[h & 1]);
-              glu_mul_bwd<false>(v[2 * h + 1], scale, bf16_hi(gs[h]), bf16_hi(us[h]), alpha,
-                                 dg[2 * h + 1], du[2 * h + 1], rd[2 + (h & 1)]);
-            }
+            for (int h = 0; h < 16; ++h)
+              glu_mul_bwd2<false, kAlphaOne>(make_float2(v[2 * h], v[2 * h + 1]), scale, gs[h],
+                                             us[h], alpha, dgw[h], duw[h], rd[h & 1]);
           }
           uint4 w[4];
-          pack_bf16x32(dg, 1.0f, w);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            w[i] = make_uint4(dgw[4 * i], dgw[4 * i + 1], dgw[4 * i + 2], dgw[4 * i + 3]);
           store_chunk(stg, w, drow0 + c, 2LL * F, nvalid);
-          pack_bf16x32(du, 1.0f, w);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            w[i] = make_uint4(duw[4 * i], duw[4 * i + 1], duw[4 * i + 2], duw[4 * i + 3]);
           store_chunk(stg, w, drow0 + F + c, 2LL * F, nvalid);
         }
         if (p.rowdot != nullptr && valid)
-          p.rowdot[grow * p.rowdot_stride + nt * 2 + half] = (rd[0] + rd[1]) + (rd[2] + rd[3]);
+          p.rowdot[grow * p.rowdot_stride + nt * 2 + half] =
+              (rd[0].x + rd[1].x) + (rd[0].y + rd[1].y);
       }
       tc_fence_before();
       __syncwarp();

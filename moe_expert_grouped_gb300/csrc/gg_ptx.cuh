@@ -320,6 +320,43 @@ __device__ __forceinline__ void glu_mul_bwd(float acc, float scale, float g, flo
   if (kDot) dot = fmaf(acc, round_bf16(gs * u), dot);
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi);
+__device__ __forceinline__ float bf16_lo(uint32_t w);
+__device__ __forceinline__ float bf16_hi(uint32_t w);
+
+// glu_mul_bwd for two neighbouring columns at once: g and u arrive as BF16
+// pairs (column 2i in the low half), dg and du leave as BF16 pairs. The
+// multiplies and adds run as packed fp32 pairs (one instruction for both
+// columns; each lane rounds exactly as the scalar operation would), the
+// exponential and reciprocal per column with the same intrinsics as
+// glu_mul, so the activation value paired with the accumulator for the
+// probability gradient is bitwise the forward's. With kDot, dot.x and dot.y
+// accumulate acc * bf16(act(g) * u) of the low and high column.
+template <bool kDot, bool kAlphaOne>
+__device__ __forceinline__ void glu_mul_bwd2(float2 acc, float scale, uint32_t gw, uint32_t uw,
+                                             float alpha, uint32_t& dg, uint32_t& du,
+                                             float2& dot) {
+  const float2 one = make_float2(1.0f, 1.0f);
+  const float2 g = make_float2(bf16_lo(gw), bf16_hi(gw));
+  const float2 u = make_float2(bf16_lo(uw), bf16_hi(uw));
+  const float2 dA = __fmul2_rn(acc, make_float2(scale, scale));
+  const float2 ag = kAlphaOne ? g : __fmul2_rn(make_float2(alpha, alpha), g);
+  const float2 y = __fadd2_rn(one, make_float2(__expf(-ag.x), __expf(-ag.y)));
+  const float2 s = make_float2(__fdividef(1.0f, y.x), __fdividef(1.0f, y.y));
+  const float2 om = __ffma2_rn(s, make_float2(-1.0f, -1.0f), one);  // 1 - s
+  const float2 dact = __fmul2_rn(s, __ffma2_rn(ag, om, one));       // s (1 + ag (1 - s))
+  const float2 gs = __fmul2_rn(g, s);
+  const float2 dg2 = __fmul2_rn(__fmul2_rn(dA, u), dact);
+  const float2 du2 = __fmul2_rn(dA, gs);
+  dg = pack_bf16x2(dg2.x, dg2.y);
+  du = pack_bf16x2(du2.x, du2.y);
+  if (kDot) {
+    const float2 a = __fmul2_rn(gs, u);
+    const uint32_t aw = pack_bf16x2(a.x, a.y);
+    dot = __ffma2_rn(acc, make_float2(bf16_lo(aw), bf16_hi(aw)), dot);
+  }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&p);
