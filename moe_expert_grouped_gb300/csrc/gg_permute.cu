@@ -474,24 +474,17 @@ combine_dprob_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ r
   }
 }
 
-// combine_kernel plus a probability gradient that is a dot product of the
-// token's row of dot_src with one permuted row per slot:
-//   kDotRows false: dprob[t*k+j] = <dot_src[t], Yp[row(t, j)]> (the pre-FC1
-//     mode: Xp[row] = prob * dot_src[t], dot_src = x, Yp = dXp);
-//   kDotRows true:  dprob[t*k+j] = <dot_src[t], dot_rows[row(t, j)]> (the
-//     probability at the combine: dot_src = dOut, dot_rows = the forward's
-//     Yp, while the sum runs over Yp = dXp).
-// Each lane keeps one partial dot per slot over its columns (the token's
-// chunk loaded once per pass), reduced across the warp in a fixed butterfly
-// order at the end; kMaxK (8 or 32) bounds k and the partials held in
-// registers.
-template <int kMaxK, bool kDotRows>
+// combine_kernel plus the pre-FC1 probability gradient: with Xp[row] =
+// prob * dot_src[t], dprob[t*k+j] = <dot_src[t], Yp[row(t, j)]>. Each lane
+// keeps one partial dot per slot over its columns (x chunk loaded once per
+// pass), reduced across the warp in a fixed butterfly order at the end;
+// kMaxK (8 or 32) bounds k and the partials held in registers.
+template <int kMaxK>
 __global__ void __launch_bounds__(256)
 combine_dot_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row_of_slot,
                    const float* __restrict__ prob, int T, int k, int vec_per_row, int R_cap,
                    uint4* __restrict__ out, const uint4* __restrict__ dot_src,
-                   const uint4* __restrict__ dot_rows, float* __restrict__ dprob,
-                   int32_t* status) {
+                   float* __restrict__ dprob, int32_t* status) {
   const int lane = threadIdx.x & 31;
   const int warp0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -529,24 +522,13 @@ combine_dot_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row
         const uint4 va = oka ? __ldcs(rp + ca) : make_uint4(0u, 0u, 0u, 0u);
         const uint4 vb = okb ? __ldcs(rp + cb) : make_uint4(0u, 0u, 0u, 0u);
         const uint32_t yw[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-        uint32_t dw[8];
-        if (kDotRows) {
-          const uint4* dp = dot_rows + static_cast<long long>(row) * vec_per_row;
-          const uint4 da = oka ? __ldcs(dp + ca) : make_uint4(0u, 0u, 0u, 0u);
-          const uint4 db = okb ? __ldcs(dp + cb) : make_uint4(0u, 0u, 0u, 0u);
-          dw[0] = da.x; dw[1] = da.y; dw[2] = da.z; dw[3] = da.w;
-          dw[4] = db.x; dw[5] = db.y; dw[6] = db.z; dw[7] = db.w;
-        } else {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) dw[q] = yw[q];
-        }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const float ylo = bf16_lo(yw[q]), yhi = bf16_hi(yw[q]);
           acc[q >> 2][2 * (q & 3)] = __fmaf_rn(pj, ylo, acc[q >> 2][2 * (q & 3)]);
           acc[q >> 2][2 * (q & 3) + 1] = __fmaf_rn(pj, yhi, acc[q >> 2][2 * (q & 3) + 1]);
-          dotp[j] = __fmaf_rn(bf16_lo(xw[q]), bf16_lo(dw[q]), dotp[j]);
-          dotp[j] = __fmaf_rn(bf16_hi(xw[q]), bf16_hi(dw[q]), dotp[j]);
+          dotp[j] = __fmaf_rn(bf16_lo(xw[q]), ylo, dotp[j]);
+          dotp[j] = __fmaf_rn(bf16_hi(xw[q]), yhi, dotp[j]);
         }
       }
       uint4* op = out + static_cast<long long>(t) * vec_per_row;
@@ -556,6 +538,97 @@ combine_dot_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row
       if (okb)
         __stcs(op + cb, make_uint4(pack_bf16x2(acc[1][0], acc[1][1]), pack_bf16x2(acc[1][2], acc[1][3]),
                                    pack_bf16x2(acc[1][4], acc[1][5]), pack_bf16x2(acc[1][6], acc[1][7])));
+    }
+    float mine = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j >= k) break;
+      float v = dotp[j];
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, m);
+      if (lane == j) mine = v;
+    }
+    if (lane < k) dprob[static_cast<long long>(t) * k + lane] = my_row >= 0 ? mine : 0.0f;
+  }
+}
+
+// out[t] = bf16(sum_j [prob] * Sp[row(t, j)]) (fp32 in slot order, one
+// rounding: bitwise the plain combine) together with dprob[t*k+j] =
+// <dot_src[t], D[row(t, j)]>. One warp per token; per pass each lane takes
+// one 16-byte column group of the token's rows and issues the loads of up to
+// eight slots' Sp and D rows before any arithmetic, so every warp keeps 16
+// row loads in flight (the rows are gathered, one DRAM round trip each).
+// Slots beyond eight are taken in further groups of eight; kMaxK (8 or 32)
+// bounds k and the dot partials held in registers.
+template <int kMaxK>
+__global__ void __launch_bounds__(256)
+combine_dot_rows_kernel(const uint4* __restrict__ Sp, const int32_t* __restrict__ row_of_slot,
+                        const float* __restrict__ prob, int T, int k, int vec_per_row,
+                        int R_cap, uint4* __restrict__ out, const uint4* __restrict__ dot_src,
+                        const uint4* __restrict__ D, float* __restrict__ dprob,
+                        int32_t* status) {
+  constexpr int kGroup = 8;
+  const int lane = threadIdx.x & 31;
+  const int warp0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = warp0; t < T; t += nwarps) {
+    int my_row = -1;
+    float my_p = 1.0f;
+    if (lane < k) {
+      my_row = row_of_slot[static_cast<long long>(t) * k + lane];
+      if (prob != nullptr) my_p = prob[static_cast<long long>(t) * k + lane];
+      if (my_row < -1 || my_row >= R_cap) {
+        set_status(status, GG_ERR_DEVICE_BAD_ROW);
+        my_row = -1;
+      }
+    }
+    float dotp[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) dotp[j] = 0.0f;
+    const uint4* xs = dot_src + static_cast<long long>(t) * vec_per_row;
+    for (int c0 = 0; c0 < vec_per_row; c0 += 32) {
+      const int c = c0 + lane;
+      const bool ok = c < vec_per_row;
+      const uint4 xv = ok ? __ldg(xs + c) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+      for (int g0 = 0; g0 < kMaxK; g0 += kGroup) {
+        if (g0 >= k) break;
+        uint4 sv[kGroup], dv[kGroup];
+        float pj[kGroup];
+#pragma unroll
+        for (int i = 0; i < kGroup; ++i) {
+          const int j = g0 + i;
+          const int row = __shfl_sync(0xFFFFFFFFu, my_row, j & 31);
+          pj[i] = __shfl_sync(0xFFFFFFFFu, my_p, j & 31);
+          const bool live = ok && j < k && row >= 0;
+          const long long off = static_cast<long long>(live ? row : 0) * vec_per_row + c;
+          sv[i] = live ? __ldcs(Sp + off) : make_uint4(0u, 0u, 0u, 0u);
+          dv[i] = live ? __ldcs(D + off) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < kGroup; ++i) {
+          const int j = g0 + i;
+          const int row = __shfl_sync(0xFFFFFFFFu, my_row, j & 31);
+          if (j >= k || row < 0) continue;  // warp-uniform
+          const uint32_t sw[4] = {sv[i].x, sv[i].y, sv[i].z, sv[i].w};
+          const uint32_t dw[4] = {dv[i].x, dv[i].y, dv[i].z, dv[i].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            acc[2 * q] = __fmaf_rn(pj[i], bf16_lo(sw[q]), acc[2 * q]);
+            acc[2 * q + 1] = __fmaf_rn(pj[i], bf16_hi(sw[q]), acc[2 * q + 1]);
+            dotp[j] = __fmaf_rn(bf16_lo(xw[q]), bf16_lo(dw[q]), dotp[j]);
+            dotp[j] = __fmaf_rn(bf16_hi(xw[q]), bf16_hi(dw[q]), dotp[j]);
+          }
+        }
+      }
+      if (ok)
+        __stcs(out + static_cast<long long>(t) * vec_per_row + c,
+               make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                          pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
     }
     float mine = 0.0f;
 #pragma unroll
@@ -679,17 +752,6 @@ cudaError_t launch_zero_pad_rows(const int32_t* slot_of_row, const int32_t* offs
   return cudaGetLastError();
 }
 
-template <int kMaxK, bool kDotRows>
-void launch_combine_dot(int blocks, const gg_bf16* Yp, const int32_t* row_of_slot,
-                        const float* prob, int T, int k, int vec, int R_cap, gg_bf16* out,
-                        const gg_bf16* dot_src, const gg_bf16* dot_rows, float* dprob,
-                        int32_t* status, cudaStream_t stream) {
-  combine_dot_kernel<kMaxK, kDotRows><<<blocks, 256, 0, stream>>>(
-      reinterpret_cast<const uint4*>(Yp), row_of_slot, prob, T, k, vec, R_cap,
-      reinterpret_cast<uint4*>(out), reinterpret_cast<const uint4*>(dot_src),
-      reinterpret_cast<const uint4*>(dot_rows), dprob, status);
-}
-
 cudaError_t launch_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const float* prob,
                            int T, int k, int H, int R_cap, gg_bf16* out, const float* rowdot,
                            int n_rowdot, const gg_bf16* dot_src, const gg_bf16* dot_rows,
@@ -702,17 +764,23 @@ cudaError_t launch_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const 
   const int nb = static_cast<int>(blocks);
   if (dprob != nullptr && dot_src != nullptr) {
     if (dot_rows != nullptr && k <= 8)
-      launch_combine_dot<8, true>(nb, Yp, row_of_slot, prob, T, k, vec, R_cap, out, dot_src,
-                                  dot_rows, dprob, status, stream);
+      combine_dot_rows_kernel<8><<<nb, 256, 0, stream>>>(
+          reinterpret_cast<const uint4*>(Yp), row_of_slot, prob, T, k, vec, R_cap,
+          reinterpret_cast<uint4*>(out), reinterpret_cast<const uint4*>(dot_src),
+          reinterpret_cast<const uint4*>(dot_rows), dprob, status);
     else if (dot_rows != nullptr)
-      launch_combine_dot<32, true>(nb, Yp, row_of_slot, prob, T, k, vec, R_cap, out, dot_src,
-                                   dot_rows, dprob, status, stream);
+      combine_dot_rows_kernel<32><<<nb, 256, 0, stream>>>(
+          reinterpret_cast<const uint4*>(Yp), row_of_slot, prob, T, k, vec, R_cap,
+          reinterpret_cast<uint4*>(out), reinterpret_cast<const uint4*>(dot_src),
+          reinterpret_cast<const uint4*>(dot_rows), dprob, status);
     else if (k <= 8)
-      launch_combine_dot<8, false>(nb, Yp, row_of_slot, prob, T, k, vec, R_cap, out, dot_src,
-                                   nullptr, dprob, status, stream);
+      combine_dot_kernel<8><<<nb, 256, 0, stream>>>(
+          reinterpret_cast<const uint4*>(Yp), row_of_slot, prob, T, k, vec, R_cap,
+          reinterpret_cast<uint4*>(out), reinterpret_cast<const uint4*>(dot_src), dprob, status);
     else
-      launch_combine_dot<32, false>(nb, Yp, row_of_slot, prob, T, k, vec, R_cap, out, dot_src,
-                                    nullptr, dprob, status, stream);
+      combine_dot_kernel<32><<<nb, 256, 0, stream>>>(
+          reinterpret_cast<const uint4*>(Yp), row_of_slot, prob, T, k, vec, R_cap,
+          reinterpret_cast<uint4*>(out), reinterpret_cast<const uint4*>(dot_src), dprob, status);
   } else if (dprob != nullptr)
     combine_dprob_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
         reinterpret_cast<const uint4*>(Yp), row_of_slot, prob, T, k, vec, R_cap,
