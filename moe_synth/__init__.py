@@ -139,7 +139,14 @@ class MoeShape:
         return 6.0 * self.R * self.H * self.F
 
     def with_tokens(self, T: int) -> "MoeShape":
-        return dataclasses.replace(self, T=T)
+        """The same workload with T tokens; the name carries the new T."""
+        import re
+
+        if re.search(r"_t\d+", self.name):
+            name = re.sub(r"_t\d+", f"_t{T}", self.name, count=1)
+        else:
+            name = re.sub(r"_k(\d+)", rf"_t{T}_k\1", self.name, count=1)
+        return dataclasses.replace(self, T=T, name=name)
 
 
 # The five workloads: a tiny correctness case, the balanced 128-expert layer,
