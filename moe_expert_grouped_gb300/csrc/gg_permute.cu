@@ -212,15 +212,43 @@ permute_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict_
   }
 }
 
+// Zero the padding rows (slot -1) below offsets[E], 32 rows per warp and step
+// of a grid-stride loop starting at warp `w0` of `nw`: a ballot over the
+// group's slots, then the group's padding rows cleared together.
+__device__ __forceinline__ void zero_pad_rows(const int32_t* __restrict__ slot_of_row,
+                                              const int32_t* __restrict__ offsets, int E,
+                                              int R_cap, int vec_per_row,
+                                              uint4* __restrict__ dst, long long w0,
+                                              long long nw) {
+  const int lane = threadIdx.x & 31;
+  // offsets may come from the caller: never past the buffer's R_cap rows
+  const long long n_rows = min(static_cast<long long>(offsets[E]), static_cast<long long>(R_cap));
+  for (long long base = w0 * 32; base < n_rows; base += nw * 32) {
+    const long long r = base + lane;
+    const bool pad = r < n_rows && slot_of_row[r] < 0;
+    uint32_t mask = __ballot_sync(0xFFFFFFFFu, pad);
+    while (mask != 0) {
+      const int b = __ffs(mask) - 1;
+      mask &= mask - 1;
+      uint4* d = dst + (base + b) * vec_per_row;
+      for (int c = lane; c < vec_per_row; c += 32) __stcs(d + c, make_uint4(0u, 0u, 0u, 0u));
+    }
+  }
+}
+
 // dst[row_of_slot[t*k+j]] = src[t] for every pair (t, j) with a row: one warp
 // per token reads the token's row once and writes its k copies (reading the
 // source in order and writing whole 16-byte-vector rows runs at copy speed;
 // the destination-ordered form re-reads source rows through L2 in random
 // order). Stores are streaming: the permuted buffer is far larger than L2.
+// With slot_of_row given, the same launch then zeroes the padding rows
+// below offsets[E] (the warps that finish their tokens first start on them,
+// so the copy and the zeroing overlap instead of running back to back).
 __global__ void __launch_bounds__(256)
 scatter_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ row_of_slot,
                     int T, int k, int vec_per_row, int R_cap, uint4* __restrict__ dst,
-                    int32_t* status) {
+                    int32_t* status, const int32_t* __restrict__ pad_slot_of_row,
+                    const int32_t* __restrict__ offsets, int E) {
   const int lane = threadIdx.x & 31;
   const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -253,6 +281,12 @@ scatter_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ r
       }
     }
   }
+  if (pad_slot_of_row != nullptr) {
+    // warps past the tokens start first: number the warps from the last one
+    const long long first = (static_cast<long long>(T) % nwarps);
+    zero_pad_rows(pad_slot_of_row, offsets, E, R_cap, vec_per_row, dst,
+                  (warp0 - first + nwarps) % nwarps, nwarps);
+  }
 }
 
 // scatter_rows_kernel with the pre-FC1 probability multiply: the copy of
@@ -260,7 +294,9 @@ scatter_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ r
 __global__ void __launch_bounds__(256)
 scatter_rows_scaled_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ row_of_slot,
                            const float* __restrict__ prob, int T, int k, int vec_per_row,
-                           int R_cap, uint4* __restrict__ dst, int32_t* status) {
+                           int R_cap, uint4* __restrict__ dst, int32_t* status,
+                           const int32_t* __restrict__ pad_slot_of_row,
+                           const int32_t* __restrict__ offsets, int E) {
   const int lane = threadIdx.x & 31;
   const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -303,28 +339,21 @@ scatter_rows_scaled_kernel(const uint4* __restrict__ src, const int32_t* __restr
       }
     }
   }
+  if (pad_slot_of_row != nullptr) {
+    const long long first = (static_cast<long long>(T) % nwarps);
+    zero_pad_rows(pad_slot_of_row, offsets, E, R_cap, vec_per_row, dst,
+                  (warp0 - first + nwarps) % nwarps, nwarps);
+  }
 }
 
-// Zero the padding rows (slot -1) below offsets[E]: each warp checks 32
-// consecutive rows and clears the padding ones together.
+// Zero the padding rows (slot -1) below offsets[E] (the standalone form, for
+// buffers no row copy writes).
 __global__ void __launch_bounds__(256)
 zero_pad_rows_kernel(const int32_t* __restrict__ slot_of_row, const int32_t* __restrict__ offsets,
-                     int E, int vec_per_row, uint4* __restrict__ dst) {
-  const int lane = threadIdx.x & 31;
-  const long long n_rows = offsets[E];
+                     int E, int R_cap, int vec_per_row, uint4* __restrict__ dst) {
   const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-  for (long long base = warp0 * 32; base < n_rows; base += nwarps * 32) {
-    const long long r = base + lane;
-    const bool pad = r < n_rows && slot_of_row[r] < 0;
-    uint32_t mask = __ballot_sync(0xFFFFFFFFu, pad);
-    while (mask != 0) {
-      const int b = __ffs(mask) - 1;
-      mask &= mask - 1;
-      uint4* d = dst + (base + b) * vec_per_row;
-      for (int c = lane; c < vec_per_row; c += 32) __stcs(d + c, make_uint4(0u, 0u, 0u, 0u));
-    }
-  }
+  zero_pad_rows(slot_of_row, offsets, E, R_cap, vec_per_row, dst, warp0, nwarps);
 }
 
 // out[t] = bf16(sum_j prob[t][j] * Yp[row_of_slot[t*k+j]]), fp32 in slot
@@ -719,22 +748,23 @@ cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* row_of_slot,
   // slowly (measured faster than one exactly resident wave).
   const long long cap = static_cast<long long>(sm_count) * 8;
   if (blocks > cap) blocks = cap;
+  // with padding, the same launch zeroes the padding rows: warps for the
+  // tokens plus one warp per 32-row group of the rows (up to the cap; past it
+  // the groups go first to the warps with one token fewer)
+  if (has_padding) {
+    const long long pad_blocks = (static_cast<long long>(R_cap) + 255) / 256;
+    blocks = blocks + pad_blocks < cap ? blocks + pad_blocks : cap;
+  }
+  const int32_t* pad_sor = has_padding ? slot_of_row : nullptr;
   if (prob != nullptr)
     scatter_rows_scaled_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
         reinterpret_cast<const uint4*>(src), row_of_slot, prob, T, k, vec, R_cap,
-        reinterpret_cast<uint4*>(dst), status);
+        reinterpret_cast<uint4*>(dst), status, pad_sor, offsets, E);
   else
     scatter_rows_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
         reinterpret_cast<const uint4*>(src), row_of_slot, T, k, vec, R_cap,
-        reinterpret_cast<uint4*>(dst), status);
+        reinterpret_cast<uint4*>(dst), status, pad_sor, offsets, E);
   count_launch();
-  if (has_padding) {
-    long long pb = (static_cast<long long>(R_cap) + 255) / 256;
-    if (pb > cap) pb = cap;
-    zero_pad_rows_kernel<<<static_cast<int>(pb), 256, 0, stream>>>(slot_of_row, offsets, E, vec,
-                                                                    reinterpret_cast<uint4*>(dst));
-    count_launch();
-  }
   return cudaGetLastError();
 }
 
@@ -745,7 +775,7 @@ cudaError_t launch_zero_pad_rows(const int32_t* slot_of_row, const int32_t* offs
   long long pb = (static_cast<long long>(R_cap) + 255) / 256;
   const long long cap = static_cast<long long>(sm_count) * 8;
   if (pb > cap) pb = cap;
-  zero_pad_rows_kernel<<<static_cast<int>(pb), 256, 0, stream>>>(slot_of_row, offsets, E,
+  zero_pad_rows_kernel<<<static_cast<int>(pb), 256, 0, stream>>>(slot_of_row, offsets, E, R_cap,
                                                                   vec_per_row,
                                                                   static_cast<uint4*>(dst));
   count_launch();
