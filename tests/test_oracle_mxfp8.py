@@ -15,7 +15,8 @@
   along one axis but not along the other;
 * the combine-mode probability gradient against a central finite difference
   of the forward (exact: out is linear in the probabilities there) and
-  against the closed form of identity weights."""
+  against the closed form of identity weights; the weighted-activation
+  probability gradient against its closed form on identity weights."""
 
 import numpy as np
 import pytest
@@ -254,4 +255,30 @@ def test_combine_mode_prob_grad_closed_form_on_identity_weights():
     for t in range(T):
         for j in range(k):
             np.testing.assert_allclose(b["dprob"][t, j], np.dot(dOut[t], y[t]), rtol=1e-13,
+                                       atol=1e-13)
+
+
+def test_weighted_activation_prob_grad_closed_form_on_identity_weights():
+    # With the probability inside the activation, A = bf16(p * act(H1)) and
+    # the quantiser of A passes the gradient straight through, so dprob is
+    # the row sum of dA0 * act(H1). With gate and up blocks [I; 0], W2 = [I 0]
+    # and representable x and dOut, dA0 = dOut (exact in every format) and
+    # act(H1) = x^2 sigmoid(x): dprob_tj = <dOut_t, x_t^2 sigmoid(x_t)>.
+    rng = np.random.default_rng(13)
+    E, H, F, T, k = 2, 64, 64, 8, 2
+    W1 = np.zeros((E, 2 * F, H))
+    W1[:, :H, :] = np.eye(H)
+    W1[:, F:F + H, :] = np.eye(H)
+    W2 = np.zeros((E, H, F))
+    W2[:, :, :H] = np.eye(H)
+    x = _representable(rng, (T, H), 1.0)
+    dOut = _representable(rng, (T, H), 0.5)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    prob = rng.uniform(0.1, 1.0, (T, k))
+    f = mxo.mx_forward(x, idx, prob, W1, W2, E, prob_mode="activation")
+    b = mxo.mx_backward(dOut, f)
+    act = x * x / (1.0 + np.exp(-x))
+    for t in range(T):
+        for j in range(k):
+            np.testing.assert_allclose(b["dprob"][t, j], np.dot(dOut[t], act[t]), rtol=1e-13,
                                        atol=1e-13)
