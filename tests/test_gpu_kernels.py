@@ -513,3 +513,36 @@ def test_combine_dot_with_separate_dot_rows(gg, k, weighted):
     got = dprob.cpu().numpy().astype(np.float64)
     assert np.all(got.reshape(-1)[rows < 0] == 0)
     assert_parity(got, ref, "dprob (dot rows)")
+
+
+@pytest.mark.parametrize("T,k,H", [(0, 4, 128), (7, 1, 64), (50, 32, 64), (129, 5, 576)])
+def test_combine_dot_rows_edge_cases(gg, T, k, H):
+    # an empty batch enqueues nothing; one slot; the 32-slot bound; a row of
+    # 576 columns (the last pass leaves most lanes without a column group)
+    R_cap = max(1, 3 * T * k)
+    rng = np.random.default_rng(61 + T + k)
+    rows = rng.permutation(R_cap)[:T * k].astype(np.int32)
+    if T * k > 3:
+        rows[1] = -1
+    Sp = normal_bf16(rng, (R_cap, H), 1.0)
+    D = normal_bf16(rng, (R_cap, H), 1.0)
+    xs = normal_bf16(rng, (max(T, 1), H), 1.0)[:T]
+    prob = rng.uniform(0, 1, (T, k)).astype(np.float32)
+    ws = gg.workspace(max(T, 1), k, 1, "cuda")
+    d_rows = torch.from_numpy(rows).cuda()
+    d_prob = torch.from_numpy(prob).cuda()
+    before = gg.launch_count()
+    out, dprob = gg.unpermute_combine_dot(bits_to_torch(Sp), d_rows, d_prob, T, k,
+                                          bits_to_torch(xs), bits_to_torch(D), ws)
+    torch.cuda.synchronize()
+    assert gg.read_status(ws) == 0
+    if T == 0:
+        assert gg.launch_count() == before
+        return
+    out2 = gg.unpermute_combine(bits_to_torch(Sp), d_rows, d_prob, T, k, ws)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(torch_to_bits(out), torch_to_bits(out2))
+    ref = oracle.prob_grad(oracle.bf16_bits_to_f64(xs), oracle.bf16_bits_to_f64(D), rows, T, k)
+    got = dprob.cpu().numpy().astype(np.float64)
+    assert np.all(got.reshape(-1)[rows < 0] == 0)
+    assert_parity(got, ref, "dprob (dot rows, edge case)")
