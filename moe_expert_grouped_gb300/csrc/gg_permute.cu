@@ -282,7 +282,9 @@ scatter_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ r
     }
   }
   if (pad_slot_of_row != nullptr) {
-    // warps past the tokens start first: number the warps from the last one
+    // the 32-row groups go first to the warps with one token fewer (those
+    // from T % nwarps on: all warps past the tokens when there are more
+    // warps than tokens)
     const long long first = (static_cast<long long>(T) % nwarps);
     zero_pad_rows(pad_slot_of_row, offsets, E, R_cap, vec_per_row, dst,
                   (warp0 - first + nwarps) % nwarps, nwarps);
