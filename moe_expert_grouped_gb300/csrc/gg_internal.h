@@ -57,11 +57,14 @@ cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* pr
 
 // dst[row_of_slot[t*k+j]] = src[t] (times prob[t*k+j] when prob is not
 // null); with has_padding, rows below offsets[E] whose slot_of_row is -1 are
-// zeroed.
+// zeroed. after_maps: the launch directly follows the kernel that writes the
+// row maps, so it may start before that kernel ends (it waits for its
+// results before its first access).
 cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* row_of_slot,
                                const int32_t* slot_of_row, const int32_t* offsets, int H, int k,
                                int E, int R_cap, int T, bool has_padding, const float* prob,
-                               gg_bf16* dst, int32_t* status, int sm_count, cudaStream_t stream);
+                               gg_bf16* dst, int32_t* status, int sm_count, cudaStream_t stream,
+                               bool after_maps = false);
 
 // dprob (nullable): dprob[t*k+j] = sum_b rowdot[row_of_slot[t*k+j]][b], rows of
 // rowdot (n_rowdot + 7) / 8 * 8 floats apart.

@@ -51,6 +51,7 @@ permute_count_kernel(const int32_t* __restrict__ idx, long long R, int E, long l
                      int32_t* __restrict__ block_hist, int32_t* status,
                      int32_t* __restrict__ slot_of_row, float* __restrict__ prob_of_row,
                      long long R_cap) {
+  grid_dependents_launch();  // the scatter kernel waits for this grid's results
   for (long long r = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; r < R_cap;
        r += static_cast<long long>(gridDim.x) * blockDim.x) {
     slot_of_row[r] = -1;
@@ -100,6 +101,10 @@ permute_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict_
   __shared__ int warp_tot[kWarps];
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int b = blockIdx.x;
+  grid_dependents_launch();  // the row copy waits for this grid's results
+  // zero the warp histograms while the count kernel finishes
+  for (int i = t; i < kWarps * E; i += kPermuteBlockThreads) wb[i] = 0;
+  grid_dependency_wait();  // block_hist, and slot_of_row marked as padding
 
   // (1) totals and counts before this block
   const int parts = max(1, kPermuteBlockThreads / E);
@@ -125,8 +130,6 @@ permute_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict_
     part_all[t] = s_all;
     part_below[t] = s_below;
   }
-  // zero the warp histograms while the partial sums settle
-  for (int i = t; i < kWarps * E; i += kPermuteBlockThreads) wb[i] = 0;
   __syncthreads();
 
   // (2) padded exclusive prefix over experts, E <= 1024 = one expert per thread
@@ -212,18 +215,31 @@ permute_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict_
   }
 }
 
-// Zero the padding rows (slot -1) below offsets[E], 32 rows per warp and step
-// of a grid-stride loop starting at warp `w0` of `nw`: a ballot over the
-// group's slots, then the group's padding rows cleared together.
+// Zero the padding rows (slot -1) below offsets[E]. The work is cut into
+// units of one 32-row group by one column slice of up to 64 16-byte vectors;
+// a unit is a ballot over the group's slots, then the slice cleared on the
+// group's padding rows. Padding rows come in runs at the ends of the experts'
+// segments, so the heavy units are neighbours: warp w of the nw (nw a
+// multiple of 8, the warps of 256-thread blocks) takes the units
+// u = (w % 8) * (nw / 8) + w / 8 + i * nw, i = 0, 1, ..., which puts
+// neighbouring units in different blocks and so spreads a run over the SMs.
 __device__ __forceinline__ void zero_pad_rows(const int32_t* __restrict__ slot_of_row,
                                               const int32_t* __restrict__ offsets, int E,
                                               int R_cap, int vec_per_row,
-                                              uint4* __restrict__ dst, long long w0,
+                                              uint4* __restrict__ dst, long long w,
                                               long long nw) {
+  constexpr int kSlice = 64;
   const int lane = threadIdx.x & 31;
   // offsets may come from the caller: never past the buffer's R_cap rows
   const long long n_rows = min(static_cast<long long>(offsets[E]), static_cast<long long>(R_cap));
-  for (long long base = w0 * 32; base < n_rows; base += nw * 32) {
+  const long long n_slices = (vec_per_row + kSlice - 1) / kSlice;
+  const long long n_units = (n_rows + 31) / 32 * n_slices;
+  const long long first = nw % 8 == 0 ? (w % 8) * (nw / 8) + w / 8 : w;
+  for (long long u = first; u < n_units; u += nw) {
+    const long long g = u / n_slices;
+    const int c_lo = static_cast<int>(u - g * n_slices) * kSlice;
+    const int c_hi = min(vec_per_row, c_lo + kSlice);
+    const long long base = g * 32;
     const long long r = base + lane;
     const bool pad = r < n_rows && slot_of_row[r] < 0;
     uint32_t mask = __ballot_sync(0xFFFFFFFFu, pad);
@@ -231,7 +247,7 @@ __device__ __forceinline__ void zero_pad_rows(const int32_t* __restrict__ slot_o
       const int b = __ffs(mask) - 1;
       mask &= mask - 1;
       uint4* d = dst + (base + b) * vec_per_row;
-      for (int c = lane; c < vec_per_row; c += 32) __stcs(d + c, make_uint4(0u, 0u, 0u, 0u));
+      for (int c = c_lo + lane; c < c_hi; c += 32) __stcs(d + c, make_uint4(0u, 0u, 0u, 0u));
     }
   }
 }
@@ -242,8 +258,8 @@ __device__ __forceinline__ void zero_pad_rows(const int32_t* __restrict__ slot_o
 // the destination-ordered form re-reads source rows through L2 in random
 // order). Stores are streaming: the permuted buffer is far larger than L2.
 // With slot_of_row given, the same launch then zeroes the padding rows
-// below offsets[E] (the warps that finish their tokens first start on them,
-// so the copy and the zeroing overlap instead of running back to back).
+// below offsets[E] (each warp after its tokens, so the copy and the zeroing
+// overlap instead of running back to back).
 __global__ void __launch_bounds__(256)
 scatter_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ row_of_slot,
                     int T, int k, int vec_per_row, int R_cap, uint4* __restrict__ dst,
@@ -252,6 +268,7 @@ scatter_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ r
   const int lane = threadIdx.x & 31;
   const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  grid_dependency_wait();  // the row maps, when launched behind their writer
   for (long long t = warp0; t < T; t += nwarps) {
     int my_row = -1;
     if (lane < k) {
@@ -281,14 +298,8 @@ scatter_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ r
       }
     }
   }
-  if (pad_slot_of_row != nullptr) {
-    // the 32-row groups go first to the warps with one token fewer (those
-    // from T % nwarps on: all warps past the tokens when there are more
-    // warps than tokens)
-    const long long first = (static_cast<long long>(T) % nwarps);
-    zero_pad_rows(pad_slot_of_row, offsets, E, R_cap, vec_per_row, dst,
-                  (warp0 - first + nwarps) % nwarps, nwarps);
-  }
+  if (pad_slot_of_row != nullptr)
+    zero_pad_rows(pad_slot_of_row, offsets, E, R_cap, vec_per_row, dst, warp0, nwarps);
 }
 
 // scatter_rows_kernel with the pre-FC1 probability multiply: the copy of
@@ -302,6 +313,7 @@ scatter_rows_scaled_kernel(const uint4* __restrict__ src, const int32_t* __restr
   const int lane = threadIdx.x & 31;
   const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  grid_dependency_wait();  // the row maps, when launched behind their writer
   for (long long t = warp0; t < T; t += nwarps) {
     int my_row = -1;
     float my_p = 0.0f;
@@ -341,11 +353,8 @@ scatter_rows_scaled_kernel(const uint4* __restrict__ src, const int32_t* __restr
       }
     }
   }
-  if (pad_slot_of_row != nullptr) {
-    const long long first = (static_cast<long long>(T) % nwarps);
-    zero_pad_rows(pad_slot_of_row, offsets, E, R_cap, vec_per_row, dst,
-                  (warp0 - first + nwarps) % nwarps, nwarps);
-  }
+  if (pad_slot_of_row != nullptr)
+    zero_pad_rows(pad_slot_of_row, offsets, E, R_cap, vec_per_row, dst, warp0, nwarps);
 }
 
 // Zero the padding rows (slot -1) below offsets[E] (the standalone form, for
@@ -690,6 +699,25 @@ __global__ void bounded_wait_selftest_kernel(int32_t* status, uint64_t limit_ns)
   __syncthreads();
 }
 
+// Launch with programmatic stream serialisation: the kernel may start while
+// the one ahead of it in the stream runs, and must call grid_dependency_wait()
+// before it touches anything that kernel writes or reads.
+template <typename... Params, typename... Args>
+cudaError_t launch_early(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                         cudaStream_t stream, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
 }  // namespace
 
 cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* prob, int T, int H,
@@ -723,15 +751,18 @@ cudaError_t launch_permute(const gg_bf16* x, const int32_t* idx, const float* pr
         idx, R, E, ppb, block_hist, status, slot_of_row, prob_of_row, R_cap);
     count_launch();
   }
-  // with no routed pairs one block writes the offsets (all zero)
-  permute_scatter_kernel<<<nb > 0 ? nb : 1, kPermuteBlockThreads, scatter_smem, stream>>>(
-      idx, prob, R, E, P, ppb, nb, block_hist, offsets, row_of_slot, slot_of_row, prob_of_row);
+  // with no routed pairs one block writes the offsets (all zero); started
+  // early behind the count kernel, it waits for the histogram rows
+  err = launch_early(permute_scatter_kernel, dim3(nb > 0 ? nb : 1), dim3(kPermuteBlockThreads),
+                     scatter_smem, stream, idx, prob, R, E, P, ppb, nb, block_hist, offsets,
+                     row_of_slot, slot_of_row, prob_of_row);
+  if (err != cudaSuccess) return err;
   count_launch();
   if (R == 0) return cudaGetLastError();
   if (Xp != nullptr) {
     err = launch_gather_rows(x, row_of_slot, slot_of_row, offsets, H, k, E,
                              static_cast<int>(R_cap), T, P > 1, nullptr, Xp, status,
-                             dev.sm_count, stream);
+                             dev.sm_count, stream, /*after_maps=*/true);
     if (err != cudaSuccess) return err;
   }
   return cudaGetLastError();
@@ -741,7 +772,7 @@ cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* row_of_slot,
                                const int32_t* slot_of_row, const int32_t* offsets, int H, int k,
                                int E, int R_cap, int T, bool has_padding, const float* prob,
                                gg_bf16* dst, int32_t* status, int sm_count,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, bool after_maps) {
   if (R_cap <= 0 || T <= 0) return cudaSuccess;
   const int vec = H / 8;
   long long blocks = (static_cast<long long>(T) + 7) / 8;
@@ -751,23 +782,35 @@ cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* row_of_slot,
   const long long cap = static_cast<long long>(sm_count) * 8;
   if (blocks > cap) blocks = cap;
   // with padding, the same launch zeroes the padding rows: warps for the
-  // tokens plus one warp per 32-row group of the rows (up to the cap; past it
-  // the groups go first to the warps with one token fewer)
+  // tokens plus one warp per 32-row group of the rows (up to the cap)
   if (has_padding) {
     const long long pad_blocks = (static_cast<long long>(R_cap) + 255) / 256;
     blocks = blocks + pad_blocks < cap ? blocks + pad_blocks : cap;
   }
   const int32_t* pad_sor = has_padding ? slot_of_row : nullptr;
-  if (prob != nullptr)
-    scatter_rows_scaled_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
-        reinterpret_cast<const uint4*>(src), row_of_slot, prob, T, k, vec, R_cap,
-        reinterpret_cast<uint4*>(dst), status, pad_sor, offsets, E);
-  else
-    scatter_rows_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
-        reinterpret_cast<const uint4*>(src), row_of_slot, T, k, vec, R_cap,
-        reinterpret_cast<uint4*>(dst), status, pad_sor, offsets, E);
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  const dim3 grid(static_cast<unsigned>(blocks)), block(256);
+  cudaError_t err;
+  if (after_maps) {
+    err = prob != nullptr
+              ? launch_early(scatter_rows_scaled_kernel, grid, block, 0, stream, s4, row_of_slot,
+                             prob, T, k, vec, R_cap, d4, status, pad_sor, offsets, E)
+              : launch_early(scatter_rows_kernel, grid, block, 0, stream, s4, row_of_slot, T, k,
+                             vec, R_cap, d4, status, pad_sor, offsets, E);
+  } else {
+    if (prob != nullptr)
+      scatter_rows_scaled_kernel<<<grid, block, 0, stream>>>(s4, row_of_slot, prob, T, k, vec,
+                                                             R_cap, d4, status, pad_sor,
+                                                             offsets, E);
+    else
+      scatter_rows_kernel<<<grid, block, 0, stream>>>(s4, row_of_slot, T, k, vec, R_cap, d4,
+                                                      status, pad_sor, offsets, E);
+    err = cudaGetLastError();
+  }
+  if (err != cudaSuccess) return err;
   count_launch();
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 cudaError_t launch_zero_pad_rows(const int32_t* slot_of_row, const int32_t* offsets, int E,

@@ -33,6 +33,21 @@ __device__ __forceinline__ void set_status(int32_t* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
 
+// ------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialisation may start while
+// the kernel ahead of it in the stream is still running. grid_dependency_wait
+// returns once that kernel has completed and its writes are visible (at once
+// without such a predecessor); grid_dependents_launch lets the next kernel's
+// blocks be scheduled before this one ends.
+
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
