@@ -49,6 +49,17 @@ __host__ __device__ constexpr int sf_byte(int r, int b) { return (r & 31) * 16 +
 // Byte of column n (0..255) of a weight scale tile.
 __host__ __device__ constexpr int sfb_byte(int n, int b) { return (n >> 7) * 512 + sf_byte(n & 127, b); }
 
+// The exponent e of a block's scale from the block's largest magnitude
+// (quantize32 gives the rule) and the exact factor 2^-e.
+__device__ __forceinline__ int block_exponent(float amax, float& inv) {
+  const uint32_t bits = __float_as_uint(amax);
+  const int biased = static_cast<int>(bits >> 23);
+  int e = biased == 0 ? -127 : biased - 135 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  e = e < -127 ? -127 : e;  // finite inputs give e <= 120
+  inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+  return e;
+}
+
 // Quantise one 32-element block. Returns the E8M0 byte (e + 127) and packs the
 // E4M3 codes into q[8] (element i in byte i % 4 of word i / 4). The exponent
 // comes from the bits of max|v|: with max|v| = 1.f * 2^p, the smallest e with
@@ -65,12 +76,8 @@ __device__ __forceinline__ uint32_t quantize32(const float (&v)[32], uint32_t (&
 #pragma unroll
     for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
   }
-  const float amax = m[0];
-  const uint32_t bits = __float_as_uint(amax);
-  const int biased = static_cast<int>(bits >> 23);
-  int e = biased == 0 ? -127 : biased - 135 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
-  e = e < -127 ? -127 : e;  // finite inputs give e <= 120
-  const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+  float inv;
+  const int e = block_exponent(m[0], inv);
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
     const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
@@ -97,12 +104,8 @@ __device__ __forceinline__ uint32_t quantize32_bf16(const uint32_t (&p)[16], uin
 #pragma unroll
     for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
   }
-  const float amax = m[0];
-  const uint32_t bits = __float_as_uint(amax);
-  const int biased = static_cast<int>(bits >> 23);
-  int e = biased == 0 ? -127 : biased - 135 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
-  e = e < -127 ? -127 : e;
-  const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+  float inv;
+  const int e = block_exponent(m[0], inv);
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
     const uint32_t a = p[2 * w], b = p[2 * w + 1];
@@ -114,6 +117,34 @@ __device__ __forceinline__ uint32_t quantize32_bf16(const uint32_t (&p)[16], uin
         __NV_SATFINITE, __NV_E4M3);
     q[w] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
   }
+  return static_cast<uint32_t>(e + 127);
+}
+
+// quantize32 of a block spread over four neighbouring lanes (lanes 4g..4g+3
+// of a warp, eight elements each as the BF16 pairs of w, each element times
+// p rounded to BF16 when kScale): the four exchange their maxima, then each
+// converts its own eight elements into q (element i in byte i % 4 of word
+// i / 4). Returns the block's E8M0 byte. All 32 lanes must take part.
+template <bool kScale>
+__device__ __forceinline__ uint32_t quantize8x4(uint4 w, float p, uint2& q) {
+  float v[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+  if (kScale) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = round_bf16(v[i] * p);
+  }
+  float m = fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
+                  fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
+  m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+  float inv;
+  const int e = block_exponent(m, inv);
+  uint32_t c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    c[i] = __nv_cvt_float2_to_fp8x2(make_float2(v[2 * i] * inv, v[2 * i + 1] * inv),
+                                    __NV_SATFINITE, __NV_E4M3);
+  q = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
   return static_cast<uint32_t>(e + 127);
 }
 

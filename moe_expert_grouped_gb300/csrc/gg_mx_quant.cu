@@ -45,20 +45,16 @@ tile_prefix_kernel(const int32_t* __restrict__ offsets, int E, int32_t* __restri
   if (t == E - 1) tb[E] = excl + v;
 }
 
-__device__ __forceinline__ void unpack_bf16x8(uint4 w, float* v) {
-  v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
-  v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
-  v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z);
-  v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
-}
-
 // One warp per token: the token's row is read once and each 32-element
 // block is quantised once (once per pair when the pairs scale it by their
 // probability) and written to the permuted row of every pair of the token,
 // its scale byte into the 128-row tile of the expert whose rows contain it.
-// Lane b0 + l owns block b0 + l; lane j < k first resolves pair j's row, its
-// expert (binary search of the offsets, staged in shared memory with the
-// scale-tile prefix once per block) and its scale position.
+// Lane j < k first resolves pair j's row, its expert (binary search of the
+// offsets, staged in shared memory with the scale-tile prefix once per
+// block) and its scale position. The row moves in passes of 256 16-byte
+// chunks: lane l holds chunks l + 32 i (i < 8), so every load and store
+// instruction covers one contiguous stretch of the row, and a block's four
+// chunks sit in four neighbouring lanes, which share its maximum.
 template <bool kScaled>  // prob != nullptr: each pair's copy is scaled by its probability
 __global__ void __launch_bounds__(256)
 quantize_scatter_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ row_of_slot,
@@ -69,7 +65,7 @@ quantize_scatter_kernel(const uint4* __restrict__ src, const int32_t* __restrict
   const int lane = threadIdx.x & 31;
   const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-  const int nblk = K / mx::kBlock;
+  const int vec = K / 8;  // 16-byte chunks of a source row; K % 128 == 0
   const long long tile_bytes = static_cast<long long>(K / mx::kKStep) * mx::kSfaBytes;
   // offsets and tiles_before in shared memory: the searches below would
   // otherwise chain seven global loads per token on the way to its stores
@@ -105,45 +101,48 @@ quantize_scatter_kernel(const uint4* __restrict__ src, const int32_t* __restrict
       }
       if (kScaled) my_p = prob[t * k + lane];
     }
-    const uint4* sp = src + t * (K / 8);
-    // two blocks per lane and pass: their eight 16-byte loads are in flight together
-    for (int b0 = 0; b0 < nblk; b0 += 64) {
-      uint4 raw[2][4];
+    const uint4* sp = src + t * vec;
+    for (int c0 = 0; c0 < vec; c0 += 256) {
+      // chunk c = c0 + lane + 32 i: elements 8c..8c+7, in block c / 4
+      uint4 raw[8];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int b = b0 + 32 * h + lane;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          raw[h][j] = b < nblk ? __ldg(sp + 4 * b + j) : make_uint4(0u, 0u, 0u, 0u);
+      for (int i = 0; i < 8; ++i) {
+        const int c = c0 + lane + 32 * i;
+        raw[i] = c < vec ? __ldg(sp + c) : make_uint4(0u, 0u, 0u, 0u);
       }
+      uint2 q[8];
+      uint32_t sw[8];  // lanes 0 and 16: the scale bytes of the 4 blocks of their 16 chunks
+      const auto quantize = [&](float pj) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int b = b0 + 32 * h + lane;
-        const bool live = b < nblk;
-        float v[32];
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t code = mx::quantize8x4<kScaled>(raw[i], pj, q[i]);
+          const int src0 = lane & 16;
+          const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, code, src0 + 4);
+          const uint32_t b2 = __shfl_sync(0xFFFFFFFFu, code, src0 + 8);
+          const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, code, src0 + 12);
+          sw[i] = code | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        }
+      };
+      if (!kScaled) quantize(1.0f);
+      for (int j = 0; j < k; ++j) {
+        const int row = __shfl_sync(0xFFFFFFFFu, my_row, j);
+        const long long sfo = __shfl_sync(0xFFFFFFFFu, my_sf, j);
+        const float pj = __shfl_sync(0xFFFFFFFFu, my_p, j);
+        if (row < 0) continue;  // the same for the whole warp
+        if (kScaled) quantize(pj);
+        uint2* d = reinterpret_cast<uint2*>(Q + static_cast<long long>(row) * K);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) unpack_bf16x8(raw[h][j], v + 8 * j);
-        const long long sf_b = (b >> 2) * static_cast<long long>(mx::kSfaBytes) + (b & 3);
-        uint32_t q[8];
-        uint32_t code = kScaled ? 0u : mx::quantize32(v, q);
-        for (int j = 0; j < k; ++j) {
-          const int row = __shfl_sync(0xFFFFFFFFu, my_row, j);
-          const long long sfo = __shfl_sync(0xFFFFFFFFu, my_sf, j);
-          const float pj = __shfl_sync(0xFFFFFFFFu, my_p, j);
-          if (row < 0) continue;
-          if (kScaled) {
-            float w[32];
+        for (int i = 0; i < 8; ++i) {
+          const int c = c0 + lane + 32 * i;
+          if (c < vec) __stcs(d + c, q[i]);
+        }
+        // the scale bytes of k-step c / 16 (four blocks) as one 32-bit cell
 #pragma unroll
-            for (int i = 0; i < 32; ++i) w[i] = round_bf16(v[i] * pj);
-            code = mx::quantize32(w, q);
-          }
-          if (live) {
-            uint4* d =
-                reinterpret_cast<uint4*>(Q + static_cast<long long>(row) * K + b * mx::kBlock);
-            __stcs(d, make_uint4(q[0], q[1], q[2], q[3]));
-            __stcs(d + 1, make_uint4(q[4], q[5], q[6], q[7]));
-            S[sfo + sf_b] = static_cast<uint8_t>(code);
-          }
+        for (int i = 0; i < 8; ++i) {
+          const int c = c0 + lane + 32 * i;
+          if ((lane & 15) == 0 && c < vec)
+            *reinterpret_cast<uint32_t*>(S + sfo + static_cast<long long>(c / 16) * mx::kSfaBytes) =
+                sw[i];
         }
       }
     }
@@ -224,8 +223,10 @@ cudaError_t launch_mx_quantize_rows(const gg_bf16* src, int T, int K, int k,
   cudaError_t e = cudaMemsetAsync(
       S, 0, static_cast<size_t>(sf_tiles_cap) * (K / mx::kKStep) * mx::kSfaBytes, stream);
   if (e != cudaSuccess || T <= 0) return e;
+  // one token per warp: the blocks, far more than fit at once, start as
+  // earlier ones finish, which balances the SMs to within one block
   long long blocks = (static_cast<long long>(T) + 7) / 8;  // 8 warps per block
-  const long long cap = static_cast<long long>(sm_count) * 8;
+  const long long cap = static_cast<long long>(sm_count) * 1024;
   if (blocks > cap) blocks = cap;
   // E <= kMaxExperts: at most 8 KB of staged tables
   const size_t tab_bytes = sizeof(int) * 2 * (static_cast<size_t>(E) + 1);
