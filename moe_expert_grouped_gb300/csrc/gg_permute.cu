@@ -775,11 +775,11 @@ cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* row_of_slot,
                                cudaStream_t stream, bool after_maps) {
   if (R_cap <= 0 || T <= 0) return cudaSuccess;
   const int vec = H / 8;
+  // one token per warp: the blocks, far more than fit at once, start as
+  // earlier ones finish, which balances tokens whose rows load slowly
+  // (measured faster than one resident wave and than two)
   long long blocks = (static_cast<long long>(T) + 7) / 8;
-  // 8 blocks per SM: more than fit at once; the blocks of the second wave
-  // start as the first ones finish, which balances tokens whose rows load
-  // slowly (measured faster than one exactly resident wave).
-  const long long cap = static_cast<long long>(sm_count) * 8;
+  const long long cap = static_cast<long long>(sm_count) * 1024;
   if (blocks > cap) blocks = cap;
   // with padding, the same launch zeroes the padding rows: warps for the
   // tokens plus one warp per 32-row group of the rows (up to the cap)
@@ -834,7 +834,9 @@ cudaError_t launch_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const 
   if (T <= 0) return cudaSuccess;
   const int vec = H / 8;
   long long blocks = (static_cast<long long>(T) + 7) / 8;
-  const long long cap = static_cast<long long>(sm_count) * 8;  // as for the row copy
+  // 8 blocks per SM: two waves at 4 resident (measured faster than one
+  // token per warp here, unlike the row copy)
+  const long long cap = static_cast<long long>(sm_count) * 8;
   if (blocks > cap) blocks = cap;
   const int nb = static_cast<int>(blocks);
   if (dprob != nullptr && dot_src != nullptr) {
