@@ -425,12 +425,12 @@ combine_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row_of_
   }
 }
 
-// combine_kernel plus the routing-probability gradient: lane j < k also adds
-// up the n_rowdot partial sums of its pair's row (the first eight as one
-// aligned 32-byte group, loaded before the column loop and added after it, in
-// fp32 in ascending order). A separate kernel so that the plain combine keeps
-// its own code.
-__global__ void __launch_bounds__(256, 4)
+// combine_kernel plus the routing-probability gradient: after the column
+// loop, lane j < k adds up the n_rowdot partial sums of its pair's row in fp32
+// in ascending order (loading them only then keeps the column loop's
+// registers, and so its occupancy, those of the plain combine). A separate
+// kernel so that the plain combine keeps its own code.
+__global__ void __launch_bounds__(256)
 combine_dprob_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ row_of_slot,
                      const float* __restrict__ prob, int T, int k, int vec_per_row, int R_cap,
                      uint4* __restrict__ out, const float* __restrict__ rowdot, int n_rowdot,
@@ -450,20 +450,6 @@ combine_dprob_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ r
       }
     }
     const int rd_stride = (n_rowdot + 7) / 8 * 8;
-    // a pair's first 8 or 16 partials, loaded before the column loop
-    float4 part[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) part[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (lane < k && my_row >= 0) {
-      const float4* rd =
-          reinterpret_cast<const float4*>(rowdot + static_cast<long long>(my_row) * rd_stride);
-      part[0] = __ldg(rd);
-      part[1] = __ldg(rd + 1);
-      if (rd_stride >= 16) {
-        part[2] = __ldg(rd + 2);
-        part[3] = __ldg(rd + 3);
-      }
-    }
     // The column loop is warp-uniform so that the shuffles below see every lane.
     for (int c0 = 0; c0 < vec_per_row; c0 += 64) {
       const int ca = c0 + lane, cb = c0 + 32 + lane;
@@ -499,16 +485,11 @@ combine_dprob_kernel(const uint4* __restrict__ Yp, const int32_t* __restrict__ r
     }
     if (lane < k) {
       float dp = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (n_rowdot > 4 * i + 0) dp += part[i].x;
-        if (n_rowdot > 4 * i + 1) dp += part[i].y;
-        if (n_rowdot > 4 * i + 2) dp += part[i].z;
-        if (n_rowdot > 4 * i + 3) dp += part[i].w;
+      if (my_row >= 0) {
+        const float* rd = rowdot + static_cast<long long>(my_row) * rd_stride;
+#pragma unroll 8
+        for (int b = 0; b < n_rowdot; ++b) dp += __ldg(rd + b);
       }
-      if (my_row >= 0)
-        for (int b = 16; b < n_rowdot; ++b)
-          dp += __ldg(rowdot + static_cast<long long>(my_row) * rd_stride + b);
       dprob[static_cast<long long>(t) * k + lane] = dp;
     }
   }

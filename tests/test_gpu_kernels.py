@@ -173,12 +173,17 @@ def _permute_case(T, E, k, seed, skew=None, dup=False):
     (700, 192, 6, 3, 256, {"dup": True}), (4096, 64, 128, 8, 256, {}),
     # more slots than experts (the grouping by rank of expert parallelism)
     (600, 64, 2, 8, 1, {"dup": True}), (300, 128, 4, 8, 16, {"dup": True}),
+    # rows of several 1 KB slices for the padding zeroing (H = 1344: 64 + 64 + 40
+    # vectors), long runs of padding rows (P = 256)
+    (512, 2048, 16, 4, 256, {}), (300, 1344, 8, 2, 64, {"skew": 3}),
 ])
 def test_permute_bit_exact(gg, T, H, E, k, P, extra):
     idx, prob = _permute_case(T, E, k, T + E, **extra)
     x = normal_bf16(np.random.default_rng(1), (T, H), 1.0)
+    # NaN where nothing is written: a padding row left unzeroed fails below
+    Xp = torch.full((gg.r_cap(T, k, E, P), H), float("nan"), dtype=torch.bfloat16, device="cuda")
     out = gg.permute(bits_to_torch(x), torch.from_numpy(idx).cuda(), torch.from_numpy(prob).cuda(),
-                     E, P)
+                     E, P, out={"Xp": Xp})
     torch.cuda.synchronize()
     assert gg.read_status(out["ws"]) == 0
     off, ros, sor = oracle.route(idx, E, P)
@@ -254,15 +259,16 @@ def test_combine_prob_gradient_sums_partials_in_order(gg):
     np.testing.assert_array_equal(torch_to_bits(out), torch_to_bits(out2))
 
 
-def test_permute_rows_gathers_token_gradient(gg):
-    T, H, E, k, P = 400, 128, 8, 2, 8
+@pytest.mark.parametrize("T,H,E,k,P", [(400, 128, 8, 2, 8), (257, 1344, 6, 3, 128)])
+def test_permute_rows_gathers_token_gradient(gg, T, H, E, k, P):
     idx, prob = _permute_case(T, E, k, 9)
     x = normal_bf16(np.random.default_rng(4), (T, H), 1.0)
     dO = normal_bf16(np.random.default_rng(5), (T, H), 1.0)
     p = gg.permute(bits_to_torch(x), torch.from_numpy(idx).cuda(), torch.from_numpy(prob).cuda(), E, P)
     R_cap = p["Xp"].shape[0]
+    dst = torch.full((R_cap, H), float("nan"), dtype=torch.bfloat16, device="cuda")
     dYp = gg.permute_rows(bits_to_torch(dO), p["row_of_slot"], p["slot_of_row"], p["offsets"], k,
-                          E, P, R_cap, p["ws"])
+                          E, P, R_cap, p["ws"], dst=dst)
     torch.cuda.synchronize()
     sor = p["slot_of_row"].cpu().numpy()
     n = int(p["offsets"][-1].item())

@@ -31,6 +31,10 @@ MX_MID = MoeShape("mx_e8_h384_f256_t300_k2", E=8, H=384, F=256, T=300, k=2, rout
                   x_std=1.0, w_std=0.05)
 MX_PAD = MoeShape("mx_e6_h256_f384_t257_k3_pad16", E=6, H=256, F=384, T=257, k=3, P=16,
                   routing="uniform", x_std=1.0, w_std=0.05)
+# H = 2688: a row of 336 16-byte chunks, one full pass of the row quantiser's
+# lanes (256 chunks) and a partial one
+MX_WIDE = MoeShape("mx_e4_h2688_f128_t70_k4_pad8", E=4, H=2688, F=128, T=70, k=4, P=8,
+                   routing="uniform", x_std=1.0, w_std=0.05)
 ACTS = {0: "swiglu", 1: "qgeglu"}
 MODES = {0: "combine", 1: "activation", 2: "pre_fc1"}
 
@@ -125,7 +129,8 @@ def _dev(inp):
 
 # ------------------------------------------------------------ quantisers
 
-@pytest.mark.parametrize("shape,scaled", [(MX_MID, False), (MX_PAD, False), (MX_PAD, True)])
+@pytest.mark.parametrize("shape,scaled", [(MX_MID, False), (MX_PAD, False), (MX_PAD, True),
+                                          (MX_WIDE, False), (MX_WIDE, True)])
 def test_quantize_rows_bit_exact(gg, shape, scaled):
     s = shape
     inp = make_inputs(s, 31)
@@ -139,7 +144,13 @@ def test_quantize_rows_bit_exact(gg, shape, scaled):
     m, off, sor = _maps(gg, d, s)
     rc = gg.r_cap(s.T, s.k, s.E, s.P)
     ws = m["ws"]
-    res = gg.mx_quantize_rows(d["x"], m, s.k, s.E, s.P, ws, prob=d["prob"] if scaled else None)
+    # E4M3 NaN codes and 0xFF scale bytes where nothing is written: padding
+    # rows or scale bytes left unwritten fail below
+    n_tiles = (rc + 127) // 128 + s.E
+    pre = dict(Q=torch.full((rc, s.H), 0x7F, dtype=torch.uint8, device="cuda"),
+               S=torch.full((n_tiles, s.H // 128, 512), 0xFF, dtype=torch.uint8, device="cuda"))
+    res = gg.mx_quantize_rows(d["x"], m, s.k, s.E, s.P, ws, prob=d["prob"] if scaled else None,
+                              n_tiles=n_tiles, out=pre)
     torch.cuda.synchronize()
     assert gg.read_status(ws) == 0
     n = int(off[-1])
