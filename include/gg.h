@@ -383,6 +383,34 @@ gg_status gg_unpermute_combine_dot(const gg_bf16* Sp, const int32_t* row_of_slot
                                    size_t ws_bytes, gg_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Helpers of expert parallelism: the all-to-all dispatch around the local
+ * grouped GEMM ([P1] "B200 throughput evidence": ordinary all-to-all
+ * dispatch; each of n_ranks ranks owns El consecutive experts).
+ *
+ * gg_ep_split_ids — for every pair i < n of the global expert ids idx[n]:
+ *   dest[i] = idx[i] / El (the owning rank), local_eid[i] = idx[i] % El (the
+ *   expert on that rank), for ids in [0, El * n_ranks). Any other id gives
+ *   dest = local_eid = -1 and sets GG_ERR_DEVICE_BAD_EXPERT_ID (a permute by
+ *   dest then leaves the pair without a row). idx, dest, local_eid int32 on
+ *   the device, owned by the caller; El * n_ranks must fit an int.
+ *
+ * gg_gather_rows32 — out[i][c] = src[index[i]][c] for i < n, c < width, on
+ *   32-bit elements (int32 or fp32 bits): src[src_rows][width],
+ *   index[n] int32, out[n][width], all on the device and owned by the
+ *   caller. index -1 gives a zero row; an index outside [-1, src_rows) gives
+ *   a zero row and sets GG_ERR_DEVICE_BAD_ROW. Used to carry each pair's
+ *   local expert id into send order and to bring the probability gradients
+ *   of the returned rows back into token order.
+ *
+ * Both write only their outputs and the status word at the start of ws
+ * (>= gg_workspace_size(1, 1, 1) bytes), and enqueue nothing when n == 0.
+ * ------------------------------------------------------------------------- */
+gg_status gg_ep_split_ids(const int32_t* idx, int n, int El, int n_ranks, int32_t* dest,
+                          int32_t* local_eid, void* ws, size_t ws_bytes, gg_stream_t stream);
+gg_status gg_gather_rows32(const void* src, int src_rows, int width, const int32_t* index,
+                           int n, void* out, void* ws, size_t ws_bytes, gg_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Whole expert layer. The caller owns one device buffer that holds every
  * intermediate; gg_moe_buffers_bind() carves it (256-byte aligned pieces).
  * ------------------------------------------------------------------------- */

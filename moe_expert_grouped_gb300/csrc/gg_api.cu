@@ -433,6 +433,38 @@ gg_status gg_unpermute_combine_dot(const gg_bf16* Sp, const int32_t* row_of_slot
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// ------------------------------------------------------ expert parallelism
+
+gg_status gg_ep_split_ids(const int32_t* idx, int n, int El, int n_ranks, int32_t* dest,
+                          int32_t* local_eid, void* ws, size_t ws_bytes, gg_stream_t stream) {
+  if (n < 0 || El <= 0 || n_ranks <= 0) return GG_ERR_INVALID_ARG;
+  if (static_cast<long long>(El) * n_ranks > 0x7FFFFFFFLL) return GG_ERR_UNSUPPORTED_SHAPE;
+  if (n > 0 && (idx == nullptr || dest == nullptr || local_eid == nullptr))
+    return GG_ERR_INVALID_ARG;
+  gg_status s = check_ws(ws, ws_bytes, kWsHeader);
+  if (s != GG_OK) return s;
+  DeviceInfo dev;
+  if ((s = device_ok(&dev)) != GG_OK) return s;
+  return from_cuda(launch_ep_split_ids(idx, n, El, n_ranks, dest, local_eid, status_ptr(ws),
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gg_status gg_gather_rows32(const void* src, int src_rows, int width, const int32_t* index,
+                           int n, void* out, void* ws, size_t ws_bytes, gg_stream_t stream) {
+  if (n < 0 || src_rows < 0 || width <= 0) return GG_ERR_INVALID_ARG;
+  if (n > 0 && (src == nullptr && src_rows > 0)) return GG_ERR_INVALID_ARG;
+  if (n > 0 && (index == nullptr || out == nullptr)) return GG_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(src) % 4 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0)
+    return GG_ERR_MISALIGNED;
+  gg_status s = check_ws(ws, ws_bytes, kWsHeader);
+  if (s != GG_OK) return s;
+  DeviceInfo dev;
+  if ((s = device_ok(&dev)) != GG_OK) return s;
+  return from_cuda(launch_gather_rows32(static_cast<const uint32_t*>(src), src_rows, width, index,
+                                        n, static_cast<uint32_t*>(out), status_ptr(ws),
+                                        dev.sm_count, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 // ------------------------------------------------------------------ composite
 
 size_t gg_moe_buffers_size(int T, int H, int F, int k, int E, int pad_multiple) {

@@ -75,6 +75,18 @@ cudaError_t launch_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const 
                            int n_rowdot, const gg_bf16* dot_src, const gg_bf16* dot_rows,
                            float* dprob, int32_t* status, int sm_count, cudaStream_t stream);
 
+// dest[i] = idx[i] / El, local_eid[i] = idx[i] % El (ids in [0, El * n_ranks);
+// -1 and the bad-expert status otherwise).
+cudaError_t launch_ep_split_ids(const int32_t* idx, long long n, int El, int n_ranks,
+                                int32_t* dest, int32_t* local_eid, int32_t* status,
+                                cudaStream_t stream);
+
+// out[i][c] = src[index[i]][c] on 32-bit elements (zero for index -1; zero and
+// the bad-row status for an index outside [-1, src_rows)).
+cudaError_t launch_gather_rows32(const uint32_t* src, int src_rows, int width,
+                                 const int32_t* index, long long n, uint32_t* out,
+                                 int32_t* status, int sm_count, cudaStream_t stream);
+
 // Zeroes row r (vec_per_row 16-byte vectors of dst) for every r < offsets[E]
 // whose slot_of_row is -1 (the padding rows).
 cudaError_t launch_zero_pad_rows(const int32_t* slot_of_row, const int32_t* offsets, int E,

@@ -664,6 +664,46 @@ combine_dot_rows_kernel(const uint4* __restrict__ Sp, const int32_t* __restrict_
   }
 }
 
+// Expert parallelism: owning rank and local expert of every pair.
+__global__ void __launch_bounds__(256)
+ep_split_ids_kernel(const int32_t* __restrict__ idx, long long n, int El, int n_ranks,
+                    int32_t* __restrict__ dest, int32_t* __restrict__ local_eid,
+                    int32_t* status) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int e = idx[i];
+    if (e >= 0 && e < El * n_ranks) {
+      const int d = e / El;
+      dest[i] = d;
+      local_eid[i] = e - d * El;
+    } else {
+      dest[i] = -1;
+      local_eid[i] = -1;
+      set_status(status, GG_ERR_DEVICE_BAD_EXPERT_ID);
+    }
+  }
+}
+
+// out[i][c] = src[index[i]][c], one thread per 32-bit element.
+__global__ void __launch_bounds__(256)
+gather_rows32_kernel(const uint32_t* __restrict__ src, int src_rows, int width,
+                     const int32_t* __restrict__ index, long long n, uint32_t* __restrict__ out,
+                     int32_t* status) {
+  const long long total = n * width;
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long i = t / width;
+    const int c = static_cast<int>(t - i * width);
+    const int r = index[i];
+    uint32_t v = 0u;
+    if (r >= 0 && r < src_rows)
+      v = src[static_cast<long long>(r) * width + c];
+    else if (r != -1)
+      set_status(status, GG_ERR_DEVICE_BAD_ROW);
+    out[t] = v;
+  }
+}
+
 __global__ void bounded_wait_selftest_kernel(int32_t* status, uint64_t limit_ns) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
@@ -792,6 +832,31 @@ cudaError_t launch_gather_rows(const gg_bf16* src, const int32_t* row_of_slot,
   if (err != cudaSuccess) return err;
   count_launch();
   return cudaSuccess;
+}
+
+cudaError_t launch_ep_split_ids(const int32_t* idx, long long n, int El, int n_ranks,
+                                int32_t* dest, int32_t* local_eid, int32_t* status,
+                                cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  long long blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  ep_split_ids_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(idx, n, El, n_ranks, dest,
+                                                                     local_eid, status);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows32(const uint32_t* src, int src_rows, int width,
+                                 const int32_t* index, long long n, uint32_t* out,
+                                 int32_t* status, int sm_count, cudaStream_t stream) {
+  if (n <= 0 || width <= 0) return cudaSuccess;
+  long long blocks = (n * width + 255) / 256;
+  const long long cap = static_cast<long long>(sm_count) * 8;
+  if (blocks > cap) blocks = cap;
+  gather_rows32_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(src, src_rows, width, index,
+                                                                      n, out, status);
+  count_launch();
+  return cudaGetLastError();
 }
 
 cudaError_t launch_zero_pad_rows(const int32_t* slot_of_row, const int32_t* offsets, int E,

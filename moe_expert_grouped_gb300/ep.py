@@ -15,8 +15,10 @@ all-to-all dispatch around the local grouped GEMM).
 
 The exchange uses torch.distributed (NCCL between GPUs, gloo on CPU); the
 rank-local steps come from an ``ops`` object: ``GgOps`` runs them with this
-library's kernels on the rank's GPU. Counts are read on the host once per
-exchange (uneven all-to-all splits need them).
+library's kernels on the rank's GPU (the split of the expert ids by rank, the
+grouping by rank, the gathers into send and token order, the expert MLP and
+the combines). Counts are read on the host once per exchange (uneven
+all-to-all splits need them).
 """
 
 from __future__ import annotations
@@ -53,11 +55,23 @@ class GgOps:
         self.gg = gg
         self.H, self.F, self.El, self.activation = H, F, El, activation
         self._layer = None
+        self._ws = None  # the forward's workspace: status word of its routing calls
+
+    def split_ids(self, idx, El: int, world: int):
+        T, k = idx.shape
+        self._ws = self.gg.workspace(T, k, world, idx.device)
+        return self.gg.ep_split_ids(idx.contiguous(), El, world, self._ws)
 
     def group_by_rank(self, x, dest, prob, world: int) -> dict:
         # the stable counting sort of the pairs by destination rank is the
         # permute with the ranks as "experts"
-        return self.gg.permute(x, dest, prob, world, 1)
+        return self.gg.permute(x, dest, prob, world, 1, ws=self._ws)
+
+    def gather(self, src, index) -> torch.Tensor:
+        return self.gg.gather_rows32(src.contiguous(), index, self._ws)
+
+    def status(self) -> int:
+        return self.gg.read_status(self._ws) if self._ws is not None else 0
 
     def to_send_order(self, src, maps: dict, k: int, world: int) -> torch.Tensor:
         n = src.shape[0] * k
@@ -110,14 +124,16 @@ class ExpertParallelLayer:
 
     def forward(self, x, idx, prob, W1_local, W2_local):
         T, k, W, El = x.shape[0], self.k, self.world, self.El
-        dest = torch.div(idx, El, rounding_mode="floor").to(torch.int32)
+        dest, local_eid = self.ops.split_ids(idx, El, W)
         maps = self.ops.group_by_rank(x, dest, prob, W)
         n = T * k
-        send = (maps["offsets"][1:] - maps["offsets"][:-1]).to(torch.int64)
-        recv = _exchange_counts(send, self.group)
-        send_l, recv_l = send.tolist(), recv.tolist()
+        off = maps["offsets"].tolist()  # the one host read: uneven splits need the counts
+        send_l = [off[r + 1] - off[r] for r in range(W)]
+        recv = _exchange_counts(torch.tensor(send_l, dtype=torch.int64,
+                                             device=maps["offsets"].device), self.group)
+        recv_l = recv.tolist()
         # local expert id of every sent row (row r carries pair slot_of_row[r])
-        eid = torch.remainder(idx.reshape(-1), El).to(torch.int32)[maps["slot_of_row"][:n].long()]
+        eid = self.ops.gather(local_eid.reshape(-1), maps["slot_of_row"][:n])
         rows = _a2a(maps["Xp"][:n], recv_l, send_l, self.group)
         eids = _a2a(eid, recv_l, send_l, self.group)
         y = self.ops.local_forward(rows, eids, W1_local, W2_local)
@@ -137,5 +153,5 @@ class ExpertParallelLayer:
         dp_back = _a2a(dp_rows, send_l, recv_l, self.group)
         # the remote rows carry no probability: weight them in the sum
         dX = self.ops.combine(dx_back, maps, prob, T, k)
-        dprob = dp_back[maps["row_of_slot"].long()].view(T, k)
+        dprob = self.ops.gather(dp_back, maps["row_of_slot"]).view(T, k)
         return dX, dprob

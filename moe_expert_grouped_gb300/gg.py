@@ -50,6 +50,8 @@ SIGNATURES = [
     ("gg_rowdot_stride", _I, [_I]),
     ("gg_unpermute_combine", _I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _Z, _P]),
     ("gg_unpermute_combine_dot", _I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
+    ("gg_ep_split_ids", _I, [_P, _I, _I, _I, _P, _P, _P, _Z, _P]),
+    ("gg_gather_rows32", _I, [_P, _I, _I, _P, _I, _P, _P, _Z, _P]),
     ("gg_moe_buffers_size", _Z, [_I, _I, _I, _I, _I, _I]),
     ("gg_moe_buffers_bind", _I, [_P, _Z, _I, _I, _I, _I, _I, _I, _P]),
     ("gg_moe_mlp_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
@@ -378,6 +380,39 @@ def unpermute_combine_dot(Sp, row_of_slot, prob, T: int, k: int, dot_src, dot_ro
                                         _ptr(ws), ws.numel(), _stream(Sp.device)),
            "gg_unpermute_combine_dot")
     return out, dprob
+
+
+def ep_split_ids(idx, El: int, n_ranks: int, ws, dest=None, local_eid=None):
+    """gg_ep_split_ids: (dest, local_eid), each shaped like idx (int32): the rank
+    owning each pair's expert and the expert's index on that rank."""
+    _need(idx, torch.int32, tuple(idx.shape), "idx")
+    if not idx.is_contiguous():
+        raise ValueError("idx: contiguous tensor expected")
+    n = idx.numel()
+    dest = torch.empty_like(idx) if dest is None else dest
+    local_eid = torch.empty_like(idx) if local_eid is None else local_eid
+    _check(LIB.gg_ep_split_ids(_ptr(idx), n, El, n_ranks, _ptr(dest), _ptr(local_eid), _ptr(ws),
+                               ws.numel(), _stream(idx.device)),
+           "gg_ep_split_ids")
+    return dest, local_eid
+
+
+def gather_rows32(src, index, ws, out=None):
+    """gg_gather_rows32: out[i] = src[index[i]] (zero where index is -1) for a
+    1-D or 2-D int32 / float32 src; index int32 [n]."""
+    if src.dtype not in (torch.int32, torch.float32) or not src.is_contiguous():
+        raise ValueError("src: contiguous int32 or float32 expected")
+    _need(index, torch.int32, (index.numel(),), "index")
+    if not index.is_contiguous():
+        raise ValueError("index: contiguous tensor expected")
+    width = 1 if src.dim() == 1 else src.shape[1]
+    n = index.numel()
+    shape = (n,) if src.dim() == 1 else (n, width)
+    out = torch.empty(shape, dtype=src.dtype, device=src.device) if out is None else out
+    _check(LIB.gg_gather_rows32(_ptr(src), src.shape[0], width, _ptr(index), n, _ptr(out),
+                                _ptr(ws), ws.numel(), _stream(src.device)),
+           "gg_gather_rows32")
+    return out
 
 
 def selftest_bounded_wait(ws, limit_ns: int) -> None:

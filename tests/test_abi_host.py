@@ -194,6 +194,25 @@ def test_validation_rejects_before_launch(gg):
     assert D(p, p, None, 4, 2, 64, 128, p, mis, p, p, ws, 1024, None) == 3
     assert D(p, p, None, 4, 2, 64, 128, p, p, mis, p, ws, 1024, None) == 3
     assert D(p, p, None, 4, 2, 64, 128, p, p, p, p, ws, 16, None) == 4
+    # gg_ep_split_ids: sizes, El * n_ranks past an int, pointers, workspace
+    S = L.gg_ep_split_ids
+    assert S(p, -1, 4, 2, p, p, ws, 1024, None) == 1
+    assert S(p, 8, 0, 2, p, p, ws, 1024, None) == 1
+    assert S(p, 8, 4, 0, p, p, ws, 1024, None) == 1
+    assert S(p, 8, 1 << 16, 1 << 16, p, p, ws, 1024, None) == 2
+    assert S(None, 8, 4, 2, p, p, ws, 1024, None) == 1
+    assert S(p, 8, 4, 2, p, None, ws, 1024, None) == 1
+    assert S(p, 8, 4, 2, p, p, ws, 16, None) == 4
+    # gg_gather_rows32: sizes, pointers, 4-byte alignment, workspace
+    G = L.gg_gather_rows32
+    assert G(p, 8, 0, p, 4, p, ws, 1024, None) == 1
+    assert G(p, -1, 1, p, 4, p, ws, 1024, None) == 1
+    assert G(p, 8, 1, p, -1, p, ws, 1024, None) == 1
+    assert G(None, 8, 1, p, 4, p, ws, 1024, None) == 1
+    assert G(p, 8, 1, None, 4, p, ws, 1024, None) == 1
+    assert G(p, 8, 1, p, 4, None, ws, 1024, None) == 1
+    assert G(ctypes.c_void_p((1 << 40) + 2), 8, 1, p, 4, p, ws, 1024, None) == 3
+    assert G(p, 8, 1, p, 4, p, ws, 16, None) == 4
     # gg_swiglu / gg_glu: F % 64, only the gated forward epilogues
     assert L.gg_swiglu(p, p, 4, 128, 96, p, None) == 2
     assert L.gg_glu(p, p, 4, 128, 96, 1, None, p, None) == 2

@@ -29,6 +29,13 @@ class OracleOps:
         self.El = El
         self._fwd = None
 
+    def split_ids(self, idx, El, world):
+        return (torch.div(idx, El, rounding_mode="floor").to(torch.int32),
+                torch.remainder(idx, El).to(torch.int32))
+
+    def gather(self, src, index):
+        return src[index.long()]
+
     def group_by_rank(self, x, dest, prob, world):
         off, ros, sor = oracle.route(dest.numpy(), world, 1)
         k = dest.shape[1]

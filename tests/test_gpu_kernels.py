@@ -278,6 +278,48 @@ def test_permute_rows_gathers_token_gradient(gg, T, H, E, k, P):
     assert np.all(got[~live] == 0)
 
 
+def test_ep_split_ids(gg):
+    # owning rank and local expert of every pair; an id outside [0, El * W)
+    # gives -1 for both and the bad-expert status
+    El, W, T, k = 6, 4, 300, 3
+    rng = np.random.default_rng(21)
+    idx = rng.integers(0, El * W, size=(T, k)).astype(np.int32)
+    idx[7, 1] = El * W
+    idx[9, 0] = -2
+    ws = gg.workspace(T, k, W, "cuda")
+    dest, leid = gg.ep_split_ids(torch.from_numpy(idx).cuda(), El, W, ws)
+    torch.cuda.synchronize()
+    assert gg.read_status(ws) == 16
+    ok = (idx >= 0) & (idx < El * W)
+    np.testing.assert_array_equal(dest.cpu().numpy(), np.where(ok, idx // El, -1))
+    np.testing.assert_array_equal(leid.cpu().numpy(), np.where(ok, idx % El, -1))
+
+
+@pytest.mark.parametrize("width", [1, 3])
+def test_gather_rows32(gg, width):
+    rng = np.random.default_rng(22 + width)
+    R, n = 57, 400
+    src = rng.standard_normal((R, width)).astype(np.float32)
+    index = rng.integers(-1, R, size=n).astype(np.int32)
+    ws = gg.workspace(1, 1, 1, "cuda")
+    s_t = torch.from_numpy(src if width > 1 else src[:, 0].copy()).cuda()
+    got = gg.gather_rows32(s_t, torch.from_numpy(index).cuda(), ws).cpu().numpy()
+    ref = np.where((index >= 0)[:, None], src[np.maximum(index, 0)], 0.0)
+    torch.cuda.synchronize()
+    assert gg.read_status(ws) == 0
+    np.testing.assert_array_equal(got.reshape(n, width), ref)  # bit-exact copies
+    # int32 rows travel unchanged too; an index past the rows zeroes and flags
+    index[5] = R
+    got_i = gg.gather_rows32(torch.arange(R * width, dtype=torch.int32).reshape(
+        (R, width) if width > 1 else (R,)).cuda(), torch.from_numpy(index).cuda(), ws)
+    torch.cuda.synchronize()
+    assert gg.read_status(ws) == 18
+    gi = got_i.cpu().numpy().reshape(n, width)
+    live = (index >= 0) & (index < R)
+    np.testing.assert_array_equal(gi[live], (index[live, None] * width + np.arange(width)))
+    assert np.all(gi[~live] == 0)
+
+
 def test_device_status_bad_expert_id(gg):
     T, H, E, k = 64, 64, 4, 2
     idx = np.tile(np.array([[0, 1]], np.int32), (T, 1))
