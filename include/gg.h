@@ -562,11 +562,12 @@ gg_status gg_mx_prepare_weights(const gg_bf16* W1, const gg_bf16* W2, int E, int
                                 void* mxw, size_t bytes, gg_stream_t stream);
 
 /* Permuted MXFP8 activation operand, from the permute's maps. Writes
- * tiles_before[E+1] from offsets, clears S (n_tiles tiles of K/128 blocks),
- * then for every (token t, slot j) with a row r = row_of_slot[t*k+j]:
- * Q[r] = the E4M3 codes of src[t] (times prob[t*k+j], rounded to BF16, when
- * prob is not NULL) and its scales into the tiles of the expert whose rows
- * contain r. Rows that no pair reaches keep code 0; padding rows
+ * tiles_before[E+1] from offsets, then for every (token t, slot j) with a
+ * row r = row_of_slot[t*k+j]: Q[r] = the E4M3 codes of src[t] (times
+ * prob[t*k+j], rounded to BF16, when prob is not NULL) and its scales into
+ * the tiles of the expert whose rows contain r. Every other scale byte of S
+ * (n_tiles tiles of K/128 blocks) is set to code 0: rows that no pair
+ * reaches, padding rows and the tiles past the last expert's; padding rows
  * (pad_multiple > 1, slot -1) of Q are zeroed. src [T][K] BF16,
  * Q [R_cap][K], K a multiple of 128. A row outside [0, R_cap) is skipped
  * and reported as GG_ERR_DEVICE_BAD_ROW. */

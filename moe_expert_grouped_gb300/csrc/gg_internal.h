@@ -183,9 +183,10 @@ cudaError_t launch_mx_tile_prefix(const int32_t* offsets, int E, int32_t* tiles_
 // gets Q[row_of_slot[t*k+j]] = the E4M3 codes of src[t] (times prob[t*k+j],
 // rounded to BF16, when prob is not null) and its scales in the 128-row tile
 // of the expert e whose rows contain it (tile tiles_before[e] + local row /
-// 128). S (sf_tiles_cap tiles of K/128 x 512 bytes) is cleared first, so rows
-// no pair reaches hold code 0; with has_padding the padding rows of Q are
-// zeroed.
+// 128). Every other cell of S (sf_tiles_cap tiles of K/128 x 512 bytes) gets
+// code 0: rows no pair reaches, padding rows, tiles past the last expert's.
+// With has_padding the padding rows of Q are zeroed. Launched behind the
+// kernel that writes tiles_before (it starts early and waits for it).
 cudaError_t launch_mx_quantize_rows(const gg_bf16* src, int T, int K, int k,
                                     const int32_t* row_of_slot, const int32_t* slot_of_row,
                                     const int32_t* offsets, const int32_t* tiles_before, int E,

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "gg_internal.h"
+#include "gg_launch.cuh"
 #include "gg_mx.cuh"
 #include "gg_ptx.cuh"
 
@@ -15,6 +16,7 @@ namespace {
 __global__ void __launch_bounds__(1024)
 tile_prefix_kernel(const int32_t* __restrict__ offsets, int E, int32_t* __restrict__ tb) {
   __shared__ int warp_sums[32];
+  grid_dependents_launch();  // the row quantiser waits for this grid's results
   const int t = threadIdx.x;
   const int lane = t & 31, warp = t >> 5;
   int v = 0;
@@ -54,10 +56,16 @@ tile_prefix_kernel(const int32_t* __restrict__ offsets, int E, int32_t* __restri
 // block) and its scale position. The row moves in passes of 256 16-byte
 // chunks: lane l holds chunks l + 32 i (i < 8), so every load and store
 // instruction covers one contiguous stretch of the row, and a block's four
-// chunks sit in four neighbouring lanes, which share its maximum.
+// chunks sit in four neighbouring lanes, which share its maximum. After
+// their tokens the warps give code 0 to every scale cell no pair writes
+// (units of 32 rows of a scale tile: rows past an expert's end in its last
+// tile, padding rows, and the tiles past the last expert's), so the scale
+// buffer needs no clearing pass. Launched behind the tile prefix kernel, it
+// waits for that kernel's results before reading them.
 template <bool kScaled>  // prob != nullptr: each pair's copy is scaled by its probability
 __global__ void __launch_bounds__(256)
 quantize_scatter_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ row_of_slot,
+                        const int32_t* __restrict__ slot_of_row, bool has_padding,
                         const float* __restrict__ prob,
                         const int32_t* __restrict__ offsets, const int32_t* __restrict__ tb,
                         int T, int k, int K, int E, int R_cap, int sf_tiles_cap,
@@ -66,12 +74,14 @@ quantize_scatter_kernel(const uint4* __restrict__ src, const int32_t* __restrict
   const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   const int vec = K / 8;  // 16-byte chunks of a source row; K % 128 == 0
-  const long long tile_bytes = static_cast<long long>(K / mx::kKStep) * mx::kSfaBytes;
+  const int KG = K / mx::kKStep;
+  const long long tile_bytes = static_cast<long long>(KG) * mx::kSfaBytes;
   // offsets and tiles_before in shared memory: the searches below would
   // otherwise chain seven global loads per token on the way to its stores
   extern __shared__ int s_tab[];  // [E + 1] offsets, then [E + 1] tiles_before
   int* s_off = s_tab;
   int* s_tb = s_tab + E + 1;
+  grid_dependency_wait();  // tiles_before
   for (int i = threadIdx.x; i <= E; i += blockDim.x) {
     s_off[i] = offsets[i];
     s_tb[i] = tb[i];
@@ -147,6 +157,34 @@ quantize_scatter_kernel(const uint4* __restrict__ src, const int32_t* __restrict
       }
     }
   }
+  // scale cells no pair writes: unit u = (tile u / 4, rows 32 (u % 4) .. +31),
+  // unit u to warp (T + u) mod nwarps, so the warps without a token go first
+  const long long n_units = static_cast<long long>(sf_tiles_cap) * (mx::kRowTile / 32);
+  const int used_tiles = s_tb[E];
+  for (long long u = ((warp0 - T) % nwarps + nwarps) % nwarps; u < n_units; u += nwarps) {
+    const int tile = static_cast<int>(u >> 2);
+    const int r = static_cast<int>(u & 3) * 32 + lane;  // row in the tile
+    bool zero = true;
+    if (tile < used_tiles) {
+      int e = 0, hi = E;  // the expert owning the tile: s_tb[e] <= tile < s_tb[e + 1]
+      while (hi - e > 1) {
+        const int mid = (e + hi) >> 1;
+        if (s_tb[mid] <= tile)
+          e = mid;
+        else
+          hi = mid;
+      }
+      const int local = (tile - s_tb[e]) * mx::kRowTile + r;
+      const long long row = static_cast<long long>(s_off[e]) + local;
+      zero = local >= s_off[e + 1] - s_off[e] ||
+             (has_padding && (row >= R_cap || slot_of_row[row] < 0));
+    }
+    if (zero) {
+      uint8_t* cell = S + static_cast<long long>(tile) * tile_bytes + mx::sf_byte(r, 0);
+      for (int m = 0; m < KG; ++m)
+        *reinterpret_cast<uint32_t*>(cell + static_cast<long long>(m) * mx::kSfaBytes) = 0u;
+    }
+  }
 }
 
 // A 32 x 32 tile of one expert's weight per block: loaded coalesced in the
@@ -219,27 +257,30 @@ cudaError_t launch_mx_quantize_rows(const gg_bf16* src, int T, int K, int k,
                                     int R_cap, bool has_padding, int sf_tiles_cap,
                                     const float* prob, uint8_t* Q, uint8_t* S, int32_t* status,
                                     int sm_count, cudaStream_t stream) {
-  // code 0 wherever no pair lands: rows past an expert's end, padding rows
-  cudaError_t e = cudaMemsetAsync(
-      S, 0, static_cast<size_t>(sf_tiles_cap) * (K / mx::kKStep) * mx::kSfaBytes, stream);
-  if (e != cudaSuccess || T <= 0) return e;
-  // one token per warp: the blocks, far more than fit at once, start as
-  // earlier ones finish, which balances the SMs to within one block
-  long long blocks = (static_cast<long long>(T) + 7) / 8;  // 8 warps per block
+  if (T < 0 || sf_tiles_cap <= 0) return cudaSuccess;
+  // one token per warp, then one warp per 32-row unit of the scale tiles: the
+  // blocks, far more than fit at once, start as earlier ones finish, which
+  // balances the SMs to within one block
+  const long long warps =
+      static_cast<long long>(T) + static_cast<long long>(sf_tiles_cap) * (mx::kRowTile / 32);
+  long long blocks = (warps + 7) / 8;  // 8 warps per block
   const long long cap = static_cast<long long>(sm_count) * 1024;
   if (blocks > cap) blocks = cap;
   // E <= kMaxExperts: at most 8 KB of staged tables
   const size_t tab_bytes = sizeof(int) * 2 * (static_cast<size_t>(E) + 1);
-  if (prob != nullptr)
-    quantize_scatter_kernel<true><<<static_cast<int>(blocks), 256, tab_bytes, stream>>>(
-        reinterpret_cast<const uint4*>(src), row_of_slot, prob, offsets, tiles_before, T, k, K,
-        E, R_cap, sf_tiles_cap, Q, S, status);
-  else
-    quantize_scatter_kernel<false><<<static_cast<int>(blocks), 256, tab_bytes, stream>>>(
-        reinterpret_cast<const uint4*>(src), row_of_slot, prob, offsets, tiles_before, T, k, K,
-        E, R_cap, sf_tiles_cap, Q, S, status);
+  const dim3 grid(static_cast<unsigned>(blocks)), block(256);
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  // behind the tile prefix kernel: started early, waits for tiles_before
+  cudaError_t e =
+      prob != nullptr
+          ? launch_early(quantize_scatter_kernel<true>, grid, block, tab_bytes, stream, s4,
+                         row_of_slot, slot_of_row, has_padding, prob, offsets, tiles_before, T,
+                         k, K, E, R_cap, sf_tiles_cap, Q, S, status)
+          : launch_early(quantize_scatter_kernel<false>, grid, block, tab_bytes, stream, s4,
+                         row_of_slot, slot_of_row, has_padding, prob, offsets, tiles_before, T,
+                         k, K, E, R_cap, sf_tiles_cap, Q, S, status);
+  if (e != cudaSuccess) return e;
   count_launch();
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (has_padding)  // E4M3 zeros on the padding rows (K bytes = K/16 vectors)
     return launch_zero_pad_rows(slot_of_row, offsets, E, R_cap, K / 16, Q, sm_count, stream);
   return cudaSuccess;
