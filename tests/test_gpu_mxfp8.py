@@ -169,6 +169,27 @@ def test_quantize_rows_bit_exact(gg, shape, scaled):
     np.testing.assert_array_equal(res["S"].cpu().numpy(), S_ref)
 
 
+@pytest.mark.parametrize("P", [1, 16])
+def test_quantize_rows_empty_batch(gg, P):
+    # no tokens: the tile prefix is all zero and every scale byte gets code 0
+    # (the buffers start as NaN codes and 0xFF scale bytes)
+    E, K, k = 5, 256, 2
+    x = torch.empty((0, K), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((0, k), dtype=torch.int32, device="cuda")
+    prob = torch.empty((0, k), dtype=torch.float32, device="cuda")
+    m = gg.permute(x, idx, prob, E, P, out={"Xp": None})
+    rc = gg.r_cap(0, k, E, P)
+    n_tiles = (rc + 127) // 128 + E
+    pre = dict(Q=torch.full((max(rc, 1), K), 0x7F, dtype=torch.uint8, device="cuda"),
+               S=torch.full((n_tiles, K // 128, 512), 0xFF, dtype=torch.uint8, device="cuda"),
+               tiles_before=torch.full((E + 1,), 7, dtype=torch.int32, device="cuda"))
+    res = gg.mx_quantize_rows(x, m, k, E, P, m["ws"], n_tiles=n_tiles, out=pre)
+    torch.cuda.synchronize()
+    assert gg.read_status(m["ws"]) == 0
+    assert np.all(res["tiles_before"].cpu().numpy() == 0)
+    assert np.all(res["S"].cpu().numpy() == 0)
+
+
 @pytest.mark.parametrize("E,H,F", [(3, 256, 384), (2, 384, 128)])
 def test_prepare_weights_bit_exact(gg, E, H, F):
     rng = np.random.default_rng(E * 1000 + F)
