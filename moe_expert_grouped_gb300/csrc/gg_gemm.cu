@@ -124,6 +124,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
   uint8_t* smem = smem_raw + pad;
   const uint32_t sbase = raw_addr + pad;  // 1024-aligned: required by the 128B swizzle
   SmemTail& st = *reinterpret_cast<SmemTail*>(smem + STAGES * STAGE_BYTES + kStagingBytes);
+  // The SwiGLU-backward GEMM keeps one stage fewer in flight: its epilogue's
+  // saved-H1 loads then compete with fewer operand loads (measured 1.4-2.3 %
+  // faster with 5 stages, 3.7 % slower with 4; the other modes lose 2-4 %
+  // with 5).
+  constexpr int kStagesUsed =
+      (MODE == kDgradSwigluBwd || MODE == kDgradQgegluBwd) ? STAGES - 1 : STAGES;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -170,7 +176,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
       st.abort_flag = 0;
       if (bad && blockIdx.x == 0) set_status(p.status, GG_ERR_DEVICE_BAD_OFFSETS);
 #pragma unroll
-      for (int s = 0; s < STAGES; ++s) {
+      for (int s = 0; s < kStagesUsed; ++s) {
         mbar_init(smem_u32(&st.full[s]), 1);   // even CTA: its producer's expect_tx
         mbar_init(smem_u32(&st.empty[s]), 1);  // the pair's MMA commit
       }
@@ -265,7 +271,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         }
         used |= 1u << stage;
         last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-        if (++stage == STAGES) {
+        if (++stage == kStagesUsed) {
           stage = 0;
           phase ^= 1u;
         }
@@ -274,7 +280,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     // Before the CTA may exit, the pair's MMAs must have consumed (and so
     // the loads must have landed in) every stage this producer filled.
     if (lane == 0)
-      for (int s = 0; s < STAGES; ++s)
+      for (int s = 0; s < kStagesUsed; ++s)
         if (used & (1u << s)) {
           if (leader)
             (void)mbar_wait_bounded(smem_u32(&st.full[s]), (last_phase >> s) & 1u, nullptr,
@@ -314,7 +320,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
           }
           // the stage is free in both CTAs once these MMAs have read it
           tc_commit_pair_mc(smem_u32(&st.empty[stage]), kClusterMask);
-          if (++stage == STAGES) {
+          if (++stage == kStagesUsed) {
             stage = 0;
             phase ^= 1u;
           }
