@@ -863,8 +863,8 @@ cudaError_t launch_combine(const gg_bf16* Yp, const int32_t* row_of_slot, const 
   if (T <= 0) return cudaSuccess;
   const int vec = H / 8;
   long long blocks = (static_cast<long long>(T) + 7) / 8;
-  // 8 blocks per SM: two waves at 4 resident (measured faster than one
-  // token per warp here, unlike the row copy)
+  // 8 blocks per SM, more than fit at once (a second, partial wave; measured
+  // faster than one token per warp here, unlike the row copy)
   const long long cap = static_cast<long long>(sm_count) * 8;
   if (blocks > cap) blocks = cap;
   const int nb = static_cast<int>(blocks);
