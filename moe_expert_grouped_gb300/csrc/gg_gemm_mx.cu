@@ -60,7 +60,7 @@ constexpr int STAGES = 6;
 constexpr int kCluster = 2;
 constexpr uint16_t kClusterMask = 0x3;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kThreads = 128 + 32 * kEpiWarps;  // producer, MMA, two idle, epilogue
 constexpr uint32_t A_BYTES = BM * kKStep;               // 16 KB
 constexpr uint32_t B_BYTES = kTileNHalf * kKStep;       // 16 KB
 constexpr uint32_t AB_STAGE = A_BYTES + B_BYTES;        // 32 KB, 1024-aligned
@@ -248,6 +248,11 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
   const int total = st.total_tiles;
   volatile int* abort_flag = &st.abort_flag;
 
+  // registers: the producer / MMA warpgroup gives its share to the epilogue
+  // warpgroups (128 x 96 + 256 x 184 <= 384 x 168)
+  constexpr bool kSplitRegs = MODE == kDgradSwigluBwd || MODE == kDgradQgegluBwd;
+  if (warp < 4) {
+  if constexpr (kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
@@ -354,19 +359,21 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
       tc_commit_pair(smem_u32(&st.mma_done));
       (void)mbar_wait_bounded(smem_u32(&st.mma_done), 0, nullptr, p.status);
     }
+  }
   } else {
+    if constexpr (kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
     // -------------------------------------------------- epilogue (kEpiWarps warps)
     // Warp w reads TMEM lanes 32*(w%4) .. +31 (its rows); the two warps of a
     // lane quadrant take half of the 256 columns each. The warp's share goes
     // to registers as BF16 (acc[16] = 4 chunks of 32 columns), the warp
     // reports the accumulator free, then works from registers.
     const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int half = (warp - 4) >> 2;
     const int r = q * 32 + lane;
     constexpr int kChunks = kTN / 64;  // 32-column chunks of this warp per tile
     int eacc = 0;                      // accumulator of the current tile
     uint32_t acc_phase = 0;
-    uint4* stg = reinterpret_cast<uint4*>(staging + (warp - 2) * kWarpStagingBytes);
+    uint4* stg = reinterpret_cast<uint4*>(staging + (warp - 4) * kWarpStagingBytes);
     const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     for (int tile = cluster_id; tile < total; tile += n_clusters) {
       int e, mp, nt;
@@ -469,7 +476,10 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
         const int c_end = min(cb0 + kTN / 2, F - n0);  // multiple of 32
         const int KGq = p.Kq / kKStep;
         uint8_t* drow0 = p.Cq + grow0 * p.Kq + n0;
-        float rd[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four independent partial sums
+        // four independent partial sums: rd[c & 1] takes column pair c, .x its
+        // low and .y its high column
+        float2 rd[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+        constexpr bool kAlphaOne = kAlpha == 1.0f;
         const bool want_dot = p.rowdot != nullptr;
 #pragma unroll
         for (int j = 0; j < kChunks; ++j) {
@@ -492,25 +502,20 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
             us[4 * i + 0] = uw[i].x; us[4 * i + 1] = uw[i].y;
             us[4 * i + 2] = uw[i].z; us[4 * i + 3] = uw[i].w;
           }
-          // dg and du go to BF16 pairs as soon as they exist (the values the
-          // block quantiser takes), which halves their live registers
+          // column pairs as packed fp32 pairs (the same rounding per column as
+          // the scalar form); dg and du leave as the BF16 pairs the block
+          // quantiser takes
           uint32_t pg[16], pu[16];
+          if (want_dot) {
 #pragma unroll
-          for (int hh = 0; hh < 16; ++hh) {
-            float g0, g1, u0, u1;
-            if (want_dot) {
-              glu_mul_bwd<true>(bf16_lo(as[hh]), prs, bf16_lo(gs[hh]), bf16_lo(us[hh]), kAlpha,
-                                g0, u0, rd[hh & 1]);
-              glu_mul_bwd<true>(bf16_hi(as[hh]), prs, bf16_hi(gs[hh]), bf16_hi(us[hh]), kAlpha,
-                                g1, u1, rd[2 + (hh & 1)]);
-            } else {
-              glu_mul_bwd<false>(bf16_lo(as[hh]), prs, bf16_lo(gs[hh]), bf16_lo(us[hh]), kAlpha,
-                                 g0, u0, rd[hh & 1]);
-              glu_mul_bwd<false>(bf16_hi(as[hh]), prs, bf16_hi(gs[hh]), bf16_hi(us[hh]), kAlpha,
-                                 g1, u1, rd[2 + (hh & 1)]);
-            }
-            pg[hh] = pack_bf16x2(g0, g1);
-            pu[hh] = pack_bf16x2(u0, u1);
+            for (int hh = 0; hh < 16; ++hh)
+              glu_mul_bwd2<true, kAlphaOne>(make_float2(bf16_lo(as[hh]), bf16_hi(as[hh])), prs,
+                                            gs[hh], us[hh], kAlpha, pg[hh], pu[hh], rd[hh & 1]);
+          } else {
+#pragma unroll
+            for (int hh = 0; hh < 16; ++hh)
+              glu_mul_bwd2<false, kAlphaOne>(make_float2(bf16_lo(as[hh]), bf16_hi(as[hh])), prs,
+                                             gs[hh], us[hh], kAlpha, pg[hh], pu[hh], rd[hh & 1]);
           }
           uint32_t qv[8];
           const uint32_t code_g = mx::quantize32_bf16(pg, qv);
@@ -526,7 +531,8 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
           }
         }
         if (p.rowdot != nullptr && valid)
-          p.rowdot[grow * p.rowdot_stride + nt * 2 + half] = (rd[0] + rd[1]) + (rd[2] + rd[3]);
+          p.rowdot[grow * p.rowdot_stride + nt * 2 + half] =
+              (rd[0].x + rd[1].x) + (rd[0].y + rd[1].y);
       }
     }
   }
