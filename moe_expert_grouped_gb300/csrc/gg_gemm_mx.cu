@@ -248,118 +248,120 @@ grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap mapA,
   const int total = st.total_tiles;
   volatile int* abort_flag = &st.abort_flag;
 
-  // registers: the producer / MMA warpgroup gives its share to the epilogue
-  // warpgroups (128 x 96 + 256 x 184 <= 384 x 168)
+  // Warpgroup 0 holds the producer and MMA warps (warps 2 and 3 idle),
+  // warpgroups 1 and 2 the epilogue warps. In the SwiGLU-backward modes the
+  // first gives registers to the other two (128 x 88 + 256 x 192 <= 384 x 168,
+  // the registers of the launch), so that epilogue runs without spills.
   constexpr bool kSplitRegs = MODE == kDgradSwigluBwd || MODE == kDgradQgegluBwd;
   if (warp < 4) {
-  if constexpr (kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
-  if (warp == 0) {
-    // ------------------------------------------------ TMA producer (both CTAs)
-    if (lane == 0) {
-      tma_prefetch_desc(&mapA);
-      tma_prefetch_desc(&mapB);
-      tma_prefetch_desc(&mapSA);
-      tma_prefetch_desc(&mapSB);
-      const int h = static_cast<int>(crank);
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t used = 0, last_phase = 0;
-      bool ok = true;
-      for (int tile = cluster_id; tile < total && ok; tile += n_clusters) {
-        int e, mp, nt;
-        decode_tile(tile, st.tiles_before, E, NT, e, mp, nt);
-        const int mt = mp * kCluster + h;
-        const int row0 = __ldg(p.offsets + e) + mt * BM;
-        const int sf_row = (st.sf_before[e] + mt) * KB;
-        const int b_row = kGatedFwd ? h * p.F + nt * kTileNHalf : nt * kTN + h * kBRows;
-        // weight scales: the 256-column tile holding this tile's columns, and
-        // for a 128-column tile the half (128 words) that covers it
-        const int sfb_row = (e * p.NTw + (kTwoAcc ? nt >> 1 : nt)) * KB;
-        const int sfb_x = kTwoAcc ? (nt & 1) * 128 : 0;
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&st.empty[stage]), phase ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = mapa_shared(smem_u32(&st.full[stage]), 0);
-          const uint32_t sa = sbase + stage * AB_STAGE;
-          const uint32_t sb = sa + A_BYTES;
-          const uint32_t ssa = sf_base + stage * SF_STAGE;
-          const uint32_t ssb = ssa + mx::kSfaBytes;
-          if (leader) mbar_arrive_expect_tx(smem_u32(&st.full[stage]), kCluster * kTx);
-          tma_load_2d_pair(sa, &mapA, fb, kb * kKStep, row0);
-          tma_load_3d_pair(sb, &mapB, fb, kb * kKStep, b_row, e);
-          tma_load_2d_pair(ssa, &mapSA, fb, 0, sf_row + kb);
-          tma_load_2d_pair(ssb, &mapSB, fb, sfb_x, sfb_row + kb);
-          used |= 1u << stage;
-          last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+    if constexpr (kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
+    if (warp == 0) {
+      // ------------------------------------------------ TMA producer (both CTAs)
+      if (lane == 0) {
+        tma_prefetch_desc(&mapA);
+        tma_prefetch_desc(&mapB);
+        tma_prefetch_desc(&mapSA);
+        tma_prefetch_desc(&mapSB);
+        const int h = static_cast<int>(crank);
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t used = 0, last_phase = 0;
+        bool ok = true;
+        for (int tile = cluster_id; tile < total && ok; tile += n_clusters) {
+          int e, mp, nt;
+          decode_tile(tile, st.tiles_before, E, NT, e, mp, nt);
+          const int mt = mp * kCluster + h;
+          const int row0 = __ldg(p.offsets + e) + mt * BM;
+          const int sf_row = (st.sf_before[e] + mt) * KB;
+          const int b_row = kGatedFwd ? h * p.F + nt * kTileNHalf : nt * kTN + h * kBRows;
+          // weight scales: the 256-column tile holding this tile's columns, and
+          // for a 128-column tile the half (128 words) that covers it
+          const int sfb_row = (e * p.NTw + (kTwoAcc ? nt >> 1 : nt)) * KB;
+          const int sfb_x = kTwoAcc ? (nt & 1) * 128 : 0;
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait_bounded(smem_u32(&st.empty[stage]), phase ^ 1u, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = mapa_shared(smem_u32(&st.full[stage]), 0);
+            const uint32_t sa = sbase + stage * AB_STAGE;
+            const uint32_t sb = sa + A_BYTES;
+            const uint32_t ssa = sf_base + stage * SF_STAGE;
+            const uint32_t ssb = ssa + mx::kSfaBytes;
+            if (leader) mbar_arrive_expect_tx(smem_u32(&st.full[stage]), kCluster * kTx);
+            tma_load_2d_pair(sa, &mapA, fb, kb * kKStep, row0);
+            tma_load_3d_pair(sb, &mapB, fb, kb * kKStep, b_row, e);
+            tma_load_2d_pair(ssa, &mapSA, fb, 0, sf_row + kb);
+            tma_load_2d_pair(ssb, &mapSB, fb, sfb_x, sfb_row + kb);
+            used |= 1u << stage;
+            last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
-      }
-      for (int s = 0; s < STAGES; ++s)
-        if (used & (1u << s)) {
-          if (leader)
-            (void)mbar_wait_bounded(smem_u32(&st.full[s]), (last_phase >> s) & 1u, nullptr,
+        for (int s = 0; s < STAGES; ++s)
+          if (used & (1u << s)) {
+            if (leader)
+              (void)mbar_wait_bounded(smem_u32(&st.full[s]), (last_phase >> s) & 1u, nullptr,
+                                      p.status);
+            (void)mbar_wait_bounded(smem_u32(&st.empty[s]), (last_phase >> s) & 1u, nullptr,
                                     p.status);
-          (void)mbar_wait_bounded(smem_u32(&st.empty[s]), (last_phase >> s) & 1u, nullptr,
-                                  p.status);
-        }
-    }
-  } else if (warp == 1) {
-    if (lane == 0 && leader) {
-      // ------------------------------------------------ MMA issuer (even CTA)
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      bool ok = true;
-      for (int tile = cluster_id; tile < total && ok; tile += n_clusters) {
-        // the epilogue has read this accumulator's previous tile out of TMEM
-        if (!mbar_wait_bounded(smem_u32(&st.tempty[acc]), acc_phase ^ 1u, abort_flag, p.status))
-          break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kTN);
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&st.full[stage]), phase, abort_flag, p.status)) {
-            ok = false;
-            break;
           }
-          tc_fence_after();
-          const uint32_t sa = sbase + stage * AB_STAGE;
-          const uint32_t sb = sa + A_BYTES;
-          const uint32_t ssa = sf_base + stage * SF_STAGE;
-          const uint32_t ssb = ssa + mx::kSfaBytes;
-          const uint32_t tsa = tmem_base + sf_col(stage);
-          const uint32_t tsb = tsa + 4;
-          mx::cp_scales_pair(tsa, ssa);
-          mx::cp_scales_pair(tsb, ssb);  // columns 0-127
-          if (!kTwoAcc) mx::cp_scales_pair(tsb + 4, ssb + 512);  // columns 128-255
-#pragma unroll
-          for (int kk = 0; kk < kKStep / 32; ++kk) {
-            const uint64_t adesc = make_sdesc(sa + kk * 32, 16, 1024);
-            const uint64_t bdesc = make_sdesc(sb + kk * 32, 16, 1024);
-            mx::mma_mx_pair(d_tmem, adesc, bdesc,
-                            mx::make_idesc_mx(kCluster * BM, kTN, kk, kk), tsa, tsb,
-                            (kb | kk) != 0 ? 1u : 0u);
-          }
-          tc_commit_pair_mc(smem_u32(&st.empty[stage]), kClusterMask);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        tc_commit_pair_mc(smem_u32(&st.tfull[acc]), kClusterMask);
-        if (kTwoAcc) acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
       }
-      tc_commit_pair(smem_u32(&st.mma_done));
-      (void)mbar_wait_bounded(smem_u32(&st.mma_done), 0, nullptr, p.status);
+    } else if (warp == 1) {
+      if (lane == 0 && leader) {
+        // ------------------------------------------------ MMA issuer (even CTA)
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int tile = cluster_id; tile < total && ok; tile += n_clusters) {
+          // the epilogue has read this accumulator's previous tile out of TMEM
+          if (!mbar_wait_bounded(smem_u32(&st.tempty[acc]), acc_phase ^ 1u, abort_flag, p.status))
+            break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kTN);
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait_bounded(smem_u32(&st.full[stage]), phase, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = sbase + stage * AB_STAGE;
+            const uint32_t sb = sa + A_BYTES;
+            const uint32_t ssa = sf_base + stage * SF_STAGE;
+            const uint32_t ssb = ssa + mx::kSfaBytes;
+            const uint32_t tsa = tmem_base + sf_col(stage);
+            const uint32_t tsb = tsa + 4;
+            mx::cp_scales_pair(tsa, ssa);
+            mx::cp_scales_pair(tsb, ssb);  // columns 0-127
+            if (!kTwoAcc) mx::cp_scales_pair(tsb + 4, ssb + 512);  // columns 128-255
+#pragma unroll
+            for (int kk = 0; kk < kKStep / 32; ++kk) {
+              const uint64_t adesc = make_sdesc(sa + kk * 32, 16, 1024);
+              const uint64_t bdesc = make_sdesc(sb + kk * 32, 16, 1024);
+              mx::mma_mx_pair(d_tmem, adesc, bdesc,
+                              mx::make_idesc_mx(kCluster * BM, kTN, kk, kk), tsa, tsb,
+                              (kb | kk) != 0 ? 1u : 0u);
+            }
+            tc_commit_pair_mc(smem_u32(&st.empty[stage]), kClusterMask);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          tc_commit_pair_mc(smem_u32(&st.tfull[acc]), kClusterMask);
+          if (kTwoAcc) acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        }
+        tc_commit_pair(smem_u32(&st.mma_done));
+        (void)mbar_wait_bounded(smem_u32(&st.mma_done), 0, nullptr, p.status);
+      }
     }
-  }
   } else {
     if constexpr (kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
     // -------------------------------------------------- epilogue (kEpiWarps warps)
